@@ -1,0 +1,330 @@
+"""Benchmark: GPT-2-124M training tokens/s (fwd + bwd + AdamW) on libgk, plus KV-cache decode.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--batch B]
+
+Prints ONE JSON line (rank 0). The workload is the GPT-2-124M-shaped training step with
+batch 16 x 1024 (fast mode: bf16 operands, fp32 master weights, moments, residual stream and
+logits), synthetic ids and N(0, 0.02) weights. A step's working set (weights, activations,
+[16384, 50304] logits) is far larger than the 129 MB L2, so consecutive steps cannot hit in
+L2. `--impl reference` times the oracle (plain float64 CPU code) on a bounded sample of the
+same workload on the host cores.
+
+Multi-GPU: the path shards by sequences with no exchange in this build (replicas only): each
+rank runs its own replica; value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "train tokens/s (fwd+bwd+AdamW) at GPT-2-124M shape; KV-cache decode tok/s"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- oracle
+def oracle_tokens_per_s(seconds_budget=20.0, T=1024):
+    """The oracle's training step (float64, host) on one sequence of the 124M model."""
+    import synth
+    from oracle import gpt as ogpt
+
+    s = synth.GPT2_124M
+    ids, targets, params = synth.training_case(s, 1, 7, T=T)
+    sh = ogpt.Shape(s.V, s.T, s.C, s.H, s.L)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        loss, grads, _, _ = ogpt.loss_and_grads(params, ids, targets, sh)
+        ogpt.adamw_step(params, grads, {}, 1, 3e-4, wd=0.01)
+        n += 1
+        el = time.perf_counter() - t0
+        if el > seconds_budget or n >= 3:
+            break
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max((i.get("num_threads") or 1) for i in threadpool_info()) if threadpool_info() else 1
+    except Exception:
+        cores = os.cpu_count() or 1
+    return n * T / el, cores, f"{n} oracle step(s) of 1 x {T} tokens (GPT-2-124M, float64 numpy/BLAS)"
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    from oracle import gpt as ogpt
+
+    s = synth.GPT2_124M
+    T = 128
+    ids, targets, params = synth.training_case(s, 1, 7, T=T)
+    sh = ogpt.Shape(s.V, s.T, s.C, s.H, s.L)
+
+    def step():
+        loss, grads, _, _ = ogpt.loss_and_grads(params, ids, targets, sh)
+        ogpt.adamw_step(params, grads, {}, 1, 3e-4, wd=0.01)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    tps = args.steps * T / el
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max((i.get("num_threads") or 1) for i in threadpool_info())
+    except Exception:
+        cores = os.cpu_count() or 1
+    sample = f"each step 1 x {T} tokens of the GPT-2-124M step (float64 oracle on the host)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"gpt2-124m train step sample, B=1 x T={T}", "l2": "inputs larger than L2"},
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ----------------------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+
+    import synth
+    from gpt_decoder_gb300 import gk
+    from gpt_decoder_gb300.model import Gpt
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    s = synth.GPT2_124M
+    B, T = args.batch, s.T
+    stream = torch.cuda.current_stream()
+    ctx = gk.Ctx(stream.cuda_stream, workspace_bytes=256 << 20)
+    ids, targets, params = synth.training_case(s, B, 5 + rank)
+    m = Gpt(ctx, s.V, s.T, s.C, s.H, s.L, B, mode=args.mode)
+    m.load(params)
+    del params
+    d_ids = torch.as_tensor(ids.reshape(-1)).cuda()
+    d_tg = torch.as_tensor(targets.reshape(-1)).cuda()
+    lr, wd = 3e-4, 0.01
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        m.train_step(d_ids, d_tg, lr, wd)
+    gk.gk_sync(ctx)
+    # timed region: K steps, device time by CUDA events on the launching stream
+    gemm_time = {}
+    m.gemm_events = []
+    barrier()
+    torch.cuda.synchronize()
+    n0 = gk.gk_launch_count(ctx)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            loss = m.train_step(d_ids, d_tg, lr, wd)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = gk.gk_launch_count(ctx) - n0
+    gk.gk_sync(ctx)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    tokens = B * T * world
+    value = tokens / (ms / 1e3)
+    # roofline of the dominant kernel class (the GEMMs): algorithmic flops / event time
+    flops, gms = 0.0, 0.0
+    for (e0, e1, f) in m.gemm_events:
+        gms += e0.elapsed_time(e1)
+        flops += f
+    m.gemm_events = None
+    n_gemm_steps = args.steps
+    hbm, bf16_burst, bf16_sus, peak_src = _peaks()
+    achieved = flops / (gms / 1e3) / 1e12 if gms > 0 else 0.0
+    # end to end: ids/targets from pinned host memory each step, loss read back
+    h_ids = torch.as_tensor(ids.reshape(-1)).pin_memory()
+    h_tg = torch.as_tensor(targets.reshape(-1)).pin_memory()
+    h_loss = torch.empty(1, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_tg.copy_(h_tg, non_blocking=True)
+        loss = m.train_step(d_ids, d_tg, lr, wd)
+        h_loss.copy_(loss, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e = tokens / ((time.perf_counter() - t0) / e2e_steps)
+    decode = None
+    if rank == 0 and not args.no_decode:
+        decode = bench_decode(ctx, m, s)
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, cores, sample = oracle_tokens_per_s()
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.mode == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": f"gpt2-124m train step (fwd+bwd+AdamW), B={B} x T={T}, "
+                               f"{'bf16 operands / fp32 master' if args.mode == 'bf16' else 'fp32 faithful'}",
+                   "l2": "inputs larger than L2 (step working set >> 129 MB)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved,
+                     "peak": bf16_sus if args.mode == "bf16" else bf16_sus / 2, "unit": "TFLOP/s",
+                     "frac": achieved / (bf16_sus if args.mode == "bf16" else bf16_sus / 2), "traffic": None,
+                     "kernel": "all GEMM launches of the step", "peak_source": f"{peak_src} bf16 sustained"
+                     + ("" if args.mode == "bf16" else " / 2 (tf32 nominal ratio)"),
+                     "gemm_ms_per_step": gms / n_gemm_steps, "gemm_tflop_per_step": flops / n_gemm_steps / 1e12},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": int(2 * B * T * 4), "d2h_bytes_per_step": 4},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "loss_last": float(loss.item()),
+    }
+    if decode:
+        out["decode"] = decode
+    print(json.dumps(out))
+
+
+def bench_decode(ctx, m, s, Tp=512, n_steps=64):
+    """Greedy KV-cache decode tok/s (fp32 weights) at batch 1 and 16 after a 512-token prompt."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    res = {}
+    stream = torch.cuda.current_stream()
+    for B in (1, 16):
+        kv = gk.KvCache(ctx, m.cfg, B, Tp + n_steps + 1)
+        prompt = torch.randint(0, s.V, (B * Tp,), dtype=torch.int32, device="cuda")
+        logits = torch.empty(B, s.V, device="cuda")
+        nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+        gk.gk_prefill(ctx, m.params, kv, prompt, Tp, logits)
+        gk.gk_sample(ctx, kv, logits, s.V, nxt, None)
+        tok = nxt.clone()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_steps):
+            gk.gk_decode_step(ctx, m.params, kv, tok, logits, tok, None)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        gk.gk_sync(ctx)
+        ms = e0.elapsed_time(e1)
+        res[f"B{B}"] = {"tok_s": B * n_steps / (ms / 1e3), "ms_per_step": ms / n_steps, "prompt": Tp,
+                        "steps": n_steps, "dtype": "f32"}
+        kv.close()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=16)
+    ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

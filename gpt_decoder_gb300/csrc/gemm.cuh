@@ -1,0 +1,50 @@
+// Internal GEMM interface: C[M,N] (=|+=) epi(sum_k A(m,k) B(k,n) + bias[n] + residual[m,n]).
+//
+// Operand majorness covers every product of the decoder step without transpose passes:
+//   A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m];
+//   B(k,n) = B[n*ldb + k] when b_kmajor, else B[k*ldb + n].
+// Epilogues: EPI_GELU stores the pre-activation v to `aux` and gelu(v) to C; EPI_DGELU
+// stores v * gelu'(aux) (the backward of a GELU fused into the GEMM producing its input
+// gradient).
+#pragma once
+
+#include "common.cuh"
+
+namespace gk {
+
+enum Epi { EPI_NONE = 0, EPI_GELU = 1, EPI_DGELU = 2 };
+
+struct Gemm {
+    int64_t M = 0, N = 0, K = 0;
+    const void* A = nullptr;
+    int64_t lda = 0;
+    bool a_kmajor = true;
+    const void* B = nullptr;
+    int64_t ldb = 0;
+    bool b_kmajor = true;
+    int ab_dtype = GK_F32;
+    void* C = nullptr;
+    int64_t ldc = 0;
+    int c_dtype = GK_F32;
+    bool accumulate = false;
+    const float* bias = nullptr;
+    const float* residual = nullptr;
+    int64_t ldr = 0;
+    int epi = EPI_NONE;
+    void* aux = nullptr;
+    int64_t ldaux = 0;
+    int aux_dtype = GK_F32;
+};
+
+// CUDA-core (SIMT) kernel: float32 or bfloat16 operands, float32 FMA accumulation.
+gk_status gemm_simt(gk_ctx* ctx, const Gemm& g);
+// Tensor-core kernel (tcgen05 + TMA + TMEM), bfloat16 operands, float32 accumulation.
+// Returns GK_ERR_UNSUPPORTED for shapes or alignments it does not take.
+gk_status gemm_tc(gk_ctx* ctx, const Gemm& g);
+// Dispatch by operand type, arithmetic mode and shape.
+gk_status gemm(gk_ctx* ctx, const Gemm& g);
+
+// dst[n] += sum over rows of src[r, n] (deterministic, float32 result).
+gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_t rows, int64_t cols, float* dst);
+
+}  // namespace gk

@@ -1,0 +1,143 @@
+// MatMul / MatMulT entry points ([LM1] = "Build a language model in C# from scratch (1):
+// the Autograd engine", Ops: MatMul listing, backward rule, op table) mapped onto the
+// internal GEMM, plus the deterministic column sum used for bias gradients.
+#include <algorithm>
+
+#include "gemm.cuh"
+
+namespace gk {
+namespace {
+
+constexpr int COLSUM_SPLITS = 64;
+
+// partial[s][c] = sum of rows r = s, s + S, s + 2S, ... of src[:, c] (ascending r).
+template <typename T>
+__global__ void colsum_partial_kernel(const T* __restrict__ src, int64_t ld, int64_t rows, int64_t cols,
+                                      float* __restrict__ partial) {
+    int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int s = blockIdx.y;
+    if (c >= cols) return;
+    float acc = 0.f;
+    for (int64_t r = s; r < rows; r += gridDim.y) acc += load_as_f32(src + r * ld + c);
+    partial[(int64_t)s * cols + c] = acc;
+}
+
+__global__ void colsum_reduce_kernel(const float* __restrict__ partial, int splits, int64_t cols, float* dst) {
+    int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += partial[(int64_t)s * cols + c];
+    dst[c] += acc;
+}
+
+}  // namespace
+
+gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_t rows, int64_t cols, float* dst) {
+    int splits = (int)std::min<int64_t>(COLSUM_SPLITS, rows);
+    float* partial = (float*)workspace(ctx, (size_t)splits * cols * sizeof(float));
+    GK_REQUIRE(ctx, partial, GK_ERR_WORKSPACE, "bias gradient needs %lld workspace bytes",
+               (long long)splits * cols * 4);
+    dim3 grid((unsigned)cdiv(cols, 128), (unsigned)splits);
+    if (dtype == GK_F32)
+        colsum_partial_kernel<float><<<grid, 128, 0, ctx->stream>>>((const float*)src, ld, rows, cols, partial);
+    else
+        colsum_partial_kernel<__nv_bfloat16><<<grid, 128, 0, ctx->stream>>>((const __nv_bfloat16*)src, ld, rows, cols,
+                                                                          partial);
+    GK_TRY(launched(ctx, "colsum_partial"));
+    colsum_reduce_kernel<<<(unsigned)cdiv(cols, 256), 256, 0, ctx->stream>>>(partial, splits, cols, dst);
+    return launched(ctx, "colsum_reduce");
+}
+
+gk_status gemm(gk_ctx* ctx, const Gemm& g) {
+    if (g.M == 0 || g.N == 0) return GK_OK;
+    if (g.ab_dtype == GK_BF16) {
+        gk_status s = gemm_tc(ctx, g);
+        if (s != GK_ERR_UNSUPPORTED) return s;
+    }
+    return gemm_simt(ctx, g);
+}
+
+}  // namespace gk
+
+using namespace gk;
+
+static bool dtype_ok(int d) { return d == GK_F32 || d == GK_BF16; }
+
+extern "C" {
+
+gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W, int64_t ldw, int transW,
+                        const float* bias, const float* residual, int64_t ldr, void* Y, int64_t ldy, int y_dtype,
+                        int64_t N, int64_t K, int64_t M, int act, void* preact, int64_t ldp) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, X && W && Y && N >= 0 && K >= 0 && M >= 0, GK_ERR_ARG, "gk_matmul_fwd: bad argument");
+    GK_REQUIRE(ctx, dtype_ok(dtype) && dtype_ok(y_dtype), GK_ERR_ARG, "gk_matmul_fwd: bad dtype");
+    GK_REQUIRE(ctx, ldx >= K && ldy >= M && ldw >= (transW ? K : M), GK_ERR_ARG, "gk_matmul_fwd: stride too small");
+    GK_REQUIRE(ctx, !residual || ldr >= M, GK_ERR_ARG, "gk_matmul_fwd: residual stride too small");
+    GK_REQUIRE(ctx, act == GK_ACT_NONE || (act == GK_ACT_GELU && preact && ldp >= M), GK_ERR_ARG,
+               "gk_matmul_fwd: GELU needs a preact buffer");
+    GK_REQUIRE(ctx, !(residual && (const void*)residual == Y) || y_dtype == GK_F32, GK_ERR_ARG,
+               "gk_matmul_fwd: in-place residual needs float32 Y");
+    if (N == 0 || M == 0) return GK_OK;
+    Gemm g;
+    g.M = N; g.N = M; g.K = K;
+    g.A = X; g.lda = ldx; g.a_kmajor = true;
+    g.B = W; g.ldb = ldw; g.b_kmajor = transW != 0;
+    g.ab_dtype = dtype;
+    g.C = Y; g.ldc = ldy; g.c_dtype = y_dtype;
+    g.bias = bias; g.residual = residual; g.ldr = ldr;
+    if (act == GK_ACT_GELU) {
+        g.epi = EPI_GELU; g.aux = preact; g.ldaux = ldp; g.aux_dtype = y_dtype;
+    }
+    if (K == 0) {
+        // no products: the result is the epilogue of zero (still a kernel, for uniformity)
+        return gemm_simt(ctx, g);
+    }
+    return gemm(ctx, g);
+}
+
+gk_status gk_matmul_bwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W, int64_t ldw, int transW,
+                        const void* dY, int64_t lddy, void* dX, int64_t lddx, int dx_dtype, int accumulate_dX,
+                        const void* preact_X, int64_t ldp, float* dW, int64_t lddw, float* dbias, int64_t N,
+                        int64_t K, int64_t M) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, dY && N >= 0 && K >= 0 && M >= 0 && lddy >= M, GK_ERR_ARG, "gk_matmul_bwd: bad argument");
+    GK_REQUIRE(ctx, dtype_ok(dtype), GK_ERR_ARG, "gk_matmul_bwd: bad dtype");
+    if (dX && N > 0 && K > 0) {
+        GK_REQUIRE(ctx, W && dtype_ok(dx_dtype) && lddx >= K && ldw >= (transW ? K : M), GK_ERR_ARG,
+                   "gk_matmul_bwd: bad dX arguments");
+        GK_REQUIRE(ctx, !accumulate_dX || dx_dtype == GK_F32, GK_ERR_ARG, "gk_matmul_bwd: accumulate needs float32 dX");
+        GK_REQUIRE(ctx, !preact_X || ldp >= K, GK_ERR_ARG, "gk_matmul_bwd: preact stride too small");
+        Gemm g;
+        g.M = N; g.N = K; g.K = M;
+        g.A = dY; g.lda = lddy; g.a_kmajor = true;
+        g.B = W; g.ldb = ldw; g.b_kmajor = transW == 0;
+        g.ab_dtype = dtype;
+        g.C = dX; g.ldc = lddx; g.c_dtype = dx_dtype;
+        g.accumulate = accumulate_dX != 0;
+        if (preact_X) {
+            g.epi = EPI_DGELU; g.aux = const_cast<void*>(preact_X); g.ldaux = ldp; g.aux_dtype = dtype;
+        }
+        GK_TRY(M == 0 ? gemm_simt(ctx, g) : gemm(ctx, g));
+    }
+    if (dW && N > 0 && K > 0 && M > 0) {
+        GK_REQUIRE(ctx, X && ldx >= K && lddw >= (transW ? K : M), GK_ERR_ARG, "gk_matmul_bwd: bad dW arguments");
+        Gemm g;
+        if (!transW) {
+            g.M = K; g.N = M; g.K = N;
+            g.A = X; g.lda = ldx; g.a_kmajor = false;
+            g.B = dY; g.ldb = lddy; g.b_kmajor = false;
+        } else {
+            g.M = M; g.N = K; g.K = N;
+            g.A = dY; g.lda = lddy; g.a_kmajor = false;
+            g.B = X; g.ldb = ldx; g.b_kmajor = false;
+        }
+        g.ab_dtype = dtype;
+        g.C = dW; g.ldc = lddw; g.c_dtype = GK_F32;
+        g.accumulate = true;
+        GK_TRY(gemm(ctx, g));
+    }
+    if (dbias && N > 0) GK_TRY(colsum_add(ctx, dY, lddy, dtype, N, M, dbias));
+    return GK_OK;
+}
+
+}  // extern "C"

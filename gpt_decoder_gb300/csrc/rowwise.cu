@@ -1,0 +1,791 @@
+// Row-wise and elementwise kernels of the decoder step: embedding, LayerNorm, GELU,
+// softmax cross-entropy, AdamW. These are HBM-bound: each reads and writes its tensors
+// once with coalesced (where alignment allows, 128-bit) accesses and reduces rows with warp
+// shuffles. Sources: [LM1] = "Build a language model in C# from scratch (1): the Autograd
+// engine", [LM4] = "... (4): running GPT-2 weights" (arabroot.io).
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+using namespace gk;
+
+namespace {
+
+// ------------------------------------------------------------------------ embedding
+// x[r, :] = wte[ids[r], :] + wpe[r % T, :]   ([LM1] op table, Embedding; [LM4] Gpt.Step)
+__global__ void embedding_fwd_kernel(const int32_t* __restrict__ ids, const float* __restrict__ wte,
+                                     const float* __restrict__ wpe, float* __restrict__ x, int64_t N, int T,
+                                     int C, int V, int* err) {
+    int64_t r = blockIdx.x;
+    if (r >= N) return;
+    int id = ids[r];
+    bool ok = id >= 0 && id < V;
+    if (!ok && threadIdx.x == 0) report(err, GK_ERR_INDEX);
+    const float* te = wte + (int64_t)(ok ? id : 0) * C;
+    const float* pe = wpe + (int64_t)(r % T) * C;
+    float* xr = x + r * C;
+    if ((C & 3) == 0) {
+        for (int c = threadIdx.x * 4; c < C; c += blockDim.x * 4) {
+            float4 a = *reinterpret_cast<const float4*>(te + c);
+            float4 b = *reinterpret_cast<const float4*>(pe + c);
+            float4 o = ok ? make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w) : make_float4(0, 0, 0, 0);
+            *reinterpret_cast<float4*>(xr + c) = o;
+        }
+    } else {
+        for (int c = threadIdx.x; c < C; c += blockDim.x) xr[c] = ok ? te[c] + pe[c] : 0.0f;
+    }
+}
+
+// dwte[id, :] += dx[r, :] for every row r with ids[r] == id, rows in ascending order.
+// Block b owns the token range [b*span, (b+1)*span). It scans all ids in chunks of
+// blockDim rows, compacts the matching rows of each chunk into shared memory in ascending
+// order (warp ballots + a prefix over warps), then its threads add those rows column by
+// column. Each (id, column) element is owned by one thread, which performs its additions
+// in ascending r: bit-identical to the sequential definition.
+constexpr int EMB_BWD_THREADS = 256;
+__global__ void __launch_bounds__(EMB_BWD_THREADS) embedding_bwd_wte_kernel(
+        const int32_t* __restrict__ ids, const float* __restrict__ dx, float* __restrict__ dwte,
+        int64_t N, int C, int V, int span, int* err) {
+    __shared__ int rows[EMB_BWD_THREADS];
+    __shared__ int warp_cnt[EMB_BWD_THREADS / 32];
+    __shared__ int total;
+    int lo = blockIdx.x * span, hi = min(V, lo + span);
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t base = 0; base < N; base += EMB_BWD_THREADS) {
+        int64_t r = base + threadIdx.x;
+        int id = r < N ? ids[r] : -1;
+        if (blockIdx.x == 0 && r < N && (id < 0 || id >= V)) report(err, GK_ERR_INDEX);
+        bool mine = id >= lo && id < hi;
+        unsigned ball = __ballot_sync(0xffffffffu, mine);
+        if (lane == 0) warp_cnt[warp] = __popc(ball);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int s = 0;
+            for (int w = 0; w < EMB_BWD_THREADS / 32; ++w) {
+                int c = warp_cnt[w];
+                warp_cnt[w] = s;
+                s += c;
+            }
+            total = s;
+        }
+        __syncthreads();
+        if (mine) rows[warp_cnt[warp] + __popc(ball & ((1u << lane) - 1u))] = (int)r;
+        __syncthreads();
+        int n = total;
+        for (int i = 0; i < n; ++i) {
+            int rr = rows[i];
+            float* dst = dwte + (int64_t)ids[rr] * C;
+            const float* src = dx + (int64_t)rr * C;
+            for (int c = threadIdx.x; c < C; c += EMB_BWD_THREADS) dst[c] += src[c];
+        }
+        __syncthreads();
+    }
+}
+
+// dwpe[t, c] += dx[b*T + t, c] for b ascending: one thread per (t, c).
+__global__ void embedding_bwd_wpe_kernel(const float* __restrict__ dx, float* __restrict__ dwpe, int B, int T,
+                                         int C) {
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)T * C) return;
+    int64_t t = i / C, c = i % C;
+    float acc = dwpe[i];
+    for (int b = 0; b < B; ++b) acc += dx[((int64_t)b * T + t) * C + c];
+    dwpe[i] = acc;
+}
+
+// ------------------------------------------------------------------------ layernorm
+// One warp per row for C <= 1024 with C % 128 == 0 rows held in registers (VPT float4 per
+// lane); two-pass mean / variance in registers, so x is read once.
+template <int VPT, typename TY>
+__global__ void layernorm_fwd_warp_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                          const float* __restrict__ beta, TY* __restrict__ y, float* mean_out,
+                                          float* rstd_out, int64_t rows, int C, float eps) {
+    int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float* xr = x + row * C;
+    float4 v[VPT];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        v[i] = *reinterpret_cast<const float4*>(xr + (i * 32 + lane) * 4);
+        s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+    float mu = warp_sum(s) / C;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        float a = v[i].x - mu, b = v[i].y - mu, c = v[i].z - mu, d = v[i].w - mu;
+        q += (a * a + b * b) + (c * c + d * d);
+    }
+    float rs = rsqrtf(warp_sum(q) / C + eps);
+    if (lane == 0) {
+        if (mean_out) mean_out[row] = mu;
+        if (rstd_out) rstd_out[row] = rs;
+    }
+    TY* yr = y + row * C;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        int c = (i * 32 + lane) * 4;
+        float4 g = *reinterpret_cast<const float4*>(gamma + c);
+        float4 b = *reinterpret_cast<const float4*>(beta + c);
+        store_from_f32(yr + c + 0, (v[i].x - mu) * rs * g.x + b.x);
+        store_from_f32(yr + c + 1, (v[i].y - mu) * rs * g.y + b.y);
+        store_from_f32(yr + c + 2, (v[i].z - mu) * rs * g.z + b.z);
+        store_from_f32(yr + c + 3, (v[i].w - mu) * rs * g.w + b.w);
+    }
+}
+
+// Block-wide sum of one float (any block size that is a multiple of 32, up to 1024).
+__device__ float block_sum(float v, float* red) {
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = lane < nw ? red[lane] : 0.f;
+    return warp_sum(t);
+}
+
+// General LayerNorm forward: one block per row; the row is staged in dynamic shared memory
+// (up to 56K floats), so x is read from HBM once.
+template <typename TY>
+__global__ void layernorm_fwd_block_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                           const float* __restrict__ beta, TY* __restrict__ y, float* mean_out,
+                                           float* rstd_out, int64_t rows, int C, float eps) {
+    extern __shared__ float srow[];
+    __shared__ float red[32];
+    int64_t row = blockIdx.x;
+    const float* xr = x + row * C;
+    float s = 0.f;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        float a = xr[c];
+        srow[c] = a;
+        s += a;
+    }
+    float mu = block_sum(s, red) / C;
+    float q = 0.f;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        float a = srow[c] - mu;
+        q += a * a;
+    }
+    float rs = rsqrtf(block_sum(q, red) / C + eps);
+    if (threadIdx.x == 0) {
+        if (mean_out) mean_out[row] = mu;
+        if (rstd_out) rstd_out[row] = rs;
+    }
+    TY* yr = y + row * C;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) store_from_f32(yr + c, (srow[c] - mu) * rs * gamma[c] + beta[c]);
+}
+
+// LayerNorm backward, one warp per row (C % 128 == 0, C <= 1024). Each block also keeps
+// per-column partial sums of dy*xhat and dy over its rows and writes them to the
+// workspace (partials [gridDim.x][2][C]); a second kernel adds them in block order.
+template <int VPT>
+__global__ void layernorm_bwd_warp_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                          const float* __restrict__ mean, const float* __restrict__ rstd,
+                                          const float* __restrict__ dy, float* __restrict__ dx, int accumulate,
+                                          __nv_bfloat16* __restrict__ dx_bf16, float* __restrict__ partial,
+                                          int64_t rows, int C) {
+    extern __shared__ float sp[];  // [nwarps][2][C] when partials are kept
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float4 pg[VPT], pb[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) pg[i] = pb[i] = make_float4(0, 0, 0, 0);
+    float4 gm[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) gm[i] = *reinterpret_cast<const float4*>(gamma + (i * 32 + lane) * 4);
+    for (int64_t row = (int64_t)blockIdx.x * nw + warp; row < rows; row += (int64_t)gridDim.x * nw) {
+        const float* xr = x + row * C;
+        const float* gr = dy + row * C;
+        float mu = mean[row], rs = rstd[row];
+        float4 xh[VPT], g[VPT];
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            int c = (i * 32 + lane) * 4;
+            float4 a = *reinterpret_cast<const float4*>(xr + c);
+            g[i] = *reinterpret_cast<const float4*>(gr + c);
+            xh[i] = make_float4((a.x - mu) * rs, (a.y - mu) * rs, (a.z - mu) * rs, (a.w - mu) * rs);
+            float h0 = g[i].x * gm[i].x, h1 = g[i].y * gm[i].y, h2 = g[i].z * gm[i].z, h3 = g[i].w * gm[i].w;
+            s1 += (h0 + h1) + (h2 + h3);
+            s2 += (h0 * xh[i].x + h1 * xh[i].y) + (h2 * xh[i].z + h3 * xh[i].w);
+            pg[i].x += g[i].x * xh[i].x; pg[i].y += g[i].y * xh[i].y;
+            pg[i].z += g[i].z * xh[i].z; pg[i].w += g[i].w * xh[i].w;
+            pb[i].x += g[i].x; pb[i].y += g[i].y; pb[i].z += g[i].z; pb[i].w += g[i].w;
+        }
+        float m1 = warp_sum(s1) / C, m2 = warp_sum(s2) / C;
+        float* dr = dx + row * C;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            int c = (i * 32 + lane) * 4;
+            float4 o;
+            o.x = rs * (g[i].x * gm[i].x - m1 - xh[i].x * m2);
+            o.y = rs * (g[i].y * gm[i].y - m1 - xh[i].y * m2);
+            o.z = rs * (g[i].z * gm[i].z - m1 - xh[i].z * m2);
+            o.w = rs * (g[i].w * gm[i].w - m1 - xh[i].w * m2);
+            if (accumulate) {
+                float4 p = *reinterpret_cast<const float4*>(dr + c);
+                o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+            }
+            *reinterpret_cast<float4*>(dr + c) = o;
+            if (dx_bf16) {
+                __nv_bfloat162 lo2 = __floats2bfloat162_rn(o.x, o.y), hi2 = __floats2bfloat162_rn(o.z, o.w);
+                uint2 packed;
+                packed.x = *reinterpret_cast<uint32_t*>(&lo2);
+                packed.y = *reinterpret_cast<uint32_t*>(&hi2);
+                *reinterpret_cast<uint2*>(dx_bf16 + row * C + c) = packed;
+            }
+        }
+    }
+    if (!partial) return;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        int c = (i * 32 + lane) * 4;
+        *reinterpret_cast<float4*>(sp + (warp * 2 + 0) * C + c) = pg[i];
+        *reinterpret_cast<float4*>(sp + (warp * 2 + 1) * C + c) = pb[i];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+        int which = c / C, col = c % C;
+        float acc = 0.f;
+        for (int w = 0; w < nw; ++w) acc += sp[(w * 2 + which) * C + col];
+        partial[((int64_t)blockIdx.x * 2 + which) * C + col] = acc;
+    }
+}
+
+// General LayerNorm backward: one block per row (row stats through a block reduction).
+// Per-column partials of dy*xhat and dy go to partial[blockIdx.x % nparts][2][C] rows
+// accumulated by a fixed set of rows per slot (rows r with r % nparts == slot, handled in
+// ascending order by one block each), keeping the sum order fixed.
+__global__ void layernorm_bwd_block_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                           const float* __restrict__ mean, const float* __restrict__ rstd,
+                                           const float* __restrict__ dy, float* __restrict__ dx, int accumulate,
+                                           __nv_bfloat16* __restrict__ dx_bf16, float* __restrict__ partial,
+                                           int64_t rows, int C) {
+    __shared__ float red[32];
+    int nparts = gridDim.x;
+    for (int64_t row = blockIdx.x; row < rows; row += nparts) {
+        const float* xr = x + row * C;
+        const float* gr = dy + row * C;
+        float mu = mean[row], rs = rstd[row];
+        float s1 = 0.f, s2 = 0.f;
+        for (int c = threadIdx.x; c < C; c += blockDim.x) {
+            float xh = (xr[c] - mu) * rs, h = gr[c] * gamma[c];
+            s1 += h;
+            s2 += h * xh;
+        }
+        float m1 = block_sum(s1, red) / C;
+        float m2 = block_sum(s2, red) / C;
+        float* dr = dx + row * C;
+        for (int c = threadIdx.x; c < C; c += blockDim.x) {
+            float xh = (xr[c] - mu) * rs, g = gr[c];
+            float o = rs * (g * gamma[c] - m1 - xh * m2);
+            if (accumulate) o += dr[c];
+            dr[c] = o;
+            if (dx_bf16) dx_bf16[row * C + c] = __float2bfloat16_rn(o);
+            if (partial) {
+                float* pp = partial + (int64_t)blockIdx.x * 2 * C;
+                if (row == blockIdx.x) {
+                    pp[c] = g * xh;
+                    pp[C + c] = g;
+                } else {
+                    pp[c] += g * xh;
+                    pp[C + c] += g;
+                }
+            }
+        }
+    }
+}
+
+// dgamma[c] += sum_p partial[p][0][c]; dbeta[c] += sum_p partial[p][1][c] (p ascending).
+__global__ void reduce_partials_kernel(const float* __restrict__ partial, int nparts, int C, float* dgamma,
+                                       float* dbeta) {
+    int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float a = 0.f, b = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+        a += partial[((int64_t)p * 2 + 0) * C + c];
+        b += partial[((int64_t)p * 2 + 1) * C + c];
+    }
+    if (dgamma) dgamma[c] += a;
+    if (dbeta) dbeta[c] += b;
+}
+
+// ----------------------------------------------------------------------------- GELU
+__global__ void gelu_fwd_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = gelu_tanh(x[i]);
+}
+__global__ void gelu_bwd_kernel(const float* __restrict__ x, const float* dy, float* dx, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dx[i] = dy[i] * gelu_tanh_grad(x[i]);
+}
+__global__ void gelu_fwd_vec_kernel(const float4* __restrict__ x, float4* __restrict__ y, int64_t n4) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        float4 a = x[i];
+        y[i] = make_float4(gelu_tanh(a.x), gelu_tanh(a.y), gelu_tanh(a.z), gelu_tanh(a.w));
+    }
+}
+__global__ void gelu_bwd_vec_kernel(const float4* __restrict__ x, const float4* dy, float4* dx, int64_t n4) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        float4 a = x[i], g = dy[i];
+        dx[i] = make_float4(g.x * gelu_tanh_grad(a.x), g.y * gelu_tanh_grad(a.y), g.z * gelu_tanh_grad(a.z),
+                            g.w * gelu_tanh_grad(a.w));
+    }
+}
+
+// ------------------------------------------------------------- softmax cross-entropy
+// One block per row: running (max, sum of exp(x - max)) per thread, merged across the
+// block; LSE = max + log(sum). Each thread first takes a vector of values, subtracts its
+// own running max once per vector, so about one exp per element.
+struct MaxSum {
+    float m, s;
+};
+__device__ __forceinline__ MaxSum ms_merge(MaxSum a, MaxSum b) {
+    float m = fmaxf(a.m, b.m);
+    if (m == -INFINITY) return {m, 0.f};
+    return {m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
+}
+__device__ __forceinline__ MaxSum ms_add4(MaxSum a, float4 v) {
+    float vm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    float m = fmaxf(a.m, vm);
+    float s = (a.m == -INFINITY ? 0.f : a.s * expf(a.m - m)) + expf(v.x - m) + expf(v.y - m) + expf(v.z - m) +
+              expf(v.w - m);
+    return {m, s};
+}
+__device__ __forceinline__ MaxSum ms_add1(MaxSum a, float v) {
+    float m = fmaxf(a.m, v);
+    return {m, (a.m == -INFINITY ? 0.f : a.s * expf(a.m - m)) + expf(v - m)};
+}
+
+constexpr int CE_THREADS = 512;
+__global__ void __launch_bounds__(CE_THREADS) softmax_ce_fwd_kernel(const float* __restrict__ logits, int64_t ldl,
+                                                                    const int32_t* __restrict__ targets,
+                                                                    float* __restrict__ lse_out,
+                                                                    float* __restrict__ row_loss, int V, int* err) {
+    __shared__ MaxSum red[CE_THREADS / 32];
+    int64_t row = blockIdx.x;
+    const float* xr = logits + row * ldl;
+    MaxSum acc = {-INFINITY, 0.f};
+    bool vec = ((ldl & 3) == 0) && aligned16(logits);
+    int V4 = vec ? V / 4 : 0;
+    for (int i = threadIdx.x; i < V4; i += CE_THREADS) acc = ms_add4(acc, reinterpret_cast<const float4*>(xr)[i]);
+    for (int c = V4 * 4 + threadIdx.x; c < V; c += CE_THREADS) acc = ms_add1(acc, xr[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        MaxSum b = {__shfl_xor_sync(0xffffffffu, acc.m, o), __shfl_xor_sync(0xffffffffu, acc.s, o)};
+        acc = ms_merge(acc, b);
+    }
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        MaxSum t = red[0];
+        for (int w = 1; w < CE_THREADS / 32; ++w) t = ms_merge(t, red[w]);
+        float lse = t.m + logf(t.s);
+        lse_out[row] = lse;
+        int tg = targets[row];
+        if (tg < 0 || tg >= V) {
+            report(err, GK_ERR_INDEX);
+            tg = 0;
+        }
+        row_loss[row] = lse - xr[tg];
+    }
+}
+
+// loss = (sum over rows, in order, in float64) / rows; one block.
+__global__ void mean_rows_kernel(const float* __restrict__ row_loss, int64_t rows, float* loss) {
+    __shared__ double red[32];
+    double s = 0.0;
+    // fixed partition: thread t sums rows t, t + blockDim, ... ascending
+    for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) s += (double)row_loss[r];
+    s = warp_sum_d(s);
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+        *loss = (float)(t / (double)rows);
+    }
+}
+
+template <typename TD>
+__global__ void softmax_ce_bwd_kernel(const float* __restrict__ logits, int64_t ldl,
+                                      const int32_t* __restrict__ targets, const float* __restrict__ lse,
+                                      const float* __restrict__ dloss, TD* __restrict__ dl, int64_t lddl,
+                                      int64_t rows, int V) {
+    int64_t row = blockIdx.y;
+    float scale = (dloss ? *dloss : 1.0f) / (float)rows;
+    float L = lse[row];
+    int tg = targets[row];
+    const float* xr = logits + row * ldl;
+    TD* dr = dl + row * lddl;
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < lddl; c += (int64_t)gridDim.x * blockDim.x) {
+        float v = 0.f;
+        if (c < V) v = scale * (expf(xr[c] - L) - (c == tg ? 1.f : 0.f));
+        store_from_f32(dr + c, v);
+    }
+}
+
+// float32 logits and float32 dlogits, aligned rows: 4 columns per thread.
+__global__ void softmax_ce_bwd_vec_kernel(const float* __restrict__ logits, int64_t ldl,
+                                          const int32_t* __restrict__ targets, const float* __restrict__ lse,
+                                          const float* __restrict__ dloss, float* dl, int64_t lddl, int64_t rows,
+                                          int V) {
+    int64_t row = blockIdx.y;
+    float scale = (dloss ? *dloss : 1.0f) / (float)rows;
+    float L = lse[row];
+    int tg = targets[row];
+    const float* xr = logits + row * ldl;
+    float* dr = dl + row * lddl;
+    for (int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; c < lddl;
+         c += (int64_t)gridDim.x * blockDim.x * 4) {
+        float4 v = make_float4(0, 0, 0, 0);
+        if (c + 3 < V) {
+            float4 a = *reinterpret_cast<const float4*>(xr + c);
+            v = make_float4(scale * expf(a.x - L), scale * expf(a.y - L), scale * expf(a.z - L), scale * expf(a.w - L));
+        } else {
+            float t[4] = {0, 0, 0, 0};
+            for (int k = 0; k < 4; ++k)
+                if (c + k < V) t[k] = scale * expf(xr[c + k] - L);
+            v = make_float4(t[0], t[1], t[2], t[3]);
+        }
+        if (tg >= c && tg < c + 4) {
+            float* vp = reinterpret_cast<float*>(&v);
+            vp[tg - c] -= scale;
+        }
+        *reinterpret_cast<float4*>(dr + c) = v;
+    }
+}
+
+// bfloat16 dlogits, aligned rows: 8 columns per thread (16-byte stores).
+__global__ void softmax_ce_bwd_bf16_kernel(const float* __restrict__ logits, int64_t ldl,
+                                           const int32_t* __restrict__ targets, const float* __restrict__ lse,
+                                           const float* __restrict__ dloss, __nv_bfloat16* dl, int64_t lddl,
+                                           int64_t rows, int V) {
+    int64_t row = blockIdx.y;
+    float scale = (dloss ? *dloss : 1.0f) / (float)rows;
+    float L = lse[row];
+    int tg = targets[row];
+    const float* xr = logits + row * ldl;
+    __nv_bfloat16* dr = dl + row * lddl;
+    for (int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; c < lddl;
+         c += (int64_t)gridDim.x * blockDim.x * 8) {
+        float t[8];
+        if (c + 7 < V) {
+            float4 a = *reinterpret_cast<const float4*>(xr + c);
+            float4 b = *reinterpret_cast<const float4*>(xr + c + 4);
+            t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w; t[4] = b.x; t[5] = b.y; t[6] = b.z; t[7] = b.w;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t[k] = scale * expf(t[k] - L);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t[k] = (c + k < V) ? scale * expf(xr[c + k] - L) : 0.f;
+        }
+        if (tg >= c && tg < c + 8) t[tg - c] -= scale;
+        uint4 packed;
+        uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(t[2 * k], t[2 * k + 1]);
+            pw[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(dr + c) = packed;
+    }
+}
+
+// ---------------------------------------------------------------------------- AdamW
+// [LM1] "The optimizer", AdamW: float32 arithmetic as on the page.
+__global__ void adamw_kernel(float* __restrict__ p, float* __restrict__ g, float* __restrict__ m,
+                             float* __restrict__ v, __nv_bfloat16* __restrict__ pb, int64_t n, float lr, float b1,
+                             float b2, float eps, float wd, float inv_bc1, float inv_bc2, int zero_grad) {
+    int64_t n4 = n / 4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        float4 pp = reinterpret_cast<float4*>(p)[i], gg = reinterpret_cast<float4*>(g)[i];
+        float4 mm = reinterpret_cast<float4*>(m)[i], vv = reinterpret_cast<float4*>(v)[i];
+        float* pe = &pp.x; float* ge = &gg.x; float* me = &mm.x; float* ve = &vv.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            me[k] = b1 * me[k] + (1.f - b1) * ge[k];
+            ve[k] = b2 * ve[k] + (1.f - b2) * ge[k] * ge[k];
+            float mhat = me[k] * inv_bc1, vhat = ve[k] * inv_bc2;
+            pe[k] -= lr * (mhat / (sqrtf(vhat) + eps) + wd * pe[k]);
+        }
+        reinterpret_cast<float4*>(p)[i] = pp;
+        reinterpret_cast<float4*>(m)[i] = mm;
+        reinterpret_cast<float4*>(v)[i] = vv;
+        if (zero_grad) reinterpret_cast<float4*>(g)[i] = make_float4(0, 0, 0, 0);
+        if (pb) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y), hi = __floats2bfloat162_rn(pp.z, pp.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(pb)[i] = packed;
+        }
+    }
+    // tail
+    for (int64_t i = n4 * 4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float gg = g[i];
+        float mm = b1 * m[i] + (1.f - b1) * gg;
+        float vv = b2 * v[i] + (1.f - b2) * gg * gg;
+        m[i] = mm;
+        v[i] = vv;
+        float pp = p[i];
+        pp -= lr * ((mm * inv_bc1) / (sqrtf(vv * inv_bc2) + eps) + wd * pp);
+        p[i] = pp;
+        if (zero_grad) g[i] = 0.f;
+        if (pb) pb[i] = __float2bfloat16_rn(pp);
+    }
+}
+
+__global__ void to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = __float2bfloat16_rn(x[i]);
+}
+
+int grid_for(gk_ctx* ctx, int64_t work, int threads, int per_sm = 8) {
+    int64_t b = cdiv(work, threads);
+    int64_t cap = (int64_t)ctx->num_sms * per_sm;
+    if (b > cap) b = cap;
+    return (int)(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+extern "C" {
+
+gk_status gk_embedding_fwd(gk_ctx* ctx, const int32_t* ids, const float* wte, const float* wpe, float* x, int B,
+                           int T, int C, int V) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, ids && wte && wpe && x && B > 0 && T > 0 && C > 0 && V > 0, GK_ERR_ARG, "gk_embedding_fwd: bad argument");
+    GK_REQUIRE(ctx, (C & 3) != 0 || (aligned16(wte) && aligned16(wpe) && aligned16(x)), GK_ERR_ALIGN,
+               "gk_embedding_fwd: float32 tables must be 16-byte aligned");
+    int64_t N = (int64_t)B * T;
+    int threads = C >= 512 ? 256 : 128;
+    embedding_fwd_kernel<<<(unsigned)N, threads, 0, ctx->stream>>>(ids, wte, wpe, x, N, T, C, V, ctx->d_err);
+    return launched(ctx, "embedding_fwd");
+}
+
+gk_status gk_embedding_bwd(gk_ctx* ctx, const int32_t* ids, const float* dx, float* dwte, float* dwpe, int B,
+                           int T, int C, int V) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, ids && dx && B > 0 && T > 0 && C > 0 && V > 0, GK_ERR_ARG, "gk_embedding_bwd: bad argument");
+    int64_t N = (int64_t)B * T;
+    if (dwte) {
+        int blocks = ctx->num_sms * 4;
+        if (blocks > V) blocks = V;
+        int span = (int)cdiv(V, blocks);
+        blocks = (int)cdiv(V, span);
+        embedding_bwd_wte_kernel<<<blocks, EMB_BWD_THREADS, 0, ctx->stream>>>(ids, dx, dwte, N, C, V, span, ctx->d_err);
+        GK_TRY(launched(ctx, "embedding_bwd_wte"));
+    }
+    if (dwpe) {
+        int64_t n = (int64_t)T * C;
+        embedding_bwd_wpe_kernel<<<(unsigned)cdiv(n, 256), 256, 0, ctx->stream>>>(dx, dwpe, B, T, C);
+        GK_TRY(launched(ctx, "embedding_bwd_wpe"));
+    }
+    return GK_OK;
+}
+
+gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, const float* beta, void* y, int y_dtype,
+                           float* mean, float* rstd, int64_t rows, int C, float eps) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, x && gamma && beta && y && rows > 0 && C > 0, GK_ERR_ARG, "gk_layernorm_fwd: bad argument");
+    GK_REQUIRE(ctx, y_dtype == GK_F32 || y_dtype == GK_BF16, GK_ERR_ARG, "gk_layernorm_fwd: bad dtype");
+    bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(gamma) && aligned16(beta);
+    if (warp_path) {
+        int wpb = 4;
+        unsigned grid = (unsigned)cdiv(rows, wpb);
+        int vpt = C / 128;
+#define LN_FWD_CASE(V)                                                                                          \
+    case V:                                                                                                     \
+        if (y_dtype == GK_F32)                                                                                  \
+            layernorm_fwd_warp_kernel<V, float><<<grid, wpb * 32, 0, ctx->stream>>>(x, gamma, beta, (float*)y,  \
+                                                                                   mean, rstd, rows, C, eps);   \
+        else                                                                                                    \
+            layernorm_fwd_warp_kernel<V, __nv_bfloat16><<<grid, wpb * 32, 0, ctx->stream>>>(                    \
+                x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps);                                   \
+        break;
+        switch (vpt) {
+            LN_FWD_CASE(1) LN_FWD_CASE(2) LN_FWD_CASE(3) LN_FWD_CASE(4)
+            LN_FWD_CASE(5) LN_FWD_CASE(6) LN_FWD_CASE(7) LN_FWD_CASE(8)
+        }
+#undef LN_FWD_CASE
+        return launched(ctx, "layernorm_fwd");
+    }
+    size_t smem = (size_t)C * sizeof(float);
+    GK_REQUIRE(ctx, smem <= 200 * 1024, GK_ERR_UNSUPPORTED, "gk_layernorm_fwd: C=%d too large", C);
+    int threads = 1024;
+    if (y_dtype == GK_F32) {
+        cudaFuncSetAttribute(layernorm_fwd_block_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        layernorm_fwd_block_kernel<float><<<(unsigned)rows, threads, smem, ctx->stream>>>(x, gamma, beta, (float*)y, mean,
+                                                                                         rstd, rows, C, eps);
+    } else {
+        cudaFuncSetAttribute(layernorm_fwd_block_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        layernorm_fwd_block_kernel<__nv_bfloat16><<<(unsigned)rows, threads, smem, ctx->stream>>>(
+            x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps);
+    }
+    return launched(ctx, "layernorm_fwd");
+}
+
+gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, const float* mean, const float* rstd,
+                           const float* dy, float* dx, int accumulate_dx, uint16_t* dx_bf16, float* dgamma,
+                           float* dbeta, int64_t rows, int C) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, x && gamma && mean && rstd && dy && dx && rows > 0 && C > 0, GK_ERR_ARG,
+               "gk_layernorm_bwd: bad argument");
+    bool want_partials = dgamma || dbeta;
+    bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(dy) && aligned16(dx) &&
+                     aligned16(gamma) && (!dx_bf16 || ((uintptr_t)dx_bf16 & 7) == 0);
+    int nparts;
+    if (warp_path) {
+        int wpb = 8;
+        nparts = (int)std::min<int64_t>(cdiv(rows, wpb), (int64_t)ctx->num_sms * 4);
+        if (nparts > 1216) nparts = 1216;
+    } else {
+        // one block per row slot; bound the partial buffer (2 x C floats per slot) for wide rows
+        int64_t cap = std::max<int64_t>(8, std::min<int64_t>(1216, (int64_t)(16 << 20) / ((int64_t)2 * C * 4)));
+        nparts = (int)std::min<int64_t>(rows, cap);
+    }
+    float* partial = nullptr;
+    if (want_partials) {
+        partial = (float*)workspace(ctx, (size_t)nparts * 2 * C * sizeof(float));
+        GK_REQUIRE(ctx, partial, GK_ERR_WORKSPACE, "gk_layernorm_bwd: needs %zu workspace bytes",
+                   (size_t)nparts * 2 * C * sizeof(float));
+    }
+    if (warp_path) {
+        int wpb = 8;
+        int vpt = C / 128;
+        size_t smem = want_partials ? (size_t)wpb * 2 * C * sizeof(float) : 0;
+#define LN_BWD_CASE(V)                                                                                       \
+    case V:                                                                                                  \
+        cudaFuncSetAttribute(layernorm_bwd_warp_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
+                             (int)smem);                                                                     \
+        layernorm_bwd_warp_kernel<V><<<nparts, wpb * 32, smem, ctx->stream>>>(                               \
+            x, gamma, mean, rstd, dy, dx, accumulate_dx, (__nv_bfloat16*)dx_bf16, partial, rows, C);         \
+        break;
+        switch (vpt) {
+            LN_BWD_CASE(1) LN_BWD_CASE(2) LN_BWD_CASE(3) LN_BWD_CASE(4)
+            LN_BWD_CASE(5) LN_BWD_CASE(6) LN_BWD_CASE(7) LN_BWD_CASE(8)
+        }
+#undef LN_BWD_CASE
+    } else {
+        layernorm_bwd_block_kernel<<<nparts, 512, 0, ctx->stream>>>(x, gamma, mean, rstd, dy, dx, accumulate_dx,
+                                                                   (__nv_bfloat16*)dx_bf16, partial, rows, C);
+    }
+    GK_TRY(launched(ctx, "layernorm_bwd"));
+    if (want_partials) {
+        reduce_partials_kernel<<<(unsigned)cdiv(C, 256), 256, 0, ctx->stream>>>(partial, nparts, C, dgamma, dbeta);
+        GK_TRY(launched(ctx, "layernorm_bwd_reduce"));
+    }
+    return GK_OK;
+}
+
+gk_status gk_gelu_fwd(gk_ctx* ctx, const float* x, float* y, int64_t n) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, x && y && n >= 0, GK_ERR_ARG, "gk_gelu_fwd: bad argument");
+    if (n == 0) return GK_OK;
+    if ((n & 3) == 0 && aligned16(x) && aligned16(y))
+        gelu_fwd_vec_kernel<<<grid_for(ctx, n / 4, 256), 256, 0, ctx->stream>>>((const float4*)x, (float4*)y, n / 4);
+    else
+        gelu_fwd_kernel<<<grid_for(ctx, n, 256), 256, 0, ctx->stream>>>(x, y, n);
+    return launched(ctx, "gelu_fwd");
+}
+
+gk_status gk_gelu_bwd(gk_ctx* ctx, const float* x, const float* dy, float* dx, int64_t n) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, x && dy && dx && n >= 0, GK_ERR_ARG, "gk_gelu_bwd: bad argument");
+    if (n == 0) return GK_OK;
+    if ((n & 3) == 0 && aligned16(x) && aligned16(dy) && aligned16(dx))
+        gelu_bwd_vec_kernel<<<grid_for(ctx, n / 4, 256), 256, 0, ctx->stream>>>((const float4*)x, (const float4*)dy,
+                                                                               (float4*)dx, n / 4);
+    else
+        gelu_bwd_kernel<<<grid_for(ctx, n, 256), 256, 0, ctx->stream>>>(x, dy, dx, n);
+    return launched(ctx, "gelu_bwd");
+}
+
+gk_status gk_softmax_ce_fwd(gk_ctx* ctx, const float* logits, int64_t ldl, const int32_t* targets, float* loss,
+                            float* lse, int64_t rows, int V) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, logits && targets && loss && lse && rows > 0 && V > 0 && ldl >= V, GK_ERR_ARG,
+               "gk_softmax_ce_fwd: bad argument");
+    GK_REQUIRE(ctx, rows < (1ll << 31), GK_ERR_UNSUPPORTED, "gk_softmax_ce_fwd: too many rows");
+    float* row_loss = (float*)workspace(ctx, (size_t)rows * sizeof(float));
+    GK_REQUIRE(ctx, row_loss, GK_ERR_WORKSPACE, "gk_softmax_ce_fwd: needs %lld workspace bytes", (long long)rows * 4);
+    softmax_ce_fwd_kernel<<<(unsigned)rows, CE_THREADS, 0, ctx->stream>>>(logits, ldl, targets, lse, row_loss, V,
+                                                                         ctx->d_err);
+    GK_TRY(launched(ctx, "softmax_ce_fwd"));
+    mean_rows_kernel<<<1, 1024, 0, ctx->stream>>>(row_loss, rows, loss);
+    return launched(ctx, "softmax_ce_mean");
+}
+
+gk_status gk_softmax_ce_bwd(gk_ctx* ctx, const float* logits, int64_t ldl, const int32_t* targets, const float* lse,
+                            const float* dloss, void* dlogits, int64_t lddl, int dl_dtype, int64_t rows, int V) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, logits && targets && lse && dlogits && rows > 0 && V > 0 && ldl >= V && lddl >= V, GK_ERR_ARG,
+               "gk_softmax_ce_bwd: bad argument");
+    GK_REQUIRE(ctx, dl_dtype == GK_F32 || dl_dtype == GK_BF16, GK_ERR_ARG, "gk_softmax_ce_bwd: bad dtype");
+    GK_REQUIRE(ctx, rows < 65536 * 4096ll, GK_ERR_UNSUPPORTED, "gk_softmax_ce_bwd: too many rows");
+    bool alias = (const void*)logits == dlogits;
+    GK_REQUIRE(ctx, !alias || (dl_dtype == GK_F32 && lddl == ldl), GK_ERR_ARG,
+               "gk_softmax_ce_bwd: in-place needs float32 and equal strides");
+    int threads = 256;
+    if (dl_dtype == GK_F32 && (ldl & 3) == 0 && (lddl & 3) == 0 && aligned16(logits) && aligned16(dlogits)) {
+        dim3 grid((unsigned)cdiv(cdiv(lddl, 4), threads), (unsigned)rows);
+        if (grid.x > 16) grid.x = 16;
+        softmax_ce_bwd_vec_kernel<<<grid, threads, 0, ctx->stream>>>(logits, ldl, targets, lse, dloss, (float*)dlogits,
+                                                                    lddl, rows, V);
+    } else if (dl_dtype == GK_BF16 && (ldl & 7) == 0 && (lddl & 7) == 0 && aligned16(logits) && aligned16(dlogits)) {
+        dim3 grid((unsigned)cdiv(cdiv(lddl, 8), threads), (unsigned)rows);
+        if (grid.x > 16) grid.x = 16;
+        softmax_ce_bwd_bf16_kernel<<<grid, threads, 0, ctx->stream>>>(logits, ldl, targets, lse, dloss,
+                                                                     (__nv_bfloat16*)dlogits, lddl, rows, V);
+    } else {
+        dim3 grid((unsigned)cdiv(lddl, threads), (unsigned)rows);
+        if (grid.x > 64) grid.x = 64;
+        if (dl_dtype == GK_F32)
+            softmax_ce_bwd_kernel<float><<<grid, threads, 0, ctx->stream>>>(logits, ldl, targets, lse, dloss,
+                                                                          (float*)dlogits, lddl, rows, V);
+        else
+            softmax_ce_bwd_kernel<__nv_bfloat16><<<grid, threads, 0, ctx->stream>>>(
+                logits, ldl, targets, lse, dloss, (__nv_bfloat16*)dlogits, lddl, rows, V);
+    }
+    return launched(ctx, "softmax_ce_bwd");
+}
+
+gk_status gk_to_bf16(gk_ctx* ctx, const float* x, uint16_t* y, int64_t n) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, x && y && n >= 0, GK_ERR_ARG, "gk_to_bf16: bad argument");
+    if (n == 0) return GK_OK;
+    to_bf16_kernel<<<grid_for(ctx, n, 256), 256, 0, ctx->stream>>>(x, (__nv_bfloat16*)y, n);
+    return launched(ctx, "to_bf16");
+}
+
+gk_status gk_adamw_step(gk_ctx* ctx, const gk_param* params, int n_params, float lr, float beta1, float beta2,
+                        float eps, float wd, int step, int zero_grad) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, params && n_params >= 0 && step >= 1, GK_ERR_ARG, "gk_adamw_step: bad argument");
+    double bc1 = 1.0 - pow((double)beta1, (double)step);
+    double bc2 = 1.0 - pow((double)beta2, (double)step);
+    float ib1 = (float)(1.0 / bc1), ib2 = (float)(1.0 / bc2);
+    for (int k = 0; k < n_params; ++k) {
+        const gk_param& q = params[k];
+        GK_REQUIRE(ctx, q.p && q.g && q.m && q.v && q.n >= 0, GK_ERR_ARG, "gk_adamw_step: bad block %d", k);
+        GK_REQUIRE(ctx, aligned16(q.p) && aligned16(q.g) && aligned16(q.m) && aligned16(q.v) &&
+                            (!q.p_bf16 || ((uintptr_t)q.p_bf16 & 7) == 0),
+                   GK_ERR_ALIGN, "gk_adamw_step: block %d not 16-byte aligned", k);
+        if (q.n == 0) continue;
+        adamw_kernel<<<grid_for(ctx, q.n / 4 + 1, 256, 8), 256, 0, ctx->stream>>>(
+            q.p, q.g, q.m, q.v, (__nv_bfloat16*)q.p_bf16, q.n, lr, beta1, beta2, eps, q.decay ? wd : 0.f, ib1, ib2,
+            zero_grad);
+        GK_TRY(launched(ctx, "adamw"));
+    }
+    return GK_OK;
+}
+
+}  // extern "C"

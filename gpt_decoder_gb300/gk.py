@@ -1,0 +1,292 @@
+"""Python binding of libgk: the same entry points as include/gk.h, argument marshalling only.
+
+Tensor arguments accept a torch tensor (its data_ptr is passed), a raw integer address or
+None (NULL). Every computation runs in libgk's CUDA kernels; there is no fallback: importing
+this module raises if libgk.so has not been built for this machine.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgk.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+_lib = ct.CDLL(LIB_PATH)
+
+# status codes and enums (include/gk.h)
+GK_OK, GK_ERR_ARG, GK_ERR_ALIGN, GK_ERR_UNSUPPORTED, GK_ERR_CUDA, GK_ERR_TIMEOUT, GK_ERR_OVERFLOW, GK_ERR_INDEX, \
+    GK_ERR_WORKSPACE = range(9)
+GK_F32, GK_BF16 = 0, 1
+GK_MATH_FP32, GK_MATH_3XTF32 = 0, 1
+GK_ACT_NONE, GK_ACT_GELU = 0, 1
+(GK_T_WTE, GK_T_WPE, GK_T_LN1_W, GK_T_LN1_B, GK_T_ATTN_W, GK_T_ATTN_B, GK_T_ATTNPROJ_W, GK_T_ATTNPROJ_B,
+ GK_T_LN2_W, GK_T_LN2_B, GK_T_FC_W, GK_T_FC_B, GK_T_MLPPROJ_W, GK_T_MLPPROJ_B, GK_T_LNF_W, GK_T_LNF_B) = range(16)
+
+STATUS_NAMES = {0: "GK_OK", 1: "GK_ERR_ARG", 2: "GK_ERR_ALIGN", 3: "GK_ERR_UNSUPPORTED", 4: "GK_ERR_CUDA",
+                5: "GK_ERR_TIMEOUT", 6: "GK_ERR_OVERFLOW", 7: "GK_ERR_INDEX", 8: "GK_ERR_WORKSPACE"}
+
+P = ct.c_void_p
+I32, I64, F32 = ct.c_int, ct.c_int64, ct.c_float
+
+
+class GkError(RuntimeError):
+    def __init__(self, status, where, msg):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class gk_param(ct.Structure):
+    _fields_ = [("p", P), ("g", P), ("m", P), ("v", P), ("n", I64), ("decay", I32), ("p_bf16", P)]
+
+
+class gk_gpt_cfg(ct.Structure):
+    _fields_ = [("V", I32), ("T", I32), ("C", I32), ("H", I32), ("L", I32)]
+
+
+class gk_sample_cfg(ct.Structure):
+    _fields_ = [("top_k", I32), ("temperature", F32), ("seed", ct.c_uint64), ("counter", ct.c_uint64)]
+
+
+_SIGS = {
+    "gk_ctx_create": (I32, [ct.POINTER(P), P, ct.c_size_t]),
+    "gk_ctx_destroy": (None, [P]),
+    "gk_ctx_set_stream": (I32, [P, P]),
+    "gk_set_math": (I32, [P, I32]),
+    "gk_sync": (I32, [P]),
+    "gk_last_error": (ct.c_char_p, [P]),
+    "gk_launch_count": (I64, [P]),
+    "gk_embedding_fwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
+    "gk_embedding_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
+    "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32]),
+    "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
+    "gk_gelu_fwd": (I32, [P, P, P, I64]),
+    "gk_gelu_bwd": (I32, [P, P, P, P, I64]),
+    "gk_matmul_fwd": (I32, [P, I32, P, I64, P, I64, I32, P, P, I64, P, I64, I32, I64, I64, I64, I32, P, I64]),
+    "gk_matmul_bwd": (I32, [P, I32, P, I64, P, I64, I32, P, I64, P, I64, I32, I32, P, I64, P, I64, P, I64, I64,
+                            I64]),
+    "gk_attn_fwd": (I32, [P, I32, P, P, P, I32, I32, I32, I32]),
+    "gk_attn_bwd": (I32, [P, I32, P, P, P, P, P, I32, I32, I32, I32]),
+    "gk_softmax_ce_fwd": (I32, [P, P, I64, P, P, P, I64, I32]),
+    "gk_softmax_ce_bwd": (I32, [P, P, I64, P, P, P, P, I64, I32, I64, I32]),
+    "gk_to_bf16": (I32, [P, P, P, I64]),
+    "gk_adamw_step": (I32, [P, ct.POINTER(gk_param), I32, F32, F32, F32, F32, F32, I32, I32]),
+    "gk_gpt_offset": (I64, [ct.POINTER(gk_gpt_cfg), I32, I32]),
+    "gk_gpt_numel": (I64, [ct.POINTER(gk_gpt_cfg)]),
+    "gk_gpt_n_decay": (I64, [ct.POINTER(gk_gpt_cfg)]),
+    "gk_kv_create": (I32, [P, ct.POINTER(P), ct.POINTER(gk_gpt_cfg), I32, I32]),
+    "gk_kv_destroy": (None, [P]),
+    "gk_kv_data": (P, [P]),
+    "gk_kv_length": (I32, [P]),
+    "gk_prefill": (I32, [P, P, P, P, I32, P]),
+    "gk_decode_step": (I32, [P, P, P, P, P, P, ct.POINTER(gk_sample_cfg)]),
+    "gk_sample": (I32, [P, P, P, I64, P, ct.POINTER(gk_sample_cfg)]),
+}
+
+EXPORTED = tuple(_SIGS)
+
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def _p(x):
+    """Address of a tensor / int / None for a pointer argument."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+class Ctx:
+    """A libgk context bound to a CUDA stream (an int handle or a torch.cuda.Stream)."""
+
+    def __init__(self, stream=0, workspace_bytes=64 << 20):
+        h = P()
+        s = stream if isinstance(stream, int) else stream.cuda_stream
+        _check(None, _lib.gk_ctx_create(ct.byref(h), P(s), workspace_bytes), "gk_ctx_create")
+        self.handle = h
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+    def set_stream(self, stream):
+        s = stream if isinstance(stream, int) else stream.cuda_stream
+        _check(self, _lib.gk_ctx_set_stream(self.handle, P(s)), "gk_ctx_set_stream")
+
+    def close(self):
+        if self.handle:
+            _lib.gk_ctx_destroy(self.handle)
+            self.handle = P()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _check(ctx, status, where):
+    if status != GK_OK:
+        msg = _lib.gk_last_error(ctx.handle).decode() if ctx is not None and ctx.handle else ""
+        raise GkError(status, where, msg)
+    return status
+
+
+# ------------------------------------------------------------------ entry points
+def gk_set_math(ctx, math):
+    return _check(ctx, _lib.gk_set_math(ctx.handle, math), "gk_set_math")
+
+
+def gk_sync(ctx):
+    return _check(ctx, _lib.gk_sync(ctx.handle), "gk_sync")
+
+
+def gk_launch_count(ctx):
+    return _lib.gk_launch_count(ctx.handle)
+
+
+def gk_embedding_fwd(ctx, ids, wte, wpe, x, B, T, C, V):
+    return _check(ctx, _lib.gk_embedding_fwd(ctx.handle, _p(ids), _p(wte), _p(wpe), _p(x), B, T, C, V),
+                  "gk_embedding_fwd")
+
+
+def gk_embedding_bwd(ctx, ids, dx, dwte, dwpe, B, T, C, V):
+    return _check(ctx, _lib.gk_embedding_bwd(ctx.handle, _p(ids), _p(dx), _p(dwte), _p(dwpe), B, T, C, V),
+                  "gk_embedding_bwd")
+
+
+def gk_layernorm_fwd(ctx, x, gamma, beta, y, y_dtype, mean, rstd, rows, C, eps=1e-5):
+    return _check(ctx, _lib.gk_layernorm_fwd(ctx.handle, _p(x), _p(gamma), _p(beta), _p(y), y_dtype, _p(mean),
+                                             _p(rstd), rows, C, eps), "gk_layernorm_fwd")
+
+
+def gk_layernorm_bwd(ctx, x, gamma, mean, rstd, dy, dx, accumulate_dx, dx_bf16, dgamma, dbeta, rows, C):
+    return _check(ctx, _lib.gk_layernorm_bwd(ctx.handle, _p(x), _p(gamma), _p(mean), _p(rstd), _p(dy), _p(dx),
+                                             int(accumulate_dx), _p(dx_bf16), _p(dgamma), _p(dbeta), rows, C),
+                  "gk_layernorm_bwd")
+
+
+def gk_gelu_fwd(ctx, x, y, n):
+    return _check(ctx, _lib.gk_gelu_fwd(ctx.handle, _p(x), _p(y), n), "gk_gelu_fwd")
+
+
+def gk_gelu_bwd(ctx, x, dy, dx, n):
+    return _check(ctx, _lib.gk_gelu_bwd(ctx.handle, _p(x), _p(dy), _p(dx), n), "gk_gelu_bwd")
+
+
+def gk_matmul_fwd(ctx, dtype, X, ldx, W, ldw, transW, bias, residual, ldr, Y, ldy, y_dtype, N, K, M,
+                  act=GK_ACT_NONE, preact=None, ldp=0):
+    return _check(ctx, _lib.gk_matmul_fwd(ctx.handle, dtype, _p(X), ldx, _p(W), ldw, int(transW), _p(bias),
+                                          _p(residual), ldr, _p(Y), ldy, y_dtype, N, K, M, act, _p(preact), ldp),
+                  "gk_matmul_fwd")
+
+
+def gk_matmul_bwd(ctx, dtype, X, ldx, W, ldw, transW, dY, lddy, dX, lddx, dx_dtype, accumulate_dX, preact_X, ldp,
+                  dW, lddw, dbias, N, K, M):
+    return _check(ctx, _lib.gk_matmul_bwd(ctx.handle, dtype, _p(X), ldx, _p(W), ldw, int(transW), _p(dY), lddy,
+                                          _p(dX), lddx, dx_dtype, int(accumulate_dX), _p(preact_X), ldp, _p(dW),
+                                          lddw, _p(dbias), N, K, M), "gk_matmul_bwd")
+
+
+def gk_attn_fwd(ctx, dtype, qkv, y, lse, B, T, H, hs):
+    return _check(ctx, _lib.gk_attn_fwd(ctx.handle, dtype, _p(qkv), _p(y), _p(lse), B, T, H, hs), "gk_attn_fwd")
+
+
+def gk_attn_bwd(ctx, dtype, qkv, y, lse, dy, dqkv, B, T, H, hs):
+    return _check(ctx, _lib.gk_attn_bwd(ctx.handle, dtype, _p(qkv), _p(y), _p(lse), _p(dy), _p(dqkv), B, T, H, hs),
+                  "gk_attn_bwd")
+
+
+def gk_softmax_ce_fwd(ctx, logits, ldl, targets, loss, lse, rows, V):
+    return _check(ctx, _lib.gk_softmax_ce_fwd(ctx.handle, _p(logits), ldl, _p(targets), _p(loss), _p(lse), rows, V),
+                  "gk_softmax_ce_fwd")
+
+
+def gk_softmax_ce_bwd(ctx, logits, ldl, targets, lse, dloss, dlogits, lddl, dl_dtype, rows, V):
+    return _check(ctx, _lib.gk_softmax_ce_bwd(ctx.handle, _p(logits), ldl, _p(targets), _p(lse), _p(dloss),
+                                              _p(dlogits), lddl, dl_dtype, rows, V), "gk_softmax_ce_bwd")
+
+
+def gk_to_bf16(ctx, x, y, n):
+    return _check(ctx, _lib.gk_to_bf16(ctx.handle, _p(x), _p(y), n), "gk_to_bf16")
+
+
+def gk_adamw_step(ctx, params, lr, beta1, beta2, eps, wd, step, zero_grad=False):
+    """params: a list of dicts with keys p, g, m, v, n, decay, p_bf16 (tensors or addresses)."""
+    arr = (gk_param * len(params))()
+    for i, q in enumerate(params):
+        arr[i] = gk_param(_p(q["p"]), _p(q["g"]), _p(q["m"]), _p(q["v"]), int(q["n"]), int(q.get("decay", 0)),
+                          _p(q.get("p_bf16")))
+    return _check(ctx, _lib.gk_adamw_step(ctx.handle, arr, len(params), lr, beta1, beta2, eps, wd, step,
+                                          int(zero_grad)), "gk_adamw_step")
+
+
+def _cfg(V, T, C, H, L):
+    return gk_gpt_cfg(V, T, C, H, L)
+
+
+def gk_gpt_offset(cfg, which, layer=0):
+    return _lib.gk_gpt_offset(ct.byref(cfg), which, layer)
+
+
+def gk_gpt_numel(cfg):
+    return _lib.gk_gpt_numel(ct.byref(cfg))
+
+
+def gk_gpt_n_decay(cfg):
+    return _lib.gk_gpt_n_decay(ct.byref(cfg))
+
+
+class KvCache:
+    """A libgk KV cache (gk_kv_create / gk_kv_destroy)."""
+
+    def __init__(self, ctx, cfg, B, Tmax):
+        h = P()
+        _check(ctx, _lib.gk_kv_create(ctx.handle, ct.byref(h), ct.byref(cfg), B, Tmax), "gk_kv_create")
+        self.handle, self.ctx = h, ctx
+
+    def data_ptr(self):
+        return _lib.gk_kv_data(self.handle)
+
+    def length(self):
+        return _lib.gk_kv_length(self.handle)
+
+    def close(self):
+        if self.handle:
+            _lib.gk_kv_destroy(self.handle)
+            self.handle = P()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _sample(s):
+    if s is None:
+        return None
+    top_k, temperature, seed, counter = s
+    return ct.byref(gk_sample_cfg(top_k, temperature, seed, counter))
+
+
+def gk_prefill(ctx, params, kv, ids, Tp, last_logits):
+    return _check(ctx, _lib.gk_prefill(ctx.handle, _p(params), kv.handle, _p(ids), Tp, _p(last_logits)),
+                  "gk_prefill")
+
+
+def gk_decode_step(ctx, params, kv, tokens, logits, next_ids, sample=None):
+    """sample: None (greedy) or (top_k, temperature, seed, counter)."""
+    return _check(ctx, _lib.gk_decode_step(ctx.handle, _p(params), kv.handle, _p(tokens), _p(logits), _p(next_ids),
+                                           _sample(sample)), "gk_decode_step")
+
+
+def gk_sample(ctx, kv, logits, ld, next_ids, sample=None):
+    return _check(ctx, _lib.gk_sample(ctx.handle, kv.handle, _p(logits), ld, _p(next_ids), _sample(sample)),
+                  "gk_sample")

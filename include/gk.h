@@ -1,0 +1,278 @@
+/*
+ * gk.h — C ABI of libgk: the forward, reverse-mode backward, AdamW update and KV-cache decode
+ * of a GPT-2-style decoder step, as hand-written CUDA kernels for one GB300 (sm_103a).
+ *
+ * Sources cited below (page title, then section):
+ *   [LM1] arabroot.io, "Build a language model in C# from scratch (1): the Autograd engine".
+ *   [LM4] arabroot.io, "Build a language model in C# from scratch (4): running GPT-2 weights".
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are row-major. A Linear weight is stored [in, out] ([LM4] "Loading weights into
+ *     our classes": the Conv1D layout, no transpose). `ld*` arguments are row strides in
+ *     elements (>= the row length), so padded rows (e.g. a vocabulary of 50257 stored with a
+ *     stride of 50304) are allowed.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; libgk never frees it.
+ *     Host pointers are named as such (`gk_param` arrays, `gk_gpt_cfg`, `gk_sample_cfg`).
+ *   - Every call is asynchronous on the context's CUDA stream, allocates nothing on the device
+ *     (context and KV-cache creation excepted) and never synchronises, so the calls can be
+ *     captured in a CUDA graph. Errors found on the host are returned at once; errors found by
+ *     a kernel (a token id outside the vocabulary, a bounded wait that gave up) set the
+ *     context's device error word and are returned by the next gk_sync.
+ *   - Backward calls ADD into parameter-gradient buffers ([LM1] "Why += and not =": a tensor
+ *     used twice receives the sum; the caller zeroes them, like ZeroGrad). Activation
+ *     gradients take an `accumulate` flag.
+ *   - dtype arguments take GK_F32 or GK_BF16 (bfloat16 stored as uint16_t bits).
+ */
+#ifndef GK_H
+#define GK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int gk_status;
+enum {
+    GK_OK = 0,
+    GK_ERR_ARG = 1,         /* null pointer, bad size, bad enum value */
+    GK_ERR_ALIGN = 2,       /* pointer or stride misses the kernel's alignment rule */
+    GK_ERR_UNSUPPORTED = 3, /* valid request this build has no kernel for */
+    GK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    GK_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (read back by gk_sync) */
+    GK_ERR_OVERFLOW = 6,    /* KV cache full */
+    GK_ERR_INDEX = 7,       /* a token id outside [0, V) (read back by gk_sync) */
+    GK_ERR_WORKSPACE = 8    /* the context's workspace is smaller than the call needs */
+};
+
+enum { GK_F32 = 0, GK_BF16 = 1 };
+/* Arithmetic of float32 GEMMs: plain fp32 FMA, or three TF32 tensor-core products with the
+ * operands split into high and low TF32 parts. Both are "faithful" (fp32-level) modes. */
+enum { GK_MATH_FP32 = 0, GK_MATH_3XTF32 = 1 };
+enum { GK_ACT_NONE = 0, GK_ACT_GELU = 1 };
+
+typedef struct gk_ctx gk_ctx;
+
+/* ------------------------------------------------------------------------------ context */
+
+/* Create a context bound to `cuda_stream` (a cudaStream_t; NULL = the legacy default
+ * stream) on the current device. It allocates a device error word and `workspace_bytes`
+ * of device scratch used by the calls that need scratch (each says how much). Returns
+ * GK_ERR_CUDA if an allocation fails. Not thread-safe: one context per host thread. */
+gk_status gk_ctx_create(gk_ctx** out, void* cuda_stream, size_t workspace_bytes);
+void gk_ctx_destroy(gk_ctx* ctx);
+/* Rebind the stream (e.g. to the stream a graph capture runs on). */
+gk_status gk_ctx_set_stream(gk_ctx* ctx, void* cuda_stream);
+/* GK_MATH_FP32 (default) or GK_MATH_3XTF32 for float32 GEMMs. */
+gk_status gk_set_math(gk_ctx* ctx, int math);
+/* Wait for the stream, then read and clear the device error word: returns the first kernel
+ * error recorded since the last gk_sync (GK_ERR_INDEX, GK_ERR_TIMEOUT, ...), else GK_OK. */
+gk_status gk_sync(gk_ctx* ctx);
+/* Human-readable text of the last host-side error of this context (static storage). */
+const char* gk_last_error(gk_ctx* ctx);
+/* Number of kernel launches this context has issued since creation. */
+int64_t gk_launch_count(gk_ctx* ctx);
+
+/* -------------------------------------------------------------------------- embedding */
+
+/* x[b*T + t, :] = wte[ids[b*T + t], :] + wpe[t, :].  [LM1] "Ops..." op table (Embedding);
+ * [LM4] "Generation with a KV cache" (the token row plus the position row).
+ * ids int32 [B*T]; wte [V, C]; wpe [>= T, C]; x [B*T, C] (all float32, contiguous).
+ * An id outside [0, V) writes zeros for its row and records GK_ERR_INDEX. */
+gk_status gk_embedding_fwd(gk_ctx* ctx, const int32_t* ids, const float* wte, const float* wpe,
+                           float* x, int B, int T, int C, int V);
+
+/* dwte[ids[r], :] += dx[r, :] and dwpe[r % T, :] += dx[r, :] for r = 0 .. B*T-1.
+ * Exact and deterministic: every gradient element receives its rows' float32 additions in
+ * ascending r, so the result is bit-identical to that sequential loop.
+ * [LM1] "Ops..." (Embedding backward scatter-adds); "Why += and not =". */
+gk_status gk_embedding_bwd(gk_ctx* ctx, const int32_t* ids, const float* dx, float* dwte,
+                           float* dwpe, int B, int T, int C, int V);
+
+/* -------------------------------------------------------------------------- layernorm */
+
+/* Per row: y = (x - mean) * rstd * gamma + beta, rstd = 1/sqrt(var + eps), var biased.
+ * [LM1] op table (LayerNorm); eps 1e-5 in GPT-2. x float32 [rows, C] contiguous; y is
+ * `y_dtype` [rows, C]; mean and rstd float32 [rows] (saved for backward, may be NULL). */
+gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, const float* beta,
+                           void* y, int y_dtype, float* mean, float* rstd, int64_t rows, int C,
+                           float eps);
+
+/* Backward of gk_layernorm_fwd for upstream dy (float32 [rows, C]):
+ *   dx (=, or += if accumulate_dx) rstd * (dy*gamma - mean(dy*gamma) - xhat*mean(dy*gamma*xhat));
+ *   dgamma += sum_rows dy*xhat;  dbeta += sum_rows dy   (deterministic order).
+ * dx_bf16, if not NULL, receives a bfloat16 copy of the resulting dx. dgamma/dbeta may be
+ * NULL. Workspace: 2 * C * P * 4 bytes, P = min(rows, 1216) partial slots (fewer for C > 1024). */
+gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, const float* mean,
+                           const float* rstd, const float* dy, float* dx, int accumulate_dx,
+                           uint16_t* dx_bf16, float* dgamma, float* dbeta, int64_t rows, int C);
+
+/* ------------------------------------------------------------------------------ GELU */
+
+/* y = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))) elementwise on float32 [n].
+ * [LM4] "Common mistakes": GPT-2 uses the tanh form ("gelu_new"), not the erf form. */
+gk_status gk_gelu_fwd(gk_ctx* ctx, const float* x, float* y, int64_t n);
+/* dx = dy * gelu'(x) (dx may alias dy). */
+gk_status gk_gelu_bwd(gk_ctx* ctx, const float* x, const float* dy, float* dx, int64_t n);
+
+/* ---------------------------------------------------------------------------- matmul */
+
+/* Y = act(X W + bias + residual) with X [N, K]; W [K, M] (transW = 0, MatMul) or W [M, K]
+ * (transW = 1, MatMulT: the tied LM head). [LM1] "Ops...", MatMul listing and op table.
+ *   dtype      GK_F32 (fp32 arithmetic per gk_set_math) or GK_BF16 (bf16 operands, fp32
+ *              accumulation on the tensor cores); X and W both have this type.
+ *   bias       float32 [M] or NULL.  residual  float32 [N, M] (stride ldr) or NULL; it may
+ *              alias Y when y_dtype is GK_F32 (in-place x += ...).
+ *   act        GK_ACT_GELU stores the pre-activation in `preact` (y_dtype, stride ldp) and
+ *              gelu(pre) in Y.
+ * bf16 operands need 16-byte aligned base pointers and strides that are multiples of 8. */
+gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W,
+                        int64_t ldw, int transW, const float* bias, const float* residual,
+                        int64_t ldr, void* Y, int64_t ldy, int y_dtype, int64_t N, int64_t K,
+                        int64_t M, int act, void* preact, int64_t ldp);
+
+/* Backward of Y = X W (transW = 0) or X W^T (transW = 1) for upstream dY [N, M]:
+ *   dX  = dY W^T (transW = 0) or dY W (transW = 1); written (=), or added (+=) if
+ *         accumulate_dX (float32 dX only). If preact_X is given (X was gelu(preact_X)),
+ *         dX = (dY W^T) * gelu'(preact_X): the GELU backward fused in. dX may be NULL.
+ *   dW += X^T dY ([K, M]) or dY^T X ([M, K]); float32; may be NULL.
+ *   dbias += sum over rows of dY; float32 [M]; may be NULL.
+ * [LM1] "Ops...", MatMul backward rule (dx = g w^T, dw = x^T g, both accumulating).
+ * dtype is the type of X, W and dY. Workspace for dbias: 64 * M * 4 bytes. */
+gk_status gk_matmul_bwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W,
+                        int64_t ldw, int transW, const void* dY, int64_t lddy, void* dX,
+                        int64_t lddx, int dx_dtype, int accumulate_dX, const void* preact_X,
+                        int64_t ldp, float* dW, int64_t lddw, float* dbias, int64_t N,
+                        int64_t K, int64_t M);
+
+/* ------------------------------------------------------------------------- attention */
+
+/* Causal multi-head self-attention of the fused projection qkv [B*T, 3C] (q, k, v in column
+ * blocks [0,C), [C,2C), [2C,3C); head h uses columns h*hs .. h*hs+hs-1 of each block):
+ * y[:, h] = softmax(q_h k_h^T / sqrt(hs), keys j <= query i) v_h, written to y [B*T, C];
+ * lse [B, H, T] float32 receives the log-sum-exp of each scaled score row (for backward).
+ * [LM1] op table (BatchMatMulT, CausalSoftmax, BatchMatMul, SplitHeads, MergeHeads);
+ * [LM4] "The 12 tensors we do not use" (the causal mask by arithmetic, visible = i + 1).
+ * dtype (GK_F32 / GK_BF16) is the type of qkv and y; scores and softmax are float32.
+ * hs must be a multiple of 4 and at most 128. */
+gk_status gk_attn_fwd(gk_ctx* ctx, int dtype, const void* qkv, void* y, float* lse, int B,
+                      int T, int H, int hs);
+
+/* dqkv [B*T, 3C] (written, same dtype) of gk_attn_fwd for upstream dy [B*T, C]: with
+ * P recomputed from q, k and lse, dv = P^T dy, dP = dy v^T, dS = P (dP - rowsum(dy * y)),
+ * dq = dS k / sqrt(hs), dk = dS^T q / sqrt(hs). Deterministic (no atomics).
+ * Workspace: B * H * T * 4 bytes. */
+gk_status gk_attn_bwd(gk_ctx* ctx, int dtype, const void* qkv, const void* y, const float* lse,
+                      const void* dy, void* dqkv, int B, int T, int H, int hs);
+
+/* ------------------------------------------------------------- softmax cross-entropy */
+
+/* loss (device float32 scalar, written) = mean over rows of (logsumexp(row) - row[target]);
+ * lse [rows] float32 receives each row's log-sum-exp. logits float32 [rows, V], stride ldl.
+ * [LM1] "Ops...", SoftmaxCrossEntropy listing. A target outside [0, V) records
+ * GK_ERR_INDEX. Workspace: rows * 4 bytes. */
+gk_status gk_softmax_ce_fwd(gk_ctx* ctx, const float* logits, int64_t ldl, const int32_t* targets,
+                            float* loss, float* lse, int64_t rows, int V);
+
+/* dlogits = (dloss / rows) (softmax(row) - onehot(target)), dloss a device float32 scalar
+ * (NULL = 1). dlogits has dl_dtype and stride lddl; columns V .. lddl-1 are written as 0.
+ * dlogits may alias logits when both are float32 with the same stride (in place).
+ * [LM1] "Ops...", SoftmaxCrossEntropy backward (probs minus one at the target). */
+gk_status gk_softmax_ce_bwd(gk_ctx* ctx, const float* logits, int64_t ldl, const int32_t* targets,
+                            const float* lse, const float* dloss, void* dlogits, int64_t lddl,
+                            int dl_dtype, int64_t rows, int V);
+
+/* Round float32 [n] to bfloat16 [n] (round to nearest even): the bf16 operand copy of a
+ * float32 tensor, e.g. the weights before the first step (AdamW refreshes it afterwards). */
+gk_status gk_to_bf16(gk_ctx* ctx, const float* x, uint16_t* y, int64_t n);
+
+/* ---------------------------------------------------------------------------- AdamW */
+
+/* One parameter block for gk_adamw_step (a host struct holding device pointers). */
+typedef struct {
+    float* p;          /* parameters, updated in place */
+    float* g;          /* gradient (zeroed after use if the call's zero_grad is set) */
+    float* m;          /* first moment */
+    float* v;          /* second moment */
+    int64_t n;         /* number of elements */
+    int decay;         /* 1: apply weight decay (tensors with >= 2 dims), 0: not */
+    uint16_t* p_bf16;  /* optional bfloat16 copy of the updated p, or NULL */
+} gk_param;
+
+/* AdamW at step `step` (>= 1) over n_params blocks (host array):
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;  mhat = m/(1-b1^step);  vhat = v/(1-b2^step);
+ *   p -= lr (mhat / (sqrt(vhat) + eps) + wd_k p),  wd_k = wd if decay else 0.
+ * [LM1] "The optimizer: from gradient to step", AdamW listing (Loshchilov & Hutter): decay
+ * applies to matrices only, and uses p before the update. zero_grad = 1 also sets g = 0
+ * (the ZeroGrad of the next step, fused). */
+gk_status gk_adamw_step(gk_ctx* ctx, const gk_param* params, int n_params, float lr, float beta1,
+                        float beta2, float eps, float wd, int step, int zero_grad);
+
+/* ------------------------------------------------------------------ flat GPT-2 layout */
+
+/* Model sizes: vocabulary, context (positions), width, heads, layers. */
+typedef struct { int V, T, C, H, L; } gk_gpt_cfg;
+
+enum {
+    GK_T_WTE = 0, GK_T_WPE, GK_T_LN1_W, GK_T_LN1_B, GK_T_ATTN_W, GK_T_ATTN_B, GK_T_ATTNPROJ_W,
+    GK_T_ATTNPROJ_B, GK_T_LN2_W, GK_T_LN2_B, GK_T_FC_W, GK_T_FC_B, GK_T_MLPPROJ_W,
+    GK_T_MLPPROJ_B, GK_T_LNF_W, GK_T_LNF_B, GK_T_COUNT
+};
+
+/* Parameters of a whole model live in ONE float32 buffer: first every tensor with >= 2 dims
+ * (wte, wpe, then per layer c_attn.w [C,3C], attn.c_proj.w [C,C], mlp.c_fc.w [C,4C],
+ * mlp.c_proj.w [4C,C]), then every vector (per layer ln_1.w, ln_1.b, c_attn.b, attn.c_proj.b,
+ * ln_2.w, ln_2.b, c_fc.b, mlp.c_proj.b; then ln_f.w, ln_f.b). So AdamW's decay boundary is
+ * one index. Gradients, moments and the bf16 copy use the same layout.
+ * Returns the element offset of tensor `which` of layer `layer` (ignored for wte, wpe and
+ * ln_f), or -1 for a bad argument. */
+int64_t gk_gpt_offset(const gk_gpt_cfg* cfg, int which, int layer);
+/* Total elements, V*C + T*C + L*(12 C^2 + 13 C) + 2 C. */
+int64_t gk_gpt_numel(const gk_gpt_cfg* cfg);
+/* Elements of the leading block of tensors with >= 2 dims (the decayed block). */
+int64_t gk_gpt_n_decay(const gk_gpt_cfg* cfg);
+
+/* ------------------------------------------------------------------- KV-cache decode */
+
+typedef struct gk_kv gk_kv;
+
+/* Sampling settings: top_k <= 0 or >= V keeps every logit; top_k == 1 or temperature <= 0
+ * is greedy (lowest index among the largest). Selection s of a cache draws
+ * u = Philox4x32-10(key = seed, counter = (counter + s, batch row, 0, 0)) word 0 >> 8, times
+ * 2^-24, and takes the first kept index whose running float64 sum of exp((l - max)/T)
+ * exceeds u times the total. [LM4] "Temperature and top-k". */
+typedef struct { int top_k; float temperature; uint64_t seed; uint64_t counter; } gk_sample_cfg;
+
+/* Allocate a float32 cache [L][2][B][H][Tmax][hs] plus the decode activations for B rows and
+ * prompts up to Tmax tokens. [LM4] "Generation with a KV cache" (one key and value row per
+ * layer per position). Owned by libgk; free with gk_kv_destroy. */
+gk_status gk_kv_create(gk_ctx* ctx, gk_kv** out, const gk_gpt_cfg* cfg, int B, int Tmax);
+void gk_kv_destroy(gk_kv* kv);
+/* Device pointer to the cache (layout above) and its current length (host mirror). */
+float* gk_kv_data(gk_kv* kv);
+int gk_kv_length(gk_kv* kv);
+
+/* Forget the cache contents and run a [B, Tp] prompt (ids int32, device) through one causal
+ * forward, writing every layer's keys and values and the logits of each row's LAST position
+ * to last_logits [B, V] (float32, stride V). Float32 weights in the flat layout. */
+gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t* ids, int Tp,
+                     float* last_logits);
+
+/* One token per row (tokens int32 [B], device) at position = the cache length: every layer
+ * appends its key and value and attends over all cached positions (no mask: the cache holds
+ * only the past), then ln_f and the tied head write logits [B, V]; if `next` is not NULL a
+ * selection (greedy if s is NULL) writes next [B]. The cache length advances by one.
+ * [LM4] "Generation with a KV cache" (Attention.Step, Gpt.Step). GK_ERR_OVERFLOW if full. */
+gk_status gk_decode_step(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t* tokens,
+                         float* logits, int32_t* next, const gk_sample_cfg* s);
+
+/* Select next [B] from logits [B, V] (stride ld) as gk_sample_cfg describes; the selection
+ * index s is the cache's selection count, which this advances by one. */
+gk_status gk_sample(gk_ctx* ctx, gk_kv* kv, const float* logits, int64_t ld, int32_t* next,
+                    const gk_sample_cfg* s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GK_H */

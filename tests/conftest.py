@@ -31,3 +31,33 @@ def golden_values(name="page_values.txt"):
 @pytest.fixture(scope="session")
 def page():
     return golden_values()
+
+
+@pytest.fixture(scope="session")
+def gkctx():
+    """A libgk context on the current torch stream (GPU tests only)."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    ctx = gk.Ctx(torch.cuda.current_stream().cuda_stream, workspace_bytes=256 << 20)
+    yield ctx
+    ctx.close()
+
+
+def rel_l2(a, b):
+    import numpy as np
+
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
+
+
+@pytest.fixture(autouse=True)
+def _float32_default_dtype():
+    """GPU buffers are allocated with torch's default dtype: keep it float32 for every test."""
+    import torch
+
+    torch.set_default_dtype(torch.float32)
+    yield

@@ -1,0 +1,159 @@
+"""KV-cache decode parity: prefill, decode steps and token selection against the oracle.
+
+Greedy ids are compared teacher-forced: both sides are fed the oracle's token at every step,
+and a step passes if the ids agree or the oracle's top-2 gap is below twice the measured
+logit error (a near-tie, reported, not failed). Top-k selection is checked bit-exactly by
+running the oracle's selection on the GPU's own logits with the same Philox draw.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import gpt as ogpt
+from oracle import sampling
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(gkctx, s, B, Tp, seed, Tmax):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+    from gpt_decoder_gb300.model import Gpt
+
+    prompt, params = synth.prompt_case(s, B, Tp, seed)
+    m = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, 1, mode="fp32")  # holds the flat parameters
+    m.load(params)
+    kv = gk.KvCache(gkctx, m.cfg, B, Tmax)
+    return prompt, params, m, kv
+
+
+def _teacher_forced(gkctx, s, B, Tp, n_steps, seed):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    prompt, params, m, kv = _setup(gkctx, s, B, Tp, seed, Tp + n_steps)
+    sh = ogpt.Shape(s.V, s.T, s.C, s.H, s.L)
+    # the oracle's greedy continuation, then both sides fed those tokens
+    picks, ologits = ogpt.generate(params, prompt, n_steps, sh, top_k=1)
+    logits = torch.empty(B, s.V, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    gk.gk_prefill(gkctx, m.params, kv, torch.as_tensor(prompt.reshape(-1)).cuda(), Tp, logits)
+    gk.gk_sample(gkctx, kv, logits, s.V, nxt, None)
+    got_logits, got_ids = [logits.cpu().numpy()], [nxt.cpu().numpy()]
+    for i in range(n_steps):
+        feed = torch.as_tensor(picks[i].astype(np.int32)).cuda()
+        gk.gk_decode_step(gkctx, m.params, kv, feed, logits, nxt, None)
+        got_logits.append(logits.cpu().numpy())
+        got_ids.append(nxt.cpu().numpy())
+    gk.gk_sync(gkctx)
+    assert kv.length() == Tp + n_steps
+    got_logits, got_ids = np.array(got_logits), np.array(got_ids)
+    err = np.abs(got_logits - ologits).max()
+    srt = np.sort(ologits, axis=-1)
+    gap = srt[..., -1] - srt[..., -2]
+    mismatch = got_ids != picks
+    near = mismatch & (gap < 2 * err)
+    kv.close()
+    return err, int(mismatch.sum()), int(near.sum()), got_ids, picks
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_tiny_decode_teacher_forced(gkctx, B):
+    err, mism, near, _, _ = _teacher_forced(gkctx, synth.TINY, B, 20, 40, 3)
+    assert err <= 5e-4
+    assert mism == near, (mism, near)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("B", [1, 16])
+def test_gpt2_decode_teacher_forced(gkctx, B):
+    err, mism, near, _, _ = _teacher_forced(gkctx, synth.GPT2_124M, B, 512, 256, 3)
+    print(f"gpt2 decode B={B}: max |logit diff| {err:.3e}, mismatched ids {mism}, near-ties {near}")
+    assert err <= 5e-4
+    assert mism == near
+
+
+def test_cached_decode_equals_training_forward(gkctx):
+    """The GPU's cached path reproduces its own full causal forward (fp32)."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+    from gpt_decoder_gb300.model import Gpt
+
+    s = synth.GptShape(V=64, T=32, C=96, H=4, L=2)
+    B, Tp, n = 2, 10, 12
+    prompt, params = synth.prompt_case(s, B, Tp + n, 5)
+    full = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, B, mode="fp32")
+    full.load(params)
+    ids = np.zeros((B, s.T), np.int32)
+    ids[:, : Tp + n] = prompt
+    d_ids = torch.as_tensor(ids.reshape(-1)).cuda()
+    full.forward(d_ids, d_ids)
+    ref = full.logits[:, : s.V].reshape(B, s.T, s.V).cpu().numpy()
+    kv = gk.KvCache(gkctx, full.cfg, B, Tp + n)
+    logits = torch.empty(B, s.V, device="cuda")
+    gk.gk_prefill(gkctx, full.params, kv, torch.as_tensor(prompt[:, :Tp].reshape(-1).copy()).cuda(), Tp, logits)
+    worst = np.abs(logits.cpu().numpy() - ref[:, Tp - 1]).max()
+    for i in range(n):
+        tok = torch.as_tensor(prompt[:, Tp + i].copy()).cuda()
+        gk.gk_decode_step(gkctx, full.params, kv, tok, logits, None, None)
+        worst = max(worst, np.abs(logits.cpu().numpy() - ref[:, Tp + i]).max())
+    gk.gk_sync(gkctx)
+    assert worst < 1e-4
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_decode_step(gkctx, full.params, kv, tok, logits, None, None)
+    assert e.value.status == gk.GK_ERR_OVERFLOW
+    kv.close()
+
+
+@pytest.mark.parametrize("top_k,temp", [(40, 1.0), (3, 0.7), (0, 1.0), (64, 2.0)])
+def test_topk_selection_matches_oracle_on_gpu_logits(gkctx, top_k, temp):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    s = synth.TINY
+    B = 4
+    prompt, params, m, kv = _setup(gkctx, s, B, 8, 9, 40)
+    logits = torch.empty(B, s.V, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    gk.gk_prefill(gkctx, m.params, kv, torch.as_tensor(prompt.reshape(-1)).cuda(), 8, logits)
+    seed, counter = 4, 100
+    for step in range(30):
+        gk.gk_decode_step(gkctx, m.params, kv, nxt if step else torch.as_tensor(prompt[:, -1].copy()).cuda(), logits,
+                          nxt, (top_k, temp, seed, counter))
+        lg = logits.cpu().numpy()
+        got = nxt.cpu().numpy()
+        for b in range(B):
+            # this selection's index is `step` (prefill made none)
+            u = sampling.uniform(seed, counter + step, b)
+            want = sampling.topk_sample(lg[b].astype(np.float64), top_k, temp, u)
+            assert got[b] == want, (step, b, got[b], want)
+    gk.gk_sync(gkctx)
+    kv.close()
+
+
+def test_topk_ties_are_kept_and_greedy_takes_lowest_index(gkctx):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    s = synth.GptShape(V=10, T=8, C=8, H=2, L=1)
+    cfg = gk.gk_gpt_cfg(s.V, s.T, s.C, s.H, s.L)
+    kv = gk.KvCache(gkctx, cfg, 3, 4)
+    row = np.array([0.5, 2.0, 1.0, 2.0, 1.0, 1.0, -3.0, 0.0, 1.0, -1.0], np.float32)
+    lg = torch.as_tensor(np.stack([row] * 3)).cuda()
+    nxt = torch.empty(3, dtype=torch.int32, device="cuda")
+    gk.gk_sample(gkctx, kv, lg, s.V, nxt, None)
+    assert list(nxt.cpu().numpy()) == [1, 1, 1]
+    for sel in range(40):
+        gk.gk_sample(gkctx, kv, lg, s.V, nxt, (3, 1.0, 11, 0))
+        got = nxt.cpu().numpy()
+        for b in range(3):
+            u = sampling.uniform(11, sel + 1, b)
+            assert got[b] == sampling.topk_sample(row, 3, 1.0, u)
+            assert row[got[b]] >= 1.0
+    gk.gk_sync(gkctx)
+    kv.close()

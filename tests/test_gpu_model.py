@@ -1,0 +1,125 @@
+"""Whole training-step parity (forward, backward, AdamW) of the libgk driver against the oracle.
+
+Workloads: the tiny character model (V=64, T=64, C=96, H=4, L=4, B=8, seed 0) in both modes,
+and the GPT-2-124M shape (B=4, T=1024, seed 2) in both modes. Tolerances: faithful (fp32)
+logits max-abs <= 5e-4, gradient relative-L2 <= 1e-4 per tensor; fast (bf16) logits
+max-abs <= 2e-2, gradient relative-L2 <= 1e-2.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import gpt as ogpt
+from tests.conftest import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp32": dict(logits=5e-4, grad=1e-4), "bf16": dict(logits=2e-2, grad=1e-2)}
+LR, WD = 3e-4, 0.01
+
+
+def _run_step(gkctx, s, B, seed, mode):
+    import torch
+
+    from gpt_decoder_gb300.model import Gpt
+
+    ids, targets, params = synth.training_case(s, B, seed)
+    m = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, B, mode=mode)
+    m.load(params)
+    d_ids = torch.as_tensor(ids.reshape(-1)).cuda()
+    d_tg = torch.as_tensor(targets.reshape(-1)).cuda()
+    loss = m.forward(d_ids, d_tg)
+    logits = m.logits[:, : s.V].cpu().numpy()
+    m.backward(d_ids, d_tg)
+    from gpt_decoder_gb300 import gk
+
+    gk.gk_sync(gkctx)
+    grads = {k: v.cpu().numpy() for k, v in m.named_slices(m.grads).items()}
+    m.adamw(LR, wd=WD, zero_grad=True)
+    gk.gk_sync(gkctx)
+    newp = {k: v.cpu().numpy() for k, v in m.named_slices(m.params).items()}
+    assert not m.grads.any().item(), "AdamW's fused ZeroGrad left a gradient"
+    return dict(loss=loss.item(), logits=logits, grads=grads, params=newp, inputs=(ids, targets, params))
+
+
+def _oracle(s, inputs):
+    ids, targets, params = inputs
+    sh = ogpt.Shape(s.V, s.T, s.C, s.H, s.L)
+    loss, grads, logits, _ = ogpt.loss_and_grads(params, ids, targets, sh)
+    newp, _ = ogpt.adamw_step(params, grads, {}, 1, LR, wd=WD)
+    return dict(loss=loss, logits=logits, grads=grads, params=newp)
+
+
+def _compare(got, ref, mode):
+    tol = TOL[mode]
+    assert abs(got["loss"] - ref["loss"]) < tol["logits"], (got["loss"], ref["loss"])
+    assert np.abs(got["logits"] - ref["logits"]).max() <= tol["logits"]
+    worst = max((rel_l2(got["grads"][k], ref["grads"][k]), k) for k in ref["grads"])
+    assert worst[0] <= tol["grad"], worst
+    # AdamW after one step: m_hat / sqrt(v_hat) = g / (|g| + eps), i.e. the sign of g once
+    # |g| >> eps, so an element whose gradient error is comparable to the gradient itself can
+    # move by 2 lr either way. The update is checked on elements whose gradient is clear:
+    # |g_ref| above 10x this element's own gradient error and above 100x AdamW's eps; the
+    # others are counted.
+    flips = 0
+    for k, p in ref["params"].items():
+        g = ref["grads"][k]
+        clear = (np.abs(g) > 10 * np.abs(got["grads"][k] - g)) & (np.abs(g) > 100 * 1e-8)
+        d = np.abs(got["params"][k] - p)
+        assert d[clear].max(initial=0.0) <= 1e-6 + 1e-3 * LR + 1e-6 * np.abs(p[clear]).max(initial=0.0), k
+        flips += int((d[~clear] > 1e-3 * LR).sum())
+    return worst, flips
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_tiny_training_step(gkctx, mode):
+    s = synth.TINY
+    got = _run_step(gkctx, s, 8, 0, mode)
+    ref = _oracle(s, got["inputs"])
+    worst, flips = _compare(got, ref, mode)
+    print(f"tiny {mode}: loss {got['loss']:.6f} vs {ref['loss']:.6f}; worst grad rel-L2 {worst}; "
+          f"small-gradient sign flips {flips}")
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_ragged_shapes_step(gkctx, mode):
+    # vocabulary, context and width that leave partial tiles everywhere
+    s = synth.GptShape(V=50, T=37, C=64, H=2, L=2)
+    got = _run_step(gkctx, s, 3, 11, mode)
+    ref = _oracle(s, got["inputs"])
+    _compare(got, ref, mode)
+
+
+_GPT2_ORACLE = {}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_gpt2_124m_training_step(gkctx, mode):
+    s = synth.GPT2_124M
+    got = _run_step(gkctx, s, 4, 2, mode)
+    if "ref" not in _GPT2_ORACLE:
+        _GPT2_ORACLE["ref"] = _oracle(s, got["inputs"])
+    ref = _GPT2_ORACLE["ref"]
+    worst, flips = _compare(got, ref, mode)
+    print(f"gpt2 {mode}: loss {got['loss']:.6f} vs {ref['loss']:.6f}; max |dlogits| "
+          f"{np.abs(got['logits'] - ref['logits']).max():.3e}; worst grad {worst}; flips {flips}")
+
+
+def test_loss_decreases_over_steps(gkctx):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+    from gpt_decoder_gb300.model import Gpt
+
+    s = synth.TINY
+    ids, targets, params = synth.training_case(s, 8, 0)
+    m = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, 8, mode="bf16")
+    m.load(params)
+    d_ids = torch.as_tensor(ids.reshape(-1)).cuda()
+    d_tg = torch.as_tensor(targets.reshape(-1)).cuda()
+    losses = []
+    for _ in range(20):
+        losses.append(m.train_step(d_ids, d_tg, 1e-3, 0.01).item())
+    gk.gk_sync(gkctx)
+    assert losses[-1] < losses[0] - 0.3, losses

@@ -1,0 +1,386 @@
+"""Single-op parity of libgk's CUDA kernels against the oracle, through the C ABI.
+
+Sizes cover the op sweep (MatMul/MatMulT at 256, 1024, 4096 and 4096x768x3072; LayerNorm,
+GELU and softmax-CE on [4096, 768] and [4096, 50257]) plus ragged shapes that leave partial
+tiles, and the degenerate cases. Tolerances: float32 kernels are compared with the float64
+oracle on the same float32 inputs; bf16-operand kernels with the oracle on the same
+bf16-rounded operands, so both measure the kernel's own accumulation error only.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import ops
+from tests.conftest import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _t():
+    import torch
+
+    return torch
+
+
+def dev(a, dtype=None):
+    torch = _t()
+    t = torch.as_tensor(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def host(t):
+    return t.float().cpu().numpy() if t.dtype != _t().int32 else t.cpu().numpy()
+
+
+def bf16_round(a):
+    torch = _t()
+    return torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def normal(seed, *shape, std=1.0):
+    return synth.Stream(seed).normal(int(np.prod(shape)), std).reshape(shape)
+
+
+# ----------------------------------------------------------------------- embedding
+@pytest.mark.parametrize("B,T,C,V", [(2, 5, 12, 9), (4, 1024, 768, 50257), (3, 7, 96, 3)])
+def test_embedding_fwd_exact(gkctx, B, T, C, V):
+    from gpt_decoder_gb300 import gk
+
+    st = synth.Stream(100 + C)
+    ids = st.ints(B * T, V).reshape(B, T)
+    wte, wpe = st.normal(V * C).reshape(V, C), st.normal(T * C).reshape(T, C)
+    x = _t().empty(B * T, C, device="cuda")
+    gk.gk_embedding_fwd(gkctx, dev(ids.reshape(-1)), dev(wte), dev(wpe), x, B, T, C, V)
+    gk.gk_sync(gkctx)
+    ref = ops.embedding_fwd(ids, wte, wpe).reshape(B * T, C).astype(np.float32)
+    assert np.array_equal(host(x), ref)
+
+
+def test_embedding_bad_id_reports_index_error(gkctx):
+    from gpt_decoder_gb300 import gk
+
+    x = _t().empty(2, 4, device="cuda")
+    ids = dev(np.array([1, 9], dtype=np.int32))
+    gk.gk_embedding_fwd(gkctx, ids, dev(np.ones((5, 4), np.float32)), dev(np.ones((2, 4), np.float32)), x, 1, 2, 4, 5)
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_sync(gkctx)
+    assert e.value.status == gk.GK_ERR_INDEX
+    gk.gk_sync(gkctx)  # the error word was cleared
+    assert np.array_equal(host(x)[1], np.zeros(4, np.float32))
+
+
+@pytest.mark.parametrize("B,T,C,V", [(3, 4, 6, 5), (8, 64, 96, 64), (4, 1024, 768, 50257), (16, 1024, 768, 50257)])
+def test_embedding_bwd_bit_exact(gkctx, B, T, C, V):
+    from gpt_decoder_gb300 import gk
+
+    st = synth.Stream(200 + B)
+    ids = st.ints(B * T, V).reshape(B, T)
+    if V > 1000:
+        ids[:, ::7] = 17  # many repeats of one token
+    dx = st.normal(B * T * C).reshape(B * T, C)
+    dwte0 = st.normal(V * C, 0.1).reshape(V, C)
+    dwpe0 = st.normal(T * C, 0.1).reshape(T, C)
+    g_te, g_pe = dev(dwte0), dev(dwpe0)
+    gk.gk_embedding_bwd(gkctx, dev(ids.reshape(-1)), dev(dx), g_te, g_pe, B, T, C, V)
+    gk.gk_sync(gkctx)
+    r_te, r_pe = dwte0.copy(), dwpe0.copy()
+    ops.embedding_bwd(ids, dx, r_te, r_pe)
+    assert np.array_equal(host(g_te), r_te)
+    assert np.array_equal(host(g_pe), r_pe)
+
+
+# ----------------------------------------------------------------------- layernorm
+@pytest.mark.parametrize("rows,C", [(4096, 768), (4096, 50257), (37, 96), (5, 130), (1, 1024), (3, 7)])
+@pytest.mark.parametrize("ydt", ["f32", "bf16"])
+def test_layernorm_fwd(gkctx, rows, C, ydt):
+    from gpt_decoder_gb300 import gk
+
+    if C == 50257 and ydt == "bf16":
+        pytest.skip("covered in float32")
+    x = normal(300 + C, rows, C) * 2 + 0.5
+    gm, bt = normal(301, C), normal(302, C)
+    torch = _t()
+    y = torch.empty(rows, C, device="cuda", dtype=torch.float32 if ydt == "f32" else torch.bfloat16)
+    mean, rstd = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+    gk.gk_layernorm_fwd(gkctx, dev(x), dev(gm), dev(bt), y, gk.GK_F32 if ydt == "f32" else gk.GK_BF16, mean, rstd,
+                        rows, C, 1e-5)
+    gk.gk_sync(gkctx)
+    ry, rm, rr = ops.layernorm_fwd(x, gm, bt)
+    tol = 2e-5 if ydt == "f32" else 2e-2
+    assert np.abs(host(y) - ry).max() < tol * max(1.0, np.abs(ry).max() / 4)
+    np.testing.assert_allclose(host(mean), rm, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(host(rstd), rr, rtol=2e-5)
+
+
+@pytest.mark.parametrize("rows,C", [(4096, 768), (4096, 50257), (37, 96), (5, 130), (1, 1024)])
+@pytest.mark.parametrize("acc", [0, 1])
+def test_layernorm_bwd(gkctx, rows, C, acc):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    x = normal(310 + C, rows, C) * 2 + 0.5
+    gm, bt = normal(311, C), normal(312, C)
+    g = normal(313, rows, C)
+    _, rm, rr = ops.layernorm_fwd(x, gm, bt)
+    dx0 = normal(314, rows, C)
+    dg0, db0 = normal(315, C), normal(316, C)
+    dx, dgm, dbt = dev(dx0), dev(dg0), dev(db0)
+    dxb = torch.empty(rows, C, device="cuda", dtype=torch.bfloat16)
+    gk.gk_layernorm_bwd(gkctx, dev(x), dev(gm), dev(rm.astype(np.float32)), dev(rr.astype(np.float32)), dev(g), dx,
+                        acc, dxb, dgm, dbt, rows, C)
+    gk.gk_sync(gkctx)
+    rdx, rdg, rdb = ops.layernorm_bwd(x, gm, rm.astype(np.float32), rr.astype(np.float32), g)
+    if acc:
+        rdx = rdx + dx0
+    assert rel_l2(host(dx), rdx) < 1e-5
+    assert rel_l2(host(dxb), host(dx)) < 5e-3
+    assert rel_l2(host(dgm), rdg + dg0) < 1e-5
+    assert rel_l2(host(dbt), rdb + db0) < 1e-5
+
+
+# ---------------------------------------------------------------------------- GELU
+@pytest.mark.parametrize("n", [4096 * 768, 4096 * 50257, 1, 1023])
+def test_gelu(gkctx, n):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    x = normal(400, n) * 3
+    g = normal(401, n)
+    y, dx = torch.empty(n, device="cuda"), torch.empty(n, device="cuda")
+    dxx = dev(x)
+    gk.gk_gelu_fwd(gkctx, dxx, y, n)
+    gk.gk_gelu_bwd(gkctx, dxx, dev(g), dx, n)
+    gk.gk_sync(gkctx)
+    assert np.abs(host(y) - ops.gelu_fwd(x)).max() < 1e-5
+    assert np.abs(host(dx) - ops.gelu_bwd(x, g)).max() < 2e-5
+
+
+# -------------------------------------------------------------------------- MatMul
+SWEEP = [(256, 256, 256), (1024, 1024, 1024), (4096, 4096, 4096), (4096, 768, 3072)]
+RAGGED = [(131, 67, 45), (1, 5, 3), (200, 1, 130), (129, 129, 257)]
+
+
+def _matmul_case(gkctx, N, K, M, transW, dt, bias, resid, act, seed):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    x = normal(seed, N, K)
+    w = normal(seed + 1, M, K) if transW else normal(seed + 1, K, M)
+    if dt == "bf16":
+        x, w = bf16_round(x), bf16_round(w)
+    b = normal(seed + 2, M) if bias else None
+    r = normal(seed + 3, N, M) if resid else None
+    gdt = gk.GK_F32 if dt == "f32" else gk.GK_BF16
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    y = torch.empty(N, M, device="cuda")
+    pre = torch.empty(N, M, device="cuda") if act else None
+    gk.gk_matmul_fwd(gkctx, gdt, dev(x, tdt), K, dev(w, tdt), w.shape[1], transW, None if b is None else dev(b),
+                     None if r is None else dev(r), M, y, M, gk.GK_F32, N, K, M,
+                     gk.GK_ACT_GELU if act else gk.GK_ACT_NONE, pre, M)
+    gk.gk_sync(gkctx)
+    ref = ops.matmul_t_fwd(x, w) if transW else ops.matmul_fwd(x, w)
+    if b is not None:
+        ref = ref + b
+    if r is not None:
+        ref = ref + r
+    if act:
+        assert rel_l2(host(pre), ref) < 2e-5
+        ref = ops.gelu_fwd(ref)
+    return host(y), ref
+
+
+@pytest.mark.parametrize("N,K,M", SWEEP + RAGGED)
+@pytest.mark.parametrize("transW", [0, 1])
+def test_matmul_fwd_f32(gkctx, N, K, M, transW):
+    y, ref = _matmul_case(gkctx, N, K, M, transW, "f32", True, False, False, 500)
+    assert rel_l2(y, ref) < 2e-5
+
+
+@pytest.mark.parametrize("N,K,M", [(4096, 768, 3072), (512, 96, 288), (131, 67, 45), (256, 256, 256)])
+@pytest.mark.parametrize("transW", [0, 1])
+def test_matmul_fwd_bf16_operands(gkctx, N, K, M, transW):
+    y, ref = _matmul_case(gkctx, N, K, M, transW, "bf16", True, False, False, 510)
+    assert rel_l2(y, ref) < 2e-5
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_matmul_fwd_epilogues(gkctx, dt):
+    y, ref = _matmul_case(gkctx, 300, 96, 384, 0, dt, True, True, False, 520)
+    assert rel_l2(y, ref) < 2e-5
+    y, ref = _matmul_case(gkctx, 300, 96, 384, 0, dt, True, False, True, 530)
+    assert rel_l2(y, ref) < 2e-5
+
+
+def _matmul_bwd_case(gkctx, N, K, M, transW, dt, acc, gelu, seed):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    x = normal(seed, N, K)
+    w = normal(seed + 1, M, K) if transW else normal(seed + 1, K, M)
+    g = normal(seed + 2, N, M)
+    pre = normal(seed + 3, N, K) if gelu else None
+    if dt == "bf16":
+        x, w, g = bf16_round(x), bf16_round(w), bf16_round(g)
+        if gelu:
+            pre = bf16_round(pre)
+    gdt = gk.GK_F32 if dt == "f32" else gk.GK_BF16
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    dx0 = normal(seed + 4, N, K)
+    dw0 = normal(seed + 5, *w.shape)
+    db0 = normal(seed + 6, M)
+    dx, dw, db = dev(dx0), dev(dw0), dev(db0)
+    gk.gk_matmul_bwd(gkctx, gdt, dev(x, tdt), K, dev(w, tdt), w.shape[1], transW, dev(g, tdt), M, dx, K, gk.GK_F32,
+                     acc, None if pre is None else dev(pre, tdt), K, dw, w.shape[1], db, N, K, M)
+    gk.gk_sync(gkctx)
+    rdx, rdw = (ops.matmul_t_bwd(x, w, g) if transW else ops.matmul_bwd(x, w, g))
+    if gelu:
+        rdx = ops.gelu_bwd(pre, rdx)
+    if acc:
+        rdx = rdx + dx0
+    return (host(dx), rdx), (host(dw), rdw + dw0), (host(db), ops.bias_bwd(g) + db0)
+
+
+@pytest.mark.parametrize("N,K,M", SWEEP + RAGGED)
+@pytest.mark.parametrize("transW", [0, 1])
+def test_matmul_bwd_f32(gkctx, N, K, M, transW):
+    (dx, rdx), (dw, rdw), (db, rdb) = _matmul_bwd_case(gkctx, N, K, M, transW, "f32", 0, False, 600)
+    assert rel_l2(dx, rdx) < 2e-5
+    assert rel_l2(dw, rdw) < 2e-5
+    assert rel_l2(db, rdb) < 2e-5
+
+
+@pytest.mark.parametrize("N,K,M", [(4096, 768, 3072), (512, 96, 288), (131, 67, 45)])
+@pytest.mark.parametrize("transW", [0, 1])
+def test_matmul_bwd_bf16_operands(gkctx, N, K, M, transW):
+    (dx, rdx), (dw, rdw), (db, rdb) = _matmul_bwd_case(gkctx, N, K, M, transW, "bf16", 1, False, 610)
+    assert rel_l2(dx, rdx) < 2e-5
+    assert rel_l2(dw, rdw) < 2e-5
+    assert rel_l2(db, rdb) < 2e-5
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_matmul_bwd_fused_gelu(gkctx, dt):
+    (dx, rdx), _, _ = _matmul_bwd_case(gkctx, 300, 384, 96, 0, dt, 0, True, 620)
+    assert rel_l2(dx, rdx) < (2e-5 if dt == "f32" else 5e-3)
+
+
+def test_matmul_rejects_bad_strides(gkctx):
+    from gpt_decoder_gb300 import gk
+
+    x = _t().zeros(4, 4, device="cuda")
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_matmul_fwd(gkctx, gk.GK_F32, x, 3, x, 4, 0, None, None, 0, x, 4, gk.GK_F32, 4, 4, 4)
+    assert e.value.status == gk.GK_ERR_ARG
+
+
+# ----------------------------------------------------------------------- attention
+ATTN = [(2, 64, 4, 24), (1, 77, 2, 64), (2, 1024, 12, 64), (1, 1, 3, 32), (3, 33, 2, 8)]
+
+
+def _attn_inputs(B, T, H, hs, seed, dt):
+    qkv = normal(seed, B, T, 3 * H * hs)
+    dy = normal(seed + 1, B, T, H * hs)
+    if dt == "bf16":
+        qkv, dy = bf16_round(qkv), bf16_round(dy)
+    return qkv, dy
+
+
+@pytest.mark.parametrize("B,T,H,hs", ATTN)
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_attention_fwd_bwd(gkctx, B, T, H, hs, dt):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    qkv, dy = _attn_inputs(B, T, H, hs, 700 + T, dt)
+    gdt = gk.GK_F32 if dt == "f32" else gk.GK_BF16
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    C = H * hs
+    d_qkv = dev(qkv.reshape(B * T, 3 * C), tdt)
+    y = torch.empty(B * T, C, device="cuda", dtype=tdt)
+    lse = torch.empty(B * H * T, device="cuda")
+    gk.gk_attn_fwd(gkctx, gdt, d_qkv, y, lse, B, T, H, hs)
+    ry, P, rl = ops.attention_fwd(qkv, H)
+    gk.gk_sync(gkctx)
+    tol_y = 2e-5 if dt == "f32" else 8e-3
+    assert rel_l2(host(y), ry.reshape(B * T, C)) < tol_y
+    np.testing.assert_allclose(host(lse), rl.reshape(-1), rtol=1e-5, atol=1e-5)
+    dqkv = torch.empty(B * T, 3 * C, device="cuda", dtype=tdt)
+    # backward from the oracle's own y (so the test isolates the backward kernel)
+    y_in = dev(ry.reshape(B * T, C), tdt)
+    gk.gk_attn_bwd(gkctx, gdt, d_qkv, y_in, dev(rl.reshape(-1).astype(np.float32)), dev(dy.reshape(B * T, C), tdt),
+                   dqkv, B, T, H, hs)
+    gk.gk_sync(gkctx)
+    rd = ops.attention_bwd(qkv, P, dy, H).reshape(B * T, 3 * C)
+    assert rel_l2(host(dqkv), rd) < (5e-5 if dt == "f32" else 1e-2)
+
+
+# --------------------------------------------------------- softmax cross-entropy
+@pytest.mark.parametrize("rows,V,ldl", [(4096, 768, 768), (4096, 50257, 50257), (4096, 50257, 50304), (7, 3, 8),
+                                        (1, 64, 64)])
+@pytest.mark.parametrize("dl_dt", ["f32", "bf16"])
+def test_softmax_ce(gkctx, rows, V, ldl, dl_dt):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    x = np.zeros((rows, ldl), np.float32)
+    x[:, :V] = normal(800 + V, rows, V) * 3
+    x[:, V:] = np.nan  # padding is never read
+    tg = synth.Stream(801).ints(rows, V)
+    loss = torch.zeros(1, device="cuda")
+    lse = torch.empty(rows, device="cuda")
+    dx = dev(x)
+    gk.gk_softmax_ce_fwd(gkctx, dx, ldl, dev(tg), loss, lse, rows, V)
+    rloss, rlse = ops.softmax_ce_fwd(x[:, :V], tg)
+    gk.gk_sync(gkctx)
+    assert abs(loss.item() - rloss) < 1e-5 * max(1.0, abs(rloss))
+    np.testing.assert_allclose(host(lse), rlse, rtol=1e-6, atol=1e-5)
+    dloss = dev(np.array([0.75], np.float32))
+    tdt = torch.float32 if dl_dt == "f32" else torch.bfloat16
+    dl = torch.full((rows, ldl), 7.0, device="cuda", dtype=tdt)
+    gk.gk_softmax_ce_bwd(gkctx, dx, ldl, dev(tg), dev(rlse.astype(np.float32)), dloss, dl, ldl,
+                         gk.GK_F32 if dl_dt == "f32" else gk.GK_BF16, rows, V)
+    gk.gk_sync(gkctx)
+    rd = ops.softmax_ce_bwd(x[:, :V], tg, rlse.astype(np.float32), 0.75)
+    got = host(dl)
+    assert rel_l2(got[:, :V], rd) < (1e-5 if dl_dt == "f32" else 5e-3)
+    assert np.all(got[:, V:] == 0)
+
+
+def test_softmax_ce_in_place(gkctx):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    rows, V = 64, 1000
+    x = normal(810, rows, V)
+    tg = synth.Stream(811).ints(rows, V)
+    dx = dev(x)
+    loss, lse = torch.zeros(1, device="cuda"), torch.empty(rows, device="cuda")
+    gk.gk_softmax_ce_fwd(gkctx, dx, V, dev(tg), loss, lse, rows, V)
+    gk.gk_softmax_ce_bwd(gkctx, dx, V, dev(tg), lse, None, dx, V, gk.GK_F32, rows, V)
+    gk.gk_sync(gkctx)
+    _, rlse = ops.softmax_ce_fwd(x, tg)
+    assert rel_l2(host(dx), ops.softmax_ce_bwd(x, tg, rlse, 1.0)) < 1e-5
+
+
+# ---------------------------------------------------------------------------- AdamW
+@pytest.mark.parametrize("n", [1, 7, 4096 * 768 + 3])
+def test_adamw(gkctx, n):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    p0, g, m0 = normal(900, n), normal(901, n), normal(902, n, std=0.1)
+    v0 = np.abs(normal(903, n, std=0.1))
+    p, dg, m, v = dev(p0), dev(g), dev(m0), dev(v0)
+    pb = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    for decay in (1, 0):
+        p.copy_(dev(p0)); m.copy_(dev(m0)); v.copy_(dev(v0)); dg.copy_(dev(g))
+        gk.gk_adamw_step(gkctx, [dict(p=p, g=dg, m=m, v=v, n=n, decay=decay, p_bf16=pb)], 3e-4, 0.9, 0.999, 1e-8,
+                         0.01, 5, zero_grad=True)
+        gk.gk_sync(gkctx)
+        rp, rm, rv = ops.adamw(p0, g, m0, v0, 5, 3e-4, 0.9, 0.999, 1e-8, 0.01 if decay else 0.0)
+        assert np.abs(host(p) - rp).max() <= 1e-6 * np.abs(rp).max()
+        assert rel_l2(host(m), rm) < 1e-6 and rel_l2(host(v), rv) < 1e-6
+        assert not host(dg).any()
+        assert rel_l2(host(pb), host(p)) < 5e-3

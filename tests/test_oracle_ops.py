@@ -10,7 +10,6 @@ import synth
 from oracle import ops
 from oracle.scalar_ad import Var, vsum
 
-torch.set_default_dtype(torch.float64)
 
 
 def _rng(seed):

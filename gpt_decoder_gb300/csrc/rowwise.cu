@@ -789,3 +789,87 @@ gk_status gk_adamw_step(gk_ctx* ctx, const gk_param* params, int n_params, float
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- LayerNorm backward without allocation
+// Some callers cannot call cudaMalloc at all: a host framework that owns every byte of device
+// memory through its own pool, a latency-critical loop that must never enter the allocator,
+// or a plugin loaded into a process whose memory budget was fixed before it arrived. They can
+// pass the inputs and outputs they own, but not the scratch this operation needs for its
+// per-block partial sums of dgamma and dbeta. gk_layernorm_bwd_noalloc takes that scratch
+// from one fixed array compiled into the library instead of from a context's workspace.
+//
+// The array is file-scope device memory of GK_LN_NOALLOC_SCRATCH_FLOATS floats (4 MiB). Every
+// GPU that loads this library keeps it until the process exits. In host code its name only
+// stands for it: the device address comes from cudaGetSymbolAddress, looked up once per device
+// on the first call made with that device current.
+namespace {
+constexpr int64_t GK_LN_NOALLOC_SCRATCH_FLOATS = 1 << 20;
+static __device__ __align__(256) float g_ln_noalloc_scratch[GK_LN_NOALLOC_SCRATCH_FLOATS];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+float* g_ln_noalloc_addr[NOALLOC_MAX_DEVICES] = {nullptr};
+
+gk_status ln_noalloc_scratch(float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GK_ERR_CUDA;
+    if (!g_ln_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ln_noalloc_scratch) != cudaSuccess || !p) return GK_ERR_CUDA;
+        g_ln_noalloc_addr[dev] = static_cast<float*>(p);
+    }
+    *out = g_ln_noalloc_addr[dev];
+    return GK_OK;
+}
+}  // namespace
+
+extern "C" gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x, const float* gamma,
+                                              const float* mean, const float* rstd, const float* dy, float* dx,
+                                              int accumulate_dx, uint16_t* dx_bf16, float* dgamma, float* dbeta,
+                                              int64_t rows, int C) {
+    if (!x || !gamma || !mean || !rstd || !dy || !dx || rows <= 0 || C <= 0) return GK_ERR_ARG;
+    // at least one partial slot of 2 x C floats must fit in the fixed array
+    if ((int64_t)2 * C > GK_LN_NOALLOC_SCRATCH_FLOATS) return GK_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    bool want_partials = dgamma || dbeta;
+    float* partial = nullptr;
+    if (want_partials) GK_TRY(ln_noalloc_scratch(&partial));
+    int64_t slots = GK_LN_NOALLOC_SCRATCH_FLOATS / ((int64_t)2 * C);
+    int num_sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return GK_ERR_CUDA;
+    bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(dy) && aligned16(dx) &&
+                     aligned16(gamma) && (!dx_bf16 || ((uintptr_t)dx_bf16 & 7) == 0);
+    int nparts;
+    if (warp_path) {
+        nparts = (int)std::min<int64_t>(std::min<int64_t>(cdiv(rows, 8), (int64_t)num_sms * 4),
+                                        std::min<int64_t>(1216, slots));
+        int vpt = C / 128;
+        size_t smem = want_partials ? (size_t)8 * 2 * C * sizeof(float) : 0;
+        switch (vpt) {
+#define LN_NA_CASE(V)                                                                                        \
+    case V:                                                                                                  \
+        if (cudaFuncSetAttribute(layernorm_bwd_warp_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                                 (int)smem) != cudaSuccess)                                                  \
+            return GK_ERR_CUDA;                                                                              \
+        layernorm_bwd_warp_kernel<V><<<nparts, 8 * 32, smem, stream>>>(                                      \
+            x, gamma, mean, rstd, dy, dx, accumulate_dx, (__nv_bfloat16*)dx_bf16, partial, rows, C);         \
+        break;
+            LN_NA_CASE(1) LN_NA_CASE(2) LN_NA_CASE(3) LN_NA_CASE(4)
+            LN_NA_CASE(5) LN_NA_CASE(6) LN_NA_CASE(7) LN_NA_CASE(8)
+#undef LN_NA_CASE
+        }
+    } else {
+        nparts = (int)std::min<int64_t>(rows, std::min<int64_t>(1216, slots));
+        layernorm_bwd_block_kernel<<<nparts, 512, 0, stream>>>(x, gamma, mean, rstd, dy, dx, accumulate_dx,
+                                                              (__nv_bfloat16*)dx_bf16, partial, rows, C);
+    }
+    if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
+    if (want_partials) {
+        // every slot the reduction reads was written in full by the kernel above
+        reduce_partials_kernel<<<(unsigned)cdiv(C, 256), 256, 0, stream>>>(partial, nparts, C, dgamma, dbeta);
+        if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
+    }
+    return GK_OK;
+}

@@ -62,6 +62,7 @@ _SIGS = {
     "gk_embedding_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32]),
     "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
+    "gk_layernorm_bwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
     "gk_gelu_fwd": (I32, [P, P, P, I64]),
     "gk_gelu_bwd": (I32, [P, P, P, P, I64]),
     "gk_matmul_fwd": (I32, [P, I32, P, I64, P, I64, I32, P, P, I64, P, I64, I32, I64, I64, I64, I32, P, I64]),
@@ -170,6 +171,15 @@ def gk_layernorm_bwd(ctx, x, gamma, mean, rstd, dy, dx, accumulate_dx, dx_bf16, 
     return _check(ctx, _lib.gk_layernorm_bwd(ctx.handle, _p(x), _p(gamma), _p(mean), _p(rstd), _p(dy), _p(dx),
                                              int(accumulate_dx), _p(dx_bf16), _p(dgamma), _p(dbeta), rows, C),
                   "gk_layernorm_bwd")
+
+
+def gk_layernorm_bwd_noalloc(stream, x, gamma, mean, rstd, dy, dx, accumulate_dx, dx_bf16, dgamma, dbeta, rows, C):
+    """gk_layernorm_bwd with its scratch in the library's fixed array; `stream` is a cudaStream_t
+    (int) or a torch.cuda.Stream. Returns the status code (GkError on failure)."""
+    s = stream if isinstance(stream, int) else stream.cuda_stream
+    return _check(None, _lib.gk_layernorm_bwd_noalloc(P(s), _p(x), _p(gamma), _p(mean), _p(rstd), _p(dy), _p(dx),
+                                                      int(accumulate_dx), _p(dx_bf16), _p(dgamma), _p(dbeta),
+                                                      rows, C), "gk_layernorm_bwd_noalloc")
 
 
 def gk_gelu_fwd(ctx, x, y, n):

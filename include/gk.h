@@ -108,6 +108,28 @@ gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, cons
                            const float* rstd, const float* dy, float* dx, int accumulate_dx,
                            uint16_t* dx_bf16, float* dgamma, float* dbeta, int64_t rows, int C);
 
+/* LayerNorm backward that allocates nothing (no counterpart on the pages: it serves callers
+ * that cannot allocate device memory). Same arguments, layout and results as
+ * gk_layernorm_bwd, but it takes a CUDA stream (cudaStream_t, NULL = legacy default) instead
+ * of a context, and its dgamma/dbeta partial sums live in a fixed 4 MiB array compiled into
+ * the library rather than in a workspace.
+ *   Who needs it: code that cannot call cudaMalloc, e.g. a host framework that owns all device
+ *   memory through its own pool, a loop that must never block in the allocator, or a plugin
+ *   whose process fixed its memory budget before loading it.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ *   capture. The array stays allocated on every GPU that loads the library until exit.
+ *   Limits: C <= 524288 (one partial slot of 2*C floats must fit); larger C returns
+ *   GK_ERR_WORKSPACE. Nothing in the array needs to start at zero: each call writes every
+ *   partial slot before reading it, and the array keeps the last call's contents.
+ *   Concurrency: all calls share the one array per device, so calls whose kernels overlap on
+ *   the GPU (other streams, other host threads) race on it; serialise them.
+ * Returns GK_ERR_ARG for null pointers or sizes <= 0, GK_ERR_CUDA if a CUDA call fails. */
+gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x, const float* gamma,
+                                   const float* mean, const float* rstd, const float* dy, float* dx,
+                                   int accumulate_dx, uint16_t* dx_bf16, float* dgamma, float* dbeta,
+                                   int64_t rows, int C);
+
 /* ------------------------------------------------------------------------------ GELU */
 
 /* y = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))) elementwise on float32 [n].

@@ -1,13 +1,463 @@
-// Tensor-core GEMM for sm_103a (tcgen05 + TMA + TMEM). Not yet enabled: every call falls
-// back to the CUDA-core kernel.
+// Tensor-core GEMM for sm_103a: C[M,N] (=|+=) epi(A B + bias + residual) with bfloat16 A and
+// B of either majorness, float32 accumulation in tensor memory (TMEM).
+//
+// Persistent kernel, one 192-thread CTA per SM, 128 x 256 output tiles:
+//   warp 0     TMA producer: streams 64-deep K slices of A and B into a 4-stage shared-memory
+//              ring (128-byte swizzled tiles), arriving on full[s] with the byte count;
+//   warp 1     MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16, kind::f16) into
+//              one of two TMEM accumulators, commits stage releases to empty[s] and a finished
+//              accumulator to tmem_full[b]; the warp also allocates and frees the 512 TMEM
+//              columns;
+//   warps 2-5  epilogue: tcgen05.ld of their 32 accumulator rows, bias / residual / GELU /
+//              GELU-backward, store, then arrive on tmem_empty[b] so the next tile's MMAs can
+//              reuse the accumulator while this one is drained.
+// Work units are (tile, K split); split K is used only for plain float32 accumulation
+// (dW += ...), whose epilogue adds with atomics.
+// Every mbarrier wait is bounded (about one second): on expiry the CTA records GK_ERR_TIMEOUT
+// in the context's error word, waits briefly for its own TMA copies and MMAs in flight, frees
+// its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "gemm.cuh"
 
 namespace gk {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;         // 16 KB per stage
+constexpr uint32_t B_BYTES = BN * BK * 2;         // 32 KB per stage
+constexpr uint32_t TMEM_COLS = 2 * BN;            // two float32 accumulators of 128 x 256
+constexpr size_t SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
+constexpr uint64_t WAIT_NS = 1000000000ull;       // bounded waits: 1 s
+constexpr uint64_t DRAIN_NS = 200000000ull;       // after an abort: 0.2 s per drain wait
+
+struct TcParams {
+    int M, N, K;
+    int tiles_m, tiles_n, splits, kbps, kblocks;
+    int a_kmajor, b_kmajor;
+    void* C;
+    int64_t ldc;
+    int c_dtype, accumulate, atomic_out;
+    const float* bias;
+    const float* residual;
+    int64_t ldr;
+    int epi;
+    void* aux;
+    int64_t ldaux;
+    int aux_dtype;
+    int* err;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity; false on timeout or when another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (globaltimer() - t0 > limit) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            saddr(dst)),
+        "l"((uint64_t)map), "r"(saddr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: start, leading / stride byte offsets (>> 4), version 1,
+// 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: float32 D, bf16 A and B, majorness, N >> 3, M >> 4.
+__device__ __forceinline__ uint32_t instr_desc(bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// --------------------------------------------------------------------- epilogue
+template <typename TC>
+__device__ __forceinline__ void store_row32(const TcParams& p, int64_t m, int64_t n0, const uint32_t (&r)[32]) {
+    TC* C = static_cast<TC*>(p.C);
+    if (p.atomic_out) {
+        float* Cf = static_cast<float*>(p.C);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            int64_t n = n0 + j;
+            if (n < p.N) atomicAdd(Cf + m * p.ldc + n, __uint_as_float(r[j]));
+        }
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        int64_t n = n0 + j;
+        if (n >= p.N) break;
+        float v = __uint_as_float(r[j]);
+        int64_t ci = m * p.ldc + n;
+        if (p.accumulate) v += load_as_f32(C + ci);
+        if (p.bias) v += p.bias[n];
+        if (p.residual) v += p.residual[m * p.ldr + n];
+        if (p.epi == EPI_GELU) {
+            if (p.aux_dtype == GK_F32)
+                static_cast<float*>(p.aux)[m * p.ldaux + n] = v;
+            else
+                static_cast<__nv_bfloat16*>(p.aux)[m * p.ldaux + n] = __float2bfloat16_rn(v);
+            v = gelu_tanh(v);
+        } else if (p.epi == EPI_DGELU) {
+            float pre = p.aux_dtype == GK_F32
+                            ? static_cast<const float*>(p.aux)[m * p.ldaux + n]
+                            : __bfloat162float(static_cast<const __nv_bfloat16*>(p.aux)[m * p.ldaux + n]);
+            v *= gelu_tanh_grad(pre);
+        }
+        store_from_f32(C + ci, v);
+    }
+}
+
+__device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, int& tn, int& kb0, int& kb1) {
+    int split = u % p.splits, tile = u / p.splits;
+    tm = tile % p.tiles_m;
+    tn = tile / p.tiles_m;
+    kb0 = split * p.kbps;
+    kb1 = min(p.kblocks, kb0 + p.kbps);
+}
+
+template <typename TC>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTES));
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = bars + 2 * STAGES + 2;
+    uint64_t* drain = bars + 2 * STAGES + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 6);
+
+    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int units = p.tiles_m * p.tiles_n * p.splits;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+            uint32_t it = 0;
+            int issued_ph[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued_ph[s] = -1;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int tm, tn, kb0, kb1;
+                unit_coords(p, u, tm, tn, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    int s = it % STAGES;
+                    uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
+                    uint8_t* a = sA + s * A_BYTES;
+                    uint8_t* b = sB + s * B_BYTES;
+                    if (p.a_kmajor) {
+                        tma_load_2d(&tmA, &full[s], a, kb * BK, tm * BM);
+                    } else {
+                        tma_load_2d(&tmA, &full[s], a, tm * BM, kb * BK);
+                        tma_load_2d(&tmA, &full[s], a + 8192, tm * BM + 64, kb * BK);
+                    }
+                    if (p.b_kmajor) {
+                        tma_load_2d(&tmB, &full[s], b, kb * BK, tn * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j) tma_load_2d(&tmB, &full[s], b + j * 8192, tn * BN + 64 * j, kb * BK);
+                    }
+                    issued_ph[s] = (int)ph;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(p.err, GK_ERR_TIMEOUT);
+                // let this CTA's copies in flight land before shared memory is released
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_ph[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_ph[s], nullptr, DRAIN_NS);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc(!p.a_kmajor, !p.b_kmajor);
+            // per 16-deep K step: K-major operands advance 32 bytes inside the swizzled row,
+            // MN-major operands advance two 8-row core-matrix groups (2 x 1024 bytes)
+            const uint32_t a_step = p.a_kmajor ? 32u : 2048u;
+            const uint32_t b_step = p.b_kmajor ? 32u : 2048u;
+            const uint32_t a_lbo = p.a_kmajor ? 16u : 8192u, b_lbo = p.b_kmajor ? 16u : 8192u;
+            uint32_t it = 0, j = 0;
+            bool ok = true, issued = false;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+                int tm, tn, kb0, kb1;
+                unit_coords(p, u, tm, tn, kb0, kb1);
+                uint32_t buf = j & 1, aph = (j >> 1) & 1;
+                if (!mbar_wait(&tempty[buf], aph ^ 1, abort_flag, WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t d_tmem = tmem_base + buf * BN;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    int s = it % STAGES;
+                    uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(&full[s], ph, abort_flag, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t a0 = saddr(sA + s * A_BYTES), b0 = saddr(sB + s * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        uint64_t ad = smem_desc(a0 + k * a_step, a_lbo, 1024);
+                        uint64_t bd = smem_desc(b0 + k * b_step, b_lbo, 1024);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                umma_commit(&tfull[buf]);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(p.err, GK_ERR_TIMEOUT);
+                if (issued) {
+                    umma_commit(drain);
+                    mbar_wait(drain, 0, nullptr, DRAIN_NS);
+                }
+            }
+        }
+    } else {
+        // epilogue warps 2..5; a warp may read TMEM lanes 32 * (warp % 4) .. + 31
+        int q = warp & 3;
+        int row = q * 32 + lane;
+        uint32_t j = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+            int tm, tn, kb0, kb1;
+            unit_coords(p, u, tm, tn, kb0, kb1);
+            uint32_t buf = j & 1, aph = (j >> 1) & 1;
+            if (!mbar_wait(&tfull[buf], aph, abort_flag, WAIT_NS)) {
+                *abort_flag = 1;
+                report(p.err, GK_ERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            int64_t m = (int64_t)tm * BM + row;
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + c0, r);
+                int64_t n0 = (int64_t)tn * BN + c0;
+                if (m < p.M && n0 < p.N) store_row32<TC>(p, m, n0, r);
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[buf]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    }
+}
+
+// ------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map: inner (contiguous) extent, outer extent, row stride in elements,
+// box {64, box_outer}, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
-    (void)ctx;
-    (void)g;
-    return GK_ERR_UNSUPPORTED;
+    if (g.ab_dtype != GK_BF16) return GK_ERR_UNSUPPORTED;
+    if (!aligned16(g.A) || !aligned16(g.B) || (g.lda & 7) || (g.ldb & 7)) return GK_ERR_UNSUPPORTED;
+    if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K >= (1ll << 31))
+        return GK_ERR_UNSUPPORTED;
+    CUtensorMap ta, tb;
+    bool ok = g.a_kmajor ? make_map(&ta, g.A, g.K, g.M, g.lda, BM) : make_map(&ta, g.A, g.M, g.K, g.lda, 64);
+    ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, BN) : make_map(&tb, g.B, g.N, g.K, g.ldb, 64));
+    if (!ok) return GK_ERR_UNSUPPORTED;
+    TcParams p{};
+    p.M = (int)g.M;
+    p.N = (int)g.N;
+    p.K = (int)g.K;
+    p.tiles_m = (int)cdiv(g.M, BM);
+    p.tiles_n = (int)cdiv(g.N, BN);
+    p.kblocks = (int)cdiv(g.K, BK);
+    p.a_kmajor = g.a_kmajor;
+    p.b_kmajor = g.b_kmajor;
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.c_dtype = g.c_dtype;
+    p.accumulate = g.accumulate;
+    p.bias = g.bias;
+    p.residual = g.residual;
+    p.ldr = g.ldr;
+    p.epi = g.epi;
+    p.aux = g.aux;
+    p.ldaux = g.ldaux;
+    p.aux_dtype = g.aux_dtype;
+    p.err = ctx->d_err;
+    int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+    p.splits = 1;
+    bool plain_acc = g.accumulate && g.c_dtype == GK_F32 && !g.bias && !g.residual && g.epi == EPI_NONE;
+    if (plain_acc && tiles < ctx->num_sms) {
+        int want = (int)cdiv(2 * (int64_t)ctx->num_sms, tiles);
+        int maxs = std::max(1, p.kblocks / 4);
+        p.splits = std::max(1, std::min(want, maxs));
+    }
+    p.kbps = (int)cdiv(p.kblocks, p.splits);
+    p.splits = (int)cdiv(p.kblocks, p.kbps);
+    p.atomic_out = p.splits > 1;
+    int64_t units = tiles * p.splits;
+    int grid = (int)std::min<int64_t>(units, ctx->num_sms);
+    if (g.c_dtype == GK_F32) {
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(gemm_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+            attr = true;
+        }
+        gemm_tc_kernel<float><<<grid, THREADS, SMEM_BYTES, ctx->stream>>>(ta, tb, p);
+    } else {
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(gemm_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES);
+            attr = true;
+        }
+        gemm_tc_kernel<__nv_bfloat16><<<grid, THREADS, SMEM_BYTES, ctx->stream>>>(ta, tb, p);
+    }
+    return launched(ctx, "gemm_tc");
 }
 
 }  // namespace gk

@@ -11,7 +11,7 @@
 // float32. Scores, softmax and accumulation are float32.
 #include <math.h>
 
-#include "common.cuh"
+#include "gemm.cuh"
 
 using namespace gk;
 
@@ -269,6 +269,8 @@ gk_status gk_attn_fwd(gk_ctx* ctx, int dtype, const void* qkv, void* y, float* l
     if (dtype == GK_F32) {
         GK_HS_SWITCH(hs, fwd_typed, float, ctx, qkv, y, lse, B, T, H)
     } else {
+        gk_status s = attn_fwd_tc(ctx, qkv, y, lse, B, T, H, hs);
+        if (s != GK_ERR_UNSUPPORTED) return s;
         GK_HS_SWITCH(hs, fwd_typed, __nv_bfloat16, ctx, qkv, y, lse, B, T, H)
     }
     return fail(ctx, GK_ERR_UNSUPPORTED, "gk_attn_fwd: head size %d not built (8,16,24,32,48,64,96,128)", hs);

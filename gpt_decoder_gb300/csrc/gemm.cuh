@@ -44,6 +44,9 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g);
 // Dispatch by operand type, arithmetic mode and shape.
 gk_status gemm(gk_ctx* ctx, const Gemm& g);
 
+// Tensor-core causal attention forward (bf16 q/k/v, head size 64); GK_ERR_UNSUPPORTED otherwise.
+gk_status attn_fwd_tc(gk_ctx* ctx, const void* qkv, void* y, float* lse, int B, int T, int H, int hs);
+
 // dst[n] += sum over rows of src[r, n] (deterministic, float32 result).
 gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_t rows, int64_t cols, float* dst);
 

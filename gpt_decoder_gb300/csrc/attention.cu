@@ -283,6 +283,10 @@ gk_status gk_attn_bwd(gk_ctx* ctx, int dtype, const void* qkv, const void* y, co
                "gk_attn_bwd: bad argument");
     GK_REQUIRE(ctx, dtype == GK_F32 || dtype == GK_BF16, GK_ERR_ARG, "gk_attn_bwd: bad dtype");
     GK_REQUIRE(ctx, (int64_t)B * H < 65536, GK_ERR_UNSUPPORTED, "gk_attn_bwd: B*H too large");
+    if (dtype == GK_BF16) {
+        gk_status s = attn_bwd_tc(ctx, qkv, y, lse, dy, dqkv, B, T, H, hs);
+        if (s != GK_ERR_UNSUPPORTED) return s;
+    }
     float* dvec = (float*)workspace(ctx, (size_t)B * H * T * sizeof(float));
     GK_REQUIRE(ctx, dvec, GK_ERR_WORKSPACE, "gk_attn_bwd: needs %lld workspace bytes", (long long)B * H * T * 4);
     if (dtype == GK_F32) {

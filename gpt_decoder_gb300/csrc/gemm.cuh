@@ -46,6 +46,9 @@ gk_status gemm(gk_ctx* ctx, const Gemm& g);
 
 // Tensor-core causal attention forward (bf16 q/k/v, head size 64); GK_ERR_UNSUPPORTED otherwise.
 gk_status attn_fwd_tc(gk_ctx* ctx, const void* qkv, void* y, float* lse, int B, int T, int H, int hs);
+// Tensor-core causal attention backward (bf16, head size 64); GK_ERR_UNSUPPORTED otherwise.
+gk_status attn_bwd_tc(gk_ctx* ctx, const void* qkv, const void* y, const float* lse, const void* dy, void* dqkv,
+                      int B, int T, int H, int hs);
 
 // dst[n] += sum over rows of src[r, n] (deterministic, float32 result).
 gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_t rows, int64_t cols, float* dst);

@@ -3,6 +3,7 @@
 // Operand majorness covers every product of the decoder step without transpose passes:
 //   A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m];
 //   B(k,n) = B[n*ldb + k] when b_kmajor, else B[k*ldb + n].
+// A bf16 operand may come with a low plane (split bf16, about 16 significant bits); see Gemm.
 // Epilogues: EPI_GELU stores the pre-activation v to `aux` and gelu(v) to C; EPI_DGELU
 // stores v * gelu'(aux) (the backward of a GELU fused into the GEMM producing its input
 // gradient).
@@ -34,6 +35,12 @@ struct Gemm {
     void* aux = nullptr;
     int64_t ldaux = 0;
     int aux_dtype = GK_F32;
+    // split-bf16 operands: a low plane (value - bf16(value)) with the same layout as A / B;
+    // the product then adds A_hi B_lo + A_lo B_hi to A_hi B_hi (bf16 operands only)
+    const void* A_lo = nullptr;
+    const void* B_lo = nullptr;
+    // > 0 with bf16 C: C's low plane (v - bf16(v)) is also written, at C + c_plane elements
+    int64_t c_plane = 0;
 };
 
 // CUDA-core (SIMT) kernel: float32 or bfloat16 operands, float32 FMA accumulation.

@@ -13,8 +13,8 @@ constexpr int BM = 128, BN = 128, BK = 8, THREADS = 256;
 constexpr int PAD = 4;
 
 template <typename T, bool KMAJOR>
-__device__ __forceinline__ void load_tile(const T* __restrict__ P, int64_t ld, int64_t rows, int64_t K, int64_t row0,
-                                          int64_t k0, float (*S)[BM + PAD]) {
+__device__ __forceinline__ void load_tile(const T* __restrict__ P, const T* __restrict__ Plo, int64_t ld, int64_t rows,
+                                          int64_t K, int64_t row0, int64_t k0, float (*S)[BM + PAD]) {
     int t = threadIdx.x;
     if (KMAJOR) {
         // element (r, k) at P[r*ld + k]: thread loads 4 consecutive k of one row
@@ -24,7 +24,10 @@ __device__ __forceinline__ void load_tile(const T* __restrict__ P, int64_t ld, i
         for (int i = 0; i < 4; ++i) {
             int64_t gk = k0 + kk + i;
             float v = 0.f;
-            if (gr < rows && gk < K) v = load_as_f32(P + gr * ld + gk);
+            if (gr < rows && gk < K) {
+                v = load_as_f32(P + gr * ld + gk);
+                if (Plo) v += load_as_f32(Plo + gr * ld + gk);
+            }
             S[kk + i][r] = v;
         }
     } else {
@@ -35,7 +38,10 @@ __device__ __forceinline__ void load_tile(const T* __restrict__ P, int64_t ld, i
         for (int i = 0; i < 4; ++i) {
             int64_t gr = row0 + r + i;
             float v = 0.f;
-            if (gr < rows && gk < K) v = load_as_f32(P + gk * ld + gr);
+            if (gr < rows && gk < K) {
+                v = load_as_f32(P + gk * ld + gr);
+                if (Plo) v += load_as_f32(Plo + gk * ld + gr);
+            }
             S[kk][r + i] = v;
         }
     }
@@ -61,6 +67,10 @@ __device__ __forceinline__ void epilogue_store(const Gemm& g, int64_t m, int64_t
         v *= gelu_tanh_grad(pre);
     }
     store_from_f32(C + ci, v);
+    if (g.c_plane) {
+        __nv_bfloat16* Cb = reinterpret_cast<__nv_bfloat16*>(C);
+        Cb[ci + g.c_plane] = __float2bfloat16_rn(v - __bfloat162float(Cb[ci]));
+    }
 }
 
 template <typename TA, bool AK, bool BKM, typename TC>
@@ -69,6 +79,8 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(const Gemm g) {
     __shared__ float Bs[2][BK][BN + PAD];
     const TA* A = static_cast<const TA*>(g.A);
     const TA* B = static_cast<const TA*>(g.B);
+    const TA* Alo = static_cast<const TA*>(g.A_lo);
+    const TA* Blo = static_cast<const TA*>(g.B_lo);
     int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
     int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     float acc[8][8];
@@ -78,14 +90,14 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(const Gemm g) {
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
     int64_t ktiles = (g.K + BK - 1) / BK;
-    load_tile<TA, AK>(A, g.lda, g.M, g.K, m0, 0, As[0]);
-    load_tile<TA, BKM>(B, g.ldb, g.N, g.K, n0, 0, Bs[0]);
+    load_tile<TA, AK>(A, Alo, g.lda, g.M, g.K, m0, 0, As[0]);
+    load_tile<TA, BKM>(B, Blo, g.ldb, g.N, g.K, n0, 0, Bs[0]);
     __syncthreads();
     for (int64_t kt = 0; kt < ktiles; ++kt) {
         int cur = kt & 1;
         if (kt + 1 < ktiles) {
-            load_tile<TA, AK>(A, g.lda, g.M, g.K, m0, (kt + 1) * BK, As[cur ^ 1]);
-            load_tile<TA, BKM>(B, g.ldb, g.N, g.K, n0, (kt + 1) * BK, Bs[cur ^ 1]);
+            load_tile<TA, AK>(A, Alo, g.lda, g.M, g.K, m0, (kt + 1) * BK, As[cur ^ 1]);
+            load_tile<TA, BKM>(B, Blo, g.ldb, g.N, g.K, n0, (kt + 1) * BK, Bs[cur ^ 1]);
         }
 #pragma unroll
         for (int k = 0; k < BK; ++k) {

@@ -24,11 +24,22 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 192;
-constexpr uint32_t A_BYTES = BM * BK * 2;         // 16 KB per stage
-constexpr uint32_t B_BYTES = BN * BK * 2;         // 32 KB per stage
+constexpr int BM = 128, BN = 256, BK = 64, THREADS = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;         // 16 KB per operand tile
+constexpr uint32_t B_BYTES = BN * BK * 2;         // 32 KB per operand tile
 constexpr uint32_t TMEM_COLS = 2 * BN;            // two float32 accumulators of 128 x 256
-constexpr size_t SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
+
+// Stage layout per split mode: bit 0 = A has a low bf16 plane, bit 1 = B has one. A stage
+// holds [A_hi | A_lo? | B_hi | B_lo?]; the ring shrinks to keep within 227 KB of shared memory.
+template <int SPLIT>
+struct StageCfg {
+    static constexpr bool A_LO = (SPLIT & 1) != 0, B_LO = (SPLIT & 2) != 0;
+    static constexpr uint32_t A_SLOT = A_BYTES * (A_LO ? 2 : 1);
+    static constexpr uint32_t B_SLOT = B_BYTES * (B_LO ? 2 : 1);
+    static constexpr uint32_t STAGE = A_SLOT + B_SLOT;
+    static constexpr int STAGES = SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2);
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 256;
+};
 constexpr uint64_t WAIT_NS = 1000000000ull;       // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;       // after an abort: 0.2 s per drain wait
 
@@ -46,6 +57,7 @@ struct TcParams {
     void* aux;
     int64_t ldaux;
     int aux_dtype;
+    int64_t c_plane;  // > 0: bf16 C also gets its low plane (v - bf16(v)) at C + c_plane
     int* err;
 };
 
@@ -84,6 +96,10 @@ __device__ __forceinline__ void store_row32(const TcParams& p, int64_t m, int64_
             v *= gelu_tanh_grad(pre);
         }
         store_from_f32(C + ci, v);
+        if (p.c_plane) {
+            __nv_bfloat16* Cb = static_cast<__nv_bfloat16*>(p.C);
+            Cb[ci + p.c_plane] = __float2bfloat16_rn(v - __bfloat162float(Cb[ci]));
+        }
     }
 }
 
@@ -95,14 +111,17 @@ __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, i
     kb1 = min(p.kblocks, kb0 + p.kbps);
 }
 
-template <typename TC>
+template <typename TC, int SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmA_lo, const __grid_constant__ CUtensorMap tmB_lo,
+                   const TcParams p) {
+    using SC = StageCfg<SPLIT>;
+    constexpr int STAGES = SC::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * (A_BYTES + B_BYTES));
+    // stage s: A_hi at smem + s*STAGE, A_lo at + A_BYTES, B_hi at + A_SLOT, B_lo at + A_SLOT + B_BYTES
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * SC::STAGE);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -139,6 +158,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+            if (SC::A_LO) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA_lo) : "memory");
+            if (SC::B_LO) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB_lo) : "memory");
             uint32_t it = 0;
             int issued_ph[STAGES];
             for (int s = 0; s < STAGES; ++s) issued_ph[s] = -1;
@@ -153,20 +174,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
-                    uint8_t* a = sA + s * A_BYTES;
-                    uint8_t* b = sB + s * B_BYTES;
-                    if (p.a_kmajor) {
-                        tma_load_2d(&tmA, &full[s], a, kb * BK, tm * BM);
-                    } else {
-                        tma_load_2d(&tmA, &full[s], a, tm * BM, kb * BK);
-                        tma_load_2d(&tmA, &full[s], a + 8192, tm * BM + 64, kb * BK);
-                    }
-                    if (p.b_kmajor) {
-                        tma_load_2d(&tmB, &full[s], b, kb * BK, tn * BN);
-                    } else {
+                    mbar_expect_tx(&full[s], SC::STAGE);
+                    uint8_t* a = smem + s * SC::STAGE;
+                    uint8_t* b = a + SC::A_SLOT;
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j) tma_load_2d(&tmB, &full[s], b + j * 8192, tn * BN + 64 * j, kb * BK);
+                    for (int pl = 0; pl < (SC::A_LO ? 2 : 1); ++pl) {
+                        const CUtensorMap* ma = pl ? &tmA_lo : &tmA;
+                        uint8_t* dst = a + pl * A_BYTES;
+                        if (p.a_kmajor) {
+                            tma_load_2d(ma, &full[s], dst, kb * BK, tm * BM);
+                        } else {
+                            tma_load_2d(ma, &full[s], dst, tm * BM, kb * BK);
+                            tma_load_2d(ma, &full[s], dst + 8192, tm * BM + 64, kb * BK);
+                        }
+                    }
+#pragma unroll
+                    for (int pl = 0; pl < (SC::B_LO ? 2 : 1); ++pl) {
+                        const CUtensorMap* mb = pl ? &tmB_lo : &tmB;
+                        uint8_t* dst = b + pl * B_BYTES;
+                        if (p.b_kmajor) {
+                            tma_load_2d(mb, &full[s], dst, kb * BK, tn * BN);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_load_2d(mb, &full[s], dst + j * 8192, tn * BN + 64 * j, kb * BK);
+                        }
                     }
                     issued_ph[s] = (int)ph;
                 }
@@ -207,12 +239,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    uint32_t a0 = saddr(sA + s * A_BYTES), b0 = saddr(sB + s * B_BYTES);
+                    uint32_t a0 = saddr(smem + s * SC::STAGE), b0 = a0 + SC::A_SLOT;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         uint64_t ad = smem_desc(a0 + k * a_step, a_lbo, 1024);
                         uint64_t bd = smem_desc(b0 + k * b_step, b_lbo, 1024);
                         umma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        // split operands: + A_hi B_lo + A_lo B_hi (the A_lo B_lo term is dropped)
+                        if (SC::B_LO)
+                            umma_bf16(d_tmem, ad, smem_desc(b0 + B_BYTES + k * b_step, b_lbo, 1024), idesc, 1u);
+                        if (SC::A_LO)
+                            umma_bf16(d_tmem, smem_desc(a0 + A_BYTES + k * a_step, a_lbo, 1024), bd, idesc, 1u);
                     }
                     issued = true;
                     umma_commit(&empty[s]);
@@ -263,6 +300,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+template <typename TC, int SPLIT>
+void launch_one(gk_ctx* ctx, int grid, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& al,
+                const CUtensorMap& bl, const TcParams& p) {
+    static bool attr = false;
+    constexpr size_t smem = StageCfg<SPLIT>::SMEM;
+    if (!attr) {
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
+    }
+    gemm_tc_kernel<TC, SPLIT><<<grid, THREADS, smem, ctx->stream>>>(a, b, al, bl, p);
+}
+
+template <typename TC>
+void launch_split(gk_ctx* ctx, int split, int grid, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& al,
+                  const CUtensorMap& bl, const TcParams& p) {
+    switch (split) {
+        case 0: launch_one<TC, 0>(ctx, grid, a, b, al, bl, p); break;
+        case 1: launch_one<TC, 1>(ctx, grid, a, b, al, bl, p); break;
+        case 2: launch_one<TC, 2>(ctx, grid, a, b, al, bl, p); break;
+        default: launch_one<TC, 3>(ctx, grid, a, b, al, bl, p); break;
+    }
+}
+
 }  // namespace
 
 gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
@@ -295,6 +355,8 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.ldaux = g.ldaux;
     p.aux_dtype = g.aux_dtype;
     p.err = ctx->d_err;
+    p.c_plane = g.c_plane;
+    if ((g.A_lo && (!aligned16(g.A_lo))) || (g.B_lo && !aligned16(g.B_lo))) return GK_ERR_UNSUPPORTED;
     int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
     p.splits = 1;
     bool plain_acc = g.accumulate && g.c_dtype == GK_F32 && !g.bias && !g.residual && g.epi == EPI_NONE;
@@ -308,22 +370,16 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.atomic_out = p.splits > 1;
     int64_t units = tiles * p.splits;
     int grid = (int)std::min<int64_t>(units, ctx->num_sms);
-    if (g.c_dtype == GK_F32) {
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(gemm_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-            attr = true;
-        }
-        gemm_tc_kernel<float><<<grid, THREADS, SMEM_BYTES, ctx->stream>>>(ta, tb, p);
-    } else {
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(gemm_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES);
-            attr = true;
-        }
-        gemm_tc_kernel<__nv_bfloat16><<<grid, THREADS, SMEM_BYTES, ctx->stream>>>(ta, tb, p);
-    }
+    int split = (g.A_lo ? 1 : 0) | (g.B_lo ? 2 : 0);
+    CUtensorMap ta_lo = ta, tb_lo = tb;
+    if (g.A_lo && !(g.a_kmajor ? make_map(&ta_lo, g.A_lo, g.K, g.M, g.lda, BM) : make_map(&ta_lo, g.A_lo, g.M, g.K, g.lda, 64)))
+        return GK_ERR_UNSUPPORTED;
+    if (g.B_lo && !(g.b_kmajor ? make_map(&tb_lo, g.B_lo, g.K, g.N, g.ldb, BN) : make_map(&tb_lo, g.B_lo, g.N, g.K, g.ldb, 64)))
+        return GK_ERR_UNSUPPORTED;
+    if (g.c_dtype == GK_F32)
+        launch_split<float>(ctx, split, grid, ta, tb, ta_lo, tb_lo, p);
+    else
+        launch_split<__nv_bfloat16>(ctx, split, grid, ta, tb, ta_lo, tb_lo, p);
     return launched(ctx, "gemm_tc");
 }
 

@@ -62,15 +62,18 @@ gk_status gemm(gk_ctx* ctx, const Gemm& g) {
 using namespace gk;
 
 static bool dtype_ok(int d) { return d == GK_F32 || d == GK_BF16; }
+static bool out_dtype_ok(int d) { return d == GK_F32 || d == GK_BF16 || d == GK_BF16X2; }
 
 extern "C" {
 
 gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W, int64_t ldw, int transW,
                         const float* bias, const float* residual, int64_t ldr, void* Y, int64_t ldy, int y_dtype,
-                        int64_t N, int64_t K, int64_t M, int act, void* preact, int64_t ldp) {
+                        int64_t N, int64_t K, int64_t M, int act, void* preact, int64_t ldp, const void* X_lo,
+                        const void* W_lo) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, X && W && Y && N >= 0 && K >= 0 && M >= 0, GK_ERR_ARG, "gk_matmul_fwd: bad argument");
-    GK_REQUIRE(ctx, dtype_ok(dtype) && dtype_ok(y_dtype), GK_ERR_ARG, "gk_matmul_fwd: bad dtype");
+    GK_REQUIRE(ctx, dtype_ok(dtype) && out_dtype_ok(y_dtype), GK_ERR_ARG, "gk_matmul_fwd: bad dtype");
+    GK_REQUIRE(ctx, (!X_lo && !W_lo) || dtype == GK_BF16, GK_ERR_ARG, "gk_matmul_fwd: low planes need bf16 operands");
     GK_REQUIRE(ctx, ldx >= K && ldy >= M && ldw >= (transW ? K : M), GK_ERR_ARG, "gk_matmul_fwd: stride too small");
     GK_REQUIRE(ctx, !residual || ldr >= M, GK_ERR_ARG, "gk_matmul_fwd: residual stride too small");
     GK_REQUIRE(ctx, act == GK_ACT_NONE || (act == GK_ACT_GELU && preact && ldp >= M), GK_ERR_ARG,
@@ -83,10 +86,12 @@ gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, cons
     g.A = X; g.lda = ldx; g.a_kmajor = true;
     g.B = W; g.ldb = ldw; g.b_kmajor = transW != 0;
     g.ab_dtype = dtype;
-    g.C = Y; g.ldc = ldy; g.c_dtype = y_dtype;
+    g.C = Y; g.ldc = ldy; g.c_dtype = y_dtype == GK_BF16X2 ? GK_BF16 : y_dtype;
+    if (y_dtype == GK_BF16X2) g.c_plane = N * ldy;
     g.bias = bias; g.residual = residual; g.ldr = ldr;
+    g.A_lo = X_lo; g.B_lo = W_lo;
     if (act == GK_ACT_GELU) {
-        g.epi = EPI_GELU; g.aux = preact; g.ldaux = ldp; g.aux_dtype = y_dtype;
+        g.epi = EPI_GELU; g.aux = preact; g.ldaux = ldp; g.aux_dtype = g.c_dtype;
     }
     if (K == 0) {
         // no products: the result is the epilogue of zero (still a kernel, for uniformity)

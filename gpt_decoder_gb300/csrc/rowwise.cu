@@ -101,7 +101,7 @@ __global__ void embedding_bwd_wpe_kernel(const float* __restrict__ dx, float* __
 template <int VPT, typename TY>
 __global__ void layernorm_fwd_warp_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
                                           const float* __restrict__ beta, TY* __restrict__ y, float* mean_out,
-                                          float* rstd_out, int64_t rows, int C, float eps) {
+                                          float* rstd_out, int64_t rows, int C, float eps, int64_t lo_plane) {
     int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -131,10 +131,13 @@ __global__ void layernorm_fwd_warp_kernel(const float* __restrict__ x, const flo
         int c = (i * 32 + lane) * 4;
         float4 g = *reinterpret_cast<const float4*>(gamma + c);
         float4 b = *reinterpret_cast<const float4*>(beta + c);
-        store_from_f32(yr + c + 0, (v[i].x - mu) * rs * g.x + b.x);
-        store_from_f32(yr + c + 1, (v[i].y - mu) * rs * g.y + b.y);
-        store_from_f32(yr + c + 2, (v[i].z - mu) * rs * g.z + b.z);
-        store_from_f32(yr + c + 3, (v[i].w - mu) * rs * g.w + b.w);
+        float o[4] = {(v[i].x - mu) * rs * g.x + b.x, (v[i].y - mu) * rs * g.y + b.y,
+                      (v[i].z - mu) * rs * g.z + b.z, (v[i].w - mu) * rs * g.w + b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            store_from_f32(yr + c + k, o[k]);
+            if (lo_plane) store_from_f32(yr + c + k + lo_plane, o[k] - to_f32(yr[c + k]));
+        }
     }
 }
 
@@ -154,7 +157,7 @@ __device__ float block_sum(float v, float* red) {
 template <typename TY>
 __global__ void layernorm_fwd_block_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
                                            const float* __restrict__ beta, TY* __restrict__ y, float* mean_out,
-                                           float* rstd_out, int64_t rows, int C, float eps) {
+                                           float* rstd_out, int64_t rows, int C, float eps, int64_t lo_plane) {
     extern __shared__ float srow[];
     __shared__ float red[32];
     int64_t row = blockIdx.x;
@@ -177,7 +180,11 @@ __global__ void layernorm_fwd_block_kernel(const float* __restrict__ x, const fl
         if (rstd_out) rstd_out[row] = rs;
     }
     TY* yr = y + row * C;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) store_from_f32(yr + c, (srow[c] - mu) * rs * gamma[c] + beta[c]);
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        float o = (srow[c] - mu) * rs * gamma[c] + beta[c];
+        store_from_f32(yr + c, o);
+        if (lo_plane) store_from_f32(yr + c + lo_plane, o - to_f32(yr[c]));
+    }
 }
 
 // LayerNorm backward, one warp per row (C % 128 == 0, C <= 1024). Each block also keeps
@@ -501,7 +508,8 @@ __global__ void softmax_ce_bwd_bf16_kernel(const float* __restrict__ logits, int
 // ---------------------------------------------------------------------------- AdamW
 // [LM1] "The optimizer", AdamW: float32 arithmetic as on the page.
 __global__ void adamw_kernel(float* __restrict__ p, float* __restrict__ g, float* __restrict__ m,
-                             float* __restrict__ v, __nv_bfloat16* __restrict__ pb, int64_t n, float lr, float b1,
+                             float* __restrict__ v, __nv_bfloat16* __restrict__ pb, __nv_bfloat16* __restrict__ pbl,
+                             int64_t n, float lr, float b1,
                              float b2, float eps, float wd, float inv_bc1, float inv_bc2, int zero_grad) {
     int64_t n4 = n / 4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
@@ -525,6 +533,14 @@ __global__ void adamw_kernel(float* __restrict__ p, float* __restrict__ g, float
             packed.x = *reinterpret_cast<uint32_t*>(&lo);
             packed.y = *reinterpret_cast<uint32_t*>(&hi);
             reinterpret_cast<uint2*>(pb)[i] = packed;
+            if (pbl) {
+                __nv_bfloat162 l0 = __floats2bfloat162_rn(pp.x - __low2float(lo), pp.y - __high2float(lo));
+                __nv_bfloat162 l1 = __floats2bfloat162_rn(pp.z - __low2float(hi), pp.w - __high2float(hi));
+                uint2 pl;
+                pl.x = *reinterpret_cast<uint32_t*>(&l0);
+                pl.y = *reinterpret_cast<uint32_t*>(&l1);
+                reinterpret_cast<uint2*>(pbl)[i] = pl;
+            }
         }
     }
     // tail
@@ -538,13 +554,21 @@ __global__ void adamw_kernel(float* __restrict__ p, float* __restrict__ g, float
         pp -= lr * ((mm * inv_bc1) / (sqrtf(vv * inv_bc2) + eps) + wd * pp);
         p[i] = pp;
         if (zero_grad) g[i] = 0.f;
-        if (pb) pb[i] = __float2bfloat16_rn(pp);
+        if (pb) {
+            __nv_bfloat16 hb = __float2bfloat16_rn(pp);
+            pb[i] = hb;
+            if (pbl) pbl[i] = __float2bfloat16_rn(pp - __bfloat162float(hb));
+        }
     }
 }
 
-__global__ void to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y, int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = __float2bfloat16_rn(x[i]);
+__global__ void to_bf16_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
+                               __nv_bfloat16* __restrict__ lo, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        __nv_bfloat16 h = __float2bfloat16_rn(x[i]);
+        y[i] = h;
+        if (lo) lo[i] = __float2bfloat16_rn(x[i] - __bfloat162float(h));
+    }
 }
 
 int grid_for(gk_ctx* ctx, int64_t work, int threads, int per_sm = 8) {
@@ -595,7 +619,10 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
                            float* mean, float* rstd, int64_t rows, int C, float eps) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, x && gamma && beta && y && rows > 0 && C > 0, GK_ERR_ARG, "gk_layernorm_fwd: bad argument");
-    GK_REQUIRE(ctx, y_dtype == GK_F32 || y_dtype == GK_BF16, GK_ERR_ARG, "gk_layernorm_fwd: bad dtype");
+    GK_REQUIRE(ctx, y_dtype == GK_F32 || y_dtype == GK_BF16 || y_dtype == GK_BF16X2, GK_ERR_ARG,
+               "gk_layernorm_fwd: bad dtype");
+    int64_t lo_plane = y_dtype == GK_BF16X2 ? rows * C : 0;
+    if (y_dtype == GK_BF16X2) y_dtype = GK_BF16;
     bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(gamma) && aligned16(beta);
     if (warp_path) {
         int wpb = 4;
@@ -605,10 +632,10 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
     case V:                                                                                                     \
         if (y_dtype == GK_F32)                                                                                  \
             layernorm_fwd_warp_kernel<V, float><<<grid, wpb * 32, 0, ctx->stream>>>(x, gamma, beta, (float*)y,  \
-                                                                                   mean, rstd, rows, C, eps);   \
+                                                                                   mean, rstd, rows, C, eps, lo_plane);   \
         else                                                                                                    \
             layernorm_fwd_warp_kernel<V, __nv_bfloat16><<<grid, wpb * 32, 0, ctx->stream>>>(                    \
-                x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps);                                   \
+                x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane);                                   \
         break;
         switch (vpt) {
             LN_FWD_CASE(1) LN_FWD_CASE(2) LN_FWD_CASE(3) LN_FWD_CASE(4)
@@ -623,12 +650,12 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
     if (y_dtype == GK_F32) {
         cudaFuncSetAttribute(layernorm_fwd_block_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         layernorm_fwd_block_kernel<float><<<(unsigned)rows, threads, smem, ctx->stream>>>(x, gamma, beta, (float*)y, mean,
-                                                                                         rstd, rows, C, eps);
+                                                                                         rstd, rows, C, eps, 0);
     } else {
         cudaFuncSetAttribute(layernorm_fwd_block_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
         layernorm_fwd_block_kernel<__nv_bfloat16><<<(unsigned)rows, threads, smem, ctx->stream>>>(
-            x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps);
+            x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane);
     }
     return launched(ctx, "layernorm_fwd");
 }
@@ -758,11 +785,11 @@ gk_status gk_softmax_ce_bwd(gk_ctx* ctx, const float* logits, int64_t ldl, const
     return launched(ctx, "softmax_ce_bwd");
 }
 
-gk_status gk_to_bf16(gk_ctx* ctx, const float* x, uint16_t* y, int64_t n) {
+gk_status gk_to_bf16(gk_ctx* ctx, const float* x, uint16_t* y, uint16_t* y_lo, int64_t n) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, x && y && n >= 0, GK_ERR_ARG, "gk_to_bf16: bad argument");
     if (n == 0) return GK_OK;
-    to_bf16_kernel<<<grid_for(ctx, n, 256), 256, 0, ctx->stream>>>(x, (__nv_bfloat16*)y, n);
+    to_bf16_kernel<<<grid_for(ctx, n, 256), 256, 0, ctx->stream>>>(x, (__nv_bfloat16*)y, (__nv_bfloat16*)y_lo, n);
     return launched(ctx, "to_bf16");
 }
 
@@ -777,11 +804,13 @@ gk_status gk_adamw_step(gk_ctx* ctx, const gk_param* params, int n_params, float
         const gk_param& q = params[k];
         GK_REQUIRE(ctx, q.p && q.g && q.m && q.v && q.n >= 0, GK_ERR_ARG, "gk_adamw_step: bad block %d", k);
         GK_REQUIRE(ctx, aligned16(q.p) && aligned16(q.g) && aligned16(q.m) && aligned16(q.v) &&
-                            (!q.p_bf16 || ((uintptr_t)q.p_bf16 & 7) == 0),
+                            (!q.p_bf16 || ((uintptr_t)q.p_bf16 & 7) == 0) &&
+                            (!q.p_bf16_lo || (q.p_bf16 && ((uintptr_t)q.p_bf16_lo & 7) == 0)),
                    GK_ERR_ALIGN, "gk_adamw_step: block %d not 16-byte aligned", k);
         if (q.n == 0) continue;
         adamw_kernel<<<grid_for(ctx, q.n / 4 + 1, 256, 8), 256, 0, ctx->stream>>>(
-            q.p, q.g, q.m, q.v, (__nv_bfloat16*)q.p_bf16, q.n, lr, beta1, beta2, eps, q.decay ? wd : 0.f, ib1, ib2,
+            q.p, q.g, q.m, q.v, (__nv_bfloat16*)q.p_bf16, (__nv_bfloat16*)q.p_bf16_lo, q.n, lr, beta1, beta2, eps,
+            q.decay ? wd : 0.f, ib1, ib2,
             zero_grad);
         GK_TRY(launched(ctx, "adamw"));
     }

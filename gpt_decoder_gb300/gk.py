@@ -19,7 +19,7 @@ _lib = ct.CDLL(LIB_PATH)
 # status codes and enums (include/gk.h)
 GK_OK, GK_ERR_ARG, GK_ERR_ALIGN, GK_ERR_UNSUPPORTED, GK_ERR_CUDA, GK_ERR_TIMEOUT, GK_ERR_OVERFLOW, GK_ERR_INDEX, \
     GK_ERR_WORKSPACE = range(9)
-GK_F32, GK_BF16 = 0, 1
+GK_F32, GK_BF16, GK_BF16X2 = 0, 1, 2
 GK_MATH_FP32, GK_MATH_3XTF32 = 0, 1
 GK_ACT_NONE, GK_ACT_GELU = 0, 1
 (GK_T_WTE, GK_T_WPE, GK_T_LN1_W, GK_T_LN1_B, GK_T_ATTN_W, GK_T_ATTN_B, GK_T_ATTNPROJ_W, GK_T_ATTNPROJ_B,
@@ -39,7 +39,7 @@ class GkError(RuntimeError):
 
 
 class gk_param(ct.Structure):
-    _fields_ = [("p", P), ("g", P), ("m", P), ("v", P), ("n", I64), ("decay", I32), ("p_bf16", P)]
+    _fields_ = [("p", P), ("g", P), ("m", P), ("v", P), ("n", I64), ("decay", I32), ("p_bf16", P), ("p_bf16_lo", P)]
 
 
 class gk_gpt_cfg(ct.Structure):
@@ -65,14 +65,14 @@ _SIGS = {
     "gk_layernorm_bwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
     "gk_gelu_fwd": (I32, [P, P, P, I64]),
     "gk_gelu_bwd": (I32, [P, P, P, P, I64]),
-    "gk_matmul_fwd": (I32, [P, I32, P, I64, P, I64, I32, P, P, I64, P, I64, I32, I64, I64, I64, I32, P, I64]),
+    "gk_matmul_fwd": (I32, [P, I32, P, I64, P, I64, I32, P, P, I64, P, I64, I32, I64, I64, I64, I32, P, I64, P, P]),
     "gk_matmul_bwd": (I32, [P, I32, P, I64, P, I64, I32, P, I64, P, I64, I32, I32, P, I64, P, I64, P, I64, I64,
                             I64]),
     "gk_attn_fwd": (I32, [P, I32, P, P, P, I32, I32, I32, I32]),
     "gk_attn_bwd": (I32, [P, I32, P, P, P, P, P, I32, I32, I32, I32]),
     "gk_softmax_ce_fwd": (I32, [P, P, I64, P, P, P, I64, I32]),
     "gk_softmax_ce_bwd": (I32, [P, P, I64, P, P, P, P, I64, I32, I64, I32]),
-    "gk_to_bf16": (I32, [P, P, P, I64]),
+    "gk_to_bf16": (I32, [P, P, P, P, I64]),
     "gk_adamw_step": (I32, [P, ct.POINTER(gk_param), I32, F32, F32, F32, F32, F32, I32, I32]),
     "gk_gpt_offset": (I64, [ct.POINTER(gk_gpt_cfg), I32, I32]),
     "gk_gpt_numel": (I64, [ct.POINTER(gk_gpt_cfg)]),
@@ -191,10 +191,10 @@ def gk_gelu_bwd(ctx, x, dy, dx, n):
 
 
 def gk_matmul_fwd(ctx, dtype, X, ldx, W, ldw, transW, bias, residual, ldr, Y, ldy, y_dtype, N, K, M,
-                  act=GK_ACT_NONE, preact=None, ldp=0):
+                  act=GK_ACT_NONE, preact=None, ldp=0, X_lo=None, W_lo=None):
     return _check(ctx, _lib.gk_matmul_fwd(ctx.handle, dtype, _p(X), ldx, _p(W), ldw, int(transW), _p(bias),
-                                          _p(residual), ldr, _p(Y), ldy, y_dtype, N, K, M, act, _p(preact), ldp),
-                  "gk_matmul_fwd")
+                                          _p(residual), ldr, _p(Y), ldy, y_dtype, N, K, M, act, _p(preact), ldp,
+                                          _p(X_lo), _p(W_lo)), "gk_matmul_fwd")
 
 
 def gk_matmul_bwd(ctx, dtype, X, ldx, W, ldw, transW, dY, lddy, dX, lddx, dx_dtype, accumulate_dX, preact_X, ldp,
@@ -223,8 +223,8 @@ def gk_softmax_ce_bwd(ctx, logits, ldl, targets, lse, dloss, dlogits, lddl, dl_d
                                               _p(dlogits), lddl, dl_dtype, rows, V), "gk_softmax_ce_bwd")
 
 
-def gk_to_bf16(ctx, x, y, n):
-    return _check(ctx, _lib.gk_to_bf16(ctx.handle, _p(x), _p(y), n), "gk_to_bf16")
+def gk_to_bf16(ctx, x, y, n, y_lo=None):
+    return _check(ctx, _lib.gk_to_bf16(ctx.handle, _p(x), _p(y), _p(y_lo), n), "gk_to_bf16")
 
 
 def gk_adamw_step(ctx, params, lr, beta1, beta2, eps, wd, step, zero_grad=False):
@@ -232,7 +232,7 @@ def gk_adamw_step(ctx, params, lr, beta1, beta2, eps, wd, step, zero_grad=False)
     arr = (gk_param * len(params))()
     for i, q in enumerate(params):
         arr[i] = gk_param(_p(q["p"]), _p(q["g"]), _p(q["m"]), _p(q["v"]), int(q["n"]), int(q.get("decay", 0)),
-                          _p(q.get("p_bf16")))
+                          _p(q.get("p_bf16")), _p(q.get("p_bf16_lo")))
     return _check(ctx, _lib.gk_adamw_step(ctx.handle, arr, len(params), lr, beta1, beta2, eps, wd, step,
                                           int(zero_grad)), "gk_adamw_step")
 

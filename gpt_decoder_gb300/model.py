@@ -14,11 +14,13 @@ runs in libgk's kernels.
 Modes: "fp32" runs every product in float32 (the faithful mode); "bf16" keeps float32
 master weights, moments, residual stream and logits, and feeds the matrix products bf16
 operands (a bf16 weight copy that AdamW refreshes, bf16 activations) with float32
-accumulation. In bf16 mode the first `hi_layers` blocks (default 2) keep float32 operands:
+accumulation. In bf16 mode the forward products of the first `hi_layers` blocks (default 2)
+use split-bf16 operands (value = hi + lo, two bf16 planes, three tensor-core products):
 block 0's output is about ten times the embedding it is added to, so its operand rounding
-sets the relative error of everything downstream; measured on the GPT-2-124M shape, all-bf16
-logits land at 0.021-0.022 max-abs from the float64 result, and float32 operands in the first
-two blocks bring that to about 0.016.
+sets the relative error of everything downstream. Measured on the GPT-2-124M shape, all-bf16
+logits land at 0.021-0.022 max-abs from the float64 result; exact operands in the first two
+blocks' products (their attention inputs and outputs still bf16) bring that to about 0.017.
+Their backward is plain bf16 on the hi planes, like every other block.
 """
 from __future__ import annotations
 
@@ -52,28 +54,37 @@ class Gpt:
         self.dt = gk.GK_F32 if mode == "fp32" else gk.GK_BF16
         adt = torch.float32 if mode == "fp32" else torch.bfloat16
         self.params_bf16 = torch.zeros(self.numel, dtype=torch.bfloat16, device=device) if mode == "bf16" else None
+        # low planes of the split-bf16 weights: the matrices of the first hi_layers blocks
+        self.hi_lo = gk.gk_gpt_offset(self.cfg, gk.GK_T_ATTN_W, 0)
+        self.hi_hi = self.hi_lo + min(hi_layers, L) * 12 * C * C if mode == "bf16" else self.hi_lo
+        self.params_bf16_lo = (torch.zeros(max(1, self.hi_hi - self.hi_lo), dtype=torch.bfloat16, device=device)
+                               if mode == "bf16" else None)
         self.step_count = 0
         N, C = self.N, C
-        # per-block operand type: float32 for every block in fp32 mode, else for the first hi_layers
-        self.ldt = [gk.GK_F32 if (mode == "fp32" or l < hi_layers) else gk.GK_BF16 for l in range(L)]
+        # per-block operand type of the products: float32 in fp32 mode, else bf16; in bf16 mode
+        # the first hi_layers blocks' forward products take split-bf16 operands (hi + lo planes)
+        self.ldt = [gk.GK_F32 if mode == "fp32" else gk.GK_BF16 for l in range(L)]
+        self.split = [mode == "bf16" and l < hi_layers for l in range(L)]
         tdt = {gk.GK_F32: torch.float32, gk.GK_BF16: torch.bfloat16}
 
-        def act(l, *shape):
+        def act(l, *shape, planes=1):
+            if planes == 2 and self.split[l]:
+                return torch.empty(2, *shape, dtype=torch.bfloat16, device=device)
             return torch.empty(*shape, dtype=tdt[self.ldt[l]], device=device)
 
         # residual stream: xs[2l] enters block l, xs[2l+1] is after its attention
         self.xs = [torch.empty(N, C, **f32) for _ in range(2 * L + 1)]
-        self.ln1 = [act(l, N, C) for l in range(L)]
+        self.ln1 = [act(l, N, C, planes=2) for l in range(L)]
         self.mu1 = [torch.empty(N, **f32) for _ in range(L)]
         self.rs1 = [torch.empty(N, **f32) for _ in range(L)]
         self.qkv = [act(l, N, 3 * C) for l in range(L)]
         self.y = [act(l, N, C) for l in range(L)]
         self.lse = [torch.empty(B * H * T, **f32) for _ in range(L)]
-        self.ln2 = [act(l, N, C) for l in range(L)]
+        self.ln2 = [act(l, N, C, planes=2) for l in range(L)]
         self.mu2 = [torch.empty(N, **f32) for _ in range(L)]
         self.rs2 = [torch.empty(N, **f32) for _ in range(L)]
         self.pre = [act(l, N, 4 * C) for l in range(L)]
-        self.h = [act(l, N, 4 * C) for l in range(L)]
+        self.h = [act(l, N, 4 * C, planes=2) for l in range(L)]
         self.lnf = torch.empty(N, C, dtype=adt, device=device)
         self.muf = torch.empty(N, **f32)
         self.rsf = torch.empty(N, **f32)
@@ -100,6 +111,12 @@ class Gpt:
         if for_gemm and self.mode == "bf16":
             return self.params_bf16.data_ptr() + 2 * o
         return self.params.data_ptr() + 4 * o
+
+    def w_lo(self, which, layer):
+        """Address of a block-weight matrix's low bf16 plane (split-bf16 blocks only)."""
+        o = self.off(which, layer)
+        assert self.hi_lo <= o < self.hi_hi
+        return self.params_bf16_lo.data_ptr() + 2 * (o - self.hi_lo)
 
     def g(self, which, layer=0):
         return self.grads.data_ptr() + 4 * self.off(which, layer)
@@ -138,6 +155,10 @@ class Gpt:
             views[k].copy_(torch.as_tensor(v, dtype=torch.float32))
         if self.params_bf16 is not None:
             gk.gk_to_bf16(self.ctx, self.params, self.params_bf16, self.numel)
+            n = self.hi_hi - self.hi_lo
+            if n > 0:
+                gk.gk_to_bf16(self.ctx, self.params.data_ptr() + 4 * self.hi_lo,
+                              self.params_bf16.data_ptr() + 2 * self.hi_lo, n, y_lo=self.params_bf16_lo)
 
     # ------------------------------------------------------------- GEMM timing hook
     gemm_events = None  # a list: every matmul call appends (start event, end event, flops)
@@ -168,21 +189,28 @@ class Gpt:
         for l in range(self.L):
             dt = self.ldt[l]
             bw = dt == gk.GK_BF16  # GEMM weights from the bf16 copy
+            sp = self.split[l]
+            lnd = gk.GK_BF16X2 if sp else dt  # LayerNorm / GELU outputs: two planes when split
+            lo = (lambda buf: buf[1]) if sp else (lambda buf: None)
+            wl = (lambda which: self.w_lo(which, l)) if sp else (lambda which: None)
             x_in, x_mid, x_out = self.xs[2 * l], self.xs[2 * l + 1], self.xs[2 * l + 2]
-            gk.gk_layernorm_fwd(c, x_in, self.w(gk.GK_T_LN1_W, l), self.w(gk.GK_T_LN1_B, l), self.ln1[l], dt,
+            gk.gk_layernorm_fwd(c, x_in, self.w(gk.GK_T_LN1_W, l), self.w(gk.GK_T_LN1_B, l), self.ln1[l], lnd,
                                 self.mu1[l], self.rs1[l], N, C, EPS)
             self._mm_fwd(c, dt, self.ln1[l], C, self.w(gk.GK_T_ATTN_W, l, bw), 3 * C, 0,
-                             self.w(gk.GK_T_ATTN_B, l), None, 0, self.qkv[l], 3 * C, dt, N, C, 3 * C)
+                         self.w(gk.GK_T_ATTN_B, l), None, 0, self.qkv[l], 3 * C, dt, N, C, 3 * C,
+                         gk.GK_ACT_NONE, None, 0, lo(self.ln1[l]), wl(gk.GK_T_ATTN_W))
             gk.gk_attn_fwd(c, dt, self.qkv[l], self.y[l], self.lse[l], B, T, H, hs)
             self._mm_fwd(c, dt, self.y[l], C, self.w(gk.GK_T_ATTNPROJ_W, l, bw), C, 0,
-                             self.w(gk.GK_T_ATTNPROJ_B, l), x_in, C, x_mid, C, gk.GK_F32, N, C, C)
-            gk.gk_layernorm_fwd(c, x_mid, self.w(gk.GK_T_LN2_W, l), self.w(gk.GK_T_LN2_B, l), self.ln2[l], dt,
+                         self.w(gk.GK_T_ATTNPROJ_B, l), x_in, C, x_mid, C, gk.GK_F32, N, C, C,
+                         gk.GK_ACT_NONE, None, 0, None, wl(gk.GK_T_ATTNPROJ_W))
+            gk.gk_layernorm_fwd(c, x_mid, self.w(gk.GK_T_LN2_W, l), self.w(gk.GK_T_LN2_B, l), self.ln2[l], lnd,
                                 self.mu2[l], self.rs2[l], N, C, EPS)
             self._mm_fwd(c, dt, self.ln2[l], C, self.w(gk.GK_T_FC_W, l, bw), 4 * C, 0,
-                             self.w(gk.GK_T_FC_B, l), None, 0, self.h[l], 4 * C, dt, N, C, 4 * C,
-                             gk.GK_ACT_GELU, self.pre[l], 4 * C)
+                         self.w(gk.GK_T_FC_B, l), None, 0, self.h[l], 4 * C, lnd, N, C, 4 * C,
+                         gk.GK_ACT_GELU, self.pre[l], 4 * C, lo(self.ln2[l]), wl(gk.GK_T_FC_W))
             self._mm_fwd(c, dt, self.h[l], 4 * C, self.w(gk.GK_T_MLPPROJ_W, l, bw), C, 0,
-                             self.w(gk.GK_T_MLPPROJ_B, l), x_mid, C, x_out, C, gk.GK_F32, N, 4 * C, C)
+                         self.w(gk.GK_T_MLPPROJ_B, l), x_mid, C, x_out, C, gk.GK_F32, N, 4 * C, C,
+                         gk.GK_ACT_NONE, None, 0, lo(self.h[l]), wl(gk.GK_T_MLPPROJ_W))
         gk.gk_layernorm_fwd(c, self.xs[-1], self.w(gk.GK_T_LNF_W), self.w(gk.GK_T_LNF_B), self.lnf, self.dt, self.muf,
                             self.rsf, N, C, EPS)
         self._mm_fwd(c, self.dt, self.lnf, C, self.w(gk.GK_T_WTE, 0, True), C, 1, None, None, 0, self.logits,
@@ -205,12 +233,13 @@ class Gpt:
             bw = dt == gk.GK_BF16
             dxg = self.dx_bf16 if bw else self.dx  # the residual gradient as this block's GEMM operand
             x_in, x_mid = self.xs[2 * l], self.xs[2 * l + 1]
+            hi = (lambda buf: buf[0]) if self.split[l] else (lambda buf: buf)  # bf16 plane of split buffers
             dpre = self.dmid[dt]
             # x_out = x_mid + h Wp + bp   (GELU backward fused into the dX product)
-            self._mm_bwd(c, dt, self.h[l], 4 * C, self.w(gk.GK_T_MLPPROJ_W, l, bw), C, 0, dxg, C, dpre,
+            self._mm_bwd(c, dt, hi(self.h[l]), 4 * C, self.w(gk.GK_T_MLPPROJ_W, l, bw), C, 0, dxg, C, dpre,
                              4 * C, dt, 0, self.pre[l], 4 * C, self.g(gk.GK_T_MLPPROJ_W, l), C,
                              self.g(gk.GK_T_MLPPROJ_B, l), N, 4 * C, C)
-            self._mm_bwd(c, dt, self.ln2[l], C, self.w(gk.GK_T_FC_W, l, bw), 4 * C, 0, dpre, 4 * C, self.dln,
+            self._mm_bwd(c, dt, hi(self.ln2[l]), C, self.w(gk.GK_T_FC_W, l, bw), 4 * C, 0, dpre, 4 * C, self.dln,
                              C, gk.GK_F32, 0, None, 0, self.g(gk.GK_T_FC_W, l), 4 * C, self.g(gk.GK_T_FC_B, l), N,
                              C, 4 * C)
             gk.gk_layernorm_bwd(c, x_mid, self.w(gk.GK_T_LN2_W, l), self.mu2[l], self.rs2[l], self.dln, self.dx, 1,
@@ -220,23 +249,32 @@ class Gpt:
             self._mm_bwd(c, dt, self.y[l], C, self.w(gk.GK_T_ATTNPROJ_W, l, bw), C, 0, dxg, C, dy, C, dt, 0,
                              None, 0, self.g(gk.GK_T_ATTNPROJ_W, l), C, self.g(gk.GK_T_ATTNPROJ_B, l), N, C, C)
             gk.gk_attn_bwd(c, dt, self.qkv[l], self.y[l], self.lse[l], dy, self.dqkv[dt], B, T, H, hs)
-            self._mm_bwd(c, dt, self.ln1[l], C, self.w(gk.GK_T_ATTN_W, l, bw), 3 * C, 0, self.dqkv[dt], 3 * C,
+            self._mm_bwd(c, dt, hi(self.ln1[l]), C, self.w(gk.GK_T_ATTN_W, l, bw), 3 * C, 0, self.dqkv[dt], 3 * C,
                              self.dln, C, gk.GK_F32, 0, None, 0, self.g(gk.GK_T_ATTN_W, l), 3 * C,
                              self.g(gk.GK_T_ATTN_B, l), N, C, 3 * C)
             gk.gk_layernorm_bwd(c, x_in, self.w(gk.GK_T_LN1_W, l), self.mu1[l], self.rs1[l], self.dln, self.dx, 1,
                                 self.dx_bf16, self.g(gk.GK_T_LN1_W, l), self.g(gk.GK_T_LN1_B, l), N, C)
         gk.gk_embedding_bwd(c, ids, self.dx, self.g(gk.GK_T_WTE), self.g(gk.GK_T_WPE), B, T, C, self.V)
 
+    def adamw_cuts(self):
+        """(start, end, decay, writes low plane) spans of the flat buffer for AdamW: decayed
+        matrices (the split-bf16 blocks' matrices also refresh their low planes), then the
+        undecayed vectors."""
+        cuts = [(0, self.hi_lo, 1, False), (self.hi_lo, self.hi_hi, 1, True), (self.hi_hi, self.n_decay, 1, False),
+                (self.n_decay, self.numel, 0, False)]
+        return [c for c in cuts if c[1] > c[0]]
+
     def adamw(self, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0, zero_grad=True):
         self.step_count += 1
         pb = self.params_bf16
-        blocks = [
-            dict(p=self.params, g=self.grads, m=self.m, v=self.v, n=self.n_decay, decay=1, p_bf16=pb),
-            dict(p=self.params.data_ptr() + 4 * self.n_decay, g=self.grads.data_ptr() + 4 * self.n_decay,
-                 m=self.m.data_ptr() + 4 * self.n_decay, v=self.v.data_ptr() + 4 * self.n_decay,
-                 n=self.numel - self.n_decay, decay=0,
-                 p_bf16=None if pb is None else pb.data_ptr() + 2 * self.n_decay),
-        ]
+        P, G, M_, V_ = (t.data_ptr() for t in (self.params, self.grads, self.m, self.v))
+
+        def blk(a, b, decay, with_lo=False):
+            return dict(p=P + 4 * a, g=G + 4 * a, m=M_ + 4 * a, v=V_ + 4 * a, n=b - a, decay=decay,
+                        p_bf16=None if pb is None else pb.data_ptr() + 2 * a,
+                        p_bf16_lo=self.params_bf16_lo.data_ptr() + 2 * (a - self.hi_lo) if with_lo else None)
+
+        blocks = [blk(a, b, d, lo) for (a, b, d, lo) in self.adamw_cuts()]
         gk.gk_adamw_step(self.ctx, blocks, lr, beta1, beta2, eps, wd, self.step_count, zero_grad)
 
     def train_step(self, ids, targets, lr, wd, beta1=0.9, beta2=0.999, eps=1e-8):

@@ -21,7 +21,9 @@
  *   - Backward calls ADD into parameter-gradient buffers ([LM1] "Why += and not =": a tensor
  *     used twice receives the sum; the caller zeroes them, like ZeroGrad). Activation
  *     gradients take an `accumulate` flag.
- *   - dtype arguments take GK_F32 or GK_BF16 (bfloat16 stored as uint16_t bits).
+ *   - dtype arguments take GK_F32 or GK_BF16 (bfloat16 stored as uint16_t bits); some outputs
+ *     also take GK_BF16X2, a float32 value kept as two bfloat16 planes: hi = bf16(v) at the
+ *     pointer, lo = bf16(v - hi) at pointer + rows * ld elements (about 16 significant bits).
  */
 #ifndef GK_H
 #define GK_H
@@ -46,7 +48,7 @@ enum {
     GK_ERR_WORKSPACE = 8    /* the context's workspace is smaller than the call needs */
 };
 
-enum { GK_F32 = 0, GK_BF16 = 1 };
+enum { GK_F32 = 0, GK_BF16 = 1, GK_BF16X2 = 2 };
 /* Arithmetic of float32 GEMMs: plain fp32 FMA, or three TF32 tensor-core products with the
  * operands split into high and low TF32 parts. Both are "faithful" (fp32-level) modes. */
 enum { GK_MATH_FP32 = 0, GK_MATH_3XTF32 = 1 };
@@ -94,7 +96,8 @@ gk_status gk_embedding_bwd(gk_ctx* ctx, const int32_t* ids, const float* dx, flo
 
 /* Per row: y = (x - mean) * rstd * gamma + beta, rstd = 1/sqrt(var + eps), var biased.
  * [LM1] op table (LayerNorm); eps 1e-5 in GPT-2. x float32 [rows, C] contiguous; y is
- * `y_dtype` [rows, C]; mean and rstd float32 [rows] (saved for backward, may be NULL). */
+ * `y_dtype` [rows, C] (GK_BF16X2: two planes of rows * C); mean and rstd float32 [rows] (saved
+ * for backward, may be NULL). */
 gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, const float* beta,
                            void* y, int y_dtype, float* mean, float* rstd, int64_t rows, int C,
                            float eps);
@@ -146,13 +149,18 @@ gk_status gk_gelu_bwd(gk_ctx* ctx, const float* x, const float* dy, float* dx, i
  *              accumulation on the tensor cores); X and W both have this type.
  *   bias       float32 [M] or NULL.  residual  float32 [N, M] (stride ldr) or NULL; it may
  *              alias Y when y_dtype is GK_F32 (in-place x += ...).
- *   act        GK_ACT_GELU stores the pre-activation in `preact` (y_dtype, stride ldp) and
- *              gelu(pre) in Y.
+ *   act        GK_ACT_GELU stores the pre-activation in `preact` (y_dtype, bf16 for
+ *              GK_BF16X2; stride ldp) and gelu(pre) in Y.
+ *   X_lo, W_lo optional low bf16 planes (same layout) of bf16 X and W: the product becomes
+ *              X_hi W_hi + X_hi W_lo + X_lo W_hi, i.e. split-bf16 operands of about 16
+ *              significant bits on the bf16 tensor cores.
+ *   y_dtype    GK_F32, GK_BF16 or GK_BF16X2 (Y's low plane at Y + N * ldy).
  * bf16 operands need 16-byte aligned base pointers and strides that are multiples of 8. */
 gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W,
                         int64_t ldw, int transW, const float* bias, const float* residual,
                         int64_t ldr, void* Y, int64_t ldy, int y_dtype, int64_t N, int64_t K,
-                        int64_t M, int act, void* preact, int64_t ldp);
+                        int64_t M, int act, void* preact, int64_t ldp, const void* X_lo,
+                        const void* W_lo);
 
 /* Backward of Y = X W (transW = 0) or X W^T (transW = 1) for upstream dY [N, M]:
  *   dX  = dY W^T (transW = 0) or dY W (transW = 1); written (=), or added (+=) if
@@ -206,8 +214,9 @@ gk_status gk_softmax_ce_bwd(gk_ctx* ctx, const float* logits, int64_t ldl, const
                             int dl_dtype, int64_t rows, int V);
 
 /* Round float32 [n] to bfloat16 [n] (round to nearest even): the bf16 operand copy of a
- * float32 tensor, e.g. the weights before the first step (AdamW refreshes it afterwards). */
-gk_status gk_to_bf16(gk_ctx* ctx, const float* x, uint16_t* y, int64_t n);
+ * float32 tensor, e.g. the weights before the first step (AdamW refreshes it afterwards).
+ * y_lo, if not NULL, receives the low plane bf16(x - y) of the split-bf16 form. */
+gk_status gk_to_bf16(gk_ctx* ctx, const float* x, uint16_t* y, uint16_t* y_lo, int64_t n);
 
 /* ---------------------------------------------------------------------------- AdamW */
 
@@ -220,6 +229,7 @@ typedef struct {
     int64_t n;         /* number of elements */
     int decay;         /* 1: apply weight decay (tensors with >= 2 dims), 0: not */
     uint16_t* p_bf16;  /* optional bfloat16 copy of the updated p, or NULL */
+    uint16_t* p_bf16_lo; /* optional low plane bf16(p - p_bf16) (needs p_bf16), or NULL */
 } gk_param;
 
 /* AdamW at step `step` (>= 1) over n_params blocks (host array):

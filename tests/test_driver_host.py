@@ -13,7 +13,16 @@ def test_driver_buffers_and_views(mode):
 
     s = synth.GptShape(V=50, T=8, C=16, H=2, L=3)
     m = Gpt(None, s.V, s.T, s.C, s.H, s.L, 2, mode=mode, device="cpu")
-    assert m.ldt == ([gk.GK_F32] * 3 if mode == "fp32" else [gk.GK_F32, gk.GK_F32, gk.GK_BF16])
+    assert m.ldt == [gk.GK_F32 if mode == "fp32" else gk.GK_BF16] * 3
+    assert m.split == ([False] * 3 if mode == "fp32" else [True, True, False])
+    cuts = m.adamw_cuts()
+    assert cuts[0][0] == 0 and cuts[-1][1] == m.numel
+    assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:]))
+    assert all(d == (e <= m.n_decay) for (_, e, d, _) in cuts)
+    if mode == "bf16":
+        lo_spans = [c for c in cuts if c[3]]
+        assert lo_spans == [(m.hi_lo, m.hi_hi, 1, True)]
+        assert m.hi_hi - m.hi_lo == 2 * 12 * s.C * s.C == m.params_bf16_lo.numel()
     assert m.Vp % 64 == 0 and m.Vp >= s.V
     views = m.named_slices(m.params)
     assert set(views) == {n for n, _ in synth.param_names_shapes(s)}

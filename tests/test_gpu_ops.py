@@ -384,3 +384,65 @@ def test_adamw(gkctx, n):
         assert rel_l2(host(m), rm) < 1e-6 and rel_l2(host(v), rv) < 1e-6
         assert not host(dg).any()
         assert rel_l2(host(pb), host(p)) < 5e-3
+
+
+# ------------------------------------------------------------------- split bf16
+def _split(a):
+    torch = _t()
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32))
+    hi = t.to(torch.bfloat16)
+    lo = (t - hi.float()).to(torch.bfloat16)
+    return hi, lo
+
+
+@pytest.mark.parametrize("N,K,M,transW", [(4096, 768, 3072, 0), (4096, 3072, 768, 0), (300, 96, 384, 0),
+                                          (256, 256, 256, 1), (131, 64, 45, 0)])
+@pytest.mark.parametrize("which", ["both", "W", "X"])
+def test_matmul_fwd_split_bf16(gkctx, N, K, M, transW, which):
+    """Split-bf16 operands (hi + lo planes, three products) track float32 operands closely."""
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    x = normal(1100 + N, N, K)
+    w = normal(1101 + K, M, K) if transW else normal(1101 + K, K, M)
+    xh, xl = _split(x)
+    wh, wl = _split(w)
+    b = normal(1102, M)
+    y = torch.empty(N, M, device="cuda")
+    use_x, use_w = which in ("both", "X"), which in ("both", "W")
+    gk.gk_matmul_fwd(gkctx, gk.GK_BF16, xh.cuda(), K, wh.cuda(), w.shape[1], transW, dev(b), None, 0, y, M, gk.GK_F32,
+                     N, K, M, gk.GK_ACT_NONE, None, 0, xl.cuda() if use_x else None, wl.cuda() if use_w else None)
+    gk.gk_sync(gkctx)
+    xe = x if use_x else xh.float().numpy()
+    we = w if use_w else wh.float().numpy()
+    ref = (ops.matmul_t_fwd(xe, we) if transW else ops.matmul_fwd(xe, we)) + b
+    # the dropped lo x lo term and the 16-bit pieces leave about 2^-16 relative error
+    assert rel_l2(host(y), ref) < 1e-4
+
+
+def test_split_outputs_hold_the_float32_value(gkctx):
+    """GK_BF16X2 outputs (GEMM with GELU, LayerNorm): hi + lo equals the float32 result."""
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    N, K, M = 300, 96, 384
+    x, w, b = normal(1200, N, K), normal(1201, K, M), normal(1202, M)
+    y2 = torch.empty(2, N, M, dtype=torch.bfloat16, device="cuda")
+    pre = torch.empty(N, M, dtype=torch.bfloat16, device="cuda")
+    xh, xl = _split(x)
+    wh, wl = _split(w)
+    gk.gk_matmul_fwd(gkctx, gk.GK_BF16, xh.cuda(), K, wh.cuda(), M, 0, dev(b), None, 0, y2, M, gk.GK_BF16X2, N, K, M,
+                     gk.GK_ACT_GELU, pre, M, xl.cuda(), wl.cuda())
+    rows, C = 37, 768
+    xx = normal(1203, rows, C) * 2 + 0.5
+    gm, bt = normal(1204, C), normal(1205, C)
+    ln2 = torch.empty(2, rows, C, dtype=torch.bfloat16, device="cuda")
+    gk.gk_layernorm_fwd(gkctx, dev(xx), dev(gm), dev(bt), ln2, gk.GK_BF16X2, None, None, rows, C, 1e-5)
+    gk.gk_sync(gkctx)
+    ref = ops.gelu_fwd(ops.matmul_fwd(x, w) + b)
+    got = y2[0].float().cpu().numpy() + y2[1].float().cpu().numpy()
+    assert rel_l2(got, ref) < 1e-4
+    assert rel_l2(y2[0].float().cpu().numpy(), ref) > 1e-4  # the hi plane alone is bf16-coarse
+    ry, _, _ = ops.layernorm_fwd(xx, gm, bt)
+    got = ln2[0].float().cpu().numpy() + ln2[1].float().cpu().numpy()
+    assert np.abs(got - ry).max() < 1e-5 * np.abs(ry).max()

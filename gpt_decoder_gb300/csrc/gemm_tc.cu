@@ -38,7 +38,8 @@ struct StageCfg {
     static constexpr uint32_t B_SLOT = B_BYTES * (B_LO ? 2 : 1);
     static constexpr uint32_t STAGE = A_SLOT + B_SLOT;
     static constexpr int STAGES = SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2);
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 256;
+    static constexpr uint32_t EPI = 4 * 32 * 32 * 4;  // 4 KB per epilogue warp
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + EPI + 1024 + 256;
 };
 constexpr uint64_t WAIT_NS = 1000000000ull;       // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;       // after an abort: 0.2 s per drain wait
@@ -58,47 +59,109 @@ struct TcParams {
     int64_t ldaux;
     int aux_dtype;
     int64_t c_plane;  // > 0: bf16 C also gets its low plane (v - bf16(v)) at C + c_plane
+    int vec;          // every epilogue pointer 16-byte aligned and every stride a multiple of 4
     int* err;
 };
 
 // --------------------------------------------------------------------- epilogue
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
 template <typename TC>
-__device__ __forceinline__ void store_row32(const TcParams& p, int64_t m, int64_t n0, const uint32_t (&r)[32]) {
-    TC* C = static_cast<TC*>(p.C);
+__device__ __forceinline__ float4 ld4c(const TC* p) {
+    if constexpr (sizeof(TC) == 4) {
+        return *reinterpret_cast<const float4*>(p);
+    } else {
+        uint2 u = *reinterpret_cast<const uint2*>(p);
+        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x), b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+        return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+    }
+}
+
+__device__ __forceinline__ void st4_bf16(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+// Epilogue of one element (the scalar path for edges and unaligned operands).
+template <typename TC>
+__device__ __forceinline__ void epi1(const TcParams& p, int64_t m, int64_t n, float v) {
+    int64_t ci = m * p.ldc + n;
     if (p.atomic_out) {
-        float* Cf = static_cast<float*>(p.C);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            int64_t n = n0 + j;
-            if (n < p.N) atomicAdd(Cf + m * p.ldc + n, __uint_as_float(r[j]));
-        }
+        atomicAdd(static_cast<float*>(p.C) + ci, v);
         return;
     }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        int64_t n = n0 + j;
-        if (n >= p.N) break;
-        float v = __uint_as_float(r[j]);
-        int64_t ci = m * p.ldc + n;
-        if (p.accumulate) v += load_as_f32(C + ci);
-        if (p.bias) v += p.bias[n];
-        if (p.residual) v += p.residual[m * p.ldr + n];
-        if (p.epi == EPI_GELU) {
-            if (p.aux_dtype == GK_F32)
-                static_cast<float*>(p.aux)[m * p.ldaux + n] = v;
-            else
-                static_cast<__nv_bfloat16*>(p.aux)[m * p.ldaux + n] = __float2bfloat16_rn(v);
-            v = gelu_tanh(v);
-        } else if (p.epi == EPI_DGELU) {
-            float pre = p.aux_dtype == GK_F32
-                            ? static_cast<const float*>(p.aux)[m * p.ldaux + n]
-                            : __bfloat162float(static_cast<const __nv_bfloat16*>(p.aux)[m * p.ldaux + n]);
-            v *= gelu_tanh_grad(pre);
-        }
-        store_from_f32(C + ci, v);
+    TC* C = static_cast<TC*>(p.C);
+    if (p.accumulate) v += load_as_f32(C + ci);
+    if (p.bias) v += p.bias[n];
+    if (p.residual) v += p.residual[m * p.ldr + n];
+    if (p.epi == EPI_GELU) {
+        if (p.aux_dtype == GK_F32)
+            static_cast<float*>(p.aux)[m * p.ldaux + n] = v;
+        else
+            static_cast<__nv_bfloat16*>(p.aux)[m * p.ldaux + n] = __float2bfloat16_rn(v);
+        v = gelu_tanh(v);
+    } else if (p.epi == EPI_DGELU) {
+        float pre = p.aux_dtype == GK_F32 ? static_cast<const float*>(p.aux)[m * p.ldaux + n]
+                                          : __bfloat162float(static_cast<const __nv_bfloat16*>(p.aux)[m * p.ldaux + n]);
+        v *= gelu_tanh_grad(pre);
+    }
+    store_from_f32(C + ci, v);
+    if (p.c_plane) {
+        __nv_bfloat16* Cb = static_cast<__nv_bfloat16*>(p.C);
+        Cb[ci + p.c_plane] = __float2bfloat16_rn(v - __bfloat162float(Cb[ci]));
+    }
+}
+
+// Epilogue of 4 consecutive columns n .. n+3 of row m (16-byte accesses when allowed).
+template <typename TC>
+__device__ __forceinline__ void epi4(const TcParams& p, int64_t m, int64_t n, float4 v) {
+    if (m >= p.M || n >= p.N) return;
+    if (!p.vec || n + 3 >= p.N) {
+        float t[4] = {v.x, v.y, v.z, v.w};
+        for (int j = 0; j < 4 && n + j < p.N; ++j) epi1<TC>(p, m, n + j, t[j]);
+        return;
+    }
+    int64_t ci = m * p.ldc + n;
+    if (p.atomic_out) {
+        atomicAdd(reinterpret_cast<float4*>(static_cast<float*>(p.C) + ci), v);
+        return;
+    }
+    TC* C = static_cast<TC*>(p.C);
+    if (p.accumulate) {
+        float4 c = ld4c<TC>(C + ci);
+        v.x += c.x; v.y += c.y; v.z += c.z; v.w += c.w;
+    }
+    if (p.bias) {
+        float4 b = ld4(p.bias + n);
+        v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+    }
+    if (p.residual) {
+        float4 r = ld4(p.residual + m * p.ldr + n);
+        v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
+    }
+    if (p.epi == EPI_GELU) {
+        if (p.aux_dtype == GK_F32)
+            *reinterpret_cast<float4*>(static_cast<float*>(p.aux) + m * p.ldaux + n) = v;
+        else
+            st4_bf16(static_cast<__nv_bfloat16*>(p.aux) + m * p.ldaux + n, v);
+        v = make_float4(gelu_tanh(v.x), gelu_tanh(v.y), gelu_tanh(v.z), gelu_tanh(v.w));
+    } else if (p.epi == EPI_DGELU) {
+        float4 pre = p.aux_dtype == GK_F32 ? ld4(static_cast<const float*>(p.aux) + m * p.ldaux + n)
+                                           : ld4c<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(p.aux) + m * p.ldaux + n);
+        v.x *= gelu_tanh_grad(pre.x); v.y *= gelu_tanh_grad(pre.y);
+        v.z *= gelu_tanh_grad(pre.z); v.w *= gelu_tanh_grad(pre.w);
+    }
+    if constexpr (sizeof(TC) == 4) {
+        *reinterpret_cast<float4*>(C + ci) = v;
+    } else {
+        __nv_bfloat16* Cb = reinterpret_cast<__nv_bfloat16*>(C);
+        st4_bf16(Cb + ci, v);
         if (p.c_plane) {
-            __nv_bfloat16* Cb = static_cast<__nv_bfloat16*>(p.C);
-            Cb[ci + p.c_plane] = __float2bfloat16_rn(v - __bfloat162float(Cb[ci]));
+            float4 h = ld4c<__nv_bfloat16>(Cb + ci);
+            st4_bf16(Cb + ci + p.c_plane, make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w));
         }
     }
 }
@@ -121,7 +184,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // stage s: A_hi at smem + s*STAGE, A_lo at + A_BYTES, B_hi at + A_SLOT, B_lo at + A_SLOT + B_BYTES
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * SC::STAGE);
+    float* epi_stage = reinterpret_cast<float*>(smem + STAGES * SC::STAGE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * SC::STAGE + SC::EPI);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -269,7 +333,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else {
         // epilogue warps 2..5; a warp may read TMEM lanes 32 * (warp % 4) .. + 31
         int q = warp & 3;
-        int row = q * 32 + lane;
         uint32_t j = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
             int tm, tn, kb0, kb1;
@@ -281,12 +344,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
-            int64_t m = (int64_t)tm * BM + row;
+            // Each 32 x 32 block of this warp's rows goes through a private, 16-byte-chunk
+            // XOR-swizzled staging tile: written one row per lane (as tcgen05.ld delivers it),
+            // read back row-contiguously (8 lanes x 4 columns per row) so that bias, residual
+            // and the stores are coalesced 16-byte accesses.
+            float* stg = epi_stage + (warp - 2) * 1024;
+            const int64_t mrow0 = (int64_t)tm * BM + q * 32;
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + c0, r);
-                int64_t n0 = (int64_t)tn * BN + c0;
-                if (m < p.M && n0 < p.N) store_row32<TC>(p, m, n0, r);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4*>(stg + lane * 32 + ((c ^ (lane & 7)) << 2)) =
+                        make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                                    __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+                __syncwarp();
+                const int64_t n0 = (int64_t)tn * BN + c0;
+                if (n0 < p.N) {
+#pragma unroll 2
+                    for (int pass = 0; pass < 8; ++pass) {
+                        int rr = pass * 4 + (lane >> 3), c = lane & 7;
+                        float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((c ^ (rr & 7)) << 2));
+                        epi4<TC>(p, mrow0 + rr, n0 + c * 4, v);
+                    }
+                }
+                __syncwarp();
             }
             tc_fence_before();
             mbar_arrive(&tempty[buf]);
@@ -356,6 +438,9 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.aux_dtype = g.aux_dtype;
     p.err = ctx->d_err;
     p.c_plane = g.c_plane;
+    p.vec = aligned16(g.C) && (g.ldc % 4 == 0) && (!g.bias || aligned16(g.bias)) &&
+            (!g.residual || (aligned16(g.residual) && g.ldr % 4 == 0)) &&
+            (!g.aux || (aligned16(g.aux) && g.ldaux % 4 == 0)) && (g.c_plane % 4 == 0);
     if ((g.A_lo && (!aligned16(g.A_lo))) || (g.B_lo && !aligned16(g.B_lo))) return GK_ERR_UNSUPPORTED;
     int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
     p.splits = 1;

@@ -8,26 +8,65 @@
 namespace gk {
 namespace {
 
-constexpr int COLSUM_SPLITS = 64;
+constexpr int COLSUM_SPLITS = 128;
+constexpr int COLSUM_VEC = 8;  // columns per thread (one 16-byte bf16 load, two float4 loads)
 
-// partial[s][c] = sum of rows r = s, s + S, s + 2S, ... of src[:, c] (ascending r).
 template <typename T>
-__global__ void colsum_partial_kernel(const T* __restrict__ src, int64_t ld, int64_t rows, int64_t cols,
-                                      float* __restrict__ partial) {
-    int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    int s = blockIdx.y;
-    if (c >= cols) return;
-    float acc = 0.f;
-    for (int64_t r = s; r < rows; r += gridDim.y) acc += load_as_f32(src + r * ld + c);
-    partial[(int64_t)s * cols + c] = acc;
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
+    if constexpr (sizeof(T) == 2) {
+        uint4 u = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __low2float(h[k]);
+            v[2 * k + 1] = __high2float(h[k]);
+        }
+    } else {
+        float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
 }
 
-__global__ void colsum_reduce_kernel(const float* __restrict__ partial, int splits, int64_t cols, float* dst) {
-    int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= cols) return;
-    float acc = 0.f;
-    for (int s = 0; s < splits; ++s) acc += partial[(int64_t)s * cols + c];
-    dst[c] += acc;
+// partial[s][c] = sum of rows r = s, s + S, s + 2S, ... of src[:, c] (ascending r). Each
+// thread takes 8 consecutive columns with one vector load per row when the row layout allows.
+template <typename T>
+__global__ void colsum_partial_kernel(const T* __restrict__ src, int64_t ld, int64_t rows, int64_t cols, int vec,
+                                      float* __restrict__ partial) {
+    int64_t c0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * COLSUM_VEC;
+    int s = blockIdx.y;
+    if (c0 >= cols) return;
+    float acc[COLSUM_VEC] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (vec && c0 + COLSUM_VEC <= cols) {
+        for (int64_t r = s; r < rows; r += gridDim.y) {
+            float v[8];
+            load8<T>(src + r * ld + c0, v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] += v[k];
+        }
+    } else {
+        for (int64_t r = s; r < rows; r += gridDim.y)
+            for (int k = 0; k < COLSUM_VEC && c0 + k < cols; ++k) acc[k] += load_as_f32(src + r * ld + c0 + k);
+    }
+    for (int k = 0; k < COLSUM_VEC && c0 + k < cols; ++k) partial[(int64_t)s * cols + c0 + k] = acc[k];
+}
+
+// dst[c] += sum_s partial[s][c]: 8 warps per 32 columns, warp w sums slots w, w + 8, ...,
+// then the warp sums are added in warp order (fixed order, deterministic).
+__global__ void __launch_bounds__(256) colsum_reduce_kernel(const float* __restrict__ partial, int splits,
+                                                           int64_t cols, float* dst) {
+    __shared__ float red[8][32];
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t c = (int64_t)blockIdx.x * 32 + lane;
+    float a = 0.f;
+    if (c < cols)
+        for (int s = warp; s < splits; s += 8) a += partial[(int64_t)s * cols + c];
+    red[warp][lane] = a;
+    __syncthreads();
+    if (warp == 0 && c < cols) {
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += red[w][lane];
+        dst[c] += t;
+    }
 }
 
 }  // namespace
@@ -37,14 +76,16 @@ gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_
     float* partial = (float*)workspace(ctx, (size_t)splits * cols * sizeof(float));
     GK_REQUIRE(ctx, partial, GK_ERR_WORKSPACE, "bias gradient needs %lld workspace bytes",
                (long long)splits * cols * 4);
-    dim3 grid((unsigned)cdiv(cols, 128), (unsigned)splits);
+    int esize = dtype == GK_F32 ? 4 : 2;
+    int vec = aligned16(src) && ((ld * esize) % 16 == 0);
+    dim3 grid((unsigned)cdiv(cdiv(cols, COLSUM_VEC), 64), (unsigned)splits);
     if (dtype == GK_F32)
-        colsum_partial_kernel<float><<<grid, 128, 0, ctx->stream>>>((const float*)src, ld, rows, cols, partial);
+        colsum_partial_kernel<float><<<grid, 64, 0, ctx->stream>>>((const float*)src, ld, rows, cols, vec, partial);
     else
-        colsum_partial_kernel<__nv_bfloat16><<<grid, 128, 0, ctx->stream>>>((const __nv_bfloat16*)src, ld, rows, cols,
-                                                                          partial);
+        colsum_partial_kernel<__nv_bfloat16><<<grid, 64, 0, ctx->stream>>>((const __nv_bfloat16*)src, ld, rows, cols,
+                                                                         vec, partial);
     GK_TRY(launched(ctx, "colsum_partial"));
-    colsum_reduce_kernel<<<(unsigned)cdiv(cols, 256), 256, 0, ctx->stream>>>(partial, splits, cols, dst);
+    colsum_reduce_kernel<<<(unsigned)cdiv(cols, 32), 256, 0, ctx->stream>>>(partial, splits, cols, dst);
     return launched(ctx, "colsum_reduce");
 }
 

@@ -307,18 +307,33 @@ __global__ void layernorm_bwd_block_kernel(const float* __restrict__ x, const fl
     }
 }
 
-// dgamma[c] += sum_p partial[p][0][c]; dbeta[c] += sum_p partial[p][1][c] (p ascending).
-__global__ void reduce_partials_kernel(const float* __restrict__ partial, int nparts, int C, float* dgamma,
-                                       float* dbeta) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
+// dgamma[c] += sum_p partial[p][0][c]; dbeta[c] += sum_p partial[p][1][c]. A block of 8 warps
+// takes 32 columns: warp w sums slots w, w + 8, ... (lane = column, coalesced rows of the
+// partial buffer), then the 8 warp sums are added in warp order: a fixed summation order.
+__global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __restrict__ partial, int nparts, int C,
+                                                             float* dgamma, float* dbeta) {
+    __shared__ float red[2][8][32];
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int c = blockIdx.x * 32 + lane;
     float a = 0.f, b = 0.f;
-    for (int p = 0; p < nparts; ++p) {
-        a += partial[((int64_t)p * 2 + 0) * C + c];
-        b += partial[((int64_t)p * 2 + 1) * C + c];
+    if (c < C) {
+        for (int p = warp; p < nparts; p += 8) {
+            a += partial[((int64_t)p * 2 + 0) * C + c];
+            b += partial[((int64_t)p * 2 + 1) * C + c];
+        }
     }
-    if (dgamma) dgamma[c] += a;
-    if (dbeta) dbeta[c] += b;
+    red[0][warp][lane] = a;
+    red[1][warp][lane] = b;
+    __syncthreads();
+    if (warp == 0 && c < C) {
+        float ta = 0.f, tb = 0.f;
+        for (int w = 0; w < 8; ++w) {
+            ta += red[0][w][lane];
+            tb += red[1][w][lane];
+        }
+        if (dgamma) dgamma[c] += ta;
+        if (dbeta) dbeta[c] += tb;
+    }
 }
 
 // ----------------------------------------------------------------------------- GELU
@@ -707,7 +722,7 @@ gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, cons
     }
     GK_TRY(launched(ctx, "layernorm_bwd"));
     if (want_partials) {
-        reduce_partials_kernel<<<(unsigned)cdiv(C, 256), 256, 0, ctx->stream>>>(partial, nparts, C, dgamma, dbeta);
+        reduce_partials_kernel<<<(unsigned)cdiv(C, 32), 256, 0, ctx->stream>>>(partial, nparts, C, dgamma, dbeta);
         GK_TRY(launched(ctx, "layernorm_bwd_reduce"));
     }
     return GK_OK;
@@ -897,7 +912,7 @@ extern "C" gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x,
     if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
     if (want_partials) {
         // every slot the reduction reads was written in full by the kernel above
-        reduce_partials_kernel<<<(unsigned)cdiv(C, 256), 256, 0, stream>>>(partial, nparts, C, dgamma, dbeta);
+        reduce_partials_kernel<<<(unsigned)cdiv(C, 32), 256, 0, stream>>>(partial, nparts, C, dgamma, dbeta);
         if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
     }
     return GK_OK;

@@ -169,7 +169,7 @@ gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, cons
  *   dW += X^T dY ([K, M]) or dY^T X ([M, K]); float32; may be NULL.
  *   dbias += sum over rows of dY; float32 [M]; may be NULL.
  * [LM1] "Ops...", MatMul backward rule (dx = g w^T, dw = x^T g, both accumulating).
- * dtype is the type of X, W and dY. Workspace for dbias: 64 * M * 4 bytes. */
+ * dtype is the type of X, W and dY. Workspace for dbias: 128 * M * 4 bytes. */
 gk_status gk_matmul_bwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W,
                         int64_t ldw, int transW, const void* dY, int64_t lddy, void* dX,
                         int64_t lddx, int dx_dtype, int accumulate_dX, const void* preact_X,

@@ -24,7 +24,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 64, THREADS = 192;
+constexpr int BM = 128, BN = 256, BK = 64, THREADS = 320;  // 2 + 8 epilogue warps
 constexpr uint32_t A_BYTES = BM * BK * 2;         // 16 KB per operand tile
 constexpr uint32_t B_BYTES = BN * BK * 2;         // 32 KB per operand tile
 constexpr uint32_t TMEM_COLS = 2 * BN;            // two float32 accumulators of 128 x 256
@@ -38,7 +38,7 @@ struct StageCfg {
     static constexpr uint32_t B_SLOT = B_BYTES * (B_LO ? 2 : 1);
     static constexpr uint32_t STAGE = A_SLOT + B_SLOT;
     static constexpr int STAGES = SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2);
-    static constexpr uint32_t EPI = 4 * 32 * 32 * 4;  // 4 KB per epilogue warp
+    static constexpr uint32_t EPI = 8 * 32 * 32 * 4;  // 4 KB per epilogue warp
     static constexpr size_t SMEM = (size_t)STAGES * STAGE + EPI + 1024 + 256;
 };
 constexpr uint64_t WAIT_NS = 1000000000ull;       // bounded waits: 1 s
@@ -60,10 +60,28 @@ struct TcParams {
     int aux_dtype;
     int64_t c_plane;  // > 0: bf16 C also gets its low plane (v - bf16(v)) at C + c_plane
     int vec;          // every epilogue pointer 16-byte aligned and every stride a multiple of 4
+    int fast_act;     // bf16 output without a low plane: GELU through the hardware tanh
     int* err;
 };
 
 // --------------------------------------------------------------------- epilogue
+// GELU (tanh form) with the hardware tanh.approx.f32 instead of tanhf: its error (about
+// 2^-11 relative) is below the bf16 rounding of the outputs it is used for.
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_hw(float x) {
+    const float k = 0.7978845608028654f;
+    return 0.5f * x * (1.0f + tanh_hw(k * (x + 0.044715f * x * x * x)));
+}
+__device__ __forceinline__ float gelu_grad_hw(float x) {
+    const float k = 0.7978845608028654f;
+    float t = tanh_hw(k * (x + 0.044715f * x * x * x));
+    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * x * x);
+}
+
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 template <typename TC>
@@ -147,12 +165,20 @@ __device__ __forceinline__ void epi4(const TcParams& p, int64_t m, int64_t n, fl
             *reinterpret_cast<float4*>(static_cast<float*>(p.aux) + m * p.ldaux + n) = v;
         else
             st4_bf16(static_cast<__nv_bfloat16*>(p.aux) + m * p.ldaux + n, v);
-        v = make_float4(gelu_tanh(v.x), gelu_tanh(v.y), gelu_tanh(v.z), gelu_tanh(v.w));
+        if (p.fast_act)
+            v = make_float4(gelu_hw(v.x), gelu_hw(v.y), gelu_hw(v.z), gelu_hw(v.w));
+        else
+            v = make_float4(gelu_tanh(v.x), gelu_tanh(v.y), gelu_tanh(v.z), gelu_tanh(v.w));
     } else if (p.epi == EPI_DGELU) {
         float4 pre = p.aux_dtype == GK_F32 ? ld4(static_cast<const float*>(p.aux) + m * p.ldaux + n)
                                            : ld4c<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(p.aux) + m * p.ldaux + n);
-        v.x *= gelu_tanh_grad(pre.x); v.y *= gelu_tanh_grad(pre.y);
-        v.z *= gelu_tanh_grad(pre.z); v.w *= gelu_tanh_grad(pre.w);
+        if (p.fast_act) {
+            v.x *= gelu_grad_hw(pre.x); v.y *= gelu_grad_hw(pre.y);
+            v.z *= gelu_grad_hw(pre.z); v.w *= gelu_grad_hw(pre.w);
+        } else {
+            v.x *= gelu_tanh_grad(pre.x); v.y *= gelu_tanh_grad(pre.y);
+            v.z *= gelu_tanh_grad(pre.z); v.w *= gelu_tanh_grad(pre.w);
+        }
     }
     if constexpr (sizeof(TC) == 4) {
         *reinterpret_cast<float4*>(C + ci) = v;
@@ -204,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 128);
+            mbar_init(&tempty[b], 256);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -331,8 +357,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else {
-        // epilogue warps 2..5; a warp may read TMEM lanes 32 * (warp % 4) .. + 31
+        // epilogue warps 2..9; a warp may read TMEM lanes 32 * (warp % 4) .. + 31; two warps
+        // share each lane quarter and take alternate halves of the tile's columns
         int q = warp & 3;
+        int half = (warp - 2) >> 2;
         uint32_t j = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
             int tm, tn, kb0, kb1;
@@ -350,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // and the stores are coalesced 16-byte accesses.
             float* stg = epi_stage + (warp - 2) * 1024;
             const int64_t mrow0 = (int64_t)tm * BM + q * 32;
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + c0, r);
 #pragma unroll
@@ -361,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 const int64_t n0 = (int64_t)tn * BN + c0;
                 if (n0 < p.N) {
-#pragma unroll 2
+#pragma unroll 4
                     for (int pass = 0; pass < 8; ++pass) {
                         int rr = pass * 4 + (lane >> 3), c = lane & 7;
                         float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((c ^ (rr & 7)) << 2));
@@ -438,6 +466,7 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.aux_dtype = g.aux_dtype;
     p.err = ctx->d_err;
     p.c_plane = g.c_plane;
+    p.fast_act = g.c_dtype == GK_BF16 && g.c_plane == 0;
     p.vec = aligned16(g.C) && (g.ldc % 4 == 0) && (!g.bias || aligned16(g.bias)) &&
             (!g.residual || (aligned16(g.residual) && g.ldr % 4 == 0)) &&
             (!g.aux || (aligned16(g.aux) && g.ldaux % 4 == 0)) && (g.c_plane % 4 == 0);

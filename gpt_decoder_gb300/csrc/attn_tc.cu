@@ -360,53 +360,51 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
     bool aborted = false;
 
-    for (int qt = first_qt; qt < n_qt; ++qt) {
+    // prologue: S^T and dP^T of the first query tile
+    bool fail0 = false;
+    if (tid == 0) {
+        bool w = mbar_wait(bar_kv, 0, nullptr, WAIT_NS) && mbar_wait(&bar_qo[0], 0, nullptr, WAIT_NS);
+        if (w) {
+            pending_kv = 0;
+            pending_qo[0] = 0;
+            tc_fence_after();
+            uint32_t k_a = saddr(sK), v_a = saddr(sV), q_a = saddr(sQ), o_a = saddr(sO);
+#pragma unroll
+            for (int k = 0; k < HS / 16; ++k)
+                umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(q_a + k * 32, 16, 1024), id_s, k > 0);
+#pragma unroll
+            for (int k = 0; k < HS / 16; ++k)
+                umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(o_a + k * 32, 16, 1024), id_s,
+                          k > 0);
+            umma_commit(bar_1);
+            if (first_qt + 1 < n_qt) {
+                mbar_expect_tx(&bar_qo[1], 2 * TILE);
+                tma_load_2d(&tm_qkv, &bar_qo[1], sQ + TILE, h * HS, row0 + (first_qt + 1) * QT);
+                tma_load_2d(&tm_dy, &bar_qo[1], sO + TILE, h * HS, row0 + (first_qt + 1) * QT);
+                pending_qo[1] = 1;
+            }
+        }
+        fail0 = !w;
+    }
+    if (__syncthreads_or(fail0)) aborted = true;
+
+    for (int qt = first_qt; !aborted && qt < n_qt; ++qt) {
         const int it = qt - first_qt;
         const int st = it & 1;
-        const uint32_t qph = (it >> 1) & 1, ph = it & 1;
+        const uint32_t ph = it & 1;
         const int q0 = qt * QT;
-        bool fail = false;
-        if (tid == 0) {
-            bool w = (it > 0 || mbar_wait(bar_kv, 0, nullptr, WAIT_NS)) && mbar_wait(&bar_qo[st], qph, nullptr, WAIT_NS);
-            if (w) {
-                pending_kv = 0;
-                pending_qo[st] = 0;
-                tc_fence_after();
-                uint32_t k_a = saddr(sK), v_a = saddr(sV), q_a = saddr(sQ + st * TILE), o_a = saddr(sO + st * TILE);
-#pragma unroll
-                for (int k = 0; k < HS / 16; ++k)
-                    umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(q_a + k * 32, 16, 1024), id_s, k > 0);
-#pragma unroll
-                for (int k = 0; k < HS / 16; ++k)
-                    umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(o_a + k * 32, 16, 1024), id_s,
-                              k > 0);
-                umma_commit(bar_1);
-                if (qt + 1 < n_qt) {
-                    // stage st^1 was last read by the previous tile's MMAs, finished at bar_2
-                    int ns = st ^ 1;
-                    mbar_expect_tx(&bar_qo[ns], 2 * TILE);
-                    tma_load_2d(&tm_qkv, &bar_qo[ns], sQ + ns * TILE, h * HS, row0 + (qt + 1) * QT);
-                    tma_load_2d(&tm_dy, &bar_qo[ns], sO + ns * TILE, h * HS, row0 + (qt + 1) * QT);
-                    pending_qo[ns] = 1;
-                }
-            }
-            fail = !w;
-        }
         {
             int q = q0 + r;
             sL[r] = q < T ? lse[(int64_t)bh * T + q] * L2E : 0.f;
             sD[r] = q < T ? dvec[(int64_t)bh * T + q] : 0.f;
         }
-        if (__syncthreads_or(fail)) {
-            aborted = true;
-            break;
-        }
+        // (the barrier below also orders these shared-memory writes before their use)
         if (__syncthreads_or(!mbar_wait(bar_1, ph, nullptr, WAIT_NS))) {
             aborted = true;
             break;
         }
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < QT; c0 += 32) {
             uint32_t sv[32], dv[32];
             tmem_ld32(lane_addr + c0, sv);
@@ -439,9 +437,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
+        bool fail = false;
         if (tid == 0) {
             tc_fence_after();
-            uint32_t pt_a = saddr(sPT), ds_a = saddr(sDS), k_a = saddr(sK);
+            uint32_t pt_a = saddr(sPT), ds_a = saddr(sDS), k_a = saddr(sK), v_a = saddr(sV);
             uint32_t q_a = saddr(sQ + st * TILE), o_a = saddr(sO + st * TILE);
 #pragma unroll
             for (int k = 0; k < QT / 16; ++k) {
@@ -456,12 +455,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                 umma_bf16(tmem + 384, smem_desc(ds_a + k * 2048, 16384, 1024), smem_desc(k_a + k * 2048, 8192, 1024),
                           id_q, k > 0);
             umma_commit(bar_2);
+            // S^T and dP^T of the next query tile right behind: they overlap the dQ accumulation
+            if (qt + 1 < n_qt) {
+                int ns = st ^ 1;
+                bool w = mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, nullptr, WAIT_NS);
+                if (w) {
+                    pending_qo[ns] = 0;
+                    tc_fence_after();
+                    uint32_t nq_a = saddr(sQ + ns * TILE), no_a = saddr(sO + ns * TILE);
+#pragma unroll
+                    for (int k = 0; k < HS / 16; ++k)
+                        umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(nq_a + k * 32, 16, 1024), id_s,
+                                  k > 0);
+#pragma unroll
+                    for (int k = 0; k < HS / 16; ++k)
+                        umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(no_a + k * 32, 16, 1024),
+                                  id_s, k > 0);
+                    umma_commit(bar_1);
+                }
+                fail = !w;
+            }
         }
-        if (__syncthreads_or(!mbar_wait(bar_2, ph, nullptr, WAIT_NS))) {
+        if (__syncthreads_or(fail || !mbar_wait(bar_2, ph, nullptr, WAIT_NS))) {
             aborted = true;
             break;
         }
         tc_fence_after();
+        // stage st (Q, dO of this tile) is free now: prefetch the tile after next into it
+        if (tid == 0 && qt + 2 < n_qt) {
+            mbar_expect_tx(&bar_qo[st], 2 * TILE);
+            tma_load_2d(&tm_qkv, &bar_qo[st], sQ + st * TILE, h * HS, row0 + (qt + 2) * QT);
+            tma_load_2d(&tm_dy, &bar_qo[st], sO + st * TILE, h * HS, row0 + (qt + 2) * QT);
+            pending_qo[st] = 1;
+        }
         {
             int q = q0 + r;
 #pragma unroll
@@ -471,7 +497,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (q < T) {
                     float* dst = dq_acc + (int64_t)(row0 + q) * C + h * HS + c0;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) atomicAdd(dst + i, __uint_as_float(v[i]) * 0.125f);
+                    for (int i = 0; i < 32; i += 4)
+                        atomicAdd(reinterpret_cast<float4*>(dst + i),
+                                  make_float4(__uint_as_float(v[i]) * 0.125f, __uint_as_float(v[i + 1]) * 0.125f,
+                                              __uint_as_float(v[i + 2]) * 0.125f, __uint_as_float(v[i + 3]) * 0.125f));
                 }
             }
         }

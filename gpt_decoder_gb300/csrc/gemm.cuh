@@ -1,4 +1,5 @@
-// Internal GEMM interface: C[M,N] (=|+=) epi(sum_k A(m,k) B(k,n) + bias[n] + residual[m,n]).
+// Internal GEMM interface: C[M,N] (=|+=) epi(sum_k A(m,k) B(k,n) + bias[n] + residual[m,n]);
+// with `accumulate` the epilogue's result is added to C (C_old + epi(...)).
 //
 // Operand majorness covers every product of the decoder step without transpose passes:
 //   A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m];

@@ -52,7 +52,6 @@ __device__ __forceinline__ void epilogue_store(const Gemm& g, int64_t m, int64_t
     if (m >= g.M || n >= g.N) return;
     TC* C = static_cast<TC*>(g.C);
     int64_t ci = m * g.ldc + n;
-    if (g.accumulate) v += load_as_f32(C + ci);
     if (g.bias) v += g.bias[n];
     if (g.residual) v += g.residual[m * g.ldr + n];
     if (g.epi == EPI_GELU) {
@@ -66,6 +65,7 @@ __device__ __forceinline__ void epilogue_store(const Gemm& g, int64_t m, int64_t
                                           : __bfloat162float(static_cast<const __nv_bfloat16*>(g.aux)[m * g.ldaux + n]);
         v *= gelu_tanh_grad(pre);
     }
+    if (g.accumulate) v += load_as_f32(C + ci);
     store_from_f32(C + ci, v);
     if (g.c_plane) {
         __nv_bfloat16* Cb = reinterpret_cast<__nv_bfloat16*>(C);

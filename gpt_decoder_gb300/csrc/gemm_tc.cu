@@ -39,7 +39,7 @@ struct StageCfg {
     static constexpr uint32_t STAGE = A_SLOT + B_SLOT;
     static constexpr int STAGES = SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2);
     static constexpr uint32_t EPI = 8 * 32 * 32 * 4;  // 4 KB per epilogue warp
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE + EPI + 1024 + 256;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + EPI + 1024 + 512;
 };
 constexpr uint64_t WAIT_NS = 1000000000ull;       // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;       // after an abort: 0.2 s per drain wait
@@ -61,8 +61,19 @@ struct TcParams {
     int64_t c_plane;  // > 0: bf16 C also gets its low plane (v - bf16(v)) at C + c_plane
     int vec;          // every epilogue pointer 16-byte aligned and every stride a multiple of 4
     int fast_act;     // bf16 output without a low plane: GELU through the hardware tanh
+    // Epilogue through shared memory and TMA (every plane has C's element type): each warp
+    // drains 32 rows x 64 bytes per chunk into a swizzled 2 KB slot that one TMA store (or
+    // float32 reduce-add) writes out; an input plane is fetched by TMA a chunk ahead.
+    int tma_epi;
+    int in_kind;      // IN_NONE / IN_C (accumulate by load) / IN_RES (residual) / IN_AUX (GELU backward)
+    int reduce_out;   // C += v by TMA reduce-add (float32 C)
+    int out_aux;      // GELU: the pre-activation plane is stored too
+    int out_lo;       // bf16 C: its low plane is stored too
     int* err;
 };
+
+enum { IN_NONE = 0, IN_C = 1, IN_RES = 2, IN_AUX = 3 };
+constexpr uint32_t SLOT = 2048;  // one epilogue chunk: 32 rows x 64 bytes
 
 // --------------------------------------------------------------------- epilogue
 // GELU (tanh form) with the hardware tanh.approx.f32 instead of tanhf: its error (about
@@ -112,7 +123,6 @@ __device__ __forceinline__ void epi1(const TcParams& p, int64_t m, int64_t n, fl
         return;
     }
     TC* C = static_cast<TC*>(p.C);
-    if (p.accumulate) v += load_as_f32(C + ci);
     if (p.bias) v += p.bias[n];
     if (p.residual) v += p.residual[m * p.ldr + n];
     if (p.epi == EPI_GELU) {
@@ -126,6 +136,7 @@ __device__ __forceinline__ void epi1(const TcParams& p, int64_t m, int64_t n, fl
                                           : __bfloat162float(static_cast<const __nv_bfloat16*>(p.aux)[m * p.ldaux + n]);
         v *= gelu_tanh_grad(pre);
     }
+    if (p.accumulate) v += load_as_f32(C + ci);
     store_from_f32(C + ci, v);
     if (p.c_plane) {
         __nv_bfloat16* Cb = static_cast<__nv_bfloat16*>(p.C);
@@ -148,10 +159,6 @@ __device__ __forceinline__ void epi4(const TcParams& p, int64_t m, int64_t n, fl
         return;
     }
     TC* C = static_cast<TC*>(p.C);
-    if (p.accumulate) {
-        float4 c = ld4c<TC>(C + ci);
-        v.x += c.x; v.y += c.y; v.z += c.z; v.w += c.w;
-    }
     if (p.bias) {
         float4 b = ld4(p.bias + n);
         v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
@@ -180,6 +187,78 @@ __device__ __forceinline__ void epi4(const TcParams& p, int64_t m, int64_t n, fl
             v.z *= gelu_tanh_grad(pre.z); v.w *= gelu_tanh_grad(pre.w);
         }
     }
+    if (p.accumulate) {
+        float4 c = ld4c<TC>(C + ci);
+        v.x += c.x; v.y += c.y; v.z += c.z; v.w += c.w;
+    }
+    if constexpr (sizeof(TC) == 4) {
+        *reinterpret_cast<float4*>(C + ci) = v;
+    } else {
+        __nv_bfloat16* Cb = reinterpret_cast<__nv_bfloat16*>(C);
+        st4_bf16(Cb + ci, v);
+        if (p.c_plane) {
+            float4 h = ld4c<__nv_bfloat16>(Cb + ci);
+            st4_bf16(Cb + ci + p.c_plane, make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w));
+        }
+    }
+}
+
+// Two-phase form of epi4 for a whole chunk: every global operand the epilogue reads (C when
+// accumulating, the residual, the GELU pre-activation) is loaded first for all rows of the
+// chunk, then the values are combined and stored; stores to C could alias those operands,
+// so this ordering is what lets the loads overlap instead of paying one latency per row.
+struct EpiIn {
+    float4 c, r, a;
+};
+
+template <typename TC>
+__device__ __forceinline__ bool epi_vec_ok(const TcParams& p, int64_t m, int64_t n) {
+    return m < p.M && p.vec && n + 3 < p.N;
+}
+
+template <typename TC>
+__device__ __forceinline__ void epi_load(const TcParams& p, int64_t m, int64_t n, EpiIn& e) {
+    if (!epi_vec_ok<TC>(p, m, n) || p.atomic_out) return;
+    if (p.accumulate) e.c = ld4c<TC>(static_cast<const TC*>(p.C) + m * p.ldc + n);
+    if (p.residual) e.r = ld4(p.residual + m * p.ldr + n);
+    if (p.epi == EPI_DGELU)
+        e.a = p.aux_dtype == GK_F32 ? ld4(static_cast<const float*>(p.aux) + m * p.ldaux + n)
+                                    : ld4c<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(p.aux) + m * p.ldaux + n);
+}
+
+template <typename TC>
+__device__ __forceinline__ void epi_finish(const TcParams& p, int64_t m, int64_t n, float4 v, const EpiIn& e) {
+    if (m >= p.M || n >= p.N) return;
+    if (!epi_vec_ok<TC>(p, m, n) || p.atomic_out) {
+        epi4<TC>(p, m, n, v);
+        return;
+    }
+    int64_t ci = m * p.ldc + n;
+    TC* C = static_cast<TC*>(p.C);
+    if (p.bias) {
+        float4 b = ld4(p.bias + n);
+        v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+    }
+    if (p.residual) { v.x += e.r.x; v.y += e.r.y; v.z += e.r.z; v.w += e.r.w; }
+    if (p.epi == EPI_GELU) {
+        if (p.aux_dtype == GK_F32)
+            *reinterpret_cast<float4*>(static_cast<float*>(p.aux) + m * p.ldaux + n) = v;
+        else
+            st4_bf16(static_cast<__nv_bfloat16*>(p.aux) + m * p.ldaux + n, v);
+        if (p.fast_act)
+            v = make_float4(gelu_hw(v.x), gelu_hw(v.y), gelu_hw(v.z), gelu_hw(v.w));
+        else
+            v = make_float4(gelu_tanh(v.x), gelu_tanh(v.y), gelu_tanh(v.z), gelu_tanh(v.w));
+    } else if (p.epi == EPI_DGELU) {
+        if (p.fast_act) {
+            v.x *= gelu_grad_hw(e.a.x); v.y *= gelu_grad_hw(e.a.y);
+            v.z *= gelu_grad_hw(e.a.z); v.w *= gelu_grad_hw(e.a.w);
+        } else {
+            v.x *= gelu_tanh_grad(e.a.x); v.y *= gelu_tanh_grad(e.a.y);
+            v.z *= gelu_tanh_grad(e.a.z); v.w *= gelu_tanh_grad(e.a.w);
+        }
+    }
+    if (p.accumulate) { v.x += e.c.x; v.y += e.c.y; v.z += e.c.z; v.w += e.c.w; }
     if constexpr (sizeof(TC) == 4) {
         *reinterpret_cast<float4*>(C + ci) = v;
     } else {
@@ -200,10 +279,304 @@ __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, i
     kb1 = min(p.kblocks, kb0 + p.kbps);
 }
 
+// ------------------------------------------------------------ TMA epilogue
+// Chunks of this warp's part of a tile: rows 32q .. 32q+31 of the tile, columns
+// half*128 .. +127 cut into chunks of W = 64 / sizeof(TC) columns; chunks wholly outside
+// the matrix are skipped.
+template <typename TC>
+__device__ __forceinline__ int epi_chunks(const TcParams& p, int tm, int tn, int q, int half) {
+    constexpr int W = 64 / (int)sizeof(TC);
+    if (tm * BM + q * 32 >= p.M) return 0;
+    int rem = p.N - (tn * BN + half * (BN / 2));
+    if (rem <= 0) return 0;
+    return min((BN / 2) / W, (rem + W - 1) / W);
+}
+
+// Advance (u, ch) to this warp's next chunk, possibly in a later unit of this CTA.
+template <typename TC>
+__device__ __forceinline__ bool epi_next(const TcParams& p, int units, int& u, int& ch, int q, int half) {
+    int tm, tn, kb0, kb1;
+    unit_coords(p, u, tm, tn, kb0, kb1);
+    if (ch + 1 < epi_chunks<TC>(p, tm, tn, q, half)) {
+        ++ch;
+        return true;
+    }
+    for (int v = u + gridDim.x; v < units; v += gridDim.x) {
+        unit_coords(p, v, tm, tn, kb0, kb1);
+        if (epi_chunks<TC>(p, tm, tn, q, half) > 0) {
+            u = v;
+            ch = 0;
+            return true;
+        }
+    }
+    return false;
+}
+
+// Slot rows are 64 bytes in the TMA 64-byte swizzle: 16-byte piece j of row r sits at piece
+// j ^ ((r >> 1) & 3). Each lane owns one row.
+__device__ __forceinline__ uint8_t* slot_piece(uint8_t* slot, int row, int j) {
+    return slot + row * 64 + ((j ^ ((row >> 1) & 3)) << 4);
+}
+
+template <typename TC>
+__device__ __forceinline__ void slot_write(uint8_t* slot, int row, const float (&v)[32]) {
+    if constexpr (sizeof(TC) == 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 w;
+            __nv_bfloat162 a = __floats2bfloat162_rn(v[8 * j], v[8 * j + 1]);
+            __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+            __nv_bfloat162 c = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+            __nv_bfloat162 d = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+            w.x = *reinterpret_cast<uint32_t*>(&a);
+            w.y = *reinterpret_cast<uint32_t*>(&b);
+            w.z = *reinterpret_cast<uint32_t*>(&c);
+            w.w = *reinterpret_cast<uint32_t*>(&d);
+            *reinterpret_cast<uint4*>(slot_piece(slot, row, j)) = w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<float4*>(slot_piece(slot, row, j)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+}
+
+template <typename TC>
+__device__ __forceinline__ void slot_read(uint8_t* slot, int row, float (&v)[32]) {
+    if constexpr (sizeof(TC) == 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 w = *reinterpret_cast<const uint4*>(slot_piece(slot, row, j));
+            uint32_t u4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u4[k]);
+                v[8 * j + 2 * k] = __low2float(h);
+                v[8 * j + 2 * k + 1] = __high2float(h);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float4 f = *reinterpret_cast<const float4*>(slot_piece(slot, row, j));
+            v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+        }
+    }
+}
+
+struct EpiMaps {
+    const CUtensorMap* C;
+    const CUtensorMap* aux;
+    const CUtensorMap* lo;
+    const CUtensorMap* in;  // the input plane's map (C, residual or aux), or null
+};
+
+// Epilogue warp (one of 8) of the TMA path. Returns false if it gave up on a wait.
+template <typename TC>
+__device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slots, uint64_t* inbar, uint64_t* tfull,
+                             uint64_t* tempty, volatile int* abort_flag, uint32_t tmem_base, int warp, int lane,
+                             int units) {
+    constexpr int W = 64 / (int)sizeof(TC);
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const bool has_in = p.in_kind != IN_NONE;
+    uint32_t g = 0;       // chunks processed by this warp
+    uint32_t kst = 0;     // single-slot stores issued (output-only path)
+    int pend_slot = -1;   // lane 0: slot of the input load in flight, for the abort drain
+    uint32_t pend_par = 0;
+    bool ok = true;
+
+    // the first chunk's input
+    if (has_in && lane == 0) {
+        int u0 = blockIdx.x, c0 = -1;
+        bool any = false;
+        for (int v = blockIdx.x; v < units && !any; v += gridDim.x) {
+            int tm, tn, kb0, kb1;
+            unit_coords(p, v, tm, tn, kb0, kb1);
+            if (epi_chunks<TC>(p, tm, tn, q, half) > 0) {
+                u0 = v;
+                c0 = 0;
+                any = true;
+            }
+        }
+        if (any) {
+            int tm, tn, kb0, kb1;
+            unit_coords(p, u0, tm, tn, kb0, kb1);
+            mbar_expect_tx(&inbar[0], SLOT);
+            tma_load_2d(mp.in, &inbar[0], slots, tn * BN + half * (BN / 2) + c0 * W, tm * BM + q * 32);
+            pend_slot = 0;
+            pend_par = 0;
+        }
+    }
+
+    uint32_t j = 0;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+        int tm, tn, kb0, kb1;
+        unit_coords(p, u, tm, tn, kb0, kb1);
+        const uint32_t buf = j & 1, aph = (j >> 1) & 1;
+        // warp-uniform outcome: every lane leaves together or none does
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], aph, abort_flag, WAIT_NS))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const int nch = epi_chunks<TC>(p, tm, tn, q, half);
+        // warm L2 with the next unit's input while this tile drains
+        if (has_in && lane == 0 && u + (int)gridDim.x < units) {
+            int tm2, tn2, a2, b2;
+            unit_coords(p, u + gridDim.x, tm2, tn2, a2, b2);
+            const int n2 = epi_chunks<TC>(p, tm2, tn2, q, half);
+            for (int c = 0; c < n2; ++c)
+                tma_prefetch_l2_2d(mp.in, tn2 * BN + half * (BN / 2) + c * W, tm2 * BM + q * 32);
+        }
+        const int y = tm * BM + q * 32;
+        for (int ch = 0; ch < nch; ++ch, ++g) {
+            const int x = tn * BN + half * (BN / 2) + ch * W;
+            const uint32_t s = g & 1;
+            // the next chunk's input goes into the other slot once its last store has read it
+            if (has_in && lane == 0) {
+                int nu = u, nc = ch;
+                if (epi_next<TC>(p, units, nu, nc, q, half)) {
+                    int tm2, tn2, a2, b2;
+                    unit_coords(p, nu, tm2, tn2, a2, b2);
+                    bulk_wait_read<0>();
+                    mbar_expect_tx(&inbar[s ^ 1], SLOT);
+                    tma_load_2d(mp.in, &inbar[s ^ 1], slots + (s ^ 1) * SLOT, tn2 * BN + half * (BN / 2) + nc * W,
+                                tm2 * BM + q * 32);
+                    pend_slot = (int)(s ^ 1);
+                    pend_par = ((g + 1) >> 1) & 1;
+                }
+            }
+            uint32_t r[32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + half * (BN / 2) + ch * W;
+            if constexpr (W == 32)
+                tmem_ld32_nowait(taddr, r);
+            else
+                tmem_ld16_nowait(taddr, r);
+            float v[32];
+            if (p.bias) {
+                if (p.vec && x + W <= p.N) {
+#pragma unroll
+                    for (int i = 0; i < W / 4; ++i) {
+                        float4 b = ld4(p.bias + x + 4 * i);
+                        v[4 * i] = b.x; v[4 * i + 1] = b.y; v[4 * i + 2] = b.z; v[4 * i + 3] = b.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < W; ++i) v[i] = x + i < p.N ? p.bias[x + i] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < W; ++i) v[i] = 0.f;
+            }
+            tmem_wait_ld(r);
+#pragma unroll
+            for (int i = 0; i < W; ++i) v[i] += __uint_as_float(r[i]);
+
+            if (has_in) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&inbar[s], (g >> 1) & 1, abort_flag, WAIT_NS))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0 && pend_slot == (int)s) pend_slot = -1;
+                float in[32];
+                slot_read<TC>(slots + s * SLOT, lane, in);
+                if (p.in_kind == IN_RES) {
+#pragma unroll
+                    for (int i = 0; i < W; ++i) v[i] += in[i];
+                } else if (p.in_kind == IN_AUX) {
+                    if (p.fast_act) {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[i] *= gelu_grad_hw(in[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[i] *= gelu_tanh_grad(in[i]);
+                    }
+                } else {  // IN_C: accumulate by load
+#pragma unroll
+                    for (int i = 0; i < W; ++i) v[i] += in[i];
+                }
+                __syncwarp();  // every lane has read its row before the slot is overwritten
+                slot_write<TC>(slots + s * SLOT, lane, v);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (p.reduce_out)
+                        tma_reduce_add_2d(mp.C, slots + s * SLOT, x, y);
+                    else
+                        tma_store_2d(mp.C, slots + s * SLOT, x, y);
+                    bulk_commit();
+                }
+            } else {
+                // up to three planes (GELU pre-activation, C, C's low plane), each through the
+                // slot whose previous store has finished reading it
+                if (p.out_aux) {
+                    const uint32_t sl = kst++ & 1;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    slot_write<TC>(slots + sl * SLOT, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(mp.aux, slots + sl * SLOT, x, y);
+                        bulk_commit();
+                    }
+                    if (p.fast_act) {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[i] = gelu_hw(v[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[i] = gelu_tanh(v[i]);
+                    }
+                }
+                {
+                    const uint32_t sl = kst++ & 1;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    slot_write<TC>(slots + sl * SLOT, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (p.reduce_out)
+                            tma_reduce_add_2d(mp.C, slots + sl * SLOT, x, y);
+                        else
+                            tma_store_2d(mp.C, slots + sl * SLOT, x, y);
+                        bulk_commit();
+                    }
+                }
+                if (p.out_lo) {
+#pragma unroll
+                    for (int i = 0; i < W; ++i) v[i] -= __bfloat162float(__float2bfloat16_rn(v[i]));
+                    const uint32_t sl = kst++ & 1;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    slot_write<TC>(slots + sl * SLOT, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(mp.lo, slots + sl * SLOT, x, y);
+                        bulk_commit();
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[buf]);
+    }
+    if (lane == 0) {
+        if (pend_slot >= 0) mbar_wait(&inbar[pend_slot], pend_par, nullptr, DRAIN_NS);
+        bulk_wait_all();
+    }
+    __syncwarp();
+    return ok;
+}
+
 template <typename TC, int SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA_lo, const __grid_constant__ CUtensorMap tmB_lo,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmAux,
+                   const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmLo,
                    const TcParams p) {
     using SC = StageCfg<SPLIT>;
     constexpr int STAGES = SC::STAGES;
@@ -217,8 +590,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = bars + 2 * STAGES + 2;
     uint64_t* drain = bars + 2 * STAGES + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 6);
+    uint64_t* inbars = bars + 2 * STAGES + 5;  // 2 per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 21);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 22);
 
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int units = p.tiles_m * p.tiles_n * p.splits;
@@ -233,6 +607,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[b], 256);
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < 16; ++i) mbar_init(&inbars[i], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -356,6 +731,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
+    } else if (p.tma_epi) {
+        EpiMaps mp{&tmC, &tmAux, &tmLo,
+                   p.in_kind == IN_C ? &tmC : p.in_kind == IN_RES ? &tmR : p.in_kind == IN_AUX ? &tmAux : nullptr};
+        uint8_t* slots = reinterpret_cast<uint8_t*>(epi_stage) + (warp - 2) * 2 * SLOT;
+        if (!epilogue_tma<TC>(p, mp, slots, inbars + 2 * (warp - 2), tfull, tempty, abort_flag, tmem_base, warp, lane,
+                              units)) {
+            *abort_flag = 1;
+            report(p.err, GK_ERR_TIMEOUT);
+        }
     } else {
         // epilogue warps 2..9; a warp may read TMEM lanes 32 * (warp % 4) .. + 31; two warps
         // share each lane quarter and take alternate halves of the tile's columns
@@ -389,11 +773,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 const int64_t n0 = (int64_t)tn * BN + c0;
                 if (n0 < p.N) {
-#pragma unroll 4
-                    for (int pass = 0; pass < 8; ++pass) {
-                        int rr = pass * 4 + (lane >> 3), c = lane & 7;
-                        float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((c ^ (rr & 7)) << 2));
-                        epi4<TC>(p, mrow0 + rr, n0 + c * 4, v);
+                    const int c = lane & 7;
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        float4 v[4];
+                        EpiIn e[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            int rr = (half * 4 + i) * 4 + (lane >> 3);
+                            v[i] = *reinterpret_cast<const float4*>(stg + rr * 32 + ((c ^ (rr & 7)) << 2));
+                            epi_load<TC>(p, mrow0 + rr, n0 + c * 4, e[i]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            epi_finish<TC>(p, mrow0 + (half * 4 + i) * 4 + (lane >> 3), n0 + c * 4, v[i], e[i]);
                     }
                 }
                 __syncwarp();
@@ -410,27 +803,60 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+struct Maps {
+    CUtensorMap a, b, al, bl, c, aux, r, lo;
+};
+
 template <typename TC, int SPLIT>
-void launch_one(gk_ctx* ctx, int grid, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& al,
-                const CUtensorMap& bl, const TcParams& p) {
+void launch_one(gk_ctx* ctx, int grid, const Maps& m, const TcParams& p) {
     static bool attr = false;
     constexpr size_t smem = StageCfg<SPLIT>::SMEM;
     if (!attr) {
         cudaFuncSetAttribute(gemm_tc_kernel<TC, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    gemm_tc_kernel<TC, SPLIT><<<grid, THREADS, smem, ctx->stream>>>(a, b, al, bl, p);
+    gemm_tc_kernel<TC, SPLIT><<<grid, THREADS, smem, ctx->stream>>>(m.a, m.b, m.al, m.bl, m.c, m.aux, m.r, m.lo, p);
 }
 
 template <typename TC>
-void launch_split(gk_ctx* ctx, int split, int grid, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& al,
-                  const CUtensorMap& bl, const TcParams& p) {
+void launch_split(gk_ctx* ctx, int split, int grid, const Maps& m, const TcParams& p) {
     switch (split) {
-        case 0: launch_one<TC, 0>(ctx, grid, a, b, al, bl, p); break;
-        case 1: launch_one<TC, 1>(ctx, grid, a, b, al, bl, p); break;
-        case 2: launch_one<TC, 2>(ctx, grid, a, b, al, bl, p); break;
-        default: launch_one<TC, 3>(ctx, grid, a, b, al, bl, p); break;
+        case 0: launch_one<TC, 0>(ctx, grid, m, p); break;
+        case 1: launch_one<TC, 1>(ctx, grid, m, p); break;
+        case 2: launch_one<TC, 2>(ctx, grid, m, p); break;
+        default: launch_one<TC, 3>(ctx, grid, m, p); break;
     }
+}
+
+// Decide whether the TMA epilogue takes this GEMM and build its tensor maps: every plane
+// (C, the GELU pre-activation, the residual, C's low plane) has C's element type, 16-byte
+// aligned bases and strides, and at most one plane is read.
+bool setup_tma_epilogue(const Gemm& g, TcParams& p, Maps& m) {
+    const bool bf = g.c_dtype == GK_BF16;
+    if (g.c_dtype != GK_BF16 && g.c_dtype != GK_F32) return false;
+    const int esz = bf ? 2 : 4, W = 64 / esz;
+    auto ok_plane = [&](const void* base, int64_t ld) {
+        return base && aligned16(base) && (ld * esz) % 16 == 0 && ld >= g.N;
+    };
+    if (!ok_plane(g.C, g.ldc)) return false;
+    if (g.bias && !aligned16(g.bias)) return false;
+    if (g.epi != EPI_NONE && (!g.aux || g.aux_dtype != g.c_dtype || !ok_plane(g.aux, g.ldaux))) return false;
+    if (g.residual && (bf || !ok_plane(g.residual, g.ldr))) return false;
+    if (g.c_plane && (!bf || (g.c_plane * 2) % 16 != 0)) return false;
+    p.reduce_out = g.accumulate && !bf && !g.c_plane;
+    int inputs = (g.residual ? 1 : 0) + (g.epi == EPI_DGELU ? 1 : 0) + (g.accumulate && !p.reduce_out ? 1 : 0);
+    // a chunk with an input plane is rewritten in place: one output plane only
+    if (inputs > 1 || (inputs == 1 && (g.epi == EPI_GELU || g.c_plane))) return false;
+    p.in_kind = g.residual ? IN_RES : g.epi == EPI_DGELU ? IN_AUX : (g.accumulate && !p.reduce_out) ? IN_C : IN_NONE;
+    p.out_aux = g.epi == EPI_GELU;
+    p.out_lo = g.c_plane != 0;
+    if (!make_map_epi(&m.c, bf, g.C, g.N, g.M, g.ldc, W)) return false;
+    m.aux = m.r = m.lo = m.c;
+    if (g.epi != EPI_NONE && !make_map_epi(&m.aux, bf, g.aux, g.N, g.M, g.ldaux, W)) return false;
+    if (g.residual && !make_map_epi(&m.r, false, g.residual, g.N, g.M, g.ldr, W)) return false;
+    if (g.c_plane && !make_map_epi(&m.lo, true, static_cast<const __nv_bfloat16*>(g.C) + g.c_plane, g.N, g.M, g.ldc, W))
+        return false;
+    return true;
 }
 
 }  // namespace
@@ -485,15 +911,25 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     int64_t units = tiles * p.splits;
     int grid = (int)std::min<int64_t>(units, ctx->num_sms);
     int split = (g.A_lo ? 1 : 0) | (g.B_lo ? 2 : 0);
-    CUtensorMap ta_lo = ta, tb_lo = tb;
-    if (g.A_lo && !(g.a_kmajor ? make_map(&ta_lo, g.A_lo, g.K, g.M, g.lda, BM) : make_map(&ta_lo, g.A_lo, g.M, g.K, g.lda, 64)))
+    Maps m;
+    m.a = ta;
+    m.b = tb;
+    m.al = ta;
+    m.bl = tb;
+    if (g.A_lo && !(g.a_kmajor ? make_map(&m.al, g.A_lo, g.K, g.M, g.lda, BM) : make_map(&m.al, g.A_lo, g.M, g.K, g.lda, 64)))
         return GK_ERR_UNSUPPORTED;
-    if (g.B_lo && !(g.b_kmajor ? make_map(&tb_lo, g.B_lo, g.K, g.N, g.ldb, BN) : make_map(&tb_lo, g.B_lo, g.N, g.K, g.ldb, 64)))
+    if (g.B_lo && !(g.b_kmajor ? make_map(&m.bl, g.B_lo, g.K, g.N, g.ldb, BN) : make_map(&m.bl, g.B_lo, g.N, g.K, g.ldb, 64)))
         return GK_ERR_UNSUPPORTED;
+    p.tma_epi = setup_tma_epilogue(g, p, m);
+    if (!p.tma_epi) {
+        m.c = m.aux = m.r = m.lo = ta;
+        p.in_kind = IN_NONE;
+        p.reduce_out = p.out_aux = p.out_lo = 0;
+    }
     if (g.c_dtype == GK_F32)
-        launch_split<float>(ctx, split, grid, ta, tb, ta_lo, tb_lo, p);
+        launch_split<float>(ctx, split, grid, m, p);
     else
-        launch_split<__nv_bfloat16>(ctx, split, grid, ta, tb, ta_lo, tb_lo, p);
+        launch_split<__nv_bfloat16>(ctx, split, grid, m, p);
     return launched(ctx, "gemm_tc");
 }
 

@@ -165,7 +165,8 @@ gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, cons
 /* Backward of Y = X W (transW = 0) or X W^T (transW = 1) for upstream dY [N, M]:
  *   dX  = dY W^T (transW = 0) or dY W (transW = 1); written (=), or added (+=) if
  *         accumulate_dX (float32 dX only). If preact_X is given (X was gelu(preact_X)),
- *         dX = (dY W^T) * gelu'(preact_X): the GELU backward fused in. dX may be NULL.
+ *         the product is (dY W^T) * gelu'(preact_X), the GELU backward fused in, and that
+ *         is what is written or added. dX may be NULL.
  *   dW += X^T dY ([K, M]) or dY^T X ([M, K]); float32; may be NULL.
  *   dbias += sum over rows of dY; float32 [M]; may be NULL.
  * [LM1] "Ops...", MatMul backward rule (dx = g w^T, dw = x^T g, both accumulating).

@@ -266,6 +266,51 @@ def test_matmul_bwd_fused_gelu(gkctx, dt):
     assert rel_l2(dx, rdx) < (2e-5 if dt == "f32" else 5e-3)
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_matmul_bwd_fused_gelu_accumulates_after_the_gelu_factor(gkctx, dt):
+    """accumulate_dX with preact_X: dX_old + (dY W^T) * gelu'(preact)."""
+    (dx, rdx), (dw, rdw), _ = _matmul_bwd_case(gkctx, 300, 384, 96, 0, dt, 1, True, 625)
+    assert rel_l2(dx, rdx) < (2e-5 if dt == "f32" else 5e-3)
+    assert rel_l2(dw, rdw) < 2e-5
+
+
+# bf16 results through the tensor-core epilogue: ragged rows and columns (partial 32-row
+# groups, partial chunks, idle column halves) next to full tiles
+BF16_OUT = [(4096, 768, 3072), (300, 96, 384), (131, 64, 45), (77, 128, 200), (1, 64, 8), (333, 96, 130),
+            (257, 64, 520)]
+
+
+@pytest.mark.parametrize("N,K,M", BF16_OUT)
+@pytest.mark.parametrize("mode", ["plain", "gelu", "dgelu"])
+def test_matmul_bf16_results(gkctx, N, K, M, mode):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    seed = 640 + N + M
+    x, w, b = bf16_round(normal(seed, N, K)), bf16_round(normal(seed + 1, K, M)), normal(seed + 2, M)
+    bf = torch.bfloat16
+    if mode == "dgelu":
+        # dX [N, K] = (dY [N, M] W^T) * gelu'(pre), all bf16
+        g, pre = bf16_round(normal(seed + 3, N, M)), bf16_round(normal(seed + 4, N, K))
+        dx = torch.full((N, K), float("nan"), dtype=bf, device="cuda")
+        gk.gk_matmul_bwd(gkctx, gk.GK_BF16, None, 0, dev(w, bf), M, 0, dev(g, bf), M, dx, K, gk.GK_BF16, 0,
+                         dev(pre, bf), K, None, 0, None, N, K, M)
+        gk.gk_sync(gkctx)
+        rdx, _ = ops.matmul_bwd(x, w, g)
+        assert rel_l2(dx.float().cpu().numpy(), ops.gelu_bwd(pre, rdx)) < 5e-3
+        return
+    y = torch.full((N, M), float("nan"), dtype=bf, device="cuda")
+    pre = torch.full((N, M), float("nan"), dtype=bf, device="cuda") if mode == "gelu" else None
+    gk.gk_matmul_fwd(gkctx, gk.GK_BF16, dev(x, bf), K, dev(w, bf), M, 0, dev(b), None, 0, y, M, gk.GK_BF16, N, K, M,
+                     gk.GK_ACT_GELU if mode == "gelu" else gk.GK_ACT_NONE, pre, M)
+    gk.gk_sync(gkctx)
+    ref = ops.matmul_fwd(x, w) + b
+    if mode == "gelu":
+        assert rel_l2(pre.float().cpu().numpy(), ref) < 5e-3
+        ref = ops.gelu_fwd(ref)
+    assert rel_l2(y.float().cpu().numpy(), ref) < 5e-3
+
+
 def test_matmul_rejects_bad_strides(gkctx):
     from gpt_decoder_gb300 import gk
 

@@ -3,16 +3,16 @@
 // CausalSoftmax, BatchMatMul); [LM4] = "... (4): running GPT-2 weights", "The 12 tensors we do
 // not use" (the causal mask by arithmetic) and "Generation with a KV cache" (1/sqrt(hs)).
 //
-// One CTA of 128 threads per (128-query tile, batch, head). Q is loaded once by TMA; K and V
-// tiles of 128 keys stream through a double buffer. For each key tile:
-//   S = Q K^T        one tcgen05 MMA chain (M=128, N=128, K=64) into TMEM columns 0..127;
-//   softmax          each thread owns one query row: it reads its S row from TMEM twice
-//                    (row max, then exp2 and row sum), applies the causal mask, and writes
-//                    P = exp(S - m) as bf16 into shared memory in the 128-byte-swizzled
-//                    K-major layout the MMA reads;
-//   O_tile = P V     a second MMA chain (M=128, N=64, K=128; V is the MN-major operand) into
-//                    TMEM columns 128..191, which the thread adds into its register
-//                    accumulator after rescaling by exp(m_old - m_new).
+// Forward: two 128-query tiles per CTA; K and V tiles of 128 keys stream through a double
+// buffer. For each key tile and query tile:
+//   S = Q K^T        tcgen05 MMA chain (M=128, N=128, K=64) into TMEM;
+//   softmax          each thread owns one query row: one read of its 128 S values from TMEM,
+//                    the causal mask on the diagonal tile only, P = 2^(S/sqrt(hs)*log2(e) - m)
+//                    as bf16 into shared memory in the 128-byte-swizzled K-major layout the MMA
+//                    reads; m moves only when the row maximum exceeds it by more than 8 (then O
+//                    is rescaled in TMEM), so P <= 2^8;
+//   O += P V         second MMA chain (M=128, N=64, K=128; V is the MN-major operand)
+//                    accumulating in TMEM across key tiles.
 // The result is O / l (bf16) and the row log-sum-exp (float32, natural log) for backward.
 // All mbarrier waits are bounded (timeout -> GK_ERR_TIMEOUT in the error word).
 #include <math.h>
@@ -24,7 +24,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int QT = 128, KT = 128, HS = 64, THREADS = 128;
+constexpr int QT = 128, KT = 128, HS = 64;
 constexpr uint32_t TILE = 128 * 64 * 2;                 // one 128 x 64 bf16 tile, 16 KB
 constexpr uint64_t WAIT_NS = 1000000000ull;
 
@@ -40,11 +40,14 @@ __device__ __forceinline__ uint32_t p_offset(int r, int c) {
 // query tile A, warps 4-7 tile B (the next one), warp 8 streams K/V tiles (shared by both) through
 // a 2-stage ring, warp 9 issues the MMAs. While one group turns its S tile into P, the tensor
 // core computes the other group's P V and its next S, so the softmax runs in the MMAs' shadow.
-// TMEM: S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383.
+// The MMA warp issues S_g(j+1) after P_g V_j, so S_g(j+1) landing also means O_g and P_g are
+// free again. TMEM: S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383.
+// Registers are granted to a block in groups of four warps, so 9- or 10-warp blocks are
+// budgeted as 12 warps: 168 registers per thread at most (hence __maxnreg__(168)).
 constexpr int FWD_THREADS = 320;
 constexpr size_t FWD_SMEM_BYTES = 10 * TILE + 1024 + 256;  // Q_A, Q_B, K[2], V[2], P_A, P_B
 
-__global__ void __maxnreg__(200)
+__global__ void __maxnreg__(168)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ y,
                        float* __restrict__ lse, int T, int H, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -149,8 +152,8 @@ __global__ void __maxnreg__(200)
 #pragma unroll
                     for (int k = 0; k < KT / 16; ++k)
                         umma_bf16(tmem + 256 + g * 64, smem_desc(p_a + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                                  smem_desc(v_a + k * 2048, 8192, 1024), id_o, k > 0);
-                    umma_commit(&bar_o[g]);
+                                  smem_desc(v_a + k * 2048, 8192, 1024), id_o, (j > 0 || k > 0) ? 1u : 0u);
+                    if (j == ng - 1) umma_commit(&bar_o[g]);
                     // the last reader of K/V stage j frees it for the tile j + 2
                     if (g == 1 || j >= nB) umma_commit(&kv_empty[j & 1]);
                     // S_g(j + 1), once K_{j+1} has landed
@@ -178,99 +181,132 @@ __global__ void __maxnreg__(200)
             }
         }
     } else {
+        // softmax warps: thread r of group g owns query row q0 + r
         const int g = warp >> 2;          // group: 0 = tile A, 1 = tile B
         const int r = (warp & 3) * 32 + lane;
         const int q0 = (qa + g) * QT;
         const int qq = q0 + r;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t o_addr = lane_addr + 256 + g * 64;
         const float sl2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
         uint8_t* myP = sP + g * 2 * TILE;
-        float o[HS];
-#pragma unroll
-        for (int d = 0; d < HS; ++d) o[d] = 0.f;
-        float m = -INFINITY, l = 0.f;
+        // m_ref: the reference the row's P and running sum l are taken against, in log2
+        // units; it moves (and O in TMEM is rescaled) only when the row maximum exceeds it by
+        // more than 8, so P <= 2^8 and most key tiles skip the rescale.
+        float m_ref = -INFINITY, l = 0.f;
         const int my_kt = g ? (has_b ? qa + 2 : 0) : qa + 1;
         for (int j = 0; j < my_kt; ++j) {
-            if (!mbar_wait(&bar_s[g], j & 1, nullptr, WAIT_NS)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[g], j & 1, nullptr, WAIT_NS))) {
                 failed = true;
                 break;
             }
             tc_fence_after();
-            const int k0 = j * KT;
-            float tmax = -INFINITY;
-#pragma unroll 1
-            for (int c0 = 0; c0 < KT; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + g * 128 + c0, v);
+            // S row (128 keys) in one go; S_g(j) complete also means P_g V_{j-1} is complete
+            uint32_t sv[4][32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    int kk = k0 + c0 + i;
-                    float t = __uint_as_float(v[i]) * sl2;
-                    if (kk <= qq && kk < T) tmax = fmaxf(tmax, t);
-                }
+            for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_addr + g * 128 + c * 32, sv[c]);
+            tmem_wait_ld_only();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) reg_fence32(sv[c]);
+            // keys k0 + i, i < lim, are visible to this row (causal; the diagonal tile only)
+            const int k0 = j * KT;
+            const bool diag = j == qa + g;
+            const int lim = diag ? min(qq, T - 1) - k0 + 1 : KT;
+            if (diag) {  // hidden keys -> -inf, so their P is exactly 0 below
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c * 32 + i >= lim) sv[c][i] = 0xff800000u;
             }
-            const float m_new = fmaxf(m, tmax);
-            const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m - m_new);
-            float psum = 0.f;
-#pragma unroll 1
-            for (int c0 = 0; c0 < KT; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + g * 128 + c0, v);
+            float mx[8];  // eight independent partial maxima instead of one 128-long chain
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[0][e]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[c][i]));
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float m_new = fmaxf(m_ref, mt * sl2);
+            // move the reference (O is rescaled after P is written, when the S row is dead)
+            float corr = 1.f;
+            const bool rescale = m_new > m_ref + 8.f;
+            if (rescale) {
+                corr = ex2_hw(m_ref - m_new);  // 0 while the row was empty
+                l *= corr;
+                m_ref = m_new;
+            }
+            // P = 2^(S * sl2 - m_ref), bf16, into the K-major swizzled tile the MMA reads
+            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
-                    float pv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        int kk = k0 + c0 + i + e;
-                        float t = __uint_as_float(v[i + e]) * sl2;
-                        pv[e] = (kk <= qq && kk < T && m_new != -INFINITY) ? exp2f(t - m_new) : 0.f;
-                        psum += pv[e];
-                    }
-                    uint4 pk;
-                    uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+                    uint32_t pw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        __nv_bfloat162 t2 = __floats2bfloat162_rn(pv[2 * e], pv[2 * e + 1]);
+                        float p0 = ex2_hw(fmaf(__uint_as_float(sv[c][i + 2 * e]), sl2, -m_ref));
+                        float p1 = ex2_hw(fmaf(__uint_as_float(sv[c][i + 2 * e + 1]), sl2, -m_ref));
+                        ps[2 * e] += p0;
+                        ps[2 * e + 1] += p1;
+                        __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
                         pw[e] = *reinterpret_cast<uint32_t*>(&t2);
                     }
-                    *reinterpret_cast<uint4*>(myP + p_offset(r, c0 + i)) = pk;
+                    *reinterpret_cast<uint4*>(myP + p_offset(r, c * 32 + i)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
             }
-            l = l * corr + psum;
-            m = m_new;
+            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            // tcgen05.ld / st are warp-collective: the warp rescales if any of its rows must
+            // (corr = 1 for the others)
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {  // O row, two 32-column halves
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32_nowait(o_addr + c * 32, ov);
+                    tmem_wait_ld_only();
+                    reg_fence32(ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+                    tmem_st32(o_addr + c * 32, ov);
+                }
+                tmem_wait_st();
+            }
             fence_proxy_async_smem();  // P's generic-proxy stores -> visible to the tensor core
             tc_fence_before();
             mbar_arrive(&bar_p[g]);
-            if (!mbar_wait(&bar_o[g], j & 1, nullptr, WAIT_NS)) {
+        }
+        if (!failed && my_kt > 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[g], 0, nullptr, WAIT_NS))) {
                 failed = true;
-                break;
-            }
-            tc_fence_after();
+            } else {
+                tc_fence_after();
+                uint32_t ov[2][32];
+                tmem_ld32_nowait(o_addr, ov[0]);
+                tmem_ld32_nowait(o_addr + 32, ov[1]);
+                tmem_wait_ld_only();
+                reg_fence32(ov[0]);
+                reg_fence32(ov[1]);
+                if (qq < T) {
+                    const float inv = 1.f / l;
+                    __nv_bfloat16* yr = y + (int64_t)(row0 + qq) * C + h * HS;
 #pragma unroll
-            for (int c0 = 0; c0 < HS; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + 256 + g * 64 + c0, v);
+                    for (int d = 0; d < HS; d += 8) {
+                        uint32_t pw[4];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[c0 + i] = o[c0 + i] * corr + __uint_as_float(v[i]);
-            }
-            tc_fence_before();
-        }
-        if (!failed && my_kt > 0 && qq < T) {
-            const float inv = 1.f / l;
-            __nv_bfloat16* yr = y + (int64_t)(row0 + qq) * C + h * HS;
-#pragma unroll
-            for (int d = 0; d < HS; d += 8) {
-                uint4 pk;
-                uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 t2 = __floats2bfloat162_rn(o[d + 2 * e] * inv, o[d + 2 * e + 1] * inv);
-                    pw[e] = *reinterpret_cast<uint32_t*>(&t2);
+                        for (int e = 0; e < 4; ++e) {
+                            const int dd = d + 2 * e;
+                            __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(ov[dd >> 5][dd & 31]) * inv,
+                                                                      __uint_as_float(ov[(dd + 1) >> 5][(dd + 1) & 31]) * inv);
+                            pw[e] = *reinterpret_cast<uint32_t*>(&t2);
+                        }
+                        *reinterpret_cast<uint4*>(yr + d) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    }
+                    lse[(int64_t)bh * T + qq] = (m_ref + log2f(l)) * 0.6931471805599453f;
                 }
-                *reinterpret_cast<uint4*>(yr + d) = pk;
             }
-            lse[(int64_t)bh * T + qq] = (m + log2f(l)) * 0.6931471805599453f;
         }
+        tc_fence_before();
     }
     if (failed) report(err, GK_ERR_TIMEOUT);
     tc_fence_before();
@@ -282,38 +318,46 @@ __global__ void __maxnreg__(200)
 }
 
 // ------------------------------------------------------------------------ backward
-// One CTA of 128 threads per (128-key tile, batch, head), looping over the query tiles at or
-// after its keys. Thread r owns key row r for S^T, dP^T, dV and dK, and query row r for the
-// per-tile dQ. Per query tile:
+// One CTA per (128-key tile, batch, head), looping over the query tiles at or after its keys.
+// Warps 0-7 compute: warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
+// query columns 64 (w / 4) .. + 63 of each tile. Warp 8 issues the TMA copies and the MMAs.
+// Per query tile:
 //   S^T = K Q^T, dP^T = V dO^T      (M=128 keys, N=128 queries, K=64)        -> TMEM 0..255
-//   P^T = exp(S^T / sqrt(hs) - lse), dS^T = P^T (dP^T - D)  as bf16 into shared memory
+//   P^T = 2^(S^T / sqrt(hs) log2(e) - lse log2(e)), dS^T = P^T (dP^T - D)
+//                                    as bf16 into shared memory (K-major, 128-byte swizzle)
 //   dV += P^T dO, dK += dS^T Q       (M=128 keys, N=64, K=128 queries)       -> TMEM 256..383
 //   dQ_tile = dS K                   (M=128 queries, N=64, K=128 keys)       -> TMEM 384..447
-// dQ_tile is added (float atomics) into a float32 accumulator; dK and dV are stored once.
-constexpr size_t BWD_SMEM_BYTES = 10 * TILE + 2048 + 1024 + 128;  // K, V, Q[2], dO[2], P^T, dS^T, lse/D
+// dQ_tile goes through a swizzled shared-memory tile into a float32 accumulator by TMA
+// reduce-add; dK and dV are stored once at the end. The MMA warp issues the next tile's S^T
+// and dP^T right behind dQ, so they run while the compute warps drain dQ.
+constexpr int BWD_THREADS = 288;
+constexpr size_t BWD_SMEM_BYTES = 12 * TILE + 2048 + 1024 + 256;  // K, V, Q[2], dO[2], P^T, dS^T, dQ, lse/D[2]
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __maxnreg__(168)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_dy,
-                       const float* __restrict__ lse, const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv,
-                       float* __restrict__ dq_acc, int T, int H, int* err) {
+                       const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+                       const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv, int T, int H, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sK = smem;
     uint8_t* sV = smem + TILE;
     uint8_t* sQ = smem + 2 * TILE;    // two stages
     uint8_t* sO = smem + 4 * TILE;    // dO, two stages
-    uint8_t* sPT = smem + 6 * TILE;   // two halves
+    uint8_t* sPT = smem + 6 * TILE;   // two halves (query columns 0..63, 64..127)
     uint8_t* sDS = smem + 8 * TILE;   // two halves
-    float* sL = reinterpret_cast<float*>(smem + 10 * TILE);
-    float* sD = sL + 128;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 10 * TILE + 2048);
+    uint8_t* sDQ = smem + 10 * TILE;  // two 128-row x 32-column float32 boxes, 128-byte swizzle
+    float* sLD = reinterpret_cast<float*>(smem + 12 * TILE);  // [2][lse 128 | D 128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 12 * TILE + 2048);
     uint64_t* bar_kv = bars;
     uint64_t* bar_qo = bars + 1;      // [2]
-    uint64_t* bar_1 = bars + 3;
-    uint64_t* bar_2 = bars + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 5);
+    uint64_t* bar_s = bars + 3;       // S^T, dP^T of the current tile in TMEM
+    uint64_t* bar_p = bars + 4;       // P^T, dS^T written (256 arrivals)
+    uint64_t* bar_mm = bars + 5;      // dV, dK, dQ of the current tile done
+    uint64_t* bar_drain = bars + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = H * HS;
     const int kt = blockIdx.x;  // heaviest (earliest keys) first
     const int k0 = kt * KT;
@@ -321,148 +365,91 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int row0 = b * T;
     const int n_qt = (T + QT - 1) / QT;
     const int first_qt = k0 / QT;
+    const int n_it = n_qt - first_qt;
 
     if (tid == 0) {
         mbar_init(bar_kv, 1);
         mbar_init(&bar_qo[0], 1);
         mbar_init(&bar_qo[1], 1);
-        mbar_init(bar_1, 1);
-        mbar_init(bar_2, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, 256);
+        mbar_init(bar_mm, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) tmem_alloc(tmem_slot, 512);
+    if (warp == 8) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    int pending_qo[2] = {0, 0}, pending_kv = 0;
-    if (tid == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_dy) : "memory");
-        mbar_expect_tx(bar_kv, 2 * TILE);
-        tma_load_2d(&tm_qkv, bar_kv, sK, C + h * HS, row0 + k0);
-        tma_load_2d(&tm_qkv, bar_kv, sV, 2 * C + h * HS, row0 + k0);
-        pending_kv = 1;
-        if (first_qt < n_qt) {
-            mbar_expect_tx(&bar_qo[0], 2 * TILE);
-            tma_load_2d(&tm_qkv, &bar_qo[0], sQ, h * HS, row0 + first_qt * QT);
-            tma_load_2d(&tm_dy, &bar_qo[0], sO, h * HS, row0 + first_qt * QT);
-            pending_qo[0] = 1;
-        }
-    }
-    const uint32_t id_s = instr_desc_bf16(false, false, 128, 128);  // S^T, dP^T
-    const uint32_t id_kv = instr_desc_bf16(false, true, 128, 64);   // dV, dK: B (dO, Q) MN-major
-    const uint32_t id_q = instr_desc_bf16(true, true, 128, 64);     // dQ: A (dS) and B (K) MN-major
-    const float sl2 = 0.125f * 1.4426950408889634f;
-    const float L2E = 1.4426950408889634f;
-    const int r = warp * 32 + (tid & 31);
-    const int kk = k0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    bool aborted = false;
 
-    // prologue: S^T and dP^T of the first query tile
-    bool fail0 = false;
-    if (tid == 0) {
-        bool w = mbar_wait(bar_kv, 0, nullptr, WAIT_NS) && mbar_wait(&bar_qo[0], 0, nullptr, WAIT_NS);
-        if (w) {
-            pending_kv = 0;
-            pending_qo[0] = 0;
-            tc_fence_after();
-            uint32_t k_a = saddr(sK), v_a = saddr(sV), q_a = saddr(sQ), o_a = saddr(sO);
-#pragma unroll
-            for (int k = 0; k < HS / 16; ++k)
-                umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(q_a + k * 32, 16, 1024), id_s, k > 0);
-#pragma unroll
-            for (int k = 0; k < HS / 16; ++k)
-                umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(o_a + k * 32, 16, 1024), id_s,
-                          k > 0);
-            umma_commit(bar_1);
-            if (first_qt + 1 < n_qt) {
-                mbar_expect_tx(&bar_qo[1], 2 * TILE);
-                tma_load_2d(&tm_qkv, &bar_qo[1], sQ + TILE, h * HS, row0 + (first_qt + 1) * QT);
-                tma_load_2d(&tm_dy, &bar_qo[1], sO + TILE, h * HS, row0 + (first_qt + 1) * QT);
-                pending_qo[1] = 1;
+    if (warp == 8) {
+        if (lane == 0 && n_it > 0) {
+            const uint32_t id_s = instr_desc_bf16(false, false, 128, 128);  // S^T, dP^T
+            const uint32_t id_kv = instr_desc_bf16(false, true, 128, 64);   // dV, dK: B (dO, Q) MN-major
+            const uint32_t id_q = instr_desc_bf16(true, true, 128, 64);     // dQ: A (dS) and B (K) MN-major
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_dy) : "memory");
+            mbar_expect_tx(bar_kv, 2 * TILE);
+            tma_load_2d(&tm_qkv, bar_kv, sK, C + h * HS, row0 + k0);
+            tma_load_2d(&tm_qkv, bar_kv, sV, 2 * C + h * HS, row0 + k0);
+            int pend[2] = {-1, -1};  // phase of the Q/dO load in flight per stage
+            for (int i = 0; i < 2 && i < n_it; ++i) {
+                mbar_expect_tx(&bar_qo[i], 2 * TILE);
+                tma_load_2d(&tm_qkv, &bar_qo[i], sQ + i * TILE, h * HS, row0 + (first_qt + i) * QT);
+                tma_load_2d(&tm_dy, &bar_qo[i], sO + i * TILE, h * HS, row0 + (first_qt + i) * QT);
+                pend[i] = 0;
             }
-        }
-        fail0 = !w;
-    }
-    if (__syncthreads_or(fail0)) aborted = true;
-
-    for (int qt = first_qt; !aborted && qt < n_qt; ++qt) {
-        const int it = qt - first_qt;
-        const int st = it & 1;
-        const uint32_t ph = it & 1;
-        const int q0 = qt * QT;
-        {
-            int q = q0 + r;
-            sL[r] = q < T ? lse[(int64_t)bh * T + q] * L2E : 0.f;
-            sD[r] = q < T ? dvec[(int64_t)bh * T + q] : 0.f;
-        }
-        // (the barrier below also orders these shared-memory writes before their use)
-        if (__syncthreads_or(!mbar_wait(bar_1, ph, nullptr, WAIT_NS))) {
-            aborted = true;
-            break;
-        }
-        tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < QT; c0 += 32) {
-            uint32_t sv[32], dv[32];
-            tmem_ld32(lane_addr + c0, sv);
-            tmem_ld32(lane_addr + 128 + c0, dv);
+            const uint32_t k_a = saddr(sK), v_a = saddr(sV);
+            bool ok = mbar_wait(bar_kv, 0, abort_flag, WAIT_NS) && mbar_wait(&bar_qo[0], 0, abort_flag, WAIT_NS);
+            bool kv_pending = !ok;
+            bool issued = false;
+            if (ok) {
+                pend[0] = -1;
+                tc_fence_after();
+                const uint32_t q_a = saddr(sQ), o_a = saddr(sO);
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                float pv[8], dsv[8];
+                for (int k = 0; k < HS / 16; ++k)
+                    umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(q_a + k * 32, 16, 1024), id_s, k > 0);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    int c = c0 + i + e, q = q0 + c;
-                    bool vis = q >= kk && q < T && kk < T;
-                    float pp = vis ? exp2f(__uint_as_float(sv[i + e]) * sl2 - sL[c]) : 0.f;
-                    pv[e] = pp;
-                    dsv[e] = pp * (__uint_as_float(dv[i + e]) - sD[c]);
+                for (int k = 0; k < HS / 16; ++k)
+                    umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(o_a + k * 32, 16, 1024), id_s,
+                              k > 0);
+                umma_commit(bar_s);
+                issued = true;
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int st = it & 1;
+                if (!mbar_wait(bar_p, it & 1, abort_flag, WAIT_NS)) {
+                    ok = false;
+                    break;
                 }
-                uint4 pk, dk;
-                uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-                uint32_t* dw = reinterpret_cast<uint32_t*>(&dk);
+                tc_fence_after();
+                const uint32_t pt_a = saddr(sPT), ds_a = saddr(sDS);
+                const uint32_t q_a = saddr(sQ + st * TILE), o_a = saddr(sO + st * TILE);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 t2 = __floats2bfloat162_rn(pv[2 * e], pv[2 * e + 1]);
-                    __nv_bfloat162 u2 = __floats2bfloat162_rn(dsv[2 * e], dsv[2 * e + 1]);
-                    pw[e] = *reinterpret_cast<uint32_t*>(&t2);
-                    dw[e] = *reinterpret_cast<uint32_t*>(&u2);
+                for (int k = 0; k < QT / 16; ++k) {
+                    const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
+                    umma_bf16(tmem + 256, smem_desc(pt_a + koff, 16, 1024), smem_desc(o_a + k * 2048, 8192, 1024),
+                              id_kv, (it > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16(tmem + 320, smem_desc(ds_a + koff, 16, 1024), smem_desc(q_a + k * 2048, 8192, 1024),
+                              id_kv, (it > 0 || k > 0) ? 1u : 0u);
                 }
-                *reinterpret_cast<uint4*>(sPT + p_offset(r, c0 + i)) = pk;
-                *reinterpret_cast<uint4*>(sDS + p_offset(r, c0 + i)) = dk;
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        bool fail = false;
-        if (tid == 0) {
-            tc_fence_after();
-            uint32_t pt_a = saddr(sPT), ds_a = saddr(sDS), k_a = saddr(sK), v_a = saddr(sV);
-            uint32_t q_a = saddr(sQ + st * TILE), o_a = saddr(sO + st * TILE);
 #pragma unroll
-            for (int k = 0; k < QT / 16; ++k) {
-                uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
-                umma_bf16(tmem + 256, smem_desc(pt_a + koff, 16, 1024), smem_desc(o_a + k * 2048, 8192, 1024), id_kv,
-                          (it > 0 || k > 0));
-                umma_bf16(tmem + 320, smem_desc(ds_a + koff, 16, 1024), smem_desc(q_a + k * 2048, 8192, 1024), id_kv,
-                          (it > 0 || k > 0));
-            }
-#pragma unroll
-            for (int k = 0; k < KT / 16; ++k)
-                umma_bf16(tmem + 384, smem_desc(ds_a + k * 2048, 16384, 1024), smem_desc(k_a + k * 2048, 8192, 1024),
-                          id_q, k > 0);
-            umma_commit(bar_2);
-            // S^T and dP^T of the next query tile right behind: they overlap the dQ accumulation
-            if (qt + 1 < n_qt) {
-                int ns = st ^ 1;
-                bool w = mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, nullptr, WAIT_NS);
-                if (w) {
-                    pending_qo[ns] = 0;
+                for (int k = 0; k < KT / 16; ++k)
+                    umma_bf16(tmem + 384, smem_desc(ds_a + k * 2048, 16384, 1024),
+                              smem_desc(k_a + k * 2048, 8192, 1024), id_q, k > 0);
+                umma_commit(bar_mm);
+                if (it + 1 < n_it) {
+                    const int ns = st ^ 1;
+                    if (!mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, abort_flag, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    pend[ns] = -1;
                     tc_fence_after();
-                    uint32_t nq_a = saddr(sQ + ns * TILE), no_a = saddr(sO + ns * TILE);
+                    const uint32_t nq_a = saddr(sQ + ns * TILE), no_a = saddr(sO + ns * TILE);
 #pragma unroll
                     for (int k = 0; k < HS / 16; ++k)
                         umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(nq_a + k * 32, 16, 1024), id_s,
@@ -471,90 +458,192 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int k = 0; k < HS / 16; ++k)
                         umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(no_a + k * 32, 16, 1024),
                                   id_s, k > 0);
-                    umma_commit(bar_1);
+                    umma_commit(bar_s);
                 }
-                fail = !w;
+                if (it + 2 < n_it) {
+                    // stage st (this tile's Q, dO) is free once dV, dK and dQ are done
+                    if (!mbar_wait(bar_mm, it & 1, abort_flag, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&bar_qo[st], 2 * TILE);
+                    tma_load_2d(&tm_qkv, &bar_qo[st], sQ + st * TILE, h * HS, row0 + (first_qt + it + 2) * QT);
+                    tma_load_2d(&tm_dy, &bar_qo[st], sO + st * TILE, h * HS, row0 + (first_qt + it + 2) * QT);
+                    pend[st] = ((it + 2) >> 1) & 1;
+                }
             }
-        }
-        if (__syncthreads_or(fail || !mbar_wait(bar_2, ph, nullptr, WAIT_NS))) {
-            aborted = true;
-            break;
-        }
-        tc_fence_after();
-        // stage st (Q, dO of this tile) is free now: prefetch the tile after next into it
-        if (tid == 0 && qt + 2 < n_qt) {
-            mbar_expect_tx(&bar_qo[st], 2 * TILE);
-            tma_load_2d(&tm_qkv, &bar_qo[st], sQ + st * TILE, h * HS, row0 + (qt + 2) * QT);
-            tma_load_2d(&tm_dy, &bar_qo[st], sO + st * TILE, h * HS, row0 + (qt + 2) * QT);
-            pending_qo[st] = 1;
-        }
-        {
-            int q = q0 + r;
-#pragma unroll
-            for (int c0 = 0; c0 < HS; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + 384 + c0, v);
-                if (q < T) {
-                    float* dst = dq_acc + (int64_t)(row0 + q) * C + h * HS + c0;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        atomicAdd(reinterpret_cast<float4*>(dst + i),
-                                  make_float4(__uint_as_float(v[i]) * 0.125f, __uint_as_float(v[i + 1]) * 0.125f,
-                                              __uint_as_float(v[i + 2]) * 0.125f, __uint_as_float(v[i + 3]) * 0.125f));
+            if (!ok) {
+                *abort_flag = 1;
+                report(err, GK_ERR_TIMEOUT);
+                // let this CTA's copies and MMAs in flight finish before shared memory and
+                // TMEM are released
+                if (kv_pending) mbar_wait(bar_kv, 0, nullptr, WAIT_NS / 5);
+                for (int i = 0; i < 2; ++i)
+                    if (pend[i] >= 0) mbar_wait(&bar_qo[i], (uint32_t)pend[i], nullptr, WAIT_NS / 5);
+                if (issued) {
+                    umma_commit(bar_drain);
+                    mbar_wait(bar_drain, 0, nullptr, WAIT_NS / 5);
                 }
             }
         }
-        tc_fence_before();
-    }
-    if (aborted) {
-        if (tid == 0) {
+    } else {
+        const int qd = warp & 3, hf = warp >> 2;
+        const int r = qd * 32 + lane;  // key row of S^T / dP^T / dV / dK; query row of dQ
+        const int kk = k0 + r;
+        const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+        const float sl2 = 0.125f * 1.4426950408889634f;
+        const float L2E = 1.4426950408889634f;
+        bool fail = false;
+        // lse (in log2 units) or D for tile 0, one value per thread
+        float ld_next = 0.f;
+        if (n_it > 0) {
+            const int q = first_qt * QT + (tid & 127);
+            ld_next = q < T ? (tid < 128 ? lse[(int64_t)bh * T + q] * L2E : dvec[(int64_t)bh * T + q]) : 0.f;
+        }
+        for (int it = 0; it < n_it; ++it) {
+            const int q0 = (first_qt + it) * QT;
+            float* sL = sLD + (it & 1) * 256;
+            sL[tid] = ld_next;
+            if (it + 1 < n_it) {
+                const int q = q0 + QT + (tid & 127);
+                ld_next = q < T ? (tid < 128 ? lse[(int64_t)bh * T + q] * L2E : dvec[(int64_t)bh * T + q]) : 0.f;
+            }
+            // the dQ staging tile is free once the previous reduce has read it
+            if (tid == 0) bulk_wait_read<0>();
+            if (named_bar_or(1, 256, fail)) {
+                fail = true;
+                break;
+            }
+            fail = !__all_sync(0xffffffffu, mbar_wait(bar_s, it & 1, abort_flag, WAIT_NS));
+            if (!fail) {
+                tc_fence_after();
+                // visible query columns c (of this warp's 64): lo <= c < hi
+                const int cbase = hf * 64;
+                int lo = 0, hi = 64;
+                if (q0 == k0) lo = r - cbase;                 // causal: query >= key on the diagonal
+                hi = min(hi, T - q0 - cbase);                 // ragged last query tile
+                if (kk >= T) hi = 0;                          // padding key rows
+                const bool masked = lo > 0 || hi < 64;
+                const float* L = sL + cbase;
+                const float* D = sL + 128 + cbase;
+                // two blocks of 32 columns (S^T and dP^T rows: 64 registers per block)
+#pragma unroll 1
+                for (int cb = 0; cb < 64; cb += 32) {
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32_nowait(lane_addr + cbase + cb, sv);
+                    tmem_ld32_nowait(lane_addr + 128 + cbase + cb, dv);
+                    tmem_wait_ld_only();
+                    reg_fence32(sv);
+                    reg_fence32(dv);
+#pragma unroll
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        const float4 l0 = *reinterpret_cast<const float4*>(L + cb + c8);
+                        const float4 l1 = *reinterpret_cast<const float4*>(L + cb + c8 + 4);
+                        const float4 d0 = *reinterpret_cast<const float4*>(D + cb + c8);
+                        const float4 d1 = *reinterpret_cast<const float4*>(D + cb + c8 + 4);
+                        const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+                        const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                        uint32_t pw[4], qw[4];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const int c = cb + c8 + e;
+                            float p0 = ex2_hw(fmaf(__uint_as_float(sv[c8 + e]), sl2, -lv[e]));
+                            float p1 = ex2_hw(fmaf(__uint_as_float(sv[c8 + e + 1]), sl2, -lv[e + 1]));
+                            float ds0 = p0 * (__uint_as_float(dv[c8 + e]) - dd[e]);
+                            float ds1 = p1 * (__uint_as_float(dv[c8 + e + 1]) - dd[e + 1]);
+                            if (masked) {  // hidden pairs contribute exactly zero
+                                const bool v0 = c >= lo && c < hi, v1 = c + 1 >= lo && c + 1 < hi;
+                                p0 = v0 ? p0 : 0.f;
+                                ds0 = v0 ? ds0 : 0.f;
+                                p1 = v1 ? p1 : 0.f;
+                                ds1 = v1 ? ds1 : 0.f;
+                            }
+                            __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                            __nv_bfloat162 u2 = __floats2bfloat162_rn(ds0, ds1);
+                            pw[e >> 1] = *reinterpret_cast<uint32_t*>(&t2);
+                            qw[e >> 1] = *reinterpret_cast<uint32_t*>(&u2);
+                        }
+                        *reinterpret_cast<uint4*>(sPT + p_offset(r, cbase + cb + c8)) =
+                            make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        *reinterpret_cast<uint4*>(sDS + p_offset(r, cbase + cb + c8)) =
+                            make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    }
+                }
+                fence_proxy_async_smem();  // P^T, dS^T generic stores -> visible to the tensor core
+                tc_fence_before();
+                mbar_arrive(bar_p);
+                // dQ tile: lane r holds query row q0 + r; this warp takes 32 of its 64 columns
+                fail = !__all_sync(0xffffffffu, mbar_wait(bar_mm, it & 1, abort_flag, WAIT_NS));
+                if (!fail) {
+                    tc_fence_after();
+                    uint32_t qv[32];
+                    tmem_ld32_nowait(lane_addr + 384 + hf * 32, qv);
+                    tmem_wait_ld_only();
+                    reg_fence32(qv);
+                    uint8_t* box = sDQ + hf * TILE;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4*>(box + r * 128 + ((j ^ (r & 7)) << 4)) =
+                            make_float4(__uint_as_float(qv[4 * j]) * 0.125f, __uint_as_float(qv[4 * j + 1]) * 0.125f,
+                                        __uint_as_float(qv[4 * j + 2]) * 0.125f,
+                                        __uint_as_float(qv[4 * j + 3]) * 0.125f);
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+            }
+            if (named_bar_or(1, 256, fail)) {
+                fail = true;
+                break;
+            }
+            if (tid == 0) {
+                // rows past this sequence carry dS = 0 (masked), so the whole box is added
+                tma_reduce_add_2d(&tm_dq, sDQ, h * HS, row0 + q0);
+                tma_reduce_add_2d(&tm_dq, sDQ + TILE, h * HS + 32, row0 + q0);
+                bulk_commit();
+            }
+        }
+        if (tid == 0) bulk_wait_all();
+        if (fail) {
+            *abort_flag = 1;
             report(err, GK_ERR_TIMEOUT);
-            if (pending_kv) mbar_wait(bar_kv, 0, nullptr, WAIT_NS / 5);
-            for (int s2 = 0; s2 < 2; ++s2)
-                if (pending_qo[s2]) mbar_wait(&bar_qo[s2], 0, nullptr, WAIT_NS / 5), mbar_wait(&bar_qo[s2], 1, nullptr, WAIT_NS / 5);
-            umma_commit(bar_1);
-            mbar_wait(bar_1, 0, nullptr, WAIT_NS / 5);
-            mbar_wait(bar_1, 1, nullptr, WAIT_NS / 5);
-        }
-    } else if (first_qt < n_qt) {
-        uint32_t v[32];
-        __nv_bfloat16* base = dqkv + (int64_t)(row0 + kk) * 3 * C + h * HS;
-#pragma unroll
-        for (int c0 = 0; c0 < HS; c0 += 32) {
-            tmem_ld32(lane_addr + 256 + c0, v);   // dV
+        } else if (n_it > 0) {
+            // dV and dK (the last bar_mm phase covered every MMA): lane r = key row kk
+            tc_fence_after();
+            uint32_t v[32];
+            __nv_bfloat16* base = dqkv + (int64_t)(row0 + kk) * 3 * C + h * HS + hf * 32;
+            tmem_ld32(lane_addr + 256 + hf * 32, v);  // dV
             if (kk < T) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
-                    uint4 pk;
-                    uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+                    uint32_t pw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(v[i + 2 * e]), __uint_as_float(v[i + 2 * e + 1]));
+                        __nv_bfloat162 t2 =
+                            __floats2bfloat162_rn(__uint_as_float(v[i + 2 * e]), __uint_as_float(v[i + 2 * e + 1]));
                         pw[e] = *reinterpret_cast<uint32_t*>(&t2);
                     }
-                    *reinterpret_cast<uint4*>(base + 2 * C + c0 + i) = pk;
+                    *reinterpret_cast<uint4*>(base + 2 * C + i) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
             }
-            tmem_ld32(lane_addr + 320 + c0, v);   // dK (times 1/sqrt(hs))
+            tmem_ld32(lane_addr + 320 + hf * 32, v);  // dK (times 1/sqrt(hs))
             if (kk < T) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
-                    uint4 pk;
-                    uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+                    uint32_t pw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(v[i + 2 * e]) * 0.125f,
                                                                   __uint_as_float(v[i + 2 * e + 1]) * 0.125f);
                         pw[e] = *reinterpret_cast<uint32_t*>(&t2);
                     }
-                    *reinterpret_cast<uint4*>(base + C + c0 + i) = pk;
+                    *reinterpret_cast<uint4*>(base + C + i) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
             }
         }
+        tc_fence_before();
     }
-    tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -629,8 +718,9 @@ gk_status attn_bwd_tc(gk_ctx* ctx, const void* qkv, const void* y, const float* 
     GK_REQUIRE(ctx, ws, GK_ERR_WORKSPACE, "gk_attn_bwd: needs %zu workspace bytes", need);
     float* dvec = (float*)ws;
     float* dq_acc = (float*)(ws + dvec_bytes);
-    CUtensorMap map_qkv, map_dy;
-    if (!make_map(&map_qkv, qkv, 3 * C, rows, 3 * C, 128) || !make_map(&map_dy, dy, C, rows, C, 128))
+    CUtensorMap map_qkv, map_dy, map_dq;
+    if (!make_map(&map_qkv, qkv, 3 * C, rows, 3 * C, 128) || !make_map(&map_dy, dy, C, rows, C, 128) ||
+        !make_map_f32(&map_dq, dq_acc, C, rows, C, 32, 128))
         return GK_ERR_UNSUPPORTED;
     attn_dvec_zero_kernel<<<(unsigned)cdiv(rows * H * 32, 256), 256, 0, ctx->stream>>>(
         (const __nv_bfloat16*)y, (const __nv_bfloat16*)dy, dvec, dq_acc, rows, T, H);
@@ -641,8 +731,8 @@ gk_status attn_bwd_tc(gk_ctx* ctx, const void* qkv, const void* y, const float* 
         attr = true;
     }
     dim3 grid((unsigned)cdiv(T, KT), (unsigned)(B * H));
-    attn_bwd_tc_kernel<<<grid, THREADS, BWD_SMEM_BYTES, ctx->stream>>>(map_qkv, map_dy, lse, dvec,
-                                                                    (__nv_bfloat16*)dqkv, dq_acc, T, H, ctx->d_err);
+    attn_bwd_tc_kernel<<<grid, BWD_THREADS, BWD_SMEM_BYTES, ctx->stream>>>(map_qkv, map_dy, map_dq, lse, dvec,
+                                                                        (__nv_bfloat16*)dqkv, T, H, ctx->d_err);
     GK_TRY(launched(ctx, "attn_bwd_tc"));
     attn_dq_store_kernel<<<(unsigned)cdiv(rows * C / 4, 256), 256, 0, ctx->stream>>>(dq_acc, (__nv_bfloat16*)dqkv,
                                                                                     rows, (int)C);

@@ -318,18 +318,20 @@ __global__ void __maxnreg__(168)
 }
 
 // ------------------------------------------------------------------------ backward
-// One CTA per (128-key tile, batch, head), looping over the query tiles at or after its keys.
-// Warps 0-7 compute: warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
-// query columns 64 (w / 4) .. + 63 of each tile. Warp 8 issues the TMA copies and the MMAs.
-// Per query tile:
-//   S^T = K Q^T, dP^T = V dO^T      (M=128 keys, N=128 queries, K=64)        -> TMEM 0..255
+// One CTA per (128-key tile, batch, head), looping over the query tiles at or after its keys,
+// each cut into two 64-query sub-tiles u (tile u / 2, half u % 2). Warps 0-7 compute: warp w
+// owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and 32 query columns (w / 4) of
+// each sub-tile. Warp 8 issues the TMA copies and the MMAs. Per sub-tile u:
+//   S^T = K Q_u^T, dP^T = V dO_u^T   (M=128 keys, N=64 queries, K=64)   -> TMEM buffer u % 2
 //   P^T = 2^(S^T / sqrt(hs) log2(e) - lse log2(e)), dS^T = P^T (dP^T - D)
-//                                    as bf16 into shared memory (K-major, 128-byte swizzle)
-//   dV += P^T dO, dK += dS^T Q       (M=128 keys, N=64, K=128 queries)       -> TMEM 256..383
-//   dQ_tile = dS K                   (M=128 queries, N=64, K=128 keys)       -> TMEM 384..447
-// dQ_tile goes through a swizzled shared-memory tile into a float32 accumulator by TMA
-// reduce-add; dK and dV are stored once at the end. The MMA warp issues the next tile's S^T
-// and dP^T right behind dQ, so they run while the compute warps drain dQ.
+//                                    bf16 into shared memory (K-major, 128-byte swizzle)
+//   dV += P^T dO_u, dK += dS^T Q_u   (M=128 keys, N=64, K=64 queries)   -> TMEM 256..383
+// and per query tile, after its second half:
+//   dQ_tile = dS K                   (M=128 queries, N=64, K=128 keys)  -> TMEM 384..447
+// With two S^T/dP^T buffers the tensor core computes one sub-tile while the compute warps turn
+// the other into P^T and dS^T. dQ_tile goes through a swizzled shared-memory tile into a
+// float32 accumulator by TMA reduce-add (drained between the next tile's halves); dK and dV
+// are stored once at the end.
 constexpr int BWD_THREADS = 288;
 constexpr size_t BWD_SMEM_BYTES = 12 * TILE + 2048 + 1024 + 256;  // K, V, Q[2], dO[2], P^T, dS^T, dQ, lse/D[2]
 
@@ -341,7 +343,7 @@ __global__ void __maxnreg__(168)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sK = smem;
     uint8_t* sV = smem + TILE;
-    uint8_t* sQ = smem + 2 * TILE;    // two stages
+    uint8_t* sQ = smem + 2 * TILE;    // two stages (query tiles)
     uint8_t* sO = smem + 4 * TILE;    // dO, two stages
     uint8_t* sPT = smem + 6 * TILE;   // two halves (query columns 0..63, 64..127)
     uint8_t* sDS = smem + 8 * TILE;   // two halves
@@ -349,13 +351,13 @@ __global__ void __maxnreg__(168)
     float* sLD = reinterpret_cast<float*>(smem + 12 * TILE);  // [2][lse 128 | D 128]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 12 * TILE + 2048);
     uint64_t* bar_kv = bars;
-    uint64_t* bar_qo = bars + 1;      // [2]
-    uint64_t* bar_s = bars + 3;       // S^T, dP^T of the current tile in TMEM
-    uint64_t* bar_p = bars + 4;       // P^T, dS^T written (256 arrivals)
-    uint64_t* bar_mm = bars + 5;      // dV, dK, dQ of the current tile done
-    uint64_t* bar_drain = bars + 6;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8);
+    uint64_t* bar_qo = bars + 1;      // [2] Q, dO of a query tile landed
+    uint64_t* bar_s = bars + 3;       // [2] S^T, dP^T of a sub-tile in TMEM buffer
+    uint64_t* bar_p = bars + 5;       // [2] P^T, dS^T of a half written (256 arrivals)
+    uint64_t* bar_mm = bars + 7;      // dV, dK and dQ of a query tile done
+    uint64_t* bar_drain = bars + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 10);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = H * HS;
@@ -366,13 +368,15 @@ __global__ void __maxnreg__(168)
     const int n_qt = (T + QT - 1) / QT;
     const int first_qt = k0 / QT;
     const int n_it = n_qt - first_qt;
+    const int n_u = 2 * n_it;
 
     if (tid == 0) {
         mbar_init(bar_kv, 1);
-        mbar_init(&bar_qo[0], 1);
-        mbar_init(&bar_qo[1], 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_p, 256);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_qo[i], 1);
+            mbar_init(&bar_s[i], 1);
+            mbar_init(&bar_p[i], 256);
+        }
         mbar_init(bar_mm, 1);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -386,7 +390,7 @@ __global__ void __maxnreg__(168)
 
     if (warp == 8) {
         if (lane == 0 && n_it > 0) {
-            const uint32_t id_s = instr_desc_bf16(false, false, 128, 128);  // S^T, dP^T
+            const uint32_t id_s = instr_desc_bf16(false, false, 128, 64);   // S^T, dP^T of a sub-tile
             const uint32_t id_kv = instr_desc_bf16(false, true, 128, 64);   // dV, dK: B (dO, Q) MN-major
             const uint32_t id_q = instr_desc_bf16(true, true, 128, 64);     // dQ: A (dS) and B (K) MN-major
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
@@ -402,66 +406,68 @@ __global__ void __maxnreg__(168)
                 pend[i] = 0;
             }
             const uint32_t k_a = saddr(sK), v_a = saddr(sV);
+            bool kv_pending = true, issued = false;
+            // S^T and dP^T of sub-tile u into TMEM buffer u % 2 (its tile's Q/dO must have landed)
+            auto issue_s = [&](int u) {
+                const int st = (u >> 1) & 1, hq = u & 1;
+                const uint32_t q_a = saddr(sQ + st * TILE) + hq * 8192, o_a = saddr(sO + st * TILE) + hq * 8192;
+                const uint32_t d = tmem + (uint32_t)(u & 1) * 128;
+#pragma unroll
+                for (int k = 0; k < HS / 16; ++k)
+                    umma_bf16(d, smem_desc(k_a + k * 32, 16, 1024), smem_desc(q_a + k * 32, 16, 1024), id_s, k > 0);
+#pragma unroll
+                for (int k = 0; k < HS / 16; ++k)
+                    umma_bf16(d + 64, smem_desc(v_a + k * 32, 16, 1024), smem_desc(o_a + k * 32, 16, 1024), id_s,
+                              k > 0);
+                umma_commit(&bar_s[u & 1]);
+            };
             bool ok = mbar_wait(bar_kv, 0, abort_flag, WAIT_NS) && mbar_wait(&bar_qo[0], 0, abort_flag, WAIT_NS);
-            bool kv_pending = !ok;
-            bool issued = false;
             if (ok) {
+                kv_pending = false;
                 pend[0] = -1;
                 tc_fence_after();
-                const uint32_t q_a = saddr(sQ), o_a = saddr(sO);
-#pragma unroll
-                for (int k = 0; k < HS / 16; ++k)
-                    umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(q_a + k * 32, 16, 1024), id_s, k > 0);
-#pragma unroll
-                for (int k = 0; k < HS / 16; ++k)
-                    umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(o_a + k * 32, 16, 1024), id_s,
-                              k > 0);
-                umma_commit(bar_s);
+                issue_s(0);
+                issue_s(1);
                 issued = true;
             }
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int st = it & 1;
-                if (!mbar_wait(bar_p, it & 1, abort_flag, WAIT_NS)) {
+            for (int u = 0; ok && u < n_u; ++u) {
+                const int it = u >> 1, hq = u & 1, st = it & 1;
+                if (!mbar_wait(&bar_p[hq], it & 1, abort_flag, WAIT_NS)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t pt_a = saddr(sPT), ds_a = saddr(sDS);
-                const uint32_t q_a = saddr(sQ + st * TILE), o_a = saddr(sO + st * TILE);
+                const uint32_t pt_a = saddr(sPT) + hq * 16384, ds_a = saddr(sDS) + hq * 16384;
+                const uint32_t q_a = saddr(sQ + st * TILE) + hq * 8192, o_a = saddr(sO + st * TILE) + hq * 8192;
 #pragma unroll
-                for (int k = 0; k < QT / 16; ++k) {
-                    const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
-                    umma_bf16(tmem + 256, smem_desc(pt_a + koff, 16, 1024), smem_desc(o_a + k * 2048, 8192, 1024),
-                              id_kv, (it > 0 || k > 0) ? 1u : 0u);
-                    umma_bf16(tmem + 320, smem_desc(ds_a + koff, 16, 1024), smem_desc(q_a + k * 2048, 8192, 1024),
-                              id_kv, (it > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) {
+                    umma_bf16(tmem + 256, smem_desc(pt_a + k * 32, 16, 1024), smem_desc(o_a + k * 2048, 8192, 1024),
+                              id_kv, (u > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16(tmem + 320, smem_desc(ds_a + k * 32, 16, 1024), smem_desc(q_a + k * 2048, 8192, 1024),
+                              id_kv, (u > 0 || k > 0) ? 1u : 0u);
                 }
+                if (hq == 1) {
+                    const uint32_t dsa = saddr(sDS);
 #pragma unroll
-                for (int k = 0; k < KT / 16; ++k)
-                    umma_bf16(tmem + 384, smem_desc(ds_a + k * 2048, 16384, 1024),
-                              smem_desc(k_a + k * 2048, 8192, 1024), id_q, k > 0);
-                umma_commit(bar_mm);
-                if (it + 1 < n_it) {
-                    const int ns = st ^ 1;
-                    if (!mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, abort_flag, WAIT_NS)) {
-                        ok = false;
-                        break;
+                    for (int k = 0; k < KT / 16; ++k)
+                        umma_bf16(tmem + 384, smem_desc(dsa + k * 2048, 16384, 1024),
+                                  smem_desc(k_a + k * 2048, 8192, 1024), id_q, k > 0);
+                    umma_commit(bar_mm);
+                }
+                if (u + 2 < n_u) {
+                    if (hq == 0) {  // the next tile's Q/dO
+                        const int ns = (it + 1) & 1;
+                        if (!mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, abort_flag, WAIT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        pend[ns] = -1;
+                        tc_fence_after();
                     }
-                    pend[ns] = -1;
-                    tc_fence_after();
-                    const uint32_t nq_a = saddr(sQ + ns * TILE), no_a = saddr(sO + ns * TILE);
-#pragma unroll
-                    for (int k = 0; k < HS / 16; ++k)
-                        umma_bf16(tmem, smem_desc(k_a + k * 32, 16, 1024), smem_desc(nq_a + k * 32, 16, 1024), id_s,
-                                  k > 0);
-#pragma unroll
-                    for (int k = 0; k < HS / 16; ++k)
-                        umma_bf16(tmem + 128, smem_desc(v_a + k * 32, 16, 1024), smem_desc(no_a + k * 32, 16, 1024),
-                                  id_s, k > 0);
-                    umma_commit(bar_s);
+                    issue_s(u + 2);
                 }
-                if (it + 2 < n_it) {
-                    // stage st (this tile's Q, dO) is free once dV, dK and dQ are done
+                if (hq == 1 && it + 2 < n_it) {
+                    // stage st (this tile's Q, dO) is free once dV, dK and dQ of the tile are done
                     if (!mbar_wait(bar_mm, it & 1, abort_flag, WAIT_NS)) {
                         ok = false;
                         break;
@@ -493,114 +499,135 @@ __global__ void __maxnreg__(168)
         const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
         const float sl2 = 0.125f * 1.4426950408889634f;
         const float L2E = 1.4426950408889634f;
+        // Every compute thread makes the same named-barrier calls in the same order; a failed
+        // wait only skips work (and raises the abort flag so every other wait ends quickly),
+        // and each barrier ORs the failure so the choices after it are block-uniform.
         bool fail = false;
-        // lse (in log2 units) or D for tile 0, one value per thread
-        float ld_next = 0.f;
-        if (n_it > 0) {
-            const int q = first_qt * QT + (tid & 127);
-            ld_next = q < T ? (tid < 128 ? lse[(int64_t)bh * T + q] * L2E : dvec[(int64_t)bh * T + q]) : 0.f;
-        }
-        for (int it = 0; it < n_it; ++it) {
-            const int q0 = (first_qt + it) * QT;
-            float* sL = sLD + (it & 1) * 256;
-            sL[tid] = ld_next;
-            if (it + 1 < n_it) {
-                const int q = q0 + QT + (tid & 127);
-                ld_next = q < T ? (tid < 128 ? lse[(int64_t)bh * T + q] * L2E : dvec[(int64_t)bh * T + q]) : 0.f;
-            }
-            // the dQ staging tile is free once the previous reduce has read it
-            if (tid == 0) bulk_wait_read<0>();
-            if (named_bar_or(1, 256, fail)) {
+        auto note_fail = [&](bool ok_) {
+            if (!ok_) {
                 fail = true;
-                break;
+                *abort_flag = 1;
             }
-            fail = !__all_sync(0xffffffffu, mbar_wait(bar_s, it & 1, abort_flag, WAIT_NS));
+        };
+        // lse (log2 units) or D of query tile t, one value per thread
+        auto ld_value = [&](int t) {
+            const int q = (first_qt + t) * QT + (tid & 127);
+            return q < T ? (tid < 128 ? lse[(int64_t)bh * T + q] * L2E : dvec[(int64_t)bh * T + q]) : 0.f;
+        };
+        if (n_it > 0) sLD[tid] = ld_value(0);
+        float ld_next = n_it > 1 ? ld_value(1) : 0.f;
+        fail = named_bar_or(1, 256, fail);
+        // dQ of query tile t: TMEM -> swizzled staging -> TMA reduce-add (called block-uniformly)
+        auto drain_dq = [&](int t) {
+            if (tid == 0) bulk_wait_read<0>();  // the previous reduce has read the staging tile
+            fail = named_bar_or(1, 256, fail);
             if (!fail) {
                 tc_fence_after();
-                // visible query columns c (of this warp's 64): lo <= c < hi
-                const int cbase = hf * 64;
-                int lo = 0, hi = 64;
+                uint32_t qv[32];
+                tmem_ld32_nowait(lane_addr + 384 + hf * 32, qv);
+                tmem_wait_ld_only();
+                reg_fence32(qv);
+                uint8_t* box = sDQ + hf * TILE;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(box + r * 128 + ((j ^ (r & 7)) << 4)) =
+                        make_float4(__uint_as_float(qv[4 * j]) * 0.125f, __uint_as_float(qv[4 * j + 1]) * 0.125f,
+                                    __uint_as_float(qv[4 * j + 2]) * 0.125f, __uint_as_float(qv[4 * j + 3]) * 0.125f);
+                fence_proxy_async_smem();
+                tc_fence_before();
+            }
+            fail = named_bar_or(1, 256, fail);
+            if (!fail && tid == 0) {
+                // rows past this sequence carry dS = 0 (masked), so the whole box is added
+                const int y0 = row0 + (first_qt + t) * QT;
+                tma_reduce_add_2d(&tm_dq, sDQ, h * HS, y0);
+                tma_reduce_add_2d(&tm_dq, sDQ + TILE, h * HS + 32, y0);
+                bulk_commit();
+            }
+        };
+        for (int u = 0; u < n_u; ++u) {
+            const int it = u >> 1, hq = u & 1;
+            const int q0 = (first_qt + it) * QT;
+            const float* sL = sLD + (it & 1) * 256;
+            if (!fail) note_fail(__all_sync(0xffffffffu, mbar_wait(&bar_s[hq], it & 1, abort_flag, WAIT_NS)));
+            if (!fail) {
+                tc_fence_after();
+                uint32_t sv[32], dv[32];
+                tmem_ld32_nowait(lane_addr + hq * 128 + hf * 32, sv);
+                tmem_ld32_nowait(lane_addr + hq * 128 + 64 + hf * 32, dv);
+                tmem_wait_ld_only();
+                reg_fence32(sv);
+                reg_fence32(dv);
+                // this warp's 32 query columns: tile columns cbase .. cbase + 31; visible c
+                // (0..31) satisfy lo <= c < hi
+                const int cbase = hq * 64 + hf * 32;
+                int lo = 0, hi = 32;
                 if (q0 == k0) lo = r - cbase;                 // causal: query >= key on the diagonal
                 hi = min(hi, T - q0 - cbase);                 // ragged last query tile
                 if (kk >= T) hi = 0;                          // padding key rows
-                const bool masked = lo > 0 || hi < 64;
+                const bool masked = lo > 0 || hi < 32;
                 const float* L = sL + cbase;
                 const float* D = sL + 128 + cbase;
-                // two blocks of 32 columns (S^T and dP^T rows: 64 registers per block)
-#pragma unroll 1
-                for (int cb = 0; cb < 64; cb += 32) {
-                    uint32_t sv[32], dv[32];
-                    tmem_ld32_nowait(lane_addr + cbase + cb, sv);
-                    tmem_ld32_nowait(lane_addr + 128 + cbase + cb, dv);
-                    tmem_wait_ld_only();
-                    reg_fence32(sv);
-                    reg_fence32(dv);
+                uint32_t pw[16], qw[16];
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) {
-                        const float4 l0 = *reinterpret_cast<const float4*>(L + cb + c8);
-                        const float4 l1 = *reinterpret_cast<const float4*>(L + cb + c8 + 4);
-                        const float4 d0 = *reinterpret_cast<const float4*>(D + cb + c8);
-                        const float4 d1 = *reinterpret_cast<const float4*>(D + cb + c8 + 4);
-                        const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-                        const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-                        uint32_t pw[4], qw[4];
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    const float4 l0 = *reinterpret_cast<const float4*>(L + c8);
+                    const float4 l1 = *reinterpret_cast<const float4*>(L + c8 + 4);
+                    const float4 d0 = *reinterpret_cast<const float4*>(D + c8);
+                    const float4 d1 = *reinterpret_cast<const float4*>(D + c8 + 4);
+                    const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+                    const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            const int c = cb + c8 + e;
-                            float p0 = ex2_hw(fmaf(__uint_as_float(sv[c8 + e]), sl2, -lv[e]));
-                            float p1 = ex2_hw(fmaf(__uint_as_float(sv[c8 + e + 1]), sl2, -lv[e + 1]));
-                            float ds0 = p0 * (__uint_as_float(dv[c8 + e]) - dd[e]);
-                            float ds1 = p1 * (__uint_as_float(dv[c8 + e + 1]) - dd[e + 1]);
-                            if (masked) {  // hidden pairs contribute exactly zero
-                                const bool v0 = c >= lo && c < hi, v1 = c + 1 >= lo && c + 1 < hi;
-                                p0 = v0 ? p0 : 0.f;
-                                ds0 = v0 ? ds0 : 0.f;
-                                p1 = v1 ? p1 : 0.f;
-                                ds1 = v1 ? ds1 : 0.f;
-                            }
-                            __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                            __nv_bfloat162 u2 = __floats2bfloat162_rn(ds0, ds1);
-                            pw[e >> 1] = *reinterpret_cast<uint32_t*>(&t2);
-                            qw[e >> 1] = *reinterpret_cast<uint32_t*>(&u2);
+                    for (int e = 0; e < 8; e += 2) {
+                        const int c = c8 + e;
+                        float p0 = ex2_hw(fmaf(__uint_as_float(sv[c]), sl2, -lv[e]));
+                        float p1 = ex2_hw(fmaf(__uint_as_float(sv[c + 1]), sl2, -lv[e + 1]));
+                        float ds0 = p0 * (__uint_as_float(dv[c]) - dd[e]);
+                        float ds1 = p1 * (__uint_as_float(dv[c + 1]) - dd[e + 1]);
+                        if (masked) {  // hidden pairs contribute exactly zero
+                            const bool v0 = c >= lo && c < hi, v1 = c + 1 >= lo && c + 1 < hi;
+                            p0 = v0 ? p0 : 0.f;
+                            ds0 = v0 ? ds0 : 0.f;
+                            p1 = v1 ? p1 : 0.f;
+                            ds1 = v1 ? ds1 : 0.f;
                         }
-                        *reinterpret_cast<uint4*>(sPT + p_offset(r, cbase + cb + c8)) =
-                            make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                        *reinterpret_cast<uint4*>(sDS + p_offset(r, cbase + cb + c8)) =
-                            make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                        __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                        __nv_bfloat162 u2 = __floats2bfloat162_rn(ds0, ds1);
+                        pw[c >> 1] = *reinterpret_cast<uint32_t*>(&t2);
+                        qw[c >> 1] = *reinterpret_cast<uint32_t*>(&u2);
                     }
                 }
-                fence_proxy_async_smem();  // P^T, dS^T generic stores -> visible to the tensor core
-                tc_fence_before();
-                mbar_arrive(bar_p);
-                // dQ tile: lane r holds query row q0 + r; this warp takes 32 of its 64 columns
-                fail = !__all_sync(0xffffffffu, mbar_wait(bar_mm, it & 1, abort_flag, WAIT_NS));
+                // half hq of P^T / dS^T is free once the previous tile's dV, dK, dQ are done
+                if (hq == 0 && it > 0)
+                    note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (it - 1) & 1, abort_flag, WAIT_NS)));
                 if (!fail) {
-                    tc_fence_after();
-                    uint32_t qv[32];
-                    tmem_ld32_nowait(lane_addr + 384 + hf * 32, qv);
-                    tmem_wait_ld_only();
-                    reg_fence32(qv);
-                    uint8_t* box = sDQ + hf * TILE;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<float4*>(box + r * 128 + ((j ^ (r & 7)) << 4)) =
-                            make_float4(__uint_as_float(qv[4 * j]) * 0.125f, __uint_as_float(qv[4 * j + 1]) * 0.125f,
-                                        __uint_as_float(qv[4 * j + 2]) * 0.125f,
-                                        __uint_as_float(qv[4 * j + 3]) * 0.125f);
-                    fence_proxy_async_smem();
+                    for (int j = 0; j < 4; ++j) {
+                        *reinterpret_cast<uint4*>(sPT + p_offset(r, cbase + 8 * j)) =
+                            make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
+                        *reinterpret_cast<uint4*>(sDS + p_offset(r, cbase + 8 * j)) =
+                            make_uint4(qw[4 * j], qw[4 * j + 1], qw[4 * j + 2], qw[4 * j + 3]);
+                    }
+                    fence_proxy_async_smem();  // P^T, dS^T generic stores -> visible to the tensor core
+                    tc_fence_before();
+                    mbar_arrive(&bar_p[hq]);
                 }
-                tc_fence_before();
             }
-            if (named_bar_or(1, 256, fail)) {
-                fail = true;
-                break;
+            if (hq == 0) {
+                // between the halves: the previous tile's dQ, and lse / D of the next tile
+                fail = named_bar_or(1, 256, fail);
+                if (it > 0) drain_dq(it - 1);
+                if (it + 1 < n_it) {
+                    sLD[((it + 1) & 1) * 256 + tid] = ld_next;
+                    if (it + 2 < n_it) ld_next = ld_value(it + 2);
+                }
+                fail = named_bar_or(1, 256, fail);
             }
-            if (tid == 0) {
-                // rows past this sequence carry dS = 0 (masked), so the whole box is added
-                tma_reduce_add_2d(&tm_dq, sDQ, h * HS, row0 + q0);
-                tma_reduce_add_2d(&tm_dq, sDQ + TILE, h * HS + 32, row0 + q0);
-                bulk_commit();
-            }
+        }
+        if (n_it > 0) {
+            if (!fail) note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (n_it - 1) & 1, abort_flag, WAIT_NS)));
+            fail = named_bar_or(1, 256, fail);
+            drain_dq(n_it - 1);
         }
         if (tid == 0) bulk_wait_all();
         if (fail) {
@@ -649,23 +676,38 @@ __global__ void __maxnreg__(168)
     }
 }
 
-// D[b,h,t] = sum_d dy * y over one head's 64 columns (one warp per (row, head)); also zeroes
-// that head's slice of the float32 dQ accumulator.
+// D[b,h,t] = sum_d dy * y over each head's 64 columns, one warp per row: lane l takes the
+// 16-byte pieces l, l + 32, ... of the row (piece p lies in head p / 8), the 8 lanes of a
+// head add their dot products by shuffles. The warp also zeroes the row of the float32 dQ
+// accumulator.
 __global__ void attn_dvec_zero_kernel(const __nv_bfloat16* __restrict__ y, const __nv_bfloat16* __restrict__ dy,
                                       float* __restrict__ dvec, float* __restrict__ dq_acc, int64_t rows, int T, int H) {
-    int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    int lane = threadIdx.x & 31;
-    if (wid >= rows * H) return;
-    int64_t r = wid / H;
-    int h = (int)(wid % H);
-    int64_t C = (int64_t)H * HS;
-    int64_t off = r * C + h * HS + lane * 2;
-    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(dy + off);
-    __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(y + off);
-    float s = __bfloat162float(a.x) * __bfloat162float(c.x) + __bfloat162float(a.y) * __bfloat162float(c.y);
-    s = warp_sum(s);
-    *reinterpret_cast<float2*>(dq_acc + off) = make_float2(0.f, 0.f);
-    if (lane == 0) dvec[((r / T) * H + h) * T + (r % T)] = s;
+    const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const int C = H * HS, pieces = C / 8;
+    const int64_t b = r / T, t = r % T;
+    for (int p0 = 0; p0 < pieces; p0 += 32) {
+        const int p = p0 + lane;
+        float s = 0.f;
+        if (p < pieces) {
+            const uint4 a = *reinterpret_cast<const uint4*>(dy + r * C + p * 8);
+            const uint4 c = *reinterpret_cast<const uint4*>(y + r * C + p * 8);
+            const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
+            const __nv_bfloat162* ch = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                s += __low2float(ah[k]) * __low2float(ch[k]) + __high2float(ah[k]) * __high2float(ch[k]);
+            float4* z = reinterpret_cast<float4*>(dq_acc + r * C + p * 8);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // pieces p0 .. p0 + 31 hold heads p0 / 8 .. p0 / 8 + 3, eight lanes each
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        if ((lane & 7) == 0 && p < pieces) dvec[(b * H + p / 8) * T + t] = s;
+    }
 }
 
 // dqkv[:, 0:C] (bf16) = dq_acc (float32)
@@ -722,7 +764,7 @@ gk_status attn_bwd_tc(gk_ctx* ctx, const void* qkv, const void* y, const float* 
     if (!make_map(&map_qkv, qkv, 3 * C, rows, 3 * C, 128) || !make_map(&map_dy, dy, C, rows, C, 128) ||
         !make_map_f32(&map_dq, dq_acc, C, rows, C, 32, 128))
         return GK_ERR_UNSUPPORTED;
-    attn_dvec_zero_kernel<<<(unsigned)cdiv(rows * H * 32, 256), 256, 0, ctx->stream>>>(
+    attn_dvec_zero_kernel<<<(unsigned)cdiv(rows * 32, 256), 256, 0, ctx->stream>>>(
         (const __nv_bfloat16*)y, (const __nv_bfloat16*)dy, dvec, dq_acc, rows, T, H);
     GK_TRY(launched(ctx, "attn_dvec_zero"));
     static bool attr = false;

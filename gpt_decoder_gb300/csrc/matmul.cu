@@ -8,8 +8,8 @@
 namespace gk {
 namespace {
 
-constexpr int COLSUM_SPLITS = 128;
-constexpr int COLSUM_VEC = 8;  // columns per thread (one 16-byte bf16 load, two float4 loads)
+constexpr int COLSUM_VEC = 8;    // columns per thread (one 16-byte bf16 load, two float4 loads)
+constexpr int COLSUM_WARPS = 8;  // warps per block, each on its own rows of the same 256 columns
 
 template <typename T>
 __device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
@@ -27,27 +27,54 @@ __device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
     }
 }
 
-// partial[s][c] = sum of rows r = s, s + S, s + 2S, ... of src[:, c] (ascending r). Each
-// thread takes 8 consecutive columns with one vector load per row when the row layout allows.
+// partial[s][c] for column block blockIdx.x (256 columns: 8 per lane) and split s = blockIdx.y:
+// warp w of the block sums rows s*8 + w + k*S*8 (k = 0, 1, ...) with four running sums
+// (k mod 4), the four are added, then the 8 warp sums in warp order: a fixed summation order.
 template <typename T>
-__global__ void colsum_partial_kernel(const T* __restrict__ src, int64_t ld, int64_t rows, int64_t cols, int vec,
-                                      float* __restrict__ partial) {
-    int64_t c0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * COLSUM_VEC;
-    int s = blockIdx.y;
-    if (c0 >= cols) return;
-    float acc[COLSUM_VEC] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+__global__ void __launch_bounds__(COLSUM_WARPS * 32)
+    colsum_partial_kernel(const T* __restrict__ src, int64_t ld, int64_t rows, int64_t cols, int vec,
+                          float* __restrict__ partial) {
+    __shared__ float red[COLSUM_WARPS][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t c0 = (int64_t)blockIdx.x * 256 + lane * COLSUM_VEC;
+    const int64_t stride = (int64_t)gridDim.y * COLSUM_WARPS;
+    float acc[4][COLSUM_VEC];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < COLSUM_VEC; ++k) acc[u][k] = 0.f;
+    int64_t r = (int64_t)blockIdx.y * COLSUM_WARPS + warp;
     if (vec && c0 + COLSUM_VEC <= cols) {
-        for (int64_t r = s; r < rows; r += gridDim.y) {
+        for (; r + 3 * stride < rows; r += 4 * stride) {
+            float v[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) load8<T>(src + (r + u * stride) * ld + c0, v[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[u][k] += v[u][k];
+        }
+        for (; r < rows; r += stride) {
             float v[8];
             load8<T>(src + r * ld + c0, v);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] += v[k];
+            for (int k = 0; k < 8; ++k) acc[0][k] += v[k];
         }
-    } else {
-        for (int64_t r = s; r < rows; r += gridDim.y)
-            for (int k = 0; k < COLSUM_VEC && c0 + k < cols; ++k) acc[k] += load_as_f32(src + r * ld + c0 + k);
+    } else if (c0 < cols) {
+        for (; r < rows; r += stride)
+            for (int k = 0; k < COLSUM_VEC && c0 + k < cols; ++k) acc[0][k] += load_as_f32(src + r * ld + c0 + k);
     }
-    for (int k = 0; k < COLSUM_VEC && c0 + k < cols; ++k) partial[(int64_t)s * cols + c0 + k] = acc[k];
+#pragma unroll
+    for (int k = 0; k < COLSUM_VEC; ++k)
+        red[warp][lane * COLSUM_VEC + k] = (acc[0][k] + acc[1][k]) + (acc[2][k] + acc[3][k]);
+    __syncthreads();
+    const int64_t c = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (c < cols) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < COLSUM_WARPS; ++w) t += red[w][threadIdx.x];
+        partial[(int64_t)blockIdx.y * cols + c] = t;
+    }
 }
 
 // dst[c] += sum_s partial[s][c]: 8 warps per 32 columns, warp w sums slots w, w + 8, ...,
@@ -72,18 +99,23 @@ __global__ void __launch_bounds__(256) colsum_reduce_kernel(const float* __restr
 }  // namespace
 
 gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_t rows, int64_t cols, float* dst) {
-    int splits = (int)std::min<int64_t>(COLSUM_SPLITS, rows);
+    // enough blocks of 8 warps to keep every SM loading: about four per SM
+    const int64_t col_blocks = cdiv(cols, 256);
+    int splits = (int)std::max<int64_t>(1, std::min<int64_t>({cdiv((int64_t)ctx->num_sms * 4, col_blocks),
+                                                               cdiv(rows, COLSUM_WARPS), 1024}));
     float* partial = (float*)workspace(ctx, (size_t)splits * cols * sizeof(float));
     GK_REQUIRE(ctx, partial, GK_ERR_WORKSPACE, "bias gradient needs %lld workspace bytes",
                (long long)splits * cols * 4);
+    GK_REQUIRE(ctx, col_blocks < (1ll << 31), GK_ERR_UNSUPPORTED, "bias gradient: too many columns");
     int esize = dtype == GK_F32 ? 4 : 2;
     int vec = aligned16(src) && ((ld * esize) % 16 == 0);
-    dim3 grid((unsigned)cdiv(cdiv(cols, COLSUM_VEC), 64), (unsigned)splits);
+    dim3 grid((unsigned)col_blocks, (unsigned)splits);
     if (dtype == GK_F32)
-        colsum_partial_kernel<float><<<grid, 64, 0, ctx->stream>>>((const float*)src, ld, rows, cols, vec, partial);
+        colsum_partial_kernel<float><<<grid, COLSUM_WARPS * 32, 0, ctx->stream>>>((const float*)src, ld, rows, cols,
+                                                                                vec, partial);
     else
-        colsum_partial_kernel<__nv_bfloat16><<<grid, 64, 0, ctx->stream>>>((const __nv_bfloat16*)src, ld, rows, cols,
-                                                                         vec, partial);
+        colsum_partial_kernel<__nv_bfloat16><<<grid, COLSUM_WARPS * 32, 0, ctx->stream>>>(
+            (const __nv_bfloat16*)src, ld, rows, cols, vec, partial);
     GK_TRY(launched(ctx, "colsum_partial"));
     colsum_reduce_kernel<<<(unsigned)cdiv(cols, 32), 256, 0, ctx->stream>>>(partial, splits, cols, dst);
     return launched(ctx, "colsum_reduce");

@@ -187,57 +187,60 @@ __global__ void layernorm_fwd_block_kernel(const float* __restrict__ x, const fl
     }
 }
 
-// LayerNorm backward, one warp per row (C % 128 == 0, C <= 1024). Each block also keeps
-// per-column partial sums of dy*xhat and dy over its rows and writes them to the
-// workspace (partials [gridDim.x][2][C]); a second kernel adds them in block order.
+// LayerNorm backward, one warp per row (C % 128 == 0, C <= 1024). All of a row's global
+// reads (x, dy and, when accumulating, dx) are issued before its two reductions, so a row
+// costs one memory round trip. Each block also keeps per-column partial sums of dy*xhat, dy
+// and (np == 3) of the resulting dx over its rows and writes them to the workspace
+// (partials [gridDim.x][np][C]); a second kernel adds them in block order.
 template <int VPT>
 __global__ void layernorm_bwd_warp_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
                                           const float* __restrict__ mean, const float* __restrict__ rstd,
                                           const float* __restrict__ dy, float* __restrict__ dx, int accumulate,
-                                          __nv_bfloat16* __restrict__ dx_bf16, float* __restrict__ partial,
+                                          __nv_bfloat16* __restrict__ dx_bf16, float* __restrict__ partial, int np,
                                           int64_t rows, int C) {
-    extern __shared__ float sp[];  // [nwarps][2][C] when partials are kept
+    extern __shared__ float sp[];  // [nwarps][np][C] when partials are kept
     int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    float4 pg[VPT], pb[VPT];
+    float4 pg[VPT], pb[VPT], pd[VPT];
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) pg[i] = pb[i] = make_float4(0, 0, 0, 0);
+    for (int i = 0; i < VPT; ++i) pg[i] = pb[i] = pd[i] = make_float4(0, 0, 0, 0);
     float4 gm[VPT];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) gm[i] = *reinterpret_cast<const float4*>(gamma + (i * 32 + lane) * 4);
     for (int64_t row = (int64_t)blockIdx.x * nw + warp; row < rows; row += (int64_t)gridDim.x * nw) {
         const float* xr = x + row * C;
         const float* gr = dy + row * C;
+        float* dr = dx + row * C;
         float mu = mean[row], rs = rstd[row];
-        float4 xh[VPT], g[VPT];
-        float s1 = 0.f, s2 = 0.f;
+        float4 a[VPT], g[VPT], p[VPT];
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             int c = (i * 32 + lane) * 4;
-            float4 a = *reinterpret_cast<const float4*>(xr + c);
+            a[i] = *reinterpret_cast<const float4*>(xr + c);
             g[i] = *reinterpret_cast<const float4*>(gr + c);
-            xh[i] = make_float4((a.x - mu) * rs, (a.y - mu) * rs, (a.z - mu) * rs, (a.w - mu) * rs);
+            p[i] = accumulate ? *reinterpret_cast<const float4*>(dr + c) : make_float4(0, 0, 0, 0);
+        }
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            a[i] = make_float4((a[i].x - mu) * rs, (a[i].y - mu) * rs, (a[i].z - mu) * rs, (a[i].w - mu) * rs);
             float h0 = g[i].x * gm[i].x, h1 = g[i].y * gm[i].y, h2 = g[i].z * gm[i].z, h3 = g[i].w * gm[i].w;
             s1 += (h0 + h1) + (h2 + h3);
-            s2 += (h0 * xh[i].x + h1 * xh[i].y) + (h2 * xh[i].z + h3 * xh[i].w);
-            pg[i].x += g[i].x * xh[i].x; pg[i].y += g[i].y * xh[i].y;
-            pg[i].z += g[i].z * xh[i].z; pg[i].w += g[i].w * xh[i].w;
+            s2 += (h0 * a[i].x + h1 * a[i].y) + (h2 * a[i].z + h3 * a[i].w);
+            pg[i].x += g[i].x * a[i].x; pg[i].y += g[i].y * a[i].y;
+            pg[i].z += g[i].z * a[i].z; pg[i].w += g[i].w * a[i].w;
             pb[i].x += g[i].x; pb[i].y += g[i].y; pb[i].z += g[i].z; pb[i].w += g[i].w;
         }
         float m1 = warp_sum(s1) / C, m2 = warp_sum(s2) / C;
-        float* dr = dx + row * C;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             int c = (i * 32 + lane) * 4;
             float4 o;
-            o.x = rs * (g[i].x * gm[i].x - m1 - xh[i].x * m2);
-            o.y = rs * (g[i].y * gm[i].y - m1 - xh[i].y * m2);
-            o.z = rs * (g[i].z * gm[i].z - m1 - xh[i].z * m2);
-            o.w = rs * (g[i].w * gm[i].w - m1 - xh[i].w * m2);
-            if (accumulate) {
-                float4 p = *reinterpret_cast<const float4*>(dr + c);
-                o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
-            }
+            o.x = rs * (g[i].x * gm[i].x - m1 - a[i].x * m2) + p[i].x;
+            o.y = rs * (g[i].y * gm[i].y - m1 - a[i].y * m2) + p[i].y;
+            o.z = rs * (g[i].z * gm[i].z - m1 - a[i].z * m2) + p[i].z;
+            o.w = rs * (g[i].w * gm[i].w - m1 - a[i].w * m2) + p[i].w;
             *reinterpret_cast<float4*>(dr + c) = o;
+            pd[i].x += o.x; pd[i].y += o.y; pd[i].z += o.z; pd[i].w += o.w;
             if (dx_bf16) {
                 __nv_bfloat162 lo2 = __floats2bfloat162_rn(o.x, o.y), hi2 = __floats2bfloat162_rn(o.z, o.w);
                 uint2 packed;
@@ -251,27 +254,28 @@ __global__ void layernorm_bwd_warp_kernel(const float* __restrict__ x, const flo
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         int c = (i * 32 + lane) * 4;
-        *reinterpret_cast<float4*>(sp + (warp * 2 + 0) * C + c) = pg[i];
-        *reinterpret_cast<float4*>(sp + (warp * 2 + 1) * C + c) = pb[i];
+        *reinterpret_cast<float4*>(sp + (warp * np + 0) * C + c) = pg[i];
+        *reinterpret_cast<float4*>(sp + (warp * np + 1) * C + c) = pb[i];
+        if (np == 3) *reinterpret_cast<float4*>(sp + (warp * np + 2) * C + c) = pd[i];
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+    for (int c = threadIdx.x; c < np * C; c += blockDim.x) {
         int which = c / C, col = c % C;
         float acc = 0.f;
-        for (int w = 0; w < nw; ++w) acc += sp[(w * 2 + which) * C + col];
-        partial[((int64_t)blockIdx.x * 2 + which) * C + col] = acc;
+        for (int w = 0; w < nw; ++w) acc += sp[(w * np + which) * C + col];
+        partial[((int64_t)blockIdx.x * np + which) * C + col] = acc;
     }
 }
 
 // General LayerNorm backward: one block per row (row stats through a block reduction).
-// Per-column partials of dy*xhat and dy go to partial[blockIdx.x % nparts][2][C] rows
+// Per-column partials of dy*xhat, dy (and dx when np == 3) go to partial[slot][np][C] rows
 // accumulated by a fixed set of rows per slot (rows r with r % nparts == slot, handled in
 // ascending order by one block each), keeping the sum order fixed.
 __global__ void layernorm_bwd_block_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
                                            const float* __restrict__ mean, const float* __restrict__ rstd,
                                            const float* __restrict__ dy, float* __restrict__ dx, int accumulate,
                                            __nv_bfloat16* __restrict__ dx_bf16, float* __restrict__ partial,
-                                           int64_t rows, int C) {
+                                           int np, int64_t rows, int C) {
     __shared__ float red[32];
     int nparts = gridDim.x;
     for (int64_t row = blockIdx.x; row < rows; row += nparts) {
@@ -294,45 +298,51 @@ __global__ void layernorm_bwd_block_kernel(const float* __restrict__ x, const fl
             dr[c] = o;
             if (dx_bf16) dx_bf16[row * C + c] = __float2bfloat16_rn(o);
             if (partial) {
-                float* pp = partial + (int64_t)blockIdx.x * 2 * C;
+                float* pp = partial + (int64_t)blockIdx.x * np * C;
                 if (row == blockIdx.x) {
                     pp[c] = g * xh;
                     pp[C + c] = g;
+                    if (np == 3) pp[2 * C + c] = o;
                 } else {
                     pp[c] += g * xh;
                     pp[C + c] += g;
+                    if (np == 3) pp[2 * C + c] += o;
                 }
             }
         }
     }
 }
 
-// dgamma[c] += sum_p partial[p][0][c]; dbeta[c] += sum_p partial[p][1][c]. A block of 8 warps
-// takes 32 columns: warp w sums slots w, w + 8, ... (lane = column, coalesced rows of the
-// partial buffer), then the 8 warp sums are added in warp order: a fixed summation order.
-__global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __restrict__ partial, int nparts, int C,
-                                                             float* dgamma, float* dbeta) {
-    __shared__ float red[2][8][32];
+// out_k[c] += sum_p partial[p][k][c] for k < np (out_0 = dgamma, out_1 = dbeta, out_2 = the
+// column sums of dx; a null output is skipped). Block (x, k) takes 32 columns of array k:
+// warp w sums slots w, w + 8, ... with four independent running sums (slot order fixed),
+// then the 8 warp sums are added in warp order: a fixed summation order.
+__global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __restrict__ partial, int nparts, int np,
+                                                             int C, float* out0, float* out1, float* out2) {
+    __shared__ float red[8][32];
     int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int c = blockIdx.x * 32 + lane;
-    float a = 0.f, b = 0.f;
+    int k = blockIdx.y, c = blockIdx.x * 32 + lane;
+    float* out = k == 0 ? out0 : k == 1 ? out1 : out2;
+    if (!out) return;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
     if (c < C) {
-        for (int p = warp; p < nparts; p += 8) {
-            a += partial[((int64_t)p * 2 + 0) * C + c];
-            b += partial[((int64_t)p * 2 + 1) * C + c];
+        const float* src = partial + (int64_t)k * C + c;
+        const int64_t step = (int64_t)np * C;
+        int p = warp;
+        for (; p + 24 < nparts; p += 32) {
+            a0 += src[p * step];
+            a1 += src[(p + 8) * step];
+            a2 += src[(p + 16) * step];
+            a3 += src[(p + 24) * step];
         }
+        for (; p < nparts; p += 8) a0 += src[p * step];
     }
-    red[0][warp][lane] = a;
-    red[1][warp][lane] = b;
+    red[warp][lane] = (a0 + a1) + (a2 + a3);
     __syncthreads();
     if (warp == 0 && c < C) {
-        float ta = 0.f, tb = 0.f;
-        for (int w = 0; w < 8; ++w) {
-            ta += red[0][w][lane];
-            tb += red[1][w][lane];
-        }
-        if (dgamma) dgamma[c] += ta;
-        if (dbeta) dbeta[c] += tb;
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += red[w][lane];
+        out[c] += t;
     }
 }
 
@@ -677,39 +687,39 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
 
 gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, const float* mean, const float* rstd,
                            const float* dy, float* dx, int accumulate_dx, uint16_t* dx_bf16, float* dgamma,
-                           float* dbeta, int64_t rows, int C) {
+                           float* dbeta, float* dx_colsum, int64_t rows, int C) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, x && gamma && mean && rstd && dy && dx && rows > 0 && C > 0, GK_ERR_ARG,
                "gk_layernorm_bwd: bad argument");
-    bool want_partials = dgamma || dbeta;
+    const bool want_partials = dgamma || dbeta || dx_colsum;
+    const int np = dx_colsum ? 3 : 2;  // partial arrays: dy*xhat, dy (, dx)
     bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(dy) && aligned16(dx) &&
                      aligned16(gamma) && (!dx_bf16 || ((uintptr_t)dx_bf16 & 7) == 0);
     int nparts;
     if (warp_path) {
         int wpb = 8;
-        nparts = (int)std::min<int64_t>(cdiv(rows, wpb), (int64_t)ctx->num_sms * 4);
-        if (nparts > 1216) nparts = 1216;
+        nparts = (int)std::min<int64_t>(cdiv(rows, wpb), (int64_t)ctx->num_sms * 2);
     } else {
-        // one block per row slot; bound the partial buffer (2 x C floats per slot) for wide rows
-        int64_t cap = std::max<int64_t>(8, std::min<int64_t>(1216, (int64_t)(16 << 20) / ((int64_t)2 * C * 4)));
+        // one block per row slot; bound the partial buffer (np x C floats per slot) for wide rows
+        int64_t cap = std::max<int64_t>(8, std::min<int64_t>(1216, (int64_t)(16 << 20) / ((int64_t)np * C * 4)));
         nparts = (int)std::min<int64_t>(rows, cap);
     }
     float* partial = nullptr;
     if (want_partials) {
-        partial = (float*)workspace(ctx, (size_t)nparts * 2 * C * sizeof(float));
+        partial = (float*)workspace(ctx, (size_t)nparts * np * C * sizeof(float));
         GK_REQUIRE(ctx, partial, GK_ERR_WORKSPACE, "gk_layernorm_bwd: needs %zu workspace bytes",
-                   (size_t)nparts * 2 * C * sizeof(float));
+                   (size_t)nparts * np * C * sizeof(float));
     }
     if (warp_path) {
         int wpb = 8;
         int vpt = C / 128;
-        size_t smem = want_partials ? (size_t)wpb * 2 * C * sizeof(float) : 0;
+        size_t smem = want_partials ? (size_t)wpb * np * C * sizeof(float) : 0;
 #define LN_BWD_CASE(V)                                                                                       \
     case V:                                                                                                  \
         cudaFuncSetAttribute(layernorm_bwd_warp_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
                              (int)smem);                                                                     \
         layernorm_bwd_warp_kernel<V><<<nparts, wpb * 32, smem, ctx->stream>>>(                               \
-            x, gamma, mean, rstd, dy, dx, accumulate_dx, (__nv_bfloat16*)dx_bf16, partial, rows, C);         \
+            x, gamma, mean, rstd, dy, dx, accumulate_dx, (__nv_bfloat16*)dx_bf16, partial, np, rows, C);     \
         break;
         switch (vpt) {
             LN_BWD_CASE(1) LN_BWD_CASE(2) LN_BWD_CASE(3) LN_BWD_CASE(4)
@@ -718,11 +728,12 @@ gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, cons
 #undef LN_BWD_CASE
     } else {
         layernorm_bwd_block_kernel<<<nparts, 512, 0, ctx->stream>>>(x, gamma, mean, rstd, dy, dx, accumulate_dx,
-                                                                   (__nv_bfloat16*)dx_bf16, partial, rows, C);
+                                                                   (__nv_bfloat16*)dx_bf16, partial, np, rows, C);
     }
     GK_TRY(launched(ctx, "layernorm_bwd"));
     if (want_partials) {
-        reduce_partials_kernel<<<(unsigned)cdiv(C, 32), 256, 0, ctx->stream>>>(partial, nparts, C, dgamma, dbeta);
+        reduce_partials_kernel<<<dim3((unsigned)cdiv(C, 32), (unsigned)np), 256, 0, ctx->stream>>>(
+            partial, nparts, np, C, dgamma, dbeta, dx_colsum);
         GK_TRY(launched(ctx, "layernorm_bwd_reduce"));
     }
     return GK_OK;
@@ -898,7 +909,7 @@ extern "C" gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x,
                                  (int)smem) != cudaSuccess)                                                  \
             return GK_ERR_CUDA;                                                                              \
         layernorm_bwd_warp_kernel<V><<<nparts, 8 * 32, smem, stream>>>(                                      \
-            x, gamma, mean, rstd, dy, dx, accumulate_dx, (__nv_bfloat16*)dx_bf16, partial, rows, C);         \
+            x, gamma, mean, rstd, dy, dx, accumulate_dx, (__nv_bfloat16*)dx_bf16, partial, 2, rows, C);      \
         break;
             LN_NA_CASE(1) LN_NA_CASE(2) LN_NA_CASE(3) LN_NA_CASE(4)
             LN_NA_CASE(5) LN_NA_CASE(6) LN_NA_CASE(7) LN_NA_CASE(8)
@@ -907,12 +918,13 @@ extern "C" gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x,
     } else {
         nparts = (int)std::min<int64_t>(rows, std::min<int64_t>(1216, slots));
         layernorm_bwd_block_kernel<<<nparts, 512, 0, stream>>>(x, gamma, mean, rstd, dy, dx, accumulate_dx,
-                                                              (__nv_bfloat16*)dx_bf16, partial, rows, C);
+                                                              (__nv_bfloat16*)dx_bf16, partial, 2, rows, C);
     }
     if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
     if (want_partials) {
         // every slot the reduction reads was written in full by the kernel above
-        reduce_partials_kernel<<<(unsigned)cdiv(C, 32), 256, 0, stream>>>(partial, nparts, C, dgamma, dbeta);
+        reduce_partials_kernel<<<dim3((unsigned)cdiv(C, 32), 2), 256, 0, stream>>>(partial, nparts, 2, C, dgamma,
+                                                                                  dbeta, nullptr);
         if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
     }
     return GK_OK;

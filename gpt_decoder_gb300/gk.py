@@ -61,7 +61,7 @@ _SIGS = {
     "gk_embedding_fwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_embedding_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32]),
-    "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
+    "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, P, I64, I32]),
     "gk_layernorm_bwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
     "gk_gelu_fwd": (I32, [P, P, P, I64]),
     "gk_gelu_bwd": (I32, [P, P, P, P, I64]),
@@ -167,10 +167,11 @@ def gk_layernorm_fwd(ctx, x, gamma, beta, y, y_dtype, mean, rstd, rows, C, eps=1
                                              _p(rstd), rows, C, eps), "gk_layernorm_fwd")
 
 
-def gk_layernorm_bwd(ctx, x, gamma, mean, rstd, dy, dx, accumulate_dx, dx_bf16, dgamma, dbeta, rows, C):
+def gk_layernorm_bwd(ctx, x, gamma, mean, rstd, dy, dx, accumulate_dx, dx_bf16, dgamma, dbeta, rows, C,
+                     dx_colsum=None):
     return _check(ctx, _lib.gk_layernorm_bwd(ctx.handle, _p(x), _p(gamma), _p(mean), _p(rstd), _p(dy), _p(dx),
-                                             int(accumulate_dx), _p(dx_bf16), _p(dgamma), _p(dbeta), rows, C),
-                  "gk_layernorm_bwd")
+                                             int(accumulate_dx), _p(dx_bf16), _p(dgamma), _p(dbeta), _p(dx_colsum),
+                                             rows, C), "gk_layernorm_bwd")
 
 
 def gk_layernorm_bwd_noalloc(stream, x, gamma, mean, rstd, dy, dx, accumulate_dx, dx_bf16, dgamma, dbeta, rows, C):

@@ -226,8 +226,11 @@ class Gpt:
         # tied head: dlnf = dlogits wte; dwte += dlogits^T lnf
         self._mm_bwd(c, self.dt, self.lnf, C, self.w(gk.GK_T_WTE, 0, True), C, 1, self.dlogits, self.Vp, self.dln, C,
                          gk.GK_F32, 0, None, 0, self.g(gk.GK_T_WTE), C, None, N, C, self.V)
+        # the LayerNorm backwards also leave the column sums of the residual gradient they
+        # produce: the bias gradients of the projections whose output gradient it is
         gk.gk_layernorm_bwd(c, self.xs[-1], self.w(gk.GK_T_LNF_W), self.muf, self.rsf, self.dln, self.dx, 0,
-                            self.dx_bf16, self.g(gk.GK_T_LNF_W), self.g(gk.GK_T_LNF_B), N, C)
+                            self.dx_bf16, self.g(gk.GK_T_LNF_W), self.g(gk.GK_T_LNF_B), N, C,
+                            dx_colsum=self.g(gk.GK_T_MLPPROJ_B, self.L - 1))
         for l in reversed(range(self.L)):
             dt = self.ldt[l]
             bw = dt == gk.GK_BF16
@@ -238,22 +241,24 @@ class Gpt:
             # x_out = x_mid + h Wp + bp   (GELU backward fused into the dX product)
             self._mm_bwd(c, dt, hi(self.h[l]), 4 * C, self.w(gk.GK_T_MLPPROJ_W, l, bw), C, 0, dxg, C, dpre,
                              4 * C, dt, 0, self.pre[l], 4 * C, self.g(gk.GK_T_MLPPROJ_W, l), C,
-                             self.g(gk.GK_T_MLPPROJ_B, l), N, 4 * C, C)
+                             None, N, 4 * C, C)
             self._mm_bwd(c, dt, hi(self.ln2[l]), C, self.w(gk.GK_T_FC_W, l, bw), 4 * C, 0, dpre, 4 * C, self.dln,
                              C, gk.GK_F32, 0, None, 0, self.g(gk.GK_T_FC_W, l), 4 * C, self.g(gk.GK_T_FC_B, l), N,
                              C, 4 * C)
             gk.gk_layernorm_bwd(c, x_mid, self.w(gk.GK_T_LN2_W, l), self.mu2[l], self.rs2[l], self.dln, self.dx, 1,
-                                self.dx_bf16, self.g(gk.GK_T_LN2_W, l), self.g(gk.GK_T_LN2_B, l), N, C)
+                                self.dx_bf16, self.g(gk.GK_T_LN2_W, l), self.g(gk.GK_T_LN2_B, l), N, C,
+                                dx_colsum=self.g(gk.GK_T_ATTNPROJ_B, l))
             # x_mid = x_in + y Wo + bo
             dy = self.dmid[dt]
             self._mm_bwd(c, dt, self.y[l], C, self.w(gk.GK_T_ATTNPROJ_W, l, bw), C, 0, dxg, C, dy, C, dt, 0,
-                             None, 0, self.g(gk.GK_T_ATTNPROJ_W, l), C, self.g(gk.GK_T_ATTNPROJ_B, l), N, C, C)
+                             None, 0, self.g(gk.GK_T_ATTNPROJ_W, l), C, None, N, C, C)
             gk.gk_attn_bwd(c, dt, self.qkv[l], self.y[l], self.lse[l], dy, self.dqkv[dt], B, T, H, hs)
             self._mm_bwd(c, dt, hi(self.ln1[l]), C, self.w(gk.GK_T_ATTN_W, l, bw), 3 * C, 0, self.dqkv[dt], 3 * C,
                              self.dln, C, gk.GK_F32, 0, None, 0, self.g(gk.GK_T_ATTN_W, l), 3 * C,
                              self.g(gk.GK_T_ATTN_B, l), N, C, 3 * C)
             gk.gk_layernorm_bwd(c, x_in, self.w(gk.GK_T_LN1_W, l), self.mu1[l], self.rs1[l], self.dln, self.dx, 1,
-                                self.dx_bf16, self.g(gk.GK_T_LN1_W, l), self.g(gk.GK_T_LN1_B, l), N, C)
+                                self.dx_bf16, self.g(gk.GK_T_LN1_W, l), self.g(gk.GK_T_LN1_B, l), N, C,
+                                dx_colsum=self.g(gk.GK_T_MLPPROJ_B, l - 1) if l > 0 else None)
         gk.gk_embedding_bwd(c, ids, self.dx, self.g(gk.GK_T_WTE), self.g(gk.GK_T_WPE), B, T, C, self.V)
 
     def adamw_cuts(self):

@@ -104,16 +104,22 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
 
 /* Backward of gk_layernorm_fwd for upstream dy (float32 [rows, C]):
  *   dx (=, or += if accumulate_dx) rstd * (dy*gamma - mean(dy*gamma) - xhat*mean(dy*gamma*xhat));
- *   dgamma += sum_rows dy*xhat;  dbeta += sum_rows dy   (deterministic order).
- * dx_bf16, if not NULL, receives a bfloat16 copy of the resulting dx. dgamma/dbeta may be
- * NULL. Workspace: 2 * C * P * 4 bytes, P = min(rows, 1216) partial slots (fewer for C > 1024). */
+ *   dgamma += sum_rows dy*xhat;  dbeta += sum_rows dy   (deterministic order);
+ *   dx_colsum += sum_rows dx, the column sums of the dx this call leaves (after accumulating):
+ *   when dx is also the output gradient of a layer with a bias (the projection feeding the
+ *   residual stream), this is that bias's gradient (the MatMul/bias backward rule), produced
+ *   here so the rows are read once.
+ * dx_bf16, if not NULL, receives a bfloat16 copy of the resulting dx. dgamma, dbeta and
+ * dx_colsum may be NULL. Workspace: np * C * P * 4 bytes, np = 3 with dx_colsum else 2,
+ * P <= 1216 partial slots (fewer for C > 1024). */
 gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, const float* mean,
                            const float* rstd, const float* dy, float* dx, int accumulate_dx,
-                           uint16_t* dx_bf16, float* dgamma, float* dbeta, int64_t rows, int C);
+                           uint16_t* dx_bf16, float* dgamma, float* dbeta, float* dx_colsum,
+                           int64_t rows, int C);
 
 /* LayerNorm backward that allocates nothing (no counterpart on the pages: it serves callers
  * that cannot allocate device memory). Same arguments, layout and results as
- * gk_layernorm_bwd, but it takes a CUDA stream (cudaStream_t, NULL = legacy default) instead
+ * gk_layernorm_bwd without dx_colsum, but it takes a CUDA stream (cudaStream_t, NULL = legacy default) instead
  * of a context, and its dgamma/dbeta partial sums live in a fixed 4 MiB array compiled into
  * the library rather than in a workspace.
  *   Who needs it: code that cannot call cudaMalloc, e.g. a host framework that owns all device

@@ -126,10 +126,11 @@ def test_layernorm_bwd(gkctx, rows, C, acc):
     _, rm, rr = ops.layernorm_fwd(x, gm, bt)
     dx0 = normal(314, rows, C)
     dg0, db0 = normal(315, C), normal(316, C)
-    dx, dgm, dbt = dev(dx0), dev(dg0), dev(db0)
+    ds0 = normal(317, C)
+    dx, dgm, dbt, dsum = dev(dx0), dev(dg0), dev(db0), dev(ds0)
     dxb = torch.empty(rows, C, device="cuda", dtype=torch.bfloat16)
     gk.gk_layernorm_bwd(gkctx, dev(x), dev(gm), dev(rm.astype(np.float32)), dev(rr.astype(np.float32)), dev(g), dx,
-                        acc, dxb, dgm, dbt, rows, C)
+                        acc, dxb, dgm, dbt, rows, C, dx_colsum=dsum)
     gk.gk_sync(gkctx)
     rdx, rdg, rdb = ops.layernorm_bwd(x, gm, rm.astype(np.float32), rr.astype(np.float32), g)
     if acc:
@@ -138,6 +139,8 @@ def test_layernorm_bwd(gkctx, rows, C, acc):
     assert rel_l2(host(dxb), host(dx)) < 5e-3
     assert rel_l2(host(dgm), rdg + dg0) < 1e-5
     assert rel_l2(host(dbt), rdb + db0) < 1e-5
+    # the column sums of the resulting dx (a bias gradient): the oracle's bias backward of dx
+    assert rel_l2(host(dsum), ops.bias_bwd(rdx) + ds0) < 1e-5
 
 
 # ---------------------------------------------------------------------------- GELU

@@ -42,7 +42,25 @@ struct Gemm {
     const void* B_lo = nullptr;
     // > 0 with bf16 C: C's low plane (v - bf16(v)) is also written, at C + c_plane elements
     int64_t c_plane = 0;
+    // Softmax cross-entropy fused into a vocabulary-projection epilogue (tensor-core kernel,
+    // TMA epilogue only). Column n of this GEMM is vocabulary entry ce_col0 + n, and
+    // ce_tgt[m] is row m's target entry.
+    //   CE_LSE: C is not written; per row and (256-column tile, column half) the epilogue
+    //     leaves (max, sum of 2^(v log2 e - max)) in ce_part[m * ce_nparts + 2 * tile + half]
+    //     (max in log2 units) and the target's logit in ce_tgt_logit[m].
+    //   CE_DLOGITS: C (bf16) = (*ce_dloss * ce_scale) * (exp(v - ce_lse[m]) - [n == target]).
+    int ce_mode = 0;
+    const int32_t* ce_tgt = nullptr;
+    int64_t ce_col0 = 0;
+    float2* ce_part = nullptr;
+    int ce_nparts = 0;
+    float* ce_tgt_logit = nullptr;
+    const float* ce_lse = nullptr;
+    const float* ce_dloss = nullptr;
+    float ce_scale = 1.f;
 };
+
+enum CeMode { CE_NONE = 0, CE_LSE = 1, CE_DLOGITS = 2 };
 
 // CUDA-core (SIMT) kernel: float32 or bfloat16 operands, float32 FMA accumulation.
 gk_status gemm_simt(gk_ctx* ctx, const Gemm& g);

@@ -69,6 +69,15 @@ struct TcParams {
     int reduce_out;   // C += v by TMA reduce-add (float32 C)
     int out_aux;      // GELU: the pre-activation plane is stored too
     int out_lo;       // bf16 C: its low plane is stored too
+    // fused softmax cross-entropy (see Gemm::ce_mode)
+    int ce_mode, ce_nparts;
+    int64_t ce_col0;
+    const int32_t* ce_tgt;
+    float2* ce_part;
+    float* ce_tgt_logit;
+    const float* ce_lse;
+    const float* ce_dloss;
+    float ce_scale;
     int* err;
 };
 
@@ -92,6 +101,8 @@ __device__ __forceinline__ float gelu_grad_hw(float x) {
     float t = tanh_hw(k * (x + 0.044715f * x * x * x));
     return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * x * x);
 }
+
+constexpr float LOG2E_F = 1.4426950408889634f;
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
@@ -430,6 +441,16 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
                 tma_prefetch_l2_2d(mp.in, tn2 * BN + half * (BN / 2) + c * W, tm2 * BM + q * 32);
         }
         const int y = tm * BM + q * 32;
+        // fused cross-entropy: this lane's row (y + lane) state over the tile's columns
+        float ce_m = -INFINITY, ce_s = 0.f, ce_l2 = 0.f, ce_g = 0.f;
+        int ce_t = -1;
+        if (p.ce_mode != CE_NONE && y + lane < p.M) {
+            ce_t = p.ce_tgt[y + lane];
+            if (p.ce_mode == CE_DLOGITS) {
+                ce_l2 = p.ce_lse[y + lane] * LOG2E_F;
+                ce_g = (p.ce_dloss ? *p.ce_dloss : 1.f) * p.ce_scale;
+            }
+        }
         for (int ch = 0; ch < nch; ++ch, ++g) {
             const int x = tn * BN + half * (BN / 2) + ch * W;
             const uint32_t s = g & 1;
@@ -472,6 +493,43 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
             tmem_wait_ld(r);
 #pragma unroll
             for (int i = 0; i < W; ++i) v[i] += __uint_as_float(r[i]);
+
+            if (p.ce_mode == CE_LSE) {
+                // online log-sum-exp of this row over its valid columns (log2 units), and the
+                // target's logit when it falls in this chunk
+                const int nv = min(W, p.N - x);
+                float cm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < W; ++i)
+                    if (i < nv) cm = fmaxf(cm, v[i] * LOG2E_F);
+                if (cm > ce_m) {
+                    ce_s *= ex2_hw(ce_m - cm);
+                    ce_m = cm;
+                }
+                float cs = 0.f;
+#pragma unroll
+                for (int i = 0; i < W; ++i)
+                    if (i < nv) cs += ex2_hw(fmaf(v[i], LOG2E_F, -ce_m));
+                ce_s += cs;
+                const int64_t tc = (int64_t)ce_t - p.ce_col0 - x;
+                if (tc >= 0 && tc < nv) {
+                    float tv = v[0];
+#pragma unroll
+                    for (int i = 1; i < W; ++i)
+                        if (i == tc) tv = v[i];
+                    p.ce_tgt_logit[y + lane] = tv;
+                }
+                continue;
+            }
+            if (p.ce_mode == CE_DLOGITS) {
+                // (dloss / rows) * (softmax - one-hot) of this row's logits
+                const int64_t tc = (int64_t)ce_t - p.ce_col0 - x;
+#pragma unroll
+                for (int i = 0; i < W; ++i) {
+                    const float pr = ex2_hw(fmaf(v[i], LOG2E_F, -ce_l2));
+                    v[i] = ce_g * (pr - (i == tc ? 1.f : 0.f));
+                }
+            }
 
             if (has_in) {
                 if (!__all_sync(0xffffffffu, mbar_wait(&inbar[s], (g >> 1) & 1, abort_flag, WAIT_NS))) {
@@ -560,6 +618,8 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
                 }
             }
         }
+        if (p.ce_mode == CE_LSE && ok && y + lane < p.M)
+            p.ce_part[(int64_t)(y + lane) * p.ce_nparts + 2 * tn + half] = make_float2(ce_m, ce_s);
         tc_fence_before();
         mbar_arrive(&tempty[buf]);
     }
@@ -832,6 +892,16 @@ void launch_split(gk_ctx* ctx, int split, int grid, const Maps& m, const TcParam
 // (C, the GELU pre-activation, the residual, C's low plane) has C's element type, 16-byte
 // aligned bases and strides, and at most one plane is read.
 bool setup_tma_epilogue(const Gemm& g, TcParams& p, Maps& m) {
+    if (g.ce_mode == CE_LSE) {  // nothing is stored through TMA; rows and columns come from the tile
+        p.reduce_out = p.out_aux = p.out_lo = 0;
+        p.in_kind = IN_NONE;
+        return g.ce_tgt && g.ce_part && g.ce_tgt_logit && !g.bias && !g.residual && g.epi == EPI_NONE &&
+               !g.accumulate && !g.c_plane;
+    }
+    if (g.ce_mode == CE_DLOGITS &&
+        (g.c_dtype != GK_BF16 || !g.ce_tgt || !g.ce_lse || g.bias || g.residual || g.epi != EPI_NONE ||
+         g.accumulate || g.c_plane))
+        return false;
     const bool bf = g.c_dtype == GK_BF16;
     if (g.c_dtype != GK_BF16 && g.c_dtype != GK_F32) return false;
     const int esz = bf ? 2 : 4, W = 64 / esz;
@@ -920,7 +990,24 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
         return GK_ERR_UNSUPPORTED;
     if (g.B_lo && !(g.b_kmajor ? make_map(&m.bl, g.B_lo, g.K, g.N, g.ldb, BN) : make_map(&m.bl, g.B_lo, g.N, g.K, g.ldb, 64)))
         return GK_ERR_UNSUPPORTED;
+    p.ce_mode = g.ce_mode;
+    p.ce_nparts = g.ce_nparts;
+    p.ce_col0 = g.ce_col0;
+    p.ce_tgt = g.ce_tgt;
+    p.ce_part = g.ce_part;
+    p.ce_tgt_logit = g.ce_tgt_logit;
+    p.ce_lse = g.ce_lse;
+    p.ce_dloss = g.ce_dloss;
+    p.ce_scale = g.ce_scale;
+    if (g.ce_mode == CE_LSE) {
+        m.c = m.aux = m.r = m.lo = ta;
+        p.tma_epi = setup_tma_epilogue(g, p, m);
+        if (!p.tma_epi) return GK_ERR_UNSUPPORTED;
+        launch_split<__nv_bfloat16>(ctx, split, grid, m, p);  // 32-column chunks; nothing is stored
+        return launched(ctx, "gemm_tc");
+    }
     p.tma_epi = setup_tma_epilogue(g, p, m);
+    if (!p.tma_epi && g.ce_mode != CE_NONE) return GK_ERR_UNSUPPORTED;
     if (!p.tma_epi) {
         m.c = m.aux = m.r = m.lo = ta;
         p.in_kind = IN_NONE;

@@ -61,6 +61,8 @@ _SIGS = {
     "gk_embedding_fwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_embedding_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32]),
+    "gk_lmhead_ce_fwd": (I32, [P, I32, P, I64, P, I64, P, P, P, I64, I64, I64]),
+    "gk_lmhead_ce_bwd": (I32, [P, I32, P, I64, P, I64, P, P, P, P, I64, I32, P, I64, P, I64, I64, I64, I64]),
     "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, P, I64, I32]),
     "gk_layernorm_bwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
     "gk_gelu_fwd": (I32, [P, P, P, I64]),
@@ -222,6 +224,18 @@ def gk_softmax_ce_fwd(ctx, logits, ldl, targets, loss, lse, rows, V):
 def gk_softmax_ce_bwd(ctx, logits, ldl, targets, lse, dloss, dlogits, lddl, dl_dtype, rows, V):
     return _check(ctx, _lib.gk_softmax_ce_bwd(ctx.handle, _p(logits), ldl, _p(targets), _p(lse), _p(dloss),
                                               _p(dlogits), lddl, dl_dtype, rows, V), "gk_softmax_ce_bwd")
+
+
+def gk_lmhead_ce_fwd(ctx, dtype, X, ldx, W, ldw, targets, loss, lse, N, C, V):
+    return _check(ctx, _lib.gk_lmhead_ce_fwd(ctx.handle, dtype, _p(X), ldx, _p(W), ldw, _p(targets), _p(loss), _p(lse),
+                                             N, C, V), "gk_lmhead_ce_fwd")
+
+
+def gk_lmhead_ce_bwd(ctx, dtype, X, ldx, W, ldw, targets, lse, dloss, dX, lddx, accumulate_dX, dW, lddw, scratch,
+                     scratch_elems, N, C, V):
+    return _check(ctx, _lib.gk_lmhead_ce_bwd(ctx.handle, dtype, _p(X), ldx, _p(W), ldw, _p(targets), _p(lse),
+                                             _p(dloss), _p(dX), lddx, int(accumulate_dX), _p(dW), lddw, _p(scratch),
+                                             scratch_elems, N, C, V), "gk_lmhead_ce_bwd")
 
 
 def gk_to_bf16(ctx, x, y, n, y_lo=None):

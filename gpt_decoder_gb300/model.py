@@ -36,9 +36,14 @@ def pad_vocab(V: int, mult: int = 64) -> int:
 
 
 class Gpt:
-    def __init__(self, ctx: gk.Ctx, V, T, C, H, L, B, mode="fp32", device="cuda", hi_layers=2):
+    def __init__(self, ctx: gk.Ctx, V, T, C, H, L, B, mode="fp32", device="cuda", hi_layers=2, fused_head=None):
         assert mode in ("fp32", "bf16")
         self.ctx, self.mode, self.device = ctx, mode, device
+        # bf16 mode: the LM head and the cross-entropy run fused (gk_lmhead_ce_*), with no
+        # [N, V] logits tensor; fused_head=False keeps the separate head GEMM and CE kernels
+        # (and self.logits) as in fp32 mode
+        self.fused_head = (mode == "bf16") if fused_head is None else bool(fused_head)
+        assert not self.fused_head or mode == "bf16", "the fused head takes bf16 operands"
         self.V, self.T, self.C, self.H, self.L, self.B = V, T, C, H, L, B
         self.hs = C // H
         self.N = B * T
@@ -88,11 +93,17 @@ class Gpt:
         self.lnf = torch.empty(N, C, dtype=adt, device=device)
         self.muf = torch.empty(N, **f32)
         self.rsf = torch.empty(N, **f32)
-        self.logits = torch.empty(N, self.Vp, **f32)
+        self.logits = None if self.fused_head else torch.empty(N, self.Vp, **f32)
         self.lse_ce = torch.empty(N, **f32)
         self.loss = torch.zeros(1, **f32)
-        # backward buffers
-        self.dlogits = torch.empty(N, self.Vp, dtype=adt, device=device)
+        # backward buffers; with the fused head dlogits is the scratch for one vocabulary chunk
+        # (up to 16384 columns, the chunks balanced)
+        if self.fused_head:
+            n_chunks = -(-V // 16384)
+            self.head_chunk = -(-(-(-V // n_chunks)) // 256) * 256
+            self.dlogits = torch.empty(N * self.head_chunk, dtype=torch.bfloat16, device=device)
+        else:
+            self.dlogits = torch.empty(N, self.Vp, dtype=adt, device=device)
         self.dx = torch.empty(N, C, **f32)
         self.dx_bf16 = torch.empty(N, C, dtype=torch.bfloat16, device=device) if mode == "bf16" else None
         self.dln = torch.empty(N, C, **f32)
@@ -213,6 +224,10 @@ class Gpt:
                          gk.GK_ACT_NONE, None, 0, lo(self.h[l]), wl(gk.GK_T_MLPPROJ_W))
         gk.gk_layernorm_fwd(c, self.xs[-1], self.w(gk.GK_T_LNF_W), self.w(gk.GK_T_LNF_B), self.lnf, self.dt, self.muf,
                             self.rsf, N, C, EPS)
+        if self.fused_head:
+            self._timed(gk.gk_lmhead_ce_fwd, (c, self.dt, self.lnf, C, self.w(gk.GK_T_WTE, 0, True), C, targets,
+                                              self.loss, self.lse_ce, N, C, self.V), 2.0 * N * C * self.V)
+            return self.loss
         self._mm_fwd(c, self.dt, self.lnf, C, self.w(gk.GK_T_WTE, 0, True), C, 1, None, None, 0, self.logits,
                          self.Vp, gk.GK_F32, N, C, self.V)
         gk.gk_softmax_ce_fwd(c, self.logits, self.Vp, targets, self.loss, self.lse_ce, N, self.V)
@@ -221,11 +236,19 @@ class Gpt:
     def backward(self, ids, targets):
         """Parameter gradients ADDED into self.grads (zero them first, or let AdamW do it)."""
         c, dt, N, C, H, hs, B, T = self.ctx, self.dt, self.N, self.C, self.H, self.hs, self.B, self.T
-        gk.gk_softmax_ce_bwd(c, self.logits, self.Vp, targets, self.lse_ce, None, self.dlogits, self.Vp, self.dt, N,
-                             self.V)
-        # tied head: dlnf = dlogits wte; dwte += dlogits^T lnf
-        self._mm_bwd(c, self.dt, self.lnf, C, self.w(gk.GK_T_WTE, 0, True), C, 1, self.dlogits, self.Vp, self.dln, C,
-                         gk.GK_F32, 0, None, 0, self.g(gk.GK_T_WTE), C, None, N, C, self.V)
+        if self.fused_head:
+            # dlnf = dlogits wte, dwte += dlogits^T lnf, the logits recomputed per vocabulary chunk
+            # (the timed FLOPs count the two products only)
+            self._timed(gk.gk_lmhead_ce_bwd, (c, self.dt, self.lnf, C, self.w(gk.GK_T_WTE, 0, True), C, targets,
+                                              self.lse_ce, None, self.dln, C, 0, self.g(gk.GK_T_WTE), C,
+                                              self.dlogits, self.dlogits.numel(), N, C, self.V),
+                        4.0 * N * C * self.V)
+        else:
+            gk.gk_softmax_ce_bwd(c, self.logits, self.Vp, targets, self.lse_ce, None, self.dlogits, self.Vp, self.dt,
+                                 N, self.V)
+            # tied head: dlnf = dlogits wte; dwte += dlogits^T lnf
+            self._mm_bwd(c, self.dt, self.lnf, C, self.w(gk.GK_T_WTE, 0, True), C, 1, self.dlogits, self.Vp, self.dln,
+                         C, gk.GK_F32, 0, None, 0, self.g(gk.GK_T_WTE), C, None, N, C, self.V)
         # the LayerNorm backwards also leave the column sums of the residual gradient they
         # produce: the bias gradients of the projections whose output gradient it is
         gk.gk_layernorm_bwd(c, self.xs[-1], self.w(gk.GK_T_LNF_W), self.muf, self.rsf, self.dln, self.dx, 0,

@@ -220,6 +220,35 @@ gk_status gk_softmax_ce_bwd(gk_ctx* ctx, const float* logits, int64_t ldl, const
                             const float* lse, const float* dloss, void* dlogits, int64_t lddl,
                             int dl_dtype, int64_t rows, int V);
 
+/* LM head fused with softmax cross-entropy: the tied projection logits = X W^T ([LM4]
+ * "... running GPT-2 weights", the output head reuses wte) and the loss of [LM1]
+ * "Ops...", SoftmaxCrossEntropy, without a [N, V] logits tensor.
+ *   X  bf16 [N, C] (row stride ldx), W bf16 [V, C] (row stride ldw; row v = vocabulary
+ *   entry v), targets int32 [N] in [0, V).
+ * gk_lmhead_ce_fwd: *loss = mean_r (lse_r - logit[r, targets[r]]) (float32 device scalar),
+ *   lse [N] = per-row natural log-sum-exp of the logits (saved for backward). Logits come
+ *   from bf16 operands with float32 accumulation. A target outside [0, V) contributes 0 and
+ *   records GK_ERR_INDEX (read back by gk_sync). Workspace: N * (8 * ceil(V / 256) * 2 + 8)
+ *   bytes (rounded up), e.g. 52 MB at N = 16384, V = 50257.
+ * gk_lmhead_ce_bwd: with g = *dloss (1 if dloss is NULL) and
+ *   dlogits = (g / N) (softmax(logits) - onehot(targets)):
+ *   dX (=, or += if accumulate_dX) dlogits W (float32 [N, C], stride lddx; may be NULL);
+ *   dW += dlogits^T X (float32 [V, C], stride lddw; may be NULL).
+ *   The logits are recomputed per vocabulary chunk and turned into bf16 dlogits in the
+ *   caller's scratch (bf16, scratch_elems elements, device memory the caller owns); the
+ *   chunk is the largest multiple of 256 columns with N * chunk <= scratch_elems, at least
+ *   256 (else GK_ERR_WORKSPACE).
+ * Both need 16-byte aligned operands with row strides a multiple of 8 elements
+ * (GK_ERR_ALIGN otherwise) and dtype GK_BF16 (GK_ERR_UNSUPPORTED otherwise). */
+gk_status gk_lmhead_ce_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W,
+                           int64_t ldw, const int32_t* targets, float* loss, float* lse, int64_t N,
+                           int64_t C, int64_t V);
+gk_status gk_lmhead_ce_bwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, const void* W,
+                           int64_t ldw, const int32_t* targets, const float* lse,
+                           const float* dloss, float* dX, int64_t lddx, int accumulate_dX,
+                           float* dW, int64_t lddw, void* scratch, int64_t scratch_elems,
+                           int64_t N, int64_t C, int64_t V);
+
 /* Round float32 [n] to bfloat16 [n] (round to nearest even): the bf16 operand copy of a
  * float32 tensor, e.g. the weights before the first step (AdamW refreshes it afterwards).
  * y_lo, if not NULL, receives the low plane bf16(x - y) of the split-bf16 form. */

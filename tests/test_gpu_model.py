@@ -1,7 +1,8 @@
 """Whole training-step parity (forward, backward, AdamW) of the libgk driver against the oracle.
 
-Workloads: the tiny character model (V=64, T=64, C=96, H=4, L=4, B=8, seed 0) in both modes,
-and the GPT-2-124M shape (B=4, T=1024, seed 2) in both modes. Tolerances: faithful (fp32)
+Workloads: the tiny character model (V=64, T=64, C=96, H=4, L=4, B=8, seed 0), a ragged shape
+and the GPT-2-124M shape (B=4, T=1024, seed 2), each in fp32, bf16 with the separate LM head and
+CE kernels, and bf16 with the fused LM head + CE (no logits tensor: loss, gradients, update). Tolerances: faithful (fp32)
 logits max-abs <= 5e-4, gradient relative-L2 <= 1e-4 per tensor; fast (bf16) logits
 max-abs <= 2e-2, gradient relative-L2 <= 1e-2.
 """
@@ -14,7 +15,9 @@ from tests.conftest import rel_l2
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"fp32": dict(logits=5e-4, grad=1e-4), "bf16": dict(logits=2e-2, grad=1e-2)}
+TOL = {"fp32": dict(logits=5e-4, grad=1e-4), "bf16": dict(logits=2e-2, grad=1e-2),
+       "bf16-fused": dict(logits=2e-2, grad=1e-2)}
+MODES = ["fp32", "bf16", "bf16-fused"]
 LR, WD = 3e-4, 0.01
 
 
@@ -24,12 +27,14 @@ def _run_step(gkctx, s, B, seed, mode):
     from gpt_decoder_gb300.model import Gpt
 
     ids, targets, params = synth.training_case(s, B, seed)
-    m = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, B, mode=mode)
+    # "bf16-fused": the fused LM head + cross-entropy (no logits tensor); "bf16": the separate
+    # head GEMM and CE kernels, whose logits are checked
+    m = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, B, mode=mode.split("-")[0], fused_head=mode == "bf16-fused")
     m.load(params)
     d_ids = torch.as_tensor(ids.reshape(-1)).cuda()
     d_tg = torch.as_tensor(targets.reshape(-1)).cuda()
     loss = m.forward(d_ids, d_tg)
-    logits = m.logits[:, : s.V].cpu().numpy()
+    logits = None if m.logits is None else m.logits[:, : s.V].cpu().numpy()
     m.backward(d_ids, d_tg)
     from gpt_decoder_gb300 import gk
 
@@ -53,7 +58,8 @@ def _oracle(s, inputs):
 def _compare(got, ref, mode):
     tol = TOL[mode]
     assert abs(got["loss"] - ref["loss"]) < tol["logits"], (got["loss"], ref["loss"])
-    assert np.abs(got["logits"] - ref["logits"]).max() <= tol["logits"]
+    if got["logits"] is not None:
+        assert np.abs(got["logits"] - ref["logits"]).max() <= tol["logits"]
     worst = max((rel_l2(got["grads"][k], ref["grads"][k]), k) for k in ref["grads"])
     assert worst[0] <= tol["grad"], worst
     # AdamW after one step: m_hat / sqrt(v_hat) = g / (|g| + eps), i.e. the sign of g once
@@ -71,7 +77,7 @@ def _compare(got, ref, mode):
     return worst, flips
 
 
-@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+@pytest.mark.parametrize("mode", MODES)
 def test_tiny_training_step(gkctx, mode):
     s = synth.TINY
     got = _run_step(gkctx, s, 8, 0, mode)
@@ -81,7 +87,7 @@ def test_tiny_training_step(gkctx, mode):
           f"small-gradient sign flips {flips}")
 
 
-@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+@pytest.mark.parametrize("mode", MODES)
 def test_ragged_shapes_step(gkctx, mode):
     # vocabulary, context and width that leave partial tiles everywhere
     s = synth.GptShape(V=50, T=37, C=64, H=2, L=2)
@@ -94,7 +100,7 @@ _GPT2_ORACLE = {}
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+@pytest.mark.parametrize("mode", MODES)
 def test_gpt2_124m_training_step(gkctx, mode):
     s = synth.GPT2_124M
     got = _run_step(gkctx, s, 4, 2, mode)
@@ -102,8 +108,9 @@ def test_gpt2_124m_training_step(gkctx, mode):
         _GPT2_ORACLE["ref"] = _oracle(s, got["inputs"])
     ref = _GPT2_ORACLE["ref"]
     worst, flips = _compare(got, ref, mode)
-    print(f"gpt2 {mode}: loss {got['loss']:.6f} vs {ref['loss']:.6f}; max |dlogits| "
-          f"{np.abs(got['logits'] - ref['logits']).max():.3e}; worst grad {worst}; flips {flips}")
+    dl = "n/a" if got["logits"] is None else f"{np.abs(got['logits'] - ref['logits']).max():.3e}"
+    print(f"gpt2 {mode}: loss {got['loss']:.6f} vs {ref['loss']:.6f}; max |dlogits| {dl}; worst grad {worst}; "
+          f"flips {flips}")
 
 
 def test_loss_decreases_over_steps(gkctx):

@@ -396,6 +396,65 @@ def test_softmax_ce(gkctx, rows, V, ldl, dl_dt):
     assert np.all(got[:, V:] == 0)
 
 
+# ------------------------------------------------------- fused LM head + cross-entropy
+@pytest.mark.parametrize("N,C,V", [(300, 96, 50), (512, 128, 1000), (77, 64, 513), (1024, 768, 50257)])
+def test_lmhead_ce_fused(gkctx, N, C, V):
+    """Loss, LSE, dX and dW of the fused head against the oracle's MatMulT + SoftmaxCE, with
+    the backward both in one vocabulary chunk and in chunks of 256 columns."""
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    seed = 1300 + V
+    x = bf16_round(normal(seed, N, C))
+    w = bf16_round(normal(seed + 1, V, C) * 0.5)
+    tg = synth.Stream(seed + 2).ints(N, V).astype(np.int32)
+    dloss = 1.7
+    logits = ops.matmul_t_fwd(x, w)
+    rloss, rlse = ops.softmax_ce_fwd(logits, tg)
+    rdl = ops.softmax_ce_bwd(logits, tg, rlse, dloss)
+    rdx, rdw = ops.matmul_t_bwd(x, w, rdl)
+    bf = torch.bfloat16
+    dx_, w_, t_ = dev(x, bf), dev(w, bf), dev(tg)
+    loss = torch.empty(1, device="cuda")
+    lse = torch.empty(N, device="cuda")
+    gk.gk_lmhead_ce_fwd(gkctx, gk.GK_BF16, dx_, C, w_, C, t_, loss, lse, N, C, V)
+    gk.gk_sync(gkctx)
+    assert abs(loss.item() - rloss) < 1e-4 * max(1.0, abs(rloss))
+    assert np.abs(host(lse) - rlse).max() < 1e-4 * max(1.0, np.abs(rlse).max())
+    dl = dev(np.array([dloss], dtype=np.float32))
+    dx0, dw0 = normal(seed + 3, N, C), normal(seed + 4, V, C)
+    for scratch_cols in (V + 300, 256):
+        dx, dw = dev(dx0), dev(dw0)
+        scratch = torch.empty(N * scratch_cols, dtype=bf, device="cuda")
+        gk.gk_lmhead_ce_bwd(gkctx, gk.GK_BF16, dx_, C, w_, C, t_, lse, dl, dx, C, 1, dw, C, scratch, N * scratch_cols,
+                            N, C, V)
+        gk.gk_sync(gkctx)
+        # dlogits pass through bf16 once: about 2^-9 relative
+        assert rel_l2(host(dx) - dx0, rdx) < 5e-3, scratch_cols
+        assert rel_l2(host(dw) - dw0, rdw) < 5e-3, scratch_cols
+
+
+def test_lmhead_ce_reports_bad_target_and_small_scratch(gkctx):
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    N, C, V = 64, 64, 300
+    x = dev(bf16_round(normal(1400, N, C)), torch.bfloat16)
+    w = dev(bf16_round(normal(1401, V, C)), torch.bfloat16)
+    tg = np.zeros(N, dtype=np.int32)
+    tg[5] = V
+    loss, lse = torch.empty(1, device="cuda"), torch.empty(N, device="cuda")
+    gk.gk_lmhead_ce_fwd(gkctx, gk.GK_BF16, x, C, w, C, dev(tg), loss, lse, N, C, V)
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_sync(gkctx)
+    assert e.value.status == gk.GK_ERR_INDEX
+    scratch = torch.empty(N * 255, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_lmhead_ce_bwd(gkctx, gk.GK_BF16, x, C, w, C, dev(np.zeros(N, np.int32)), lse, None, None, C, 0, None, C,
+                            scratch, N * 255, N, C, V)
+    assert e.value.status == gk.GK_ERR_WORKSPACE
+
+
 def test_softmax_ce_in_place(gkctx):
     from gpt_decoder_gb300 import gk
 

@@ -278,34 +278,42 @@ def run_ours(args):
     print(json.dumps(out))
 
 
-def bench_decode(ctx, m, s, Tp=512, n_steps=64):
-    """Greedy KV-cache decode tok/s (fp32 weights) at batch 1 and 16 after a 512-token prompt."""
+def bench_decode(ctx, m, s, Tp=512, n_steps=256):
+    """Greedy KV-cache decode tok/s (fp32 weights) at batch 1 and 16: a 512-token prompt, then
+    n_steps decode steps timed (prefill excluded), each step one replay of the captured step
+    graph (gk_decode_run) on a stream of its own."""
     import torch
 
     from gpt_decoder_gb300 import gk
 
     res = {}
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
+    dctx = gk.Ctx(stream, workspace_bytes=64 << 20)
+    torch.cuda.synchronize()
+    warm = 8
     for B in (1, 16):
-        kv = gk.KvCache(ctx, m.cfg, B, Tp + n_steps + 1)
-        prompt = torch.randint(0, s.V, (B * Tp,), dtype=torch.int32, device="cuda")
-        logits = torch.empty(B, s.V, device="cuda")
-        nxt = torch.empty(B, dtype=torch.int32, device="cuda")
-        gk.gk_prefill(ctx, m.params, kv, prompt, Tp, logits)
-        gk.gk_sample(ctx, kv, logits, s.V, nxt, None)
-        tok = nxt.clone()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_steps):
-            gk.gk_decode_step(ctx, m.params, kv, tok, logits, tok, None)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        gk.gk_sync(ctx)
+        with torch.cuda.stream(stream):
+            kv = gk.KvCache(dctx, m.cfg, B, Tp + warm + n_steps)
+            prompt = torch.randint(0, s.V, (B * Tp,), dtype=torch.int32, device="cuda")
+            logits = torch.empty(B, s.V, device="cuda")
+            tok = torch.empty(B, dtype=torch.int32, device="cuda")
+            gk.gk_prefill(dctx, m.params, kv, prompt, Tp, logits)
+            gk.gk_sample(dctx, kv, logits, s.V, tok, None)
+            gk.gk_decode_run(dctx, m.params, kv, tok, logits, tok, warm)  # records the step graph
+            l0 = gk.gk_launch_count(dctx)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            stream.synchronize()
+            e0.record(stream)
+            gk.gk_decode_run(dctx, m.params, kv, tok, logits, tok, n_steps)
+            e1.record(stream)
+        stream.synchronize()
+        gk.gk_sync(dctx)
         ms = e0.elapsed_time(e1)
         res[f"B{B}"] = {"tok_s": B * n_steps / (ms / 1e3), "ms_per_step": ms / n_steps, "prompt": Tp,
-                        "steps": n_steps, "dtype": "f32"}
+                        "steps": n_steps, "dtype": "f32", "launches_per_step": (gk.gk_launch_count(dctx) - l0) / n_steps,
+                        "launch": "CUDA graph per step"}
         kv.close()
+    dctx.close()
     return res
 
 

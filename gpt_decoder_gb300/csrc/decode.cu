@@ -25,6 +25,12 @@ struct gk_kv {
     float* partial = nullptr;  // split-K partial sums
     size_t partial_floats = 0;
     float* attn_part = nullptr;  // decode attention partials [B*H][chunks][hs + 2]
+    // gk_decode_run: one captured decode step (instantiated graph) and what it was captured for
+    cudaGraphExec_t graph = nullptr;
+    int64_t graph_launches = 0;
+    const void* graph_key[6] = {};
+    gk_sample_cfg graph_s{};
+    bool graph_has_s = false;
 };
 
 using namespace gk;
@@ -270,6 +276,11 @@ __global__ void gather_last_kernel(const float* __restrict__ x, int B, int Tp, i
     last[i] = x[((int64_t)b * Tp + Tp - 1) * C + c];
 }
 
+__global__ void copy_ids_kernel(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int n) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = src[i];
+}
+
 __global__ void set_state_kernel(int* state, int length, int selections) {
     state[0] = length;
     state[1] = selections;
@@ -504,6 +515,12 @@ struct W {
     const float* t(int which, int layer = 0) const { return p + gk_gpt_offset(&c, which, layer); }
 };
 
+void drop_graph(gk_kv* kv) {
+    if (kv->graph) cudaGraphExecDestroy(kv->graph);
+    kv->graph = nullptr;
+    kv->graph_launches = 0;
+}
+
 gk_status check_kv_args(gk_ctx* ctx, const float* params, gk_kv* kv) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, params && kv, GK_ERR_ARG, "decode: null params or cache");
@@ -564,6 +581,7 @@ gk_status gk_kv_create(gk_ctx* ctx, gk_kv** out, const gk_gpt_cfg* cfg, int B, i
 
 void gk_kv_destroy(gk_kv* kv) {
     if (!kv) return;
+    drop_graph(kv);
     float* ptrs[] = {kv->cache, kv->x, kv->ln, kv->qkv, kv->y, kv->pre, kv->h, kv->mean, kv->rstd, kv->lse, kv->last,
                      kv->partial, kv->attn_part};
     for (float* p : ptrs)
@@ -613,11 +631,14 @@ gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t*
     return GK_OK;
 }
 
-gk_status gk_decode_step(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t* tokens, float* logits,
-                         int32_t* next, const gk_sample_cfg* s) {
-    GK_TRY(check_kv_args(ctx, params, kv));
-    GK_REQUIRE(ctx, tokens && logits, GK_ERR_ARG, "gk_decode_step: bad argument");
-    GK_REQUIRE(ctx, kv->length < kv->Tmax, GK_ERR_OVERFLOW, "gk_decode_step: cache full (%d)", kv->Tmax);
+}  // extern "C"
+
+namespace {
+
+// The launches of one decode step (arguments checked by the caller); the host mirror of the
+// cache length is left to the caller.
+gk_status decode_step_launches(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t* tokens, float* logits,
+                               int32_t* next, const gk_sample_cfg* s) {
     const gk_gpt_cfg& c = kv->cfg;
     W w{params, c};
     int B = kv->B, C = c.C, H = c.H, hs = C / H;
@@ -660,8 +681,81 @@ gk_status gk_decode_step(gk_ctx* ctx, const float* params, gk_kv* kv, const int3
         dsel = 1;
     }
     advance_kernel<<<1, 1, 0, ctx->stream>>>(kv->state, 1, dsel);
-    GK_TRY(launched(ctx, "advance"));
+    return launched(ctx, "advance");
+}
+
+}  // namespace
+
+extern "C" {
+
+gk_status gk_decode_step(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t* tokens, float* logits,
+                         int32_t* next, const gk_sample_cfg* s) {
+    GK_TRY(check_kv_args(ctx, params, kv));
+    GK_REQUIRE(ctx, tokens && logits, GK_ERR_ARG, "gk_decode_step: bad argument");
+    GK_REQUIRE(ctx, kv->length < kv->Tmax, GK_ERR_OVERFLOW, "gk_decode_step: cache full (%d)", kv->Tmax);
+    GK_TRY(decode_step_launches(ctx, params, kv, tokens, logits, next, s));
     kv->length += 1;
+    return GK_OK;
+}
+
+gk_status gk_decode_run(gk_ctx* ctx, const float* params, gk_kv* kv, int32_t* tokens, float* logits, int32_t* next,
+                        const gk_sample_cfg* s, int n_steps) {
+    GK_TRY(check_kv_args(ctx, params, kv));
+    GK_REQUIRE(ctx, tokens && logits && next && n_steps >= 0, GK_ERR_ARG, "gk_decode_run: bad argument");
+    GK_REQUIRE(ctx, (int64_t)kv->length + n_steps <= kv->Tmax, GK_ERR_OVERFLOW,
+               "gk_decode_run: %d steps from length %d overflow the cache (%d)", n_steps, kv->length, kv->Tmax);
+    if (n_steps == 0) return GK_OK;
+    auto step = [&]() -> gk_status {
+        GK_TRY(decode_step_launches(ctx, params, kv, tokens, logits, next, s));
+        if (next != tokens) {
+            copy_ids_kernel<<<1, 32 * (int)cdiv(kv->B, 32), 0, ctx->stream>>>(next, tokens, kv->B);
+            GK_TRY(launched(ctx, "copy_ids"));
+        }
+        return GK_OK;
+    };
+    if (!ctx->stream) {  // the legacy default stream cannot be captured: plain launches
+        for (int i = 0; i < n_steps; ++i) {
+            GK_TRY(step());
+            kv->length += 1;
+        }
+        return GK_OK;
+    }
+    const void* key[6] = {params, tokens, logits, next, ctx->stream, ctx};
+    const bool same_s = (s != nullptr) == kv->graph_has_s &&
+                        (!s || (s->top_k == kv->graph_s.top_k && s->temperature == kv->graph_s.temperature &&
+                                s->seed == kv->graph_s.seed && s->counter == kv->graph_s.counter));
+    if (!kv->graph || !same_s || !std::equal(key, key + 6, kv->graph_key)) {
+        drop_graph(kv);
+        const int64_t l0 = ctx->launches;
+        if (cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeRelaxed) != cudaSuccess)
+            return fail(ctx, GK_ERR_CUDA, "gk_decode_run: stream capture failed to start");
+        gk_status st = step();
+        cudaGraph_t g = nullptr;
+        cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
+        const int64_t per_step = ctx->launches - l0;
+        ctx->launches = l0;  // captured, not run
+        if (st != GK_OK) {
+            if (g) cudaGraphDestroy(g);
+            return st;
+        }
+        if (e != cudaSuccess || !g) return fail(ctx, GK_ERR_CUDA, "gk_decode_run: capture failed: %s", cudaGetErrorString(e));
+        e = cudaGraphInstantiate(&kv->graph, g, 0);
+        cudaGraphDestroy(g);
+        if (e != cudaSuccess) {
+            kv->graph = nullptr;
+            return fail(ctx, GK_ERR_CUDA, "gk_decode_run: graph instantiation failed: %s", cudaGetErrorString(e));
+        }
+        kv->graph_launches = per_step;
+        std::copy(key, key + 6, kv->graph_key);
+        kv->graph_has_s = s != nullptr;
+        if (s) kv->graph_s = *s;
+    }
+    for (int i = 0; i < n_steps; ++i) {
+        cudaError_t e = cudaGraphLaunch(kv->graph, ctx->stream);
+        if (e != cudaSuccess) return fail(ctx, GK_ERR_CUDA, "gk_decode_run: graph launch failed: %s", cudaGetErrorString(e));
+        ctx->launches += kv->graph_launches;
+        kv->length += 1;
+    }
     return GK_OK;
 }
 

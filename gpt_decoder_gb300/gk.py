@@ -63,6 +63,7 @@ _SIGS = {
     "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32]),
     "gk_lmhead_ce_fwd": (I32, [P, I32, P, I64, P, I64, P, P, P, I64, I64, I64]),
     "gk_lmhead_ce_bwd": (I32, [P, I32, P, I64, P, I64, P, P, P, P, I64, I32, P, I64, P, I64, I64, I64, I64]),
+    "gk_decode_run": (I32, [P, P, P, P, P, P, P, I32]),
     "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, P, I64, I32]),
     "gk_layernorm_bwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
     "gk_gelu_fwd": (I32, [P, P, P, I64]),
@@ -310,6 +311,13 @@ def gk_decode_step(ctx, params, kv, tokens, logits, next_ids, sample=None):
     """sample: None (greedy) or (top_k, temperature, seed, counter)."""
     return _check(ctx, _lib.gk_decode_step(ctx.handle, _p(params), kv.handle, _p(tokens), _p(logits), _p(next_ids),
                                            _sample(sample)), "gk_decode_step")
+
+
+def gk_decode_run(ctx, params, kv, tokens, logits, next_ids, n_steps, sample=None):
+    """n_steps decode steps, each feeding its selection back through tokens (one captured step
+    replayed as a CUDA graph). sample: None (greedy) or (top_k, temperature, seed, counter)."""
+    return _check(ctx, _lib.gk_decode_run(ctx.handle, _p(params), kv.handle, _p(tokens), _p(logits), _p(next_ids),
+                                          _sample(sample), n_steps), "gk_decode_run")
 
 
 def gk_sample(ctx, kv, logits, ld, next_ids, sample=None):

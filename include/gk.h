@@ -335,6 +335,19 @@ gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t*
 gk_status gk_decode_step(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t* tokens,
                          float* logits, int32_t* next, const gk_sample_cfg* s);
 
+/* n_steps decode steps in a row, each one gk_decode_step(ctx, params, kv, tokens, logits,
+ * next, s) followed by copying next into tokens (skipped when they are the same buffer), so
+ * every step feeds the token just selected: [LM4] "Generation with a KV cache"
+ * (GenerateCached's loop). tokens and next are device int32 [B]; logits [B, V] holds the
+ * last step's logits. The first call for a given (params, tokens, logits, next, s values,
+ * stream) records one step as a CUDA graph kept with the cache; later calls replay it, one
+ * graph launch per step (on the legacy default stream, which cannot be captured, the steps
+ * are launched one by one). Results are those of the step-by-step calls. GK_ERR_OVERFLOW
+ * (nothing run) if the cache length plus n_steps exceeds Tmax; GK_ERR_ARG for null
+ * pointers or n_steps < 0. */
+gk_status gk_decode_run(gk_ctx* ctx, const float* params, gk_kv* kv, int32_t* tokens,
+                        float* logits, int32_t* next, const gk_sample_cfg* s, int n_steps);
+
 /* Select next [B] from logits [B, V] (stride ld) as gk_sample_cfg describes; the selection
  * index s is the cache's selection count, which this advances by one. */
 gk_status gk_sample(gk_ctx* ctx, gk_kv* kv, const float* logits, int64_t ld, int32_t* next,

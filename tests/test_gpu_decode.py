@@ -75,6 +75,69 @@ def test_gpt2_decode_teacher_forced(gkctx, B):
     assert mism == near
 
 
+@pytest.mark.parametrize("sample", [None, (5, 0.8, 11, 3)])
+def test_decode_run_matches_step_by_step(gkctx, sample):
+    """gk_decode_run (one captured step replayed as a graph) gives bit-identical logits,
+    selections and cache to gk_decode_step called step by step, across two runs (the second
+    replays the same graph), with tokens and next as one buffer or two."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    s, B, Tp, n1, n2 = synth.TINY, 3, 9, 6, 5
+    stream = torch.cuda.Stream()
+    ctx = gk.Ctx(stream, 64 << 20)
+    outs = []
+    for path in ("steps", "run-shared", "run-separate"):
+        prompt, params, m, kv = _setup(ctx, s, B, Tp, 7, Tp + n1 + n2)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            logits = torch.empty(B, s.V, device="cuda")
+            tok = torch.empty(B, dtype=torch.int32, device="cuda")
+            gk.gk_prefill(ctx, m.params, kv, torch.as_tensor(prompt.reshape(-1)).cuda(), Tp, logits)
+            gk.gk_sample(ctx, kv, logits, s.V, tok, sample)
+            seen = []
+            if path == "steps":
+                for i in range(n1 + n2):
+                    gk.gk_decode_step(ctx, m.params, kv, tok, logits, tok, sample)
+                    seen.append(tok.clone())
+            else:
+                nxt = tok if path == "run-shared" else torch.empty_like(tok)
+                for n in (n1, n2):
+                    gk.gk_decode_run(ctx, m.params, kv, tok, logits, nxt, n, sample)
+                    seen.append(nxt.clone())
+        gk.gk_sync(ctx)
+        assert kv.length() == Tp + n1 + n2
+        outs.append((logits.cpu().numpy(), tok.cpu().numpy(), [t.cpu().numpy() for t in seen]))
+        kv.close()
+    ref_logits, ref_tok, ref_seen = outs[0]
+    for got_logits, got_tok, got_seen in outs[1:]:
+        assert np.array_equal(got_logits, ref_logits)
+        assert np.array_equal(got_tok, ref_tok)
+        assert np.array_equal(got_seen[0], ref_seen[n1 - 1]) and np.array_equal(got_seen[1], ref_seen[-1])
+    ctx.close()
+
+
+def test_decode_run_overflow_runs_nothing(gkctx):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    s, B, Tp = synth.TINY, 2, 5
+    prompt, params, m, kv = _setup(gkctx, s, B, Tp, 7, Tp + 3)
+    logits = torch.empty(B, s.V, device="cuda")
+    tok = torch.zeros(B, dtype=torch.int32, device="cuda")
+    gk.gk_prefill(gkctx, m.params, kv, torch.as_tensor(prompt.reshape(-1)).cuda(), Tp, logits)
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_decode_run(gkctx, m.params, kv, tok, logits, tok, 4)
+    assert e.value.status == gk.GK_ERR_OVERFLOW
+    assert kv.length() == Tp
+    gk.gk_decode_run(gkctx, m.params, kv, tok, logits, tok, 3)
+    gk.gk_sync(gkctx)
+    assert kv.length() == Tp + 3
+    kv.close()
+
+
 def test_cached_decode_equals_training_forward(gkctx):
     """The GPU's cached path reproduces its own full causal forward (fp32)."""
     import torch

@@ -5,8 +5,11 @@
 //
 // Decode is bound by reading the weights once per step, so the per-token matrix products are
 // split-K GEMV kernels that stream each weight row once and reuse it for every batch row.
-// The cache position and the selection count live on the device, so a decode step is a
-// fixed sequence of launches that can be captured once in a CUDA graph and replayed.
+// A step is five launches per layer: the GEMVs apply the preceding LayerNorm to their input
+// rows themselves, and the last block of each column block adds the split-K slices (fixed
+// order) with bias, residual, GELU and the key/value append; the attention's last chunk block
+// combines the chunks. The cache position and the selection count live on the device, so a
+// decode step is a fixed sequence of launches that can be captured once in a CUDA graph.
 #include <math.h>
 
 #include <algorithm>
@@ -25,6 +28,7 @@ struct gk_kv {
     float* partial = nullptr;  // split-K partial sums
     size_t partial_floats = 0;
     float* attn_part = nullptr;  // decode attention partials [B*H][chunks][hs + 2]
+    int* tickets = nullptr;      // last-block tickets: [0, 1024) GEMV column blocks, [1024, 2048) attention
     // gk_decode_run: one captured decode step (instantiated graph) and what it was captured for
     cudaGraphExec_t graph = nullptr;
     int64_t graph_launches = 0;
@@ -41,33 +45,111 @@ constexpr int GEMV_THREADS = 256;  // 8 warps; a warp covers 128 columns (float4
 constexpr int GEMV_COLS = 128;
 constexpr int KCHUNK = 64;         // keys per decode-attention block
 
-// partial[s][b][n] = sum over k in slice s of X[b, k] W[k, n], for n in this block's columns.
+__device__ __forceinline__ int64_t cache_index(int l, int kv, int b, int h, int t, int B, int H, int Tmax, int hs) {
+    return ((((int64_t)(l * 2 + kv) * B + b) * H + h) * Tmax + t) * hs;
+}
+
+// Mean and rstd (biased variance, eps 1e-5) of rows b < B of X (K columns), one warp per
+// row, into st[2 * b], st[2 * b + 1]; the LayerNorm of [LM1]'s op table applied by the
+// kernels that consume its output.
+__device__ __forceinline__ void row_stats(const float* __restrict__ X, int64_t ldx, int B, int K, float* st) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int b = warp; b < B; b += nw) {
+        const float* xr = X + (int64_t)b * ldx;
+        float s = 0.f;
+        for (int k = lane; k < K; k += 32) s += xr[k];
+        const float mu = warp_sum(s) / K;
+        float v = 0.f;
+        for (int k = lane; k < K; k += 32) {
+            const float d = xr[k] - mu;
+            v += d * d;
+        }
+        v = warp_sum(v) / K;
+        if (lane == 0) {
+            st[2 * b] = mu;
+            st[2 * b + 1] = rsqrtf(v + 1e-5f);
+        }
+    }
+}
+
+struct GemvArgs {
+    const float* X;
+    int64_t ldx;
+    const float* ln_g;  // not null: the rows of X go through LayerNorm(ln_g, ln_b) first
+    const float* ln_b;
+    const float* W;
+    int64_t ldw;
+    int B, K, M, kslice;
+    float* partial;
+    int* tickets;
+    const float* bias;
+    const float* residual;
+    float* Y;
+    int64_t ldy;
+    int act;
+    float* preact;
+    // not null: columns [C, 3C) of Y (keys, values) are also appended to the cache at the
+    // device position state[0]
+    float* cache;
+    int layer, H, hs, Tmax;
+    const int* state;
+};
+
+// Split-K GEMV: block (column block, slice s) forms partial[s][b][n] = sum over k in slice s
+// of X'[b, k] W[k, n] (X' = X or its LayerNorm); the last block of a column block to finish
+// (atomic ticket) adds the slices in slice order and applies bias, residual, GELU and the
+// key/value append. No block waits on another.
 template <int NB>
-__global__ void __launch_bounds__(GEMV_THREADS) gemv_partial_kernel(const float* __restrict__ X, int64_t ldx,
-                                                                    const float* __restrict__ W, int64_t ldw, int B,
-                                                                    int K, int M, int kslice,
-                                                                    float* __restrict__ partial) {
-    extern __shared__ float sm[];  // Xs[NB][kslice] then red[8][NB][128]
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
+    extern __shared__ float sm[];  // Xs[NB][kslice], red[8][NB][128], st[2 * NB]
     float* Xs = sm;
-    float* red = sm + NB * kslice;
-    int s = blockIdx.y;
-    int k0 = s * kslice, k1 = min(K, k0 + kslice);
-    int n = blockIdx.x * GEMV_COLS + (threadIdx.x & 31) * 4;
-    int warp = threadIdx.x >> 5;
-    for (int e = threadIdx.x; e < NB * kslice; e += GEMV_THREADS) {
-        int b = e / kslice, k = k0 + e % kslice;
-        Xs[e] = (b < B && k < k1) ? X[(int64_t)b * ldx + k] : 0.f;
+    float* red = sm + NB * a.kslice;
+    float* st = red + 8 * NB * GEMV_COLS;
+    __shared__ int last;
+    const int s = blockIdx.y;
+    const int k0 = s * a.kslice, k1 = min(a.K, k0 + a.kslice);
+    const int n = blockIdx.x * GEMV_COLS + (threadIdx.x & 31) * 4;
+    const int warp = threadIdx.x >> 5;
+    if (a.ln_g) {
+        row_stats(a.X, a.ldx, a.B, a.K, st);
+        __syncthreads();
+    }
+    for (int e = threadIdx.x; e < NB * a.kslice; e += GEMV_THREADS) {
+        const int b = e / a.kslice, k = k0 + e % a.kslice;
+        float v = 0.f;
+        if (b < a.B && k < k1) {
+            v = a.X[(int64_t)b * a.ldx + k];
+            if (a.ln_g) v = (v - st[2 * b]) * st[2 * b + 1] * a.ln_g[k] + a.ln_b[k];
+        }
+        Xs[e] = v;
     }
     __syncthreads();
     float acc[NB][4];
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
-    if (n < M) {
-        for (int k = k0 + warp; k < k1; k += 8) {
-            float4 w = *reinterpret_cast<const float4*>(W + (int64_t)k * ldw + n);
+    if (n < a.M) {
+        // four weight rows in flight per warp (rows k, k + 8, k + 16, k + 24)
+        int k = k0 + warp;
+        for (; k + 24 < k1; k += 32) {
+            float4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) w[u] = *reinterpret_cast<const float4*>(a.W + (int64_t)(k + 8 * u) * a.ldw + n);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float xv = Xs[b * a.kslice + (k + 8 * u - k0)];
+                    acc[b][0] = fmaf(xv, w[u].x, acc[b][0]);
+                    acc[b][1] = fmaf(xv, w[u].y, acc[b][1]);
+                    acc[b][2] = fmaf(xv, w[u].z, acc[b][2]);
+                    acc[b][3] = fmaf(xv, w[u].w, acc[b][3]);
+                }
+        }
+        for (; k < k1; k += 8) {
+            const float4 w = *reinterpret_cast<const float4*>(a.W + (int64_t)k * a.ldw + n);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                float xv = Xs[b * kslice + (k - k0)];
+                const float xv = Xs[b * a.kslice + (k - k0)];
                 acc[b][0] = fmaf(xv, w.x, acc[b][0]);
                 acc[b][1] = fmaf(xv, w.y, acc[b][1]);
                 acc[b][2] = fmaf(xv, w.z, acc[b][2]);
@@ -75,69 +157,117 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_partial_kernel(const float*
             }
         }
     }
-    int col = (threadIdx.x & 31) * 4;
+    const int col = (threadIdx.x & 31) * 4;
 #pragma unroll
     for (int b = 0; b < NB; ++b)
 #pragma unroll
         for (int j = 0; j < 4; ++j) red[(warp * NB + b) * GEMV_COLS + col + j] = acc[b][j];
     __syncthreads();
     for (int e = threadIdx.x; e < NB * GEMV_COLS; e += GEMV_THREADS) {
-        int b = e / GEMV_COLS, c = e % GEMV_COLS;
-        int nn = blockIdx.x * GEMV_COLS + c;
-        if (b >= B || nn >= M) continue;
+        const int b = e / GEMV_COLS, c = e % GEMV_COLS;
+        const int nn = blockIdx.x * GEMV_COLS + c;
+        if (b >= a.B || nn >= a.M) continue;
         float t = 0.f;
         for (int w = 0; w < 8; ++w) t += red[(w * NB + b) * GEMV_COLS + c];
-        partial[((int64_t)s * B + b) * M + nn] = t;
+        a.partial[((int64_t)s * a.B + b) * a.M + nn] = t;
     }
-}
-
-// Y[b, n] = act(sum_s partial[s][b][n] + bias[n] + residual[b, n]) (slices in order).
-__global__ void gemv_finish_kernel(const float* __restrict__ partial, int S, int B, int M, const float* bias,
-                                   const float* residual, float* Y, int64_t ldy, int act, float* preact) {
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)B * M) return;
-    int b = (int)(i / M), n = (int)(i % M);
-    float t = 0.f;
-    for (int s = 0; s < S; ++s) t += partial[((int64_t)s * B + b) * M + n];
-    if (bias) t += bias[n];
-    if (residual) t += residual[(int64_t)b * ldy + n];
-    if (act == GK_ACT_GELU) {
-        if (preact) preact[(int64_t)b * M + n] = t;
-        t = gelu_tanh(t);
+    // the last slice of this column block to arrive finishes it
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&a.tickets[blockIdx.x], 1) == (int)gridDim.y - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const int pos = a.cache ? a.state[0] : 0;
+    const int C = a.H * a.hs;
+    for (int e = threadIdx.x; e < a.B * GEMV_COLS; e += GEMV_THREADS) {
+        const int b = e / GEMV_COLS, nn = blockIdx.x * GEMV_COLS + e % GEMV_COLS;
+        if (nn >= a.M) continue;
+        // the slices in slice order, eight loads in flight at a time
+        const float* src = a.partial + (int64_t)b * a.M + nn;
+        const int64_t step = (int64_t)a.B * a.M;
+        const int S = (int)gridDim.y;
+        float t = 0.f;
+        int q = 0;
+        for (; q + 8 <= S; q += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (q + u) * step);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) t += v[u];
+        }
+        for (; q < S; ++q) t += __ldcg(src + q * step);
+        if (a.bias) t += a.bias[nn];
+        if (a.residual) t += a.residual[(int64_t)b * a.ldy + nn];
+        if (a.act == GK_ACT_GELU) {
+            if (a.preact) a.preact[(int64_t)b * a.M + nn] = t;
+            t = gelu_tanh(t);
+        }
+        a.Y[(int64_t)b * a.ldy + nn] = t;
+        if (a.cache && nn >= C && pos < a.Tmax) {
+            const int which = nn / C - 1, c = nn % C;
+            a.cache[cache_index(a.layer, which, b, c / a.hs, pos, a.B, a.H, a.Tmax, a.hs) + c % a.hs] = t;
+        }
     }
-    Y[(int64_t)b * ldy + n] = t;
+    if (threadIdx.x == 0) a.tickets[blockIdx.x] = 0;  // ready for the next launch
 }
 
 // logits[b, v] = sum_c X[b, c] wte[v, c]: one warp per vocabulary row (MatMulT head).
+// With ln_g, the rows of X go through LayerNorm(ln_g, ln_b) first (ln_f fused in).
 template <int NB>
-__global__ void lm_head_kernel(const float* __restrict__ X, const float* __restrict__ wte, int B, int C, int V,
+__global__ void lm_head_kernel(const float* __restrict__ X, const float* __restrict__ ln_g,
+                               const float* __restrict__ ln_b, const float* __restrict__ wte, int B, int C, int V,
                                float* __restrict__ logits, int64_t ldl) {
-    extern __shared__ float xs[];  // [NB][C]
-    for (int e = threadIdx.x; e < NB * C; e += blockDim.x) xs[e] = (e / C) < B ? X[e] : 0.f;
+    extern __shared__ float xs[];  // [NB][C], then row statistics [2 NB]
+    float* st = xs + NB * C;
+    if (ln_g) {
+        row_stats(X, C, B, C, st);
+        __syncthreads();
+    }
+    for (int e = threadIdx.x; e < NB * C; e += blockDim.x) {
+        const int b = e / C, c = e % C;
+        float v = b < B ? X[e] : 0.f;
+        if (ln_g && b < B) v = (v - st[2 * b]) * st[2 * b + 1] * ln_g[c] + ln_b[c];
+        xs[e] = v;
+    }
     __syncthreads();
-    int lane = threadIdx.x & 31;
-    int warps = blockDim.x >> 5;
-    for (int v = blockIdx.x * warps + (threadIdx.x >> 5); v < V; v += gridDim.x * warps) {
-        const float* row = wte + (int64_t)v * C;
-        float acc[NB];
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    // four vocabulary rows per warp and pass: each x value read from shared memory serves four
+    // weight values
+    for (int v0 = (blockIdx.x * warps + (threadIdx.x >> 5)) * 4; v0 < V; v0 += gridDim.x * warps * 4) {
+        float acc[4][NB];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
         for (int c = lane * 4; c < C; c += 128) {
-            float4 w = *reinterpret_cast<const float4*>(row + c);
+            float4 w[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                w[r] = v0 + r < V ? *reinterpret_cast<const float4*>(wte + (int64_t)(v0 + r) * C + c)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const float* xb = xs + b * C + c;
-                acc[b] = fmaf(w.x, xb[0], fmaf(w.y, xb[1], fmaf(w.z, xb[2], fmaf(w.w, xb[3], acc[b]))));
+                const float4 xb = *reinterpret_cast<const float4*>(xs + b * C + c);
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    acc[r][b] = fmaf(w[r].x, xb.x, fmaf(w[r].y, xb.y, fmaf(w[r].z, xb.z, fmaf(w[r].w, xb.w, acc[r][b]))));
             }
         }
 #pragma unroll
-        for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
-        if (lane < NB && lane < B) {
-            float r = 0.f;
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int b = 0; b < NB; ++b)
-                if (b == lane) r = acc[b];
-            logits[(int64_t)lane * ldl + v] = r;
+            for (int b = 0; b < NB; ++b) acc[r][b] = warp_sum(acc[r][b]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            if (lane < NB && lane < B && v0 + r < V) {
+                float o = 0.f;
+#pragma unroll
+                for (int b = 0; b < NB; ++b)
+                    if (b == lane) o = acc[r][b];
+                logits[(int64_t)lane * ldl + v0 + r] = o;
+            }
         }
     }
 }
@@ -155,23 +285,6 @@ __global__ void embed_step_kernel(const int32_t* __restrict__ tokens, const floa
         x[(int64_t)b * C + c] = ok ? wte[(int64_t)id * C + c] + wpe[(int64_t)pos * C + c] : 0.f;
 }
 
-__device__ __forceinline__ int64_t cache_index(int l, int kv, int b, int h, int t, int B, int H, int Tmax, int hs) {
-    return ((((int64_t)(l * 2 + kv) * B + b) * H + h) * Tmax + t) * hs;
-}
-
-// Append this step's key and value rows (columns [C, 2C) and [2C, 3C) of qkv) at pos.
-__global__ void kv_append_kernel(const float* __restrict__ qkv, float* __restrict__ cache, int l, int B, int H, int hs,
-                                 int Tmax, const int* __restrict__ state) {
-    int pos = state[0];
-    if (pos >= Tmax) return;
-    int C = H * hs;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)B * C) return;
-    int b = (int)(i / C), c = (int)(i % C), h = c / hs, d = c % hs;
-    cache[cache_index(l, 0, b, h, pos, B, H, Tmax, hs) + d] = qkv[(int64_t)b * 3 * C + C + c];
-    cache[cache_index(l, 1, b, h, pos, B, H, Tmax, hs) + d] = qkv[(int64_t)b * 3 * C + 2 * C + c];
-}
-
 // Prefill: keys and values of positions 0 .. Tp-1 from qkv [B*Tp, 3C].
 __global__ void kv_write_prefill_kernel(const float* __restrict__ qkv, float* __restrict__ cache, int l, int B,
                                         int Tp, int H, int hs, int Tmax) {
@@ -186,87 +299,112 @@ __global__ void kv_write_prefill_kernel(const float* __restrict__ qkv, float* __
 }
 
 // Decode attention, split over key chunks of KCHUNK (flash-decoding): block (chunk, b*H+h)
-// writes (max, sum, unnormalised output[hs]) of its chunk; no mask (the cache holds the past).
-__global__ void __launch_bounds__(128) decode_attn_partial_kernel(const float* __restrict__ qkv,
-                                                                  const float* __restrict__ cache, int l, int B,
-                                                                  int H, int hs, int Tmax,
-                                                                  const int* __restrict__ state,
-                                                                  float* __restrict__ part, int nchunks) {
-    __shared__ float q[128];
-    __shared__ float p[KCHUNK];
-    __shared__ float red[4];
+// of two warps writes (max, sum, unnormalised output[hs]) of its chunk (no mask: the cache
+// holds the past). Scores: lane = key, the key's row read as float4s; output: lane = head
+// dimension(s), the warp's 32 keys taken in turn (coalesced rows of V). The last chunk of
+// (b, h) to arrive (atomic ticket) combines the chunks in chunk order into y; no block waits
+// on another.
+__global__ void __launch_bounds__(64) decode_attn_kernel(const float* __restrict__ qkv,
+                                                         const float* __restrict__ cache, int l, int B, int H, int hs,
+                                                         int Tmax, const int* __restrict__ state,
+                                                         float* __restrict__ part, int nchunks, int* tickets,
+                                                         float* __restrict__ y) {
+    __shared__ __align__(16) float q[128];
+    __shared__ float red[2][2];
     __shared__ float ored[2][128];
-    int chunk = blockIdx.x, bh = blockIdx.y, b = bh / H, h = bh % H;
-    int n = min(state[0] + 1, Tmax);  // keys 0 .. pos (the current one was appended)
-    int j0 = chunk * KCHUNK;
+    __shared__ int last;
+    const int chunk = blockIdx.x, bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n = min(state[0] + 1, Tmax);  // keys 0 .. pos (the current one was appended)
+    const int j0 = chunk * KCHUNK;
     float* out = part + ((int64_t)bh * nchunks + chunk) * (hs + 2);
+    const int C = H * hs;
     if (j0 >= n) {
         if (threadIdx.x == 0) {
             out[0] = -INFINITY;
             out[1] = 0.f;
         }
-        return;
+    } else {
+        for (int d = threadIdx.x; d < hs; d += blockDim.x) q[d] = qkv[(int64_t)b * 3 * C + h * hs + d];
+        __syncthreads();
+        const float* K = cache + cache_index(l, 0, b, h, 0, B, H, Tmax, hs);
+        const float* Vc = cache + cache_index(l, 1, b, h, 0, B, H, Tmax, hs);
+        const int jw = j0 + warp * 32;  // this warp's first key
+        const int j = jw + lane;
+        float sc = -INFINITY;
+        if (j < n) {
+            const float* kr = K + (int64_t)j * hs;
+            float a0 = 0.f, a1 = 0.f;
+            for (int d = 0; d < hs; d += 8) {
+                const float4 k4 = *reinterpret_cast<const float4*>(kr + d);
+                const float4 q4 = *reinterpret_cast<const float4*>(q + d);
+                a0 = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, a0))));
+                if (d + 4 < hs) {
+                    const float4 k5 = *reinterpret_cast<const float4*>(kr + d + 4);
+                    const float4 q5 = *reinterpret_cast<const float4*>(q + d + 4);
+                    a1 = fmaf(q5.x, k5.x, fmaf(q5.y, k5.y, fmaf(q5.z, k5.z, fmaf(q5.w, k5.w, a1))));
+                }
+            }
+            sc = (a0 + a1) * rsqrtf((float)hs);
+        }
+        float m = warp_max(sc);
+        if (lane == 0) red[0][warp] = m;
+        __syncthreads();
+        m = fmaxf(red[0][0], red[0][1]);
+        const float p = j < n ? expf(sc - m) : 0.f;
+        const float ls = warp_sum(p);
+        if (lane == 0) red[1][warp] = ls;
+        // output: lane takes dimensions lane, lane + 32, ...; the warp's keys in turn
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        const int nk = max(0, min(32, n - jw));
+        // eight keys' rows of V in flight at a time
+        for (int t0 = 0; t0 < nk; t0 += 8) {
+            float vv[8][4];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    vv[u][i] = (t0 + u < nk && lane + 32 * i < hs) ? Vc[(int64_t)(jw + t0 + u) * hs + lane + 32 * i] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float pt = __shfl_sync(0xffffffffu, p, (t0 + u) & 31);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[i] = fmaf(t0 + u < nk ? pt : 0.f, vv[u][i], o[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (lane + 32 * i < hs) ored[warp][lane + 32 * i] = o[i];
+        __syncthreads();
+        for (int d = threadIdx.x; d < hs; d += blockDim.x) out[2 + d] = ored[0][d] + ored[1][d];
+        if (threadIdx.x == 0) {
+            out[0] = m;
+            out[1] = red[1][0] + red[1][1];
+        }
     }
-    int C = H * hs;
-    for (int d = threadIdx.x; d < hs; d += blockDim.x) q[d] = qkv[(int64_t)b * 3 * C + h * hs + d];
+    __threadfence();
     __syncthreads();
-    const float scale = rsqrtf((float)hs);
-    const float* K = cache + cache_index(l, 0, b, h, 0, B, H, Tmax, hs);
-    const float* Vc = cache + cache_index(l, 1, b, h, 0, B, H, Tmax, hs);
-    // two threads per key: each takes half of the dimensions
-    int kk = threadIdx.x >> 1, half = threadIdx.x & 1;
-    int j = j0 + kk;
-    float s = 0.f;
-    if (j < n) {
-        const float* kr = K + (int64_t)j * hs;
-        int d0 = half * (hs / 2), d1 = d0 + hs / 2;
-        for (int d = d0; d < d1; ++d) s = fmaf(q[d], kr[d], s);
-    }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s = (j < n) ? s * scale : -INFINITY;
-    float m = warp_max(s);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    if (threadIdx.x == 0) last = atomicAdd(&tickets[bh], 1) == nchunks - 1;
     __syncthreads();
-    m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    float e = (j < n) ? expf(s - m) : 0.f;
-    if (half == 0) p[kk] = e;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float l_ = 0.f;
-        for (int t = 0; t < KCHUNK; ++t) l_ += p[t];
-        out[0] = m;
-        out[1] = l_;
-    }
-    // output: thread (d, g) sums keys g, g+2, ... of the chunk for dimension d
-    int g = threadIdx.x / 64, d = threadIdx.x % 64;
-    for (int dd = d; dd < hs; dd += 64) {
-        float o = 0.f;
-        for (int t = g; t < KCHUNK && j0 + t < n; t += 2) o = fmaf(p[t], Vc[(int64_t)(j0 + t) * hs + dd], o);
-        ored[g][dd] = o;
-    }
-    __syncthreads();
-    for (int dd = threadIdx.x; dd < hs; dd += blockDim.x) out[2 + dd] = ored[0][dd] + ored[1][dd];
-}
-
-__global__ void decode_attn_combine_kernel(const float* __restrict__ part, int nchunks, int H, int hs,
-                                           float* __restrict__ y) {
-    int bh = blockIdx.x, b = bh / H, h = bh % H;
+    if (!last) return;
+    __threadfence();
     const float* pp = part + (int64_t)bh * nchunks * (hs + 2);
     float M = -INFINITY;
-    for (int c = 0; c < nchunks; ++c) M = fmaxf(M, pp[c * (hs + 2)]);
+    for (int c = 0; c < nchunks; ++c) M = fmaxf(M, __ldcg(pp + c * (hs + 2)));
     float L = 0.f;
     for (int c = 0; c < nchunks; ++c) {
-        float mc = pp[c * (hs + 2)];
-        if (mc != -INFINITY) L += pp[c * (hs + 2) + 1] * expf(mc - M);
+        const float mc = __ldcg(pp + c * (hs + 2));
+        if (mc != -INFINITY) L += __ldcg(pp + c * (hs + 2) + 1) * expf(mc - M);
     }
     for (int d = threadIdx.x; d < hs; d += blockDim.x) {
         float o = 0.f;
         for (int c = 0; c < nchunks; ++c) {
-            float mc = pp[c * (hs + 2)];
-            if (mc != -INFINITY) o += pp[c * (hs + 2) + 2 + d] * expf(mc - M);
+            const float mc = __ldcg(pp + c * (hs + 2));
+            if (mc != -INFINITY) o += __ldcg(pp + c * (hs + 2) + 2 + d) * expf(mc - M);
         }
-        y[(int64_t)b * H * hs + h * hs + d] = o / L;
+        y[(int64_t)b * C + h * hs + d] = o / L;
     }
+    if (threadIdx.x == 0) tickets[bh] = 0;  // ready for the next launch
 }
 
 __global__ void gather_last_kernel(const float* __restrict__ x, int B, int Tp, int C, float* __restrict__ last) {
@@ -465,42 +603,50 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
 
 int gemv_nb(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16; }
 
-gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float* W, int64_t ldw, int K, int M,
-               const float* bias, const float* residual, float* Y, int act, float* preact) {
+// Y [B, M] = act(LN?(X) W + bias + residual), one launch (see gemv_kernel); append_layer >= 0
+// also appends the key/value columns to that layer of the cache.
+gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float* ln_g, const float* ln_b,
+               const float* W, int64_t ldw, int K, int M, const float* bias, const float* residual, float* Y, int act,
+               float* preact, int append_layer = -1) {
     int B = kv->B;
     int colblocks = (int)cdiv(M, GEMV_COLS);
+    GK_REQUIRE(ctx, colblocks <= 1024, GK_ERR_UNSUPPORTED, "decode gemv: %d columns", M);
     int S = (int)std::max<int64_t>(1, std::min<int64_t>(K / 8, cdiv(2 * ctx->num_sms, colblocks)));
     int kslice = (int)cdiv(K, S);
     S = (int)cdiv(K, kslice);
     GK_REQUIRE(ctx, (size_t)S * B * M <= kv->partial_floats, GK_ERR_WORKSPACE, "decode gemv: partial buffer too small");
     int nb = gemv_nb(B);
-    size_t smem = ((size_t)nb * kslice + 8 * (size_t)nb * GEMV_COLS) * sizeof(float);
+    size_t smem = ((size_t)nb * kslice + 8 * (size_t)nb * GEMV_COLS + 2 * (size_t)nb) * sizeof(float);
+    GemvArgs a;
+    a.X = X; a.ldx = ldx; a.ln_g = ln_g; a.ln_b = ln_b; a.W = W; a.ldw = ldw;
+    a.B = B; a.K = K; a.M = M; a.kslice = kslice;
+    a.partial = kv->partial; a.tickets = kv->tickets;
+    a.bias = bias; a.residual = residual; a.Y = Y; a.ldy = M; a.act = act; a.preact = preact;
+    a.cache = append_layer >= 0 ? kv->cache : nullptr;
+    a.layer = append_layer; a.H = kv->cfg.H; a.hs = kv->cfg.C / kv->cfg.H; a.Tmax = kv->Tmax; a.state = kv->state;
     dim3 grid(colblocks, S);
 #define GEMV_CASE(NBV)                                                                                       \
     case NBV:                                                                                                \
-        cudaFuncSetAttribute(gemv_partial_kernel<NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-        gemv_partial_kernel<NBV><<<grid, GEMV_THREADS, smem, ctx->stream>>>(X, ldx, W, ldw, B, K, M, kslice,   \
-                                                                            kv->partial);                    \
+        cudaFuncSetAttribute(gemv_kernel<NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
+        gemv_kernel<NBV><<<grid, GEMV_THREADS, smem, ctx->stream>>>(a);                                      \
         break;
     switch (nb) {
         GEMV_CASE(1) GEMV_CASE(2) GEMV_CASE(4) GEMV_CASE(8) GEMV_CASE(16)
     }
 #undef GEMV_CASE
-    GK_TRY(launched(ctx, "gemv_partial"));
-    gemv_finish_kernel<<<(unsigned)cdiv((int64_t)B * M, 256), 256, 0, ctx->stream>>>(kv->partial, S, B, M, bias,
-                                                                                   residual, Y, M, act, preact);
-    return launched(ctx, "gemv_finish");
+    return launched(ctx, "gemv");
 }
 
-gk_status lm_head(gk_ctx* ctx, gk_kv* kv, const float* X, const float* wte, float* logits, int64_t ldl) {
+gk_status lm_head(gk_ctx* ctx, gk_kv* kv, const float* X, const float* ln_g, const float* ln_b, const float* wte,
+                  float* logits, int64_t ldl) {
     int B = kv->B, C = kv->cfg.C, V = kv->cfg.V;
     int nb = gemv_nb(B);
-    size_t smem = (size_t)nb * C * sizeof(float);
+    size_t smem = ((size_t)nb * C + 2 * (size_t)nb) * sizeof(float);
     int blocks = ctx->num_sms * 4;
 #define LM_CASE(NBV)                                                                                         \
     case NBV:                                                                                                \
         cudaFuncSetAttribute(lm_head_kernel<NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
-        lm_head_kernel<NBV><<<blocks, 256, smem, ctx->stream>>>(X, wte, B, C, V, logits, ldl);                 \
+        lm_head_kernel<NBV><<<blocks, 256, smem, ctx->stream>>>(X, ln_g, ln_b, wte, B, C, V, logits, ldl);    \
         break;
     switch (nb) {
         LM_CASE(1) LM_CASE(2) LM_CASE(4) LM_CASE(8) LM_CASE(16)
@@ -539,7 +685,9 @@ gk_status gk_kv_create(gk_ctx* ctx, gk_kv** out, const gk_gpt_cfg* cfg, int B, i
     GK_REQUIRE(ctx, B >= 1 && B <= 16, GK_ERR_UNSUPPORTED, "gk_kv_create: batch %d outside 1..16", B);
     GK_REQUIRE(ctx, Tmax >= 1 && Tmax <= cfg->T, GK_ERR_ARG, "gk_kv_create: Tmax %d outside 1..T", Tmax);
     int hs = cfg->C / cfg->H;
-    GK_REQUIRE(ctx, hs <= 128 && cfg->C % 4 == 0, GK_ERR_UNSUPPORTED, "gk_kv_create: head size / width unsupported");
+    GK_REQUIRE(ctx, hs <= 128 && hs % 4 == 0 && cfg->C % 4 == 0, GK_ERR_UNSUPPORTED,
+               "gk_kv_create: head size / width unsupported");
+    GK_REQUIRE(ctx, (int64_t)B * cfg->H <= 1024, GK_ERR_UNSUPPORTED, "gk_kv_create: batch x heads above 1024");
     gk_kv* kv = new gk_kv();
     kv->cfg = *cfg;
     kv->B = B;
@@ -570,6 +718,8 @@ gk_status gk_kv_create(gk_ctx* ctx, gk_kv** out, const gk_gpt_cfg* cfg, int B, i
         }
     }
     if (cudaMalloc(&kv->state, 2 * sizeof(int)) != cudaSuccess || cudaMemset(kv->state, 0, 2 * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&kv->tickets, 2048 * sizeof(int)) != cudaSuccess ||
+        cudaMemset(kv->tickets, 0, 2048 * sizeof(int)) != cudaSuccess ||
         cudaMemset(kv->cache, 0, (size_t)cfg->L * 2 * rows * C * sizeof(float)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         gk_kv_destroy(kv);
@@ -587,6 +737,7 @@ void gk_kv_destroy(gk_kv* kv) {
     for (float* p : ptrs)
         if (p) cudaFree(p);
     if (kv->state) cudaFree(kv->state);
+    if (kv->tickets) cudaFree(kv->tickets);
     delete kv;
 }
 
@@ -624,7 +775,7 @@ gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t*
     GK_TRY(launched(ctx, "gather_last"));
     GK_TRY(gk_layernorm_fwd(ctx, kv->last, w.t(GK_T_LNF_W), w.t(GK_T_LNF_B), kv->ln, GK_F32, nullptr, nullptr, B, C,
                             1e-5f));
-    GK_TRY(lm_head(ctx, kv, kv->ln, w.t(GK_T_WTE), last_logits, c.V));
+    GK_TRY(lm_head(ctx, kv, kv->ln, nullptr, nullptr, w.t(GK_T_WTE), last_logits, c.V));
     set_state_kernel<<<1, 1, 0, ctx->stream>>>(kv->state, Tp, 0);
     GK_TRY(launched(ctx, "set_state"));
     kv->length = Tp;
@@ -646,31 +797,23 @@ gk_status decode_step_launches(gk_ctx* ctx, const float* params, gk_kv* kv, cons
     embed_step_kernel<<<B, 256, 0, ctx->stream>>>(tokens, w.t(GK_T_WTE), w.t(GK_T_WPE), kv->x, B, C, c.V, kv->Tmax,
                                                   kv->state, ctx->d_err);
     GK_TRY(launched(ctx, "embed_step"));
+    // per layer: LN1 + QKV (+ key/value append), attention, projection + residual,
+    // LN2 + MLP up + GELU, MLP down + residual: five launches
     for (int l = 0; l < c.L; ++l) {
-        GK_TRY(gk_layernorm_fwd(ctx, kv->x, w.t(GK_T_LN1_W, l), w.t(GK_T_LN1_B, l), kv->ln, GK_F32, nullptr, nullptr, B,
-                                C, 1e-5f));
-        GK_TRY(gemv(ctx, kv, kv->ln, C, w.t(GK_T_ATTN_W, l), 3 * C, C, 3 * C, w.t(GK_T_ATTN_B, l), nullptr, kv->qkv,
-                    GK_ACT_NONE, nullptr));
-        kv_append_kernel<<<(unsigned)cdiv((int64_t)B * C, 256), 256, 0, ctx->stream>>>(kv->qkv, kv->cache, l, B, H, hs,
-                                                                                      kv->Tmax, kv->state);
-        GK_TRY(launched(ctx, "kv_append"));
-        decode_attn_partial_kernel<<<dim3(nchunks, B * H), 128, 0, ctx->stream>>>(kv->qkv, kv->cache, l, B, H, hs,
-                                                                                  kv->Tmax, kv->state, kv->attn_part,
-                                                                                  nchunks);
-        GK_TRY(launched(ctx, "decode_attn_partial"));
-        decode_attn_combine_kernel<<<B * H, 64, 0, ctx->stream>>>(kv->attn_part, nchunks, H, hs, kv->y);
-        GK_TRY(launched(ctx, "decode_attn_combine"));
-        GK_TRY(gemv(ctx, kv, kv->y, C, w.t(GK_T_ATTNPROJ_W, l), C, C, C, w.t(GK_T_ATTNPROJ_B, l), kv->x, kv->x,
-                    GK_ACT_NONE, nullptr));
-        GK_TRY(gk_layernorm_fwd(ctx, kv->x, w.t(GK_T_LN2_W, l), w.t(GK_T_LN2_B, l), kv->ln, GK_F32, nullptr, nullptr, B,
-                                C, 1e-5f));
-        GK_TRY(gemv(ctx, kv, kv->ln, C, w.t(GK_T_FC_W, l), 4 * C, C, 4 * C, w.t(GK_T_FC_B, l), nullptr, kv->h,
-                    GK_ACT_GELU, kv->pre));
-        GK_TRY(gemv(ctx, kv, kv->h, 4 * C, w.t(GK_T_MLPPROJ_W, l), C, 4 * C, C, w.t(GK_T_MLPPROJ_B, l), kv->x, kv->x,
-                    GK_ACT_NONE, nullptr));
+        GK_TRY(gemv(ctx, kv, kv->x, C, w.t(GK_T_LN1_W, l), w.t(GK_T_LN1_B, l), w.t(GK_T_ATTN_W, l), 3 * C, C, 3 * C,
+                    w.t(GK_T_ATTN_B, l), nullptr, kv->qkv, GK_ACT_NONE, nullptr, l));
+        decode_attn_kernel<<<dim3(nchunks, B * H), 64, 0, ctx->stream>>>(kv->qkv, kv->cache, l, B, H, hs, kv->Tmax,
+                                                                          kv->state, kv->attn_part, nchunks,
+                                                                          kv->tickets + 1024, kv->y);
+        GK_TRY(launched(ctx, "decode_attn"));
+        GK_TRY(gemv(ctx, kv, kv->y, C, nullptr, nullptr, w.t(GK_T_ATTNPROJ_W, l), C, C, C, w.t(GK_T_ATTNPROJ_B, l),
+                    kv->x, kv->x, GK_ACT_NONE, nullptr));
+        GK_TRY(gemv(ctx, kv, kv->x, C, w.t(GK_T_LN2_W, l), w.t(GK_T_LN2_B, l), w.t(GK_T_FC_W, l), 4 * C, C, 4 * C,
+                    w.t(GK_T_FC_B, l), nullptr, kv->h, GK_ACT_GELU, kv->pre));
+        GK_TRY(gemv(ctx, kv, kv->h, 4 * C, nullptr, nullptr, w.t(GK_T_MLPPROJ_W, l), C, 4 * C, C,
+                    w.t(GK_T_MLPPROJ_B, l), kv->x, kv->x, GK_ACT_NONE, nullptr));
     }
-    GK_TRY(gk_layernorm_fwd(ctx, kv->x, w.t(GK_T_LNF_W), w.t(GK_T_LNF_B), kv->ln, GK_F32, nullptr, nullptr, B, C, 1e-5f));
-    GK_TRY(lm_head(ctx, kv, kv->ln, w.t(GK_T_WTE), logits, c.V));
+    GK_TRY(lm_head(ctx, kv, kv->x, w.t(GK_T_LNF_W), w.t(GK_T_LNF_B), w.t(GK_T_WTE), logits, c.V));
     int dsel = 0;
     if (next) {
         int top_k = s ? s->top_k : 1;

@@ -44,6 +44,30 @@ namespace {
 constexpr int GEMV_THREADS = 256;  // 8 warps; a warp covers 128 columns (float4 per lane)
 constexpr int GEMV_COLS = 128;
 constexpr int KCHUNK = 64;         // keys per decode-attention block
+constexpr int GEMV_PF = 8;         // weight rows per warp loaded before the previous kernel ends
+
+// Programmatic dependent launch: a decode kernel lets the next one start as soon as all its
+// blocks are running (trigger), and waits for its predecessor's completion and memory before
+// touching anything a previous kernel wrote (wait). Only the weights, which nothing in a
+// decode step writes, are read before the wait. Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 __device__ __forceinline__ int64_t cache_index(int l, int kv, int b, int h, int t, int B, int H, int Tmax, int hs) {
     return ((((int64_t)(l * 2 + kv) * B + b) * H + h) * Tmax + t) * hs;
@@ -55,18 +79,20 @@ __device__ __forceinline__ int64_t cache_index(int l, int kv, int b, int h, int 
 __device__ __forceinline__ void row_stats(const float* __restrict__ X, int64_t ldx, int B, int K, float* st) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     for (int b = warp; b < B; b += nw) {
+        // one pass over the row, shifted by its first element so that E[d^2] - E[d]^2 does
+        // not cancel when the mean is large against the spread
         const float* xr = X + (int64_t)b * ldx;
-        float s = 0.f;
-        for (int k = lane; k < K; k += 32) s += xr[k];
-        const float mu = warp_sum(s) / K;
-        float v = 0.f;
+        const float sh = xr[0];
+        float s = 0.f, q = 0.f;
         for (int k = lane; k < K; k += 32) {
-            const float d = xr[k] - mu;
-            v += d * d;
+            const float d = xr[k] - sh;
+            s += d;
+            q = fmaf(d, d, q);
         }
-        v = warp_sum(v) / K;
+        const float md = warp_sum(s) / K;
+        const float v = fmaxf(warp_sum(q) / K - md * md, 0.f);
         if (lane == 0) {
-            st[2 * b] = mu;
+            st[2 * b] = sh + md;
             st[2 * b + 1] = rsqrtf(v + 1e-5f);
         }
     }
@@ -110,6 +136,16 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
     const int k0 = s * a.kslice, k1 = min(a.K, k0 + a.kslice);
     const int n = blockIdx.x * GEMV_COLS + (threadIdx.x & 31) * 4;
     const int warp = threadIdx.x >> 5;
+    pdl_trigger();
+    // this warp's first weight rows (k0 + warp + 8 i) while the previous kernel finishes
+    float4 wpre[GEMV_PF];
+#pragma unroll
+    for (int i = 0; i < GEMV_PF; ++i) {
+        const int k = k0 + warp + 8 * i;
+        wpre[i] = (n < a.M && k < k1) ? *reinterpret_cast<const float4*>(a.W + (int64_t)k * a.ldw + n)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
     if (a.ln_g) {
         row_stats(a.X, a.ldx, a.B, a.K, st);
         __syncthreads();
@@ -128,8 +164,20 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
     if (n < a.M) {
-        // four weight rows in flight per warp (rows k, k + 8, k + 16, k + 24)
-        int k = k0 + warp;
+#pragma unroll
+        for (int i = 0; i < GEMV_PF; ++i) {
+            const int kk = warp + 8 * i;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float xv = k0 + kk < k1 ? Xs[b * a.kslice + kk] : 0.f;
+                acc[b][0] = fmaf(xv, wpre[i].x, acc[b][0]);
+                acc[b][1] = fmaf(xv, wpre[i].y, acc[b][1]);
+                acc[b][2] = fmaf(xv, wpre[i].z, acc[b][2]);
+                acc[b][3] = fmaf(xv, wpre[i].w, acc[b][3]);
+            }
+        }
+        // the remaining rows, four in flight per warp (rows k, k + 8, k + 16, k + 24)
+        int k = k0 + warp + 8 * GEMV_PF;
         for (; k + 24 < k1; k += 32) {
             float4 w[4];
 #pragma unroll
@@ -218,6 +266,8 @@ template <int NB>
 __global__ void lm_head_kernel(const float* __restrict__ X, const float* __restrict__ ln_g,
                                const float* __restrict__ ln_b, const float* __restrict__ wte, int B, int C, int V,
                                float* __restrict__ logits, int64_t ldl) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ float xs[];  // [NB][C], then row statistics [2 NB]
     float* st = xs + NB * C;
     if (ln_g) {
@@ -276,6 +326,8 @@ __global__ void lm_head_kernel(const float* __restrict__ X, const float* __restr
 __global__ void embed_step_kernel(const int32_t* __restrict__ tokens, const float* __restrict__ wte,
                                   const float* __restrict__ wpe, float* __restrict__ x, int B, int C, int V,
                                   int Tmax, const int* __restrict__ state, int* err) {
+    pdl_trigger();
+    pdl_wait();
     int b = blockIdx.x;
     int pos = state[0];
     int id = tokens[b];
@@ -309,6 +361,8 @@ __global__ void __launch_bounds__(64) decode_attn_kernel(const float* __restrict
                                                          int Tmax, const int* __restrict__ state,
                                                          float* __restrict__ part, int nchunks, int* tickets,
                                                          float* __restrict__ y) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ __align__(16) float q[128];
     __shared__ float red[2][2];
     __shared__ float ored[2][128];
@@ -415,6 +469,8 @@ __global__ void gather_last_kernel(const float* __restrict__ x, int B, int Tp, i
 }
 
 __global__ void copy_ids_kernel(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int n) {
+    pdl_trigger();
+    pdl_wait();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) dst[i] = src[i];
 }
@@ -425,6 +481,8 @@ __global__ void set_state_kernel(int* state, int length, int selections) {
 }
 
 __global__ void advance_kernel(int* state, int dlen, int dsel) {
+    pdl_trigger();
+    pdl_wait();
     state[0] += dlen;
     state[1] += dsel;
 }
@@ -468,6 +526,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
                                                              int top_k, float temperature, uint64_t seed,
                                                              uint64_t counter, const int* __restrict__ state,
                                                              int32_t* __restrict__ next) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ unsigned hist[256];
     __shared__ float fred[32];
     __shared__ int ired[32];
@@ -628,7 +688,7 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
 #define GEMV_CASE(NBV)                                                                                       \
     case NBV:                                                                                                \
         cudaFuncSetAttribute(gemv_kernel<NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
-        gemv_kernel<NBV><<<grid, GEMV_THREADS, smem, ctx->stream>>>(a);                                      \
+        launch_pdl(gemv_kernel<NBV>, grid, dim3(GEMV_THREADS), smem, ctx->stream, a);                       \
         break;
     switch (nb) {
         GEMV_CASE(1) GEMV_CASE(2) GEMV_CASE(4) GEMV_CASE(8) GEMV_CASE(16)
@@ -646,7 +706,8 @@ gk_status lm_head(gk_ctx* ctx, gk_kv* kv, const float* X, const float* ln_g, con
 #define LM_CASE(NBV)                                                                                         \
     case NBV:                                                                                                \
         cudaFuncSetAttribute(lm_head_kernel<NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
-        lm_head_kernel<NBV><<<blocks, 256, smem, ctx->stream>>>(X, ln_g, ln_b, wte, B, C, V, logits, ldl);    \
+        launch_pdl(lm_head_kernel<NBV>, dim3(blocks), dim3(256), smem, ctx->stream, X, ln_g, ln_b, wte, B, C, V, \
+                   logits, ldl);                                                                             \
         break;
     switch (nb) {
         LM_CASE(1) LM_CASE(2) LM_CASE(4) LM_CASE(8) LM_CASE(16)
@@ -794,17 +855,17 @@ gk_status decode_step_launches(gk_ctx* ctx, const float* params, gk_kv* kv, cons
     W w{params, c};
     int B = kv->B, C = c.C, H = c.H, hs = C / H;
     int nchunks = (int)cdiv(kv->Tmax, KCHUNK);
-    embed_step_kernel<<<B, 256, 0, ctx->stream>>>(tokens, w.t(GK_T_WTE), w.t(GK_T_WPE), kv->x, B, C, c.V, kv->Tmax,
-                                                  kv->state, ctx->d_err);
+    launch_pdl(embed_step_kernel, dim3(B), dim3(256), 0, ctx->stream, tokens, w.t(GK_T_WTE), w.t(GK_T_WPE), kv->x, B,
+               C, c.V, kv->Tmax, (const int*)kv->state, ctx->d_err);
     GK_TRY(launched(ctx, "embed_step"));
     // per layer: LN1 + QKV (+ key/value append), attention, projection + residual,
     // LN2 + MLP up + GELU, MLP down + residual: five launches
     for (int l = 0; l < c.L; ++l) {
         GK_TRY(gemv(ctx, kv, kv->x, C, w.t(GK_T_LN1_W, l), w.t(GK_T_LN1_B, l), w.t(GK_T_ATTN_W, l), 3 * C, C, 3 * C,
                     w.t(GK_T_ATTN_B, l), nullptr, kv->qkv, GK_ACT_NONE, nullptr, l));
-        decode_attn_kernel<<<dim3(nchunks, B * H), 64, 0, ctx->stream>>>(kv->qkv, kv->cache, l, B, H, hs, kv->Tmax,
-                                                                          kv->state, kv->attn_part, nchunks,
-                                                                          kv->tickets + 1024, kv->y);
+        launch_pdl(decode_attn_kernel, dim3(nchunks, B * H), dim3(64), 0, ctx->stream, (const float*)kv->qkv,
+                   (const float*)kv->cache, l, B, H, hs, kv->Tmax, (const int*)kv->state, kv->attn_part, nchunks,
+                   kv->tickets + 1024, kv->y);
         GK_TRY(launched(ctx, "decode_attn"));
         GK_TRY(gemv(ctx, kv, kv->y, C, nullptr, nullptr, w.t(GK_T_ATTNPROJ_W, l), C, C, C, w.t(GK_T_ATTNPROJ_B, l),
                     kv->x, kv->x, GK_ACT_NONE, nullptr));
@@ -818,12 +879,13 @@ gk_status decode_step_launches(gk_ctx* ctx, const float* params, gk_kv* kv, cons
     if (next) {
         int top_k = s ? s->top_k : 1;
         float temp = s ? s->temperature : 0.f;
-        select_kernel<<<B, SEL_THREADS, 0, ctx->stream>>>(logits, c.V, c.V, top_k, temp, s ? s->seed : 0,
-                                                          s ? s->counter : 0, kv->state, next);
+        launch_pdl(select_kernel, dim3(B), dim3(SEL_THREADS), 0, ctx->stream, (const float*)logits, (int64_t)c.V, c.V,
+                   top_k, temp, (uint64_t)(s ? s->seed : 0), (uint64_t)(s ? s->counter : 0), (const int*)kv->state,
+                   next);
         GK_TRY(launched(ctx, "select"));
         dsel = 1;
     }
-    advance_kernel<<<1, 1, 0, ctx->stream>>>(kv->state, 1, dsel);
+    launch_pdl(advance_kernel, dim3(1), dim3(1), 0, ctx->stream, kv->state, 1, dsel);
     return launched(ctx, "advance");
 }
 
@@ -851,7 +913,8 @@ gk_status gk_decode_run(gk_ctx* ctx, const float* params, gk_kv* kv, int32_t* to
     auto step = [&]() -> gk_status {
         GK_TRY(decode_step_launches(ctx, params, kv, tokens, logits, next, s));
         if (next != tokens) {
-            copy_ids_kernel<<<1, 32 * (int)cdiv(kv->B, 32), 0, ctx->stream>>>(next, tokens, kv->B);
+            launch_pdl(copy_ids_kernel, dim3(1), dim3(32 * (int)cdiv(kv->B, 32)), 0, ctx->stream, (const int32_t*)next,
+                       tokens, kv->B);
             GK_TRY(launched(ctx, "copy_ids"));
         }
         return GK_OK;

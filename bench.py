@@ -263,7 +263,9 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (step working set >> 129 MB)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved,
                      "peak": bf16_sus if args.mode == "bf16" else bf16_sus / 2, "unit": "TFLOP/s",
-                     "frac": achieved / (bf16_sus if args.mode == "bf16" else bf16_sus / 2), "traffic": None,
+                     "frac": achieved / (bf16_sus if args.mode == "bf16" else bf16_sus / 2),
+                     "traffic": gemm_traffic_per_step(B, args.mode),
+                     "traffic_source": "profiles/gemm_tc_traffic_gpt2_b4.md (ncu at B=4, scaled by tokens)",
                      "kernel": "all GEMM launches of the step", "peak_source": f"{peak_src} bf16 sustained"
                      + ("" if args.mode == "bf16" else " / 2 (tf32 nominal ratio)"),
                      "gemm_ms_per_step": gms / n_gemm_steps, "gemm_tflop_per_step": flops / n_gemm_steps / 1e12},
@@ -276,6 +278,26 @@ def run_ours(args):
     if decode:
         out["decode"] = decode
     print(json.dumps(out))
+
+
+def gemm_traffic_per_step(B, mode):
+    """DRAM bytes of a step's GEMM launches from the committed ncu summary, while the kernel's
+    source is the one that was measured (sha256 recorded beside the figure); else None."""
+    import hashlib
+
+    here = os.path.dirname(os.path.abspath(__file__))
+    path = os.path.join(here, "profiles", "gemm_tc_traffic_gpt2_b4.md")
+    if B != 16 or mode != "bf16" or not os.path.exists(path):
+        return None
+    value, ok = None, True
+    for line in open(path):
+        if line.startswith("traffic_bytes_per_step_b16:"):
+            value = int(line.split(":")[1])
+        elif line.startswith("source_sha256 "):
+            rel, digest = line[len("source_sha256 "):].rsplit(":", 1)
+            src = os.path.join(here, rel.strip())
+            ok = ok and os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == digest.strip()
+    return value if ok else None
 
 
 def bench_decode(ctx, m, s, Tp=512, n_steps=256):
@@ -320,7 +342,7 @@ def bench_decode(ctx, m, s, Tp=512, n_steps=256):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=16)

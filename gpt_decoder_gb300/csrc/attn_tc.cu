@@ -327,13 +327,15 @@ __global__ void __maxnreg__(168)
 //                                    bf16 into shared memory (K-major, 128-byte swizzle)
 //   dV += P^T dO_u, dK += dS^T Q_u   (M=128 keys, N=64, K=64 queries)   -> TMEM 256..383
 // and per query tile, after its second half:
-//   dQ_tile = dS K                   (M=128 queries, N=64, K=128 keys)  -> TMEM 384..447
+//   dQ_tile = dS K                   (M=128 queries, N=64, K=128 keys)  -> TMEM 384 + 64 (tile % 2)
 // With two S^T/dP^T buffers the tensor core computes one sub-tile while the compute warps turn
-// the other into P^T and dS^T. dQ_tile goes through a swizzled shared-memory tile into a
-// float32 accumulator by TMA reduce-add (drained between the next tile's halves); dK and dV
-// are stored once at the end.
+// the other into P^T and dS^T. dQ_tile, double-buffered in TMEM, goes through a swizzled
+// shared-memory tile into a float32 accumulator by TMA reduce-add at the end of the next tile
+// (while the tensor core works on that tile's last products); dK and dV are stored once at
+// the end. TMEM: S^T/dP^T buffers 0..255, dV 256..319, dK 320..383, dQ 384..511.
 constexpr int BWD_THREADS = 288;
-constexpr size_t BWD_SMEM_BYTES = 12 * TILE + 2048 + 1024 + 256;  // K, V, Q[2], dO[2], P^T, dS^T, dQ, lse/D[2]
+// K, V, Q[2], dO[2], P^T, dS^T, dQ staging (a 4 KB box per compute warp), lse/D (512 B per warp)
+constexpr size_t BWD_SMEM_BYTES = 12 * TILE + 4096 + 1024 + 256;
 
 __global__ void __maxnreg__(168)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_dy,
@@ -347,17 +349,18 @@ __global__ void __maxnreg__(168)
     uint8_t* sO = smem + 4 * TILE;    // dO, two stages
     uint8_t* sPT = smem + 6 * TILE;   // two halves (query columns 0..63, 64..127)
     uint8_t* sDS = smem + 8 * TILE;   // two halves
-    uint8_t* sDQ = smem + 10 * TILE;  // two 128-row x 32-column float32 boxes, 128-byte swizzle
-    float* sLD = reinterpret_cast<float*>(smem + 12 * TILE);  // [2][lse 128 | D 128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 12 * TILE + 2048);
+    uint8_t* sDQ = smem + 10 * TILE;  // per compute warp a 32-row x 32-column float32 box, 128-byte swizzle
+    float* sLD = reinterpret_cast<float*>(smem + 12 * TILE);  // per compute warp [2 buffers][lse 32 | D 32]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 12 * TILE + 4096);
     uint64_t* bar_kv = bars;
     uint64_t* bar_qo = bars + 1;      // [2] Q, dO of a query tile landed
     uint64_t* bar_s = bars + 3;       // [2] S^T, dP^T of a sub-tile in TMEM buffer
     uint64_t* bar_p = bars + 5;       // [2] P^T, dS^T of a half written (256 arrivals)
-    uint64_t* bar_mm = bars + 7;      // dV, dK and dQ of a query tile done
+    uint64_t* bar_mm = bars + 7;      // dQ of a query tile (and every product before it) done
     uint64_t* bar_drain = bars + 8;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 10);
+    uint64_t* bar_st = bars + 9;      // a query tile's last dV, dK done: its Q/dO stage is free
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 11);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = H * HS;
@@ -379,6 +382,7 @@ __global__ void __maxnreg__(168)
         }
         mbar_init(bar_mm, 1);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_st, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -439,6 +443,16 @@ __global__ void __maxnreg__(168)
                 tc_fence_after();
                 const uint32_t pt_a = saddr(sPT) + hq * 16384, ds_a = saddr(sDS) + hq * 16384;
                 const uint32_t q_a = saddr(sQ + st * TILE) + hq * 8192, o_a = saddr(sO + st * TILE) + hq * 8192;
+                if (hq == 1) {
+                    // dQ of the tile first (both dS halves are in): its completion frees the P^T /
+                    // dS^T buffers for the next tile's first half
+                    const uint32_t dsa = saddr(sDS);
+#pragma unroll
+                    for (int k = 0; k < KT / 16; ++k)
+                        umma_bf16(tmem + 384 + (uint32_t)(it & 1) * 64, smem_desc(dsa + k * 2048, 16384, 1024),
+                                  smem_desc(k_a + k * 2048, 8192, 1024), id_q, k > 0);
+                    umma_commit(bar_mm);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     umma_bf16(tmem + 256, smem_desc(pt_a + k * 32, 16, 1024), smem_desc(o_a + k * 2048, 8192, 1024),
@@ -446,14 +460,7 @@ __global__ void __maxnreg__(168)
                     umma_bf16(tmem + 320, smem_desc(ds_a + k * 32, 16, 1024), smem_desc(q_a + k * 2048, 8192, 1024),
                               id_kv, (u > 0 || k > 0) ? 1u : 0u);
                 }
-                if (hq == 1) {
-                    const uint32_t dsa = saddr(sDS);
-#pragma unroll
-                    for (int k = 0; k < KT / 16; ++k)
-                        umma_bf16(tmem + 384, smem_desc(dsa + k * 2048, 16384, 1024),
-                                  smem_desc(k_a + k * 2048, 8192, 1024), id_q, k > 0);
-                    umma_commit(bar_mm);
-                }
+                if (hq == 1) umma_commit(bar_st);
                 if (u + 2 < n_u) {
                     if (hq == 0) {  // the next tile's Q/dO
                         const int ns = (it + 1) & 1;
@@ -467,8 +474,8 @@ __global__ void __maxnreg__(168)
                     issue_s(u + 2);
                 }
                 if (hq == 1 && it + 2 < n_it) {
-                    // stage st (this tile's Q, dO) is free once dV, dK and dQ of the tile are done
-                    if (!mbar_wait(bar_mm, it & 1, abort_flag, WAIT_NS)) {
+                    // stage st (this tile's Q, dO) is free once the tile's last dV, dK are done
+                    if (!mbar_wait(bar_st, it & 1, abort_flag, WAIT_NS)) {
                         ok = false;
                         break;
                     }
@@ -499,9 +506,9 @@ __global__ void __maxnreg__(168)
         const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
         const float sl2 = 0.125f * 1.4426950408889634f;
         const float L2E = 1.4426950408889634f;
-        // Every compute thread makes the same named-barrier calls in the same order; a failed
-        // wait only skips work (and raises the abort flag so every other wait ends quickly),
-        // and each barrier ORs the failure so the choices after it are block-uniform.
+        // No block barrier in this loop: each warp loads its own lse / D values and drains
+        // its own 32 x 32 box of dQ. A failed wait only skips the warp's work and raises the
+        // abort flag, so every other wait in the CTA ends quickly.
         bool fail = false;
         auto note_fail = [&](bool ok_) {
             if (!ok_) {
@@ -509,46 +516,49 @@ __global__ void __maxnreg__(168)
                 *abort_flag = 1;
             }
         };
-        // lse (log2 units) or D of query tile t, one value per thread
-        auto ld_value = [&](int t) {
-            const int q = (first_qt + t) * QT + (tid & 127);
-            return q < T ? (tid < 128 ? lse[(int64_t)bh * T + q] * L2E : dvec[(int64_t)bh * T + q]) : 0.f;
+        float* myLD = sLD + warp * 128;            // [2 buffers][lse 32 | D 32]
+        uint8_t* myDQ = sDQ + warp * 4096;         // 32 rows x 128 bytes
+        // lane c's lse (log2 units) and D for query column c of this warp in sub-tile v
+        auto ld_pair = [&](int v, float& lv, float& dvv) {
+            const int q = (first_qt + (v >> 1)) * QT + (v & 1) * 64 + hf * 32 + lane;
+            lv = q < T ? lse[(int64_t)bh * T + q] * L2E : 0.f;
+            dvv = q < T ? dvec[(int64_t)bh * T + q] : 0.f;
         };
-        if (n_it > 0) sLD[tid] = ld_value(0);
-        float ld_next = n_it > 1 ? ld_value(1) : 0.f;
-        fail = named_bar_or(1, 256, fail);
-        // dQ of query tile t: TMEM -> swizzled staging -> TMA reduce-add (called block-uniformly)
+        float nl = 0.f, nd = 0.f;
+        if (n_u > 0) ld_pair(0, nl, nd);
+        // dQ of query tile t (TMEM buffer t % 2, complete): this warp's 32 rows x 32 columns
+        // through its swizzled staging box into the float32 accumulator by TMA reduce-add
         auto drain_dq = [&](int t) {
-            if (tid == 0) bulk_wait_read<0>();  // the previous reduce has read the staging tile
-            fail = named_bar_or(1, 256, fail);
-            if (!fail) {
-                tc_fence_after();
-                uint32_t qv[32];
-                tmem_ld32_nowait(lane_addr + 384 + hf * 32, qv);
-                tmem_wait_ld_only();
-                reg_fence32(qv);
-                uint8_t* box = sDQ + hf * TILE;
+            if (lane == 0) bulk_wait_read<0>();  // this warp's previous reduce has read the box
+            __syncwarp();
+            tc_fence_after();
+            uint32_t qv[32];
+            tmem_ld32_nowait(lane_addr + 384 + (uint32_t)(t & 1) * 64 + hf * 32, qv);
+            tmem_wait_ld_only();
+            reg_fence32(qv);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<float4*>(box + r * 128 + ((j ^ (r & 7)) << 4)) =
-                        make_float4(__uint_as_float(qv[4 * j]) * 0.125f, __uint_as_float(qv[4 * j + 1]) * 0.125f,
-                                    __uint_as_float(qv[4 * j + 2]) * 0.125f, __uint_as_float(qv[4 * j + 3]) * 0.125f);
-                fence_proxy_async_smem();
-                tc_fence_before();
-            }
-            fail = named_bar_or(1, 256, fail);
-            if (!fail && tid == 0) {
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4*>(myDQ + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                    make_float4(__uint_as_float(qv[4 * j]) * 0.125f, __uint_as_float(qv[4 * j + 1]) * 0.125f,
+                                __uint_as_float(qv[4 * j + 2]) * 0.125f, __uint_as_float(qv[4 * j + 3]) * 0.125f);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
                 // rows past this sequence carry dS = 0 (masked), so the whole box is added
-                const int y0 = row0 + (first_qt + t) * QT;
-                tma_reduce_add_2d(&tm_dq, sDQ, h * HS, y0);
-                tma_reduce_add_2d(&tm_dq, sDQ + TILE, h * HS + 32, y0);
+                tma_reduce_add_2d(&tm_dq, myDQ, h * HS + hf * 32, row0 + (first_qt + t) * QT + qd * 32);
                 bulk_commit();
             }
         };
         for (int u = 0; u < n_u; ++u) {
             const int it = u >> 1, hq = u & 1;
             const int q0 = (first_qt + it) * QT;
-            const float* sL = sLD + (it & 1) * 256;
+            // this sub-tile's lse / D into the warp's buffer u % 2; the next sub-tile's on the way
+            float* L = myLD + (u & 1) * 64;
+            L[lane] = nl;
+            L[32 + lane] = nd;
+            if (u + 1 < n_u) ld_pair(u + 1, nl, nd);
+            __syncwarp();
             if (!fail) note_fail(__all_sync(0xffffffffu, mbar_wait(&bar_s[hq], it & 1, abort_flag, WAIT_NS)));
             if (!fail) {
                 tc_fence_after();
@@ -566,8 +576,7 @@ __global__ void __maxnreg__(168)
                 hi = min(hi, T - q0 - cbase);                 // ragged last query tile
                 if (kk >= T) hi = 0;                          // padding key rows
                 const bool masked = lo > 0 || hi < 32;
-                const float* L = sL + cbase;
-                const float* D = sL + 128 + cbase;
+                const float* D = L + 32;
                 uint32_t pw[16], qw[16];
 #pragma unroll
                 for (int c8 = 0; c8 < 32; c8 += 8) {
@@ -597,7 +606,9 @@ __global__ void __maxnreg__(168)
                         qw[c >> 1] = *reinterpret_cast<uint32_t*>(&u2);
                     }
                 }
-                // half hq of P^T / dS^T is free once the previous tile's dV, dK, dQ are done
+                // the P^T / dS^T buffers are free for a new tile once the previous tile's dQ
+                // (issued after its last dS) is done; the half-1 products of the previous tile
+                // finished before this tile's S^T of half 1 (waited above)
                 if (hq == 0 && it > 0)
                     note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (it - 1) & 1, abort_flag, WAIT_NS)));
                 if (!fail) {
@@ -613,23 +624,16 @@ __global__ void __maxnreg__(168)
                     mbar_arrive(&bar_p[hq]);
                 }
             }
-            if (hq == 0) {
-                // between the halves: the previous tile's dQ, and lse / D of the next tile
-                fail = named_bar_or(1, 256, fail);
-                if (it > 0) drain_dq(it - 1);
-                if (it + 1 < n_it) {
-                    sLD[((it + 1) & 1) * 256 + tid] = ld_next;
-                    if (it + 2 < n_it) ld_next = ld_value(it + 2);
-                }
-                fail = named_bar_or(1, 256, fail);
-            }
+            // the previous tile's dQ (double-buffered in TMEM; waited above) while the tensor
+            // core runs this tile's dQ, dV and dK
+            if (hq == 1 && it > 0 && !fail) drain_dq(it - 1);
         }
-        if (n_it > 0) {
-            if (!fail) note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (n_it - 1) & 1, abort_flag, WAIT_NS)));
-            fail = named_bar_or(1, 256, fail);
-            drain_dq(n_it - 1);
+        if (n_it > 0 && !fail) {  // the last tile's dQ
+            note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (n_it - 1) & 1, abort_flag, WAIT_NS)));
+            if (!fail) drain_dq(n_it - 1);
         }
-        if (tid == 0) bulk_wait_all();
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
         if (fail) {
             *abort_flag = 1;
             report(err, GK_ERR_TIMEOUT);
@@ -762,7 +766,7 @@ gk_status attn_bwd_tc(gk_ctx* ctx, const void* qkv, const void* y, const float* 
     float* dq_acc = (float*)(ws + dvec_bytes);
     CUtensorMap map_qkv, map_dy, map_dq;
     if (!make_map(&map_qkv, qkv, 3 * C, rows, 3 * C, 128) || !make_map(&map_dy, dy, C, rows, C, 128) ||
-        !make_map_f32(&map_dq, dq_acc, C, rows, C, 32, 128))
+        !make_map_f32(&map_dq, dq_acc, C, rows, C, 32, 32))
         return GK_ERR_UNSUPPORTED;
     attn_dvec_zero_kernel<<<(unsigned)cdiv(rows * 32, 256), 256, 0, ctx->stream>>>(
         (const __nv_bfloat16*)y, (const __nv_bfloat16*)dy, dvec, dq_acc, rows, T, H);

@@ -45,7 +45,7 @@ __device__ __forceinline__ uint32_t p_offset(int r, int c) {
 // Registers are granted to a block in groups of four warps, so 9- or 10-warp blocks are
 // budgeted as 12 warps: 168 registers per thread at most (hence __maxnreg__(168)).
 constexpr int FWD_THREADS = 320;
-constexpr size_t FWD_SMEM_BYTES = 10 * TILE + 1024 + 256;  // Q_A, Q_B, K[2], V[2], P_A, P_B
+constexpr size_t FWD_SMEM_BYTES = 6 * TILE + 1024 + 256;  // Q_A, Q_B, K[2], V[2]
 
 __global__ void __maxnreg__(168)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ y,
@@ -55,8 +55,7 @@ __global__ void __maxnreg__(168)
     uint8_t* sQ = smem;              // [2] (A, B)
     uint8_t* sK = smem + 2 * TILE;   // [2] stages
     uint8_t* sV = smem + 4 * TILE;   // [2] stages
-    uint8_t* sP = smem + 6 * TILE;   // [2] groups x two halves
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 10 * TILE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * TILE);
     uint64_t* bar_q = bars;          // Q_A and Q_B landed
     uint64_t* kv_full = bars + 1;    // [2]
     uint64_t* kv_empty = bars + 3;   // [2]
@@ -147,12 +146,12 @@ __global__ void __maxnreg__(168)
                     ok = mbar_wait(&bar_p[g], j & 1, nullptr, WAIT_NS);
                     if (!ok) break;
                     tc_fence_after();
-                    // O_g(j) = P_g V_j
-                    uint32_t p_a = saddr(sP + g * 2 * TILE), v_a = saddr(sV + (j & 1) * TILE);
+                    // O_g(j) = P_g V_j, P_g read from TMEM (bf16 pairs over S_g's first 64 columns)
+                    const uint32_t v_a = saddr(sV + (j & 1) * TILE);
 #pragma unroll
                     for (int k = 0; k < KT / 16; ++k)
-                        umma_bf16(tmem + 256 + g * 64, smem_desc(p_a + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                                  smem_desc(v_a + k * 2048, 8192, 1024), id_o, (j > 0 || k > 0) ? 1u : 0u);
+                        umma_bf16_ts(tmem + 256 + g * 64, tmem + g * 128 + k * 8, smem_desc(v_a + k * 2048, 8192, 1024),
+                                     id_o, (j > 0 || k > 0) ? 1u : 0u);
                     if (j == ng - 1) umma_commit(&bar_o[g]);
                     // the last reader of K/V stage j frees it for the tile j + 2
                     if (g == 1 || j >= nB) umma_commit(&kv_empty[j & 1]);
@@ -189,7 +188,6 @@ __global__ void __maxnreg__(168)
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t o_addr = lane_addr + 256 + g * 64;
         const float sl2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
-        uint8_t* myP = sP + g * 2 * TILE;
         // m_ref: the reference the row's P and running sum l are taken against, in log2
         // units; it moves (and O in TMEM is rescaled) only when the row maximum exceeds it by
         // more than 8, so P <= 2^8 and most key tiles skip the rescale.
@@ -237,24 +235,22 @@ __global__ void __maxnreg__(168)
                 l *= corr;
                 m_ref = m_new;
             }
-            // P = 2^(S * sl2 - m_ref), bf16, into the K-major swizzled tile the MMA reads
+            // P = 2^(S * sl2 - m_ref) as bf16 pairs into TMEM over S_g's first 64 columns (this
+            // thread's row, already read), where the P V product takes its A operand
             float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                uint32_t pw[16];
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint32_t pw[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float p0 = ex2_hw(fmaf(__uint_as_float(sv[c][i + 2 * e]), sl2, -m_ref));
-                        float p1 = ex2_hw(fmaf(__uint_as_float(sv[c][i + 2 * e + 1]), sl2, -m_ref));
-                        ps[2 * e] += p0;
-                        ps[2 * e + 1] += p1;
-                        __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                        pw[e] = *reinterpret_cast<uint32_t*>(&t2);
-                    }
-                    *reinterpret_cast<uint4*>(myP + p_offset(r, c * 32 + i)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                for (int e = 0; e < 16; ++e) {
+                    float p0 = ex2_hw(fmaf(__uint_as_float(sv[c][2 * e]), sl2, -m_ref));
+                    float p1 = ex2_hw(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl2, -m_ref));
+                    ps[(2 * e) & 7] += p0;
+                    ps[(2 * e + 1) & 7] += p1;
+                    __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                    pw[e] = *reinterpret_cast<uint32_t*>(&t2);
                 }
+                tmem_st16(lane_addr + g * 128 + c * 16, pw);
             }
             l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             // tcgen05.ld / st are warp-collective: the warp rescales if any of its rows must
@@ -270,9 +266,8 @@ __global__ void __maxnreg__(168)
                     for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
                     tmem_st32(o_addr + c * 32, ov);
                 }
-                tmem_wait_st();
             }
-            fence_proxy_async_smem();  // P's generic-proxy stores -> visible to the tensor core
+            tmem_wait_st();  // P (and a rescaled O) in TMEM before the MMA warp is told
             tc_fence_before();
             mbar_arrive(&bar_p[g]);
         }

@@ -816,7 +816,7 @@ gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t*
     GK_TRY(gk_embedding_fwd(ctx, ids, w.t(GK_T_WTE), w.t(GK_T_WPE), kv->x, B, Tp, C, c.V));
     for (int l = 0; l < c.L; ++l) {
         GK_TRY(gk_layernorm_fwd(ctx, kv->x, w.t(GK_T_LN1_W, l), w.t(GK_T_LN1_B, l), kv->ln, GK_F32, nullptr, nullptr, N,
-                                C, 1e-5f));
+                                C, 1e-5f, nullptr));
         GK_TRY(gk_matmul_fwd(ctx, GK_F32, kv->ln, C, w.t(GK_T_ATTN_W, l), 3 * C, 0, w.t(GK_T_ATTN_B, l), nullptr, 0,
                              kv->qkv, 3 * C, GK_F32, N, C, 3 * C, GK_ACT_NONE, nullptr, 0, nullptr, nullptr));
         kv_write_prefill_kernel<<<(unsigned)cdiv(N * C, 256), 256, 0, ctx->stream>>>(kv->qkv, kv->cache, l, B, Tp, H,
@@ -826,7 +826,7 @@ gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t*
         GK_TRY(gk_matmul_fwd(ctx, GK_F32, kv->y, C, w.t(GK_T_ATTNPROJ_W, l), C, 0, w.t(GK_T_ATTNPROJ_B, l), kv->x, C,
                              kv->x, C, GK_F32, N, C, C, GK_ACT_NONE, nullptr, 0, nullptr, nullptr));
         GK_TRY(gk_layernorm_fwd(ctx, kv->x, w.t(GK_T_LN2_W, l), w.t(GK_T_LN2_B, l), kv->ln, GK_F32, nullptr, nullptr, N,
-                                C, 1e-5f));
+                                C, 1e-5f, nullptr));
         GK_TRY(gk_matmul_fwd(ctx, GK_F32, kv->ln, C, w.t(GK_T_FC_W, l), 4 * C, 0, w.t(GK_T_FC_B, l), nullptr, 0, kv->h,
                              4 * C, GK_F32, N, C, 4 * C, GK_ACT_GELU, kv->pre, 4 * C, nullptr, nullptr));
         GK_TRY(gk_matmul_fwd(ctx, GK_F32, kv->h, 4 * C, w.t(GK_T_MLPPROJ_W, l), C, 0, w.t(GK_T_MLPPROJ_B, l), kv->x, C,
@@ -835,7 +835,7 @@ gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t*
     gather_last_kernel<<<(unsigned)cdiv((int64_t)B * C, 256), 256, 0, ctx->stream>>>(kv->x, B, Tp, C, kv->last);
     GK_TRY(launched(ctx, "gather_last"));
     GK_TRY(gk_layernorm_fwd(ctx, kv->last, w.t(GK_T_LNF_W), w.t(GK_T_LNF_B), kv->ln, GK_F32, nullptr, nullptr, B, C,
-                            1e-5f));
+                            1e-5f, nullptr));
     GK_TRY(lm_head(ctx, kv, kv->ln, nullptr, nullptr, w.t(GK_T_WTE), last_logits, c.V));
     set_state_kernel<<<1, 1, 0, ctx->stream>>>(kv->state, Tp, 0);
     GK_TRY(launched(ctx, "set_state"));

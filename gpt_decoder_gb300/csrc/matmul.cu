@@ -162,6 +162,12 @@ gk_status gk_matmul_fwd(gk_ctx* ctx, int dtype, const void* X, int64_t ldx, cons
     g.C = Y; g.ldc = ldy; g.c_dtype = y_dtype == GK_BF16X2 ? GK_BF16 : y_dtype;
     if (y_dtype == GK_BF16X2) g.c_plane = N * ldy;
     g.bias = bias; g.residual = residual; g.ldr = ldr;
+    if (residual && (const void*)residual == Y && ldr == ldy && act == GK_ACT_NONE) {
+        // in place, Y += X W + bias: an accumulation, which the tensor-core epilogue does by TMA
+        // reduce-add (no read of the residual through the SM) with the same sum
+        g.residual = nullptr;
+        g.accumulate = true;
+    }
     g.A_lo = X_lo; g.B_lo = W_lo;
     if (act == GK_ACT_GELU) {
         g.epi = EPI_GELU; g.aux = preact; g.ldaux = ldp; g.aux_dtype = g.c_dtype;

@@ -101,7 +101,8 @@ __global__ void embedding_bwd_wpe_kernel(const float* __restrict__ dx, float* __
 template <int VPT, typename TY>
 __global__ void layernorm_fwd_warp_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
                                           const float* __restrict__ beta, TY* __restrict__ y, float* mean_out,
-                                          float* rstd_out, int64_t rows, int C, float eps, int64_t lo_plane) {
+                                          float* rstd_out, int64_t rows, int C, float eps, int64_t lo_plane,
+                                          float* __restrict__ x_copy) {
     int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -129,14 +130,28 @@ __global__ void layernorm_fwd_warp_kernel(const float* __restrict__ x, const flo
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         int c = (i * 32 + lane) * 4;
+        if (x_copy) *reinterpret_cast<float4*>(x_copy + row * C + c) = v[i];
         float4 g = *reinterpret_cast<const float4*>(gamma + c);
         float4 b = *reinterpret_cast<const float4*>(beta + c);
         float o[4] = {(v[i].x - mu) * rs * g.x + b.x, (v[i].y - mu) * rs * g.y + b.y,
                       (v[i].z - mu) * rs * g.z + b.z, (v[i].w - mu) * rs * g.w + b.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            store_from_f32(yr + c + k, o[k]);
-            if (lo_plane) store_from_f32(yr + c + k + lo_plane, o[k] - to_f32(yr[c + k]));
+        if constexpr (sizeof(TY) == 4) {
+            *reinterpret_cast<float4*>(yr + c) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+            // four bf16 in one 8-byte store; the low plane holds what the rounding dropped
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]), h1 = __floats2bfloat162_rn(o[2], o[3]);
+            uint2 hw;
+            hw.x = *reinterpret_cast<uint32_t*>(&h0);
+            hw.y = *reinterpret_cast<uint32_t*>(&h1);
+            *reinterpret_cast<uint2*>(yr + c) = hw;
+            if (lo_plane) {
+                __nv_bfloat162 l0 = __floats2bfloat162_rn(o[0] - __low2float(h0), o[1] - __high2float(h0));
+                __nv_bfloat162 l1 = __floats2bfloat162_rn(o[2] - __low2float(h1), o[3] - __high2float(h1));
+                uint2 lw;
+                lw.x = *reinterpret_cast<uint32_t*>(&l0);
+                lw.y = *reinterpret_cast<uint32_t*>(&l1);
+                *reinterpret_cast<uint2*>(yr + c + lo_plane) = lw;
+            }
         }
     }
 }
@@ -157,7 +172,8 @@ __device__ float block_sum(float v, float* red) {
 template <typename TY>
 __global__ void layernorm_fwd_block_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
                                            const float* __restrict__ beta, TY* __restrict__ y, float* mean_out,
-                                           float* rstd_out, int64_t rows, int C, float eps, int64_t lo_plane) {
+                                           float* rstd_out, int64_t rows, int C, float eps, int64_t lo_plane,
+                                           float* __restrict__ x_copy) {
     extern __shared__ float srow[];
     __shared__ float red[32];
     int64_t row = blockIdx.x;
@@ -166,6 +182,7 @@ __global__ void layernorm_fwd_block_kernel(const float* __restrict__ x, const fl
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
         float a = xr[c];
         srow[c] = a;
+        if (x_copy) x_copy[row * C + c] = a;
         s += a;
     }
     float mu = block_sum(s, red) / C;
@@ -641,14 +658,18 @@ gk_status gk_embedding_bwd(gk_ctx* ctx, const int32_t* ids, const float* dx, flo
 }
 
 gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, const float* beta, void* y, int y_dtype,
-                           float* mean, float* rstd, int64_t rows, int C, float eps) {
+                           float* mean, float* rstd, int64_t rows, int C, float eps, float* x_copy) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, x && gamma && beta && y && rows > 0 && C > 0, GK_ERR_ARG, "gk_layernorm_fwd: bad argument");
     GK_REQUIRE(ctx, y_dtype == GK_F32 || y_dtype == GK_BF16 || y_dtype == GK_BF16X2, GK_ERR_ARG,
                "gk_layernorm_fwd: bad dtype");
     int64_t lo_plane = y_dtype == GK_BF16X2 ? rows * C : 0;
     if (y_dtype == GK_BF16X2) y_dtype = GK_BF16;
-    bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(gamma) && aligned16(beta);
+    GK_REQUIRE(ctx, !x_copy || (x_copy + rows * C <= x || x + rows * C <= x_copy), GK_ERR_ARG,
+               "gk_layernorm_fwd: x_copy overlaps x");
+    bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(gamma) && aligned16(beta) &&
+                     (!x_copy || aligned16(x_copy)) &&
+                     (y_dtype == GK_F32 ? aligned16(y) : ((uintptr_t)y & 7) == 0);
     if (warp_path) {
         int wpb = 4;
         unsigned grid = (unsigned)cdiv(rows, wpb);
@@ -657,10 +678,11 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
     case V:                                                                                                     \
         if (y_dtype == GK_F32)                                                                                  \
             layernorm_fwd_warp_kernel<V, float><<<grid, wpb * 32, 0, ctx->stream>>>(x, gamma, beta, (float*)y,  \
-                                                                                   mean, rstd, rows, C, eps, lo_plane);   \
+                                                                                   mean, rstd, rows, C, eps, lo_plane, \
+                                                                                   x_copy);                          \
         else                                                                                                    \
             layernorm_fwd_warp_kernel<V, __nv_bfloat16><<<grid, wpb * 32, 0, ctx->stream>>>(                    \
-                x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane);                                   \
+                x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane, x_copy);                    \
         break;
         switch (vpt) {
             LN_FWD_CASE(1) LN_FWD_CASE(2) LN_FWD_CASE(3) LN_FWD_CASE(4)
@@ -675,12 +697,12 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
     if (y_dtype == GK_F32) {
         cudaFuncSetAttribute(layernorm_fwd_block_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         layernorm_fwd_block_kernel<float><<<(unsigned)rows, threads, smem, ctx->stream>>>(x, gamma, beta, (float*)y, mean,
-                                                                                         rstd, rows, C, eps, 0);
+                                                                                         rstd, rows, C, eps, 0, x_copy);
     } else {
         cudaFuncSetAttribute(layernorm_fwd_block_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
         layernorm_fwd_block_kernel<__nv_bfloat16><<<(unsigned)rows, threads, smem, ctx->stream>>>(
-            x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane);
+            x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane, x_copy);
     }
     return launched(ctx, "layernorm_fwd");
 }

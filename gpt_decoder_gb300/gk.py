@@ -60,7 +60,7 @@ _SIGS = {
     "gk_launch_count": (I64, [P]),
     "gk_embedding_fwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_embedding_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
-    "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32]),
+    "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32, P]),
     "gk_lmhead_ce_fwd": (I32, [P, I32, P, I64, P, I64, P, P, P, I64, I64, I64]),
     "gk_lmhead_ce_bwd": (I32, [P, I32, P, I64, P, I64, P, P, P, P, I64, I32, P, I64, P, I64, I64, I64, I64]),
     "gk_decode_run": (I32, [P, P, P, P, P, P, P, I32]),
@@ -165,9 +165,9 @@ def gk_embedding_bwd(ctx, ids, dx, dwte, dwpe, B, T, C, V):
                   "gk_embedding_bwd")
 
 
-def gk_layernorm_fwd(ctx, x, gamma, beta, y, y_dtype, mean, rstd, rows, C, eps=1e-5):
+def gk_layernorm_fwd(ctx, x, gamma, beta, y, y_dtype, mean, rstd, rows, C, eps=1e-5, x_copy=None):
     return _check(ctx, _lib.gk_layernorm_fwd(ctx.handle, _p(x), _p(gamma), _p(beta), _p(y), y_dtype, _p(mean),
-                                             _p(rstd), rows, C, eps), "gk_layernorm_fwd")
+                                             _p(rstd), rows, C, eps, _p(x_copy)), "gk_layernorm_fwd")
 
 
 def gk_layernorm_bwd(ctx, x, gamma, mean, rstd, dy, dx, accumulate_dx, dx_bf16, dgamma, dbeta, rows, C,

@@ -205,22 +205,24 @@ class Gpt:
             lo = (lambda buf: buf[1]) if sp else (lambda buf: None)
             wl = (lambda which: self.w_lo(which, l)) if sp else (lambda which: None)
             x_in, x_mid, x_out = self.xs[2 * l], self.xs[2 * l + 1], self.xs[2 * l + 2]
+            # the LayerNorms also copy their input into the next residual buffer, which the
+            # projection then adds into in place (a TMA reduce-add in the GEMM epilogue)
             gk.gk_layernorm_fwd(c, x_in, self.w(gk.GK_T_LN1_W, l), self.w(gk.GK_T_LN1_B, l), self.ln1[l], lnd,
-                                self.mu1[l], self.rs1[l], N, C, EPS)
+                                self.mu1[l], self.rs1[l], N, C, EPS, x_copy=x_mid)
             self._mm_fwd(c, dt, self.ln1[l], C, self.w(gk.GK_T_ATTN_W, l, bw), 3 * C, 0,
                          self.w(gk.GK_T_ATTN_B, l), None, 0, self.qkv[l], 3 * C, dt, N, C, 3 * C,
                          gk.GK_ACT_NONE, None, 0, lo(self.ln1[l]), wl(gk.GK_T_ATTN_W))
             gk.gk_attn_fwd(c, dt, self.qkv[l], self.y[l], self.lse[l], B, T, H, hs)
             self._mm_fwd(c, dt, self.y[l], C, self.w(gk.GK_T_ATTNPROJ_W, l, bw), C, 0,
-                         self.w(gk.GK_T_ATTNPROJ_B, l), x_in, C, x_mid, C, gk.GK_F32, N, C, C,
+                         self.w(gk.GK_T_ATTNPROJ_B, l), x_mid, C, x_mid, C, gk.GK_F32, N, C, C,
                          gk.GK_ACT_NONE, None, 0, None, wl(gk.GK_T_ATTNPROJ_W))
             gk.gk_layernorm_fwd(c, x_mid, self.w(gk.GK_T_LN2_W, l), self.w(gk.GK_T_LN2_B, l), self.ln2[l], lnd,
-                                self.mu2[l], self.rs2[l], N, C, EPS)
+                                self.mu2[l], self.rs2[l], N, C, EPS, x_copy=x_out)
             self._mm_fwd(c, dt, self.ln2[l], C, self.w(gk.GK_T_FC_W, l, bw), 4 * C, 0,
                          self.w(gk.GK_T_FC_B, l), None, 0, self.h[l], 4 * C, lnd, N, C, 4 * C,
                          gk.GK_ACT_GELU, self.pre[l], 4 * C, lo(self.ln2[l]), wl(gk.GK_T_FC_W))
             self._mm_fwd(c, dt, self.h[l], 4 * C, self.w(gk.GK_T_MLPPROJ_W, l, bw), C, 0,
-                         self.w(gk.GK_T_MLPPROJ_B, l), x_mid, C, x_out, C, gk.GK_F32, N, 4 * C, C,
+                         self.w(gk.GK_T_MLPPROJ_B, l), x_out, C, x_out, C, gk.GK_F32, N, 4 * C, C,
                          gk.GK_ACT_NONE, None, 0, lo(self.h[l]), wl(gk.GK_T_MLPPROJ_W))
         gk.gk_layernorm_fwd(c, self.xs[-1], self.w(gk.GK_T_LNF_W), self.w(gk.GK_T_LNF_B), self.lnf, self.dt, self.muf,
                             self.rsf, N, C, EPS)

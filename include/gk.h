@@ -97,10 +97,13 @@ gk_status gk_embedding_bwd(gk_ctx* ctx, const int32_t* ids, const float* dx, flo
 /* Per row: y = (x - mean) * rstd * gamma + beta, rstd = 1/sqrt(var + eps), var biased.
  * [LM1] op table (LayerNorm); eps 1e-5 in GPT-2. x float32 [rows, C] contiguous; y is
  * `y_dtype` [rows, C] (GK_BF16X2: two planes of rows * C); mean and rstd float32 [rows] (saved
- * for backward, may be NULL). */
+ * for backward, may be NULL). x_copy (float32 [rows, C], may be NULL, must not overlap x)
+ * receives a copy of x: the residual stream's next buffer, which a projection then adds into
+ * in place (x_next = x + f(y), "residual reuse" of the GPT-2 block), while x stays as the
+ * saved input of this LayerNorm. */
 gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, const float* beta,
                            void* y, int y_dtype, float* mean, float* rstd, int64_t rows, int C,
-                           float eps);
+                           float eps, float* x_copy);
 
 /* Backward of gk_layernorm_fwd for upstream dy (float32 [rows, C]):
  *   dx (=, or += if accumulate_dx) rstd * (dy*gamma - mean(dy*gamma) - xhat*mean(dy*gamma*xhat));

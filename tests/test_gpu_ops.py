@@ -104,9 +104,11 @@ def test_layernorm_fwd(gkctx, rows, C, ydt):
     torch = _t()
     y = torch.empty(rows, C, device="cuda", dtype=torch.float32 if ydt == "f32" else torch.bfloat16)
     mean, rstd = torch.empty(rows, device="cuda"), torch.empty(rows, device="cuda")
+    xc = torch.full((rows, C), float("nan"), device="cuda")
     gk.gk_layernorm_fwd(gkctx, dev(x), dev(gm), dev(bt), y, gk.GK_F32 if ydt == "f32" else gk.GK_BF16, mean, rstd,
-                        rows, C, 1e-5)
+                        rows, C, 1e-5, x_copy=xc)
     gk.gk_sync(gkctx)
+    assert np.array_equal(host(xc), x.astype(np.float32))  # the residual-stream copy is exact
     ry, rm, rr = ops.layernorm_fwd(x, gm, bt)
     tol = 2e-5 if ydt == "f32" else 2e-2
     assert np.abs(host(y) - ry).max() < tol * max(1.0, np.abs(ry).max() / 4)
@@ -214,6 +216,29 @@ def test_matmul_fwd_epilogues(gkctx, dt):
     assert rel_l2(y, ref) < 2e-5
     y, ref = _matmul_case(gkctx, 300, 96, 384, 0, dt, True, False, True, 530)
     assert rel_l2(y, ref) < 2e-5
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("N,K,M", [(300, 96, 384), (4096, 768, 768), (77, 64, 200)])
+def test_matmul_in_place_residual_is_bit_identical(gkctx, dt, N, K, M):
+    """Y = X W + b + Y in place (an accumulation, TMA reduce-add on the tensor cores) equals
+    the out-of-place residual result bit for bit."""
+    from gpt_decoder_gb300 import gk
+
+    torch = _t()
+    x, w, b, r = normal(540, N, K), normal(541, K, M), normal(542, M), normal(543, N, M)
+    if dt == "bf16":
+        x, w = bf16_round(x), bf16_round(w)
+    gdt = gk.GK_F32 if dt == "f32" else gk.GK_BF16
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    dx_, dw_, db_ = dev(x, tdt), dev(w, tdt), dev(b)
+    y_out = torch.empty(N, M, device="cuda")
+    gk.gk_matmul_fwd(gkctx, gdt, dx_, K, dw_, M, 0, db_, dev(r), M, y_out, M, gk.GK_F32, N, K, M)
+    y_in = dev(r)
+    gk.gk_matmul_fwd(gkctx, gdt, dx_, K, dw_, M, 0, db_, y_in, M, y_in, M, gk.GK_F32, N, K, M)
+    gk.gk_sync(gkctx)
+    assert np.array_equal(host(y_in), host(y_out))
+    assert rel_l2(host(y_in), ops.matmul_fwd(x, w) + b + r) < 2e-5
 
 
 def _matmul_bwd_case(gkctx, N, K, M, transW, dt, acc, gelu, seed):

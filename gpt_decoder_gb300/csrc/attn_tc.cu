@@ -28,6 +28,9 @@ constexpr int QT = 128, KT = 128, HS = 64;
 constexpr uint32_t TILE = 128 * 64 * 2;                 // one 128 x 64 bf16 tile, 16 KB
 constexpr uint64_t WAIT_NS = 1000000000ull;
 
+// One of two descriptors (kept in registers: an indexed array would live in local memory).
+__device__ __forceinline__ uint64_t pick(uint64_t d0, uint64_t d1, int i) { return i ? d1 : d0; }
+
 // Byte offset of element (row r, column c) of a [128 x 128] bf16 tile stored as two K-major
 // 128-byte-swizzle halves (columns 0..63, 64..127), each 128 rows x 128 bytes.
 __device__ __forceinline__ uint32_t p_offset(int r, int c) {
@@ -68,10 +71,11 @@ __global__ void __maxnreg__(168)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = H * HS;
     const int n_qt = (T + QT - 1) / QT;
-    const int pair = gridDim.x - 1 - blockIdx.x;  // heaviest pairs first
+    // blocks are dispatched x fastest: every (batch, head) of the heaviest pair goes first
+    const int pair = gridDim.y - 1 - blockIdx.y;
     const int qa = 2 * pair;
     const bool has_b = qa + 1 < n_qt;
-    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int row0 = b * T;
     const int n_kv = has_b ? qa + 2 : qa + 1;      // key tiles the CTA needs (B needs one more)
 
@@ -121,62 +125,75 @@ __global__ void __maxnreg__(168)
             }
         }
     } else if (warp == 9) {
-        if (lane == 0) {
-            const uint32_t id_s = instr_desc_bf16(false, false, 128, 128);
-            const uint32_t id_o = instr_desc_bf16(false, true, 128, 64);
-            const int nA = qa + 1, nB = has_b ? qa + 2 : 0;
-            bool issued = false;
-            bool ok = mbar_wait(bar_q, 0, nullptr, WAIT_NS) && mbar_wait(&kv_full[0], 0, nullptr, WAIT_NS);
-            if (ok) {
-                tc_fence_after();
+        // The whole warp walks the schedule (warp-uniform descriptors); one elected lane
+        // issues each group of MMAs together with the commits that track them.
+        const uint32_t id_s = instr_desc_bf16(false, false, 128, 128);
+        const uint32_t id_o = instr_desc_bf16(false, true, 128, 64);
+        const int nA = qa + 1, nB = has_b ? qa + 2 : 0;
+        const uint64_t q_d0 = smem_desc(saddr(sQ), 16, 1024), q_d1 = smem_desc(saddr(sQ + TILE), 16, 1024);
+        const uint64_t k_d0 = smem_desc(saddr(sK), 16, 1024), k_d1 = smem_desc(saddr(sK + TILE), 16, 1024);
+        const uint64_t v_d0 = smem_desc(saddr(sV), 8192, 1024), v_d1 = smem_desc(saddr(sV + TILE), 8192, 1024);
+        bool issued = false;
+        bool ok = __all_sync(0xffffffffu,
+                             mbar_wait(bar_q, 0, nullptr, WAIT_NS) && mbar_wait(&kv_full[0], 0, nullptr, WAIT_NS));
+        if (ok) {
+            tc_fence_after();
+            if (elect_one()) {
                 for (int g = 0; g < (has_b ? 2 : 1); ++g) {
-                    uint32_t q_a = saddr(sQ + g * TILE), k_a = saddr(sK);
 #pragma unroll
                     for (int k = 0; k < HS / 16; ++k)
-                        umma_bf16(tmem + g * 128, smem_desc(q_a + k * 32, 16, 1024), smem_desc(k_a + k * 32, 16, 1024),
-                                  id_s, k > 0);
+                        umma_bf16(tmem + g * 128, desc_add(pick(q_d0, q_d1, g), k * 32), desc_add(k_d0, k * 32), id_s, k > 0);
                     umma_commit(&bar_s[g]);
                 }
-                issued = true;
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                for (int g = 0; g < 2 && ok; ++g) {
-                    const int ng = g ? nB : nA;
-                    if (j >= ng) continue;
-                    ok = mbar_wait(&bar_p[g], j & 1, nullptr, WAIT_NS);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // O_g(j) = P_g V_j, P_g read from TMEM (bf16 pairs over S_g's first 64 columns)
-                    const uint32_t v_a = saddr(sV + (j & 1) * TILE);
+            __syncwarp();
+            issued = true;
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+            for (int g = 0; g < 2 && ok; ++g) {
+                const int ng = g ? nB : nA;
+                if (j >= ng) continue;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_p[g], j & 1, nullptr, WAIT_NS));
+                if (!ok) break;
+                tc_fence_after();
+                // O_g(j) = P_g V_j, P_g read from TMEM (bf16 pairs over S_g's first 64 columns)
+                if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < KT / 16; ++k)
-                        umma_bf16_ts(tmem + 256 + g * 64, tmem + g * 128 + k * 8, smem_desc(v_a + k * 2048, 8192, 1024),
-                                     id_o, (j > 0 || k > 0) ? 1u : 0u);
+                        umma_bf16_ts(tmem + 256 + g * 64, tmem + g * 128 + k * 8, desc_add(pick(v_d0, v_d1, j & 1), k * 2048), id_o,
+                                     (j > 0 || k > 0) ? 1u : 0u);
                     if (j == ng - 1) umma_commit(&bar_o[g]);
                     // the last reader of K/V stage j frees it for the tile j + 2
                     if (g == 1 || j >= nB) umma_commit(&kv_empty[j & 1]);
-                    // S_g(j + 1), once K_{j+1} has landed
-                    if (j + 1 < ng) {
-                        if (g == 0 || j + 1 >= nA) {
-                            ok = mbar_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, nullptr, WAIT_NS);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        uint32_t q_a = saddr(sQ + g * TILE), k_a = saddr(sK + ((j + 1) & 1) * TILE);
+                }
+                __syncwarp();
+                // S_g(j + 1), once K_{j+1} has landed
+                if (j + 1 < ng) {
+                    if (g == 0 || j + 1 >= nA) {
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, nullptr, WAIT_NS));
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    if (elect_one()) {
 #pragma unroll
                         for (int k = 0; k < HS / 16; ++k)
-                            umma_bf16(tmem + g * 128, smem_desc(q_a + k * 32, 16, 1024),
-                                      smem_desc(k_a + k * 32, 16, 1024), id_s, k > 0);
+                            umma_bf16(tmem + g * 128, desc_add(pick(q_d0, q_d1, g), k * 32),
+                                      desc_add(pick(k_d0, k_d1, (j + 1) & 1), k * 32), id_s, k > 0);
                         umma_commit(&bar_s[g]);
                     }
+                    __syncwarp();
                 }
             }
-            if (!ok) {
-                failed = true;
-                if (issued) {
+        }
+        if (!ok) {
+            failed = true;
+            if (issued) {
+                if (elect_one()) {
                     umma_commit(bar_drain);
                     mbar_wait(bar_drain, 0, nullptr, WAIT_NS / 5);
                 }
+                __syncwarp();
             }
         }
     } else {
@@ -359,9 +376,11 @@ __global__ void __maxnreg__(168)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = H * HS;
-    const int kt = blockIdx.x;  // heaviest (earliest keys) first
+    // blocks are dispatched x fastest: every (batch, head) of the heaviest key tile (the
+    // earliest keys, which meet the most queries) goes first
+    const int kt = blockIdx.y;
     const int k0 = kt * KT;
-    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int row0 = b * T;
     const int n_qt = (T + QT - 1) / QT;
     const int first_qt = k0 / QT;
@@ -388,110 +407,133 @@ __global__ void __maxnreg__(168)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 8) {
-        if (lane == 0 && n_it > 0) {
+        // TMA copies and MMAs. The whole warp walks the schedule (warp-uniform descriptors);
+        // one elected lane issues each group of copies or MMAs with the commits that track them.
+        if (n_it > 0) {
             const uint32_t id_s = instr_desc_bf16(false, false, 128, 64);   // S^T, dP^T of a sub-tile
             const uint32_t id_kv = instr_desc_bf16(false, true, 128, 64);   // dV, dK: B (dO, Q) MN-major
             const uint32_t id_q = instr_desc_bf16(true, true, 128, 64);     // dQ: A (dS) and B (K) MN-major
-            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_dy) : "memory");
-            mbar_expect_tx(bar_kv, 2 * TILE);
-            tma_load_2d(&tm_qkv, bar_kv, sK, C + h * HS, row0 + k0);
-            tma_load_2d(&tm_qkv, bar_kv, sV, 2 * C + h * HS, row0 + k0);
-            int pend[2] = {-1, -1};  // phase of the Q/dO load in flight per stage
-            for (int i = 0; i < 2 && i < n_it; ++i) {
-                mbar_expect_tx(&bar_qo[i], 2 * TILE);
-                tma_load_2d(&tm_qkv, &bar_qo[i], sQ + i * TILE, h * HS, row0 + (first_qt + i) * QT);
-                tma_load_2d(&tm_dy, &bar_qo[i], sO + i * TILE, h * HS, row0 + (first_qt + i) * QT);
-                pend[i] = 0;
+            const uint64_t k_d = smem_desc(saddr(sK), 16, 1024), v_d = smem_desc(saddr(sV), 16, 1024);
+            const uint64_t kq_d = smem_desc(saddr(sK), 8192, 1024);    // K as dQ's MN-major B
+            const uint64_t ds_d = smem_desc(saddr(sDS), 16384, 1024);  // dS as dQ's MN-major A
+            const uint64_t pt_d = smem_desc(saddr(sPT), 16, 1024), dst_d = smem_desc(saddr(sDS), 16, 1024);
+            // Q / dO stages: K-major (S^T, dP^T) and MN-major (dK, dV) views
+            const uint64_t q_d0 = smem_desc(saddr(sQ), 16, 1024), q_d1 = smem_desc(saddr(sQ + TILE), 16, 1024);
+            const uint64_t o_d0 = smem_desc(saddr(sO), 16, 1024), o_d1 = smem_desc(saddr(sO + TILE), 16, 1024);
+            const uint64_t qm_d0 = smem_desc(saddr(sQ), 8192, 1024), qm_d1 = smem_desc(saddr(sQ + TILE), 8192, 1024);
+            const uint64_t om_d0 = smem_desc(saddr(sO), 8192, 1024), om_d1 = smem_desc(saddr(sO + TILE), 8192, 1024);
+            if (elect_one()) {
+                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
+                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_dy) : "memory");
+                mbar_expect_tx(bar_kv, 2 * TILE);
+                tma_load_2d(&tm_qkv, bar_kv, sK, C + h * HS, row0 + k0);
+                tma_load_2d(&tm_qkv, bar_kv, sV, 2 * C + h * HS, row0 + k0);
+                for (int i = 0; i < 2 && i < n_it; ++i) {
+                    mbar_expect_tx(&bar_qo[i], 2 * TILE);
+                    tma_load_2d(&tm_qkv, &bar_qo[i], sQ + i * TILE, h * HS, row0 + (first_qt + i) * QT);
+                    tma_load_2d(&tm_dy, &bar_qo[i], sO + i * TILE, h * HS, row0 + (first_qt + i) * QT);
+                }
             }
-            const uint32_t k_a = saddr(sK), v_a = saddr(sV);
+            __syncwarp();
+            int pend[2] = {0, n_it > 1 ? 0 : -1};  // phase of the Q/dO load in flight per stage
             bool kv_pending = true, issued = false;
             // S^T and dP^T of sub-tile u into TMEM buffer u % 2 (its tile's Q/dO must have landed)
             auto issue_s = [&](int u) {
                 const int st = (u >> 1) & 1, hq = u & 1;
-                const uint32_t q_a = saddr(sQ + st * TILE) + hq * 8192, o_a = saddr(sO + st * TILE) + hq * 8192;
                 const uint32_t d = tmem + (uint32_t)(u & 1) * 128;
 #pragma unroll
                 for (int k = 0; k < HS / 16; ++k)
-                    umma_bf16(d, smem_desc(k_a + k * 32, 16, 1024), smem_desc(q_a + k * 32, 16, 1024), id_s, k > 0);
+                    umma_bf16(d, desc_add(k_d, k * 32), desc_add(pick(q_d0, q_d1, st), hq * 8192 + k * 32), id_s, k > 0);
 #pragma unroll
                 for (int k = 0; k < HS / 16; ++k)
-                    umma_bf16(d + 64, smem_desc(v_a + k * 32, 16, 1024), smem_desc(o_a + k * 32, 16, 1024), id_s,
-                              k > 0);
+                    umma_bf16(d + 64, desc_add(v_d, k * 32), desc_add(pick(o_d0, o_d1, st), hq * 8192 + k * 32), id_s, k > 0);
                 umma_commit(&bar_s[u & 1]);
             };
-            bool ok = mbar_wait(bar_kv, 0, abort_flag, WAIT_NS) && mbar_wait(&bar_qo[0], 0, abort_flag, WAIT_NS);
+            bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, abort_flag, WAIT_NS) &&
+                                                  mbar_wait(&bar_qo[0], 0, abort_flag, WAIT_NS));
             if (ok) {
                 kv_pending = false;
                 pend[0] = -1;
                 tc_fence_after();
-                issue_s(0);
-                issue_s(1);
+                if (elect_one()) {
+                    issue_s(0);
+                    issue_s(1);
+                }
+                __syncwarp();
                 issued = true;
             }
             for (int u = 0; ok && u < n_u; ++u) {
                 const int it = u >> 1, hq = u & 1, st = it & 1;
-                if (!mbar_wait(&bar_p[hq], it & 1, abort_flag, WAIT_NS)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_p[hq], it & 1, abort_flag, WAIT_NS))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t pt_a = saddr(sPT) + hq * 16384, ds_a = saddr(sDS) + hq * 16384;
-                const uint32_t q_a = saddr(sQ + st * TILE) + hq * 8192, o_a = saddr(sO + st * TILE) + hq * 8192;
-                if (hq == 1) {
-                    // dQ of the tile first (both dS halves are in): its completion frees the P^T /
-                    // dS^T buffers for the next tile's first half
-                    const uint32_t dsa = saddr(sDS);
+                if (elect_one()) {
+                    if (hq == 1) {
+                        // dQ of the tile first (both dS halves are in): its completion frees the
+                        // P^T / dS^T buffers for the next tile's first half
 #pragma unroll
-                    for (int k = 0; k < KT / 16; ++k)
-                        umma_bf16(tmem + 384 + (uint32_t)(it & 1) * 64, smem_desc(dsa + k * 2048, 16384, 1024),
-                                  smem_desc(k_a + k * 2048, 8192, 1024), id_q, k > 0);
-                    umma_commit(bar_mm);
-                }
+                        for (int k = 0; k < KT / 16; ++k)
+                            umma_bf16(tmem + 384 + (uint32_t)(it & 1) * 64, desc_add(ds_d, k * 2048),
+                                      desc_add(kq_d, k * 2048), id_q, k > 0);
+                        umma_commit(bar_mm);
+                    }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    umma_bf16(tmem + 256, smem_desc(pt_a + k * 32, 16, 1024), smem_desc(o_a + k * 2048, 8192, 1024),
-                              id_kv, (u > 0 || k > 0) ? 1u : 0u);
-                    umma_bf16(tmem + 320, smem_desc(ds_a + k * 32, 16, 1024), smem_desc(q_a + k * 2048, 8192, 1024),
-                              id_kv, (u > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t acc = (u > 0 || k > 0) ? 1u : 0u;
+                        umma_bf16(tmem + 256, desc_add(pt_d, hq * 16384 + k * 32),
+                                  desc_add(pick(om_d0, om_d1, st), hq * 8192 + k * 2048), id_kv, acc);
+                        umma_bf16(tmem + 320, desc_add(dst_d, hq * 16384 + k * 32),
+                                  desc_add(pick(qm_d0, qm_d1, st), hq * 8192 + k * 2048), id_kv, acc);
+                    }
+                    if (hq == 1) umma_commit(bar_st);
                 }
-                if (hq == 1) umma_commit(bar_st);
+                __syncwarp();
                 if (u + 2 < n_u) {
                     if (hq == 0) {  // the next tile's Q/dO
                         const int ns = (it + 1) & 1;
-                        if (!mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, abort_flag, WAIT_NS)) {
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, abort_flag, WAIT_NS))) {
                             ok = false;
                             break;
                         }
                         pend[ns] = -1;
                         tc_fence_after();
                     }
-                    issue_s(u + 2);
+                    if (elect_one()) issue_s(u + 2);
+                    __syncwarp();
                 }
                 if (hq == 1 && it + 2 < n_it) {
                     // stage st (this tile's Q, dO) is free once the tile's last dV, dK are done
-                    if (!mbar_wait(bar_st, it & 1, abort_flag, WAIT_NS)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_st, it & 1, abort_flag, WAIT_NS))) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(&bar_qo[st], 2 * TILE);
-                    tma_load_2d(&tm_qkv, &bar_qo[st], sQ + st * TILE, h * HS, row0 + (first_qt + it + 2) * QT);
-                    tma_load_2d(&tm_dy, &bar_qo[st], sO + st * TILE, h * HS, row0 + (first_qt + it + 2) * QT);
+                    if (elect_one()) {
+                        mbar_expect_tx(&bar_qo[st], 2 * TILE);
+                        tma_load_2d(&tm_qkv, &bar_qo[st], sQ + st * TILE, h * HS, row0 + (first_qt + it + 2) * QT);
+                        tma_load_2d(&tm_dy, &bar_qo[st], sO + st * TILE, h * HS, row0 + (first_qt + it + 2) * QT);
+                    }
+                    __syncwarp();
                     pend[st] = ((it + 2) >> 1) & 1;
                 }
             }
             if (!ok) {
-                *abort_flag = 1;
-                report(err, GK_ERR_TIMEOUT);
-                // let this CTA's copies and MMAs in flight finish before shared memory and
-                // TMEM are released
-                if (kv_pending) mbar_wait(bar_kv, 0, nullptr, WAIT_NS / 5);
-                for (int i = 0; i < 2; ++i)
-                    if (pend[i] >= 0) mbar_wait(&bar_qo[i], (uint32_t)pend[i], nullptr, WAIT_NS / 5);
-                if (issued) {
-                    umma_commit(bar_drain);
-                    mbar_wait(bar_drain, 0, nullptr, WAIT_NS / 5);
+                if (elect_one()) {
+                    *abort_flag = 1;
+                    report(err, GK_ERR_TIMEOUT);
+                    // let this CTA's copies and MMAs in flight finish before shared memory and
+                    // TMEM are released
+                    if (kv_pending) mbar_wait(bar_kv, 0, nullptr, WAIT_NS / 5);
+                    for (int i = 0; i < 2; ++i)
+                        if (pend[i] >= 0) mbar_wait(&bar_qo[i], (uint32_t)pend[i], nullptr, WAIT_NS / 5);
+                    if (issued) {
+                        umma_commit(bar_drain);
+                        mbar_wait(bar_drain, 0, nullptr, WAIT_NS / 5);
+                    }
                 }
+                __syncwarp();
             }
         }
     } else {
@@ -629,11 +671,14 @@ __global__ void __maxnreg__(168)
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
+        // dV and dK: the last tile's dV, dK products follow its dQ, so they are waited for on
+        // their own barrier (whose previous phase completed before bar_mm's last one)
+        if (!fail && n_it > 0)
+            note_fail(__all_sync(0xffffffffu, mbar_wait(bar_st, (n_it - 1) & 1, abort_flag, WAIT_NS)));
         if (fail) {
             *abort_flag = 1;
             report(err, GK_ERR_TIMEOUT);
-        } else if (n_it > 0) {
-            // dV and dK (the last bar_mm phase covered every MMA): lane r = key row kk
+        } else if (n_it > 0) {  // lane r = key row kk
             tc_fence_after();
             uint32_t v[32];
             __nv_bfloat16* base = dqkv + (int64_t)(row0 + kk) * 3 * C + h * HS + hf * 32;
@@ -738,7 +783,7 @@ gk_status attn_fwd_tc(gk_ctx* ctx, const void* qkv, void* y, float* lse, int B, 
         cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FWD_SMEM_BYTES);
         attr = true;
     }
-    dim3 grid((unsigned)cdiv(cdiv(T, QT), 2), (unsigned)(B * H));
+    dim3 grid((unsigned)(B * H), (unsigned)cdiv(cdiv(T, QT), 2));
     attn_fwd_tc_kernel<<<grid, FWD_THREADS, FWD_SMEM_BYTES, ctx->stream>>>(map, static_cast<__nv_bfloat16*>(y), lse,
                                                                          T, H, ctx->d_err);
     return launched(ctx, "attn_fwd_tc");
@@ -771,7 +816,7 @@ gk_status attn_bwd_tc(gk_ctx* ctx, const void* qkv, const void* y, const float* 
         cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BWD_SMEM_BYTES);
         attr = true;
     }
-    dim3 grid((unsigned)cdiv(T, KT), (unsigned)(B * H));
+    dim3 grid((unsigned)(B * H), (unsigned)cdiv(T, KT));
     attn_bwd_tc_kernel<<<grid, BWD_THREADS, BWD_SMEM_BYTES, ctx->stream>>>(map_qkv, map_dy, map_dq, lse, dvec,
                                                                         (__nv_bfloat16*)dqkv, T, H, ctx->d_err);
     GK_TRY(launched(ctx, "attn_bwd_tc"));

@@ -737,52 +737,55 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = instr_desc_bf16(!p.a_kmajor, !p.b_kmajor, BM, BN);
-            // per 16-deep K step: K-major operands advance 32 bytes inside the swizzled row,
-            // MN-major operands advance two 8-row core-matrix groups (2 x 1024 bytes)
-            const uint32_t a_step = p.a_kmajor ? 32u : 2048u;
-            const uint32_t b_step = p.b_kmajor ? 32u : 2048u;
-            const uint32_t a_lbo = p.a_kmajor ? 16u : 8192u, b_lbo = p.b_kmajor ? 16u : 8192u;
-            uint32_t it = 0, j = 0;
-            bool ok = true, issued = false;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
-                int tm, tn, kb0, kb1;
-                unit_coords(p, u, tm, tn, kb0, kb1);
-                uint32_t buf = j & 1, aph = (j >> 1) & 1;
-                if (!mbar_wait(&tempty[buf], aph ^ 1, abort_flag, WAIT_NS)) {
+        // The whole warp walks the loop in step (so the descriptors stay warp-uniform) and one
+        // elected lane issues the MMAs and commits.
+        const uint32_t idesc = instr_desc_bf16(!p.a_kmajor, !p.b_kmajor, BM, BN);
+        // per 16-deep K step: K-major operands advance 32 bytes inside the swizzled row,
+        // MN-major operands advance two 8-row core-matrix groups (2 x 1024 bytes)
+        const uint32_t a_step = p.a_kmajor ? 32u : 2048u;
+        const uint32_t b_step = p.b_kmajor ? 32u : 2048u;
+        const uint32_t a_lbo = p.a_kmajor ? 16u : 8192u, b_lbo = p.b_kmajor ? 16u : 8192u;
+        uint32_t it = 0, j = 0;
+        bool ok = true, issued = false;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+            int tm, tn, kb0, kb1;
+            unit_coords(p, u, tm, tn, kb0, kb1);
+            uint32_t buf = j & 1, aph = (j >> 1) & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tempty[buf], aph ^ 1, abort_flag, WAIT_NS))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t d_tmem = tmem_base + buf * BN;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                int s = it % STAGES;
+                uint32_t ph = (it / STAGES) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, WAIT_NS))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t d_tmem = tmem_base + buf * BN;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    int s = it % STAGES;
-                    uint32_t ph = (it / STAGES) & 1;
-                    if (!mbar_wait(&full[s], ph, abort_flag, WAIT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint32_t a0 = saddr(smem + s * SC::STAGE), b0 = a0 + SC::A_SLOT;
+                const uint32_t a0 = saddr(smem + s * SC::STAGE), b0 = a0 + SC::A_SLOT;
+                const uint64_t ad0 = smem_desc(a0, a_lbo, 1024), bd0 = smem_desc(b0, b_lbo, 1024);
+                if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        uint64_t ad = smem_desc(a0 + k * a_step, a_lbo, 1024);
-                        uint64_t bd = smem_desc(b0 + k * b_step, b_lbo, 1024);
+                        const uint64_t ad = desc_add(ad0, k * a_step), bd = desc_add(bd0, k * b_step);
                         umma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         // split operands: + A_hi B_lo + A_lo B_hi (the A_lo B_lo term is dropped)
-                        if (SC::B_LO)
-                            umma_bf16(d_tmem, ad, smem_desc(b0 + B_BYTES + k * b_step, b_lbo, 1024), idesc, 1u);
-                        if (SC::A_LO)
-                            umma_bf16(d_tmem, smem_desc(a0 + A_BYTES + k * a_step, a_lbo, 1024), bd, idesc, 1u);
+                        if (SC::B_LO) umma_bf16(d_tmem, ad, desc_add(bd0, B_BYTES + k * b_step), idesc, 1u);
+                        if (SC::A_LO) umma_bf16(d_tmem, desc_add(ad0, A_BYTES + k * a_step), bd, idesc, 1u);
                     }
-                    issued = true;
                     umma_commit(&empty[s]);
+                    // commits track the MMAs of the thread that issues them: same lane, same block
+                    if (kb == kb1 - 1) umma_commit(&tfull[buf]);
                 }
-                if (!ok) break;
-                umma_commit(&tfull[buf]);
+                __syncwarp();
+                issued = true;
             }
-            if (!ok) {
+        }
+        if (!ok) {
+            if (elect_one()) {
                 *abort_flag = 1;
                 report(p.err, GK_ERR_TIMEOUT);
                 if (issued) {
@@ -790,6 +793,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_wait(drain, 0, nullptr, DRAIN_NS);
                 }
             }
+            __syncwarp();
         }
     } else if (p.tma_epi) {
         EpiMaps mp{&tmC, &tmAux, &tmLo,

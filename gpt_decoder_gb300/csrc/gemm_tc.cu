@@ -29,15 +29,20 @@ constexpr uint32_t A_BYTES = BM * BK * 2;         // 16 KB per operand tile
 constexpr uint32_t B_BYTES = BN * BK * 2;         // 32 KB per operand tile
 constexpr uint32_t TMEM_COLS = 2 * BN;            // two float32 accumulators of 128 x 256
 
-// Stage layout per split mode: bit 0 = A has a low bf16 plane, bit 1 = B has one. A stage
-// holds [A_hi | A_lo? | B_hi | B_lo?]; the ring shrinks to keep within 227 KB of shared memory.
+// Stage layout per mode: bit 0 = A has a low bf16 plane, bit 1 = B has one; mode PAIR_MODE is
+// a CTA pair sharing 256 x 256 tiles (each CTA holds its 128 rows of A and 128 of the 256
+// columns of B). A stage holds [A_hi | A_lo? | B_hi | B_lo?]; the ring is as deep as 227 KB of
+// shared memory allows.
+constexpr int PAIR_MODE = 4;
 template <int SPLIT>
 struct StageCfg {
-    static constexpr bool A_LO = (SPLIT & 1) != 0, B_LO = (SPLIT & 2) != 0;
+    static constexpr bool PAIR = SPLIT == PAIR_MODE;
+    static constexpr bool A_LO = !PAIR && (SPLIT & 1) != 0, B_LO = !PAIR && (SPLIT & 2) != 0;
     static constexpr uint32_t A_SLOT = A_BYTES * (A_LO ? 2 : 1);
-    static constexpr uint32_t B_SLOT = B_BYTES * (B_LO ? 2 : 1);
+    static constexpr uint32_t B_TILE = PAIR ? B_BYTES / 2 : B_BYTES;  // the B columns this CTA loads
+    static constexpr uint32_t B_SLOT = B_TILE * (B_LO ? 2 : 1);
     static constexpr uint32_t STAGE = A_SLOT + B_SLOT;
-    static constexpr int STAGES = SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2);
+    static constexpr int STAGES = PAIR ? 6 : SPLIT == 0 ? 4 : (SPLIT == 1 ? 3 : 2);
     static constexpr uint32_t EPI = 8 * 32 * 32 * 4;  // 4 KB per epilogue warp
     static constexpr size_t SMEM = (size_t)STAGES * STAGE + EPI + 1024 + 512;
 };
@@ -47,6 +52,7 @@ constexpr uint64_t DRAIN_NS = 200000000ull;       // after an abort: 0.2 s per d
 struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, splits, kbps, kblocks;
+    int pair, tiles_m2;  // CTA pairs: a unit is a 256-row tile pair; tiles_m2 = ceil(tiles_m / 2)
     int a_kmajor, b_kmajor;
     void* C;
     int64_t ldc;
@@ -282,10 +288,19 @@ __device__ __forceinline__ void epi_finish(const TcParams& p, int64_t m, int64_t
     }
 }
 
+// Units of work of this CTA: u = unit_first(p), + unit_step(p), ... Both CTAs of a pair walk
+// the same units; tm is this CTA's own 128-row tile.
+__device__ __forceinline__ int unit_first(const TcParams& p) { return p.pair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x; }
+__device__ __forceinline__ int unit_step(const TcParams& p) { return p.pair ? (int)(gridDim.x >> 1) : (int)gridDim.x; }
 __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, int& tn, int& kb0, int& kb1) {
     int split = u % p.splits, tile = u / p.splits;
-    tm = tile % p.tiles_m;
-    tn = tile / p.tiles_m;
+    if (p.pair) {
+        tm = (tile % p.tiles_m2) * 2 + (int)(blockIdx.x & 1);
+        tn = tile / p.tiles_m2;
+    } else {
+        tm = tile % p.tiles_m;
+        tn = tile / p.tiles_m;
+    }
     kb0 = split * p.kbps;
     kb1 = min(p.kblocks, kb0 + p.kbps);
 }
@@ -312,7 +327,7 @@ __device__ __forceinline__ bool epi_next(const TcParams& p, int units, int& u, i
         ++ch;
         return true;
     }
-    for (int v = u + gridDim.x; v < units; v += gridDim.x) {
+    for (int v = u + unit_step(p); v < units; v += unit_step(p)) {
         unit_coords(p, v, tm, tn, kb0, kb1);
         if (epi_chunks<TC>(p, tm, tn, q, half) > 0) {
             u = v;
@@ -384,6 +399,19 @@ struct EpiMaps {
 };
 
 // Epilogue warp (one of 8) of the TMA path. Returns false if it gave up on a wait.
+// An epilogue warp hands its accumulator buffer back to the MMA issuer (the even CTA of a pair).
+// Its TMEM loads are complete (tcgen05.wait::ld) before it gets here.
+__device__ __forceinline__ void release_accumulator(const TcParams& p, uint64_t* bar, int lane) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+        if (p.pair && (blockIdx.x & 1))
+            mbar_arrive_cluster_relaxed(mapa_shared(saddr(bar), 0));
+        else
+            mbar_arrive(bar);
+    }
+}
+
 template <typename TC>
 __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slots, uint64_t* inbar, uint64_t* tfull,
                              uint64_t* tempty, volatile int* abort_flag, uint32_t tmem_base, int warp, int lane,
@@ -399,9 +427,9 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
 
     // the first chunk's input
     if (has_in && lane == 0) {
-        int u0 = blockIdx.x, c0 = -1;
+        int u0 = unit_first(p), c0 = -1;
         bool any = false;
-        for (int v = blockIdx.x; v < units && !any; v += gridDim.x) {
+        for (int v = unit_first(p); v < units && !any; v += unit_step(p)) {
             int tm, tn, kb0, kb1;
             unit_coords(p, v, tm, tn, kb0, kb1);
             if (epi_chunks<TC>(p, tm, tn, q, half) > 0) {
@@ -421,7 +449,7 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
     }
 
     uint32_t j = 0;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+    for (int u = unit_first(p); u < units && ok; u += unit_step(p), ++j) {
         int tm, tn, kb0, kb1;
         unit_coords(p, u, tm, tn, kb0, kb1);
         const uint32_t buf = j & 1, aph = (j >> 1) & 1;
@@ -433,9 +461,9 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
         tc_fence_after();
         const int nch = epi_chunks<TC>(p, tm, tn, q, half);
         // warm L2 with the next unit's input while this tile drains
-        if (has_in && lane == 0 && u + (int)gridDim.x < units) {
+        if (has_in && lane == 0 && u + unit_step(p) < units) {
             int tm2, tn2, a2, b2;
-            unit_coords(p, u + gridDim.x, tm2, tn2, a2, b2);
+            unit_coords(p, u + unit_step(p), tm2, tn2, a2, b2);
             const int n2 = epi_chunks<TC>(p, tm2, tn2, q, half);
             for (int c = 0; c < n2; ++c)
                 tma_prefetch_l2_2d(mp.in, tn2 * BN + half * (BN / 2) + c * W, tm2 * BM + q * 32);
@@ -620,8 +648,7 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
         }
         if (p.ce_mode == CE_LSE && ok && y + lane < p.M)
             p.ce_part[(int64_t)(y + lane) * p.ce_nparts + 2 * tn + half] = make_float2(ce_m, ce_s);
-        tc_fence_before();
-        mbar_arrive(&tempty[buf]);
+        release_accumulator(p, &tempty[buf], lane);
     }
     if (lane == 0) {
         if (pend_slot >= 0) mbar_wait(&inbar[pend_slot], pend_par, nullptr, DRAIN_NS);
@@ -640,6 +667,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const TcParams p) {
     using SC = StageCfg<SPLIT>;
     constexpr int STAGES = SC::STAGES;
+    constexpr bool PAIR = SC::PAIR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // stage s: A_hi at smem + s*STAGE, A_lo at + A_BYTES, B_hi at + A_SLOT, B_lo at + A_SLOT + B_BYTES
@@ -655,7 +683,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 22);
 
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int units = p.tiles_m * p.tiles_n * p.splits;
+    int units = (PAIR ? p.tiles_m2 : p.tiles_m) * p.tiles_n * p.splits;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -664,7 +693,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 256);
+            mbar_init(&tempty[b], PAIR ? 16 : 8);  // one arrival per epilogue warp (of both CTAs)
         }
         mbar_init(drain, 1);
         for (int i = 0; i < 16; ++i) mbar_init(&inbars[i], 1);
@@ -672,10 +701,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
+        if (PAIR)
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        else
+            tmem_alloc(tmem_slot, TMEM_COLS);
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // the peer's barriers are initialised before anything arrives on them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -689,7 +722,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int issued_ph[STAGES];
             for (int s = 0; s < STAGES; ++s) issued_ph[s] = -1;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            for (int u = unit_first(p); u < units && ok; u += unit_step(p)) {
                 int tm, tn, kb0, kb1;
                 unit_coords(p, u, tm, tn, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -699,7 +732,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(&full[s], SC::STAGE);
+                    // a pair's stage is complete when both CTAs' copies have landed: all of them
+                    // count on the even CTA's full[s], which the even CTA arms for both
+                    const uint32_t fb = PAIR ? mapa_shared(saddr(&full[s]), 0) : 0u;
+                    if (!PAIR || rank == 0) mbar_expect_tx(&full[s], PAIR ? 2 * SC::STAGE : SC::STAGE);
+                    auto load = [&](const CUtensorMap* map, void* dst, int x, int y) {
+                        if (PAIR)
+                            tma_load_2d_pair(map, fb, dst, x, y);
+                        else
+                            tma_load_2d(map, &full[s], dst, x, y);
+                    };
                     uint8_t* a = smem + s * SC::STAGE;
                     uint8_t* b = a + SC::A_SLOT;
 #pragma unroll
@@ -707,22 +749,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const CUtensorMap* ma = pl ? &tmA_lo : &tmA;
                         uint8_t* dst = a + pl * A_BYTES;
                         if (p.a_kmajor) {
-                            tma_load_2d(ma, &full[s], dst, kb * BK, tm * BM);
+                            load(ma, dst, kb * BK, tm * BM);
                         } else {
-                            tma_load_2d(ma, &full[s], dst, tm * BM, kb * BK);
-                            tma_load_2d(ma, &full[s], dst + 8192, tm * BM + 64, kb * BK);
+                            load(ma, dst, tm * BM, kb * BK);
+                            load(ma, dst + 8192, tm * BM + 64, kb * BK);
                         }
                     }
 #pragma unroll
                     for (int pl = 0; pl < (SC::B_LO ? 2 : 1); ++pl) {
                         const CUtensorMap* mb = pl ? &tmB_lo : &tmB;
-                        uint8_t* dst = b + pl * B_BYTES;
+                        uint8_t* dst = b + pl * SC::B_TILE;
+                        // this CTA's columns of the tile's B (all of them, or its half in a pair)
+                        constexpr int BNC = (int)(SC::B_TILE / (BK * 2));
+                        const int n0 = tn * BN + (int)rank * BNC;
                         if (p.b_kmajor) {
-                            tma_load_2d(mb, &full[s], dst, kb * BK, tn * BN);
+                            load(mb, dst, kb * BK, n0);
                         } else {
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                tma_load_2d(mb, &full[s], dst + j * 8192, tn * BN + 64 * j, kb * BK);
+                            for (int j = 0; j < BNC / 64; ++j) load(mb, dst + j * 8192, n0 + 64 * j, kb * BK);
                         }
                     }
                     issued_ph[s] = (int)ph;
@@ -731,15 +775,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) {
                 *abort_flag = 1;
                 report(p.err, GK_ERR_TIMEOUT);
-                // let this CTA's copies in flight land before shared memory is released
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued_ph[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_ph[s], nullptr, DRAIN_NS);
+                // let this CTA's copies in flight land before shared memory is released (the odd
+                // CTA of a pair cannot see their completion: it gives them a millisecond)
+                if (PAIR && rank != 0) {
+                    const uint64_t t0 = globaltimer();
+                    while (globaltimer() - t0 < 1000000ull) {
+                    }
+                } else {
+                    for (int s = 0; s < STAGES; ++s)
+                        if (issued_ph[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_ph[s], nullptr, DRAIN_NS);
+                }
             }
         }
+    } else if (PAIR && warp == 1 && rank != 0) {
+        // odd CTA of a pair: the even CTA issues the MMAs
     } else if (warp == 1) {
         // The whole warp walks the loop in step (so the descriptors stay warp-uniform) and one
-        // elected lane issues the MMAs and commits.
-        const uint32_t idesc = instr_desc_bf16(!p.a_kmajor, !p.b_kmajor, BM, BN);
+        // elected lane issues the MMAs and commits. In a pair this is the even CTA, issuing
+        // 256-row MMAs whose commits reach both CTAs' barriers.
+        const uint32_t idesc = instr_desc_bf16(!p.a_kmajor, !p.b_kmajor, PAIR ? 2 * BM : BM, BN);
         // per 16-deep K step: K-major operands advance 32 bytes inside the swizzled row,
         // MN-major operands advance two 8-row core-matrix groups (2 x 1024 bytes)
         const uint32_t a_step = p.a_kmajor ? 32u : 2048u;
@@ -747,7 +801,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t a_lbo = p.a_kmajor ? 16u : 8192u, b_lbo = p.b_kmajor ? 16u : 8192u;
         uint32_t it = 0, j = 0;
         bool ok = true, issued = false;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+        for (int u = unit_first(p); u < units && ok; u += unit_step(p), ++j) {
             int tm, tn, kb0, kb1;
             unit_coords(p, u, tm, tn, kb0, kb1);
             uint32_t buf = j & 1, aph = (j >> 1) & 1;
@@ -771,14 +825,24 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t ad = desc_add(ad0, k * a_step), bd = desc_add(bd0, k * b_step);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                        // split operands: + A_hi B_lo + A_lo B_hi (the A_lo B_lo term is dropped)
-                        if (SC::B_LO) umma_bf16(d_tmem, ad, desc_add(bd0, B_BYTES + k * b_step), idesc, 1u);
-                        if (SC::A_LO) umma_bf16(d_tmem, desc_add(ad0, A_BYTES + k * a_step), bd, idesc, 1u);
+                        const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+                        if (PAIR) {
+                            umma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                        } else {
+                            umma_bf16(d_tmem, ad, bd, idesc, acc);
+                            // split operands: + A_hi B_lo + A_lo B_hi (the A_lo B_lo term is dropped)
+                            if (SC::B_LO) umma_bf16(d_tmem, ad, desc_add(bd0, B_BYTES + k * b_step), idesc, 1u);
+                            if (SC::A_LO) umma_bf16(d_tmem, desc_add(ad0, A_BYTES + k * a_step), bd, idesc, 1u);
+                        }
                     }
-                    umma_commit(&empty[s]);
                     // commits track the MMAs of the thread that issues them: same lane, same block
-                    if (kb == kb1 - 1) umma_commit(&tfull[buf]);
+                    if (PAIR) {
+                        umma_commit_pair_mc(&empty[s], 3);
+                        if (kb == kb1 - 1) umma_commit_pair_mc(&tfull[buf], 3);
+                    } else {
+                        umma_commit(&empty[s]);
+                        if (kb == kb1 - 1) umma_commit(&tfull[buf]);
+                    }
                 }
                 __syncwarp();
                 issued = true;
@@ -789,7 +853,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *abort_flag = 1;
                 report(p.err, GK_ERR_TIMEOUT);
                 if (issued) {
-                    umma_commit(drain);
+                    if (PAIR)
+                        umma_commit_pair(drain);
+                    else
+                        umma_commit(drain);
                     mbar_wait(drain, 0, nullptr, DRAIN_NS);
                 }
             }
@@ -810,11 +877,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         int q = warp & 3;
         int half = (warp - 2) >> 2;
         uint32_t j = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+        for (int u = unit_first(p); u < units; u += unit_step(p), ++j) {
             int tm, tn, kb0, kb1;
             unit_coords(p, u, tm, tn, kb0, kb1);
             uint32_t buf = j & 1, aph = (j >> 1) & 1;
-            if (!mbar_wait(&tfull[buf], aph, abort_flag, WAIT_NS)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], aph, abort_flag, WAIT_NS))) {
                 *abort_flag = 1;
                 report(p.err, GK_ERR_TIMEOUT);
                 break;
@@ -855,16 +922,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 __syncwarp();
             }
-            tc_fence_before();
-            mbar_arrive(&tempty[buf]);
+            release_accumulator(p, &tempty[buf], lane);
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // no MMA, commit or arrival of the pair is still in flight
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if (PAIR) cluster_sync();
 }
 
 struct Maps {
@@ -879,7 +950,24 @@ void launch_one(gk_ctx* ctx, int grid, const Maps& m, const TcParams& p) {
         cudaFuncSetAttribute(gemm_tc_kernel<TC, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    gemm_tc_kernel<TC, SPLIT><<<grid, THREADS, smem, ctx->stream>>>(m.a, m.b, m.al, m.bl, m.c, m.aux, m.r, m.lo, p);
+    if constexpr (SPLIT == PAIR_MODE) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = ctx->stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC, SPLIT>, m.a, m.b, m.al, m.bl, m.c, m.aux, m.r, m.lo, p);
+    } else {
+        gemm_tc_kernel<TC, SPLIT><<<grid, THREADS, smem, ctx->stream>>>(m.a, m.b, m.al, m.bl, m.c, m.aux, m.r, m.lo,
+                                                                         p);
+    }
 }
 
 template <typename TC>
@@ -888,8 +976,36 @@ void launch_split(gk_ctx* ctx, int split, int grid, const Maps& m, const TcParam
         case 0: launch_one<TC, 0>(ctx, grid, m, p); break;
         case 1: launch_one<TC, 1>(ctx, grid, m, p); break;
         case 2: launch_one<TC, 2>(ctx, grid, m, p); break;
-        default: launch_one<TC, 3>(ctx, grid, m, p); break;
+        case 3: launch_one<TC, 3>(ctx, grid, m, p); break;
+        default: launch_one<TC, PAIR_MODE>(ctx, grid, m, p); break;
     }
+}
+
+// How many CTA pairs of the pair kernel can be resident at once (clusters need both SMs of a
+// pair free); 0 if the query fails.
+template <typename TC>
+int max_pairs() {
+    static int n = -1;
+    if (n < 0) {
+        constexpr size_t smem = StageCfg<PAIR_MODE>::SMEM;
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int c = 0;
+        n = cudaOccupancyMaxActiveClusters(&c, gemm_tc_kernel<TC, PAIR_MODE>, &cfg) == cudaSuccess ? c : 0;
+        cudaGetLastError();
+    }
+    return n;
 }
 
 // Decide whether the TMA epilogue takes this GEMM and build its tensor maps: every plane
@@ -940,16 +1056,25 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     if (!aligned16(g.A) || !aligned16(g.B) || (g.lda & 7) || (g.ldb & 7)) return GK_ERR_UNSUPPORTED;
     if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K >= (1ll << 31))
         return GK_ERR_UNSUPPORTED;
+    const int split = (g.A_lo ? 1 : 0) | (g.B_lo ? 2 : 0);
+    // CTA pairs (256 x 256 tiles, half of B per CTA) for the single-plane products with at least
+    // four 128-row tiles; the split-precision products keep one CTA per tile
+    const bool c_f32 = g.ce_mode != CE_LSE && g.c_dtype == GK_F32;
+    const int pairs = split == 0 && cdiv(g.M, BM) >= 4 ? (c_f32 ? max_pairs<float>() : max_pairs<__nv_bfloat16>()) : 0;
+    const bool pair = pairs > 0;
     CUtensorMap ta, tb;
     bool ok = g.a_kmajor ? make_map(&ta, g.A, g.K, g.M, g.lda, BM) : make_map(&ta, g.A, g.M, g.K, g.lda, 64);
-    ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, BN) : make_map(&tb, g.B, g.N, g.K, g.ldb, 64));
+    ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, pair ? BN / 2 : BN)
+                           : make_map(&tb, g.B, g.N, g.K, g.ldb, 64));
     if (!ok) return GK_ERR_UNSUPPORTED;
     TcParams p{};
+    p.pair = pair ? 1 : 0;
     p.M = (int)g.M;
     p.N = (int)g.N;
     p.K = (int)g.K;
     p.tiles_m = (int)cdiv(g.M, BM);
     p.tiles_n = (int)cdiv(g.N, BN);
+    p.tiles_m2 = (int)cdiv(p.tiles_m, 2);
     p.kblocks = (int)cdiv(g.K, BK);
     p.a_kmajor = g.a_kmajor;
     p.b_kmajor = g.b_kmajor;
@@ -971,11 +1096,13 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
             (!g.residual || (aligned16(g.residual) && g.ldr % 4 == 0)) &&
             (!g.aux || (aligned16(g.aux) && g.ldaux % 4 == 0)) && (g.c_plane % 4 == 0);
     if ((g.A_lo && (!aligned16(g.A_lo))) || (g.B_lo && !aligned16(g.B_lo))) return GK_ERR_UNSUPPORTED;
-    int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+    // persistent grid: one CTA per SM, or one pair per resident cluster
+    const int slots = pair ? pairs : ctx->num_sms;
+    int64_t tiles = (int64_t)(pair ? p.tiles_m2 : p.tiles_m) * p.tiles_n;
     p.splits = 1;
     bool plain_acc = g.accumulate && g.c_dtype == GK_F32 && !g.bias && !g.residual && g.epi == EPI_NONE;
-    if (plain_acc && tiles < ctx->num_sms) {
-        int want = (int)cdiv(2 * (int64_t)ctx->num_sms, tiles);
+    if (plain_acc && tiles < slots) {
+        int want = (int)cdiv(2 * (int64_t)slots, tiles);
         int maxs = std::max(1, p.kblocks / 4);
         p.splits = std::max(1, std::min(want, maxs));
     }
@@ -983,8 +1110,8 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.splits = (int)cdiv(p.kblocks, p.kbps);
     p.atomic_out = p.splits > 1;
     int64_t units = tiles * p.splits;
-    int grid = (int)std::min<int64_t>(units, ctx->num_sms);
-    int split = (g.A_lo ? 1 : 0) | (g.B_lo ? 2 : 0);
+    int grid = (int)std::min<int64_t>(units, slots) * (pair ? 2 : 1);
+    const int mode = pair ? PAIR_MODE : split;
     Maps m;
     m.a = ta;
     m.b = tb;
@@ -1007,7 +1134,7 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
         m.c = m.aux = m.r = m.lo = ta;
         p.tma_epi = setup_tma_epilogue(g, p, m);
         if (!p.tma_epi) return GK_ERR_UNSUPPORTED;
-        launch_split<__nv_bfloat16>(ctx, split, grid, m, p);  // 32-column chunks; nothing is stored
+        launch_split<__nv_bfloat16>(ctx, mode, grid, m, p);  // 32-column chunks; nothing is stored
         return launched(ctx, "gemm_tc");
     }
     p.tma_epi = setup_tma_epilogue(g, p, m);
@@ -1018,9 +1145,9 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
         p.reduce_out = p.out_aux = p.out_lo = 0;
     }
     if (g.c_dtype == GK_F32)
-        launch_split<float>(ctx, split, grid, m, p);
+        launch_split<float>(ctx, mode, grid, m, p);
     else
-        launch_split<__nv_bfloat16>(ctx, split, grid, m, p);
+        launch_split<__nv_bfloat16>(ctx, mode, grid, m, p);
     return launched(ctx, "gemm_tc");
 }
 

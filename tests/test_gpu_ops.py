@@ -203,7 +203,8 @@ def test_matmul_fwd_f32(gkctx, N, K, M, transW):
     assert rel_l2(y, ref) < 2e-5
 
 
-@pytest.mark.parametrize("N,K,M", [(4096, 768, 3072), (512, 96, 288), (131, 67, 45), (256, 256, 256)])
+@pytest.mark.parametrize("N,K,M", [(4096, 768, 3072), (512, 96, 288), (131, 67, 45), (256, 256, 256),
+                                   (1160, 200, 520), (640, 64, 256)])
 @pytest.mark.parametrize("transW", [0, 1])
 def test_matmul_fwd_bf16_operands(gkctx, N, K, M, transW):
     y, ref = _matmul_case(gkctx, N, K, M, transW, "bf16", True, False, False, 510)
@@ -279,7 +280,7 @@ def test_matmul_bwd_f32(gkctx, N, K, M, transW):
     assert rel_l2(db, rdb) < 2e-5
 
 
-@pytest.mark.parametrize("N,K,M", [(4096, 768, 3072), (512, 96, 288), (131, 67, 45)])
+@pytest.mark.parametrize("N,K,M", [(4096, 768, 3072), (512, 96, 288), (131, 67, 45), (1160, 520, 200)])
 @pytest.mark.parametrize("transW", [0, 1])
 def test_matmul_bwd_bf16_operands(gkctx, N, K, M, transW):
     (dx, rdx), (dw, rdw), (db, rdb) = _matmul_bwd_case(gkctx, N, K, M, transW, "bf16", 1, False, 610)
@@ -304,8 +305,10 @@ def test_matmul_bwd_fused_gelu_accumulates_after_the_gelu_factor(gkctx, dt):
 
 # bf16 results through the tensor-core epilogue: ragged rows and columns (partial 32-row
 # groups, partial chunks, idle column halves) next to full tiles
+# (with at least four 128-row tiles the products run on CTA pairs: an odd tile count leaves the
+# last pair's second CTA past the rows, 700 leaves it a partial tile)
 BF16_OUT = [(4096, 768, 3072), (300, 96, 384), (131, 64, 45), (77, 128, 200), (1, 64, 8), (333, 96, 130),
-            (257, 64, 520)]
+            (257, 64, 520), (640, 96, 384), (700, 200, 520)]
 
 
 @pytest.mark.parametrize("N,K,M", BF16_OUT)

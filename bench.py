@@ -335,6 +335,25 @@ def bench_decode(ctx, m, s, Tp=512, n_steps=256):
                         "steps": n_steps, "dtype": "f32", "launches_per_step": (gk.gk_launch_count(dctx) - l0) / n_steps,
                         "launch": "CUDA graph per step"}
         kv.close()
+    # uncached generation ([LM4] Generate: the whole sequence re-run per token) at batch 1 from
+    # the same prompt length, the baseline the cached loop is compared with
+    n_unc = 16
+    with torch.cuda.stream(stream):
+        kv = gk.KvCache(dctx, m.cfg, 1, Tp + n_unc + 1)
+        ids = torch.zeros(1, Tp + n_unc + 1, dtype=torch.int32, device="cuda")
+        ids[:, :Tp] = torch.randint(0, s.V, (1, Tp), dtype=torch.int32, device="cuda")
+        logits = torch.empty(1, s.V, device="cuda")
+        gk.gk_generate_uncached(dctx, m.params, kv, ids, Tp, 1, logits)  # warm-up
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gk.gk_generate_uncached(dctx, m.params, kv, ids, Tp, n_unc, logits)
+        e1.record(stream)
+    stream.synchronize()
+    gk.gk_sync(dctx)
+    ms = e0.elapsed_time(e1)
+    res["B1_uncached"] = {"tok_s": n_unc / (ms / 1e3), "ms_per_token": ms / n_unc, "prompt": Tp, "steps": n_unc,
+                          "dtype": "f32", "launch": "one full causal forward per token"}
+    kv.close()
     dctx.close()
     return res
 

@@ -29,6 +29,7 @@ struct gk_kv {
     size_t partial_floats = 0;
     float* attn_part = nullptr;  // decode attention partials [B*H][chunks][hs + 2]
     int* tickets = nullptr;      // last-block tickets: [0, 1024) GEMV column blocks, [1024, 2048) attention
+    int32_t* ids = nullptr;      // gk_generate_uncached: the prefix [B, t] of each step, then next [B]
     // gk_decode_run: one captured decode step (instantiated graph) and what it was captured for
     cudaGraphExec_t graph = nullptr;
     int64_t graph_launches = 0;
@@ -475,6 +476,21 @@ __global__ void copy_ids_kernel(const int32_t* __restrict__ src, int32_t* __rest
     if (i < n) dst[i] = src[i];
 }
 
+// out [B, t] = the first t columns of ids [B, stride]
+__global__ void gather_prefix_kernel(const int32_t* __restrict__ ids, int64_t stride, int B, int t,
+                                     int32_t* __restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)B * t) return;
+    out[i] = ids[(i / t) * stride + i % t];
+}
+
+// ids[b, pos] = next[b]
+__global__ void put_column_kernel(const int32_t* __restrict__ next, int B, int32_t* __restrict__ ids, int64_t stride,
+                                  int pos) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) ids[(int64_t)b * stride + pos] = next[b];
+}
+
 __global__ void set_state_kernel(int* state, int length, int selections) {
     state[0] = length;
     state[1] = selections;
@@ -779,6 +795,7 @@ gk_status gk_kv_create(gk_ctx* ctx, gk_kv** out, const gk_gpt_cfg* cfg, int B, i
         }
     }
     if (cudaMalloc(&kv->state, 2 * sizeof(int)) != cudaSuccess || cudaMemset(kv->state, 0, 2 * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&kv->ids, ((size_t)rows + B) * sizeof(int32_t)) != cudaSuccess ||
         cudaMalloc(&kv->tickets, 2048 * sizeof(int)) != cudaSuccess ||
         cudaMemset(kv->tickets, 0, 2048 * sizeof(int)) != cudaSuccess ||
         cudaMemset(kv->cache, 0, (size_t)cfg->L * 2 * rows * C * sizeof(float)) != cudaSuccess ||
@@ -799,6 +816,7 @@ void gk_kv_destroy(gk_kv* kv) {
         if (p) cudaFree(p);
     if (kv->state) cudaFree(kv->state);
     if (kv->tickets) cudaFree(kv->tickets);
+    if (kv->ids) cudaFree(kv->ids);
     delete kv;
 }
 
@@ -975,6 +993,30 @@ gk_status gk_sample(gk_ctx* ctx, gk_kv* kv, const float* logits, int64_t ld, int
     GK_TRY(launched(ctx, "select"));
     advance_kernel<<<1, 1, 0, ctx->stream>>>(kv->state, 0, 1);
     return launched(ctx, "advance");
+}
+
+gk_status gk_generate_uncached(gk_ctx* ctx, const float* params, gk_kv* kv, int32_t* ids, int Tp, int n_new,
+                               float* logits, const gk_sample_cfg* s) {
+    GK_TRY(check_kv_args(ctx, params, kv));
+    GK_REQUIRE(ctx, ids && logits && Tp >= 1 && n_new >= 0, GK_ERR_ARG, "gk_generate_uncached: bad argument");
+    GK_REQUIRE(ctx, (int64_t)Tp + n_new - 1 <= kv->Tmax, GK_ERR_OVERFLOW,
+               "gk_generate_uncached: %d + %d tokens exceed the cache (%d)", Tp, n_new, kv->Tmax);
+    const int B = kv->B;
+    const int64_t stride = (int64_t)Tp + n_new;
+    int32_t* next = kv->ids + (int64_t)B * kv->Tmax;
+    for (int i = 0; i < n_new; ++i) {
+        const int t = Tp + i;
+        gather_prefix_kernel<<<(unsigned)cdiv((int64_t)B * t, 256), 256, 0, ctx->stream>>>(ids, stride, B, t, kv->ids);
+        GK_TRY(launched(ctx, "gather_prefix"));
+        GK_TRY(gk_prefill(ctx, params, kv, kv->ids, t, logits));
+        // selection i, as in the cached loop (the prompt's selection, then one per step)
+        set_state_kernel<<<1, 1, 0, ctx->stream>>>(kv->state, t, i);
+        GK_TRY(launched(ctx, "set_state"));
+        GK_TRY(gk_sample(ctx, kv, logits, kv->cfg.V, next, s));
+        put_column_kernel<<<1, 32 * (unsigned)cdiv(B, 32), 0, ctx->stream>>>(next, B, ids, stride, t);
+        GK_TRY(launched(ctx, "put_column"));
+    }
+    return GK_OK;
 }
 
 }  // extern "C"

@@ -64,6 +64,7 @@ _SIGS = {
     "gk_lmhead_ce_fwd": (I32, [P, I32, P, I64, P, I64, P, P, P, I64, I64, I64]),
     "gk_lmhead_ce_bwd": (I32, [P, I32, P, I64, P, I64, P, P, P, P, I64, I32, P, I64, P, I64, I64, I64, I64]),
     "gk_decode_run": (I32, [P, P, P, P, P, P, P, I32]),
+    "gk_generate_uncached": (I32, [P, P, P, P, I32, I32, P, P]),
     "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, P, I64, I32]),
     "gk_layernorm_bwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
     "gk_gelu_fwd": (I32, [P, P, P, I64]),
@@ -318,6 +319,13 @@ def gk_decode_run(ctx, params, kv, tokens, logits, next_ids, n_steps, sample=Non
     replayed as a CUDA graph). sample: None (greedy) or (top_k, temperature, seed, counter)."""
     return _check(ctx, _lib.gk_decode_run(ctx.handle, _p(params), kv.handle, _p(tokens), _p(logits), _p(next_ids),
                                           _sample(sample), n_steps), "gk_decode_run")
+
+
+def gk_generate_uncached(ctx, params, kv, ids, Tp, n_new, logits, sample=None):
+    """n_new tokens by re-running the whole prefix per token: ids [B, Tp + n_new] (device int32)
+    holds the prompt in its first Tp columns and receives the selections."""
+    return _check(ctx, _lib.gk_generate_uncached(ctx.handle, _p(params), kv.handle, _p(ids), Tp, n_new, _p(logits),
+                                                 _sample(sample)), "gk_generate_uncached")
 
 
 def gk_sample(ctx, kv, logits, ld, next_ids, sample=None):

@@ -351,6 +351,18 @@ gk_status gk_decode_step(gk_ctx* ctx, const float* params, gk_kv* kv, const int3
 gk_status gk_decode_run(gk_ctx* ctx, const float* params, gk_kv* kv, int32_t* tokens,
                         float* logits, int32_t* next, const gk_sample_cfg* s, int n_steps);
 
+/* Uncached generation, [LM4] "Generation with a KV cache" (Generate: the whole sequence runs
+ * through the model again for every new token, the baseline the cached loop is measured
+ * against). ids: device int32 [B, Tp + n_new], row stride Tp + n_new, holding the prompt in
+ * its first Tp columns. For i = 0 .. n_new-1 the prefix ids[:, :Tp+i] goes through one causal
+ * forward (as gk_prefill; the cache serves as scratch and is overwritten every step) and
+ * selection i (as gk_sample, the cache's selection count set to i, so the draws are those of
+ * gk_prefill + gk_sample + gk_decode_run) is written to ids[:, Tp+i]. logits [B, V] holds the
+ * last step's logits. GK_ERR_OVERFLOW (nothing run) if Tp + n_new - 1 exceeds the cache;
+ * GK_ERR_ARG for null pointers, Tp < 1 or n_new < 0. */
+gk_status gk_generate_uncached(gk_ctx* ctx, const float* params, gk_kv* kv, int32_t* ids, int Tp,
+                               int n_new, float* logits, const gk_sample_cfg* s);
+
 /* Select next [B] from logits [B, V] (stride ld) as gk_sample_cfg describes; the selection
  * index s is the cache's selection count, which this advances by one. */
 gk_status gk_sample(gk_ctx* ctx, gk_kv* kv, const float* logits, int64_t ld, int32_t* next,

@@ -220,3 +220,84 @@ def test_topk_ties_are_kept_and_greedy_takes_lowest_index(gkctx):
             assert row[got[b]] >= 1.0
     gk.gk_sync(gkctx)
     kv.close()
+
+
+def _uncached(gkctx, s, B, Tp, n_new, seed, sample):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    prompt, params, m, kv = _setup(gkctx, s, B, Tp, seed, Tp + n_new)
+    ids = torch.zeros(B, Tp + n_new, dtype=torch.int32, device="cuda")
+    ids[:, :Tp] = torch.as_tensor(prompt.reshape(B, Tp))
+    logits = torch.empty(B, s.V, device="cuda")
+    gk.gk_generate_uncached(gkctx, m.params, kv, ids, Tp, n_new, logits, sample)
+    gk.gk_sync(gkctx)
+    out = ids.cpu().numpy()
+    kv.close()
+    return prompt, params, m, out
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_uncached_generate_matches_oracle_greedy(gkctx, B):
+    """[LM4] Generate (a full forward per token): the prompt columns are left alone and each
+    row's greedy continuation is the oracle's up to its first near-tie."""
+    s, Tp, n = synth.TINY, 12, 16
+    prompt, params, _, out = _uncached(gkctx, s, B, Tp, n + 1, 5, None)
+    assert np.array_equal(out[:, :Tp], prompt.reshape(B, Tp))
+    picks, ologits = ogpt.generate(params, prompt, n, ogpt.Shape(s.V, s.T, s.C, s.H, s.L), top_k=1)
+    got = out[:, Tp:].T  # [n + 1, B], like picks
+    srt = np.sort(ologits, axis=-1)
+    gap = srt[..., -1] - srt[..., -2]
+    for b in range(B):
+        bad = np.nonzero(got[:, b] != picks[:, b])[0]
+        if len(bad):
+            j = bad[0]
+            assert gap[j, b] < 1e-3, (b, j, gap[j, b])
+
+
+@pytest.mark.parametrize("sample", [None, (5, 0.8, 11, 3)])
+def test_uncached_generate_equals_cached_loop(gkctx, sample):
+    """Uncached and cached generation select the same tokens with the same draws: selection i
+    of the uncached loop uses the counter the cached loop gives its i-th selection."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    s, B, Tp, n = synth.TINY, 2, 10, 12
+    _, _, _, out = _uncached(gkctx, s, B, Tp, n + 1, 9, sample)
+    prompt, params, m, kv = _setup(gkctx, s, B, Tp, 9, Tp + n)
+    logits = torch.empty(B, s.V, device="cuda")
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    gk.gk_prefill(gkctx, m.params, kv, torch.as_tensor(prompt.reshape(-1)).cuda(), Tp, logits)
+    gk.gk_sample(gkctx, kv, logits, s.V, tok, sample)
+    seen = [tok.cpu().numpy()]
+    for _ in range(n):
+        gk.gk_decode_step(gkctx, m.params, kv, tok, logits, tok, sample)
+        seen.append(tok.cpu().numpy())
+    gk.gk_sync(gkctx)
+    kv.close()
+    assert np.array_equal(out[:, Tp:].T, np.array(seen))
+
+
+def test_uncached_generate_overflow_runs_nothing(gkctx):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    s, B, Tp = synth.TINY, 2, 5
+    prompt, params, m, kv = _setup(gkctx, s, B, Tp, 7, Tp + 3)
+    ids = torch.full((B, Tp + 5), -1, dtype=torch.int32, device="cuda")
+    ids[:, :Tp] = torch.as_tensor(prompt.reshape(B, Tp))
+    logits = torch.empty(B, s.V, device="cuda")
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_generate_uncached(gkctx, m.params, kv, ids, Tp, 5, logits)
+    assert e.value.status == gk.GK_ERR_OVERFLOW
+    assert (ids[:, Tp:].cpu().numpy() == -1).all()
+    ids4 = ids[:, :Tp + 4].contiguous()  # row stride Tp + n_new
+    gk.gk_generate_uncached(gkctx, m.params, kv, ids4, Tp, 4, logits)  # Tp + 3 positions: fits
+    gk.gk_sync(gkctx)
+    got = ids4.cpu().numpy()
+    assert np.array_equal(got[:, :Tp], prompt.reshape(B, Tp))
+    assert ((got[:, Tp:] >= 0) & (got[:, Tp:] < s.V)).all()
+    kv.close()

@@ -272,3 +272,68 @@ def adamw(p, g, m, v, t, lr, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0):
     mhat = m / (1.0 - beta1 ** t)
     vhat = v / (1.0 - beta2 ** t)
     return p - lr * (mhat / (np.sqrt(vhat) + eps) + wd * p), m, v
+
+
+# ------------------------------------------------------------------- generic ops, SGD
+def add_fwd(a, b):
+    """a + b with b broadcast over a's leading dimensions (b's shape is a's trailing shape).
+
+    [LM1] "Ops..." op table: Add, with broadcast (a bias added to every row).
+    """
+    return _f64(a) + _f64(b)
+
+
+def add_bwd(g, b_shape):
+    """Contributions (da, db) of Add: da = g; db = g summed over the broadcast (leading)
+    dimensions, so that it has b's shape. The reading of the broadcast rule: every row used
+    b once, so b's gradient collects every row's."""
+    g = _f64(g)
+    lead = g.ndim - len(b_shape)
+    return g.copy(), g.sum(axis=tuple(range(lead))).reshape(b_shape)
+
+
+def mul_fwd(a, b):
+    """Elementwise product. [LM1] "Ops...", Mul listing."""
+    return _f64(a) * _f64(b)
+
+
+def mul_bwd(a, b, g):
+    """Mul's backward rule ([LM1] Mul listing): da += g b, db += g a."""
+    g = _f64(g)
+    return g * _f64(b), g * _f64(a)
+
+
+def scale_fwd(a, s):
+    """s a for a scalar s. [LM1] "Ops..." op table: Scale."""
+    return float(s) * _f64(a)
+
+
+def scale_bwd(s, g):
+    """Scale's backward: da += s g."""
+    return float(s) * _f64(g)
+
+
+def sum_fwd(a):
+    """The sum of every element (a scalar). [LM1] "Ops..." op table: Sum."""
+    return float(np.sum(_f64(a)))
+
+
+def sum_bwd(a_shape, g):
+    """Sum's backward: every element of a receives the scalar upstream gradient g."""
+    return np.full(a_shape, float(g), dtype=F64)
+
+
+def tanh_fwd(x):
+    """tanh elementwise. [LM1] "Ops..." op table: Tanh; [AD] Step 5 (the tanh neuron)."""
+    return np.tanh(_f64(x))
+
+
+def tanh_bwd(y, g):
+    """Tanh's backward from its output y = tanh(x): dx += g (1 - y^2) ([AD] Step 5)."""
+    y = _f64(y)
+    return _f64(g) * (1.0 - y * y)
+
+
+def sgd(p, g, lr):
+    """Plain SGD: p - lr g. [LM1] "The optimizer: from gradient to step", Sgd listing."""
+    return _f64(p) - float(lr) * _f64(g)

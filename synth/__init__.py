@@ -165,3 +165,27 @@ def prompt_case(s: GptShape, B: int, Tp: int, seed: int):
     prompt = st.ints(B * Tp, s.V).reshape(B, Tp)
     params = gpt_params(s, st)
     return prompt, params
+
+
+def circle_case(seed: int, n: int = 256, hidden: int = 16):
+    """The circle task's seeded inputs: n points uniform in [-1, 1)^2 (float32 [n, 2]), label 1
+    inside the circle x^2 + y^2 < 0.5 else 0 (int32 [n]), and the 2 -> hidden -> 2 network's
+    initial weights: N(0, 0.5^2) matrices [in, out], zero biases."""
+    st = Stream(seed)
+    xs = (st.uniform(2 * n) * 2.0 - 1.0).astype(np.float32).reshape(n, 2)
+    x64 = xs.astype(np.float64)
+    ys = ((x64[:, 0] ** 2 + x64[:, 1] ** 2) < 0.5).astype(np.int32)
+    w1 = st.normal(2 * hidden, 0.5).reshape(2, hidden)
+    w2 = st.normal(hidden * 2, 0.5).reshape(hidden, 2)
+    return xs, ys, (w1, np.zeros(hidden, np.float32), w2, np.zeros(2, np.float32))
+
+
+def xor_case(seed: int, hidden: int = 4):
+    """XOR's four points (float32 [4, 2]), targets -1 / 1 (float32 [4, 1]) and the [2, hidden, 1]
+    network's initial weights: uniform in [-1, 1) matrices [in, out], zero biases."""
+    st = Stream(seed)
+    xs = np.array([[0, 0], [0, 1], [1, 0], [1, 1]], np.float32)
+    ys = np.array([[-1], [1], [1], [-1]], np.float32)
+    w1 = (st.uniform(2 * hidden) * 2.0 - 1.0).astype(np.float32).reshape(2, hidden)
+    w2 = (st.uniform(hidden) * 2.0 - 1.0).astype(np.float32).reshape(hidden, 1)
+    return xs, ys, (w1, np.zeros(hidden, np.float32), w2, np.zeros(1, np.float32))

@@ -245,9 +245,10 @@ def run_ours(args):
         h_loss.copy_(loss, non_blocking=True)
         torch.cuda.synchronize()
     e2e = tokens / ((time.perf_counter() - t0) / e2e_steps)
-    decode = None
+    decode = generic = None
     if rank == 0 and not args.no_decode:
         decode = bench_decode(ctx, m, s)
+        generic = bench_generic(ctx)
     if rank != 0:
         return
     cpu = None
@@ -277,6 +278,8 @@ def run_ours(args):
     }
     if decode:
         out["decode"] = decode
+    if generic:
+        out["generic_ops"] = generic
     print(json.dumps(out))
 
 
@@ -298,6 +301,38 @@ def gemm_traffic_per_step(B, mode):
             src = os.path.join(here, rel.strip())
             ok = ok and os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == digest.strip()
     return value if ok else None
+
+
+def bench_generic(ctx, n=1 << 26, reps=10):
+    """HBM bandwidth of the generic elementwise ops and the Sum reduction over n float32
+    elements (256 MB per operand, larger than L2): algorithmic bytes (each operand read or
+    written once) over the median CUDA-event time, against the measured copy bandwidth."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    hbm = _peaks()[0]
+    a, b, y = (torch.randn(n, device="cuda") for _ in range(3))
+    out = torch.empty(1, device="cuda")
+    cases = {"mul_fwd": (lambda: gk.gk_mul_fwd(ctx, a, b, y, n), 12 * n),
+             "add_bwd_acc": (lambda: gk.gk_add_bwd(ctx, a, y, None, n, n, 1), 12 * n),
+             "tanh_bwd": (lambda: gk.gk_tanh_bwd(ctx, a, b, y, n, 0), 12 * n),
+             "sum_fwd": (lambda: gk.gk_sum_fwd(ctx, a, out, n), 4 * n)}
+    res = {"n": n, "peak_gbs": hbm}
+    for name, (fn, nbytes) in cases.items():
+        fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = sorted(ts)[len(ts) // 2]
+        res[name] = {"gbs": nbytes / (ms / 1e3) / 1e9, "frac": nbytes / (ms / 1e3) / 1e9 / hbm, "us": ms * 1e3}
+    gk.gk_sync(ctx)
+    return res
 
 
 def bench_decode(ctx, m, s, Tp=512, n_steps=256):
@@ -353,6 +388,32 @@ def bench_decode(ctx, m, s, Tp=512, n_steps=256):
     ms = e0.elapsed_time(e1)
     res["B1_uncached"] = {"tok_s": n_unc / (ms / 1e3), "ms_per_token": ms / n_unc, "prompt": Tp, "steps": n_unc,
                           "dtype": "f32", "launch": "one full causal forward per token"}
+    kv.close()
+    # the pages' own generation workload: batch 1, a 5-token prompt, 40 new tokens, top-k 40 at
+    # temperature 0.8, cached (prefill + selection + 39 decode steps) and uncached
+    Tq, n_new, samp = 5, 40, (40, 0.8, 1234, 0)
+    with torch.cuda.stream(stream):
+        kv = gk.KvCache(dctx, m.cfg, 1, Tq + n_new)
+        ids = torch.zeros(1, Tq + n_new, dtype=torch.int32, device="cuda")
+        ids[:, :Tq] = torch.randint(0, s.V, (1, Tq), dtype=torch.int32, device="cuda")
+        logits = torch.empty(1, s.V, device="cuda")
+        tok = torch.empty(1, dtype=torch.int32, device="cuda")
+        times = {}
+        for rep in range(2):  # the first pass records the step graph and warms up
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            gk.gk_prefill(dctx, m.params, kv, ids[:, :Tq].contiguous(), Tq, logits)
+            gk.gk_sample(dctx, kv, logits, s.V, tok, samp)
+            gk.gk_decode_run(dctx, m.params, kv, tok, logits, tok, n_new - 1, samp)
+            e1.record(stream)
+            gk.gk_generate_uncached(dctx, m.params, kv, ids, Tq, n_new, logits, samp)
+            e2.record(stream)
+            stream.synchronize()
+            times = {"cached": e0.elapsed_time(e1), "uncached": e1.elapsed_time(e2)}
+    gk.gk_sync(dctx)
+    res["page_workload"] = {"prompt": Tq, "new_tokens": n_new, "top_k": 40, "temperature": 0.8, "dtype": "f32",
+                            "cached_tok_s": n_new / (times["cached"] / 1e3),
+                            "uncached_tok_s": n_new / (times["uncached"] / 1e3)}
     kv.close()
     dctx.close()
     return res

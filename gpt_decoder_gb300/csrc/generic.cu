@@ -1,0 +1,268 @@
+// Generic tensor ops of the autograd engine and plain SGD, float32, HBM-bound elementwise
+// kernels. [LM1] = "Build a language model in C# from scratch (1)": Ops (Mul and its backward
+// rule), the op table (Add with broadcast, Scale, Sum, Tanh), "Why += and not =", Gradient
+// Check, The optimizer (SGD); [AD] = "Chain rule and automatic differentiation", Steps 1-5
+// (the tanh neuron and its derivative 1 - tanh^2).
+//
+// Elementwise outputs may alias an input of the same index (y == a, da == g).
+// Every backward entry point takes `accumulate`: 0 writes the gradient, 1 adds it to what the
+// buffer holds (the pages' += rule, with ZeroGrad the caller's job). Reductions (Sum, the
+// broadcast bias gradient) run in a fixed order in double, so results do not depend on timing.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace gk {
+namespace {
+
+constexpr int EW_THREADS = 256;
+
+// Grid of a grid-stride elementwise kernel: enough blocks to fill the SMs several times over.
+unsigned ew_blocks(const gk_ctx* ctx, int64_t n) {
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS), (int64_t)ctx->num_sms * 16));
+}
+
+__global__ void add_fwd_kernel(const float* a, const float* b, float* y,
+                               int64_t n, int64_t m) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = a[i] + b[m == n ? i : i % m];
+}
+
+// dst (+)= src
+__global__ void copy_acc_kernel(const float* src, float* dst, int64_t n, int acc) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = acc ? dst[i] + src[i] : src[i];
+}
+
+// part[p, c] = sum of g[r, c] over the rows r of chunk p ([R, m] row-major), in row order
+__global__ void colsum_chunks_kernel(const float* __restrict__ g, int64_t R, int64_t m, int64_t rows_per,
+                                     double* __restrict__ part) {
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= m) return;
+    const int64_t r0 = (int64_t)blockIdx.y * rows_per, r1 = min(R, r0 + rows_per);
+    double s = 0.0;
+    for (int64_t r = r0; r < r1; ++r) s += (double)g[r * m + c];
+    part[(int64_t)blockIdx.y * m + c] = s;
+}
+
+// db[c] (+)= sum over chunks p in order of part[p, c]
+__global__ void colsum_finish_kernel(const double* __restrict__ part, int64_t P, int64_t m, float* __restrict__ db,
+                                     int acc) {
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= m) return;
+    double s = 0.0;
+    for (int64_t p = 0; p < P; ++p) s += part[p * m + c];
+    db[c] = acc ? db[c] + (float)s : (float)s;
+}
+
+__global__ void mul_fwd_kernel(const float* a, const float* b, float* y,
+                               int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = a[i] * b[i];
+}
+
+// da (+)= g * b, db (+)= g * a (either may be null)
+__global__ void mul_bwd_kernel(const float* g, const float* a, const float* b,
+                               float* da, float* db, int64_t n, int acc) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float gi = g[i];
+        if (da) da[i] = acc ? da[i] + gi * b[i] : gi * b[i];
+        if (db) db[i] = acc ? db[i] + gi * a[i] : gi * a[i];
+    }
+}
+
+// y = s * a (forward), or da (+)= s * g (backward: the same map with accumulation)
+__global__ void scale_kernel(const float* a, float s, float* y, int64_t n, int acc) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = acc ? y[i] + s * a[i] : s * a[i];
+}
+
+// part[block] = sum of this block's grid-stride elements (double, fixed order per thread and
+// tree order across the block)
+__global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, double* __restrict__ part) {
+    __shared__ double red[EW_THREADS / 32];
+    double s = 0.0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        s += (double)a[i];
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < EW_THREADS / 32; ++w) t += red[w];
+        part[blockIdx.x] = t;
+    }
+}
+
+// y[0] = sum of part[0 .. P) in index order
+__global__ void sum_finish_kernel(const double* __restrict__ part, int P, float* __restrict__ y) {
+    if (threadIdx.x != 0) return;
+    double t = 0.0;
+    for (int p = 0; p < P; ++p) t += part[p];
+    *y = (float)t;
+}
+
+// da (+)= g[0] for every element
+__global__ void sum_bwd_kernel(const float* g, float* da, int64_t n, int acc) {
+    const float gv = *g;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        da[i] = acc ? da[i] + gv : gv;
+}
+
+__global__ void tanh_fwd_kernel(const float* x, float* y, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = tanhf(x[i]);
+}
+
+// dx (+)= g (1 - y^2), y = tanh(x) saved by the forward
+__global__ void tanh_bwd_kernel(const float* y, const float* g, float* dx,
+                                int64_t n, int acc) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float yi = y[i];
+        const float v = g[i] * (1.f - yi * yi);
+        dx[i] = acc ? dx[i] + v : v;
+    }
+}
+
+// p -= lr * g
+__global__ void sgd_kernel(float* p, const float* g, int64_t n, float lr) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        p[i] -= lr * g[i];
+}
+
+}  // namespace
+}  // namespace gk
+
+using namespace gk;
+
+extern "C" {
+
+gk_status gk_add_fwd(gk_ctx* ctx, const float* a, const float* b, float* y, int64_t n, int64_t m) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0 && m >= 1 && (n == 0 || n % m == 0), GK_ERR_ARG,
+               "gk_add_fwd: b's %lld elements do not tile a's %lld", (long long)m, (long long)n);
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, a && b && y, GK_ERR_ARG, "gk_add_fwd: null pointer");
+    add_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, b, y, n, m);
+    return launched(ctx, "add_fwd");
+}
+
+gk_status gk_add_bwd(gk_ctx* ctx, const float* g, float* da, float* db, int64_t n, int64_t m, int accumulate) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0 && m >= 1 && (n == 0 || n % m == 0), GK_ERR_ARG,
+               "gk_add_bwd: b's %lld elements do not tile a's %lld", (long long)m, (long long)n);
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, g, GK_ERR_ARG, "gk_add_bwd: null gradient");
+    if (da) {
+        copy_acc_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, da, n, accumulate != 0);
+        GK_TRY(launched(ctx, "add_bwd_a"));
+    }
+    if (!db) return GK_OK;
+    if (m == n) {
+        copy_acc_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, db, n, accumulate != 0);
+        return launched(ctx, "add_bwd_b");
+    }
+    // db = column sums of g viewed as [R, m]: row chunks in parallel, then the chunks in order
+    const int64_t R = n / m;
+    int64_t P = std::min<int64_t>(R, std::max<int64_t>(1, cdiv((int64_t)ctx->num_sms * 2048, m)));
+    P = std::min<int64_t>(P, std::max<int64_t>(1, (int64_t)(ctx->ws_bytes / ((size_t)m * sizeof(double)))));
+    const int64_t rows_per = cdiv(R, P);
+    P = cdiv(R, rows_per);
+    double* part = static_cast<double*>(workspace(ctx, (size_t)P * m * sizeof(double)));
+    GK_REQUIRE(ctx, part && P <= 65535, GK_ERR_WORKSPACE, "gk_add_bwd: needs %zu workspace bytes",
+               (size_t)P * m * sizeof(double));
+    colsum_chunks_kernel<<<dim3((unsigned)cdiv(m, EW_THREADS), (unsigned)P), EW_THREADS, 0, ctx->stream>>>(
+        g, R, m, rows_per, part);
+    GK_TRY(launched(ctx, "add_bwd_colsum"));
+    colsum_finish_kernel<<<(unsigned)cdiv(m, EW_THREADS), EW_THREADS, 0, ctx->stream>>>(part, P, m, db,
+                                                                                        accumulate != 0);
+    return launched(ctx, "add_bwd_finish");
+}
+
+gk_status gk_mul_fwd(gk_ctx* ctx, const float* a, const float* b, float* y, int64_t n) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_mul_fwd: negative size");
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, a && b && y, GK_ERR_ARG, "gk_mul_fwd: null pointer");
+    mul_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, b, y, n);
+    return launched(ctx, "mul_fwd");
+}
+
+gk_status gk_mul_bwd(gk_ctx* ctx, const float* g, const float* a, const float* b, float* da, float* db, int64_t n,
+                     int accumulate) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_mul_bwd: negative size");
+    if (n == 0 || (!da && !db)) return GK_OK;
+    GK_REQUIRE(ctx, g && (!da || b) && (!db || a), GK_ERR_ARG, "gk_mul_bwd: null pointer");
+    mul_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, a, b, da, db, n, accumulate != 0);
+    return launched(ctx, "mul_bwd");
+}
+
+gk_status gk_scale_fwd(gk_ctx* ctx, const float* a, float s, float* y, int64_t n) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_scale_fwd: negative size");
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, a && y, GK_ERR_ARG, "gk_scale_fwd: null pointer");
+    scale_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, s, y, n, 0);
+    return launched(ctx, "scale_fwd");
+}
+
+gk_status gk_scale_bwd(gk_ctx* ctx, const float* g, float s, float* da, int64_t n, int accumulate) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_scale_bwd: negative size");
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, g && da, GK_ERR_ARG, "gk_scale_bwd: null pointer");
+    scale_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, s, da, n, accumulate != 0);
+    return launched(ctx, "scale_bwd");
+}
+
+gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0 && y && (n == 0 || a), GK_ERR_ARG, "gk_sum_fwd: bad argument");
+    const int P = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS * 8), 1024));
+    double* part = static_cast<double*>(workspace(ctx, (size_t)P * sizeof(double)));
+    GK_REQUIRE(ctx, part, GK_ERR_WORKSPACE, "gk_sum_fwd: needs %zu workspace bytes", (size_t)P * sizeof(double));
+    sum_partial_kernel<<<P, EW_THREADS, 0, ctx->stream>>>(a, n, part);
+    GK_TRY(launched(ctx, "sum_partial"));
+    sum_finish_kernel<<<1, 32, 0, ctx->stream>>>(part, P, y);
+    return launched(ctx, "sum_finish");
+}
+
+gk_status gk_sum_bwd(gk_ctx* ctx, const float* g, float* da, int64_t n, int accumulate) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_sum_bwd: negative size");
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, g && da, GK_ERR_ARG, "gk_sum_bwd: null pointer");
+    sum_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, da, n, accumulate != 0);
+    return launched(ctx, "sum_bwd");
+}
+
+gk_status gk_tanh_fwd(gk_ctx* ctx, const float* x, float* y, int64_t n) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_tanh_fwd: negative size");
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, x && y, GK_ERR_ARG, "gk_tanh_fwd: null pointer");
+    tanh_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(x, y, n);
+    return launched(ctx, "tanh_fwd");
+}
+
+gk_status gk_tanh_bwd(gk_ctx* ctx, const float* y, const float* g, float* dx, int64_t n, int accumulate) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_tanh_bwd: negative size");
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, y && g && dx, GK_ERR_ARG, "gk_tanh_bwd: null pointer");
+    tanh_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(y, g, dx, n, accumulate != 0);
+    return launched(ctx, "tanh_bwd");
+}
+
+gk_status gk_sgd_step(gk_ctx* ctx, float* p, const float* g, int64_t n, float lr) {
+    if (!ctx) return GK_ERR_ARG;
+    GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_sgd_step: negative size");
+    if (n == 0) return GK_OK;
+    GK_REQUIRE(ctx, p && g, GK_ERR_ARG, "gk_sgd_step: null pointer");
+    sgd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(p, g, n, lr);
+    return launched(ctx, "sgd");
+}
+
+}  // extern "C"

@@ -65,6 +65,17 @@ _SIGS = {
     "gk_lmhead_ce_bwd": (I32, [P, I32, P, I64, P, I64, P, P, P, P, I64, I32, P, I64, P, I64, I64, I64, I64]),
     "gk_decode_run": (I32, [P, P, P, P, P, P, P, I32]),
     "gk_generate_uncached": (I32, [P, P, P, P, I32, I32, P, P]),
+    "gk_add_fwd": (I32, [P, P, P, P, I64, I64]),
+    "gk_add_bwd": (I32, [P, P, P, P, I64, I64, I32]),
+    "gk_mul_fwd": (I32, [P, P, P, P, I64]),
+    "gk_mul_bwd": (I32, [P, P, P, P, P, P, I64, I32]),
+    "gk_scale_fwd": (I32, [P, P, F32, P, I64]),
+    "gk_scale_bwd": (I32, [P, P, F32, P, I64, I32]),
+    "gk_sum_fwd": (I32, [P, P, P, I64]),
+    "gk_sum_bwd": (I32, [P, P, P, I64, I32]),
+    "gk_tanh_fwd": (I32, [P, P, P, I64]),
+    "gk_tanh_bwd": (I32, [P, P, P, P, I64, I32]),
+    "gk_sgd_step": (I32, [P, P, P, I64, F32]),
     "gk_layernorm_bwd": (I32, [P, P, P, P, P, P, P, I32, P, P, P, P, I64, I32]),
     "gk_layernorm_bwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, P, P, P, I64, I32]),
     "gk_gelu_fwd": (I32, [P, P, P, I64]),
@@ -326,6 +337,52 @@ def gk_generate_uncached(ctx, params, kv, ids, Tp, n_new, logits, sample=None):
     holds the prompt in its first Tp columns and receives the selections."""
     return _check(ctx, _lib.gk_generate_uncached(ctx.handle, _p(params), kv.handle, _p(ids), Tp, n_new, _p(logits),
                                                  _sample(sample)), "gk_generate_uncached")
+
+
+# ---- generic ops of the autograd engine (float32 device tensors of n elements) and SGD
+def gk_add_fwd(ctx, a, b, y, n, m):
+    return _check(ctx, _lib.gk_add_fwd(ctx.handle, _p(a), _p(b), _p(y), n, m), "gk_add_fwd")
+
+
+def gk_add_bwd(ctx, g, da, db, n, m, accumulate=0):
+    return _check(ctx, _lib.gk_add_bwd(ctx.handle, _p(g), _p(da), _p(db), n, m, accumulate), "gk_add_bwd")
+
+
+def gk_mul_fwd(ctx, a, b, y, n):
+    return _check(ctx, _lib.gk_mul_fwd(ctx.handle, _p(a), _p(b), _p(y), n), "gk_mul_fwd")
+
+
+def gk_mul_bwd(ctx, g, a, b, da, db, n, accumulate=0):
+    return _check(ctx, _lib.gk_mul_bwd(ctx.handle, _p(g), _p(a), _p(b), _p(da), _p(db), n, accumulate),
+                  "gk_mul_bwd")
+
+
+def gk_scale_fwd(ctx, a, s, y, n):
+    return _check(ctx, _lib.gk_scale_fwd(ctx.handle, _p(a), s, _p(y), n), "gk_scale_fwd")
+
+
+def gk_scale_bwd(ctx, g, s, da, n, accumulate=0):
+    return _check(ctx, _lib.gk_scale_bwd(ctx.handle, _p(g), s, _p(da), n, accumulate), "gk_scale_bwd")
+
+
+def gk_sum_fwd(ctx, a, y, n):
+    return _check(ctx, _lib.gk_sum_fwd(ctx.handle, _p(a), _p(y), n), "gk_sum_fwd")
+
+
+def gk_sum_bwd(ctx, g, da, n, accumulate=0):
+    return _check(ctx, _lib.gk_sum_bwd(ctx.handle, _p(g), _p(da), n, accumulate), "gk_sum_bwd")
+
+
+def gk_tanh_fwd(ctx, x, y, n):
+    return _check(ctx, _lib.gk_tanh_fwd(ctx.handle, _p(x), _p(y), n), "gk_tanh_fwd")
+
+
+def gk_tanh_bwd(ctx, y, g, dx, n, accumulate=0):
+    return _check(ctx, _lib.gk_tanh_bwd(ctx.handle, _p(y), _p(g), _p(dx), n, accumulate), "gk_tanh_bwd")
+
+
+def gk_sgd_step(ctx, p, g, n, lr):
+    return _check(ctx, _lib.gk_sgd_step(ctx.handle, _p(p), _p(g), n, lr), "gk_sgd_step")
 
 
 def gk_sample(ctx, kv, logits, ld, next_ids, sample=None):

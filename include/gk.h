@@ -368,6 +368,43 @@ gk_status gk_generate_uncached(gk_ctx* ctx, const float* params, gk_kv* kv, int3
 gk_status gk_sample(gk_ctx* ctx, gk_kv* kv, const float* logits, int64_t ld, int32_t* next,
                     const gk_sample_cfg* s);
 
+/* ---- Generic ops of the autograd engine and plain SGD ([LM1] "Build a language model in C#
+ * from scratch (1)": Ops, the op table (Add with broadcast, Scale, Sum, Tanh), "Why += and not =",
+ * The optimizer; [AD] "Chain rule and automatic differentiation", Steps 1-5: the tanh neuron).
+ * All tensors are float32 device buffers of n elements, row-major. Backward calls take
+ * `accumulate`: 0 writes the gradient, 1 adds it to the buffer (the pages' += rule; zeroing
+ * before a backward pass is the caller's job). Elementwise outputs may alias an input of the
+ * same index. n == 0 is a no-op. GK_ERR_ARG for null pointers or n < 0. */
+
+/* y = a + b, b broadcast over the leading dimensions: b has m elements and m divides n (m == n
+ * is the plain sum, m = the row width is the bias added to every row). GK_ERR_ARG if m does not
+ * divide n. */
+gk_status gk_add_fwd(gk_ctx* ctx, const float* a, const float* b, float* y, int64_t n, int64_t m);
+/* da (+)= g; db (+)= g summed over the rows of g viewed as [n / m, m] (the broadcast's
+ * gradient; in double, fixed order). Either output may be NULL. Needs (chunks x m) doubles of
+ * workspace for m < n (GK_ERR_WORKSPACE if the context's workspace is smaller than m doubles). */
+gk_status gk_add_bwd(gk_ctx* ctx, const float* g, float* da, float* db, int64_t n, int64_t m, int accumulate);
+/* y = a * b elementwise. */
+gk_status gk_mul_fwd(gk_ctx* ctx, const float* a, const float* b, float* y, int64_t n);
+/* da (+)= g * b, db (+)= g * a (either may be NULL). */
+gk_status gk_mul_bwd(gk_ctx* ctx, const float* g, const float* a, const float* b, float* da, float* db,
+                     int64_t n, int accumulate);
+/* y = s * a, s a host scalar. */
+gk_status gk_scale_fwd(gk_ctx* ctx, const float* a, float s, float* y, int64_t n);
+/* da (+)= s * g. */
+gk_status gk_scale_bwd(gk_ctx* ctx, const float* g, float s, float* da, int64_t n, int accumulate);
+/* y[0] = sum of a (double accumulation in a fixed order; n == 0 gives 0). Needs up to 8 KB of
+ * workspace. */
+gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n);
+/* da (+)= g[0] for every element (g: one float32 on the device). */
+gk_status gk_sum_bwd(gk_ctx* ctx, const float* g, float* da, int64_t n, int accumulate);
+/* y = tanh(x). */
+gk_status gk_tanh_fwd(gk_ctx* ctx, const float* x, float* y, int64_t n);
+/* dx (+)= g * (1 - y^2), y the forward's output. */
+gk_status gk_tanh_bwd(gk_ctx* ctx, const float* y, const float* g, float* dx, int64_t n, int accumulate);
+/* Plain SGD step ([LM1] The optimizer, Sgd): p -= lr * g. */
+gk_status gk_sgd_step(gk_ctx* ctx, float* p, const float* g, int64_t n, float lr);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,20 +18,48 @@ namespace {
 constexpr int EW_THREADS = 256;
 
 // Grid of a grid-stride elementwise kernel: enough blocks to fill the SMs several times over.
+// float4 path: every operand (null ones aside) 16-byte aligned
+bool al(const void* p) { return !p || aligned16(p); }
+template <typename... Ps>
+bool vec4(const Ps*... ps) {
+    return (al(ps) && ...);
+}
+
 unsigned ew_blocks(const gk_ctx* ctx, int64_t n) {
     return (unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS), (int64_t)ctx->num_sms * 16));
 }
 
-__global__ void add_fwd_kernel(const float* a, const float* b, float* y,
-                               int64_t n, int64_t m) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = a[i] + b[m == n ? i : i % m];
+// Elementwise kernels walk float4 groups when every operand is 16-byte aligned (`vec`), then
+// the scalar tail; element i of every operand sits at the same index.
+template <typename V, typename S>
+__device__ __forceinline__ void ew_loops(int64_t n, bool vec, V vbody, S sbody) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t n4 = vec ? n / 4 : 0;
+    for (int64_t j = tid; j < n4; j += stride) vbody(j);
+    for (int64_t i = 4 * n4 + tid; i < n; i += stride) sbody(i);
+}
+
+__device__ __forceinline__ float4 f4(const float* p, int64_t j) { return reinterpret_cast<const float4*>(p)[j]; }
+__device__ __forceinline__ void st4(float* p, int64_t j, float4 v) { reinterpret_cast<float4*>(p)[j] = v; }
+
+// y = a + b[i % m] (vec needs m % 4 == 0)
+__global__ void add_fwd_kernel(const float* a, const float* b, float* y, int64_t n, int64_t m, bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        const float4 x = f4(a, j), c = f4(b, (4 * j) % m / 4);
+        st4(y, j, make_float4(x.x + c.x, x.y + c.y, x.z + c.z, x.w + c.w));
+    }, [&](int64_t i) { y[i] = a[i] + b[m == n ? i : i % m]; });
 }
 
 // dst (+)= src
-__global__ void copy_acc_kernel(const float* src, float* dst, int64_t n, int acc) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        dst[i] = acc ? dst[i] + src[i] : src[i];
+__global__ void copy_acc_kernel(const float* src, float* dst, int64_t n, int acc, bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        float4 v = f4(src, j);
+        if (acc) {
+            const float4 d = f4(dst, j);
+            v = make_float4(d.x + v.x, d.y + v.y, d.z + v.z, d.w + v.w);
+        }
+        st4(dst, j, v);
+    }, [&](int64_t i) { dst[i] = acc ? dst[i] + src[i] : src[i]; });
 }
 
 // part[p, c] = sum of g[r, c] over the rows r of chunk p ([R, m] row-major), in row order
@@ -55,35 +83,83 @@ __global__ void colsum_finish_kernel(const double* __restrict__ part, int64_t P,
     db[c] = acc ? db[c] + (float)s : (float)s;
 }
 
-__global__ void mul_fwd_kernel(const float* a, const float* b, float* y,
-                               int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = a[i] * b[i];
+__global__ void mul_fwd_kernel(const float* a, const float* b, float* y, int64_t n, bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        const float4 x = f4(a, j), z = f4(b, j);
+        st4(y, j, make_float4(x.x * z.x, x.y * z.y, x.z * z.z, x.w * z.w));
+    }, [&](int64_t i) { y[i] = a[i] * b[i]; });
 }
 
 // da (+)= g * b, db (+)= g * a (either may be null)
-__global__ void mul_bwd_kernel(const float* g, const float* a, const float* b,
-                               float* da, float* db, int64_t n, int acc) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+__global__ void mul_bwd_kernel(const float* g, const float* a, const float* b, float* da, float* db, int64_t n, int acc,
+                               bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        const float4 gv = f4(g, j);
+        if (da) {
+            const float4 bv = f4(b, j);
+            float4 v = make_float4(gv.x * bv.x, gv.y * bv.y, gv.z * bv.z, gv.w * bv.w);
+            if (acc) {
+                const float4 o = f4(da, j);
+                v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+            }
+            st4(da, j, v);
+        }
+        if (db) {
+            const float4 av = f4(a, j);
+            float4 v = make_float4(gv.x * av.x, gv.y * av.y, gv.z * av.z, gv.w * av.w);
+            if (acc) {
+                const float4 o = f4(db, j);
+                v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+            }
+            st4(db, j, v);
+        }
+    }, [&](int64_t i) {
         const float gi = g[i];
         if (da) da[i] = acc ? da[i] + gi * b[i] : gi * b[i];
         if (db) db[i] = acc ? db[i] + gi * a[i] : gi * a[i];
-    }
+    });
 }
 
 // y = s * a (forward), or da (+)= s * g (backward: the same map with accumulation)
-__global__ void scale_kernel(const float* a, float s, float* y, int64_t n, int acc) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = acc ? y[i] + s * a[i] : s * a[i];
+__global__ void scale_kernel(const float* a, float s, float* y, int64_t n, int acc, bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        const float4 x = f4(a, j);
+        float4 v = make_float4(s * x.x, s * x.y, s * x.z, s * x.w);
+        if (acc) {
+            const float4 o = f4(y, j);
+            v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+        }
+        st4(y, j, v);
+    }, [&](int64_t i) { y[i] = acc ? y[i] + s * a[i] : s * a[i]; });
 }
 
-// part[block] = sum of this block's grid-stride elements (double, fixed order per thread and
-// tree order across the block)
-__global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, double* __restrict__ part) {
+// part[block] = sum of this block's grid-stride elements, in a fixed order: each aligned float4
+// group is added in float ((x + y) + (z + w)); a thread's k-th group goes to its double
+// accumulator k % 4 (four independent chains), the tail to the first; then the accumulators in
+// order, and the block's threads in tree order
+__global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, double* __restrict__ part, bool vec) {
     __shared__ double red[EW_THREADS / 32];
-    double s = 0.0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        s += (double)a[i];
+    double acc4[4] = {0.0, 0.0, 0.0, 0.0};
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t n4 = vec ? n / 4 : 0;
+    int64_t j = tid;
+    for (; j + 3 * stride < n4; j += 4 * stride) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 v = f4(a, j + k * stride);
+            acc4[k] += (double)((v.x + v.y) + (v.z + v.w));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {  // fewer than four groups left
+        if (j < n4) {
+            const float4 v = f4(a, j);
+            acc4[k] += (double)((v.x + v.y) + (v.z + v.w));
+            j += stride;
+        }
+    }
+    for (int64_t i = 4 * n4 + tid; i < n; i += stride) acc4[0] += (double)a[i];
+    double s = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) red[warp] = s;
@@ -104,31 +180,49 @@ __global__ void sum_finish_kernel(const double* __restrict__ part, int P, float*
 }
 
 // da (+)= g[0] for every element
-__global__ void sum_bwd_kernel(const float* g, float* da, int64_t n, int acc) {
+__global__ void sum_bwd_kernel(const float* g, float* da, int64_t n, int acc, bool vec) {
     const float gv = *g;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        da[i] = acc ? da[i] + gv : gv;
+    ew_loops(n, vec, [&](int64_t j) {
+        float4 v = make_float4(gv, gv, gv, gv);
+        if (acc) {
+            const float4 o = f4(da, j);
+            v = make_float4(o.x + gv, o.y + gv, o.z + gv, o.w + gv);
+        }
+        st4(da, j, v);
+    }, [&](int64_t i) { da[i] = acc ? da[i] + gv : gv; });
 }
 
-__global__ void tanh_fwd_kernel(const float* x, float* y, int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = tanhf(x[i]);
+__global__ void tanh_fwd_kernel(const float* x, float* y, int64_t n, bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        const float4 v = f4(x, j);
+        st4(y, j, make_float4(tanhf(v.x), tanhf(v.y), tanhf(v.z), tanhf(v.w)));
+    }, [&](int64_t i) { y[i] = tanhf(x[i]); });
 }
 
 // dx (+)= g (1 - y^2), y = tanh(x) saved by the forward
-__global__ void tanh_bwd_kernel(const float* y, const float* g, float* dx,
-                                int64_t n, int acc) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+__global__ void tanh_bwd_kernel(const float* y, const float* g, float* dx, int64_t n, int acc, bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        const float4 yv = f4(y, j), gv = f4(g, j);
+        float4 v = make_float4(gv.x * (1.f - yv.x * yv.x), gv.y * (1.f - yv.y * yv.y), gv.z * (1.f - yv.z * yv.z),
+                               gv.w * (1.f - yv.w * yv.w));
+        if (acc) {
+            const float4 o = f4(dx, j);
+            v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+        }
+        st4(dx, j, v);
+    }, [&](int64_t i) {
         const float yi = y[i];
         const float v = g[i] * (1.f - yi * yi);
         dx[i] = acc ? dx[i] + v : v;
-    }
+    });
 }
 
 // p -= lr * g
-__global__ void sgd_kernel(float* p, const float* g, int64_t n, float lr) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        p[i] -= lr * g[i];
+__global__ void sgd_kernel(float* p, const float* g, int64_t n, float lr, bool vec) {
+    ew_loops(n, vec, [&](int64_t j) {
+        const float4 pv = f4(p, j), gv = f4(g, j);
+        st4(p, j, make_float4(pv.x - lr * gv.x, pv.y - lr * gv.y, pv.z - lr * gv.z, pv.w - lr * gv.w));
+    }, [&](int64_t i) { p[i] -= lr * g[i]; });
 }
 
 }  // namespace
@@ -144,7 +238,7 @@ gk_status gk_add_fwd(gk_ctx* ctx, const float* a, const float* b, float* y, int6
                "gk_add_fwd: b's %lld elements do not tile a's %lld", (long long)m, (long long)n);
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, a && b && y, GK_ERR_ARG, "gk_add_fwd: null pointer");
-    add_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, b, y, n, m);
+    add_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, b, y, n, m, vec4(a, b, y) && (m == n || m % 4 == 0));
     return launched(ctx, "add_fwd");
 }
 
@@ -155,12 +249,12 @@ gk_status gk_add_bwd(gk_ctx* ctx, const float* g, float* da, float* db, int64_t 
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, g, GK_ERR_ARG, "gk_add_bwd: null gradient");
     if (da) {
-        copy_acc_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, da, n, accumulate != 0);
+        copy_acc_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, da, n, accumulate != 0, vec4(g, da));
         GK_TRY(launched(ctx, "add_bwd_a"));
     }
     if (!db) return GK_OK;
     if (m == n) {
-        copy_acc_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, db, n, accumulate != 0);
+        copy_acc_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, db, n, accumulate != 0, vec4(g, db));
         return launched(ctx, "add_bwd_b");
     }
     // db = column sums of g viewed as [R, m]: row chunks in parallel, then the chunks in order
@@ -185,7 +279,7 @@ gk_status gk_mul_fwd(gk_ctx* ctx, const float* a, const float* b, float* y, int6
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_mul_fwd: negative size");
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, a && b && y, GK_ERR_ARG, "gk_mul_fwd: null pointer");
-    mul_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, b, y, n);
+    mul_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, b, y, n, vec4(a, b, y));
     return launched(ctx, "mul_fwd");
 }
 
@@ -195,7 +289,8 @@ gk_status gk_mul_bwd(gk_ctx* ctx, const float* g, const float* a, const float* b
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_mul_bwd: negative size");
     if (n == 0 || (!da && !db)) return GK_OK;
     GK_REQUIRE(ctx, g && (!da || b) && (!db || a), GK_ERR_ARG, "gk_mul_bwd: null pointer");
-    mul_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, a, b, da, db, n, accumulate != 0);
+    mul_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, a, b, da, db, n, accumulate != 0,
+                                                                     vec4(g, da ? b : nullptr, db ? a : nullptr, da, db));
     return launched(ctx, "mul_bwd");
 }
 
@@ -204,7 +299,7 @@ gk_status gk_scale_fwd(gk_ctx* ctx, const float* a, float s, float* y, int64_t n
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_scale_fwd: negative size");
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, a && y, GK_ERR_ARG, "gk_scale_fwd: null pointer");
-    scale_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, s, y, n, 0);
+    scale_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(a, s, y, n, 0, vec4(a, y));
     return launched(ctx, "scale_fwd");
 }
 
@@ -213,7 +308,7 @@ gk_status gk_scale_bwd(gk_ctx* ctx, const float* g, float s, float* da, int64_t 
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_scale_bwd: negative size");
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, g && da, GK_ERR_ARG, "gk_scale_bwd: null pointer");
-    scale_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, s, da, n, accumulate != 0);
+    scale_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, s, da, n, accumulate != 0, vec4(g, da));
     return launched(ctx, "scale_bwd");
 }
 
@@ -223,7 +318,7 @@ gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n) {
     const int P = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS * 8), 1024));
     double* part = static_cast<double*>(workspace(ctx, (size_t)P * sizeof(double)));
     GK_REQUIRE(ctx, part, GK_ERR_WORKSPACE, "gk_sum_fwd: needs %zu workspace bytes", (size_t)P * sizeof(double));
-    sum_partial_kernel<<<P, EW_THREADS, 0, ctx->stream>>>(a, n, part);
+    sum_partial_kernel<<<P, EW_THREADS, 0, ctx->stream>>>(a, n, part, vec4(a));
     GK_TRY(launched(ctx, "sum_partial"));
     sum_finish_kernel<<<1, 32, 0, ctx->stream>>>(part, P, y);
     return launched(ctx, "sum_finish");
@@ -234,7 +329,7 @@ gk_status gk_sum_bwd(gk_ctx* ctx, const float* g, float* da, int64_t n, int accu
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_sum_bwd: negative size");
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, g && da, GK_ERR_ARG, "gk_sum_bwd: null pointer");
-    sum_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, da, n, accumulate != 0);
+    sum_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(g, da, n, accumulate != 0, vec4(da));
     return launched(ctx, "sum_bwd");
 }
 
@@ -243,7 +338,7 @@ gk_status gk_tanh_fwd(gk_ctx* ctx, const float* x, float* y, int64_t n) {
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_tanh_fwd: negative size");
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, x && y, GK_ERR_ARG, "gk_tanh_fwd: null pointer");
-    tanh_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(x, y, n);
+    tanh_fwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(x, y, n, vec4(x, y));
     return launched(ctx, "tanh_fwd");
 }
 
@@ -252,7 +347,7 @@ gk_status gk_tanh_bwd(gk_ctx* ctx, const float* y, const float* g, float* dx, in
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_tanh_bwd: negative size");
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, y && g && dx, GK_ERR_ARG, "gk_tanh_bwd: null pointer");
-    tanh_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(y, g, dx, n, accumulate != 0);
+    tanh_bwd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(y, g, dx, n, accumulate != 0, vec4(y, g, dx));
     return launched(ctx, "tanh_bwd");
 }
 
@@ -261,7 +356,7 @@ gk_status gk_sgd_step(gk_ctx* ctx, float* p, const float* g, int64_t n, float lr
     GK_REQUIRE(ctx, n >= 0, GK_ERR_ARG, "gk_sgd_step: negative size");
     if (n == 0) return GK_OK;
     GK_REQUIRE(ctx, p && g, GK_ERR_ARG, "gk_sgd_step: null pointer");
-    sgd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(p, g, n, lr);
+    sgd_kernel<<<ew_blocks(ctx, n), EW_THREADS, 0, ctx->stream>>>(p, g, n, lr, vec4(p, g));
     return launched(ctx, "sgd");
 }
 

@@ -393,8 +393,8 @@ gk_status gk_mul_bwd(gk_ctx* ctx, const float* g, const float* a, const float* b
 gk_status gk_scale_fwd(gk_ctx* ctx, const float* a, float s, float* y, int64_t n);
 /* da (+)= s * g. */
 gk_status gk_scale_bwd(gk_ctx* ctx, const float* g, float s, float* da, int64_t n, int accumulate);
-/* y[0] = sum of a (double accumulation in a fixed order; n == 0 gives 0). Needs up to 8 KB of
- * workspace. */
+/* y[0] = sum of a in a fixed order (aligned groups of four added in float32, the groups and the
+ * partial sums in double; n == 0 gives 0). Needs up to 8 KB of workspace. */
 gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n);
 /* da (+)= g[0] for every element (g: one float32 on the device). */
 gk_status gk_sum_bwd(gk_ctx* ctx, const float* g, float* da, int64_t n, int accumulate);

@@ -11,7 +11,8 @@ Only F32 is read; any other dtype is refused.
 
 Readings where the pages are silent: the writer lays the tensors out back to back in the
 order given, pads the JSON with spaces to a multiple of 8 bytes (so the data starts aligned;
-JSON allows the trailing whitespace), and stores float32 little-endian.
+JSON allows the trailing whitespace), keeps non-ASCII names as UTF-8 rather than JSON
+unicode escapes, and stores float32 little-endian.
 """
 from __future__ import annotations
 
@@ -37,7 +38,7 @@ def write(path, tensors, metadata=None):
             raise FormatError(f"{name}: only float32 is written")
         header[name] = {"dtype": "F32", "shape": list(a.shape), "data_offsets": [begin, begin + a.nbytes]}
         begin += a.nbytes
-    text = json.dumps(header, separators=(",", ":")).encode()
+    text = json.dumps(header, separators=(",", ":"), ensure_ascii=False).encode("utf-8")
     text += b" " * (-len(text) % 8)
     with open(path, "wb") as f:
         f.write(struct.pack("<Q", len(text)))

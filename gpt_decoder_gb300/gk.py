@@ -18,7 +18,7 @@ _lib = ct.CDLL(LIB_PATH)
 
 # status codes and enums (include/gk.h)
 GK_OK, GK_ERR_ARG, GK_ERR_ALIGN, GK_ERR_UNSUPPORTED, GK_ERR_CUDA, GK_ERR_TIMEOUT, GK_ERR_OVERFLOW, GK_ERR_INDEX, \
-    GK_ERR_WORKSPACE = range(9)
+    GK_ERR_WORKSPACE, GK_ERR_IO, GK_ERR_FORMAT = range(11)
 GK_F32, GK_BF16, GK_BF16X2 = 0, 1, 2
 GK_MATH_FP32, GK_MATH_3XTF32 = 0, 1
 GK_ACT_NONE, GK_ACT_GELU = 0, 1
@@ -26,7 +26,8 @@ GK_ACT_NONE, GK_ACT_GELU = 0, 1
  GK_T_LN2_W, GK_T_LN2_B, GK_T_FC_W, GK_T_FC_B, GK_T_MLPPROJ_W, GK_T_MLPPROJ_B, GK_T_LNF_W, GK_T_LNF_B) = range(16)
 
 STATUS_NAMES = {0: "GK_OK", 1: "GK_ERR_ARG", 2: "GK_ERR_ALIGN", 3: "GK_ERR_UNSUPPORTED", 4: "GK_ERR_CUDA",
-                5: "GK_ERR_TIMEOUT", 6: "GK_ERR_OVERFLOW", 7: "GK_ERR_INDEX", 8: "GK_ERR_WORKSPACE"}
+                5: "GK_ERR_TIMEOUT", 6: "GK_ERR_OVERFLOW", 7: "GK_ERR_INDEX", 8: "GK_ERR_WORKSPACE", 9: "GK_ERR_IO",
+                10: "GK_ERR_FORMAT"}
 
 P = ct.c_void_p
 I32, I64, F32 = ct.c_int, ct.c_int64, ct.c_float
@@ -99,6 +100,19 @@ _SIGS = {
     "gk_prefill": (I32, [P, P, P, P, I32, P]),
     "gk_decode_step": (I32, [P, P, P, P, P, P, ct.POINTER(gk_sample_cfg)]),
     "gk_sample": (I32, [P, P, P, I64, P, ct.POINTER(gk_sample_cfg)]),
+    "gk_st_open": (I32, [ct.c_char_p, ct.POINTER(P)]),
+    "gk_st_close": (None, [P]),
+    "gk_st_count": (I32, [P]),
+    "gk_st_name": (ct.c_char_p, [P, I32]),
+    "gk_st_dtype": (ct.c_char_p, [P, I32]),
+    "gk_st_ndim": (I32, [P, I32]),
+    "gk_st_shape": (ct.POINTER(I64), [P, I32]),
+    "gk_st_find": (I32, [P, ct.c_char_p]),
+    "gk_st_metadata": (ct.c_char_p, [P, ct.c_char_p]),
+    "gk_st_read_f32": (I32, [P, I32, P, I64, I32]),
+    "gk_st_write_f32": (I32, [ct.c_char_p, I32, ct.POINTER(ct.c_char_p), ct.POINTER(I32), ct.POINTER(I64),
+                              ct.POINTER(P), I32, I32, ct.POINTER(ct.c_char_p), ct.POINTER(ct.c_char_p)]),
+    "gk_st_last_error": (ct.c_char_p, []),
 }
 
 EXPORTED = tuple(_SIGS)
@@ -388,3 +402,92 @@ def gk_sgd_step(ctx, p, g, n, lr):
 def gk_sample(ctx, kv, logits, ld, next_ids, sample=None):
     return _check(ctx, _lib.gk_sample(ctx.handle, kv.handle, _p(logits), ld, _p(next_ids), _sample(sample)),
                   "gk_sample")
+
+
+# ---- safetensors files of float32 tensors (host code in libgk; arrays on the host or the GPU)
+def _st_check(status, where):
+    if status != GK_OK:
+        raise GkError(status, where, _lib.gk_st_last_error().decode())
+
+
+class SafeTensors:
+    """An open safetensors file: names (header order), shapes, dtypes, metadata, and reads of
+    float32 tensors into new host arrays or into given host / CUDA tensors."""
+
+    def __init__(self, path):
+        h = P()
+        _st_check(_lib.gk_st_open(os.fsencode(path), ct.byref(h)), "gk_st_open")
+        self.handle = h
+
+    def close(self):
+        if self.handle:
+            _lib.gk_st_close(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def names(self):
+        return [_lib.gk_st_name(self.handle, i).decode() for i in range(_lib.gk_st_count(self.handle))]
+
+    def _index(self, name):
+        i = _lib.gk_st_find(self.handle, name.encode())
+        if i < 0:
+            raise KeyError(name)
+        return i
+
+    def shape(self, name):
+        i = self._index(name)
+        sh = _lib.gk_st_shape(self.handle, i)
+        return tuple(sh[k] for k in range(_lib.gk_st_ndim(self.handle, i)))
+
+    def dtype(self, name):
+        return _lib.gk_st_dtype(self.handle, self._index(name)).decode()
+
+    def metadata(self, key):
+        v = _lib.gk_st_metadata(self.handle, key.encode())
+        return None if v is None else v.decode()
+
+    def read(self, name, out=None):
+        """Into `out` (a contiguous float32 torch tensor, host or CUDA) or a new numpy array."""
+        import numpy as np
+
+        i = self._index(name)
+        if out is None:
+            arr = np.empty(self.shape(name), np.float32)
+            _st_check(_lib.gk_st_read_f32(self.handle, i, arr.ctypes.data, arr.size, 0), "gk_st_read_f32")
+            return arr
+        _st_check(_lib.gk_st_read_f32(self.handle, i, out.data_ptr(), out.numel(), int(out.is_cuda)),
+                  "gk_st_read_f32")
+        return out
+
+
+def write_safetensors(path, tensors, metadata=None):
+    """tensors: (name, array) pairs or a dict, each a float32 numpy array or a contiguous
+    float32 torch tensor (all on the host, or all on the GPU); metadata: str -> str."""
+    import numpy as np
+
+    items = list(tensors.items()) if isinstance(tensors, dict) else list(tensors)
+    keep, ptrs, ndims, shapes = [], [], [], []
+    on_dev = 0
+    for _, a in items:
+        if hasattr(a, "data_ptr"):
+            on_dev = int(a.is_cuda)
+            keep.append(a)
+            ptrs.append(a.data_ptr())
+        else:
+            a = np.require(a, dtype=np.float32, requirements="C")  # keeps 0-d arrays 0-d
+            keep.append(a)
+            ptrs.append(a.ctypes.data)
+        ndims.append(len(a.shape))
+        shapes += list(a.shape)
+    n, meta = len(items), list((metadata or {}).items())
+    names = (ct.c_char_p * max(n, 1))(*[k.encode() for k, _ in items])
+    mk = (ct.c_char_p * max(len(meta), 1))(*[str(k).encode() for k, _ in meta])
+    mv = (ct.c_char_p * max(len(meta), 1))(*[str(v).encode() for _, v in meta])
+    _st_check(_lib.gk_st_write_f32(os.fsencode(path), n, names, (I32 * max(n, 1))(*ndims),
+                                   (I64 * max(len(shapes), 1))(*shapes), (P * max(n, 1))(*ptrs), on_dev, len(meta),
+                                   mk, mv), "gk_st_write_f32")

@@ -164,6 +164,10 @@ class Gpt:
         views = self.named_slices(self.params)
         for k, v in named.items():
             views[k].copy_(torch.as_tensor(v, dtype=torch.float32))
+        self.refresh_bf16()
+
+    def refresh_bf16(self):
+        """Recompute the bf16 operand copies (and low planes) from the float32 parameters."""
         if self.params_bf16 is not None:
             gk.gk_to_bf16(self.ctx, self.params, self.params_bf16, self.numel)
             n = self.hi_hi - self.hi_lo

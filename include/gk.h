@@ -45,7 +45,9 @@ enum {
     GK_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (read back by gk_sync) */
     GK_ERR_OVERFLOW = 6,    /* KV cache full */
     GK_ERR_INDEX = 7,       /* a token id outside [0, V) (read back by gk_sync) */
-    GK_ERR_WORKSPACE = 8    /* the context's workspace is smaller than the call needs */
+    GK_ERR_WORKSPACE = 8,   /* the context's workspace is smaller than the call needs */
+    GK_ERR_IO = 9,          /* a file could not be opened, read, written or renamed */
+    GK_ERR_FORMAT = 10      /* a malformed file, or a dtype this build does not read */
 };
 
 enum { GK_F32 = 0, GK_BF16 = 1, GK_BF16X2 = 2 };
@@ -404,6 +406,42 @@ gk_status gk_tanh_fwd(gk_ctx* ctx, const float* x, float* y, int64_t n);
 gk_status gk_tanh_bwd(gk_ctx* ctx, const float* y, const float* g, float* dx, int64_t n, int accumulate);
 /* Plain SGD step ([LM1] The optimizer, Sgd): p -= lr * g. */
 gk_status gk_sgd_step(gk_ctx* ctx, float* p, const float* g, int64_t n, float lr);
+
+/* ---- safetensors files of float32 tensors ([LM4] "Build a language model in C# from scratch
+ * (4): running GPT-2 weights", "The safetensors format"): an 8-byte little-endian header length
+ * N, N bytes of JSON giving each tensor's dtype, shape and data_offsets [begin, end) (byte
+ * offsets from the end of the header) and an optional "__metadata__" object of strings, then
+ * the raw little-endian bytes. Host code; no context. A failing call returns its status and
+ * leaves a message for gk_st_last_error (per host thread). */
+typedef struct gk_st gk_st;
+/* Open and check a file: the header must parse, every entry must have a dtype string, a shape
+ * of non-negative integers and data_offsets inside the file (GK_ERR_FORMAT otherwise; GK_ERR_IO
+ * if it cannot be opened or read). Close with gk_st_close. */
+gk_status gk_st_open(const char* path, gk_st** out);
+void gk_st_close(gk_st* st);
+/* Tensors in header order (metadata excluded): count, name, dtype, rank and shape (owned by st);
+ * NULL / -1 for a bad index. gk_st_find gives a name's index or -1. */
+int gk_st_count(const gk_st* st);
+const char* gk_st_name(const gk_st* st, int i);
+const char* gk_st_dtype(const gk_st* st, int i);
+int gk_st_ndim(const gk_st* st, int i);
+const int64_t* gk_st_shape(const gk_st* st, int i);
+int gk_st_find(const gk_st* st, const char* name);
+/* A "__metadata__" value, or NULL. */
+const char* gk_st_metadata(const gk_st* st, const char* key);
+/* Read tensor i (n = its element count, else GK_ERR_ARG) into dst, a host buffer or, with
+ * dst_on_device, a device buffer (staged through host memory, synchronous). GK_ERR_FORMAT for
+ * a dtype other than F32 or data_offsets that do not span 4 bytes per element. */
+gk_status gk_st_read_f32(const gk_st* st, int i, float* dst, int64_t n, int dst_on_device);
+/* Write n float32 tensors (names unique, not "__metadata__"; ndims[t] extents each, taken in
+ * order from shapes; data[t] host or, with data_on_device, device pointers) and n_meta metadata
+ * strings. Tensors are laid out back to back in the order given, the JSON padded with spaces to
+ * a multiple of 8 bytes; the file is written as path + ".tmp" and renamed over path. */
+gk_status gk_st_write_f32(const char* path, int n, const char* const* names, const int* ndims,
+                          const int64_t* shapes, const float* const* data, int data_on_device,
+                          int n_meta, const char* const* meta_keys, const char* const* meta_values);
+/* The message of the last failing gk_st_* call on this host thread ("" if none). */
+const char* gk_st_last_error(void);
 
 #ifdef __cplusplus
 }

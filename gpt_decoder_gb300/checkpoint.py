@@ -11,16 +11,24 @@ from . import gk
 FORMAT = "gpt_decoder_gb300"
 
 
+def _gpt2_order(named):
+    """(name, view) pairs in GPT-2's order: embeddings, the blocks in order, then ln_f."""
+    keys = list(named)
+    order = ([k for k in keys if not k.startswith(("h.", "ln_f."))] + [k for k in keys if k.startswith("h.")]
+             + [k for k in keys if k.startswith("ln_f.")])
+    return [(k, named[k]) for k in order]
+
+
 def save(path, model, with_optimizer=True):
     """Write `model`'s parameters (and, with_optimizer, its AdamW state) to `path`."""
     import torch
 
     torch.cuda.current_stream().synchronize()
     gk.gk_sync(model.ctx)
-    tensors = list(model.named_slices(model.params).items())
+    tensors = _gpt2_order(model.named_slices(model.params))
     if with_optimizer:
-        tensors += [("adamw.m." + k, v) for k, v in model.named_slices(model.m).items()]
-        tensors += [("adamw.v." + k, v) for k, v in model.named_slices(model.v).items()]
+        tensors += [("adamw.m." + k, v) for k, v in _gpt2_order(model.named_slices(model.m))]
+        tensors += [("adamw.v." + k, v) for k, v in _gpt2_order(model.named_slices(model.v))]
     meta = {"format": FORMAT, "step": str(model.step_count),
             "shape": f"V={model.V} T={model.T} C={model.C} H={model.H} L={model.L}"}
     gk.write_safetensors(path, [(k, v.contiguous()) for k, v in tensors], meta)

@@ -130,3 +130,40 @@ def test_loss_decreases_over_steps(gkctx):
         losses.append(m.train_step(d_ids, d_tg, 1e-3, 0.01).item())
     gk.gk_sync(gkctx)
     assert losses[-1] < losses[0] - 0.3, losses
+
+
+def test_bench_batch_equals_its_four_quarters(gkctx):
+    """bench.py's configuration (GPT-2-124M, B=16 x T=1024, bf16 with the fused head), checked
+    through a property that holds at any size: the step's loss is the mean of the losses of its
+    four B=4 quarters, and its gradient the mean of theirs (B=4 is checked against the oracle
+    above). Rows do not interact, so only float32 summation orders differ: the B=16 launches
+    (their tile counts, CTA-pair grids and split-K choices) must not change any row's result."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+    from gpt_decoder_gb300.model import Gpt
+
+    s = synth.GPT2_124M
+    ids, targets, params = synth.training_case(s, 16, 2)
+    dev = lambda a: torch.as_tensor(np.ascontiguousarray(a).reshape(-1)).cuda()
+    m16 = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, 16, mode="bf16")
+    m16.load(params)
+    loss16 = m16.forward(dev(ids), dev(targets))
+    m16.backward(dev(ids), dev(targets))
+    m4 = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, 4, mode="bf16")
+    m4.load(params)
+    acc, losses = torch.zeros_like(m4.grads), []
+    for k in range(4):
+        q = slice(4 * k, 4 * k + 4)
+        losses.append(float(m4.forward(dev(ids[q]), dev(targets[q])).item()))  # forward's loss buffer is reused
+        m4.backward(dev(ids[q]), dev(targets[q]))
+        acc += m4.grads
+        m4.grads.zero_()
+    gk.gk_sync(gkctx)
+    mean4 = sum(losses) / 4
+    assert abs(float(loss16.item()) - mean4) < 1e-4, (loss16.item(), mean4)
+    acc /= 4
+    g16 = m16.named_slices(m16.grads)
+    worst = max((torch.linalg.vector_norm(g16[k] - v) / torch.linalg.vector_norm(v).clamp_min(1e-30)).item()
+                for k, v in m4.named_slices(acc).items())
+    assert worst < 2e-4, worst

@@ -61,11 +61,30 @@ struct Parser {
         } else if (c < 0x800) {
             s += (char)(0xC0 | (c >> 6));
             s += (char)(0x80 | (c & 0x3F));
-        } else {
+        } else if (c < 0x10000) {
             s += (char)(0xE0 | (c >> 12));
             s += (char)(0x80 | ((c >> 6) & 0x3F));
             s += (char)(0x80 | (c & 0x3F));
+        } else {
+            s += (char)(0xF0 | (c >> 18));
+            s += (char)(0x80 | ((c >> 12) & 0x3F));
+            s += (char)(0x80 | ((c >> 6) & 0x3F));
+            s += (char)(0x80 | (c & 0x3F));
         }
+    }
+    // four hex digits of a \u escape
+    bool hex4(uint32_t& v) {
+        if (e - p < 4) return fail("short \\u escape");
+        for (int k = 0; k < 4; ++k) {
+            const char h = *p++;
+            const int d = h >= '0' && h <= '9' ? h - '0'
+                          : h >= 'a' && h <= 'f' ? h - 'a' + 10
+                          : h >= 'A' && h <= 'F' ? h - 'A' + 10
+                                                 : -1;
+            if (d < 0) return fail("bad \\u escape");
+            v = v * 16 + (uint32_t)d;
+        }
+        return true;
     }
     bool string(std::string& out) {
         if (p >= e || *p != '"') return fail("expected a string");
@@ -89,16 +108,17 @@ struct Parser {
                 case 'r': out += '\r'; break;
                 case 't': out += '\t'; break;
                 case 'u': {
-                    if (e - p < 4) return fail("short \\u escape");
                     uint32_t c4 = 0;
-                    for (int k = 0; k < 4; ++k) {
-                        const char h = *p++;
-                        const int d = h >= '0' && h <= '9' ? h - '0'
-                                      : h >= 'a' && h <= 'f' ? h - 'a' + 10
-                                      : h >= 'A' && h <= 'F' ? h - 'A' + 10
-                                                             : -1;
-                        if (d < 0) return fail("bad \\u escape");
-                        c4 = c4 * 16 + (uint32_t)d;
+                    if (!hex4(c4)) return false;
+                    if (c4 >= 0xD800 && c4 <= 0xDBFF) {  // a high surrogate: its low half must follow
+                        uint32_t lo = 0;
+                        if (e - p < 2 || p[0] != '\\' || p[1] != 'u') return fail("lone surrogate");
+                        p += 2;
+                        if (!hex4(lo)) return false;
+                        if (lo < 0xDC00 || lo > 0xDFFF) return fail("lone surrogate");
+                        c4 = 0x10000 + ((c4 - 0xD800) << 10) + (lo - 0xDC00);
+                    } else if (c4 >= 0xDC00 && c4 <= 0xDFFF) {
+                        return fail("lone surrogate");
                     }
                     put_utf8(out, c4);
                     break;
@@ -212,6 +232,40 @@ struct Parser {
     }
 };
 
+// JSON text is UTF-8: well-formed sequences only (no overlongs, surrogates or code points past
+// U+10FFFF)
+bool valid_utf8(const std::string& t) {
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(t.data());
+    const unsigned char* e = p + t.size();
+    while (p < e) {
+        const unsigned c = *p++;
+        if (c < 0x80) continue;
+        int more;
+        unsigned cp;
+        if (c >= 0xC2 && c <= 0xDF) {
+            more = 1;
+            cp = c & 0x1F;
+        } else if (c >= 0xE0 && c <= 0xEF) {
+            more = 2;
+            cp = c & 0x0F;
+        } else if (c >= 0xF0 && c <= 0xF4) {
+            more = 3;
+            cp = c & 0x07;
+        } else {
+            return false;
+        }
+        if (e - p < more) return false;
+        for (int k = 0; k < more; ++k) {
+            if ((p[k] & 0xC0) != 0x80) return false;
+            cp = (cp << 6) | (p[k] & 0x3F);
+        }
+        p += more;
+        if ((more == 2 && cp < 0x800) || (more == 3 && cp < 0x10000) || cp > 0x10FFFF || (cp >= 0xD800 && cp <= 0xDFFF))
+            return false;
+    }
+    return true;
+}
+
 const Json* field(const Json& o, const char* key) {
     for (auto& kv : o.obj)
         if (kv.first == key) return &kv.second;
@@ -280,6 +334,7 @@ gk_status gk_st_open(const char* path, gk_st** out) {
         return st_fail(GK_ERR_IO, "gk_st_open: short read of the header");
     }
     fclose(f);
+    if (!valid_utf8(text)) return st_fail(GK_ERR_FORMAT, "gk_st_open: header is not valid UTF-8");
     Parser ps{text.data(), text.data() + text.size(), {}};
     Json root;
     bool ok = ps.value(root, 0);

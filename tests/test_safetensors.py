@@ -85,6 +85,9 @@ def _raw(p, text, data=b""):
     (b'{"x":{"shape":[1],"data_offsets":[0,4]}}', b"\0" * 4, True),                    # no dtype
     (b'{"__metadata__":{"a":1}}', b"", True),                                           # non-string metadata
     (b'[1,2]', b"", True),                                                              # not an object
+    (b'{"\xc3(":{"dtype":"F32","shape":[0],"data_offsets":[0,0]}}', b"", True),      # invalid UTF-8
+    (b'{"\\ud800x":{"dtype":"F32","shape":[0],"data_offsets":[0,0]}}', b"", True),  # lone surrogate
+    (b'{"\\udc00":{"dtype":"F32","shape":[0],"data_offsets":[0,0]}}', b"", True),   # lone low surrogate
     (b'{"x":{"dtype":"F16","shape":[2],"data_offsets":[0,4]}}', b"\0" * 4, False),    # dtype refused
     (b'{"x":{"dtype":"F32","shape":[3],"data_offsets":[0,8]}}', b"\0" * 8, False),    # offsets vs shape
 ])
@@ -134,3 +137,55 @@ def test_json_escapes_round_trip(gk, tmp_path):
     with gk.SafeTensors(p) as f:
         assert f.names() == ["tab\thereé/"]
         assert f.read("tab\thereé/")[0] == 2.5
+    # a surrogate pair is one character outside the basic plane
+    _raw(p, '{"\\ud83d\\ude00":{"dtype":"F32","shape":[0],"data_offsets":[0,0]}}'.encode())
+    with gk.SafeTensors(p) as f:
+        assert f.names() == ["\U0001F600"]
+
+
+def test_mutated_headers_are_opened_or_refused(gk, tmp_path):
+    """Byte flips, insertions and truncations of a valid file's header either still parse or
+    are refused with GK_ERR_FORMAT; the parser never reads past what the file holds."""
+    import random
+
+    p = tmp_path / "base.safetensors"
+    ost.write(p, _items(), {"format": "pt"})
+    base = p.read_bytes()
+    (n,) = struct.unpack("<Q", base[:8])
+    rng = random.Random(1)
+    alphabet = b'{}[]:,"\\0123456789-eE.tfnu ' + bytes(range(0x7F, 0x83)) + b"\xc3\xa9\xff"
+    q = tmp_path / "mut.safetensors"
+    outcomes = set()
+    for trial in range(400):
+        hdr = bytearray(base[8:8 + n])
+        for _ in range(rng.randint(1, 4)):
+            kind, at = rng.randrange(3), rng.randrange(len(hdr))
+            if kind == 0:
+                hdr[at] = rng.choice(alphabet)
+            elif kind == 1:
+                hdr[at:at] = bytes([rng.choice(alphabet)])
+            else:
+                del hdr[at:]
+                break
+        q.write_bytes(struct.pack("<Q", len(hdr)) + bytes(hdr) + base[8 + n:])
+        try:
+            with gk.SafeTensors(q) as f:
+                for name in f.names():
+                    try:
+                        f.read(name)
+                    except gk.GkError as e:  # an entry whose offsets no longer match its shape
+                        assert "GK_ERR_FORMAT" in str(e), str(e)
+            outcomes.add("ok")
+        except gk.GkError as e:
+            assert "GK_ERR_FORMAT" in str(e), str(e)
+            outcomes.add("refused")
+    assert outcomes == {"ok", "refused"}
+
+
+def test_checkpoint_order_is_gpt2s():
+    from gpt_decoder_gb300.checkpoint import _gpt2_order
+
+    names = [k for k, _ in synth.param_names_shapes(synth.TINY)]
+    scrambled = {k: i for i, k in enumerate(["wte.weight", "wpe.weight", "ln_f.weight", "ln_f.bias"]
+                                             + [k for k in names if k.startswith("h.")])}
+    assert [k for k, _ in _gpt2_order(scrambled)] == names

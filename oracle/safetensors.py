@@ -57,7 +57,10 @@ def read_header(path):
         text = f.read(n)
         if len(text) != n:
             raise FormatError("header runs past the end of the file")
-    obj = json.loads(text)
+    try:
+        obj = json.loads(text.decode("utf-8"))  # JSON text is UTF-8
+    except (UnicodeDecodeError, json.JSONDecodeError) as e:
+        raise FormatError(f"header: {e}") from None
     if not isinstance(obj, dict):
         raise FormatError("header is not a JSON object")
     return n, obj

@@ -83,6 +83,11 @@ def test_refusals(tmp_path):
     q.write_bytes(struct.pack("<Q", len(text)) + text + b"\0" * 8)  # 8 of 16 bytes
     with pytest.raises(ost.FormatError):
         ost.read(q)
+    u = tmp_path / "utf8.safetensors"
+    text = b'{"\xc3(":{"dtype":"F32","shape":[0],"data_offsets":[0,0]}}'
+    u.write_bytes(struct.pack("<Q", len(text)) + text)
+    with pytest.raises(ost.FormatError):
+        ost.read(u)
     r = tmp_path / "trunc.safetensors"
     r.write_bytes(struct.pack("<Q", 100) + b"{}")
     with pytest.raises(ost.FormatError):

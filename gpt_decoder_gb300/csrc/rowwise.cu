@@ -6,6 +6,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 
@@ -883,18 +884,24 @@ namespace {
 constexpr int64_t GK_LN_NOALLOC_SCRATCH_FLOATS = 1 << 20;
 static __device__ __align__(256) float g_ln_noalloc_scratch[GK_LN_NOALLOC_SCRATCH_FLOATS];
 
+// Per-device cache of the array's device address. Host threads making their first call at the
+// same time may both look it up; they store the same value, and the atomics make that well
+// defined. The cache assumes the device is not reset (cudaDeviceReset) while the library is
+// loaded: a reset would invalidate the address.
 constexpr int NOALLOC_MAX_DEVICES = 64;
-float* g_ln_noalloc_addr[NOALLOC_MAX_DEVICES] = {nullptr};
+std::atomic<float*> g_ln_noalloc_addr[NOALLOC_MAX_DEVICES];
 
 gk_status ln_noalloc_scratch(float** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GK_ERR_CUDA;
-    if (!g_ln_noalloc_addr[dev]) {
+    float* a = g_ln_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!a) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_ln_noalloc_scratch) != cudaSuccess || !p) return GK_ERR_CUDA;
-        g_ln_noalloc_addr[dev] = static_cast<float*>(p);
+        a = static_cast<float*>(p);
+        g_ln_noalloc_addr[dev].store(a, std::memory_order_release);
     }
-    *out = g_ln_noalloc_addr[dev];
+    *out = a;
     return GK_OK;
 }
 }  // namespace
@@ -906,6 +913,9 @@ extern "C" gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x,
     if (!x || !gamma || !mean || !rstd || !dy || !dx || rows <= 0 || C <= 0) return GK_ERR_ARG;
     // at least one partial slot of 2 x C floats must fit in the fixed array
     if ((int64_t)2 * C > GK_LN_NOALLOC_SCRATCH_FLOATS) return GK_ERR_WORKSPACE;
+    // an error left pending by earlier, unrelated CUDA work is reported (and left pending)
+    // instead of being read back below as this call's launch status
+    if (cudaPeekAtLastError() != cudaSuccess) return GK_ERR_CUDA;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     bool want_partials = dgamma || dbeta;
     float* partial = nullptr;

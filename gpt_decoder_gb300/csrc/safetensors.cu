@@ -366,8 +366,13 @@ gk_status gk_st_open(const char* path, gk_st** out) {
         gk_st::Entry e;
         e.name = kv.first;
         e.dtype = dt->str;
+        // the element count times 4 bytes must stay within int64: a product that wrapped could
+        // otherwise match data_offsets for a nonsensical shape
+        int64_t count = 1;
         for (auto& d : sh->arr) {
             if (d.kind != Json::NUM || !d.is_int || d.ival < 0) return bad(kv.first + ": bad shape");
+            if (d.ival > 0 && count > (INT64_MAX / 4) / d.ival) return bad(kv.first + ": shape too large");
+            count *= d.ival;
             e.shape.push_back(d.ival);
         }
         for (auto& o : off->arr)

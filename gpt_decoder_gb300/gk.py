@@ -59,6 +59,7 @@ _SIGS = {
     "gk_sync": (I32, [P]),
     "gk_last_error": (ct.c_char_p, [P]),
     "gk_launch_count": (I64, [P]),
+    "gk_selftest_wait_timeout": (I32, [P, I64, I32, P]),
     "gk_embedding_fwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_embedding_bwd": (I32, [P, P, P, P, P, I32, I32, I32, I32]),
     "gk_layernorm_fwd": (I32, [P, P, P, P, P, I32, P, P, I64, I32, F32, P]),
@@ -179,6 +180,11 @@ def gk_sync(ctx):
 
 def gk_launch_count(ctx):
     return _lib.gk_launch_count(ctx.handle)
+
+
+def gk_selftest_wait_timeout(ctx, limit_ns, arrive, elapsed_ns=None):
+    return _check(ctx, _lib.gk_selftest_wait_timeout(ctx.handle, int(limit_ns), int(arrive), _p(elapsed_ns)),
+                  "gk_selftest_wait_timeout")
 
 
 def gk_embedding_fwd(ctx, ids, wte, wpe, x, B, T, C, V):

@@ -78,6 +78,15 @@ const char* gk_last_error(gk_ctx* ctx);
 /* Number of kernel launches this context has issued since creation. */
 int64_t gk_launch_count(gk_ctx* ctx);
 
+/* Self-test of the bounded-wait failure path (no counterpart on the pages: it checks this
+ * library's own failure detection). One CTA allocates tensor memory, waits on an mbarrier
+ * with the same bounded wait the tensor-core kernels use, limit `limit_ns` (0 < limit <= 1 s),
+ * then frees the tensor memory and exits. With arrive = 0 no thread arrives: the wait expires,
+ * GK_ERR_TIMEOUT is recorded in the device error word (returned by the next gk_sync) and the
+ * context stays usable. With arrive != 0 one thread arrives first and nothing is recorded.
+ * elapsed_ns (device int64, may be NULL) receives the time the wait took. */
+gk_status gk_selftest_wait_timeout(gk_ctx* ctx, int64_t limit_ns, int arrive, long long* elapsed_ns);
+
 /* -------------------------------------------------------------------------- embedding */
 
 /* x[b*T + t, :] = wte[ids[b*T + t], :] + wpe[t, :].  [LM1] "Ops..." op table (Embedding);
@@ -137,8 +146,13 @@ gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, cons
  *   GK_ERR_WORKSPACE. Nothing in the array needs to start at zero: each call writes every
  *   partial slot before reading it, and the array keeps the last call's contents.
  *   Concurrency: all calls share the one array per device, so calls whose kernels overlap on
- *   the GPU (other streams, other host threads) race on it; serialise them.
- * Returns GK_ERR_ARG for null pointers or sizes <= 0, GK_ERR_CUDA if a CUDA call fails. */
+ *   the GPU (other streams, other host threads) race on it; serialise them. The per-device
+ *   address lookup itself is safe to race from several host threads. The cached address
+ *   assumes the device is not reset (cudaDeviceReset) while the library stays loaded.
+ * Returns GK_ERR_ARG for null pointers or sizes <= 0, GK_ERR_CUDA if a CUDA call fails. A
+ * CUDA error already pending from the caller's earlier work (cudaPeekAtLastError) makes the
+ * call return GK_ERR_CUDA before it launches anything, and that error is left pending for the
+ * caller; otherwise GK_ERR_CUDA is the status of this call's own launches. */
 gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x, const float* gamma,
                                    const float* mean, const float* rstd, const float* dy, float* dx,
                                    int accumulate_dx, uint16_t* dx_bf16, float* dgamma, float* dbeta,

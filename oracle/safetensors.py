@@ -17,6 +17,7 @@ unicode escapes, and stores float32 little-endian.
 from __future__ import annotations
 
 import json
+import math
 import struct
 
 import numpy as np
@@ -82,7 +83,7 @@ def read(path):
                 raise FormatError(f"{name}: dtype {e['dtype']}, only F32 is handled")
             begin, end = e["data_offsets"]
             shape = tuple(int(s) for s in e["shape"])
-            count = int(np.prod(shape, dtype=np.int64)) if shape else 1
+            count = math.prod(shape)  # exact (Python integers): a shape whose size overflows is refused below
             if end - begin != 4 * count or begin < 0 or data_start + end > size:
                 raise FormatError(f"{name}: data_offsets {begin}, {end} do not fit shape {shape} and the file")
             f.seek(data_start + begin)

@@ -132,12 +132,15 @@ def test_loss_decreases_over_steps(gkctx):
     assert losses[-1] < losses[0] - 0.3, losses
 
 
-def test_bench_batch_equals_its_four_quarters(gkctx):
-    """bench.py's configuration (GPT-2-124M, B=16 x T=1024, bf16 with the fused head), checked
-    through a property that holds at any size: the step's loss is the mean of the losses of its
-    four B=4 quarters, and its gradient the mean of theirs (B=4 is checked against the oracle
-    above). Rows do not interact, so only float32 summation orders differ: the B=16 launches
-    (their tile counts, CTA-pair grids and split-K choices) must not change any row's result."""
+def test_bench_batch_forward_equals_its_four_quarters(gkctx):
+    """bench.py's configuration (GPT-2-124M, B=16 x T=1024, bf16 with the fused head): rows do
+    not interact in the forward, and every forward kernel reduces within a row in an order that
+    does not depend on the batch, so the B=16 launches (their tile counts, CTA-pair grids) must
+    leave every row's residual stream and log-sum-exp bit-identical to those of the four B=4
+    quarters, and the loss equal to the mean of the quarters' losses up to float32 rounding.
+    (The backward is checked against the oracle at B=16 below: there, float32 reductions whose
+    order depends on the launch shape, re-rounded to bf16 at every block, make B=16 and B=4
+    differ at the bf16 error level, not bit for bit.)"""
     import torch
 
     from gpt_decoder_gb300 import gk
@@ -148,22 +151,47 @@ def test_bench_batch_equals_its_four_quarters(gkctx):
     dev = lambda a: torch.as_tensor(np.ascontiguousarray(a).reshape(-1)).cuda()
     m16 = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, 16, mode="bf16")
     m16.load(params)
-    loss16 = m16.forward(dev(ids), dev(targets))
-    m16.backward(dev(ids), dev(targets))
+    loss16 = float(m16.forward(dev(ids), dev(targets)).item())
+    keep = {f"xs{i}": m16.xs[i].clone() for i in range(1, len(m16.xs))}
+    keep["lse"] = m16.lse_ce.clone()
+    del m16
     m4 = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, 4, mode="bf16")
     m4.load(params)
-    acc, losses = torch.zeros_like(m4.grads), []
+    losses = []
+    n = 4 * s.T
     for k in range(4):
         q = slice(4 * k, 4 * k + 4)
-        losses.append(float(m4.forward(dev(ids[q]), dev(targets[q])).item()))  # forward's loss buffer is reused
-        m4.backward(dev(ids[q]), dev(targets[q]))
-        acc += m4.grads
-        m4.grads.zero_()
-    gk.gk_sync(gkctx)
-    mean4 = sum(losses) / 4
-    assert abs(float(loss16.item()) - mean4) < 1e-4, (loss16.item(), mean4)
-    acc /= 4
-    g16 = m16.named_slices(m16.grads)
-    worst = max((torch.linalg.vector_norm(g16[k] - v) / torch.linalg.vector_norm(v).clamp_min(1e-30)).item()
-                for k, v in m4.named_slices(acc).items())
-    assert worst < 2e-4, worst
+        losses.append(float(m4.forward(dev(ids[q]), dev(targets[q])).item()))
+        gk.gk_sync(gkctx)
+        for name, full in keep.items():
+            part = m4.lse_ce if name == "lse" else m4.xs[int(name[2:])]
+            assert torch.equal(full[k * n:(k + 1) * n], part), (k, name)
+    assert abs(loss16 - sum(losses) / 4) < 1e-5, (loss16, losses)
+
+
+_GPT2_B16_ORACLE = {}
+
+
+@pytest.mark.slow
+def test_gpt2_124m_bench_config_step_vs_oracle(gkctx):
+    """The step bench.py times (GPT-2-124M, B=16 x T=1024, bf16 with the fused LM head) against
+    the oracle at the fast-mode tolerances: loss, per-tensor gradient relative-L2 and the AdamW
+    update. The oracle's B=16 gradient is the mean of its four B=4 quarters' gradients (float64;
+    the loss is a mean over rows, so this is the same quantity), which keeps its host memory at
+    the B=4 size."""
+    s = synth.GPT2_124M
+    got = _run_step(gkctx, s, 16, 2, "bf16-fused")
+    if "ref" not in _GPT2_B16_ORACLE:
+        ids, targets, params = got["inputs"]
+        sh = ogpt.Shape(s.V, s.T, s.C, s.H, s.L)
+        loss, grads = 0.0, None
+        for k in range(4):
+            q = slice(4 * k, 4 * k + 4)
+            lq, gq, _, _ = ogpt.loss_and_grads(params, ids[q], targets[q], sh)
+            loss += lq / 4
+            grads = {n: v / 4 for n, v in gq.items()} if grads is None else {n: grads[n] + gq[n] / 4 for n in grads}
+        newp, _ = ogpt.adamw_step(params, grads, {}, 1, LR, wd=WD)
+        _GPT2_B16_ORACLE["ref"] = dict(loss=loss, logits=None, grads=grads, params=newp)
+    ref = _GPT2_B16_ORACLE["ref"]
+    worst, flips = _compare(got, ref, "bf16-fused")
+    print(f"gpt2 B=16 bf16-fused: loss {got['loss']:.6f} vs {ref['loss']:.6f}; worst grad {worst}; flips {flips}")

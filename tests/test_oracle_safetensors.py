@@ -92,3 +92,12 @@ def test_refusals(tmp_path):
     r.write_bytes(struct.pack("<Q", 100) + b"{}")
     with pytest.raises(ost.FormatError):
         ost.read(r)
+
+
+def test_shape_whose_size_overflows_is_refused(tmp_path):
+    # 2^32 x 2^32 elements: a 64-bit product wraps to 0 and would match empty data_offsets
+    p = tmp_path / "wrap.safetensors"
+    text = b'{"x":{"dtype":"F32","shape":[4294967296,4294967296],"data_offsets":[0,0]}}'
+    p.write_bytes(struct.pack("<Q", len(text)) + text)
+    with pytest.raises(ost.FormatError):
+        ost.read(p)

@@ -90,6 +90,8 @@ def _raw(p, text, data=b""):
     (b'{"\\udc00":{"dtype":"F32","shape":[0],"data_offsets":[0,0]}}', b"", True),   # lone low surrogate
     (b'{"x":{"dtype":"F16","shape":[2],"data_offsets":[0,4]}}', b"\0" * 4, False),    # dtype refused
     (b'{"x":{"dtype":"F32","shape":[3],"data_offsets":[0,8]}}', b"\0" * 8, False),    # offsets vs shape
+    (b'{"x":{"dtype":"F32","shape":[4294967296,4294967296],"data_offsets":[0,0]}}', b"", True),  # count wraps
+    (b'{"x":{"dtype":"F32","shape":[4611686018427387904,4],"data_offsets":[0,0]}}', b"", True),  # bytes wrap
 ])
 def test_malformed_files_are_refused(gk, tmp_path, text, data, at_open):
     p = _raw(tmp_path / "bad.safetensors", text, data)

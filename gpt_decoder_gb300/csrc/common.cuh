@@ -16,7 +16,7 @@ struct gk_ctx {
     int* d_err = nullptr;      // device error word: first kernel-side error code
     void* ws = nullptr;        // device workspace
     size_t ws_bytes = 0;
-    int math = GK_MATH_FP32;
+    int math = GK_MATH_3XTF32;
     int64_t launches = 0;
     char msg[512] = {0};
 };

@@ -42,6 +42,10 @@ struct Gemm {
     const void* B_lo = nullptr;
     // > 0 with bf16 C: C's low plane (v - bf16(v)) is also written, at C + c_plane elements
     int64_t c_plane = 0;
+    // tf32: A, A_lo, B, B_lo are float32 containers of TF32 values, hi and lo planes of float32
+    // operands (value = hi + lo), both K-major; the tensor-core kernel then adds the three
+    // products A_hi B_hi + A_hi B_lo + A_lo B_hi (3xTF32)
+    bool tf32 = false;
     // Softmax cross-entropy fused into a vocabulary-projection epilogue (tensor-core kernel,
     // TMA epilogue only). Column n of this GEMM is vocabulary entry ce_col0 + n, and
     // ce_tgt[m] is row m's target entry.
@@ -69,6 +73,10 @@ gk_status gemm_simt(gk_ctx* ctx, const Gemm& g);
 gk_status gemm_tc(gk_ctx* ctx, const Gemm& g);
 // Dispatch by operand type, arithmetic mode and shape.
 gk_status gemm(gk_ctx* ctx, const Gemm& g);
+// Float32 operands (either majorness) in 3xTF32 on the tensor cores: each operand is split
+// into TF32 hi / lo planes (K-major, in the context's workspace, in chunks of the output or of
+// K when the whole does not fit), then gemm_tc adds the three products.
+gk_status gemm_3xtf32(gk_ctx* ctx, const Gemm& g);
 
 // Tensor-core causal attention forward (bf16 q/k/v, head size 64); GK_ERR_UNSUPPORTED otherwise.
 gk_status attn_fwd_tc(gk_ctx* ctx, const void* qkv, void* y, float* lse, int B, int T, int H, int hs);

@@ -658,7 +658,9 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
     return ok;
 }
 
-template <typename TC, int SPLIT>
+// F32OP: the operands are float32 containers of TF32 values (K-major, hi and lo planes; SPLIT
+// is 3): kind::tf32 MMAs, 32-deep K slices of the same 128-byte rows.
+template <typename TC, int SPLIT, bool F32OP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA_lo, const __grid_constant__ CUtensorMap tmB_lo,
@@ -668,6 +670,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     using SC = StageCfg<SPLIT>;
     constexpr int STAGES = SC::STAGES;
     constexpr bool PAIR = SC::PAIR;
+    constexpr int BKE = F32OP ? BK / 2 : BK;  // K elements per 128-byte row of a stage
+    static_assert(!F32OP || (SPLIT == 3 && !PAIR), "TF32 operands come as hi and lo planes");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // stage s: A_hi at smem + s*STAGE, A_lo at + A_BYTES, B_hi at + A_SLOT, B_lo at + A_SLOT + B_BYTES
@@ -748,8 +752,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int pl = 0; pl < (SC::A_LO ? 2 : 1); ++pl) {
                         const CUtensorMap* ma = pl ? &tmA_lo : &tmA;
                         uint8_t* dst = a + pl * A_BYTES;
-                        if (p.a_kmajor) {
-                            load(ma, dst, kb * BK, tm * BM);
+                        if (F32OP || p.a_kmajor) {
+                            load(ma, dst, kb * BKE, tm * BM);
                         } else {
                             load(ma, dst, tm * BM, kb * BK);
                             load(ma, dst + 8192, tm * BM + 64, kb * BK);
@@ -762,8 +766,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // this CTA's columns of the tile's B (all of them, or its half in a pair)
                         constexpr int BNC = (int)(SC::B_TILE / (BK * 2));
                         const int n0 = tn * BN + (int)rank * BNC;
-                        if (p.b_kmajor) {
-                            load(mb, dst, kb * BK, n0);
+                        if (F32OP || p.b_kmajor) {
+                            load(mb, dst, kb * BKE, n0);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BNC / 64; ++j) load(mb, dst + j * 8192, n0 + 64 * j, kb * BK);
@@ -793,7 +797,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // The whole warp walks the loop in step (so the descriptors stay warp-uniform) and one
         // elected lane issues the MMAs and commits. In a pair this is the even CTA, issuing
         // 256-row MMAs whose commits reach both CTAs' barriers.
-        const uint32_t idesc = instr_desc_bf16(!p.a_kmajor, !p.b_kmajor, PAIR ? 2 * BM : BM, BN);
+        const uint32_t idesc = F32OP ? instr_desc_tf32(BM, BN)
+                                     : instr_desc_bf16(!p.a_kmajor, !p.b_kmajor, PAIR ? 2 * BM : BM, BN);
         // per 16-deep K step: K-major operands advance 32 bytes inside the swizzled row,
         // MN-major operands advance two 8-row core-matrix groups (2 x 1024 bytes)
         const uint32_t a_step = p.a_kmajor ? 32u : 2048u;
@@ -826,7 +831,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t ad = desc_add(ad0, k * a_step), bd = desc_add(bd0, k * b_step);
                         const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-                        if (PAIR) {
+                        if constexpr (F32OP) {
+                            // 3xTF32: A_hi B_hi + A_hi B_lo + A_lo B_hi (A_lo B_lo, about 2^-22
+                            // relative, is dropped)
+                            umma_tf32(d_tmem, ad, bd, idesc, acc);
+                            umma_tf32(d_tmem, ad, desc_add(bd0, B_BYTES + k * b_step), idesc, 1u);
+                            umma_tf32(d_tmem, desc_add(ad0, A_BYTES + k * a_step), bd, idesc, 1u);
+                        } else if (PAIR) {
                             umma_bf16_pair(d_tmem, ad, bd, idesc, acc);
                         } else {
                             umma_bf16(d_tmem, ad, bd, idesc, acc);
@@ -942,12 +953,12 @@ struct Maps {
     CUtensorMap a, b, al, bl, c, aux, r, lo;
 };
 
-template <typename TC, int SPLIT>
+template <typename TC, int SPLIT, bool F32OP = false>
 void launch_one(gk_ctx* ctx, int grid, const Maps& m, const TcParams& p) {
     static bool attr = false;
     constexpr size_t smem = StageCfg<SPLIT>::SMEM;
     if (!attr) {
-        cudaFuncSetAttribute(gemm_tc_kernel<TC, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, SPLIT, F32OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
     if constexpr (SPLIT == PAIR_MODE) {
@@ -963,10 +974,10 @@ void launch_one(gk_ctx* ctx, int grid, const Maps& m, const TcParams& p) {
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC, SPLIT>, m.a, m.b, m.al, m.bl, m.c, m.aux, m.r, m.lo, p);
+        cudaLaunchKernelEx(&cfg, gemm_tc_kernel<TC, SPLIT, false>, m.a, m.b, m.al, m.bl, m.c, m.aux, m.r, m.lo, p);
     } else {
-        gemm_tc_kernel<TC, SPLIT><<<grid, THREADS, smem, ctx->stream>>>(m.a, m.b, m.al, m.bl, m.c, m.aux, m.r, m.lo,
-                                                                         p);
+        gemm_tc_kernel<TC, SPLIT, F32OP><<<grid, THREADS, smem, ctx->stream>>>(m.a, m.b, m.al, m.bl, m.c, m.aux, m.r,
+                                                                                m.lo, p);
     }
 }
 
@@ -988,8 +999,9 @@ int max_pairs() {
     static int n = -1;
     if (n < 0) {
         constexpr size_t smem = StageCfg<PAIR_MODE>::SMEM;
-        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(2);
         cfg.blockDim = dim3(THREADS);
@@ -1002,7 +1014,7 @@ int max_pairs() {
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int c = 0;
-        n = cudaOccupancyMaxActiveClusters(&c, gemm_tc_kernel<TC, PAIR_MODE>, &cfg) == cudaSuccess ? c : 0;
+        n = cudaOccupancyMaxActiveClusters(&c, gemm_tc_kernel<TC, PAIR_MODE, false>, &cfg) == cudaSuccess ? c : 0;
         cudaGetLastError();
     }
     return n;
@@ -1052,8 +1064,15 @@ bool setup_tma_epilogue(const Gemm& g, TcParams& p, Maps& m) {
 }  // namespace
 
 gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
-    if (g.ab_dtype != GK_BF16) return GK_ERR_UNSUPPORTED;
-    if (!aligned16(g.A) || !aligned16(g.B) || (g.lda & 7) || (g.ldb & 7)) return GK_ERR_UNSUPPORTED;
+    const bool f32op = g.tf32;  // TF32 hi / lo planes in float32 containers, K-major
+    if (f32op) {
+        if (g.ab_dtype != GK_F32 || !g.a_kmajor || !g.b_kmajor || !g.A_lo || !g.B_lo || g.ce_mode != CE_NONE ||
+            g.c_dtype != GK_F32 || (g.lda & 3) || (g.ldb & 3) || !aligned16(g.A_lo) || !aligned16(g.B_lo))
+            return GK_ERR_UNSUPPORTED;
+    } else if (g.ab_dtype != GK_BF16 || (g.lda & 7) || (g.ldb & 7)) {
+        return GK_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(g.A) || !aligned16(g.B)) return GK_ERR_UNSUPPORTED;
     if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.M >= (1ll << 31) || g.N >= (1ll << 31) || g.K >= (1ll << 31))
         return GK_ERR_UNSUPPORTED;
     const int split = (g.A_lo ? 1 : 0) | (g.B_lo ? 2 : 0);
@@ -1063,9 +1082,14 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     const int pairs = split == 0 && cdiv(g.M, BM) >= 4 ? (c_f32 ? max_pairs<float>() : max_pairs<__nv_bfloat16>()) : 0;
     const bool pair = pairs > 0;
     CUtensorMap ta, tb;
-    bool ok = g.a_kmajor ? make_map(&ta, g.A, g.K, g.M, g.lda, BM) : make_map(&ta, g.A, g.M, g.K, g.lda, 64);
-    ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, pair ? BN / 2 : BN)
-                           : make_map(&tb, g.B, g.N, g.K, g.ldb, 64));
+    bool ok;
+    if (f32op) {
+        ok = make_map_f32(&ta, g.A, g.K, g.M, g.lda, BK / 2, BM) && make_map_f32(&tb, g.B, g.K, g.N, g.ldb, BK / 2, BN);
+    } else {
+        ok = g.a_kmajor ? make_map(&ta, g.A, g.K, g.M, g.lda, BM) : make_map(&ta, g.A, g.M, g.K, g.lda, 64);
+        ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, pair ? BN / 2 : BN)
+                               : make_map(&tb, g.B, g.N, g.K, g.ldb, 64));
+    }
     if (!ok) return GK_ERR_UNSUPPORTED;
     TcParams p{};
     p.pair = pair ? 1 : 0;
@@ -1075,7 +1099,7 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.tiles_m = (int)cdiv(g.M, BM);
     p.tiles_n = (int)cdiv(g.N, BN);
     p.tiles_m2 = (int)cdiv(p.tiles_m, 2);
-    p.kblocks = (int)cdiv(g.K, BK);
+    p.kblocks = (int)cdiv(g.K, f32op ? BK / 2 : BK);
     p.a_kmajor = g.a_kmajor;
     p.b_kmajor = g.b_kmajor;
     p.C = g.C;
@@ -1117,10 +1141,18 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     m.b = tb;
     m.al = ta;
     m.bl = tb;
-    if (g.A_lo && !(g.a_kmajor ? make_map(&m.al, g.A_lo, g.K, g.M, g.lda, BM) : make_map(&m.al, g.A_lo, g.M, g.K, g.lda, 64)))
-        return GK_ERR_UNSUPPORTED;
-    if (g.B_lo && !(g.b_kmajor ? make_map(&m.bl, g.B_lo, g.K, g.N, g.ldb, BN) : make_map(&m.bl, g.B_lo, g.N, g.K, g.ldb, 64)))
-        return GK_ERR_UNSUPPORTED;
+    if (f32op) {
+        if (!make_map_f32(&m.al, g.A_lo, g.K, g.M, g.lda, BK / 2, BM) ||
+            !make_map_f32(&m.bl, g.B_lo, g.K, g.N, g.ldb, BK / 2, BN))
+            return GK_ERR_UNSUPPORTED;
+    } else {
+        if (g.A_lo && !(g.a_kmajor ? make_map(&m.al, g.A_lo, g.K, g.M, g.lda, BM)
+                                   : make_map(&m.al, g.A_lo, g.M, g.K, g.lda, 64)))
+            return GK_ERR_UNSUPPORTED;
+        if (g.B_lo && !(g.b_kmajor ? make_map(&m.bl, g.B_lo, g.K, g.N, g.ldb, BN)
+                                   : make_map(&m.bl, g.B_lo, g.N, g.K, g.ldb, 64)))
+            return GK_ERR_UNSUPPORTED;
+    }
     p.ce_mode = g.ce_mode;
     p.ce_nparts = g.ce_nparts;
     p.ce_col0 = g.ce_col0;
@@ -1144,7 +1176,9 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
         p.in_kind = IN_NONE;
         p.reduce_out = p.out_aux = p.out_lo = 0;
     }
-    if (g.c_dtype == GK_F32)
+    if (f32op)
+        launch_one<float, 3, true>(ctx, grid, m, p);
+    else if (g.c_dtype == GK_F32)
         launch_split<float>(ctx, mode, grid, m, p);
     else
         launch_split<__nv_bfloat16>(ctx, mode, grid, m, p);

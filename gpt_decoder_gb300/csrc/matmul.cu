@@ -127,6 +127,12 @@ gk_status gemm(gk_ctx* ctx, const Gemm& g) {
         gk_status s = gemm_tc(ctx, g);
         if (s != GK_ERR_UNSUPPORTED) return s;
     }
+    if (g.ab_dtype == GK_F32 && ctx->math == GK_MATH_3XTF32) {
+        // float32 products with float32 results; other output types (a bf16 result of float32
+        // operands) keep the float32 FMA kernel
+        gk_status s = gemm_3xtf32(ctx, g);
+        if (s != GK_ERR_UNSUPPORTED) return s;
+    }
     return gemm_simt(ctx, g);
 }
 

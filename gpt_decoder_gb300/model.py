@@ -11,8 +11,10 @@ pass over two contiguous blocks (decayed matrices, undecayed vectors).
 This module only allocates device memory (torch) and sequences calls; every arithmetic step
 runs in libgk's kernels.
 
-Modes: "fp32" runs every product in float32 (the faithful mode); "bf16" keeps float32
-master weights, moments, residual stream and logits, and feeds the matrix products bf16
+Modes: "fp32" runs every product on float32 operands (the faithful mode), by default as
+3xTF32 on the tensor cores (math="3xtf32": each operand split into TF32 hi and lo parts, three
+products accumulated in float32) or with math="fp32" as float32 FMA on the CUDA cores; "bf16"
+keeps float32 master weights, moments, residual stream and logits, and feeds the matrix products bf16
 operands (a bf16 weight copy that AdamW refreshes, bf16 activations) with float32
 accumulation. In bf16 mode the forward products of the first `hi_layers` blocks (default 2)
 use split-bf16 operands (value = hi + lo, two bf16 planes, three tensor-core products):
@@ -36,9 +38,13 @@ def pad_vocab(V: int, mult: int = 64) -> int:
 
 
 class Gpt:
-    def __init__(self, ctx: gk.Ctx, V, T, C, H, L, B, mode="fp32", device="cuda", hi_layers=2, fused_head=None):
+    def __init__(self, ctx: gk.Ctx, V, T, C, H, L, B, mode="fp32", device="cuda", hi_layers=2, fused_head=None,
+                 math="3xtf32"):
         assert mode in ("fp32", "bf16")
+        assert math in ("3xtf32", "fp32")
         self.ctx, self.mode, self.device = ctx, mode, device
+        # arithmetic of the float32 products (the context's math mode, set before each pass)
+        self.math = gk.GK_MATH_3XTF32 if math == "3xtf32" else gk.GK_MATH_FP32
         # bf16 mode: the LM head and the cross-entropy run fused (gk_lmhead_ce_*), with no
         # [N, V] logits tensor; fused_head=False keeps the separate head GEMM and CE kernels
         # (and self.logits) as in fp32 mode
@@ -200,6 +206,7 @@ class Gpt:
     def forward(self, ids, targets):
         """Logits and loss of one batch (ids, targets: int32 device tensors [B*T])."""
         c, dt, N, C, H, hs, B, T = self.ctx, self.dt, self.N, self.C, self.H, self.hs, self.B, self.T
+        gk.gk_set_math(c, self.math)
         gk.gk_embedding_fwd(c, ids, self.w(gk.GK_T_WTE), self.w(gk.GK_T_WPE), self.xs[0], B, T, C, self.V)
         for l in range(self.L):
             dt = self.ldt[l]
@@ -242,6 +249,7 @@ class Gpt:
     def backward(self, ids, targets):
         """Parameter gradients ADDED into self.grads (zero them first, or let AdamW do it)."""
         c, dt, N, C, H, hs, B, T = self.ctx, self.dt, self.N, self.C, self.H, self.hs, self.B, self.T
+        gk.gk_set_math(c, self.math)
         if self.fused_head:
             # dlnf = dlogits wte, dwte += dlogits^T lnf, the logits recomputed per vocabulary chunk
             # (the timed FLOPs count the two products only)

@@ -51,8 +51,15 @@ enum {
 };
 
 enum { GK_F32 = 0, GK_BF16 = 1, GK_BF16X2 = 2 };
-/* Arithmetic of float32 GEMMs: plain fp32 FMA, or three TF32 tensor-core products with the
- * operands split into high and low TF32 parts. Both are "faithful" (fp32-level) modes. */
+/* Arithmetic of the products with float32 operands (the faithful mode):
+ *   GK_MATH_3XTF32 (default): each operand x is split into TF32 parts hi = tf32(x) and
+ *     lo = tf32(x - hi) (about 22 significant bits together), and the product is
+ *     A_hi B_hi + A_hi B_lo + A_lo B_hi on the tensor cores (kind::tf32, float32 accumulation in
+ *     tensor memory); the planes are written K-major into the context's workspace, in blocks
+ *     of the output (and of K for plain sums) when the whole does not fit, so it needs at
+ *     least 8 * Kc * (128 + 256) bytes for some K slice Kc (GK_ERR_WORKSPACE otherwise).
+ *     Products with a bf16 result keep the FMA kernel.
+ *   GK_MATH_FP32: float32 FMA on the CUDA cores (exact float32 products, float32 sums). */
 enum { GK_MATH_FP32 = 0, GK_MATH_3XTF32 = 1 };
 enum { GK_ACT_NONE = 0, GK_ACT_GELU = 1 };
 
@@ -68,7 +75,7 @@ gk_status gk_ctx_create(gk_ctx** out, void* cuda_stream, size_t workspace_bytes)
 void gk_ctx_destroy(gk_ctx* ctx);
 /* Rebind the stream (e.g. to the stream a graph capture runs on). */
 gk_status gk_ctx_set_stream(gk_ctx* ctx, void* cuda_stream);
-/* GK_MATH_FP32 (default) or GK_MATH_3XTF32 for float32 GEMMs. */
+/* GK_MATH_3XTF32 (default) or GK_MATH_FP32 for the float32 products of later calls. */
 gk_status gk_set_math(gk_ctx* ctx, int math);
 /* Wait for the stream, then read and clear the device error word: returns the first kernel
  * error recorded since the last gk_sync (GK_ERR_INDEX, GK_ERR_TIMEOUT, ...), else GK_OK. */

@@ -54,6 +54,27 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
 
 
+def assert_close(got, ref, tol, what=""):
+    """Parity of a GPU output with its reference: EVERY element within tol * max|ref| (a wrong
+    tile, edge, row or column fails this even where a norm over millions of elements would not),
+    and the relative L2 of the whole below tol."""
+    import numpy as np
+
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if got.size == 0:
+        return
+    err = np.abs(got - ref)
+    scale = max(float(np.abs(ref).max()), 1e-30)
+    worst = float(err.max())
+    if not worst <= tol * scale:
+        at = np.unravel_index(int(np.nanargmax(err)), err.shape)
+        raise AssertionError(f"{what}: max |err| {worst:.3e} at {at} exceeds {tol} x max|ref| {scale:.3e}")
+    r = rel_l2(got, ref)
+    assert r < tol, f"{what}: relative L2 {r:.3e} >= {tol}"
+
+
 @pytest.fixture(autouse=True)
 def _float32_default_dtype():
     """GPU buffers are allocated with torch's default dtype: keep it float32 for every test."""

@@ -15,9 +15,11 @@ from tests.conftest import rel_l2
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"fp32": dict(logits=5e-4, grad=1e-4), "bf16": dict(logits=2e-2, grad=1e-2),
-       "bf16-fused": dict(logits=2e-2, grad=1e-2)}
-MODES = ["fp32", "bf16", "bf16-fused"]
+TOL = {"fp32": dict(logits=5e-4, grad=1e-4), "fp32-fma": dict(logits=5e-4, grad=1e-4),
+       "bf16": dict(logits=2e-2, grad=1e-2), "bf16-fused": dict(logits=2e-2, grad=1e-2)}
+# "fp32": the faithful mode's float32 products as 3xTF32 on the tensor cores; "fp32-fma": the
+# same mode with float32 FMA on the CUDA cores
+MODES = ["fp32", "fp32-fma", "bf16", "bf16-fused"]
 LR, WD = 3e-4, 0.01
 
 
@@ -29,7 +31,8 @@ def _run_step(gkctx, s, B, seed, mode):
     ids, targets, params = synth.training_case(s, B, seed)
     # "bf16-fused": the fused LM head + cross-entropy (no logits tensor); "bf16": the separate
     # head GEMM and CE kernels, whose logits are checked
-    m = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, B, mode=mode.split("-")[0], fused_head=mode == "bf16-fused")
+    m = Gpt(gkctx, s.V, s.T, s.C, s.H, s.L, B, mode=mode.split("-")[0], fused_head=mode == "bf16-fused",
+            math="fp32" if mode == "fp32-fma" else "3xtf32")
     m.load(params)
     d_ids = torch.as_tensor(ids.reshape(-1)).cuda()
     d_tg = torch.as_tensor(targets.reshape(-1)).cuda()

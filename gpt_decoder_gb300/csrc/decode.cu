@@ -16,27 +16,7 @@
 
 #include "gemm.cuh"
 
-struct gk_kv {
-    gk_gpt_cfg cfg{};
-    int B = 0, Tmax = 0;
-    float* cache = nullptr;  // [L][2][B][H][Tmax][hs]
-    int* state = nullptr;    // device: [0] cache length, [1] selections made
-    int length = 0;          // host mirror of state[0]
-    // activations (prefill uses B*Tmax rows, decode B rows)
-    float *x = nullptr, *ln = nullptr, *qkv = nullptr, *y = nullptr, *pre = nullptr, *h = nullptr;
-    float *mean = nullptr, *rstd = nullptr, *lse = nullptr, *last = nullptr;
-    float* partial = nullptr;  // split-K partial sums
-    size_t partial_floats = 0;
-    float* attn_part = nullptr;  // decode attention partials [B*H][chunks][hs + 2]
-    int* tickets = nullptr;      // last-block tickets: [0, 1024) GEMV column blocks, [1024, 2048) attention
-    int32_t* ids = nullptr;      // gk_generate_uncached: the prefix [B, t] of each step, then next [B]
-    // gk_decode_run: one captured decode step (instantiated graph) and what it was captured for
-    cudaGraphExec_t graph = nullptr;
-    int64_t graph_launches = 0;
-    const void* graph_key[6] = {};
-    gk_sample_cfg graph_s{};
-    bool graph_has_s = false;
-};
+#include "decode.cuh"
 
 using namespace gk;
 
@@ -770,7 +750,9 @@ gk_status gk_kv_create(gk_ctx* ctx, gk_kv** out, const gk_gpt_cfg* cfg, int B, i
     kv->B = B;
     kv->Tmax = Tmax;
     int64_t C = cfg->C, rows = (int64_t)B * Tmax;
-    int nchunks = (int)cdiv(Tmax, KCHUNK);
+    // attention partial slots: chunks of 32 keys (the persistent step's) cover the 64-key chunks
+    // of the per-layer path too
+    int nchunks = (int)cdiv(Tmax, 32);
     kv->partial_floats = (size_t)2 * ctx->num_sms * 16 * 4 * C + (size_t)64 * 16 * 4 * C;
     struct A {
         float** p;
@@ -798,11 +780,14 @@ gk_status gk_kv_create(gk_ctx* ctx, gk_kv** out, const gk_gpt_cfg* cfg, int B, i
         cudaMalloc(&kv->ids, ((size_t)rows + B) * sizeof(int32_t)) != cudaSuccess ||
         cudaMalloc(&kv->tickets, 2048 * sizeof(int)) != cudaSuccess ||
         cudaMemset(kv->tickets, 0, 2048 * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&kv->bar, 64 * sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(kv->bar, 0, 64 * sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(kv->cache, 0, (size_t)cfg->L * 2 * rows * C * sizeof(float)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         gk_kv_destroy(kv);
         return fail(ctx, GK_ERR_CUDA, "gk_kv_create: device setup failed");
     }
+    mega_setup(ctx, kv);
     *out = kv;
     return GK_OK;
 }
@@ -816,6 +801,7 @@ void gk_kv_destroy(gk_kv* kv) {
         if (p) cudaFree(p);
     if (kv->state) cudaFree(kv->state);
     if (kv->tickets) cudaFree(kv->tickets);
+    if (kv->bar) cudaFree(kv->bar);
     if (kv->ids) cudaFree(kv->ids);
     delete kv;
 }
@@ -865,6 +851,32 @@ gk_status gk_prefill(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t*
 
 namespace {
 
+// Selection of the next tokens (if `next`) and the device cache position's advance; `pdl`:
+// launched as programmatic dependents of the kernel before them (the per-layer path).
+gk_status select_and_advance(gk_ctx* ctx, gk_kv* kv, const float* logits, int32_t* next, const gk_sample_cfg* s,
+                             bool pdl) {
+    const int V = kv->cfg.V;
+    int dsel = 0;
+    if (next) {
+        int top_k = s ? s->top_k : 1;
+        float temp = s ? s->temperature : 0.f;
+        const uint64_t seed = s ? s->seed : 0, counter = s ? s->counter : 0;
+        if (pdl)
+            launch_pdl(select_kernel, dim3(kv->B), dim3(SEL_THREADS), 0, ctx->stream, logits, (int64_t)V, V, top_k,
+                       temp, seed, counter, (const int*)kv->state, next);
+        else
+            select_kernel<<<kv->B, SEL_THREADS, 0, ctx->stream>>>(logits, (int64_t)V, V, top_k, temp, seed, counter,
+                                                                  kv->state, next);
+        GK_TRY(launched(ctx, "select"));
+        dsel = 1;
+    }
+    if (pdl)
+        launch_pdl(advance_kernel, dim3(1), dim3(1), 0, ctx->stream, kv->state, 1, dsel);
+    else
+        advance_kernel<<<1, 1, 0, ctx->stream>>>(kv->state, 1, dsel);
+    return launched(ctx, "advance");
+}
+
 // The launches of one decode step (arguments checked by the caller); the host mirror of the
 // cache length is left to the caller.
 gk_status decode_step_launches(gk_ctx* ctx, const float* params, gk_kv* kv, const int32_t* tokens, float* logits,
@@ -873,6 +885,11 @@ gk_status decode_step_launches(gk_ctx* ctx, const float* params, gk_kv* kv, cons
     W w{params, c};
     int B = kv->B, C = c.C, H = c.H, hs = C / H;
     int nchunks = (int)cdiv(kv->Tmax, KCHUNK);
+    if (kv->mega) {
+        // the whole step (embedding, layers, ln_f and head) in one persistent kernel
+        GK_TRY(mega_step(ctx, kv, params, tokens, logits));
+        return select_and_advance(ctx, kv, logits, next, s, false);
+    }
     launch_pdl(embed_step_kernel, dim3(B), dim3(256), 0, ctx->stream, tokens, w.t(GK_T_WTE), w.t(GK_T_WPE), kv->x, B,
                C, c.V, kv->Tmax, (const int*)kv->state, ctx->d_err);
     GK_TRY(launched(ctx, "embed_step"));
@@ -893,18 +910,7 @@ gk_status decode_step_launches(gk_ctx* ctx, const float* params, gk_kv* kv, cons
                     w.t(GK_T_MLPPROJ_B, l), kv->x, kv->x, GK_ACT_NONE, nullptr));
     }
     GK_TRY(lm_head(ctx, kv, kv->x, w.t(GK_T_LNF_W), w.t(GK_T_LNF_B), w.t(GK_T_WTE), logits, c.V));
-    int dsel = 0;
-    if (next) {
-        int top_k = s ? s->top_k : 1;
-        float temp = s ? s->temperature : 0.f;
-        launch_pdl(select_kernel, dim3(B), dim3(SEL_THREADS), 0, ctx->stream, (const float*)logits, (int64_t)c.V, c.V,
-                   top_k, temp, (uint64_t)(s ? s->seed : 0), (uint64_t)(s ? s->counter : 0), (const int*)kv->state,
-                   next);
-        GK_TRY(launched(ctx, "select"));
-        dsel = 1;
-    }
-    launch_pdl(advance_kernel, dim3(1), dim3(1), 0, ctx->stream, kv->state, 1, dsel);
-    return launched(ctx, "advance");
+    return select_and_advance(ctx, kv, logits, next, s, true);
 }
 
 }  // namespace

@@ -59,7 +59,7 @@ def _teacher_forced(gkctx, s, B, Tp, n_steps, seed):
     return err, int(mismatch.sum()), int(near.sum()), got_ids, picks
 
 
-@pytest.mark.parametrize("B", [1, 4])
+@pytest.mark.parametrize("B", [1, 2, 4])
 def test_tiny_decode_teacher_forced(gkctx, B):
     err, mism, near, _, _ = _teacher_forced(gkctx, synth.TINY, B, 20, 40, 3)
     assert err <= 5e-4
@@ -76,7 +76,8 @@ def test_gpt2_decode_teacher_forced(gkctx, B):
 
 
 @pytest.mark.parametrize("sample", [None, (5, 0.8, 11, 3)])
-def test_decode_run_matches_step_by_step(gkctx, sample):
+@pytest.mark.parametrize("B", [2, 3])  # the persistent step, the per-layer launches
+def test_decode_run_matches_step_by_step(gkctx, sample, B):
     """gk_decode_run (one captured step replayed as a graph) gives bit-identical logits,
     selections and cache to gk_decode_step called step by step, across two runs (the second
     replays the same graph), with tokens and next as one buffer or two."""
@@ -84,7 +85,7 @@ def test_decode_run_matches_step_by_step(gkctx, sample):
 
     from gpt_decoder_gb300 import gk
 
-    s, B, Tp, n1, n2 = synth.TINY, 3, 9, 6, 5
+    s, Tp, n1, n2 = synth.TINY, 9, 6, 5
     stream = torch.cuda.Stream()
     ctx = gk.Ctx(stream, 64 << 20)
     outs = []
@@ -301,3 +302,41 @@ def test_uncached_generate_overflow_runs_nothing(gkctx):
     assert np.array_equal(got[:, :Tp], prompt.reshape(B, Tp))
     assert ((got[:, Tp:] >= 0) & (got[:, Tp:] < s.V)).all()
     kv.close()
+
+
+def _launches_per_step(gkctx, s, B, n_steps=4, Tp=6):
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    prompt, params, m, kv = _setup(gkctx, s, B, Tp, 9, Tp + n_steps)
+    logits = torch.empty(B, s.V, device="cuda")
+    tok = torch.as_tensor(prompt[:, -1].copy()).cuda()
+    gk.gk_prefill(gkctx, m.params, kv, torch.as_tensor(prompt.reshape(-1)).cuda(), Tp, logits)
+    l0 = gk.gk_launch_count(gkctx)
+    for _ in range(n_steps):
+        gk.gk_decode_step(gkctx, m.params, kv, tok, logits, tok, None)
+    gk.gk_sync(gkctx)
+    kv.close()
+    return (gk.gk_launch_count(gkctx) - l0) / n_steps
+
+
+def test_decode_step_is_one_persistent_launch_plus_selection(gkctx):
+    """A decode step at batch 1 or 2 runs as one persistent kernel (embedding, every layer, ln_f
+    and the head), then the selection and the position advance: three launches. From batch 4 on
+    the step keeps the per-layer launches (five per layer)."""
+    s = synth.GptShape(V=64, T=32, C=96, H=4, L=4)
+    assert _launches_per_step(gkctx, s, 1) == 3
+    assert _launches_per_step(gkctx, s, 2) == 3
+    assert _launches_per_step(gkctx, s, 4) > 5 * s.L
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_deep_model_decodes_with_per_layer_launches(gkctx, B):
+    """A model deeper than the persistent kernel's parameters hold (25 layers) decodes with the
+    per-layer launches (five per layer), against the oracle teacher-forced."""
+    s = synth.GptShape(V=64, T=32, C=32, H=2, L=25)
+    assert _launches_per_step(gkctx, s, B) > 5 * 25
+    err, mism, near, _, _ = _teacher_forced(gkctx, s, B, 8, 12, 4)
+    assert err <= 5e-4
+    assert mism == near, (mism, near)

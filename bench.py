@@ -122,6 +122,13 @@ def oracle_tokens_per_s(seconds_budget=20.0, T=1024):
     return n * T / el, cores, f"{n} oracle step(s) of 1 x {T} tokens (GPT-2-124M, float64 numpy/BLAS)"
 
 
+def workload_config(B, mode, world):
+    """The `config` of the training-step line (shared by both arms)."""
+    return {"workload": f"gpt2-124m train step (fwd+bwd+AdamW), B={B} x T=1024, "
+                        f"{'bf16 operands / fp32 master' if mode == 'bf16' else 'fp32 faithful'}",
+            "l2": "inputs larger than L2 (step working set >> 129 MB)", "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -130,8 +137,10 @@ def run_reference(args):
     from oracle import gpt as ogpt
 
     s = synth.GPT2_124M
-    T = 128
-    ids, targets, params = synth.training_case(s, 1, 7, T=T)
+    # each step: a bounded sample of the workload, the first 512 positions of one of its
+    # sequences (the oracle takes seconds per sequence on the host cores)
+    T = 512
+    ids, targets, params = synth.training_case(s, 1, 5, T=T)
     sh = ogpt.Shape(s.V, s.T, s.C, s.H, s.L)
 
     def step():
@@ -151,18 +160,54 @@ def run_reference(args):
         cores = max((i.get("num_threads") or 1) for i in threadpool_info())
     except Exception:
         cores = os.cpu_count() or 1
-    sample = f"each step 1 x {T} tokens of the GPT-2-124M step (float64 oracle on the host)"
+    sample = (f"each step: 1 sequence x {T} positions of the GPT-2-124M training step (fwd+bwd+AdamW), "
+              f"float64 oracle on the host; tokens/s = {T} x steps / time")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"gpt2-124m train step sample, B=1 x T={T}", "l2": "inputs larger than L2"},
+        "config": workload_config(args.batch, args.mode, world),
         "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 
 # ----------------------------------------------------------------------------- ours
+def time_events(fn, reps, stream=None, flush=None):
+    """Median CUDA-event time (ms) of fn() on `stream` (the current stream by default); with
+    `flush` (a tensor larger than L2) it is overwritten before every timed call, outside the
+    events."""
+    import torch
+
+    st = stream or torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        fn()
+        e1.record(st)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return sorted(ts)[len(ts) // 2]
+
+
+def gemm_breakdown(m, ids, tg, lr, wd, steps=2):
+    """Per-step GEMM time and algorithmic FLOPs of the training step, from CUDA events around
+    every product launch: a separate, untimed pass (the events sit between launches)."""
+    m.gemm_events = []
+    for _ in range(steps):
+        m.train_step(ids, tg, lr, wd)
+    import torch
+
+    torch.cuda.synchronize()
+    gms = sum(e0.elapsed_time(e1) for (e0, e1, _) in m.gemm_events) / steps
+    flops = sum(f for (_, _, f) in m.gemm_events) / steps
+    m.gemm_events = None
+    return gms, flops
+
+
 def run_ours(args):
     import torch
 
@@ -179,7 +224,7 @@ def run_ours(args):
     s = synth.GPT2_124M
     B, T = args.batch, s.T
     stream = torch.cuda.current_stream()
-    ctx = gk.Ctx(stream.cuda_stream, workspace_bytes=256 << 20)
+    ctx = gk.Ctx(stream.cuda_stream, workspace_bytes=(256 << 20) if args.mode == "bf16" else (2 << 30))
     ids, targets, params = synth.training_case(s, B, 5 + rank)
     m = Gpt(ctx, s.V, s.T, s.C, s.H, s.L, B, mode=args.mode)
     m.load(params)
@@ -198,8 +243,6 @@ def run_ours(args):
         m.train_step(d_ids, d_tg, lr, wd)
     gk.gk_sync(ctx)
     # timed region: K steps, device time by CUDA events on the launching stream
-    gemm_time = {}
-    m.gemm_events = []
     barrier()
     torch.cuda.synchronize()
     n0 = gk.gk_launch_count(ctx)
@@ -222,13 +265,8 @@ def run_ours(args):
         ms = t.item()
     tokens = B * T * world
     value = tokens / (ms / 1e3)
-    # roofline of the dominant kernel class (the GEMMs): algorithmic flops / event time
-    flops, gms = 0.0, 0.0
-    for (e0, e1, f) in m.gemm_events:
-        gms += e0.elapsed_time(e1)
-        flops += f
-    m.gemm_events = None
-    n_gemm_steps = args.steps
+    # roofline of the dominant kernel class (the GEMMs), from a separate instrumented pass
+    gms, flops = gemm_breakdown(m, d_ids, d_tg, lr, wd)
     hbm, bf16_burst, bf16_sus, peak_src = _peaks()
     achieved = flops / (gms / 1e3) / 1e12 if gms > 0 else 0.0
     # end to end: ids/targets from pinned host memory each step, loss read back
@@ -245,62 +283,185 @@ def run_ours(args):
         h_loss.copy_(loss, non_blocking=True)
         torch.cuda.synchronize()
     e2e = tokens / ((time.perf_counter() - t0) / e2e_steps)
-    decode = generic = None
+    loss_last = float(h_loss.item())
+    extra = {}
     if rank == 0 and not args.no_decode:
-        decode = bench_decode(ctx, m, s)
-        generic = bench_generic(ctx)
+        decode_params = m.params
+        extra["decode"] = bench_decode(ctx, m, s)
+        del decode_params
+    if rank == 0 and not args.no_sweep:
+        del m
+        torch.cuda.empty_cache()
+        extra["step_b4"] = bench_step_b4(s)
+        extra["op_sweep"] = bench_op_sweep()
+        extra["generic_ops"] = bench_generic(ctx)
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, sample = oracle_tokens_per_s()
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    tf32 = bf16_sus / 2
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if args.mode == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": f"gpt2-124m train step (fwd+bwd+AdamW), B={B} x T={T}, "
-                               f"{'bf16 operands / fp32 master' if args.mode == 'bf16' else 'fp32 faithful'}",
-                   "l2": "inputs larger than L2 (step working set >> 129 MB)", "parallelism": f"replicas x{world}"},
+        "config": workload_config(B, args.mode, world),
         "roofline": {"bound": "tensor", "achieved": achieved,
-                     "peak": bf16_sus if args.mode == "bf16" else bf16_sus / 2, "unit": "TFLOP/s",
-                     "frac": achieved / (bf16_sus if args.mode == "bf16" else bf16_sus / 2),
+                     "peak": bf16_sus if args.mode == "bf16" else tf32 / 3, "unit": "TFLOP/s",
+                     "frac": achieved / (bf16_sus if args.mode == "bf16" else tf32 / 3),
                      "traffic": gemm_traffic_per_step(B, args.mode),
-                     "traffic_source": "profiles/gemm_tc_traffic_gpt2_b4.md (ncu at B=4, scaled by tokens)",
-                     "kernel": "all GEMM launches of the step", "peak_source": f"{peak_src} bf16 sustained"
-                     + ("" if args.mode == "bf16" else " / 2 (tf32 nominal ratio)"),
-                     "gemm_ms_per_step": gms / n_gemm_steps, "gemm_tflop_per_step": flops / n_gemm_steps / 1e12},
+                     "kernel": "all GEMM launches of the step (timed in a separate pass)",
+                     "peak_source": f"{peak_src} bf16 sustained"
+                     + ("" if args.mode == "bf16" else " / 2 (tf32 nominal ratio) / 3 (3xTF32 products)"),
+                     "gemm_ms_per_step": gms, "gemm_tflop_per_step": flops / 1e12},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": int(2 * B * T * 4), "d2h_bytes_per_step": 4},
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
-        "loss_last": float(loss.item()),
+        "loss_last": loss_last,
     }
-    if decode:
-        out["decode"] = decode
-    if generic:
-        out["generic_ops"] = generic
+    out.update(extra)
     print(json.dumps(out))
 
 
+def bench_step_b4(s, steps=5, warmup=2):
+    """The GPT-2-124M step at batch 4 x 1024 in both modes: fp32 faithful (float32 products as
+    3xTF32 on the tensor cores; attention, LayerNorm, softmax-CE and AdamW in float32) and bf16.
+    For the faithful step the GEMM roofline is stated both ways: algorithmic FLOPs against the
+    TF32 peak / 3, and the tensor cores' rate (three TF32 products per FLOP) against the TF32 peak."""
+    import torch
+
+    import synth
+    from gpt_decoder_gb300 import gk
+    from gpt_decoder_gb300.model import Gpt
+
+    hbm, _, bf16_sus, peak_src = _peaks()
+    tf32 = bf16_sus / 2
+    ids, targets, params = synth.training_case(s, 4, 2)
+    d_ids = torch.as_tensor(ids.reshape(-1)).cuda()
+    d_tg = torch.as_tensor(targets.reshape(-1)).cuda()
+    res = {}
+    for mode in ("fp32", "bf16"):
+        ctx = gk.Ctx(torch.cuda.current_stream().cuda_stream, workspace_bytes=2 << 30)
+        m = Gpt(ctx, s.V, s.T, s.C, s.H, s.L, 4, mode=mode)
+        m.load(params)
+        for _ in range(warmup):
+            m.train_step(d_ids, d_tg, 3e-4, 0.01)
+        ms = time_events(lambda: [m.train_step(d_ids, d_tg, 3e-4, 0.01) for _ in range(steps)], 1) / steps
+        gms, flops = gemm_breakdown(m, d_ids, d_tg, 3e-4, 0.01, steps=1)
+        gk.gk_sync(ctx)
+        ach = flops / (gms / 1e3) / 1e12
+        r = {"ms_per_step": ms, "tokens_s": 4 * 1024 / (ms / 1e3), "gemm_ms_per_step": gms,
+             "gemm_tflop_per_step": flops / 1e12, "gemm_tflops": ach}
+        if mode == "fp32":
+            r.update({"math": "3xTF32", "gemm_frac_algorithmic": ach / (tf32 / 3),
+                      "gemm_frac_hardware": 3 * ach / tf32, "tf32_peak_tflops": tf32,
+                      "peak_source": f"{peak_src} bf16 sustained / 2 (tf32 nominal ratio)"})
+        else:
+            r.update({"gemm_frac": ach / bf16_sus, "peak_source": f"{peak_src} bf16 sustained"})
+        res[mode] = r
+        del m
+        ctx.close()
+        torch.cuda.empty_cache()
+    return res
+
+
+def bench_op_sweep(reps=5):
+    """The float32 op sweep on seeded N(0, 1) inputs: MatMul / MatMulT forward and backward at
+    M = N = K in {256, 1024, 4096} and (M, K, N) = (4096, 768, 3072), as 3xTF32 (TFLOP/s; the
+    fraction against TF32 peak / 3) and as float32 FMA on the CUDA cores; LayerNorm, GELU and
+    softmax-CE forward and backward on [4096, C], C in {768, 50257} (GB/s of the algorithmic
+    bytes against the measured copy bandwidth). L2 is overwritten before every timed call."""
+    import torch
+
+    import synth
+    from gpt_decoder_gb300 import gk
+
+    hbm, _, bf16_sus, _ = _peaks()
+    tf32 = bf16_sus / 2
+    fma_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 FLOP x max clock
+    flush = torch.empty(64 << 20, device="cuda")  # 256 MB, twice L2
+    ctx = gk.Ctx(torch.cuda.current_stream().cuda_stream, workspace_bytes=2 << 30)
+    st = synth.Stream(1)
+    dn = lambda *shape: torch.as_tensor(st.normal(int(np.prod(shape))).reshape(shape)).cuda()
+    res = {"gemm": {}, "rowwise": {}}
+    for (M, K, N) in [(256, 256, 256), (1024, 1024, 1024), (4096, 4096, 4096), (4096, 768, 3072)]:
+        x, g = dn(M, K), dn(M, N)
+        for transW in (0, 1):
+            w = dn(N, K) if transW else dn(K, N)
+            ldw = w.shape[1]
+            y, dx, dw = torch.empty(M, N, device="cuda"), torch.empty(M, K, device="cuda"), torch.zeros_like(w)
+            key = f"{'matmul_t' if transW else 'matmul'}_{M}x{K}x{N}"
+            r = {}
+            for math, name in ((gk.GK_MATH_3XTF32, "3xtf32"), (gk.GK_MATH_FP32, "fma")):
+                gk.gk_set_math(ctx, math)
+                fwd = lambda: gk.gk_matmul_fwd(ctx, gk.GK_F32, x, K, w, ldw, transW, None, None, 0, y, N, gk.GK_F32,
+                                               M, K, N)
+                bwd = lambda: gk.gk_matmul_bwd(ctx, gk.GK_F32, x, K, w, ldw, transW, g, N, dx, K, gk.GK_F32, 0, None,
+                                               0, dw, ldw, None, M, K, N)
+                fwd(), bwd()
+                tf = time_events(fwd, reps, flush=flush)
+                tb = time_events(bwd, reps, flush=flush)
+                ff, fb = 2.0 * M * N * K / (tf / 1e3) / 1e12, 4.0 * M * N * K / (tb / 1e3) / 1e12
+                peak = tf32 / 3 if name == "3xtf32" else fma_peak
+                r[name] = {"fwd_tflops": ff, "bwd_tflops": fb, "fwd_frac": ff / peak, "bwd_frac": fb / peak,
+                           "fwd_us": tf * 1e3, "bwd_us": tb * 1e3}
+            gk.gk_set_math(ctx, gk.GK_MATH_FP32)
+            res["gemm"][key] = r
+            del w, y, dx, dw
+        del x, g
+    res["gemm_peaks_tflops"] = {"3xtf32": tf32 / 3, "fma": fma_peak,
+                                "note": "3xtf32: measured bf16 sustained / 2 / 3; fma: 152 SMs x 128 lanes x 2 x 2.07 GHz"}
+    for C in (768, 50257):
+        R = 4096
+        x, gm, bt, g = dn(R, C), dn(C), dn(C), dn(R, C)
+        y, dx = torch.empty(R, C, device="cuda"), torch.empty(R, C, device="cuda")
+        mu, rs = torch.empty(R, device="cuda"), torch.empty(R, device="cuda")
+        dgm, dbt = torch.zeros(C, device="cuda"), torch.zeros(C, device="cuda")
+        tg = torch.as_tensor(st.ints(R, C)).cuda()
+        loss, lse = torch.zeros(1, device="cuda"), torch.empty(R, device="cuda")
+        n = R * C
+        cases = {
+            "layernorm_fwd": (lambda: gk.gk_layernorm_fwd(ctx, x, gm, bt, y, gk.GK_F32, mu, rs, R, C, 1e-5), 8 * n + 8 * R),
+            "layernorm_bwd": (lambda: gk.gk_layernorm_bwd(ctx, x, gm, mu, rs, g, dx, 0, None, dgm, dbt, R, C),
+                              12 * n + 8 * R),
+            "gelu_fwd": (lambda: gk.gk_gelu_fwd(ctx, x, y, n), 8 * n),
+            "gelu_bwd": (lambda: gk.gk_gelu_bwd(ctx, x, g, dx, n), 12 * n),
+            "softmax_ce_fwd": (lambda: gk.gk_softmax_ce_fwd(ctx, x, C, tg, loss, lse, R, C), 4 * n + 8 * R),
+            "softmax_ce_bwd": (lambda: gk.gk_softmax_ce_bwd(ctx, x, C, tg, lse, None, dx, C, gk.GK_F32, R, C),
+                               8 * n + 8 * R),
+        }
+        for name, (fn, nbytes) in cases.items():
+            fn()
+            t = time_events(fn, reps, flush=flush)
+            res["rowwise"][f"{name}_{R}x{C}"] = {"gbs": nbytes / (t / 1e3) / 1e9, "frac": nbytes / (t / 1e3) / 1e9 / hbm,
+                                                  "us": t * 1e3}
+        del x, g, y, dx
+    res["rowwise_peak_gbs"] = hbm
+    gk.gk_sync(ctx)
+    ctx.close()
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def gemm_traffic_per_step(B, mode):
-    """DRAM bytes of a step's GEMM launches from the committed ncu summary, while the kernel's
-    source is the one that was measured (sha256 recorded beside the figure); else None."""
+    """DRAM bytes of one step's GEMM launches at batch B (bf16 mode) from the data file of the
+    committed ncu capture, while every source file the capture measured is unchanged (sha256
+    recorded beside the figure); else None."""
     import hashlib
 
-    here = os.path.dirname(os.path.abspath(__file__))
-    path = os.path.join(here, "profiles", "gemm_tc_traffic_gpt2_b4.md")
-    if B != 16 or mode != "bf16" or not os.path.exists(path):
+    path = os.path.join(ROOT, "profiles", "gemm_tc_traffic_gpt2.json")
+    if mode != "bf16" or not os.path.exists(path):
         return None
-    value, ok = None, True
-    for line in open(path):
-        if line.startswith("traffic_bytes_per_step_b16:"):
-            value = int(line.split(":")[1])
-        elif line.startswith("source_sha256 "):
-            rel, digest = line[len("source_sha256 "):].rsplit(":", 1)
-            src = os.path.join(here, rel.strip())
-            ok = ok and os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == digest.strip()
-    return value if ok else None
+    with open(path) as f:
+        d = json.load(f)
+    for rel, digest in d.get("source_sha256", {}).items():
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != digest:
+            return None
+    return d.get("bytes_per_step", {}).get(f"B{B}")
 
 
 def bench_generic(ctx, n=1 << 26, reps=10):
@@ -348,27 +509,38 @@ def bench_decode(ctx, m, s, Tp=512, n_steps=256):
     dctx = gk.Ctx(stream, workspace_bytes=64 << 20)
     torch.cuda.synchronize()
     warm = 8
-    for B in (1, 16):
+    hbm = _peaks()[0]
+    # bytes a step must move: every float32 weight once (wpe: one row) and each sequence's cache
+    # (keys and values of every layer up to the current length)
+    w_bytes = 4 * (gk.gk_gpt_numel(m.cfg) - (s.T - 1) * s.C)
+    runs = [(1, None, "B1"), (16, None, "B16"), (1, (40, 1.0, 4, 0), "B1_topk40"), (16, (40, 1.0, 4, 0), "B16_topk40")]
+    for B, samp, key in runs:
         with torch.cuda.stream(stream):
             kv = gk.KvCache(dctx, m.cfg, B, Tp + warm + n_steps)
             prompt = torch.randint(0, s.V, (B * Tp,), dtype=torch.int32, device="cuda")
             logits = torch.empty(B, s.V, device="cuda")
             tok = torch.empty(B, dtype=torch.int32, device="cuda")
             gk.gk_prefill(dctx, m.params, kv, prompt, Tp, logits)
-            gk.gk_sample(dctx, kv, logits, s.V, tok, None)
-            gk.gk_decode_run(dctx, m.params, kv, tok, logits, tok, warm)  # records the step graph
+            gk.gk_sample(dctx, kv, logits, s.V, tok, samp)
+            gk.gk_decode_run(dctx, m.params, kv, tok, logits, tok, warm, samp)  # records the step graph
             l0 = gk.gk_launch_count(dctx)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             stream.synchronize()
             e0.record(stream)
-            gk.gk_decode_run(dctx, m.params, kv, tok, logits, tok, n_steps)
+            gk.gk_decode_run(dctx, m.params, kv, tok, logits, tok, n_steps, samp)
             e1.record(stream)
         stream.synchronize()
         gk.gk_sync(dctx)
         ms = e0.elapsed_time(e1)
-        res[f"B{B}"] = {"tok_s": B * n_steps / (ms / 1e3), "ms_per_step": ms / n_steps, "prompt": Tp,
-                        "steps": n_steps, "dtype": "f32", "launches_per_step": (gk.gk_launch_count(dctx) - l0) / n_steps,
-                        "launch": "CUDA graph per step"}
+        t_avg = Tp + warm + (n_steps + 1) / 2  # mean cache length the timed steps attend over
+        step_bytes = w_bytes + B * 2 * s.L * s.C * 4 * t_avg
+        gbs = step_bytes / (ms / n_steps / 1e3) / 1e9
+        res[key] = {"tok_s": B * n_steps / (ms / 1e3), "ms_per_step": ms / n_steps, "prompt": Tp,
+                    "steps": n_steps, "dtype": "f32", "launches_per_step": (gk.gk_launch_count(dctx) - l0) / n_steps,
+                    "launch": "CUDA graph per step",
+                    "selection": "greedy" if samp is None else "top-k 40, temperature 1.0, Philox seed 4",
+                    "roofline": {"bound": "hbm", "bytes_per_step": step_bytes, "achieved_gbs": gbs, "peak_gbs": hbm,
+                                 "frac": gbs / hbm}}
         kv.close()
     # uncached generation ([LM4] Generate: the whole sequence re-run per token) at batch 1 from
     # the same prompt length, the baseline the cached loop is compared with
@@ -429,6 +601,7 @@ def main():
     ap.add_argument("--mode", default="bf16", choices=["bf16", "fp32"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -133,33 +133,45 @@ __global__ void scale_kernel(const float* a, float s, float* y, int64_t n, int a
     }, [&](int64_t i) { y[i] = acc ? y[i] + s * a[i] : s * a[i]; });
 }
 
+// Compensated (Kahan) float32 addition: s + c carries the running sum to about one ulp of the
+// sum, whatever the number of terms (Kahan 1965).
+__device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
+    const float y = v - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+}
+
 // part[block] = sum of this block's grid-stride elements, in a fixed order: each aligned float4
-// group is added in float ((x + y) + (z + w)); a thread's k-th group goes to its double
-// accumulator k % 4 (four independent chains), the tail to the first; then the accumulators in
-// order, and the block's threads in tree order
+// group is added in float ((x + y) + (z + w)); a thread's k-th group goes to its compensated
+// float32 chain k % 4 (four independent chains, so four loads are in flight), the tail to the
+// first; the chains are combined in double, then the block's threads in tree order. Double
+// arithmetic (a slow pipe on this GPU) is used only for those few combining steps.
 __global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, double* __restrict__ part, bool vec) {
     __shared__ double red[EW_THREADS / 32];
-    double acc4[4] = {0.0, 0.0, 0.0, 0.0};
+    float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t n4 = vec ? n / 4 : 0;
     int64_t j = tid;
     for (; j + 3 * stride < n4; j += 4 * stride) {
+        float4 v[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 v = f4(a, j + k * stride);
-            acc4[k] += (double)((v.x + v.y) + (v.z + v.w));
-        }
+        for (int k = 0; k < 4; ++k) v[k] = f4(a, j + k * stride);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) kahan_add(s4[k], c4[k], (v[k].x + v[k].y) + (v[k].z + v[k].w));
     }
 #pragma unroll
     for (int k = 0; k < 3; ++k) {  // fewer than four groups left
         if (j < n4) {
             const float4 v = f4(a, j);
-            acc4[k] += (double)((v.x + v.y) + (v.z + v.w));
+            kahan_add(s4[k], c4[k], (v.x + v.y) + (v.z + v.w));
             j += stride;
         }
     }
-    for (int64_t i = 4 * n4 + tid; i < n; i += stride) acc4[0] += (double)a[i];
-    double s = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+    for (int64_t i = 4 * n4 + tid; i < n; i += stride) kahan_add(s4[0], c4[0], a[i]);
+    double s = 0.0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s += (double)s4[k] - (double)c4[k];
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) red[warp] = s;
@@ -315,7 +327,8 @@ gk_status gk_scale_bwd(gk_ctx* ctx, const float* g, float s, float* da, int64_t 
 gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, n >= 0 && y && (n == 0 || a), GK_ERR_ARG, "gk_sum_fwd: bad argument");
-    const int P = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS * 8), 1024));
+    // about four blocks per SM, each thread at least 32 elements
+    const int P = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS * 32), 4 * (int64_t)ctx->num_sms));
     double* part = static_cast<double*>(workspace(ctx, (size_t)P * sizeof(double)));
     GK_REQUIRE(ctx, part, GK_ERR_WORKSPACE, "gk_sum_fwd: needs %zu workspace bytes", (size_t)P * sizeof(double));
     sum_partial_kernel<<<P, EW_THREADS, 0, ctx->stream>>>(a, n, part, vec4(a));

@@ -144,24 +144,27 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
 
 // part[block] = sum of this block's grid-stride elements, in a fixed order: each aligned float4
 // group is added in float ((x + y) + (z + w)); a thread's k-th group goes to its compensated
-// float32 chain k % 4 (four independent chains, so four loads are in flight), the tail to the
-// first; the chains are combined in double, then the block's threads in tree order. Double
-// arithmetic (a slow pipe on this GPU) is used only for those few combining steps.
+// float32 chain k % SC (SC independent chains, so SC loads are in flight per round trip), the
+// tail to the first; the chains are combined in double, then the block's threads in tree
+// order. Double arithmetic (a slow pipe on this GPU) is used only for those few combining steps.
+constexpr int SC = 4;
 __global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, double* __restrict__ part, bool vec) {
     __shared__ double red[EW_THREADS / 32];
-    float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
+    float s4[SC], c4[SC];
+#pragma unroll
+    for (int k = 0; k < SC; ++k) s4[k] = c4[k] = 0.f;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t n4 = vec ? n / 4 : 0;
     int64_t j = tid;
-    for (; j + 3 * stride < n4; j += 4 * stride) {
-        float4 v[4];
+    for (; j + (SC - 1) * stride < n4; j += SC * stride) {
+        float4 v[SC];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = f4(a, j + k * stride);
+        for (int k = 0; k < SC; ++k) v[k] = f4(a, j + k * stride);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) kahan_add(s4[k], c4[k], (v[k].x + v[k].y) + (v[k].z + v[k].w));
+        for (int k = 0; k < SC; ++k) kahan_add(s4[k], c4[k], (v[k].x + v[k].y) + (v[k].z + v[k].w));
     }
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {  // fewer than four groups left
+    for (int k = 0; k < SC - 1; ++k) {  // fewer than SC groups left
         if (j < n4) {
             const float4 v = f4(a, j);
             kahan_add(s4[k], c4[k], (v.x + v.y) + (v.z + v.w));
@@ -171,7 +174,7 @@ __global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, doubl
     for (int64_t i = 4 * n4 + tid; i < n; i += stride) kahan_add(s4[0], c4[0], a[i]);
     double s = 0.0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) s += (double)s4[k] - (double)c4[k];
+    for (int k = 0; k < SC; ++k) s += (double)s4[k] - (double)c4[k];
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) red[warp] = s;
@@ -327,7 +330,8 @@ gk_status gk_scale_bwd(gk_ctx* ctx, const float* g, float s, float* da, int64_t 
 gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, n >= 0 && y && (n == 0 || a), GK_ERR_ARG, "gk_sum_fwd: bad argument");
-    // about four blocks per SM, each thread at least 32 elements
+    // about four blocks per SM, each thread at least 32 elements (measured: 82 us for 2^26
+    // floats, against 135 us with eight blocks per SM and eight chains)
     const int P = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS * 32), 4 * (int64_t)ctx->num_sms));
     double* part = static_cast<double*>(workspace(ctx, (size_t)P * sizeof(double)));
     GK_REQUIRE(ctx, part, GK_ERR_WORKSPACE, "gk_sum_fwd: needs %zu workspace bytes", (size_t)P * sizeof(double));

@@ -168,40 +168,150 @@ __device__ float block_sum(float v, float* red) {
     return warp_sum(t);
 }
 
-// General LayerNorm forward: one block per row; the row is staged in dynamic shared memory
-// (up to 56K floats), so x is read from HBM once.
+// Block-wide sums of two floats (blocks of 256 threads).
+__device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    a = warp_sum(a);
+    b = warp_sum(b);
+    __syncthreads();
+    if (lane == 0) red[warp] = make_float2(a, b);
+    __syncthreads();
+    float2 t = lane < nw ? red[lane] : make_float2(0.f, 0.f);
+    return make_float2(warp_sum(t.x), warp_sum(t.y));
+}
+
+// General LayerNorm forward (any C): one 256-thread block per row, several rows in flight per
+// SM. Pass 1 sums x - s and (x - s)^2 with s the row's first element (so the variance does not
+// cancel when the mean is large against the spread); pass 2 re-reads the row, which is still
+// in L2, and writes y (and the copy of x): DRAM sees about one read and one write per element.
 template <typename TY>
-__global__ void layernorm_fwd_block_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
-                                           const float* __restrict__ beta, TY* __restrict__ y, float* mean_out,
-                                           float* rstd_out, int64_t rows, int C, float eps, int64_t lo_plane,
-                                           float* __restrict__ x_copy) {
-    extern __shared__ float srow[];
-    __shared__ float red[32];
-    int64_t row = blockIdx.x;
-    const float* xr = x + row * C;
-    float s = 0.f;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        float a = xr[c];
-        srow[c] = a;
-        if (x_copy) x_copy[row * C + c] = a;
-        s += a;
+__global__ void __launch_bounds__(256) layernorm_fwd_rows_kernel(const float* __restrict__ x,
+                                                                 const float* __restrict__ gamma,
+                                                                 const float* __restrict__ beta, TY* __restrict__ y,
+                                                                 float* mean_out, float* rstd_out, int64_t rows, int C,
+                                                                 float eps, int64_t lo_plane, float* __restrict__ x_copy,
+                                                                 int vec) {
+    __shared__ float2 red[8];
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * C;
+        const float sh = xr[0];
+        float s = 0.f, q = 0.f;
+        if (vec) {
+#pragma unroll 4
+            for (int c = threadIdx.x * 4; c < C; c += 1024) {
+                const float4 v = *reinterpret_cast<const float4*>(xr + c);
+                const float a = v.x - sh, b = v.y - sh, d = v.z - sh, e = v.w - sh;
+                s += (a + b) + (d + e);
+                q += (a * a + b * b) + (d * d + e * e);
+            }
+        } else {
+            for (int c = threadIdx.x; c < C; c += 256) {
+                const float a = xr[c] - sh;
+                s += a;
+                q = fmaf(a, a, q);
+            }
+        }
+        const float2 t = block_sum2(s, q, red);
+        const float md = t.x / C;
+        const float mu = sh + md, rs = rsqrtf(fmaxf(t.y / C - md * md, 0.f) + eps);
+        if (threadIdx.x == 0) {
+            if (mean_out) mean_out[row] = mu;
+            if (rstd_out) rstd_out[row] = rs;
+        }
+        TY* yr = y + row * C;
+        for (int c = threadIdx.x; c < C; c += 256) {
+            const float a = xr[c];
+            if (x_copy) x_copy[row * C + c] = a;
+            const float o = (a - mu) * rs * gamma[c] + beta[c];
+            store_from_f32(yr + c, o);
+            if (lo_plane) store_from_f32(yr + c + lo_plane, o - to_f32(yr[c]));
+        }
     }
-    float mu = block_sum(s, red) / C;
-    float q = 0.f;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        float a = srow[c] - mu;
-        q += a * a;
+}
+
+// A row of n floats at p, cut at 16-byte boundaries: `head` leading floats before the first
+// boundary, `nb` aligned float4 pieces, `tail` trailing floats (rows of any width and offset,
+// the buffers' bases 16-byte aligned). Thread t < head + tail holds edge element edge_index(t).
+struct RowCut {
+    int head, nb, tail;
+    __device__ RowCut(const float* p, int n) {
+        head = (int)(((16u - ((uint32_t)(uintptr_t)p & 15u)) & 15u) >> 2);
+        if (head > n) head = n;
+        nb = (n - head) / 4;
+        tail = n - head - 4 * nb;
     }
-    float rs = rsqrtf(block_sum(q, red) / C + eps);
-    if (threadIdx.x == 0) {
-        if (mean_out) mean_out[row] = mu;
-        if (rstd_out) rstd_out[row] = rs;
-    }
-    TY* yr = y + row * C;
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        float o = (srow[c] - mu) * rs * gamma[c] + beta[c];
-        store_from_f32(yr + c, o);
-        if (lo_plane) store_from_f32(yr + c + lo_plane, o - to_f32(yr[c]));
+    __device__ int edge_index(int t) const { return t < head ? t : t < head + tail ? head + 4 * nb + (t - head) : -1; }
+};
+
+// Wide rows (C <= LNR_MAXC) held in registers: one 512-thread block per row, every piece of
+// the row requested at once (about 200 KB in flight per SM at C = 50257), the mean and then
+// the variance of the deviations from registers, and y written from them: DRAM sees one read
+// and one write per element. x, y and x_copy must have 16-byte aligned bases.
+constexpr int LNR_THREADS = 512, LNR_V4 = 25, LNR_MAXC = LNR_THREADS * 4 * LNR_V4;
+template <typename TY>
+__global__ void __launch_bounds__(LNR_THREADS, 1) layernorm_fwd_reg_kernel(const float* __restrict__ x,
+                                                                           const float* __restrict__ gamma,
+                                                                           const float* __restrict__ beta,
+                                                                           TY* __restrict__ y, float* mean_out,
+                                                                           float* rstd_out, int64_t rows, int C,
+                                                                           float eps, int64_t lo_plane,
+                                                                           float* __restrict__ x_copy) {
+    __shared__ float2 red[LNR_THREADS / 32];
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * C;
+        const RowCut cut(xr, C);
+        const float4* xb = reinterpret_cast<const float4*>(xr + cut.head);
+        float4 v[LNR_V4];
+#pragma unroll
+        for (int i = 0; i < LNR_V4; ++i) {
+            const int q = threadIdx.x + i * LNR_THREADS;
+            v[i] = q < cut.nb ? xb[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const int ei = cut.edge_index(threadIdx.x);
+        const float ev = ei >= 0 ? xr[ei] : 0.f;
+        float s = ev;
+#pragma unroll
+        for (int i = 0; i < LNR_V4; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+        const float mu = block_sum2(s, 0.f, red).x / C;
+        float q2 = ei >= 0 ? (ev - mu) * (ev - mu) : 0.f;
+#pragma unroll
+        for (int i = 0; i < LNR_V4; ++i) {
+            if (threadIdx.x + i * LNR_THREADS < cut.nb) {
+                const float a = v[i].x - mu, b = v[i].y - mu, d = v[i].z - mu, e = v[i].w - mu;
+                q2 += (a * a + b * b) + (d * d + e * e);
+            }
+        }
+        const float rs = rsqrtf(block_sum2(q2, 0.f, red).x / C + eps);
+        if (threadIdx.x == 0) {
+            if (mean_out) mean_out[row] = mu;
+            if (rstd_out) rstd_out[row] = rs;
+        }
+        TY* yr = y + row * C;
+        if (ei >= 0) {
+            if (x_copy) x_copy[row * C + ei] = ev;
+            const float o = (ev - mu) * rs * gamma[ei] + beta[ei];
+            store_from_f32(yr + ei, o);
+            if (lo_plane) store_from_f32(yr + ei + lo_plane, o - to_f32(yr[ei]));
+        }
+#pragma unroll
+        for (int i = 0; i < LNR_V4; ++i) {
+            const int q = threadIdx.x + i * LNR_THREADS;
+            if (q >= cut.nb) break;
+            const int c = cut.head + 4 * q;
+            if (x_copy) *reinterpret_cast<float4*>(x_copy + row * C + c) = v[i];
+            const float o[4] = {(v[i].x - mu) * rs * gamma[c] + beta[c], (v[i].y - mu) * rs * gamma[c + 1] + beta[c + 1],
+                                (v[i].z - mu) * rs * gamma[c + 2] + beta[c + 2],
+                                (v[i].w - mu) * rs * gamma[c + 3] + beta[c + 3]};
+            if constexpr (sizeof(TY) == 4) {
+                *reinterpret_cast<float4*>(yr + c) = make_float4(o[0], o[1], o[2], o[3]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    store_from_f32(yr + c + k, o[k]);
+                    if (lo_plane) store_from_f32(yr + c + k + lo_plane, o[k] - to_f32(yr[c + k]));
+                }
+            }
+        }
     }
 }
 
@@ -331,6 +441,84 @@ __global__ void layernorm_bwd_block_kernel(const float* __restrict__ x, const fl
     }
 }
 
+// Wide-row LayerNorm backward, pass 1: per row, m1 = mean(dy * gamma) and m2 =
+// mean(dy * gamma * xhat) into stats[2 row], stats[2 row + 1]; one 256-thread block per row.
+__global__ void __launch_bounds__(256) layernorm_bwd_stats_kernel(const float* __restrict__ x,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ mean,
+                                                                  const float* __restrict__ rstd,
+                                                                  const float* __restrict__ dy, float* __restrict__ stats,
+                                                                  int64_t rows, int C, int vec) {
+    __shared__ float2 red[8];
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = x + row * C;
+        const float* gr = dy + row * C;
+        const float mu = mean[row], rs = rstd[row];
+        float s1 = 0.f, s2 = 0.f;
+        if (vec) {
+            for (int c = threadIdx.x * 4; c < C; c += 1024) {
+                const float4 xv = *reinterpret_cast<const float4*>(xr + c);
+                const float4 gv = *reinterpret_cast<const float4*>(gr + c);
+                const float4 w = *reinterpret_cast<const float4*>(gamma + c);
+                const float h0 = gv.x * w.x, h1 = gv.y * w.y, h2 = gv.z * w.z, h3 = gv.w * w.w;
+                s1 += (h0 + h1) + (h2 + h3);
+                s2 += (h0 * ((xv.x - mu) * rs) + h1 * ((xv.y - mu) * rs)) +
+                      (h2 * ((xv.z - mu) * rs) + h3 * ((xv.w - mu) * rs));
+            }
+        } else {
+            for (int c = threadIdx.x; c < C; c += 256) {
+                const float h = gr[c] * gamma[c];
+                s1 += h;
+                s2 += h * ((xr[c] - mu) * rs);
+            }
+        }
+        const float2 t = block_sum2(s1, s2, red);
+        if (threadIdx.x == 0) {
+            stats[2 * row] = t.x / C;
+            stats[2 * row + 1] = t.y / C;
+        }
+    }
+}
+
+// Wide-row LayerNorm backward, pass 2: a block takes 256 columns (one per thread) of LNB_ROWS
+// consecutive rows, writes dx (and its bf16 copy), and leaves the column partials of dy * xhat,
+// dy (and, np == 3, dx) over its rows in partial[row block][np][C] (rows in ascending order:
+// a fixed summation order).
+constexpr int LNB_ROWS = 32;
+__global__ void __launch_bounds__(256) layernorm_bwd_cols_kernel(const float* __restrict__ x,
+                                                                 const float* __restrict__ gamma,
+                                                                 const float* __restrict__ mean,
+                                                                 const float* __restrict__ rstd,
+                                                                 const float* __restrict__ dy,
+                                                                 const float* __restrict__ stats, float* __restrict__ dx,
+                                                                 int accumulate, __nv_bfloat16* __restrict__ dx_bf16,
+                                                                 float* __restrict__ partial, int np, int64_t rows,
+                                                                 int C) {
+    const int64_t c = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.y * LNB_ROWS, r1 = std::min<int64_t>(rows, r0 + LNB_ROWS);
+    if (c >= C) return;
+    const float w = gamma[c];
+    float pg = 0.f, pb = 0.f, pd = 0.f;
+    for (int64_t r = r0; r < r1; ++r) {
+        const int64_t i = r * C + c;
+        const float mu = mean[r], rs = rstd[r], m1 = stats[2 * r], m2 = stats[2 * r + 1];
+        const float xh = (x[i] - mu) * rs, g = dy[i];
+        float o = rs * (g * w - m1 - xh * m2);
+        if (accumulate) o += dx[i];
+        dx[i] = o;
+        if (dx_bf16) dx_bf16[i] = __float2bfloat16_rn(o);
+        pg += g * xh;
+        pb += g;
+        pd += o;
+    }
+    if (partial) {
+        float* pp = partial + (int64_t)blockIdx.y * np * C;
+        pp[c] = pg;
+        pp[C + c] = pb;
+        if (np == 3) pp[2 * C + c] = pd;
+    }
+}
+
 // out_k[c] += sum_p partial[p][k][c] for k < np (out_0 = dgamma, out_1 = dbeta, out_2 = the
 // column sums of dx; a null output is skipped). Block (x, k) takes 32 columns of array k:
 // warp w sums slots w, w + 8, ... with four independent running sums (slot order fixed),
@@ -446,6 +634,103 @@ __global__ void __launch_bounds__(CE_THREADS) softmax_ce_fwd_kernel(const float*
     }
 }
 
+// The same per row for narrow rows (V <= 4096, float4-aligned): one warp per row, eight rows
+// per block, each lane an online (max, sum) over its float4 pieces, merged across the warp.
+__global__ void __launch_bounds__(256) softmax_ce_fwd_warp_kernel(const float* __restrict__ logits, int64_t ldl,
+                                                                  const int32_t* __restrict__ targets,
+                                                                  float* __restrict__ lse_out,
+                                                                  float* __restrict__ row_loss, int64_t rows, int V,
+                                                                  int* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const float* xr = logits + row * ldl;
+    MaxSum acc = {-INFINITY, 0.f};
+    const int V4 = V / 4;
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // every piece of the row requested before the first use
+        const int q = lane + 32 * i;
+        v[i] = q < V4 ? reinterpret_cast<const float4*>(xr)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (lane + 32 * i < V4) acc = ms_add4(acc, v[i]);
+    for (int c = V4 * 4 + lane; c < V; c += 32) acc = ms_add1(acc, xr[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        MaxSum b = {__shfl_xor_sync(0xffffffffu, acc.m, o), __shfl_xor_sync(0xffffffffu, acc.s, o)};
+        acc = ms_merge(acc, b);
+    }
+    if (lane == 0) {
+        const float lse = acc.m + logf(acc.s);
+        lse_out[row] = lse;
+        int tg = targets[row];
+        if (tg < 0 || tg >= V) {
+            report(err, GK_ERR_INDEX);
+            tg = 0;
+        }
+        row_loss[row] = lse - xr[tg];
+    }
+}
+
+// Wide rows (V <= 512 * 4 * 25; any width and offset, 16-byte aligned base) held in
+// registers: one 512-thread block per row with every piece of the row requested at once; the
+// maximum, then the sum of exp(x - max), both from registers (one read of each logit).
+constexpr int CER_THREADS = 512, CER_V4 = 25;
+__global__ void __launch_bounds__(CER_THREADS, 1) softmax_ce_fwd_reg_kernel(const float* __restrict__ logits,
+                                                                            int64_t ldl,
+                                                                            const int32_t* __restrict__ targets,
+                                                                            float* __restrict__ lse_out,
+                                                                            float* __restrict__ row_loss, int64_t rows,
+                                                                            int V, int* err) {
+    __shared__ float red[CER_THREADS / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float* xr = logits + row * ldl;
+        const RowCut cut(xr, V);
+        const float4* xb = reinterpret_cast<const float4*>(xr + cut.head);
+        float4 v[CER_V4];
+#pragma unroll
+        for (int i = 0; i < CER_V4; ++i) {
+            const int q = threadIdx.x + i * CER_THREADS;
+            v[i] = q < cut.nb ? xb[q] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        const int ei = cut.edge_index(threadIdx.x);
+        const float ev = ei >= 0 ? xr[ei] : -INFINITY;
+        float m = ev;
+#pragma unroll
+        for (int i = 0; i < CER_V4; ++i) m = fmaxf(m, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
+        m = warp_max(m);
+        __syncthreads();
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        m = red[0];
+        for (int w = 1; w < CER_THREADS / 32; ++w) m = fmaxf(m, red[w]);
+        float sum = ei >= 0 ? expf(ev - m) : 0.f;
+#pragma unroll
+        for (int i = 0; i < CER_V4; ++i)
+            if (threadIdx.x + i * CER_THREADS < cut.nb)
+                sum += (expf(v[i].x - m) + expf(v[i].y - m)) + (expf(v[i].z - m) + expf(v[i].w - m));
+        sum = warp_sum(sum);
+        __syncthreads();
+        if (lane == 0) red[warp] = sum;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float t = 0.f;
+            for (int w = 0; w < CER_THREADS / 32; ++w) t += red[w];
+            const float lse = m + logf(t);
+            lse_out[row] = lse;
+            int tg = targets[row];
+            if (tg < 0 || tg >= V) {
+                report(err, GK_ERR_INDEX);
+                tg = 0;
+            }
+            row_loss[row] = lse - xr[tg];
+        }
+    }
+}
+
 // loss = (sum over rows, in order, in float64) / rows; one block.
 __global__ void mean_rows_kernel(const float* __restrict__ row_loss, int64_t rows, float* loss) {
     __shared__ double red[32];
@@ -482,33 +767,91 @@ __global__ void softmax_ce_bwd_kernel(const float* __restrict__ logits, int64_t 
 }
 
 // float32 logits and float32 dlogits, aligned rows: 4 columns per thread.
+constexpr int CEB_U = 4;
+// float32 dlogits, aligned rows: the float4 pieces of every row (lddl / 4 per row) in one
+// grid-stride sweep, CEB_U pieces per thread and pass loaded before any store (dl may alias the
+// logits: each thread writes only what it has read).
 __global__ void softmax_ce_bwd_vec_kernel(const float* __restrict__ logits, int64_t ldl,
                                           const int32_t* __restrict__ targets, const float* __restrict__ lse,
                                           const float* __restrict__ dloss, float* dl, int64_t lddl, int64_t rows,
                                           int V) {
-    int64_t row = blockIdx.y;
-    float scale = (dloss ? *dloss : 1.0f) / (float)rows;
-    float L = lse[row];
-    int tg = targets[row];
+    const float scale = (dloss ? *dloss : 1.0f) / (float)rows;
+    const int64_t q4 = lddl / 4, total = rows * q4;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e0 < total; e0 += CEB_U * step) {
+        float4 a[CEB_U];
+#pragma unroll
+        for (int u = 0; u < CEB_U; ++u) {
+            const int64_t e = e0 + u * step;
+            a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < total) {
+                const int64_t row = e / q4, c = (e - row * q4) * 4;
+                const float* xr = logits + row * ldl;
+                if (c + 3 < V) {
+                    a[u] = *reinterpret_cast<const float4*>(xr + c);
+                } else if (c < V) {
+                    float t[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int k = 0; k < 4; ++k)
+                        if (c + k < V) t[k] = xr[c + k];
+                    a[u] = make_float4(t[0], t[1], t[2], t[3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < CEB_U; ++u) {
+            const int64_t e = e0 + u * step;
+            if (e >= total) break;
+            const int64_t row = e / q4, c = (e - row * q4) * 4;
+            const float L = lse[row];
+            const int tg = targets[row];
+            float t[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) t[k] = c + k < V ? scale * expf(t[k] - L) : 0.f;
+            if (tg >= c && tg < c + 4) t[tg - c] -= scale;
+            *reinterpret_cast<float4*>(dl + row * lddl + c) = make_float4(t[0], t[1], t[2], t[3]);
+        }
+    }
+}
+
+// float32 dlogits for rows of any width and offset (16-byte aligned bases, (ldl - lddl) % 4 ==
+// 0 so that a row of the logits and of dlogits start at the same offset): block (x, row) takes
+// float4 pieces of the row's aligned body, CEB_U per thread loaded before any store; block 0
+// also the row's leading and trailing floats.
+__global__ void softmax_ce_bwd_cut_kernel(const float* __restrict__ logits, int64_t ldl,
+                                          const int32_t* __restrict__ targets, const float* __restrict__ lse,
+                                          const float* __restrict__ dloss, float* dl, int64_t lddl, int64_t rows,
+                                          int V) {
+    const int64_t row = blockIdx.y;
+    const float scale = (dloss ? *dloss : 1.0f) / (float)rows;
+    const float L = lse[row];
+    const int tg = targets[row];
     const float* xr = logits + row * ldl;
     float* dr = dl + row * lddl;
-    for (int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; c < lddl;
-         c += (int64_t)gridDim.x * blockDim.x * 4) {
-        float4 v = make_float4(0, 0, 0, 0);
-        if (c + 3 < V) {
-            float4 a = *reinterpret_cast<const float4*>(xr + c);
-            v = make_float4(scale * expf(a.x - L), scale * expf(a.y - L), scale * expf(a.z - L), scale * expf(a.w - L));
-        } else {
-            float t[4] = {0, 0, 0, 0};
-            for (int k = 0; k < 4; ++k)
-                if (c + k < V) t[k] = scale * expf(xr[c + k] - L);
-            v = make_float4(t[0], t[1], t[2], t[3]);
+    const RowCut cut(xr, V);
+    const int step = gridDim.x * blockDim.x;
+    for (int q0 = blockIdx.x * blockDim.x + threadIdx.x; q0 < cut.nb; q0 += CEB_U * step) {
+        float4 a[CEB_U];
+#pragma unroll
+        for (int u = 0; u < CEB_U; ++u) {
+            const int q = q0 + u * step;
+            a[u] = q < cut.nb ? reinterpret_cast<const float4*>(xr + cut.head)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        if (tg >= c && tg < c + 4) {
-            float* vp = reinterpret_cast<float*>(&v);
-            vp[tg - c] -= scale;
+#pragma unroll
+        for (int u = 0; u < CEB_U; ++u) {
+            const int q = q0 + u * step;
+            if (q >= cut.nb) break;
+            const int c = cut.head + 4 * q;
+            float t[4] = {scale * expf(a[u].x - L), scale * expf(a[u].y - L), scale * expf(a[u].z - L),
+                          scale * expf(a[u].w - L)};
+            if (tg >= c && tg < c + 4) t[tg - c] -= scale;
+            *reinterpret_cast<float4*>(dr + c) = make_float4(t[0], t[1], t[2], t[3]);
         }
-        *reinterpret_cast<float4*>(dr + c) = v;
+    }
+    if (blockIdx.x == 0) {
+        const int ei = cut.edge_index(threadIdx.x);
+        if (ei >= 0) dr[ei] = scale * (expf(xr[ei] - L) - (ei == tg ? 1.f : 0.f));
+        // padding columns [V, lddl) of dlogits
+        for (int64_t c = V + threadIdx.x; c < lddl; c += blockDim.x) dr[c] = 0.f;
     }
 }
 
@@ -692,19 +1035,25 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
 #undef LN_FWD_CASE
         return launched(ctx, "layernorm_fwd");
     }
-    size_t smem = (size_t)C * sizeof(float);
-    GK_REQUIRE(ctx, smem <= 200 * 1024, GK_ERR_UNSUPPORTED, "gk_layernorm_fwd: C=%d too large", C);
-    int threads = 1024;
-    if (y_dtype == GK_F32) {
-        cudaFuncSetAttribute(layernorm_fwd_block_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        layernorm_fwd_block_kernel<float><<<(unsigned)rows, threads, smem, ctx->stream>>>(x, gamma, beta, (float*)y, mean,
-                                                                                         rstd, rows, C, eps, 0, x_copy);
-    } else {
-        cudaFuncSetAttribute(layernorm_fwd_block_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        layernorm_fwd_block_kernel<__nv_bfloat16><<<(unsigned)rows, threads, smem, ctx->stream>>>(
-            x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane, x_copy);
+    const int vec = (C % 4 == 0) && aligned16(x);
+    if (C > 4096 && C <= LNR_MAXC && aligned16(x) && (!x_copy || aligned16(x_copy)) && aligned16(y)) {
+        // wide rows held in registers: one read and one write of each element
+        const unsigned g = (unsigned)std::min<int64_t>(rows, (int64_t)ctx->num_sms * 2);
+        if (y_dtype == GK_F32)
+            layernorm_fwd_reg_kernel<float><<<g, LNR_THREADS, 0, ctx->stream>>>(x, gamma, beta, (float*)y, mean, rstd,
+                                                                               rows, C, eps, 0, x_copy);
+        else
+            layernorm_fwd_reg_kernel<__nv_bfloat16><<<g, LNR_THREADS, 0, ctx->stream>>>(
+                x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane, x_copy);
+        return launched(ctx, "layernorm_fwd");
     }
+    const unsigned grid = (unsigned)std::min<int64_t>(rows, (int64_t)ctx->num_sms * 8);
+    if (y_dtype == GK_F32)
+        layernorm_fwd_rows_kernel<float><<<grid, 256, 0, ctx->stream>>>(x, gamma, beta, (float*)y, mean, rstd, rows, C,
+                                                                       eps, 0, x_copy, vec);
+    else
+        layernorm_fwd_rows_kernel<__nv_bfloat16><<<grid, 256, 0, ctx->stream>>>(
+            x, gamma, beta, (__nv_bfloat16*)y, mean, rstd, rows, C, eps, lo_plane, x_copy, vec);
     return launched(ctx, "layernorm_fwd");
 }
 
@@ -718,21 +1067,27 @@ gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, cons
     const int np = dx_colsum ? 3 : 2;  // partial arrays: dy*xhat, dy (, dx)
     bool warp_path = (C % 128 == 0) && C <= 1024 && aligned16(x) && aligned16(dy) && aligned16(dx) &&
                      aligned16(gamma) && (!dx_bf16 || ((uintptr_t)dx_bf16 & 7) == 0);
+    // rows wider than 1024: a statistics pass, then a pass over column strips of 32 rows (the
+    // one-block-per-row kernel cannot keep enough bytes in flight at those widths)
+    const bool wide = !warp_path && C > 1024;
     int nparts;
     if (warp_path) {
         int wpb = 8;
         nparts = (int)std::min<int64_t>(cdiv(rows, wpb), (int64_t)ctx->num_sms * 2);
+    } else if (wide) {
+        nparts = (int)cdiv(rows, LNB_ROWS);  // row blocks of the column kernel
     } else {
-        // one block per row slot; bound the partial buffer (np x C floats per slot) for wide rows
+        // one block per row slot; bound the partial buffer (np x C floats per slot)
         int64_t cap = std::max<int64_t>(8, std::min<int64_t>(1216, (int64_t)(16 << 20) / ((int64_t)np * C * 4)));
         nparts = (int)std::min<int64_t>(rows, cap);
     }
-    float* partial = nullptr;
-    if (want_partials) {
-        partial = (float*)workspace(ctx, (size_t)nparts * np * C * sizeof(float));
-        GK_REQUIRE(ctx, partial, GK_ERR_WORKSPACE, "gk_layernorm_bwd: needs %zu workspace bytes",
-                   (size_t)nparts * np * C * sizeof(float));
-    }
+    // workspace: the partial sums, then (wide rows) the per-row statistics
+    const size_t part_bytes = want_partials ? (((size_t)nparts * np * C * sizeof(float) + 255) & ~size_t(255)) : 0;
+    const size_t stat_bytes = wide ? (size_t)rows * 2 * sizeof(float) : 0;
+    char* ws = (char*)workspace(ctx, part_bytes + stat_bytes);
+    GK_REQUIRE(ctx, ws || part_bytes + stat_bytes == 0, GK_ERR_WORKSPACE, "gk_layernorm_bwd: needs %zu workspace bytes",
+               part_bytes + stat_bytes);
+    float* partial = want_partials ? (float*)ws : nullptr;
     if (warp_path) {
         int wpb = 8;
         int vpt = C / 128;
@@ -749,9 +1104,18 @@ gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, cons
             LN_BWD_CASE(5) LN_BWD_CASE(6) LN_BWD_CASE(7) LN_BWD_CASE(8)
         }
 #undef LN_BWD_CASE
-    } else {
+    } else if (!wide) {
         layernorm_bwd_block_kernel<<<nparts, 512, 0, ctx->stream>>>(x, gamma, mean, rstd, dy, dx, accumulate_dx,
                                                                    (__nv_bfloat16*)dx_bf16, partial, np, rows, C);
+    } else {
+        GK_REQUIRE(ctx, cdiv(rows, LNB_ROWS) <= 65535, GK_ERR_UNSUPPORTED, "gk_layernorm_bwd: too many rows");
+        float* stats = (float*)(ws + part_bytes);
+        const int vec = (C % 4 == 0) && aligned16(x) && aligned16(dy) && aligned16(gamma);
+        layernorm_bwd_stats_kernel<<<(unsigned)std::min<int64_t>(rows, (int64_t)ctx->num_sms * 8), 256, 0,
+                                     ctx->stream>>>(x, gamma, mean, rstd, dy, stats, rows, C, vec);
+        GK_TRY(launched(ctx, "layernorm_bwd_stats"));
+        layernorm_bwd_cols_kernel<<<dim3((unsigned)cdiv(C, 256), (unsigned)nparts), 256, 0, ctx->stream>>>(
+            x, gamma, mean, rstd, dy, stats, dx, accumulate_dx, (__nv_bfloat16*)dx_bf16, partial, np, rows, C);
     }
     GK_TRY(launched(ctx, "layernorm_bwd"));
     if (want_partials) {
@@ -793,8 +1157,16 @@ gk_status gk_softmax_ce_fwd(gk_ctx* ctx, const float* logits, int64_t ldl, const
     GK_REQUIRE(ctx, rows < (1ll << 31), GK_ERR_UNSUPPORTED, "gk_softmax_ce_fwd: too many rows");
     float* row_loss = (float*)workspace(ctx, (size_t)rows * sizeof(float));
     GK_REQUIRE(ctx, row_loss, GK_ERR_WORKSPACE, "gk_softmax_ce_fwd: needs %lld workspace bytes", (long long)rows * 4);
-    softmax_ce_fwd_kernel<<<(unsigned)rows, CE_THREADS, 0, ctx->stream>>>(logits, ldl, targets, lse, row_loss, V,
-                                                                         ctx->d_err);
+    const bool al = (ldl & 3) == 0 && aligned16(logits);
+    if (V <= 4096 && al)
+        softmax_ce_fwd_warp_kernel<<<(unsigned)cdiv(rows, 8), 256, 0, ctx->stream>>>(logits, ldl, targets, lse, row_loss,
+                                                                                    rows, V, ctx->d_err);
+    else if (aligned16(logits) && V <= CER_THREADS * CER_V4 * 4)
+        softmax_ce_fwd_reg_kernel<<<(unsigned)std::min<int64_t>(rows, (int64_t)ctx->num_sms * 2), CER_THREADS, 0,
+                                    ctx->stream>>>(logits, ldl, targets, lse, row_loss, rows, V, ctx->d_err);
+    else
+        softmax_ce_fwd_kernel<<<(unsigned)rows, CE_THREADS, 0, ctx->stream>>>(logits, ldl, targets, lse, row_loss, V,
+                                                                             ctx->d_err);
     GK_TRY(launched(ctx, "softmax_ce_fwd"));
     mean_rows_kernel<<<1, 1024, 0, ctx->stream>>>(row_loss, rows, loss);
     return launched(ctx, "softmax_ce_mean");
@@ -812,9 +1184,14 @@ gk_status gk_softmax_ce_bwd(gk_ctx* ctx, const float* logits, int64_t ldl, const
                "gk_softmax_ce_bwd: in-place needs float32 and equal strides");
     int threads = 256;
     if (dl_dtype == GK_F32 && (ldl & 3) == 0 && (lddl & 3) == 0 && aligned16(logits) && aligned16(dlogits)) {
-        dim3 grid((unsigned)cdiv(cdiv(lddl, 4), threads), (unsigned)rows);
-        if (grid.x > 16) grid.x = 16;
+        const unsigned grid = (unsigned)std::min<int64_t>(cdiv(rows * (lddl / 4), (int64_t)threads * CEB_U),
+                                                          (int64_t)ctx->num_sms * 8);
         softmax_ce_bwd_vec_kernel<<<grid, threads, 0, ctx->stream>>>(logits, ldl, targets, lse, dloss, (float*)dlogits,
+                                                                    lddl, rows, V);
+    } else if (dl_dtype == GK_F32 && aligned16(logits) && aligned16(dlogits) && ((ldl - lddl) & 3) == 0 &&
+               rows <= 65535) {
+        dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(cdiv(V / 4, threads * CEB_U), 64)), (unsigned)rows);
+        softmax_ce_bwd_cut_kernel<<<grid, threads, 0, ctx->stream>>>(logits, ldl, targets, lse, dloss, (float*)dlogits,
                                                                     lddl, rows, V);
     } else if (dl_dtype == GK_BF16 && (ldl & 7) == 0 && (lddl & 7) == 0 && aligned16(logits) && aligned16(dlogits)) {
         dim3 grid((unsigned)cdiv(cdiv(lddl, 8), threads), (unsigned)rows);

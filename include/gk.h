@@ -131,8 +131,10 @@ gk_status gk_layernorm_fwd(gk_ctx* ctx, const float* x, const float* gamma, cons
  *   residual stream), this is that bias's gradient (the MatMul/bias backward rule), produced
  *   here so the rows are read once.
  * dx_bf16, if not NULL, receives a bfloat16 copy of the resulting dx. dgamma, dbeta and
- * dx_colsum may be NULL. Workspace: np * C * P * 4 bytes, np = 3 with dx_colsum else 2,
- * P <= 1216 partial slots (fewer for C > 1024). */
+ * dx_colsum may be NULL. Workspace: np * C * P * 4 bytes (np = 3 with dx_colsum, else 2, and
+ * none without dgamma, dbeta and dx_colsum), with P <= 1216 partial slots for C <= 1024
+ * (fewer for wide rows), and for C > 1024 P = ceil(rows / 32) plus 8 * rows bytes of row
+ * statistics. */
 gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, const float* mean,
                            const float* rstd, const float* dy, float* dx, int accumulate_dx,
                            uint16_t* dx_bf16, float* dgamma, float* dbeta, float* dx_colsum,

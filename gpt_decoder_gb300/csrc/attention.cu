@@ -267,6 +267,10 @@ gk_status gk_attn_fwd(gk_ctx* ctx, int dtype, const void* qkv, void* y, float* l
     GK_REQUIRE(ctx, dtype == GK_F32 || dtype == GK_BF16, GK_ERR_ARG, "gk_attn_fwd: bad dtype");
     GK_REQUIRE(ctx, (int64_t)B * H < 65536, GK_ERR_UNSUPPORTED, "gk_attn_fwd: B*H too large");
     if (dtype == GK_F32) {
+        if (ctx->math == GK_MATH_3XTF32) {
+            gk_status s = attn_fwd_3xtf32(ctx, static_cast<const float*>(qkv), static_cast<float*>(y), lse, B, T, H, hs);
+            if (s != GK_ERR_UNSUPPORTED) return s;
+        }
         GK_HS_SWITCH(hs, fwd_typed, float, ctx, qkv, y, lse, B, T, H)
     } else {
         gk_status s = attn_fwd_tc(ctx, qkv, y, lse, B, T, H, hs);
@@ -285,6 +289,10 @@ gk_status gk_attn_bwd(gk_ctx* ctx, int dtype, const void* qkv, const void* y, co
     GK_REQUIRE(ctx, (int64_t)B * H < 65536, GK_ERR_UNSUPPORTED, "gk_attn_bwd: B*H too large");
     if (dtype == GK_BF16) {
         gk_status s = attn_bwd_tc(ctx, qkv, y, lse, dy, dqkv, B, T, H, hs);
+        if (s != GK_ERR_UNSUPPORTED) return s;
+    } else if (ctx->math == GK_MATH_3XTF32) {
+        gk_status s = attn_bwd_3xtf32(ctx, static_cast<const float*>(qkv), static_cast<const float*>(y), lse,
+                                      static_cast<const float*>(dy), static_cast<float*>(dqkv), B, T, H, hs);
         if (s != GK_ERR_UNSUPPORTED) return s;
     }
     float* dvec = (float*)workspace(ctx, (size_t)B * H * T * sizeof(float));

@@ -46,6 +46,18 @@ struct Gemm {
     // operands (value = hi + lo), both K-major; the tensor-core kernel then adds the three
     // products A_hi B_hi + A_hi B_lo + A_lo B_hi (3xTF32)
     bool tf32 = false;
+    // nz > 1: nz independent products of the same shape (a batch), all through the same tensor
+    // maps. For product zl (global index zg = z0 + zl) the TMA coordinates of operand o (0 = A,
+    // 1 = B, 2 = C) are shifted along x (inner) and y (outer) by
+    //   (zg % zh) * zo[o][c][0] + (zg / zh) * zo[o][c][1] + zl * zo[o][c][2]   (c = 0: x, 1: y),
+    // e.g. zg = batch row * heads + head. Plain stores only (no bias, residual, accumulate or
+    // epilogue function); M a multiple of 128 and N of the store chunk, so that no tile crosses
+    // into a neighbouring product.
+    int nz = 1, zh = 1, z0 = 0;
+    int zo[3][2][3] = {};
+    // with nz > 1: the extents (inner, outer) of the whole buffers A, B and C that the products
+    // index into, for their tensor maps
+    int64_t a_ext[2] = {0, 0}, b_ext[2] = {0, 0}, c_ext[2] = {0, 0};
     // Softmax cross-entropy fused into a vocabulary-projection epilogue (tensor-core kernel,
     // TMA epilogue only). Column n of this GEMM is vocabulary entry ce_col0 + n, and
     // ce_tgt[m] is row m's target entry.
@@ -77,7 +89,30 @@ gk_status gemm(gk_ctx* ctx, const Gemm& g);
 // into TF32 hi / lo planes (K-major, in the context's workspace, in chunks of the output or of
 // K when the whole does not fit), then gemm_tc adds the three products.
 gk_status gemm_3xtf32(gk_ctx* ctx, const Gemm& g);
+// TF32 hi / lo planes [R][ldp] of rows row0 .. row0 + R - 1 and K range k0 .. k0 + kc - 1 of a
+// float32 operand (K-major: element (i, k) at src[i * ld + k]; else at src[k * ld + i]).
+gk_status split_planes(gk_ctx* ctx, const float* src, int64_t ld, bool kmajor, int64_t row0, int64_t k0, int64_t R,
+                       int64_t kc, float* hi, float* lo, int64_t ldp);
 
+// x = hi + lo with hi = tf32(x) (round to nearest, ties away from zero) and lo = tf32(x - hi);
+// x - hi is exact in float32.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - hi);
+}
+
+// Faithful-mode (float32) causal attention with its products as batched 3xTF32 tensor-core
+// products (T a multiple of 128, head size a multiple of 32); GK_ERR_UNSUPPORTED for other shapes
+// or when the context's workspace cannot hold one head's score buffers (the float32 CUDA-core
+// kernels then run).
+gk_status attn_fwd_3xtf32(gk_ctx* ctx, const float* qkv, float* y, float* lse, int B, int T, int H, int hs);
+gk_status attn_bwd_3xtf32(gk_ctx* ctx, const float* qkv, const float* y, const float* lse, const float* dy, float* dqkv,
+                          int B, int T, int H, int hs);
 // Tensor-core causal attention forward (bf16 q/k/v, head size 64); GK_ERR_UNSUPPORTED otherwise.
 gk_status attn_fwd_tc(gk_ctx* ctx, const void* qkv, void* y, float* lse, int B, int T, int H, int hs);
 // Tensor-core causal attention backward (bf16, head size 64); GK_ERR_UNSUPPORTED otherwise.

@@ -85,6 +85,9 @@ struct TcParams {
     const float* ce_dloss;
     float ce_scale;
     int* err;
+    // a batch of products (see Gemm::nz)
+    int nz, zh, z0;
+    int zo[3][2][3];
 };
 
 enum { IN_NONE = 0, IN_C = 1, IN_RES = 2, IN_AUX = 3 };
@@ -294,6 +297,7 @@ __device__ __forceinline__ int unit_first(const TcParams& p) { return p.pair ? (
 __device__ __forceinline__ int unit_step(const TcParams& p) { return p.pair ? (int)(gridDim.x >> 1) : (int)gridDim.x; }
 __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, int& tn, int& kb0, int& kb1) {
     int split = u % p.splits, tile = u / p.splits;
+    if (p.nz > 1) tile %= p.tiles_m * p.tiles_n;  // the tile within its product of the batch
     if (p.pair) {
         tm = (tile % p.tiles_m2) * 2 + (int)(blockIdx.x & 1);
         tn = tile / p.tiles_m2;
@@ -303,6 +307,16 @@ __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, i
     }
     kb0 = split * p.kbps;
     kb1 = min(p.kblocks, kb0 + p.kbps);
+}
+
+// Batch position of unit u, and the TMA coordinate shift of operand o along c (0 = x, 1 = y).
+__device__ __forceinline__ int unit_z(const TcParams& p, int u) {
+    return p.nz > 1 ? (u / p.splits) / (p.tiles_m * p.tiles_n) : 0;
+}
+__device__ __forceinline__ int zshift(const TcParams& p, int o, int c, int zl) {
+    if (p.nz <= 1) return 0;
+    const int zg = p.z0 + zl;
+    return (zg % p.zh) * p.zo[o][c][0] + (zg / p.zh) * p.zo[o][c][1] + zl * p.zo[o][c][2];
 }
 
 // ------------------------------------------------------------ TMA epilogue
@@ -469,6 +483,7 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
                 tma_prefetch_l2_2d(mp.in, tn2 * BN + half * (BN / 2) + c * W, tm2 * BM + q * 32);
         }
         const int y = tm * BM + q * 32;
+        const int zl = unit_z(p, u), cxs = zshift(p, 2, 0, zl), cys = zshift(p, 2, 1, zl);  // batch: C's shift
         // fused cross-entropy: this lane's row (y + lane) state over the tile's columns
         float ce_m = -INFINITY, ce_s = 0.f, ce_l2 = 0.f, ce_g = 0.f;
         int ce_t = -1;
@@ -624,9 +639,9 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
                     __syncwarp();
                     if (lane == 0) {
                         if (p.reduce_out)
-                            tma_reduce_add_2d(mp.C, slots + sl * SLOT, x, y);
+                            tma_reduce_add_2d(mp.C, slots + sl * SLOT, x + cxs, y + cys);
                         else
-                            tma_store_2d(mp.C, slots + sl * SLOT, x, y);
+                            tma_store_2d(mp.C, slots + sl * SLOT, x + cxs, y + cys);
                         bulk_commit();
                     }
                 }
@@ -687,7 +702,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 22);
 
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int units = (PAIR ? p.tiles_m2 : p.tiles_m) * p.tiles_n * p.splits;
+    int units = (PAIR ? p.tiles_m2 : p.tiles_m) * p.tiles_n * p.splits * p.nz;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
 
     if (threadIdx.x == 0) {
@@ -748,12 +763,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     };
                     uint8_t* a = smem + s * SC::STAGE;
                     uint8_t* b = a + SC::A_SLOT;
+                    const int zl = unit_z(p, u);
+                    const int axs = zshift(p, 0, 0, zl), ays = zshift(p, 0, 1, zl);
+                    const int bxs = zshift(p, 1, 0, zl), bys = zshift(p, 1, 1, zl);
 #pragma unroll
                     for (int pl = 0; pl < (SC::A_LO ? 2 : 1); ++pl) {
                         const CUtensorMap* ma = pl ? &tmA_lo : &tmA;
                         uint8_t* dst = a + pl * A_BYTES;
                         if (F32OP || p.a_kmajor) {
-                            load(ma, dst, kb * BKE, tm * BM);
+                            load(ma, dst, kb * BKE + axs, tm * BM + ays);
                         } else {
                             load(ma, dst, tm * BM, kb * BK);
                             load(ma, dst + 8192, tm * BM + 64, kb * BK);
@@ -767,7 +785,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         constexpr int BNC = (int)(SC::B_TILE / (BK * 2));
                         const int n0 = tn * BN + (int)rank * BNC;
                         if (F32OP || p.b_kmajor) {
-                            load(mb, dst, kb * BKE, n0);
+                            load(mb, dst, kb * BKE + bxs, n0 + bys);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BNC / 64; ++j) load(mb, dst + j * 8192, n0 + 64 * j, kb * BK);
@@ -1052,7 +1070,8 @@ bool setup_tma_epilogue(const Gemm& g, TcParams& p, Maps& m) {
     p.in_kind = g.residual ? IN_RES : g.epi == EPI_DGELU ? IN_AUX : (g.accumulate && !p.reduce_out) ? IN_C : IN_NONE;
     p.out_aux = g.epi == EPI_GELU;
     p.out_lo = g.c_plane != 0;
-    if (!make_map_epi(&m.c, bf, g.C, g.N, g.M, g.ldc, W)) return false;
+    const int64_t cn = g.nz > 1 ? g.c_ext[0] : g.N, cm = g.nz > 1 ? g.c_ext[1] : g.M;
+    if (!make_map_epi(&m.c, bf, g.C, cn, cm, g.ldc, W)) return false;
     m.aux = m.r = m.lo = m.c;
     if (g.epi != EPI_NONE && !make_map_epi(&m.aux, bf, g.aux, g.N, g.M, g.ldaux, W)) return false;
     if (g.residual && !make_map_epi(&m.r, false, g.residual, g.N, g.M, g.ldr, W)) return false;
@@ -1079,12 +1098,24 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     // CTA pairs (256 x 256 tiles, half of B per CTA) for the single-plane products with at least
     // four 128-row tiles; the split-precision products keep one CTA per tile
     const bool c_f32 = g.ce_mode != CE_LSE && g.c_dtype == GK_F32;
-    const int pairs = split == 0 && cdiv(g.M, BM) >= 4 ? (c_f32 ? max_pairs<float>() : max_pairs<__nv_bfloat16>()) : 0;
+    const bool batched = g.nz > 1;
+    if (batched && (g.bias || g.residual || g.accumulate || g.epi != EPI_NONE || g.ce_mode != CE_NONE || g.c_plane ||
+                    g.M % BM != 0 || g.N % (64 / (g.c_dtype == GK_F32 ? 4 : 2)) != 0 || g.zh < 1 || g.z0 < 0 ||
+                    (int64_t)g.nz * cdiv(g.M, BM) * cdiv(g.N, BN) >= (1ll << 31)))
+        return GK_ERR_UNSUPPORTED;
+    const int pairs = !batched && split == 0 && cdiv(g.M, BM) >= 4
+                          ? (c_f32 ? max_pairs<float>() : max_pairs<__nv_bfloat16>())
+                          : 0;
     const bool pair = pairs > 0;
     CUtensorMap ta, tb;
     bool ok;
+    // a batch indexes into whole buffers: their maps span them
+    const int64_t ak = batched ? g.a_ext[0] : g.K, am = batched ? g.a_ext[1] : g.M;
+    const int64_t bk = batched ? g.b_ext[0] : g.K, bn = batched ? g.b_ext[1] : g.N;
+    if (batched && (!f32op || ak <= 0 || am <= 0 || bk <= 0 || bn <= 0 || g.c_ext[0] <= 0 || g.c_ext[1] <= 0))
+        return GK_ERR_UNSUPPORTED;
     if (f32op) {
-        ok = make_map_f32(&ta, g.A, g.K, g.M, g.lda, BK / 2, BM) && make_map_f32(&tb, g.B, g.K, g.N, g.ldb, BK / 2, BN);
+        ok = make_map_f32(&ta, g.A, ak, am, g.lda, BK / 2, BM) && make_map_f32(&tb, g.B, bk, bn, g.ldb, BK / 2, BN);
     } else {
         ok = g.a_kmajor ? make_map(&ta, g.A, g.K, g.M, g.lda, BM) : make_map(&ta, g.A, g.M, g.K, g.lda, 64);
         ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, pair ? BN / 2 : BN)
@@ -1114,6 +1145,12 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.ldaux = g.ldaux;
     p.aux_dtype = g.aux_dtype;
     p.err = ctx->d_err;
+    p.nz = batched ? g.nz : 1;
+    p.zh = g.zh;
+    p.z0 = g.z0;
+    for (int o = 0; o < 3; ++o)
+        for (int c = 0; c < 2; ++c)
+            for (int t = 0; t < 3; ++t) p.zo[o][c][t] = g.zo[o][c][t];
     p.c_plane = g.c_plane;
     p.fast_act = g.c_dtype == GK_BF16 && g.c_plane == 0;
     p.vec = aligned16(g.C) && (g.ldc % 4 == 0) && (!g.bias || aligned16(g.bias)) &&
@@ -1124,7 +1161,7 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     const int slots = pair ? pairs : ctx->num_sms;
     int64_t tiles = (int64_t)(pair ? p.tiles_m2 : p.tiles_m) * p.tiles_n;
     p.splits = 1;
-    bool plain_acc = g.accumulate && g.c_dtype == GK_F32 && !g.bias && !g.residual && g.epi == EPI_NONE;
+    bool plain_acc = !batched && g.accumulate && g.c_dtype == GK_F32 && !g.bias && !g.residual && g.epi == EPI_NONE;
     if (plain_acc && tiles < slots) {
         int want = (int)cdiv(2 * (int64_t)slots, tiles);
         int maxs = std::max(1, p.kblocks / 4);
@@ -1133,7 +1170,7 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.kbps = (int)cdiv(p.kblocks, p.splits);
     p.splits = (int)cdiv(p.kblocks, p.kbps);
     p.atomic_out = p.splits > 1;
-    int64_t units = tiles * p.splits;
+    int64_t units = tiles * p.splits * p.nz;
     int grid = (int)std::min<int64_t>(units, slots) * (pair ? 2 : 1);
     const int mode = pair ? PAIR_MODE : split;
     Maps m;
@@ -1142,8 +1179,8 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     m.al = ta;
     m.bl = tb;
     if (f32op) {
-        if (!make_map_f32(&m.al, g.A_lo, g.K, g.M, g.lda, BK / 2, BM) ||
-            !make_map_f32(&m.bl, g.B_lo, g.K, g.N, g.ldb, BK / 2, BN))
+        if (!make_map_f32(&m.al, g.A_lo, ak, am, g.lda, BK / 2, BM) ||
+            !make_map_f32(&m.bl, g.B_lo, bk, bn, g.ldb, BK / 2, BN))
             return GK_ERR_UNSUPPORTED;
     } else {
         if (g.A_lo && !(g.a_kmajor ? make_map(&m.al, g.A_lo, g.K, g.M, g.lda, BM)
@@ -1170,7 +1207,7 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
         return launched(ctx, "gemm_tc");
     }
     p.tma_epi = setup_tma_epilogue(g, p, m);
-    if (!p.tma_epi && g.ce_mode != CE_NONE) return GK_ERR_UNSUPPORTED;
+    if (!p.tma_epi && (g.ce_mode != CE_NONE || batched)) return GK_ERR_UNSUPPORTED;
     if (!p.tma_epi) {
         m.c = m.aux = m.r = m.lo = ta;
         p.in_kind = IN_NONE;

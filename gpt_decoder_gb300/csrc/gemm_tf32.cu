@@ -21,17 +21,6 @@
 namespace gk {
 namespace {
 
-__device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
-__device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
-    hi = tf32_rna(x);
-    lo = tf32_rna(x - hi);
-}
-
 // K-major source: plane element (r, k) = src[(row0 + r) * ld + k0 + k], k < kc. Each thread
 // takes four consecutive k of one row (16-byte accesses when `vec`).
 __global__ void tf32_split_rows_kernel(const float* __restrict__ src, int64_t ld, int64_t row0, int64_t k0, int64_t R,
@@ -84,8 +73,14 @@ __global__ void __launch_bounds__(256) tf32_split_cols_kernel(const float* __res
     }
 }
 
-// hi / lo planes [R][ldp] of rows row0 .. row0 + R - 1 and K range k0 .. k0 + kc - 1 of an
-// operand (K-major: element (i, k) at src[i * ld + k]; else at src[k * ld + i]).
+inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// Workspace bytes for planes of an Mc x Kc block of A and an Nc x Kc block of B.
+inline size_t plane_bytes(int64_t rows, int64_t kc) { return (size_t)round_up(rows * round_up(kc, 4) * 4, 256); }
+inline size_t chunk_bytes(int64_t mc, int64_t nc, int64_t kc) { return 2 * plane_bytes(mc, kc) + 2 * plane_bytes(nc, kc); }
+
+}  // namespace
+
 gk_status split_planes(gk_ctx* ctx, const float* src, int64_t ld, bool kmajor, int64_t row0, int64_t k0, int64_t R,
                        int64_t kc, float* hi, float* lo, int64_t ldp) {
     if (kmajor) {
@@ -100,14 +95,6 @@ gk_status split_planes(gk_ctx* ctx, const float* src, int64_t ld, bool kmajor, i
     tf32_split_cols_kernel<<<grid, dim3(32, 8), 0, ctx->stream>>>(src, ld, row0, k0, R, kc, hi, lo, ldp);
     return launched(ctx, "tf32_split_cols");
 }
-
-inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
-
-// Workspace bytes for planes of an Mc x Kc block of A and an Nc x Kc block of B.
-inline size_t plane_bytes(int64_t rows, int64_t kc) { return (size_t)round_up(rows * round_up(kc, 4) * 4, 256); }
-inline size_t chunk_bytes(int64_t mc, int64_t nc, int64_t kc) { return 2 * plane_bytes(mc, kc) + 2 * plane_bytes(nc, kc); }
-
-}  // namespace
 
 gk_status gemm_3xtf32(gk_ctx* ctx, const Gemm& g) {
     if (g.ab_dtype != GK_F32 || g.tf32 || g.A_lo || g.B_lo || g.ce_mode != CE_NONE || g.c_dtype != GK_F32 ||

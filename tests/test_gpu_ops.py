@@ -434,12 +434,16 @@ def _attn_inputs(B, T, H, hs, seed, dt):
     return qkv, dy
 
 
-@pytest.mark.parametrize("B,T,H,hs", ATTN)
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("B,T,H,hs", ATTN + [(1, 256, 3, 32), (2, 384, 2, 64)])
+@pytest.mark.parametrize("dt", ["f32", "3xtf32", "bf16"])
 def test_attention_fwd_bwd(gkctx, B, T, H, hs, dt):
+    """f32: float32 FMA on the CUDA cores; 3xtf32: the products on the tensor cores (T a multiple of
+    128, other shapes take the float32 kernels); bf16: the bf16 tensor-core kernels (hs = 64)."""
     from gpt_decoder_gb300 import gk
 
     torch = _t()
+    math_dt = dt
+    dt = _set_math(gkctx, dt)
     qkv, dy = _attn_inputs(B, T, H, hs, 700 + T, dt)
     gdt = gk.GK_F32 if dt == "f32" else gk.GK_BF16
     tdt = torch.float32 if dt == "f32" else torch.bfloat16
@@ -450,7 +454,7 @@ def test_attention_fwd_bwd(gkctx, B, T, H, hs, dt):
     gk.gk_attn_fwd(gkctx, gdt, d_qkv, y, lse, B, T, H, hs)
     ry, P, rl = ops.attention_fwd(qkv, H)
     gk.gk_sync(gkctx)
-    tol_y = 2e-5 if dt == "f32" else 8e-3
+    tol_y = _tol(math_dt, T, 2e-5) if dt == "f32" else 8e-3
     assert_close(host(y), ry.reshape(B * T, C), tol_y)
     np.testing.assert_allclose(host(lse), rl.reshape(-1), rtol=1e-5, atol=1e-5)
     dqkv = torch.empty(B * T, 3 * C, device="cuda", dtype=tdt)
@@ -459,8 +463,9 @@ def test_attention_fwd_bwd(gkctx, B, T, H, hs, dt):
     gk.gk_attn_bwd(gkctx, gdt, d_qkv, y_in, dev(rl.reshape(-1).astype(np.float32)), dev(dy.reshape(B * T, C), tdt),
                    dqkv, B, T, H, hs)
     gk.gk_sync(gkctx)
+    _restore_math(gkctx)
     rd = ops.attention_bwd(qkv, P, dy, H).reshape(B * T, 3 * C)
-    assert_close(host(dqkv), rd, (5e-5 if dt == "f32" else 1e-2))
+    assert_close(host(dqkv), rd, (_tol(math_dt, T, 5e-5) if dt == "f32" else 1e-2))
 
 
 # --------------------------------------------------------- softmax cross-entropy

@@ -294,6 +294,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         extra["step_b4"] = bench_step_b4(s)
         extra["op_sweep"] = bench_op_sweep()
+        extra["gemm_bf16_gpt2_b16"] = bench_gemm_shapes()
         extra["generic_ops"] = bench_generic(ctx)
     if rank != 0:
         return
@@ -444,6 +445,76 @@ def bench_op_sweep(reps=5):
     del flush
     torch.cuda.empty_cache()
     return res
+
+
+def bench_gemm_shapes(reps=7):
+    """The bf16 products of one transformer block of the GPT-2-124M step at B=16 x T=1024
+    (16384 rows), called as the training step calls them (bias, residual added in place,
+    GELU with its pre-activation, the GELU backward fused into dX, dW accumulated), each timed
+    alone with L2 overwritten before every call: TFLOP/s against the measured bf16 peak, and
+    torch.matmul (cuBLAS) on the same plain shape as a library reference."""
+    import torch
+
+    from gpt_decoder_gb300 import gk
+
+    _, bf16, bf16_sus, _ = _peaks()
+    flush = torch.empty(64 << 20, device="cuda")
+    ctx = gk.Ctx(torch.cuda.current_stream().cuda_stream)
+    gk.gk_set_math(ctx, gk.GK_MATH_FP32)
+    N, C = 16384, 768
+    BF = torch.bfloat16
+    g = torch.Generator(device="cuda").manual_seed(3)
+    rn = lambda *sh, dt=BF: (torch.randn(*sh, device="cuda", generator=g) * 0.5).to(dt)
+    x768, x3072 = rn(N, C), rn(N, 4 * C)
+    w_qkv, w_proj, w_fc, w_mp = rn(C, 3 * C), rn(C, C), rn(C, 4 * C), rn(4 * C, C)
+    b3, b1, b4 = rn(3 * C, dt=torch.float32), rn(C, dt=torch.float32), rn(4 * C, dt=torch.float32)
+    res = rn(N, C, dt=torch.float32)
+    y2304, y3072, pre = torch.empty(N, 3 * C, dtype=BF, device="cuda"), torch.empty(N, 4 * C, dtype=BF, device="cuda"), \
+        torch.empty(N, 4 * C, dtype=BF, device="cuda")
+    dy768, dy2304, dy3072 = rn(N, C), rn(N, 3 * C), rn(N, 4 * C)
+    dx768f, dx768b, dx3072b = torch.empty(N, C, device="cuda"), torch.empty(N, C, dtype=BF, device="cuda"), \
+        torch.empty(N, 4 * C, dtype=BF, device="cuda")
+    dw = torch.zeros(4 * C * C, device="cuda")
+    db = torch.zeros(4 * C, device="cuda")
+    fwd = lambda *a: gk.gk_matmul_fwd(ctx, gk.GK_BF16, *a)
+    bwd = lambda *a: gk.gk_matmul_bwd(ctx, gk.GK_BF16, *a)
+    A, NONE = gk.GK_ACT_NONE, None
+    cases = {
+        "qkv_fwd": (lambda: fwd(x768, C, w_qkv, 3 * C, 0, b3, NONE, 0, y2304, 3 * C, gk.GK_BF16, N, C, 3 * C, A,
+                                NONE, 0, NONE, NONE), 2 * N * C * 3 * C, (x768, w_qkv)),
+        "proj_fwd_residual": (lambda: fwd(x768, C, w_proj, C, 0, b1, res, C, res, C, gk.GK_F32, N, C, C, A, NONE, 0,
+                                          NONE, NONE), 2 * N * C * C, (x768, w_proj)),
+        "fc_fwd_gelu": (lambda: fwd(x768, C, w_fc, 4 * C, 0, b4, NONE, 0, y3072, 4 * C, gk.GK_BF16, N, C, 4 * C,
+                                    gk.GK_ACT_GELU, pre, 4 * C, NONE, NONE), 2 * N * C * 4 * C, (x768, w_fc)),
+        "mlpproj_fwd_residual": (lambda: fwd(x3072, 4 * C, w_mp, C, 0, b1, res, C, res, C, gk.GK_F32, N, 4 * C, C, A,
+                                             NONE, 0, NONE, NONE), 2 * N * 4 * C * C, (x3072, w_mp)),
+        "mlpproj_bwd_dgelu": (lambda: bwd(x3072, 4 * C, w_mp, C, 0, dy768, C, dx3072b, 4 * C, gk.GK_BF16, 0, pre,
+                                          4 * C, dw, C, NONE, N, 4 * C, C), 4 * N * 4 * C * C, None),
+        "fc_bwd": (lambda: bwd(x768, C, w_fc, 4 * C, 0, dy3072, 4 * C, dx768f, C, gk.GK_F32, 0, NONE, 0, dw, 4 * C,
+                               db, N, C, 4 * C), 4 * N * C * 4 * C, None),
+        "proj_bwd": (lambda: bwd(x768, C, w_proj, C, 0, dy768, C, dx768b, C, gk.GK_BF16, 0, NONE, 0, dw, C, NONE, N,
+                                 C, C), 4 * N * C * C, None),
+        "qkv_bwd": (lambda: bwd(x768, C, w_qkv, 3 * C, 0, dy2304, 3 * C, dx768f, C, gk.GK_F32, 0, NONE, 0, dw, 3 * C,
+                                db, N, C, 3 * C), 4 * N * C * 3 * C, None),
+    }
+    out = {}
+    for name, (fn, flops, plain) in cases.items():
+        fn()
+        t = time_events(fn, reps, flush=flush)
+        r = {"tflops": flops / (t / 1e3) / 1e12, "us": t * 1e3}
+        r["frac"] = r["tflops"] / bf16
+        if plain is not None:
+            a, b = plain
+            tl = time_events(lambda: torch.matmul(a, b), reps, flush=flush)
+            r["cublas_tflops"] = flops / (tl / 1e3) / 1e12
+        out[name] = r
+    gk.gk_sync(ctx)
+    ctx.close()
+    out["peak_tflops"] = bf16
+    out["peak_source"] = "measured bf16 burst (each product timed alone)"
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def gemm_traffic_per_step(B, mode):
@@ -602,8 +673,19 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--only", choices=["sweep", "gemm-shapes"],
+                    help="run only the float32 op sweep, or only the bf16 products of one GPT-2 block at "
+                         "16384 rows, and print the result as one JSON line")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.only:
+        import torch
+
+        torch.cuda.init()
+        if args.only == "sweep":
+            print(json.dumps({"op_sweep": bench_op_sweep()}))
+        else:
+            print(json.dumps({"gemm_bf16_gpt2_b16": bench_gemm_shapes()}))
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

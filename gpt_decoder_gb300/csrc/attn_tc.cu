@@ -17,6 +17,8 @@
 // All mbarrier waits are bounded (timeout -> GK_ERR_TIMEOUT in the error word).
 #include <math.h>
 
+#include <algorithm>
+
 #include "tcgen05.cuh"
 
 namespace gk {
@@ -39,49 +41,62 @@ __device__ __forceinline__ uint32_t p_offset(int r, int c) {
     return (uint32_t)(half * 16384 + r * 128 + (((chunk ^ (r & 7)) << 4) | (byte & 15)));
 }
 
-// Forward, two query tiles per CTA played against each other ("ping-pong"): warps 0-3 own
-// query tile A, warps 4-7 tile B (the next one), warp 8 streams K/V tiles (shared by both) through
-// a 2-stage ring, warp 9 issues the MMAs. While one group turns its S tile into P, the tensor
-// core computes the other group's P V and its next S, so the softmax runs in the MMAs' shadow.
-// The MMA warp issues S_g(j+1) after P_g V_j, so S_g(j+1) landing also means O_g and P_g are
-// free again. TMEM: S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383.
+// Forward, two query tiles per work item played against each other ("ping-pong"): warps 0-3
+// own query tile A, warps 4-7 tile B (the next one), warp 8 streams Q and the K/V tiles (shared
+// by both) through shared memory, warp 9 issues the MMAs. While one group turns its S tile into
+// P, the tensor core computes the other group's P V and its next S, so the softmax runs in the
+// MMAs' shadow. The MMA warp issues S_g(j+1) after P_g V_j, so S_g(j+1) landing also means O_g
+// and P_g are free again. TMEM: S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383.
+//
+// The kernel is persistent: one CTA per SM walks a list of work items (batch x head, pair of
+// query tiles), so the tensor memory, the barriers and the pipeline are set up once, and the
+// next item's Q and K/V tiles load while the current one finishes (Q is double-buffered: the
+// items alternate between two Q sets; the K/V ring runs on across items). The items are ordered
+// heaviest first (the last query tiles see the most keys) and dealt to the CTAs in snake order
+// (round r: CTA c takes item r G + c for even r, r G + G - 1 - c for odd r), which evens out the
+// CTAs' total work. Every role walks the same item sequence and keeps its barrier phases running
+// across items.
 // Registers are granted to a block in groups of four warps, so 9- or 10-warp blocks are
 // budgeted as 12 warps: 168 registers per thread at most (hence __maxnreg__(168)).
 constexpr int FWD_THREADS = 320;
-constexpr size_t FWD_SMEM_BYTES = 6 * TILE + 1024 + 256;  // Q_A, Q_B, K[2], V[2]
+constexpr size_t FWD_SMEM_BYTES = 8 * TILE + 1024 + 256;  // Q[2 sets][A, B], K[2], V[2]
+
+// The r-th work item of this CTA, or -1 when it has no more: item k runs query-tile pair
+// n_pairs - 1 - k / BH of (batch x head) k % BH.
+__device__ __forceinline__ int fwd_item(int r, int n_items) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int k = r * G + ((r & 1) ? G - 1 - c : c);
+    return k < n_items ? k : -1;
+}
 
 __global__ void __maxnreg__(168)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, __nv_bfloat16* __restrict__ y,
-                       float* __restrict__ lse, int T, int H, int* err) {
+                       float* __restrict__ lse, int T, int H, int BH, int n_items, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;              // [2] (A, B)
-    uint8_t* sK = smem + 2 * TILE;   // [2] stages
-    uint8_t* sV = smem + 4 * TILE;   // [2] stages
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * TILE);
-    uint64_t* bar_q = bars;          // Q_A and Q_B landed
-    uint64_t* kv_full = bars + 1;    // [2]
-    uint64_t* kv_empty = bars + 3;   // [2]
-    uint64_t* bar_s = bars + 5;      // [2] S_g ready
-    uint64_t* bar_p = bars + 7;      // [2] P_g written (128 arrivals)
-    uint64_t* bar_o = bars + 9;      // [2] O_g tile ready
-    uint64_t* bar_drain = bars + 11;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+    uint8_t* sQ = smem;              // [2 sets][A, B]
+    uint8_t* sK = smem + 4 * TILE;   // [2] stages
+    uint8_t* sV = smem + 6 * TILE;   // [2] stages
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 8 * TILE);
+    uint64_t* bar_q = bars;          // [2] Q set landed
+    uint64_t* q_empty = bars + 2;    // [2] Q set free again (the item's MMAs are done)
+    uint64_t* kv_full = bars + 4;    // [2]
+    uint64_t* kv_empty = bars + 6;   // [2]
+    uint64_t* bar_s = bars + 8;      // [2] S_g ready
+    uint64_t* bar_p = bars + 10;     // [2] P_g written (128 arrivals)
+    uint64_t* bar_o = bars + 12;     // [2] O_g tile ready
+    uint64_t* bar_drain = bars + 14;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = H * HS;
     const int n_qt = (T + QT - 1) / QT;
-    // blocks are dispatched x fastest: every (batch, head) of the heaviest pair goes first
-    const int pair = gridDim.y - 1 - blockIdx.y;
-    const int qa = 2 * pair;
-    const bool has_b = qa + 1 < n_qt;
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int row0 = b * T;
-    const int n_kv = has_b ? qa + 2 : qa + 1;      // key tiles the CTA needs (B needs one more)
+    const int n_pairs = (n_qt + 1) / 2;
 
     if (tid == 0) {
-        mbar_init(bar_q, 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_q[i], 1);
+            mbar_init(&q_empty[i], 1);
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
             mbar_init(&bar_s[i], 1);
@@ -101,27 +116,44 @@ __global__ void __maxnreg__(168)
     if (warp == 8) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
-            mbar_expect_tx(bar_q, has_b ? 2 * TILE : TILE);
-            tma_load_2d(&tm_qkv, bar_q, sQ, h * HS, row0 + qa * QT);
-            if (has_b) tma_load_2d(&tm_qkv, bar_q, sQ + TILE, h * HS, row0 + (qa + 1) * QT);
-            int last_ph[2] = {-1, -1};
-            for (int j = 0; j < n_kv; ++j) {
-                int st = j & 1;
-                uint32_t ph = (j >> 1) & 1;
-                if (!mbar_wait(&kv_empty[st], ph ^ 1, nullptr, WAIT_NS)) {
+            int kvj = 0;  // K/V tiles issued so far (all items)
+            int last_kv[2] = {-1, -1}, last_q[2] = {-1, -1};
+            for (int r = 0, it = 0;; ++r, ++it) {
+                const int k = fwd_item(r, n_items);
+                if (k < 0) break;
+                const int qa = 2 * (n_pairs - 1 - k / BH), bh = k % BH;
+                const bool has_b = qa + 1 < n_qt;
+                const int h = bh % H, row0 = (bh / H) * T;
+                const int n_kv = has_b ? qa + 2 : qa + 1;
+                const int qs = it & 1;
+                if (it >= 2 && !mbar_wait(&q_empty[qs], ((it >> 1) - 1) & 1, nullptr, WAIT_NS)) {
                     failed = true;
                     break;
                 }
-                mbar_expect_tx(&kv_full[st], 2 * TILE);
-                tma_load_2d(&tm_qkv, &kv_full[st], sK + st * TILE, C + h * HS, row0 + j * KT);
-                tma_load_2d(&tm_qkv, &kv_full[st], sV + st * TILE, 2 * C + h * HS, row0 + j * KT);
-                last_ph[st] = (int)ph;
+                mbar_expect_tx(&bar_q[qs], has_b ? 2 * TILE : TILE);
+                tma_load_2d(&tm_qkv, &bar_q[qs], sQ + 2 * qs * TILE, h * HS, row0 + qa * QT);
+                if (has_b) tma_load_2d(&tm_qkv, &bar_q[qs], sQ + (2 * qs + 1) * TILE, h * HS, row0 + (qa + 1) * QT);
+                last_q[qs] = (it >> 1) & 1;
+                for (int j = 0; j < n_kv && !failed; ++j, ++kvj) {
+                    const int st = kvj & 1;
+                    const uint32_t ph = (kvj >> 1) & 1;
+                    if (!mbar_wait(&kv_empty[st], ph ^ 1, nullptr, WAIT_NS)) {
+                        failed = true;
+                        break;
+                    }
+                    mbar_expect_tx(&kv_full[st], 2 * TILE);
+                    tma_load_2d(&tm_qkv, &kv_full[st], sK + st * TILE, C + h * HS, row0 + j * KT);
+                    tma_load_2d(&tm_qkv, &kv_full[st], sV + st * TILE, 2 * C + h * HS, row0 + j * KT);
+                    last_kv[st] = (int)ph;
+                }
+                if (failed) break;
             }
             if (failed) {
                 // let this CTA's copies in flight land before shared memory is released
-                mbar_wait(bar_q, 0, nullptr, WAIT_NS / 5);
-                for (int st = 0; st < 2; ++st)
-                    if (last_ph[st] >= 0) mbar_wait(&kv_full[st], (uint32_t)last_ph[st], nullptr, WAIT_NS / 5);
+                for (int i = 0; i < 2; ++i) {
+                    if (last_q[i] >= 0) mbar_wait(&bar_q[i], (uint32_t)last_q[i], nullptr, WAIT_NS / 5);
+                    if (last_kv[i] >= 0) mbar_wait(&kv_full[i], (uint32_t)last_kv[i], nullptr, WAIT_NS / 5);
+                }
             }
         }
     } else if (warp == 9) {
@@ -129,63 +161,81 @@ __global__ void __maxnreg__(168)
         // issues each group of MMAs together with the commits that track them.
         const uint32_t id_s = instr_desc_bf16(false, false, 128, 128);
         const uint32_t id_o = instr_desc_bf16(false, true, 128, 64);
-        const int nA = qa + 1, nB = has_b ? qa + 2 : 0;
-        const uint64_t q_d0 = smem_desc(saddr(sQ), 16, 1024), q_d1 = smem_desc(saddr(sQ + TILE), 16, 1024);
         const uint64_t k_d0 = smem_desc(saddr(sK), 16, 1024), k_d1 = smem_desc(saddr(sK + TILE), 16, 1024);
         const uint64_t v_d0 = smem_desc(saddr(sV), 8192, 1024), v_d1 = smem_desc(saddr(sV + TILE), 8192, 1024);
-        bool issued = false;
-        bool ok = __all_sync(0xffffffffu,
-                             mbar_wait(bar_q, 0, nullptr, WAIT_NS) && mbar_wait(&kv_full[0], 0, nullptr, WAIT_NS));
-        if (ok) {
+        bool issued = false, ok = true;
+        int kvj = 0, pc[2] = {0, 0}, it = 0;
+        for (int r = 0; ok; ++r, ++it) {
+            const int k = fwd_item(r, n_items);
+            if (k < 0) break;
+            const int qa = 2 * (n_pairs - 1 - k / BH);
+            const bool has_b = qa + 1 < n_qt;
+            const int nA = qa + 1, nB = has_b ? qa + 2 : 0, n_kv = has_b ? qa + 2 : qa + 1;
+            const int qs = it & 1;
+            const uint64_t q_d0 = smem_desc(saddr(sQ + 2 * qs * TILE), 16, 1024);
+            const uint64_t q_d1 = smem_desc(saddr(sQ + (2 * qs + 1) * TILE), 16, 1024);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_q[qs], (it >> 1) & 1, nullptr, WAIT_NS) &&
+                                             mbar_wait(&kv_full[kvj & 1], (kvj >> 1) & 1, nullptr, WAIT_NS));
+            if (!ok) break;
             tc_fence_after();
             if (elect_one()) {
                 for (int g = 0; g < (has_b ? 2 : 1); ++g) {
 #pragma unroll
-                    for (int k = 0; k < HS / 16; ++k)
-                        umma_bf16(tmem + g * 128, desc_add(pick(q_d0, q_d1, g), k * 32), desc_add(k_d0, k * 32), id_s, k > 0);
+                    for (int kk = 0; kk < HS / 16; ++kk)
+                        umma_bf16(tmem + g * 128, desc_add(pick(q_d0, q_d1, g), kk * 32),
+                                  desc_add(pick(k_d0, k_d1, kvj & 1), kk * 32), id_s, kk > 0);
                     umma_commit(&bar_s[g]);
                 }
             }
             __syncwarp();
             issued = true;
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-            for (int g = 0; g < 2 && ok; ++g) {
-                const int ng = g ? nB : nA;
-                if (j >= ng) continue;
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar_p[g], j & 1, nullptr, WAIT_NS));
-                if (!ok) break;
-                tc_fence_after();
-                // O_g(j) = P_g V_j, P_g read from TMEM (bf16 pairs over S_g's first 64 columns)
-                if (elect_one()) {
-#pragma unroll
-                    for (int k = 0; k < KT / 16; ++k)
-                        umma_bf16_ts(tmem + 256 + g * 64, tmem + g * 128 + k * 8, desc_add(pick(v_d0, v_d1, j & 1), k * 2048), id_o,
-                                     (j > 0 || k > 0) ? 1u : 0u);
-                    if (j == ng - 1) umma_commit(&bar_o[g]);
-                    // the last reader of K/V stage j frees it for the tile j + 2
-                    if (g == 1 || j >= nB) umma_commit(&kv_empty[j & 1]);
-                }
-                __syncwarp();
-                // S_g(j + 1), once K_{j+1} has landed
-                if (j + 1 < ng) {
-                    if (g == 0 || j + 1 >= nA) {
-                        ok = __all_sync(0xffffffffu,
-                                        mbar_wait(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, nullptr, WAIT_NS));
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int sj = (kvj + j) & 1, sn = (kvj + j + 1) & 1;
+                for (int g = 0; g < 2 && ok; ++g) {
+                    const int ng = g ? nB : nA;
+                    if (j >= ng) continue;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar_p[g], pc[g] & 1, nullptr, WAIT_NS));
+                    if (!ok) break;
+                    ++pc[g];
+                    tc_fence_after();
+                    // O_g(j) = P_g V_j, P_g read from TMEM (bf16 pairs over S_g's first 64 columns)
                     if (elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < HS / 16; ++k)
-                            umma_bf16(tmem + g * 128, desc_add(pick(q_d0, q_d1, g), k * 32),
-                                      desc_add(pick(k_d0, k_d1, (j + 1) & 1), k * 32), id_s, k > 0);
-                        umma_commit(&bar_s[g]);
+                        for (int kk = 0; kk < KT / 16; ++kk)
+                            umma_bf16_ts(tmem + 256 + g * 64, tmem + g * 128 + kk * 8,
+                                         desc_add(pick(v_d0, v_d1, sj), kk * 2048), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+                        if (j == ng - 1) umma_commit(&bar_o[g]);
+                        // the last reader of K/V stage j frees it for the tile two ahead
+                        if (g == 1 || j >= nB) umma_commit(&kv_empty[sj]);
                     }
                     __syncwarp();
+                    // S_g(j + 1), once K_{j+1} has landed
+                    if (j + 1 < ng) {
+                        if (g == 0 || j + 1 >= nA) {
+                            ok = __all_sync(0xffffffffu,
+                                            mbar_wait(&kv_full[sn], ((kvj + j + 1) >> 1) & 1, nullptr, WAIT_NS));
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        if (elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < HS / 16; ++kk)
+                                umma_bf16(tmem + g * 128, desc_add(pick(q_d0, q_d1, g), kk * 32),
+                                          desc_add(pick(k_d0, k_d1, sn), kk * 32), id_s, kk > 0);
+                            umma_commit(&bar_s[g]);
+                        }
+                        __syncwarp();
+                    }
                 }
             }
+            if (!ok) break;
+            // every MMA of the item that reads this Q set has been issued
+            if (elect_one()) umma_commit(&q_empty[qs]);
+            __syncwarp();
+            kvj += n_kv;
         }
+        // the last item's MMAs (and the commits tracking them) complete before the CTA exits
+        if (ok && it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&q_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, nullptr, WAIT_NS));
         if (!ok) {
             failed = true;
             if (issued) {
@@ -197,126 +247,139 @@ __global__ void __maxnreg__(168)
             }
         }
     } else {
-        // softmax warps: thread r of group g owns query row q0 + r
+        // softmax warps: thread r of group g owns query row q0 + r of each item
         const int g = warp >> 2;          // group: 0 = tile A, 1 = tile B
-        const int r = (warp & 3) * 32 + lane;
-        const int q0 = (qa + g) * QT;
-        const int qq = q0 + r;
+        const int rr = (warp & 3) * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t o_addr = lane_addr + 256 + g * 64;
         const float sl2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
-        // m_ref: the reference the row's P and running sum l are taken against, in log2
-        // units; it moves (and O in TMEM is rescaled) only when the row maximum exceeds it by
-        // more than 8, so P <= 2^8 and most key tiles skip the rescale.
-        float m_ref = -INFINITY, l = 0.f;
-        const int my_kt = g ? (has_b ? qa + 2 : 0) : qa + 1;
-        for (int j = 0; j < my_kt; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[g], j & 1, nullptr, WAIT_NS))) {
-                failed = true;
-                break;
-            }
-            tc_fence_after();
-            // S row (128 keys) in one go; S_g(j) complete also means P_g V_{j-1} is complete
-            uint32_t sv[4][32];
+        int sc = 0, oc = 0;  // S_g tiles and O_g results waited for so far
+        for (int r = 0; !failed; ++r) {
+            const int k = fwd_item(r, n_items);
+            if (k < 0) break;
+            const int qa = 2 * (n_pairs - 1 - k / BH), bh = k % BH;
+            const bool has_b = qa + 1 < n_qt;
+            const int h = bh % H, row0 = (bh / H) * T;
+            const int q0 = (qa + g) * QT;
+            const int qq = q0 + rr;
+            const int my_kt = g ? (has_b ? qa + 2 : 0) : qa + 1;
+            if (my_kt == 0) continue;
+            // m_ref: the reference the row's P and running sum l are taken against, in log2
+            // units; it moves (and O in TMEM is rescaled) only when the row maximum exceeds it
+            // by more than 8, so P <= 2^8 and most key tiles skip the rescale.
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < my_kt; ++j) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[g], sc & 1, nullptr, WAIT_NS))) {
+                    failed = true;
+                    break;
+                }
+                ++sc;
+                tc_fence_after();
+                // S row (128 keys) in one go; S_g(j) complete also means P_g V_{j-1} is complete
+                uint32_t sv[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_addr + g * 128 + c * 32, sv[c]);
-            tmem_wait_ld_only();
+                for (int c = 0; c < 4; ++c) tmem_ld32_nowait(lane_addr + g * 128 + c * 32, sv[c]);
+                tmem_wait_ld_only();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) reg_fence32(sv[c]);
-            // keys k0 + i, i < lim, are visible to this row (causal; the diagonal tile only)
-            const int k0 = j * KT;
-            const bool diag = j == qa + g;
-            const int lim = diag ? min(qq, T - 1) - k0 + 1 : KT;
-            if (diag) {  // hidden keys -> -inf, so their P is exactly 0 below
+                for (int c = 0; c < 4; ++c) reg_fence32(sv[c]);
+                // keys k0 + i, i < lim, are visible to this row (causal; the diagonal tile only)
+                const int k0 = j * KT;
+                const bool diag = j == qa + g;
+                const int lim = diag ? min(qq, T - 1) - k0 + 1 : KT;
+                if (diag) {  // hidden keys -> -inf, so their P is exactly 0 below
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c * 32 + i >= lim) sv[c][i] = 0xff800000u;
+                }
+                float mx[8];  // eight independent partial maxima instead of one 128-long chain
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[0][e]);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (c * 32 + i >= lim) sv[c][i] = 0xff800000u;
-            }
-            float mx[8];  // eight independent partial maxima instead of one 128-long chain
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[0][e]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[c][i]));
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float m_new = fmaxf(m_ref, mt * sl2);
-            // move the reference (O is rescaled after P is written, when the S row is dead)
-            float corr = 1.f;
-            const bool rescale = m_new > m_ref + 8.f;
-            if (rescale) {
-                corr = ex2_hw(m_ref - m_new);  // 0 while the row was empty
-                l *= corr;
-                m_ref = m_new;
-            }
-            // P = 2^(S * sl2 - m_ref) as bf16 pairs into TMEM over S_g's first 64 columns (this
-            // thread's row, already read), where the P V product takes its A operand
-            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pw[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float p0 = ex2_hw(fmaf(__uint_as_float(sv[c][2 * e]), sl2, -m_ref));
-                    float p1 = ex2_hw(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl2, -m_ref));
-                    ps[(2 * e) & 7] += p0;
-                    ps[(2 * e + 1) & 7] += p1;
-                    __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                    pw[e] = *reinterpret_cast<uint32_t*>(&t2);
+                    for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[c][i]));
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float m_new = fmaxf(m_ref, mt * sl2);
+                // move the reference (O is rescaled after P is written, when the S row is dead)
+                float corr = 1.f;
+                const bool rescale = m_new > m_ref + 8.f;
+                if (rescale) {
+                    corr = ex2_hw(m_ref - m_new);  // 0 while the row was empty
+                    l *= corr;
+                    m_ref = m_new;
                 }
-                tmem_st16(lane_addr + g * 128 + c * 16, pw);
-            }
-            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            // tcgen05.ld / st are warp-collective: the warp rescales if any of its rows must
-            // (corr = 1 for the others)
-            if (j > 0 && __any_sync(0xffffffffu, rescale)) {  // O row, two 32-column halves
+                // P = 2^(S * sl2 - m_ref) as bf16 pairs into TMEM over S_g's first 64 columns
+                // (this thread's row, already read), where the P V product takes its A operand
+                float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32_nowait(o_addr + c * 32, ov);
-                    tmem_wait_ld_only();
-                    reg_fence32(ov);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pw[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
-                    tmem_st32(o_addr + c * 32, ov);
-                }
-            }
-            tmem_wait_st();  // P (and a rescaled O) in TMEM before the MMA warp is told
-            tc_fence_before();
-            mbar_arrive(&bar_p[g]);
-        }
-        if (!failed && my_kt > 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[g], 0, nullptr, WAIT_NS))) {
-                failed = true;
-            } else {
-                tc_fence_after();
-                uint32_t ov[2][32];
-                tmem_ld32_nowait(o_addr, ov[0]);
-                tmem_ld32_nowait(o_addr + 32, ov[1]);
-                tmem_wait_ld_only();
-                reg_fence32(ov[0]);
-                reg_fence32(ov[1]);
-                if (qq < T) {
-                    const float inv = 1.f / l;
-                    __nv_bfloat16* yr = y + (int64_t)(row0 + qq) * C + h * HS;
-#pragma unroll
-                    for (int d = 0; d < HS; d += 8) {
-                        uint32_t pw[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int dd = d + 2 * e;
-                            __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(ov[dd >> 5][dd & 31]) * inv,
-                                                                      __uint_as_float(ov[(dd + 1) >> 5][(dd + 1) & 31]) * inv);
-                            pw[e] = *reinterpret_cast<uint32_t*>(&t2);
-                        }
-                        *reinterpret_cast<uint4*>(yr + d) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    for (int e = 0; e < 16; ++e) {
+                        float p0 = ex2_hw(fmaf(__uint_as_float(sv[c][2 * e]), sl2, -m_ref));
+                        float p1 = ex2_hw(fmaf(__uint_as_float(sv[c][2 * e + 1]), sl2, -m_ref));
+                        ps[(2 * e) & 7] += p0;
+                        ps[(2 * e + 1) & 7] += p1;
+                        __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                        pw[e] = *reinterpret_cast<uint32_t*>(&t2);
                     }
-                    lse[(int64_t)bh * T + qq] = (m_ref + log2f(l)) * 0.6931471805599453f;
+                    tmem_st16(lane_addr + g * 128 + c * 16, pw);
                 }
+                l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                // tcgen05.ld / st are warp-collective: the warp rescales if any of its rows must
+                // (corr = 1 for the others)
+                if (j > 0 && __any_sync(0xffffffffu, rescale)) {  // O row, two 32-column halves
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32_nowait(o_addr + c * 32, ov);
+                        tmem_wait_ld_only();
+                        reg_fence32(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+                        tmem_st32(o_addr + c * 32, ov);
+                    }
+                }
+                tmem_wait_st();  // P (and a rescaled O) in TMEM before the MMA warp is told
+                tc_fence_before();
+                mbar_arrive(&bar_p[g]);
             }
+            if (failed) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_o[g], oc & 1, nullptr, WAIT_NS))) {
+                failed = true;
+                break;
+            }
+            ++oc;
+            tc_fence_after();
+            uint32_t ov[2][32];
+            tmem_ld32_nowait(o_addr, ov[0]);
+            tmem_ld32_nowait(o_addr + 32, ov[1]);
+            tmem_wait_ld_only();
+            reg_fence32(ov[0]);
+            reg_fence32(ov[1]);
+            if (qq < T) {
+                const float inv = 1.f / l;
+                __nv_bfloat16* yr = y + (int64_t)(row0 + qq) * C + h * HS;
+#pragma unroll
+                for (int d = 0; d < HS; d += 8) {
+                    uint32_t pw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int dd = d + 2 * e;
+                        __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(ov[dd >> 5][dd & 31]) * inv,
+                                                                  __uint_as_float(ov[(dd + 1) >> 5][(dd + 1) & 31]) * inv);
+                        pw[e] = *reinterpret_cast<uint32_t*>(&t2);
+                    }
+                    *reinterpret_cast<uint4*>(yr + d) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                }
+                lse[(int64_t)bh * T + qq] = (m_ref + log2f(l)) * 0.6931471805599453f;
+            }
+            // O_g is read: the next item's first P_g V (which overwrites it) is issued only after
+            // this warp arrives on bar_p[g] again
+            tc_fence_before();
         }
         tc_fence_before();
     }
@@ -783,9 +846,12 @@ gk_status attn_fwd_tc(gk_ctx* ctx, const void* qkv, void* y, float* lse, int B, 
         cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FWD_SMEM_BYTES);
         attr = true;
     }
-    dim3 grid((unsigned)(B * H), (unsigned)cdiv(cdiv(T, QT), 2));
+    // persistent: one CTA per SM (each holds all 512 TMEM columns) over the work items
+    const int BH = B * H, n_items = BH * (int)cdiv(cdiv(T, QT), 2);
+    if (n_items == 0) return GK_OK;
+    const int grid = std::min(n_items, ctx->num_sms);
     attn_fwd_tc_kernel<<<grid, FWD_THREADS, FWD_SMEM_BYTES, ctx->stream>>>(map, static_cast<__nv_bfloat16*>(y), lse,
-                                                                         T, H, ctx->d_err);
+                                                                         T, H, BH, n_items, ctx->d_err);
     return launched(ctx, "attn_fwd_tc");
 }
 

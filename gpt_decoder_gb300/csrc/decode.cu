@@ -65,7 +65,19 @@ __device__ __forceinline__ void row_stats(const float* __restrict__ X, int64_t l
         const float* xr = X + (int64_t)b * ldx;
         const float sh = xr[0];
         float s = 0.f, q = 0.f;
-        for (int k = lane; k < K; k += 32) {
+        int k = lane;
+        for (; k + 224 < K; k += 256) {  // eight loads in flight per lane
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = xr[k + 32 * u];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float d = v[u] - sh;
+                s += d;
+                q = fmaf(d, d, q);
+            }
+        }
+        for (; k < K; k += 32) {
             const float d = xr[k] - sh;
             s += d;
             q = fmaf(d, d, q);
@@ -209,23 +221,39 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
     __threadfence();
     const int pos = a.cache ? a.state[0] : 0;
     const int C = a.H * a.hs;
-    for (int e = threadIdx.x; e < a.B * GEMV_COLS; e += GEMV_THREADS) {
-        const int b = e / GEMV_COLS, nn = blockIdx.x * GEMV_COLS + e % GEMV_COLS;
-        if (nn >= a.M) continue;
-        // the slices in slice order, eight loads in flight at a time
-        const float* src = a.partial + (int64_t)b * a.M + nn;
-        const int64_t step = (int64_t)a.B * a.M;
-        const int S = (int)gridDim.y;
-        float t = 0.f;
-        int q = 0;
-        for (; q + 8 <= S; q += 8) {
-            float v[8];
+    // this thread's outputs e = threadIdx.x + 256 i (row e / 128, column e % 128 of the block);
+    // each adds the slices in slice order, the loads of all its outputs for four slices in
+    // flight together
+    constexpr int EPT = NB >= 2 ? NB / 2 : 1;
+    const int S = (int)gridDim.y;
+    const int64_t step = (int64_t)a.B * a.M;
+    float tsum[EPT];
+    const float* src[EPT];
+    bool valid[EPT];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (q + u) * step);
+    for (int i = 0; i < EPT; ++i) {
+        const int e = threadIdx.x + GEMV_THREADS * i, b = e / GEMV_COLS, nn = blockIdx.x * GEMV_COLS + e % GEMV_COLS;
+        valid[i] = e < NB * GEMV_COLS && b < a.B && nn < a.M;
+        src[i] = a.partial + (int64_t)b * a.M + nn;
+        tsum[i] = 0.f;
+    }
+    for (int q = 0; q < S; q += 4) {
+        float v[EPT][4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) t += v[u];
-        }
-        for (; q < S; ++q) t += __ldcg(src + q * step);
+        for (int i = 0; i < EPT; ++i)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[i][u] = (valid[i] && q + u < S) ? __ldcg(src[i] + (q + u) * step) : 0.f;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (q + u < S) tsum[i] += v[i][u];
+    }
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+        if (!valid[i]) continue;
+        const int e = threadIdx.x + GEMV_THREADS * i, b = e / GEMV_COLS, nn = blockIdx.x * GEMV_COLS + e % GEMV_COLS;
+        float t = tsum[i];
         if (a.bias) t += a.bias[nn];
         if (a.residual) t += a.residual[(int64_t)b * a.ldy + nn];
         if (a.act == GK_ACT_GELU) {
@@ -667,7 +695,11 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
     int B = kv->B;
     int colblocks = (int)cdiv(M, GEMV_COLS);
     GK_REQUIRE(ctx, colblocks <= 1024, GK_ERR_UNSUPPORTED, "decode gemv: %d columns", M);
-    int S = (int)std::max<int64_t>(1, std::min<int64_t>(K / 8, cdiv(2 * ctx->num_sms, colblocks)));
+    // K slices: enough blocks for two per SM; at wide batches (more arithmetic per weight row,
+    // and every slice adds B x 128 partial sums for the finishing block to read) each slice
+    // keeps at least 64 rows
+    const int min_rows = B >= 4 ? 64 : 8;
+    int S = (int)std::max<int64_t>(1, std::min<int64_t>(K / min_rows, cdiv(2 * ctx->num_sms, colblocks)));
     int kslice = (int)cdiv(K, S);
     S = (int)cdiv(K, kslice);
     GK_REQUIRE(ctx, (size_t)S * B * M <= kv->partial_floats, GK_ERR_WORKSPACE, "decode gemv: partial buffer too small");

@@ -53,6 +53,7 @@ struct TcParams {
     int M, N, K;
     int tiles_m, tiles_n, splits, kbps, kblocks;
     int pair, tiles_m2;  // CTA pairs: a unit is a 256-row tile pair; tiles_m2 = ceil(tiles_m / 2)
+    int n_fast;          // tile order: column tiles of a row block consecutive (else row tiles)
     int a_kmajor, b_kmajor;
     void* C;
     int64_t ldc;
@@ -295,26 +296,28 @@ __device__ __forceinline__ void epi_finish(const TcParams& p, int64_t m, int64_t
 // the same units; tm is this CTA's own 128-row tile.
 __device__ __forceinline__ int unit_first(const TcParams& p) { return p.pair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x; }
 __device__ __forceinline__ int unit_step(const TcParams& p) { return p.pair ? (int)(gridDim.x >> 1) : (int)gridDim.x; }
+// BATCH: the kernel may run a batch of products (p.nz > 1; only the float32-operand kernels are
+// built for it, so the others keep no trace of the batch arithmetic).
+template <bool BATCH>
 __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, int& tn, int& kb0, int& kb1) {
     int split = u % p.splits, tile = u / p.splits;
-    if (p.nz > 1) tile %= p.tiles_m * p.tiles_n;  // the tile within its product of the batch
-    if (p.pair) {
-        tm = (tile % p.tiles_m2) * 2 + (int)(blockIdx.x & 1);
-        tn = tile / p.tiles_m2;
-    } else {
-        tm = tile % p.tiles_m;
-        tn = tile / p.tiles_m;
-    }
+    if (BATCH && p.nz > 1) tile %= p.tiles_m * p.tiles_n;  // the tile within its product of the batch
+    const int rows = p.pair ? p.tiles_m2 : p.tiles_m;
+    const int tr = p.n_fast ? tile / p.tiles_n : tile % rows;
+    tn = p.n_fast ? tile % p.tiles_n : tile / rows;
+    tm = p.pair ? tr * 2 + (int)(blockIdx.x & 1) : tr;
     kb0 = split * p.kbps;
     kb1 = min(p.kblocks, kb0 + p.kbps);
 }
 
 // Batch position of unit u, and the TMA coordinate shift of operand o along c (0 = x, 1 = y).
+template <bool BATCH>
 __device__ __forceinline__ int unit_z(const TcParams& p, int u) {
-    return p.nz > 1 ? (u / p.splits) / (p.tiles_m * p.tiles_n) : 0;
+    return BATCH && p.nz > 1 ? (u / p.splits) / (p.tiles_m * p.tiles_n) : 0;
 }
+template <bool BATCH>
 __device__ __forceinline__ int zshift(const TcParams& p, int o, int c, int zl) {
-    if (p.nz <= 1) return 0;
+    if (!BATCH || p.nz <= 1) return 0;
     const int zg = p.z0 + zl;
     return (zg % p.zh) * p.zo[o][c][0] + (zg / p.zh) * p.zo[o][c][1] + zl * p.zo[o][c][2];
 }
@@ -333,16 +336,16 @@ __device__ __forceinline__ int epi_chunks(const TcParams& p, int tm, int tn, int
 }
 
 // Advance (u, ch) to this warp's next chunk, possibly in a later unit of this CTA.
-template <typename TC>
+template <typename TC, bool BATCH>
 __device__ __forceinline__ bool epi_next(const TcParams& p, int units, int& u, int& ch, int q, int half) {
     int tm, tn, kb0, kb1;
-    unit_coords(p, u, tm, tn, kb0, kb1);
+    unit_coords<BATCH>(p, u, tm, tn, kb0, kb1);
     if (ch + 1 < epi_chunks<TC>(p, tm, tn, q, half)) {
         ++ch;
         return true;
     }
     for (int v = u + unit_step(p); v < units; v += unit_step(p)) {
-        unit_coords(p, v, tm, tn, kb0, kb1);
+        unit_coords<BATCH>(p, v, tm, tn, kb0, kb1);
         if (epi_chunks<TC>(p, tm, tn, q, half) > 0) {
             u = v;
             ch = 0;
@@ -426,7 +429,7 @@ __device__ __forceinline__ void release_accumulator(const TcParams& p, uint64_t*
     }
 }
 
-template <typename TC>
+template <typename TC, bool BATCH>
 __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slots, uint64_t* inbar, uint64_t* tfull,
                              uint64_t* tempty, volatile int* abort_flag, uint32_t tmem_base, int warp, int lane,
                              int units) {
@@ -445,7 +448,7 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
         bool any = false;
         for (int v = unit_first(p); v < units && !any; v += unit_step(p)) {
             int tm, tn, kb0, kb1;
-            unit_coords(p, v, tm, tn, kb0, kb1);
+            unit_coords<BATCH>(p, v, tm, tn, kb0, kb1);
             if (epi_chunks<TC>(p, tm, tn, q, half) > 0) {
                 u0 = v;
                 c0 = 0;
@@ -454,7 +457,7 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
         }
         if (any) {
             int tm, tn, kb0, kb1;
-            unit_coords(p, u0, tm, tn, kb0, kb1);
+            unit_coords<BATCH>(p, u0, tm, tn, kb0, kb1);
             mbar_expect_tx(&inbar[0], SLOT);
             tma_load_2d(mp.in, &inbar[0], slots, tn * BN + half * (BN / 2) + c0 * W, tm * BM + q * 32);
             pend_slot = 0;
@@ -465,7 +468,7 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
     uint32_t j = 0;
     for (int u = unit_first(p); u < units && ok; u += unit_step(p), ++j) {
         int tm, tn, kb0, kb1;
-        unit_coords(p, u, tm, tn, kb0, kb1);
+        unit_coords<BATCH>(p, u, tm, tn, kb0, kb1);
         const uint32_t buf = j & 1, aph = (j >> 1) & 1;
         // warp-uniform outcome: every lane leaves together or none does
         if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], aph, abort_flag, WAIT_NS))) {
@@ -477,13 +480,13 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
         // warm L2 with the next unit's input while this tile drains
         if (has_in && lane == 0 && u + unit_step(p) < units) {
             int tm2, tn2, a2, b2;
-            unit_coords(p, u + unit_step(p), tm2, tn2, a2, b2);
+            unit_coords<BATCH>(p, u + unit_step(p), tm2, tn2, a2, b2);
             const int n2 = epi_chunks<TC>(p, tm2, tn2, q, half);
             for (int c = 0; c < n2; ++c)
                 tma_prefetch_l2_2d(mp.in, tn2 * BN + half * (BN / 2) + c * W, tm2 * BM + q * 32);
         }
         const int y = tm * BM + q * 32;
-        const int zl = unit_z(p, u), cxs = zshift(p, 2, 0, zl), cys = zshift(p, 2, 1, zl);  // batch: C's shift
+        const int zl = unit_z<BATCH>(p, u), cxs = zshift<BATCH>(p, 2, 0, zl), cys = zshift<BATCH>(p, 2, 1, zl);  // batch: C's shift
         // fused cross-entropy: this lane's row (y + lane) state over the tile's columns
         float ce_m = -INFINITY, ce_s = 0.f, ce_l2 = 0.f, ce_g = 0.f;
         int ce_t = -1;
@@ -500,9 +503,9 @@ __device__ bool epilogue_tma(const TcParams& p, const EpiMaps& mp, uint8_t* slot
             // the next chunk's input goes into the other slot once its last store has read it
             if (has_in && lane == 0) {
                 int nu = u, nc = ch;
-                if (epi_next<TC>(p, units, nu, nc, q, half)) {
+                if (epi_next<TC, BATCH>(p, units, nu, nc, q, half)) {
                     int tm2, tn2, a2, b2;
-                    unit_coords(p, nu, tm2, tn2, a2, b2);
+                    unit_coords<BATCH>(p, nu, tm2, tn2, a2, b2);
                     bulk_wait_read<0>();
                     mbar_expect_tx(&inbar[s ^ 1], SLOT);
                     tma_load_2d(mp.in, &inbar[s ^ 1], slots + (s ^ 1) * SLOT, tn2 * BN + half * (BN / 2) + nc * W,
@@ -743,7 +746,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             for (int u = unit_first(p); u < units && ok; u += unit_step(p)) {
                 int tm, tn, kb0, kb1;
-                unit_coords(p, u, tm, tn, kb0, kb1);
+                unit_coords<F32OP>(p, u, tm, tn, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     int s = it % STAGES;
                     uint32_t ph = (it / STAGES) & 1;
@@ -763,9 +766,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     };
                     uint8_t* a = smem + s * SC::STAGE;
                     uint8_t* b = a + SC::A_SLOT;
-                    const int zl = unit_z(p, u);
-                    const int axs = zshift(p, 0, 0, zl), ays = zshift(p, 0, 1, zl);
-                    const int bxs = zshift(p, 1, 0, zl), bys = zshift(p, 1, 1, zl);
+                    const int zl = unit_z<F32OP>(p, u);
+                    const int axs = zshift<F32OP>(p, 0, 0, zl), ays = zshift<F32OP>(p, 0, 1, zl);
+                    const int bxs = zshift<F32OP>(p, 1, 0, zl), bys = zshift<F32OP>(p, 1, 1, zl);
 #pragma unroll
                     for (int pl = 0; pl < (SC::A_LO ? 2 : 1); ++pl) {
                         const CUtensorMap* ma = pl ? &tmA_lo : &tmA;
@@ -826,7 +829,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true, issued = false;
         for (int u = unit_first(p); u < units && ok; u += unit_step(p), ++j) {
             int tm, tn, kb0, kb1;
-            unit_coords(p, u, tm, tn, kb0, kb1);
+            unit_coords<F32OP>(p, u, tm, tn, kb0, kb1);
             uint32_t buf = j & 1, aph = (j >> 1) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&tempty[buf], aph ^ 1, abort_flag, WAIT_NS))) {
                 ok = false;
@@ -895,7 +898,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         EpiMaps mp{&tmC, &tmAux, &tmLo,
                    p.in_kind == IN_C ? &tmC : p.in_kind == IN_RES ? &tmR : p.in_kind == IN_AUX ? &tmAux : nullptr};
         uint8_t* slots = reinterpret_cast<uint8_t*>(epi_stage) + (warp - 2) * 2 * SLOT;
-        if (!epilogue_tma<TC>(p, mp, slots, inbars + 2 * (warp - 2), tfull, tempty, abort_flag, tmem_base, warp, lane,
+        if (!epilogue_tma<TC, F32OP>(p, mp, slots, inbars + 2 * (warp - 2), tfull, tempty, abort_flag, tmem_base, warp, lane,
                               units)) {
             *abort_flag = 1;
             report(p.err, GK_ERR_TIMEOUT);
@@ -908,7 +911,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t j = 0;
         for (int u = unit_first(p); u < units; u += unit_step(p), ++j) {
             int tm, tn, kb0, kb1;
-            unit_coords(p, u, tm, tn, kb0, kb1);
+            unit_coords<F32OP>(p, u, tm, tn, kb0, kb1);
             uint32_t buf = j & 1, aph = (j >> 1) & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], aph, abort_flag, WAIT_NS))) {
                 *abort_flag = 1;
@@ -1130,6 +1133,12 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.tiles_m = (int)cdiv(g.M, BM);
     p.tiles_n = (int)cdiv(g.N, BN);
     p.tiles_m2 = (int)cdiv(p.tiles_m, 2);
+    // Units run in waves of one per CTA (pair), in unit order. With few column tiles and A the
+    // larger operand (M > N: activations against weights, or the LM head's dlogits), the column
+    // tiles of a row block go consecutively, so the CTAs that need a block of A rows load it
+    // at the same time and A comes from DRAM once; in row order each column tile would stream
+    // all of A again.
+    p.n_fast = g.M > g.N && p.tiles_n <= 8;
     p.kblocks = (int)cdiv(g.K, f32op ? BK / 2 : BK);
     p.a_kmajor = g.a_kmajor;
     p.b_kmajor = g.b_kmajor;

@@ -186,12 +186,24 @@ __global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, doubl
     }
 }
 
-// y[0] = sum of part[0 .. P) in index order
-__global__ void sum_finish_kernel(const double* __restrict__ part, int P, float* __restrict__ y) {
-    if (threadIdx.x != 0) return;
+// y[0] = sum of part[0 .. P): thread t adds part[t], part[t + 256], ... in index order, then
+// the 256 thread sums are combined in a fixed tree (lane xor-tree, then warps in order). The
+// order depends only on P, so the result is deterministic; one thread walking all P partials
+// would wait out P / 4 dependent L2 round trips.
+constexpr int SUM_FINISH_THREADS = 256;
+__global__ void __launch_bounds__(SUM_FINISH_THREADS) sum_finish_kernel(const double* __restrict__ part, int P,
+                                                                      float* __restrict__ y) {
+    __shared__ double red[SUM_FINISH_THREADS / 32];
     double t = 0.0;
-    for (int p = 0; p < P; ++p) t += part[p];
-    *y = (float)t;
+    for (int p = threadIdx.x; p < P; p += SUM_FINISH_THREADS) t += part[p];
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double s = 0.0;
+        for (int w = 0; w < SUM_FINISH_THREADS / 32; ++w) s += red[w];
+        *y = (float)s;
+    }
 }
 
 // da (+)= g[0] for every element
@@ -337,7 +349,7 @@ gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n) {
     GK_REQUIRE(ctx, part, GK_ERR_WORKSPACE, "gk_sum_fwd: needs %zu workspace bytes", (size_t)P * sizeof(double));
     sum_partial_kernel<<<P, EW_THREADS, 0, ctx->stream>>>(a, n, part, vec4(a));
     GK_TRY(launched(ctx, "sum_partial"));
-    sum_finish_kernel<<<1, 32, 0, ctx->stream>>>(part, P, y);
+    sum_finish_kernel<<<1, SUM_FINISH_THREADS, 0, ctx->stream>>>(part, P, y);
     return launched(ctx, "sum_finish");
 }
 

@@ -77,32 +77,55 @@ __global__ void __launch_bounds__(COLSUM_WARPS * 32)
     }
 }
 
-// dst[c] += sum_s partial[s][c]: 8 warps per 32 columns, warp w sums slots w, w + 8, ...,
-// then the warp sums are added in warp order (fixed order, deterministic).
-__global__ void __launch_bounds__(256) colsum_reduce_kernel(const float* __restrict__ partial, int splits,
-                                                           int64_t cols, float* dst) {
-    __shared__ float red[8][32];
-    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int64_t c = (int64_t)blockIdx.x * 32 + lane;
-    float a = 0.f;
-    if (c < cols)
-        for (int s = warp; s < splits; s += 8) a += partial[(int64_t)s * cols + c];
-    red[warp][lane] = a;
+// dst[c] += sum_s partial[s][c]: 32 warps per 32 columns, warp w sums slots w, w + 32, ...
+// (four independent running sums, so four loads are in flight), then the warp sums are added
+// in warp order (fixed order, deterministic).
+constexpr int COLSUM_RED_WARPS = 32;
+__global__ void __launch_bounds__(COLSUM_RED_WARPS * 32)
+    colsum_reduce_kernel(const float* __restrict__ partial, int splits, int64_t cols, float* dst) {
+    __shared__ float red[COLSUM_RED_WARPS][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t c = (int64_t)blockIdx.x * 32 + lane;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    if (c < cols) {
+        int s = warp;
+        for (; s + 3 * COLSUM_RED_WARPS < splits; s += 4 * COLSUM_RED_WARPS)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a[u] += partial[(int64_t)(s + u * COLSUM_RED_WARPS) * cols + c];
+        for (; s < splits; s += COLSUM_RED_WARPS) a[0] += partial[(int64_t)s * cols + c];
+    }
+    red[warp][lane] = (a[0] + a[1]) + (a[2] + a[3]);
     __syncthreads();
     if (warp == 0 && c < cols) {
         float t = 0.f;
-        for (int w = 0; w < 8; ++w) t += red[w][lane];
+        for (int w = 0; w < COLSUM_RED_WARPS; ++w) t += red[w][lane];
         dst[c] += t;
     }
+}
+
+// Resident blocks of colsum_partial_kernel<T> per SM (the grid is sized to one full wave).
+template <typename T>
+int colsum_blocks_per_sm() {
+    static int n = 0;
+    if (n == 0) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, colsum_partial_kernel<T>, COLSUM_WARPS * 32, 0) !=
+                cudaSuccess || b < 1)
+            b = 1;
+        n = b;
+    }
+    return n;
 }
 
 }  // namespace
 
 gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_t rows, int64_t cols, float* dst) {
-    // enough blocks of 8 warps to keep every SM loading: about four per SM
+    // one full wave of resident blocks (a second, partial wave would leave most SMs idle
+    // while it drains)
     const int64_t col_blocks = cdiv(cols, 256);
-    int splits = (int)std::max<int64_t>(1, std::min<int64_t>({cdiv((int64_t)ctx->num_sms * 4, col_blocks),
-                                                               cdiv(rows, COLSUM_WARPS), 1024}));
+    const int64_t resident =
+        (int64_t)ctx->num_sms * (dtype == GK_F32 ? colsum_blocks_per_sm<float>() : colsum_blocks_per_sm<__nv_bfloat16>());
+    int splits = (int)std::max<int64_t>(1, std::min<int64_t>({resident / col_blocks, cdiv(rows, COLSUM_WARPS), 1024}));
     float* partial = (float*)workspace(ctx, (size_t)splits * cols * sizeof(float));
     GK_REQUIRE(ctx, partial, GK_ERR_WORKSPACE, "bias gradient needs %lld workspace bytes",
                (long long)splits * cols * 4);
@@ -117,7 +140,8 @@ gk_status colsum_add(gk_ctx* ctx, const void* src, int64_t ld, int dtype, int64_
         colsum_partial_kernel<__nv_bfloat16><<<grid, COLSUM_WARPS * 32, 0, ctx->stream>>>(
             (const __nv_bfloat16*)src, ld, rows, cols, vec, partial);
     GK_TRY(launched(ctx, "colsum_partial"));
-    colsum_reduce_kernel<<<(unsigned)cdiv(cols, 32), 256, 0, ctx->stream>>>(partial, splits, cols, dst);
+    colsum_reduce_kernel<<<(unsigned)cdiv(cols, 32), COLSUM_RED_WARPS * 32, 0, ctx->stream>>>(partial, splits, cols,
+                                                                                             dst);
     return launched(ctx, "colsum_reduce");
 }
 

@@ -521,11 +521,14 @@ __global__ void __launch_bounds__(256) layernorm_bwd_cols_kernel(const float* __
 
 // out_k[c] += sum_p partial[p][k][c] for k < np (out_0 = dgamma, out_1 = dbeta, out_2 = the
 // column sums of dx; a null output is skipped). Block (x, k) takes 32 columns of array k:
-// warp w sums slots w, w + 8, ... with four independent running sums (slot order fixed),
-// then the 8 warp sums are added in warp order: a fixed summation order.
-__global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __restrict__ partial, int nparts, int np,
-                                                             int C, float* out0, float* out1, float* out2) {
-    __shared__ float red[8][32];
+// warp w sums slots w, w + 32, ... with four independent running sums (slot order fixed),
+// then the 32 warp sums are added in warp order: a fixed summation order. With 32 warps a
+// warp has few slots, so the reduction is a few load round trips long.
+constexpr int RP_WARPS = 32;
+__global__ void __launch_bounds__(RP_WARPS * 32) reduce_partials_kernel(const float* __restrict__ partial, int nparts,
+                                                                       int np, int C, float* out0, float* out1,
+                                                                       float* out2) {
+    __shared__ float red[RP_WARPS][32];
     int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int k = blockIdx.y, c = blockIdx.x * 32 + lane;
     float* out = k == 0 ? out0 : k == 1 ? out1 : out2;
@@ -535,19 +538,19 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(const float* __res
         const float* src = partial + (int64_t)k * C + c;
         const int64_t step = (int64_t)np * C;
         int p = warp;
-        for (; p + 24 < nparts; p += 32) {
+        for (; p + 3 * RP_WARPS < nparts; p += 4 * RP_WARPS) {
             a0 += src[p * step];
-            a1 += src[(p + 8) * step];
-            a2 += src[(p + 16) * step];
-            a3 += src[(p + 24) * step];
+            a1 += src[(p + RP_WARPS) * step];
+            a2 += src[(p + 2 * RP_WARPS) * step];
+            a3 += src[(p + 3 * RP_WARPS) * step];
         }
-        for (; p < nparts; p += 8) a0 += src[p * step];
+        for (; p < nparts; p += RP_WARPS) a0 += src[p * step];
     }
     red[warp][lane] = (a0 + a1) + (a2 + a3);
     __syncthreads();
     if (warp == 0 && c < C) {
         float t = 0.f;
-        for (int w = 0; w < 8; ++w) t += red[w][lane];
+        for (int w = 0; w < RP_WARPS; ++w) t += red[w][lane];
         out[c] += t;
     }
 }
@@ -1119,7 +1122,7 @@ gk_status gk_layernorm_bwd(gk_ctx* ctx, const float* x, const float* gamma, cons
     }
     GK_TRY(launched(ctx, "layernorm_bwd"));
     if (want_partials) {
-        reduce_partials_kernel<<<dim3((unsigned)cdiv(C, 32), (unsigned)np), 256, 0, ctx->stream>>>(
+        reduce_partials_kernel<<<dim3((unsigned)cdiv(C, 32), (unsigned)np), RP_WARPS * 32, 0, ctx->stream>>>(
             partial, nparts, np, C, dgamma, dbeta, dx_colsum);
         GK_TRY(launched(ctx, "layernorm_bwd_reduce"));
     }
@@ -1332,7 +1335,7 @@ extern "C" gk_status gk_layernorm_bwd_noalloc(void* cuda_stream, const float* x,
     if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
     if (want_partials) {
         // every slot the reduction reads was written in full by the kernel above
-        reduce_partials_kernel<<<dim3((unsigned)cdiv(C, 32), 2), 256, 0, stream>>>(partial, nparts, 2, C, dgamma,
+        reduce_partials_kernel<<<dim3((unsigned)cdiv(C, 32), 2), RP_WARPS * 32, 0, stream>>>(partial, nparts, 2, C, dgamma,
                                                                                   dbeta, nullptr);
         if (cudaGetLastError() != cudaSuccess) return GK_ERR_CUDA;
     }

@@ -677,52 +677,65 @@ __global__ void __launch_bounds__(256) softmax_ce_fwd_warp_kernel(const float* _
     }
 }
 
-// Wide rows (V <= 512 * 4 * 25; any width and offset, 16-byte aligned base) held in
-// registers: one 512-thread block per row with every piece of the row requested at once; the
-// maximum, then the sum of exp(x - max), both from registers (one read of each logit).
-constexpr int CER_THREADS = 512, CER_V4 = 25;
-__global__ void __launch_bounds__(CER_THREADS, 1) softmax_ce_fwd_reg_kernel(const float* __restrict__ logits,
-                                                                            int64_t ldl,
-                                                                            const int32_t* __restrict__ targets,
-                                                                            float* __restrict__ lse_out,
-                                                                            float* __restrict__ row_loss, int64_t rows,
-                                                                            int V, int* err) {
-    __shared__ float red[CER_THREADS / 32];
+// Wide rows streamed once: one 256-thread block per row (several blocks per SM, so the loads
+// of one row overlap the reductions of others). Each thread keeps a running maximum m and a
+// sum s of exp(x - m) over its elements, eight float4 pieces at a time (s is rescaled by
+// exp(m_old - m_new) when a piece raises the maximum); the threads' (m, s) pairs are combined
+// in a fixed tree (lanes, then warps in order), lse = m + log(s). Same result as the two-pass
+// form up to float32 rounding; DRAM sees one read per element.
+constexpr int CES_THREADS = 256, CES_U = 8;
+__device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
+    const float M = fmaxf(m, m2);
+    if (M == -INFINITY) return;  // both empty
+    s = s * expf(m - M) + s2 * expf(m2 - M);
+    m = M;
+}
+__global__ void __launch_bounds__(CES_THREADS) softmax_ce_fwd_stream_kernel(const float* __restrict__ logits,
+                                                                          int64_t ldl,
+                                                                          const int32_t* __restrict__ targets,
+                                                                          float* __restrict__ lse_out,
+                                                                          float* __restrict__ row_loss, int64_t rows,
+                                                                          int V, int* err) {
+    __shared__ float2 red[CES_THREADS / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const float* xr = logits + row * ldl;
         const RowCut cut(xr, V);
         const float4* xb = reinterpret_cast<const float4*>(xr + cut.head);
-        float4 v[CER_V4];
-#pragma unroll
-        for (int i = 0; i < CER_V4; ++i) {
-            const int q = threadIdx.x + i * CER_THREADS;
-            v[i] = q < cut.nb ? xb[q] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
         const int ei = cut.edge_index(threadIdx.x);
-        const float ev = ei >= 0 ? xr[ei] : -INFINITY;
-        float m = ev;
+        float m = ei >= 0 ? xr[ei] : -INFINITY;
+        float s = ei >= 0 ? 1.f : 0.f;
+        for (int q0 = threadIdx.x; q0 < cut.nb; q0 += CES_U * CES_THREADS) {
+            float4 v[CES_U];
 #pragma unroll
-        for (int i = 0; i < CER_V4; ++i) m = fmaxf(m, fmaxf(fmaxf(v[i].x, v[i].y), fmaxf(v[i].z, v[i].w)));
-        m = warp_max(m);
-        __syncthreads();
-        if (lane == 0) red[warp] = m;
-        __syncthreads();
-        m = red[0];
-        for (int w = 1; w < CER_THREADS / 32; ++w) m = fmaxf(m, red[w]);
-        float sum = ei >= 0 ? expf(ev - m) : 0.f;
+            for (int u = 0; u < CES_U; ++u) {
+                const int q = q0 + u * CES_THREADS;
+                v[u] = q < cut.nb ? xb[q] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            float cm = m;
 #pragma unroll
-        for (int i = 0; i < CER_V4; ++i)
-            if (threadIdx.x + i * CER_THREADS < cut.nb)
-                sum += (expf(v[i].x - m) + expf(v[i].y - m)) + (expf(v[i].z - m) + expf(v[i].w - m));
-        sum = warp_sum(sum);
-        __syncthreads();
-        if (lane == 0) red[warp] = sum;
+            for (int u = 0; u < CES_U; ++u) cm = fmaxf(cm, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+            if (cm == -INFINITY) continue;  // nothing in this piece yet
+            s *= expf(m - cm);  // 0 while s = 0 and m = -inf: exp(-inf) = 0
+            m = cm;
+            float t = 0.f;
+#pragma unroll
+            for (int u = 0; u < CES_U; ++u)
+                t += (expf(v[u].x - m) + expf(v[u].y - m)) + (expf(v[u].z - m) + expf(v[u].w - m));
+            s += t;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            lse_combine(m, s, m2, s2);
+        }
+        __syncthreads();  // the previous row's reads of red are done
+        if (lane == 0) red[warp] = make_float2(m, s);
         __syncthreads();
         if (threadIdx.x == 0) {
-            float t = 0.f;
-            for (int w = 0; w < CER_THREADS / 32; ++w) t += red[w];
-            const float lse = m + logf(t);
+            float M = red[0].x, S = red[0].y;
+            for (int w = 1; w < CES_THREADS / 32; ++w) lse_combine(M, S, red[w].x, red[w].y);
+            const float lse = M + logf(S);
             lse_out[row] = lse;
             int tg = targets[row];
             if (tg < 0 || tg >= V) {
@@ -732,6 +745,19 @@ __global__ void __launch_bounds__(CER_THREADS, 1) softmax_ce_fwd_reg_kernel(cons
             row_loss[row] = lse - xr[tg];
         }
     }
+}
+
+// Resident blocks of softmax_ce_fwd_stream_kernel per SM.
+int ce_stream_blocks_per_sm() {
+    static int n = 0;
+    if (n == 0) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, softmax_ce_fwd_stream_kernel, CES_THREADS, 0) !=
+                cudaSuccess || b < 1)
+            b = 1;
+        n = b;
+    }
+    return n;
 }
 
 // loss = (sum over rows, in order, in float64) / rows; one block.
@@ -1164,9 +1190,10 @@ gk_status gk_softmax_ce_fwd(gk_ctx* ctx, const float* logits, int64_t ldl, const
     if (V <= 4096 && al)
         softmax_ce_fwd_warp_kernel<<<(unsigned)cdiv(rows, 8), 256, 0, ctx->stream>>>(logits, ldl, targets, lse, row_loss,
                                                                                     rows, V, ctx->d_err);
-    else if (aligned16(logits) && V <= CER_THREADS * CER_V4 * 4)
-        softmax_ce_fwd_reg_kernel<<<(unsigned)std::min<int64_t>(rows, (int64_t)ctx->num_sms * 2), CER_THREADS, 0,
-                                    ctx->stream>>>(logits, ldl, targets, lse, row_loss, rows, V, ctx->d_err);
+    else if (aligned16(logits))
+        softmax_ce_fwd_stream_kernel<<<(unsigned)std::min<int64_t>(rows, (int64_t)ctx->num_sms * ce_stream_blocks_per_sm()),
+                                       CES_THREADS, 0, ctx->stream>>>(logits, ldl, targets, lse, row_loss, rows, V,
+                                                                      ctx->d_err);
     else
         softmax_ce_fwd_kernel<<<(unsigned)rows, CE_THREADS, 0, ctx->stream>>>(logits, ldl, targets, lse, row_loss, V,
                                                                              ctx->d_err);

@@ -59,6 +59,34 @@ __device__ __forceinline__ int64_t cache_index(int l, int kv, int b, int h, int 
 // kernels that consume its output.
 __device__ __forceinline__ void row_stats(const float* __restrict__ X, int64_t ldx, int B, int K, float* st) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (K % 128 == 0 && K <= 1024 && ldx % 4 == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0) {
+        // the whole row in registers (K / 128 float4 per lane, all requested at once): the
+        // mean, then the variance of the deviations from it
+        for (int b = warp; b < B; b += nw) {
+            const float4* xr = reinterpret_cast<const float4*>(X + (int64_t)b * ldx);
+            const int n4 = K / 128;
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = i < n4 ? xr[lane + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+            const float mu = warp_sum(s) / K;
+            float q = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < n4) {
+                    const float a = v[i].x - mu, c = v[i].y - mu, d = v[i].z - mu, e = v[i].w - mu;
+                    q += (a * a + c * c) + (d * d + e * e);
+                }
+            const float var = warp_sum(q) / K;
+            if (lane == 0) {
+                st[2 * b] = mu;
+                st[2 * b + 1] = rsqrtf(var + 1e-5f);
+            }
+        }
+        return;
+    }
     for (int b = warp; b < B; b += nw) {
         // one pass over the row, shifted by its first element so that E[d^2] - E[d]^2 does
         // not cancel when the mean is large against the spread
@@ -698,7 +726,9 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
     // K slices: enough blocks for two per SM; at wide batches (more arithmetic per weight row,
     // and every slice adds B x 128 partial sums for the finishing block to read) each slice
     // keeps at least 64 rows
-    const int min_rows = B >= 4 ? 64 : 8;
+    // (at least 128 rows for long K at wide batches: the finishing block reads S x B x 128
+    // partial sums, S / 4 rounds of loads)
+    const int min_rows = B >= 4 ? (K >= 2048 ? 128 : 64) : 8;
     int S = (int)std::max<int64_t>(1, std::min<int64_t>(K / min_rows, cdiv(2 * ctx->num_sms, colblocks)));
     int kslice = (int)cdiv(K, S);
     S = (int)cdiv(K, kslice);

@@ -32,11 +32,15 @@ constexpr uint32_t TMEM_COLS = 2 * BN;            // two float32 accumulators of
 // Stage layout per mode: bit 0 = A has a low bf16 plane, bit 1 = B has one; mode PAIR_MODE is
 // a CTA pair sharing 256 x 256 tiles (each CTA holds its 128 rows of A and 128 of the 256
 // columns of B). A stage holds [A_hi | A_lo? | B_hi | B_lo?]; the ring is as deep as 227 KB of
-// shared memory allows.
-constexpr int PAIR_MODE = 4;
+// shared memory allows. PAIR4_MODE: clusters of two pairs on tiles with the same columns (B):
+// each CTA loads its A rows and half of its B columns, and multicasts that half to the CTA of
+// the other pair that needs the same columns, so a CTA requests 24 of the 32 KB it receives per
+// stage.
+constexpr int PAIR_MODE = 4, PAIR4_MODE = 5;
 template <int SPLIT>
 struct StageCfg {
-    static constexpr bool PAIR = SPLIT == PAIR_MODE;
+    static constexpr bool MC = SPLIT == PAIR4_MODE;
+    static constexpr bool PAIR = SPLIT == PAIR_MODE || MC;
     static constexpr bool A_LO = !PAIR && (SPLIT & 1) != 0, B_LO = !PAIR && (SPLIT & 2) != 0;
     static constexpr uint32_t A_SLOT = A_BYTES * (A_LO ? 2 : 1);
     static constexpr uint32_t B_TILE = PAIR ? B_BYTES / 2 : B_BYTES;  // the B columns this CTA loads
@@ -54,6 +58,7 @@ struct TcParams {
     int tiles_m, tiles_n, splits, kbps, kblocks;
     int pair, tiles_m2;  // CTA pairs: a unit is a 256-row tile pair; tiles_m2 = ceil(tiles_m / 2)
     int n_fast;          // tile order: column tiles of a row block consecutive (else row tiles)
+    int mc, tiles_m4;    // clusters of two pairs: a unit is two pair tiles in one column block
     int a_kmajor, b_kmajor;
     void* C;
     int64_t ldc;
@@ -294,18 +299,24 @@ __device__ __forceinline__ void epi_finish(const TcParams& p, int64_t m, int64_t
 
 // Units of work of this CTA: u = unit_first(p), + unit_step(p), ... Both CTAs of a pair walk
 // the same units; tm is this CTA's own 128-row tile.
-__device__ __forceinline__ int unit_first(const TcParams& p) { return p.pair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x; }
-__device__ __forceinline__ int unit_step(const TcParams& p) { return p.pair ? (int)(gridDim.x >> 1) : (int)gridDim.x; }
+__device__ __forceinline__ int unit_first(const TcParams& p) {
+    return p.mc ? (int)(blockIdx.x >> 2) : p.pair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+}
+__device__ __forceinline__ int unit_step(const TcParams& p) {
+    return p.mc ? (int)(gridDim.x >> 2) : p.pair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+}
 // BATCH: the kernel may run a batch of products (p.nz > 1; only the float32-operand kernels are
 // built for it, so the others keep no trace of the batch arithmetic).
 template <bool BATCH>
 __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int& tm, int& tn, int& kb0, int& kb1) {
     int split = u % p.splits, tile = u / p.splits;
     if (BATCH && p.nz > 1) tile %= p.tiles_m * p.tiles_n;  // the tile within its product of the batch
-    const int rows = p.pair ? p.tiles_m2 : p.tiles_m;
+    const int rows = p.mc ? p.tiles_m4 : p.pair ? p.tiles_m2 : p.tiles_m;
     const int tr = p.n_fast ? tile / p.tiles_n : tile % rows;
     tn = p.n_fast ? tile % p.tiles_n : tile / rows;
-    tm = p.pair ? tr * 2 + (int)(blockIdx.x & 1) : tr;
+    // a cluster of two pairs takes pair rows 2 tr and 2 tr + 1 (bit 1 of the CTA's index)
+    const int tp = p.mc ? tr * 2 + (int)((blockIdx.x >> 1) & 1) : tr;
+    tm = p.pair ? tp * 2 + (int)(blockIdx.x & 1) : tp;
     kb0 = split * p.kbps;
     kb1 = min(p.kblocks, kb0 + p.kbps);
 }
@@ -423,7 +434,7 @@ __device__ __forceinline__ void release_accumulator(const TcParams& p, uint64_t*
     __syncwarp();
     if (lane == 0) {
         if (p.pair && (blockIdx.x & 1))
-            mbar_arrive_cluster_relaxed(mapa_shared(saddr(bar), 0));
+            mbar_arrive_cluster_relaxed(mapa_shared(saddr(bar), cluster_ctarank() & ~1u));
         else
             mbar_arrive(bar);
     }
@@ -705,13 +716,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 22);
 
     int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int units = (PAIR ? p.tiles_m2 : p.tiles_m) * p.tiles_n * p.splits * p.nz;
+    int units = (SC::MC ? p.tiles_m4 : PAIR ? p.tiles_m2 : p.tiles_m) * p.tiles_n * p.splits * p.nz;
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const uint32_t prank = rank & 1u, leader = rank & ~1u;  // rank within the pair, the pair's even CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], SC::MC ? 2 : 1);  // with multicast both pairs read every stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -756,8 +768,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     // a pair's stage is complete when both CTAs' copies have landed: all of them
                     // count on the even CTA's full[s], which the even CTA arms for both
-                    const uint32_t fb = PAIR ? mapa_shared(saddr(&full[s]), 0) : 0u;
-                    if (!PAIR || rank == 0) mbar_expect_tx(&full[s], PAIR ? 2 * SC::STAGE : SC::STAGE);
+                    const uint32_t fb = PAIR ? mapa_shared(saddr(&full[s]), leader) : 0u;
+                    if (!PAIR || prank == 0) mbar_expect_tx(&full[s], PAIR ? 2 * SC::STAGE : SC::STAGE);
                     auto load = [&](const CUtensorMap* map, void* dst, int x, int y) {
                         if (PAIR)
                             tma_load_2d_pair(map, fb, dst, x, y);
@@ -786,8 +798,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                         uint8_t* dst = b + pl * SC::B_TILE;
                         // this CTA's columns of the tile's B (all of them, or its half in a pair)
                         constexpr int BNC = (int)(SC::B_TILE / (BK * 2));
-                        const int n0 = tn * BN + (int)rank * BNC;
-                        if (F32OP || p.b_kmajor) {
+                        const int n0 = tn * BN + (int)prank * BNC;
+                        if constexpr (SC::MC) {
+                            // this CTA's B columns in two 64-column halves: it loads half `pair
+                            // index` for itself and the same CTA of the other pair
+                            const int j = (int)(rank >> 1);
+                            const uint16_t mask = (uint16_t)((1u << rank) | (1u << (rank ^ 2u)));
+                            if (p.b_kmajor)
+                                tma_load_2d_pair_mc(mb, fb, dst + j * 8192, kb * BK, n0 + 64 * j, mask);
+                            else
+                                tma_load_2d_pair_mc(mb, fb, dst + j * 8192, n0 + 64 * j, kb * BK, mask);
+                        } else if (F32OP || p.b_kmajor) {
                             load(mb, dst, kb * BKE + bxs, n0 + bys);
                         } else {
 #pragma unroll
@@ -802,7 +823,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 report(p.err, GK_ERR_TIMEOUT);
                 // let this CTA's copies in flight land before shared memory is released (the odd
                 // CTA of a pair cannot see their completion: it gives them a millisecond)
-                if (PAIR && rank != 0) {
+                if (PAIR && prank != 0) {
                     const uint64_t t0 = globaltimer();
                     while (globaltimer() - t0 < 1000000ull) {
                     }
@@ -812,7 +833,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
-    } else if (PAIR && warp == 1 && rank != 0) {
+    } else if (PAIR && warp == 1 && prank != 0) {
         // odd CTA of a pair: the even CTA issues the MMAs
     } else if (warp == 1) {
         // The whole warp walks the loop in step (so the descriptors stay warp-uniform) and one
@@ -869,8 +890,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     // commits track the MMAs of the thread that issues them: same lane, same block
                     if (PAIR) {
-                        umma_commit_pair_mc(&empty[s], 3);
-                        if (kb == kb1 - 1) umma_commit_pair_mc(&tfull[buf], 3);
+                        // the stage is free once every pair that reads it is done with it
+                        umma_commit_pair_mc(&empty[s], SC::MC ? 0xF : 3);
+                        if (kb == kb1 - 1) umma_commit_pair_mc(&tfull[buf], (uint16_t)(3u << leader));
                     } else {
                         umma_commit(&empty[s]);
                         if (kb == kb1 - 1) umma_commit(&tfull[buf]);
@@ -982,7 +1004,7 @@ void launch_one(gk_ctx* ctx, int grid, const Maps& m, const TcParams& p) {
         cudaFuncSetAttribute(gemm_tc_kernel<TC, SPLIT, F32OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    if constexpr (SPLIT == PAIR_MODE) {
+    if constexpr (StageCfg<SPLIT>::PAIR) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(THREADS);
@@ -990,7 +1012,7 @@ void launch_one(gk_ctx* ctx, int grid, const Maps& m, const TcParams& p) {
         cfg.stream = ctx->stream;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.x = StageCfg<SPLIT>::MC ? 4 : 2;
         at[0].val.clusterDim.y = 1;
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
@@ -1009,33 +1031,35 @@ void launch_split(gk_ctx* ctx, int split, int grid, const Maps& m, const TcParam
         case 1: launch_one<TC, 1>(ctx, grid, m, p); break;
         case 2: launch_one<TC, 2>(ctx, grid, m, p); break;
         case 3: launch_one<TC, 3>(ctx, grid, m, p); break;
-        default: launch_one<TC, PAIR_MODE>(ctx, grid, m, p); break;
+        case PAIR_MODE: launch_one<TC, PAIR_MODE>(ctx, grid, m, p); break;
+        default: launch_one<TC, PAIR4_MODE>(ctx, grid, m, p); break;
     }
 }
 
 // How many CTA pairs of the pair kernel can be resident at once (clusters need both SMs of a
 // pair free); 0 if the query fails.
-template <typename TC>
+template <typename TC, int MODE = PAIR_MODE>
 int max_pairs() {
     static int n = -1;
     if (n < 0) {
-        constexpr size_t smem = StageCfg<PAIR_MODE>::SMEM;
-        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        constexpr size_t smem = StageCfg<MODE>::SMEM;
+        constexpr int CS = StageCfg<MODE>::MC ? 4 : 2;
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
-        cudaFuncSetAttribute(gemm_tc_kernel<TC, PAIR_MODE, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        cudaFuncSetAttribute(gemm_tc_kernel<TC, MODE, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
         cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(2);
+        cfg.gridDim = dim3(CS);
         cfg.blockDim = dim3(THREADS);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.x = CS;
         at[0].val.clusterDim.y = 1;
         at[0].val.clusterDim.z = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int c = 0;
-        n = cudaOccupancyMaxActiveClusters(&c, gemm_tc_kernel<TC, PAIR_MODE, false>, &cfg) == cudaSuccess ? c : 0;
+        n = cudaOccupancyMaxActiveClusters(&c, gemm_tc_kernel<TC, MODE, false>, &cfg) == cudaSuccess ? c : 0;
         cudaGetLastError();
     }
     return n;
@@ -1110,6 +1134,14 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
                           ? (c_f32 ? max_pairs<float>() : max_pairs<__nv_bfloat16>())
                           : 0;
     const bool pair = pairs > 0;
+    // clusters of two pairs (B multicast) when there are at least two pair rows of tiles;
+    // not for the GELU forward, whose epilogue sets its time (36 clusters of four hold 144
+    // SMs against 152 for pairs). Measured at 16384 rows: QKV 49.9 -> 47.7 us, MLP down with
+    // residual 64.2 -> 62.1, GELU-backward dX 201 -> 181; GELU forward 84.6 -> 88.7.
+    const int quads = pair && cdiv(g.M, BM) >= 8 && g.epi != EPI_GELU
+                          ? (c_f32 ? max_pairs<float, PAIR4_MODE>() : max_pairs<__nv_bfloat16, PAIR4_MODE>())
+                          : 0;
+    const bool mc = quads >= 16;
     CUtensorMap ta, tb;
     bool ok;
     // a batch indexes into whole buffers: their maps span them
@@ -1121,7 +1153,7 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
         ok = make_map_f32(&ta, g.A, ak, am, g.lda, BK / 2, BM) && make_map_f32(&tb, g.B, bk, bn, g.ldb, BK / 2, BN);
     } else {
         ok = g.a_kmajor ? make_map(&ta, g.A, g.K, g.M, g.lda, BM) : make_map(&ta, g.A, g.M, g.K, g.lda, 64);
-        ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, pair ? BN / 2 : BN)
+        ok = ok && (g.b_kmajor ? make_map(&tb, g.B, g.K, g.N, g.ldb, mc ? BN / 4 : pair ? BN / 2 : BN)
                                : make_map(&tb, g.B, g.N, g.K, g.ldb, 64));
     }
     if (!ok) return GK_ERR_UNSUPPORTED;
@@ -1133,6 +1165,8 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.tiles_m = (int)cdiv(g.M, BM);
     p.tiles_n = (int)cdiv(g.N, BN);
     p.tiles_m2 = (int)cdiv(p.tiles_m, 2);
+    p.mc = mc ? 1 : 0;
+    p.tiles_m4 = (int)cdiv(p.tiles_m2, 2);
     // Units run in waves of one per CTA (pair), in unit order. With few column tiles and A the
     // larger operand (M > N: activations against weights, or the LM head's dlogits), the column
     // tiles of a row block go consecutively, so the CTAs that need a block of A rows load it
@@ -1167,8 +1201,8 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
             (!g.aux || (aligned16(g.aux) && g.ldaux % 4 == 0)) && (g.c_plane % 4 == 0);
     if ((g.A_lo && (!aligned16(g.A_lo))) || (g.B_lo && !aligned16(g.B_lo))) return GK_ERR_UNSUPPORTED;
     // persistent grid: one CTA per SM, or one pair per resident cluster
-    const int slots = pair ? pairs : ctx->num_sms;
-    int64_t tiles = (int64_t)(pair ? p.tiles_m2 : p.tiles_m) * p.tiles_n;
+    const int slots = mc ? quads : pair ? pairs : ctx->num_sms;
+    int64_t tiles = (int64_t)(mc ? p.tiles_m4 : pair ? p.tiles_m2 : p.tiles_m) * p.tiles_n;
     p.splits = 1;
     bool plain_acc = !batched && g.accumulate && g.c_dtype == GK_F32 && !g.bias && !g.residual && g.epi == EPI_NONE;
     if (plain_acc && tiles < slots) {
@@ -1180,8 +1214,8 @@ gk_status gemm_tc(gk_ctx* ctx, const Gemm& g) {
     p.splits = (int)cdiv(p.kblocks, p.kbps);
     p.atomic_out = p.splits > 1;
     int64_t units = tiles * p.splits * p.nz;
-    int grid = (int)std::min<int64_t>(units, slots) * (pair ? 2 : 1);
-    const int mode = pair ? PAIR_MODE : split;
+    int grid = (int)std::min<int64_t>(units, slots) * (mc ? 4 : pair ? 2 : 1);
+    const int mode = mc ? PAIR4_MODE : pair ? PAIR_MODE : split;
     Maps m;
     m.a = ta;
     m.b = tb;

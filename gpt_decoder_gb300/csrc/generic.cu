@@ -342,9 +342,16 @@ gk_status gk_scale_bwd(gk_ctx* ctx, const float* g, float s, float* da, int64_t 
 gk_status gk_sum_fwd(gk_ctx* ctx, const float* a, float* y, int64_t n) {
     if (!ctx) return GK_ERR_ARG;
     GK_REQUIRE(ctx, n >= 0 && y && (n == 0 || a), GK_ERR_ARG, "gk_sum_fwd: bad argument");
-    // about four blocks per SM, each thread at least 32 elements (measured: 82 us for 2^26
-    // floats, against 135 us with eight blocks per SM and eight chains)
-    const int P = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS * 32), 4 * (int64_t)ctx->num_sms));
+    // one full wave of resident blocks (64 bytes of loads in flight per thread), each thread at
+    // least 32 elements
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, sum_partial_kernel, EW_THREADS, 0) != cudaSuccess || b < 1)
+            b = 1;
+        per_sm = b;
+    }
+    const int P = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(n, EW_THREADS * 32), (int64_t)per_sm * ctx->num_sms));
     double* part = static_cast<double*>(workspace(ctx, (size_t)P * sizeof(double)));
     GK_REQUIRE(ctx, part, GK_ERR_WORKSPACE, "gk_sum_fwd: needs %zu workspace bytes", (size_t)P * sizeof(double));
     sum_partial_kernel<<<P, EW_THREADS, 0, ctx->stream>>>(a, n, part, vec4(a));

@@ -307,6 +307,17 @@ __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_
         "l"((uint64_t)map), "r"(bar_cluster), "r"(x), "r"(y)
         : "memory");
 }
+// The same copy multicast to every CTA of `mask` (each receives it at the offset of dst): in each
+// destination's pair the bytes are counted on the mbarrier at bar_cluster's offset in the pair's
+// even CTA.
+__device__ __forceinline__ void tma_load_2d_pair_mc(const CUtensorMap* map, uint32_t bar_cluster, void* dst, int x, int y,
+                                                    uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2 "
+        "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(saddr(dst)),
+        "l"((uint64_t)map), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
 // M = 256 MMA over the CTA pair: A rows 0..127 and B columns 0..N/2-1 come from the even CTA's
 // shared memory, A rows 128..255 and B columns N/2.. from the odd CTA's (same offsets); each
 // CTA's TMEM receives its 128 rows of D. Issued by one thread of the even CTA.

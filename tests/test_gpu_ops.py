@@ -92,7 +92,8 @@ def test_embedding_bwd_bit_exact(gkctx, B, T, C, V):
 
 
 # ----------------------------------------------------------------------- layernorm
-@pytest.mark.parametrize("rows,C", [(4096, 768), (4096, 50257), (37, 96), (5, 130), (1, 1024), (3, 7)])
+@pytest.mark.parametrize("rows,C", [(4096, 768), (4096, 50257), (37, 96), (5, 130), (1, 1024), (3, 7), (64, 8192),
+                                    (9, 5003)])
 @pytest.mark.parametrize("ydt", ["f32", "bf16"])
 def test_layernorm_fwd(gkctx, rows, C, ydt):
     from gpt_decoder_gb300 import gk

@@ -393,7 +393,9 @@ __global__ void __maxnreg__(168)
 }
 
 // ------------------------------------------------------------------------ backward
-// One CTA per (128-key tile, batch, head), looping over the query tiles at or after its keys,
+// Persistent: one CTA per SM walks work items (128-key tile, batch, head) — the earliest key
+// tiles, which meet the most queries, first, dealt in snake order — and for each loops over
+// the query tiles at or after its keys,
 // each cut into two 64-query sub-tiles u (tile u / 2, half u % 2). Warps 0-7 compute: warp w
 // owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and 32 query columns (w / 4) of
 // each sub-tile. Warp 8 issues the TMA copies and the MMAs. Per sub-tile u:
@@ -407,15 +409,23 @@ __global__ void __maxnreg__(168)
 // the other into P^T and dS^T. dQ_tile, double-buffered in TMEM, goes through a swizzled
 // shared-memory tile into a float32 accumulator by TMA reduce-add at the end of the next tile
 // (while the tensor core works on that tile's last products); dK and dV are stored once at
-// the end. TMEM: S^T/dP^T buffers 0..255, dV 256..319, dK 320..383, dQ 384..511.
+// the end. TMEM: S^T/dP^T buffers 0..255, dV 256..319, dK 320..383, dQ 384..511. The barrier
+// phases, the Q/dO stages and the dQ buffers run on across items (counted in query tiles); an
+// item's K and V are loaded once the previous item's products are complete, while the compute
+// warps store that item's dV and dK.
 constexpr int BWD_THREADS = 288;
 // K, V, Q[2], dO[2], P^T, dS^T, dQ staging (a 4 KB box per compute warp), lse/D (512 B per warp)
 constexpr size_t BWD_SMEM_BYTES = 12 * TILE + 4096 + 1024 + 256;
 
+// The r-th work item of this CTA (snake order, as fwd_item), or -1: item k is key tile k / BH of
+// (batch x head) k % BH.
+__device__ __forceinline__ int bwd_item(int r, int n_items) { return fwd_item(r, n_items); }
+
 __global__ void __maxnreg__(168)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_dy,
                        const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
-                       const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv, int T, int H, int* err) {
+                       const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv, int T, int H, int BH,
+                       int n_items, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sK = smem;
@@ -439,16 +449,7 @@ __global__ void __maxnreg__(168)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int C = H * HS;
-    // blocks are dispatched x fastest: every (batch, head) of the heaviest key tile (the
-    // earliest keys, which meet the most queries) goes first
-    const int kt = blockIdx.y;
-    const int k0 = kt * KT;
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int row0 = b * T;
     const int n_qt = (T + QT - 1) / QT;
-    const int first_qt = k0 / QT;
-    const int n_it = n_qt - first_qt;
-    const int n_u = 2 * n_it;
 
     if (tid == 0) {
         mbar_init(bar_kv, 1);
@@ -472,62 +473,78 @@ __global__ void __maxnreg__(168)
     if (warp == 8) {
         // TMA copies and MMAs. The whole warp walks the schedule (warp-uniform descriptors);
         // one elected lane issues each group of copies or MMAs with the commits that track them.
-        if (n_it > 0) {
-            const uint32_t id_s = instr_desc_bf16(false, false, 128, 64);   // S^T, dP^T of a sub-tile
-            const uint32_t id_kv = instr_desc_bf16(false, true, 128, 64);   // dV, dK: B (dO, Q) MN-major
-            const uint32_t id_q = instr_desc_bf16(true, true, 128, 64);     // dQ: A (dS) and B (K) MN-major
-            const uint64_t k_d = smem_desc(saddr(sK), 16, 1024), v_d = smem_desc(saddr(sV), 16, 1024);
-            const uint64_t kq_d = smem_desc(saddr(sK), 8192, 1024);    // K as dQ's MN-major B
-            const uint64_t ds_d = smem_desc(saddr(sDS), 16384, 1024);  // dS as dQ's MN-major A
-            const uint64_t pt_d = smem_desc(saddr(sPT), 16, 1024), dst_d = smem_desc(saddr(sDS), 16, 1024);
-            // Q / dO stages: K-major (S^T, dP^T) and MN-major (dK, dV) views
-            const uint64_t q_d0 = smem_desc(saddr(sQ), 16, 1024), q_d1 = smem_desc(saddr(sQ + TILE), 16, 1024);
-            const uint64_t o_d0 = smem_desc(saddr(sO), 16, 1024), o_d1 = smem_desc(saddr(sO + TILE), 16, 1024);
-            const uint64_t qm_d0 = smem_desc(saddr(sQ), 8192, 1024), qm_d1 = smem_desc(saddr(sQ + TILE), 8192, 1024);
-            const uint64_t om_d0 = smem_desc(saddr(sO), 8192, 1024), om_d1 = smem_desc(saddr(sO + TILE), 8192, 1024);
+        const uint32_t id_s = instr_desc_bf16(false, false, 128, 64);   // S^T, dP^T of a sub-tile
+        const uint32_t id_kv = instr_desc_bf16(false, true, 128, 64);   // dV, dK: B (dO, Q) MN-major
+        const uint32_t id_q = instr_desc_bf16(true, true, 128, 64);     // dQ: A (dS) and B (K) MN-major
+        const uint64_t k_d = smem_desc(saddr(sK), 16, 1024), v_d = smem_desc(saddr(sV), 16, 1024);
+        const uint64_t kq_d = smem_desc(saddr(sK), 8192, 1024);    // K as dQ's MN-major B
+        const uint64_t ds_d = smem_desc(saddr(sDS), 16384, 1024);  // dS as dQ's MN-major A
+        const uint64_t pt_d = smem_desc(saddr(sPT), 16, 1024), dst_d = smem_desc(saddr(sDS), 16, 1024);
+        // Q / dO stages: K-major (S^T, dP^T) and MN-major (dK, dV) views
+        const uint64_t q_d0 = smem_desc(saddr(sQ), 16, 1024), q_d1 = smem_desc(saddr(sQ + TILE), 16, 1024);
+        const uint64_t o_d0 = smem_desc(saddr(sO), 16, 1024), o_d1 = smem_desc(saddr(sO + TILE), 16, 1024);
+        const uint64_t qm_d0 = smem_desc(saddr(sQ), 8192, 1024), qm_d1 = smem_desc(saddr(sQ + TILE), 8192, 1024);
+        const uint64_t om_d0 = smem_desc(saddr(sO), 8192, 1024), om_d1 = smem_desc(saddr(sO + TILE), 8192, 1024);
+        if (elect_one()) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_dy) : "memory");
+        }
+        __syncwarp();
+        int gt = 0;                // query tiles of the items before this one
+        int pend[2] = {-1, -1};    // phase of the Q/dO load in flight per stage
+        int kv_pend = -1;          // phase of the K/V load in flight
+        bool ok = true, issued = false;
+        for (int r = 0, ii = 0; ok; ++r, ++ii) {
+            const int item = bwd_item(r, n_items);
+            if (item < 0) break;
+            const int kt = item / BH, bh = item % BH, h = bh % H;
+            const int row0 = (bh / H) * T, k0 = kt * KT, first_qt = k0 / QT;
+            const int n_it = n_qt - first_qt, n_u = 2 * n_it;
+            // the previous item's products are complete (its last commit): K, V, both Q/dO stages
+            // and the S^T/dP^T buffers are free again
+            if (ii > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_st, (gt - 1) & 1, abort_flag, WAIT_NS))))
+                break;
             if (elect_one()) {
-                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_qkv) : "memory");
-                asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_dy) : "memory");
                 mbar_expect_tx(bar_kv, 2 * TILE);
                 tma_load_2d(&tm_qkv, bar_kv, sK, C + h * HS, row0 + k0);
                 tma_load_2d(&tm_qkv, bar_kv, sV, 2 * C + h * HS, row0 + k0);
                 for (int i = 0; i < 2 && i < n_it; ++i) {
-                    mbar_expect_tx(&bar_qo[i], 2 * TILE);
-                    tma_load_2d(&tm_qkv, &bar_qo[i], sQ + i * TILE, h * HS, row0 + (first_qt + i) * QT);
-                    tma_load_2d(&tm_dy, &bar_qo[i], sO + i * TILE, h * HS, row0 + (first_qt + i) * QT);
+                    const int st = (gt + i) & 1;
+                    mbar_expect_tx(&bar_qo[st], 2 * TILE);
+                    tma_load_2d(&tm_qkv, &bar_qo[st], sQ + st * TILE, h * HS, row0 + (first_qt + i) * QT);
+                    tma_load_2d(&tm_dy, &bar_qo[st], sO + st * TILE, h * HS, row0 + (first_qt + i) * QT);
                 }
             }
             __syncwarp();
-            int pend[2] = {0, n_it > 1 ? 0 : -1};  // phase of the Q/dO load in flight per stage
-            bool kv_pending = true, issued = false;
+            kv_pend = ii & 1;
+            for (int i = 0; i < 2 && i < n_it; ++i) pend[(gt + i) & 1] = ((gt + i) >> 1) & 1;
             // S^T and dP^T of sub-tile u into TMEM buffer u % 2 (its tile's Q/dO must have landed)
             auto issue_s = [&](int u) {
-                const int st = (u >> 1) & 1, hq = u & 1;
-                const uint32_t d = tmem + (uint32_t)(u & 1) * 128;
+                const int st = (gt + (u >> 1)) & 1, hq = u & 1;
+                const uint32_t d = tmem + (uint32_t)hq * 128;
 #pragma unroll
                 for (int k = 0; k < HS / 16; ++k)
                     umma_bf16(d, desc_add(k_d, k * 32), desc_add(pick(q_d0, q_d1, st), hq * 8192 + k * 32), id_s, k > 0);
 #pragma unroll
                 for (int k = 0; k < HS / 16; ++k)
                     umma_bf16(d + 64, desc_add(v_d, k * 32), desc_add(pick(o_d0, o_d1, st), hq * 8192 + k * 32), id_s, k > 0);
-                umma_commit(&bar_s[u & 1]);
+                umma_commit(&bar_s[hq]);
             };
-            bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, abort_flag, WAIT_NS) &&
-                                                  mbar_wait(&bar_qo[0], 0, abort_flag, WAIT_NS));
-            if (ok) {
-                kv_pending = false;
-                pend[0] = -1;
-                tc_fence_after();
-                if (elect_one()) {
-                    issue_s(0);
-                    issue_s(1);
-                }
-                __syncwarp();
-                issued = true;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, ii & 1, abort_flag, WAIT_NS) &&
+                                             mbar_wait(&bar_qo[gt & 1], (gt >> 1) & 1, abort_flag, WAIT_NS));
+            if (!ok) break;
+            kv_pend = -1;
+            pend[gt & 1] = -1;
+            tc_fence_after();
+            if (elect_one()) {
+                issue_s(0);
+                issue_s(1);
             }
+            __syncwarp();
+            issued = true;
             for (int u = 0; ok && u < n_u; ++u) {
-                const int it = u >> 1, hq = u & 1, st = it & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar_p[hq], it & 1, abort_flag, WAIT_NS))) {
+                const int it = u >> 1, hq = u & 1, tg = gt + it, st = tg & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_p[hq], tg & 1, abort_flag, WAIT_NS))) {
                     ok = false;
                     break;
                 }
@@ -538,7 +555,7 @@ __global__ void __maxnreg__(168)
                         // P^T / dS^T buffers for the next tile's first half
 #pragma unroll
                         for (int k = 0; k < KT / 16; ++k)
-                            umma_bf16(tmem + 384 + (uint32_t)(it & 1) * 64, desc_add(ds_d, k * 2048),
+                            umma_bf16(tmem + 384 + (uint32_t)(tg & 1) * 64, desc_add(ds_d, k * 2048),
                                       desc_add(kq_d, k * 2048), id_q, k > 0);
                         umma_commit(bar_mm);
                     }
@@ -555,9 +572,9 @@ __global__ void __maxnreg__(168)
                 __syncwarp();
                 if (u + 2 < n_u) {
                     if (hq == 0) {  // the next tile's Q/dO
-                        const int ns = (it + 1) & 1;
+                        const int ns = (tg + 1) & 1;
                         if (!__all_sync(0xffffffffu,
-                                        mbar_wait(&bar_qo[ns], ((it + 1) >> 1) & 1, abort_flag, WAIT_NS))) {
+                                        mbar_wait(&bar_qo[ns], ((tg + 1) >> 1) & 1, abort_flag, WAIT_NS))) {
                             ok = false;
                             break;
                         }
@@ -569,7 +586,7 @@ __global__ void __maxnreg__(168)
                 }
                 if (hq == 1 && it + 2 < n_it) {
                     // stage st (this tile's Q, dO) is free once the tile's last dV, dK are done
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_st, it & 1, abort_flag, WAIT_NS))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_st, tg & 1, abort_flag, WAIT_NS))) {
                         ok = false;
                         break;
                     }
@@ -579,30 +596,30 @@ __global__ void __maxnreg__(168)
                         tma_load_2d(&tm_dy, &bar_qo[st], sO + st * TILE, h * HS, row0 + (first_qt + it + 2) * QT);
                     }
                     __syncwarp();
-                    pend[st] = ((it + 2) >> 1) & 1;
+                    pend[st] = ((tg + 2) >> 1) & 1;
                 }
             }
-            if (!ok) {
-                if (elect_one()) {
-                    *abort_flag = 1;
-                    report(err, GK_ERR_TIMEOUT);
-                    // let this CTA's copies and MMAs in flight finish before shared memory and
-                    // TMEM are released
-                    if (kv_pending) mbar_wait(bar_kv, 0, nullptr, WAIT_NS / 5);
-                    for (int i = 0; i < 2; ++i)
-                        if (pend[i] >= 0) mbar_wait(&bar_qo[i], (uint32_t)pend[i], nullptr, WAIT_NS / 5);
-                    if (issued) {
-                        umma_commit(bar_drain);
-                        mbar_wait(bar_drain, 0, nullptr, WAIT_NS / 5);
-                    }
+            gt += n_it;
+        }
+        if (!ok) {
+            if (elect_one()) {
+                *abort_flag = 1;
+                report(err, GK_ERR_TIMEOUT);
+                // let this CTA's copies and MMAs in flight finish before shared memory and
+                // TMEM are released
+                if (kv_pend >= 0) mbar_wait(bar_kv, (uint32_t)kv_pend, nullptr, WAIT_NS / 5);
+                for (int i = 0; i < 2; ++i)
+                    if (pend[i] >= 0) mbar_wait(&bar_qo[i], (uint32_t)pend[i], nullptr, WAIT_NS / 5);
+                if (issued) {
+                    umma_commit(bar_drain);
+                    mbar_wait(bar_drain, 0, nullptr, WAIT_NS / 5);
                 }
-                __syncwarp();
             }
+            __syncwarp();
         }
     } else {
         const int qd = warp & 3, hf = warp >> 2;
         const int r = qd * 32 + lane;  // key row of S^T / dP^T / dV / dK; query row of dQ
-        const int kk = k0 + r;
         const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
         const float sl2 = 0.125f * 1.4426950408889634f;
         const float L2E = 1.4426950408889634f;
@@ -618,130 +635,139 @@ __global__ void __maxnreg__(168)
         };
         float* myLD = sLD + warp * 128;            // [2 buffers][lse 32 | D 32]
         uint8_t* myDQ = sDQ + warp * 4096;         // 32 rows x 128 bytes
-        // lane c's lse (log2 units) and D for query column c of this warp in sub-tile v
-        auto ld_pair = [&](int v, float& lv, float& dvv) {
-            const int q = (first_qt + (v >> 1)) * QT + (v & 1) * 64 + hf * 32 + lane;
-            lv = q < T ? lse[(int64_t)bh * T + q] * L2E : 0.f;
-            dvv = q < T ? dvec[(int64_t)bh * T + q] : 0.f;
-        };
-        float nl = 0.f, nd = 0.f;
-        if (n_u > 0) ld_pair(0, nl, nd);
-        // dQ of query tile t (TMEM buffer t % 2, complete): this warp's 32 rows x 32 columns
-        // through its swizzled staging box into the float32 accumulator by TMA reduce-add
-        auto drain_dq = [&](int t) {
-            if (lane == 0) bulk_wait_read<0>();  // this warp's previous reduce has read the box
-            __syncwarp();
-            tc_fence_after();
-            uint32_t qv[32];
-            tmem_ld32_nowait(lane_addr + 384 + (uint32_t)(t & 1) * 64 + hf * 32, qv);
-            tmem_wait_ld_only();
-            reg_fence32(qv);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<float4*>(myDQ + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                    make_float4(__uint_as_float(qv[4 * j]) * 0.125f, __uint_as_float(qv[4 * j + 1]) * 0.125f,
-                                __uint_as_float(qv[4 * j + 2]) * 0.125f, __uint_as_float(qv[4 * j + 3]) * 0.125f);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                // rows past this sequence carry dS = 0 (masked), so the whole box is added
-                tma_reduce_add_2d(&tm_dq, myDQ, h * HS + hf * 32, row0 + (first_qt + t) * QT + qd * 32);
-                bulk_commit();
-            }
-        };
-        for (int u = 0; u < n_u; ++u) {
-            const int it = u >> 1, hq = u & 1;
-            const int q0 = (first_qt + it) * QT;
-            // this sub-tile's lse / D into the warp's buffer u % 2; the next sub-tile's on the way
-            float* L = myLD + (u & 1) * 64;
-            L[lane] = nl;
-            L[32 + lane] = nd;
-            if (u + 1 < n_u) ld_pair(u + 1, nl, nd);
-            __syncwarp();
-            if (!fail) note_fail(__all_sync(0xffffffffu, mbar_wait(&bar_s[hq], it & 1, abort_flag, WAIT_NS)));
-            if (!fail) {
+        int gt = 0;                                // query tiles of the items before this one
+        for (int ri = 0; !fail; ++ri) {
+            const int item = bwd_item(ri, n_items);
+            if (item < 0) break;
+            const int kt = item / BH, bh = item % BH, h = bh % H;
+            const int row0 = (bh / H) * T, k0 = kt * KT, first_qt = k0 / QT;
+            const int n_it = n_qt - first_qt, n_u = 2 * n_it;
+            const int kk = k0 + r;
+            // lane c's lse (log2 units) and D for query column c of this warp in sub-tile v
+            auto ld_pair = [&](int v, float& lv, float& dvv) {
+                const int q = (first_qt + (v >> 1)) * QT + (v & 1) * 64 + hf * 32 + lane;
+                lv = q < T ? lse[(int64_t)bh * T + q] * L2E : 0.f;
+                dvv = q < T ? dvec[(int64_t)bh * T + q] : 0.f;
+            };
+            float nl = 0.f, nd = 0.f;
+            ld_pair(0, nl, nd);
+            // dQ of this item's query tile t (TMEM buffer (gt + t) % 2, complete): this warp's
+            // 32 rows x 32 columns through its swizzled staging box into the float32
+            // accumulator by TMA reduce-add
+            auto drain_dq = [&](int t) {
+                if (lane == 0) bulk_wait_read<0>();  // this warp's previous reduce has read the box
+                __syncwarp();
                 tc_fence_after();
-                uint32_t sv[32], dv[32];
-                tmem_ld32_nowait(lane_addr + hq * 128 + hf * 32, sv);
-                tmem_ld32_nowait(lane_addr + hq * 128 + 64 + hf * 32, dv);
+                uint32_t qv[32];
+                tmem_ld32_nowait(lane_addr + 384 + (uint32_t)((gt + t) & 1) * 64 + hf * 32, qv);
                 tmem_wait_ld_only();
-                reg_fence32(sv);
-                reg_fence32(dv);
-                // this warp's 32 query columns: tile columns cbase .. cbase + 31; visible c
-                // (0..31) satisfy lo <= c < hi
-                const int cbase = hq * 64 + hf * 32;
-                int lo = 0, hi = 32;
-                if (q0 == k0) lo = r - cbase;                 // causal: query >= key on the diagonal
-                hi = min(hi, T - q0 - cbase);                 // ragged last query tile
-                if (kk >= T) hi = 0;                          // padding key rows
-                const bool masked = lo > 0 || hi < 32;
-                const float* D = L + 32;
-                uint32_t pw[16], qw[16];
+                reg_fence32(qv);
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8) {
-                    const float4 l0 = *reinterpret_cast<const float4*>(L + c8);
-                    const float4 l1 = *reinterpret_cast<const float4*>(L + c8 + 4);
-                    const float4 d0 = *reinterpret_cast<const float4*>(D + c8);
-                    const float4 d1 = *reinterpret_cast<const float4*>(D + c8 + 4);
-                    const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-                    const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const int c = c8 + e;
-                        float p0 = ex2_hw(fmaf(__uint_as_float(sv[c]), sl2, -lv[e]));
-                        float p1 = ex2_hw(fmaf(__uint_as_float(sv[c + 1]), sl2, -lv[e + 1]));
-                        float ds0 = p0 * (__uint_as_float(dv[c]) - dd[e]);
-                        float ds1 = p1 * (__uint_as_float(dv[c + 1]) - dd[e + 1]);
-                        if (masked) {  // hidden pairs contribute exactly zero
-                            const bool v0 = c >= lo && c < hi, v1 = c + 1 >= lo && c + 1 < hi;
-                            p0 = v0 ? p0 : 0.f;
-                            ds0 = v0 ? ds0 : 0.f;
-                            p1 = v1 ? p1 : 0.f;
-                            ds1 = v1 ? ds1 : 0.f;
-                        }
-                        __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                        __nv_bfloat162 u2 = __floats2bfloat162_rn(ds0, ds1);
-                        pw[c >> 1] = *reinterpret_cast<uint32_t*>(&t2);
-                        qw[c >> 1] = *reinterpret_cast<uint32_t*>(&u2);
-                    }
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(myDQ + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_float4(__uint_as_float(qv[4 * j]) * 0.125f, __uint_as_float(qv[4 * j + 1]) * 0.125f,
+                                    __uint_as_float(qv[4 * j + 2]) * 0.125f, __uint_as_float(qv[4 * j + 3]) * 0.125f);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    // rows past this sequence carry dS = 0 (masked), so the whole box is added
+                    tma_reduce_add_2d(&tm_dq, myDQ, h * HS + hf * 32, row0 + (first_qt + t) * QT + qd * 32);
+                    bulk_commit();
                 }
-                // the P^T / dS^T buffers are free for a new tile once the previous tile's dQ
-                // (issued after its last dS) is done; the half-1 products of the previous tile
-                // finished before this tile's S^T of half 1 (waited above)
-                if (hq == 0 && it > 0)
-                    note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (it - 1) & 1, abort_flag, WAIT_NS)));
+            };
+            for (int u = 0; u < n_u; ++u) {
+                const int it = u >> 1, hq = u & 1, tg = gt + it;
+                const int q0 = (first_qt + it) * QT;
+                // this sub-tile's lse / D into the warp's buffer u % 2; the next sub-tile's on the way
+                float* L = myLD + (u & 1) * 64;
+                L[lane] = nl;
+                L[32 + lane] = nd;
+                if (u + 1 < n_u) ld_pair(u + 1, nl, nd);
+                __syncwarp();
+                if (!fail) note_fail(__all_sync(0xffffffffu, mbar_wait(&bar_s[hq], tg & 1, abort_flag, WAIT_NS)));
                 if (!fail) {
+                    tc_fence_after();
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32_nowait(lane_addr + hq * 128 + hf * 32, sv);
+                    tmem_ld32_nowait(lane_addr + hq * 128 + 64 + hf * 32, dv);
+                    tmem_wait_ld_only();
+                    reg_fence32(sv);
+                    reg_fence32(dv);
+                    // this warp's 32 query columns: tile columns cbase .. cbase + 31; visible c
+                    // (0..31) satisfy lo <= c < hi
+                    const int cbase = hq * 64 + hf * 32;
+                    int lo = 0, hi = 32;
+                    if (q0 == k0) lo = r - cbase;                 // causal: query >= key on the diagonal
+                    hi = min(hi, T - q0 - cbase);                 // ragged last query tile
+                    if (kk >= T) hi = 0;                          // padding key rows
+                    const bool masked = lo > 0 || hi < 32;
+                    const float* D = L + 32;
+                    uint32_t pw[16], qw[16];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        *reinterpret_cast<uint4*>(sPT + p_offset(r, cbase + 8 * j)) =
-                            make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
-                        *reinterpret_cast<uint4*>(sDS + p_offset(r, cbase + 8 * j)) =
-                            make_uint4(qw[4 * j], qw[4 * j + 1], qw[4 * j + 2], qw[4 * j + 3]);
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        const float4 l0 = *reinterpret_cast<const float4*>(L + c8);
+                        const float4 l1 = *reinterpret_cast<const float4*>(L + c8 + 4);
+                        const float4 d0 = *reinterpret_cast<const float4*>(D + c8);
+                        const float4 d1 = *reinterpret_cast<const float4*>(D + c8 + 4);
+                        const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+                        const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const int c = c8 + e;
+                            float p0 = ex2_hw(fmaf(__uint_as_float(sv[c]), sl2, -lv[e]));
+                            float p1 = ex2_hw(fmaf(__uint_as_float(sv[c + 1]), sl2, -lv[e + 1]));
+                            float ds0 = p0 * (__uint_as_float(dv[c]) - dd[e]);
+                            float ds1 = p1 * (__uint_as_float(dv[c + 1]) - dd[e + 1]);
+                            if (masked) {  // hidden pairs contribute exactly zero
+                                const bool v0 = c >= lo && c < hi, v1 = c + 1 >= lo && c + 1 < hi;
+                                p0 = v0 ? p0 : 0.f;
+                                ds0 = v0 ? ds0 : 0.f;
+                                p1 = v1 ? p1 : 0.f;
+                                ds1 = v1 ? ds1 : 0.f;
+                            }
+                            __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                            __nv_bfloat162 u2 = __floats2bfloat162_rn(ds0, ds1);
+                            pw[c >> 1] = *reinterpret_cast<uint32_t*>(&t2);
+                            qw[c >> 1] = *reinterpret_cast<uint32_t*>(&u2);
+                        }
                     }
-                    fence_proxy_async_smem();  // P^T, dS^T generic stores -> visible to the tensor core
-                    tc_fence_before();
-                    mbar_arrive(&bar_p[hq]);
+                    // the P^T / dS^T buffers are free for a new tile once the previous tile's dQ
+                    // (issued after its last dS) is done; the half-1 products of the previous tile
+                    // finished before this tile's S^T of half 1 (waited above). An item's first
+                    // tile follows the previous item's last products, waited for at its end.
+                    if (hq == 0 && it > 0)
+                        note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (tg - 1) & 1, abort_flag, WAIT_NS)));
+                    if (!fail) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            *reinterpret_cast<uint4*>(sPT + p_offset(r, cbase + 8 * j)) =
+                                make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
+                            *reinterpret_cast<uint4*>(sDS + p_offset(r, cbase + 8 * j)) =
+                                make_uint4(qw[4 * j], qw[4 * j + 1], qw[4 * j + 2], qw[4 * j + 3]);
+                        }
+                        fence_proxy_async_smem();  // P^T, dS^T generic stores -> visible to the tensor core
+                        tc_fence_before();
+                        mbar_arrive(&bar_p[hq]);
+                    }
                 }
+                // the previous tile's dQ (double-buffered in TMEM; waited above) while the tensor
+                // core runs this tile's dQ, dV and dK
+                if (hq == 1 && it > 0 && !fail) drain_dq(it - 1);
             }
-            // the previous tile's dQ (double-buffered in TMEM; waited above) while the tensor
-            // core runs this tile's dQ, dV and dK
-            if (hq == 1 && it > 0 && !fail) drain_dq(it - 1);
-        }
-        if (n_it > 0 && !fail) {  // the last tile's dQ
-            note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (n_it - 1) & 1, abort_flag, WAIT_NS)));
-            if (!fail) drain_dq(n_it - 1);
-        }
-        if (lane == 0) bulk_wait_all();
-        __syncwarp();
-        // dV and dK: the last tile's dV, dK products follow its dQ, so they are waited for on
-        // their own barrier (whose previous phase completed before bar_mm's last one)
-        if (!fail && n_it > 0)
-            note_fail(__all_sync(0xffffffffu, mbar_wait(bar_st, (n_it - 1) & 1, abort_flag, WAIT_NS)));
-        if (fail) {
-            *abort_flag = 1;
-            report(err, GK_ERR_TIMEOUT);
-        } else if (n_it > 0) {  // lane r = key row kk
+            if (!fail) {  // the last tile's dQ
+                note_fail(__all_sync(0xffffffffu, mbar_wait(bar_mm, (gt + n_it - 1) & 1, abort_flag, WAIT_NS)));
+                if (!fail) drain_dq(n_it - 1);
+            }
+            if (lane == 0) bulk_wait_all();
+            __syncwarp();
+            // dV and dK: the last tile's dV, dK products follow its dQ, so they are waited for on
+            // their own barrier (whose previous phase completed before bar_mm's last one); their
+            // completion also frees every buffer of this item for the next one
+            if (!fail)
+                note_fail(__all_sync(0xffffffffu, mbar_wait(bar_st, (gt + n_it - 1) & 1, abort_flag, WAIT_NS)));
+            if (fail) break;
+            // lane r = key row kk
             tc_fence_after();
             uint32_t v[32];
             __nv_bfloat16* base = dqkv + (int64_t)(row0 + kk) * 3 * C + h * HS + hf * 32;
@@ -773,6 +799,14 @@ __global__ void __maxnreg__(168)
                     *reinterpret_cast<uint4*>(base + C + i) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
             }
+            // dV, dK are read: the next item's first dV / dK products (issued after this warp's
+            // next bar_p arrival) may overwrite them
+            tc_fence_before();
+            gt += n_it;
+        }
+        if (fail) {
+            *abort_flag = 1;
+            report(err, GK_ERR_TIMEOUT);
         }
         tc_fence_before();
     }
@@ -882,9 +916,12 @@ gk_status attn_bwd_tc(gk_ctx* ctx, const void* qkv, const void* y, const float* 
         cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BWD_SMEM_BYTES);
         attr = true;
     }
-    dim3 grid((unsigned)(B * H), (unsigned)cdiv(T, KT));
+    // persistent: one CTA per SM over the (key tile, batch x head) items, heaviest first
+    const int BH = B * H, n_items = BH * (int)cdiv(T, KT);
+    const int grid = std::min(n_items, ctx->num_sms);
     attn_bwd_tc_kernel<<<grid, BWD_THREADS, BWD_SMEM_BYTES, ctx->stream>>>(map_qkv, map_dy, map_dq, lse, dvec,
-                                                                        (__nv_bfloat16*)dqkv, T, H, ctx->d_err);
+                                                                        (__nv_bfloat16*)dqkv, T, H, BH, n_items,
+                                                                        ctx->d_err);
     GK_TRY(launched(ctx, "attn_bwd_tc"));
     attn_dq_store_kernel<<<(unsigned)cdiv(rows * C / 4, 256), 256, 0, ctx->stream>>>(dq_acc, (__nv_bfloat16*)dqkv,
                                                                                     rows, (int)C);

@@ -142,11 +142,21 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
     s = t;
 }
 
+// Double-float arithmetic: (hi, lo) stands for the unevaluated sum hi + lo of two float32
+// values, about 48 significant bits (Knuth's TwoSum for the exact error of a float addition).
+__device__ __forceinline__ float2 df_add(float2 x, float2 y) {
+    const float s = x.x + y.x, bp = s - x.x;
+    const float e = ((x.x - (s - bp)) + (y.x - bp)) + (x.y + y.y);
+    const float hi = s + e;
+    return make_float2(hi, e - (hi - s));
+}
+
 // part[block] = sum of this block's grid-stride elements, in a fixed order: each aligned float4
 // group is added in float ((x + y) + (z + w)); a thread's k-th group goes to its compensated
 // float32 chain k % SC (SC independent chains, so SC loads are in flight per round trip), the
-// tail to the first; the chains are combined in double, then the block's threads in tree
-// order. Double arithmetic (a slow pipe on this GPU) is used only for those few combining steps.
+// tail to the first; the chains, then the lanes of a warp (xor tree) are combined in double-float,
+// the warps in double. Double arithmetic is a slow pipe on this GPU: a per-thread double tree
+// over every block ended each wave with microseconds of float64 work.
 constexpr int SC = 4;
 __global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, double* __restrict__ part, bool vec) {
     __shared__ double red[EW_THREADS / 32];
@@ -172,12 +182,13 @@ __global__ void sum_partial_kernel(const float* __restrict__ a, int64_t n, doubl
         }
     }
     for (int64_t i = 4 * n4 + tid; i < n; i += stride) kahan_add(s4[0], c4[0], a[i]);
-    double s = 0.0;
+    float2 s = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < SC; ++k) s += (double)s4[k] - (double)c4[k];
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    for (int k = 0; k < SC; ++k) s = df_add(s, make_float2(s4[k], -c4[k]));
+    for (int o = 16; o > 0; o >>= 1)
+        s = df_add(s, make_float2(__shfl_xor_sync(0xffffffffu, s.x, o), __shfl_xor_sync(0xffffffffu, s.y, o)));
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) red[warp] = s;
+    if (lane == 0) red[warp] = (double)s.x + (double)s.y;
     __syncthreads();
     if (threadIdx.x == 0) {
         double t = 0.0;

@@ -64,10 +64,33 @@ __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+
+// Double-float arithmetic: (hi, lo) stands for the unevaluated sum hi + lo of two float32
+// values, about 48 significant bits (Knuth's TwoSum gives the exact error of a float addition).
+// Float64 runs on a slow pipe on this GPU; these run on the float32 one.
+__device__ __forceinline__ float2 df_add(float2 x, float2 y) {
+    const float s = x.x + y.x, bp = s - x.x;
+    const float e = ((x.x - (s - bp)) + (y.x - bp)) + (x.y + y.y);
+    const float hi = s + e;
+    return make_float2(hi, e - (hi - s));
+}
+
+// *out = (sum of v[0 .. n)) / n by one block in a fixed order: thread t adds v[t], v[t + blockDim],
+// ... in double-float, a lane xor tree in double-float, then the warps in order in double.
+__device__ __forceinline__ void block_mean_fixed(const float* __restrict__ v, int64_t n, float* out) {
+    __shared__ double red[32];
+    float2 s = make_float2(0.f, 0.f);
+    for (int64_t r = threadIdx.x; r < n; r += blockDim.x) s = df_add(s, make_float2(v[r], 0.f));
+    for (int o = 16; o > 0; o >>= 1)
+        s = df_add(s, make_float2(__shfl_xor_sync(0xffffffffu, s.x, o), __shfl_xor_sync(0xffffffffu, s.y, o)));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = (double)s.x + (double)s.y;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+        *out = (float)(t / (double)n);
+    }
 }
 
 // Record the first kernel-side error of a launch in the context's error word.

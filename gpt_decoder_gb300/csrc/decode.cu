@@ -642,9 +642,18 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
             __syncthreads();
             uint32_t pre = prefix_s;
             uint32_t mask_hi = pass == 0 ? 0u : (0xFFFFFFFFu << (32 - 8 * pass));
-            for (int i = threadIdx.x; i < V; i += SEL_THREADS) {
-                uint32_t k = ord_key(x[i]);
-                if ((k & mask_hi) == pre) atomicAdd(&hist[(k >> shift) & 0xFF], 1u);
+            // warp-aggregated counts: the lanes of a warp that fall in the same bin add once
+            // (logits crowd into a few bins of each byte, so per-lane atomics would serialise)
+            for (int i0 = warp * 32; i0 < V; i0 += SEL_THREADS) {
+                const int i = i0 + lane;
+                const uint32_t k = i < V ? ord_key(x[i]) : 0u;
+                const bool in = i < V && (k & mask_hi) == pre;
+                const unsigned act = __ballot_sync(0xffffffffu, in);
+                if (in) {
+                    const uint32_t bin = (k >> shift) & 0xFF;
+                    const unsigned same = __match_any_sync(act, bin);
+                    if ((unsigned)lane == (unsigned)(__ffs(same) - 1)) atomicAdd(&hist[bin], (unsigned)__popc(same));
+                }
             }
             __syncthreads();
             if (threadIdx.x == 0) {

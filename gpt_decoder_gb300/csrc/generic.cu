@@ -62,15 +62,16 @@ __global__ void copy_acc_kernel(const float* src, float* dst, int64_t n, int acc
     }, [&](int64_t i) { dst[i] = acc ? dst[i] + src[i] : src[i]; });
 }
 
-// part[p, c] = sum of g[r, c] over the rows r of chunk p ([R, m] row-major), in row order
+// part[p, c] = sum of g[r, c] over the rows r of chunk p ([R, m] row-major), in row order, in
+// double-float (the float32 pipe; float64 is a slow one on this GPU)
 __global__ void colsum_chunks_kernel(const float* __restrict__ g, int64_t R, int64_t m, int64_t rows_per,
                                      double* __restrict__ part) {
     const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= m) return;
     const int64_t r0 = (int64_t)blockIdx.y * rows_per, r1 = min(R, r0 + rows_per);
-    double s = 0.0;
-    for (int64_t r = r0; r < r1; ++r) s += (double)g[r * m + c];
-    part[(int64_t)blockIdx.y * m + c] = s;
+    float2 s = make_float2(0.f, 0.f);
+    for (int64_t r = r0; r < r1; ++r) s = df_add(s, make_float2(g[r * m + c], 0.f));
+    part[(int64_t)blockIdx.y * m + c] = (double)s.x + (double)s.y;
 }
 
 // db[c] (+)= sum over chunks p in order of part[p, c]
@@ -140,15 +141,6 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
     const float t = s + y;
     c = (t - s) - y;
     s = t;
-}
-
-// Double-float arithmetic: (hi, lo) stands for the unevaluated sum hi + lo of two float32
-// values, about 48 significant bits (Knuth's TwoSum for the exact error of a float addition).
-__device__ __forceinline__ float2 df_add(float2 x, float2 y) {
-    const float s = x.x + y.x, bp = s - x.x;
-    const float e = ((x.x - (s - bp)) + (y.x - bp)) + (x.y + y.y);
-    const float hi = s + e;
-    return make_float2(hi, e - (hi - s));
 }
 
 // part[block] = sum of this block's grid-stride elements, in a fixed order: each aligned float4

@@ -54,20 +54,9 @@ __global__ void ce_combine_kernel(const float2* __restrict__ part, int P, const 
     }
 }
 
-// *loss = mean of row_loss (fixed partition, double accumulation).
+// *loss = mean of row_loss (fixed partition, double-float accumulation).
 __global__ void ce_mean_kernel(const float* __restrict__ row_loss, int64_t rows, float* loss) {
-    __shared__ double red[32];
-    double s = 0.0;
-    for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) s += (double)row_loss[r];
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) red[warp] = s;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-        *loss = (float)(t / (double)rows);
-    }
+    block_mean_fixed(row_loss, rows, loss);
 }
 
 bool ok_operand(const void* p, int64_t ld, int64_t inner) { return p && aligned16(p) && ld >= inner && ld % 8 == 0; }

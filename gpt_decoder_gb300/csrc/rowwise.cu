@@ -760,21 +760,9 @@ int ce_stream_blocks_per_sm() {
     return n;
 }
 
-// loss = (sum over rows, in order, in float64) / rows; one block.
+// loss = (sum over rows, in a fixed order, in double-float) / rows; one block.
 __global__ void mean_rows_kernel(const float* __restrict__ row_loss, int64_t rows, float* loss) {
-    __shared__ double red[32];
-    double s = 0.0;
-    // fixed partition: thread t sums rows t, t + blockDim, ... ascending
-    for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) s += (double)row_loss[r];
-    s = warp_sum_d(s);
-    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) red[warp] = s;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-        *loss = (float)(t / (double)rows);
-    }
+    block_mean_fixed(row_loss, rows, loss);
 }
 
 template <typename TD>

@@ -440,6 +440,18 @@ def _attn_inputs(B, T, H, hs, seed, dt):
 def test_attention_fwd_bwd(gkctx, B, T, H, hs, dt):
     """f32: float32 FMA on the CUDA cores; 3xtf32: the products on the tensor cores (T a multiple of
     128, other shapes take the float32 kernels); bf16: the bf16 tensor-core kernels (hs = 64)."""
+    _attention_case(gkctx, B, T, H, hs, dt)
+
+
+@pytest.mark.parametrize("B,T,H,hs", [(4, 1024, 12, 64), (8, 300, 12, 64)])
+def test_attention_bf16_several_work_items_per_cta(gkctx, B, T, H, hs):
+    """The persistent bf16 kernels with more work items than SMs (forward 192, backward 384 and
+    288 items), so CTAs carry barrier phases and buffers from one item to the next; T = 300 also
+    has items whose second query tile is missing and a ragged last tile."""
+    _attention_case(gkctx, B, T, H, hs, "bf16")
+
+
+def _attention_case(gkctx, B, T, H, hs, dt):
     from gpt_decoder_gb300 import gk
 
     torch = _t()

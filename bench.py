@@ -662,6 +662,26 @@ def bench_decode(ctx, m, s, Tp=512, n_steps=256):
     return res
 
 
+def bench_decode_only():
+    """The decode runs of bench_decode on the same random-init GPT-2-124M weights as the training
+    bench (seed 5), without the training step's buffers."""
+    import torch
+
+    import synth
+    from gpt_decoder_gb300 import gk
+    from gpt_decoder_gb300.model import Gpt
+
+    s = synth.GPT2_124M
+    ctx = gk.Ctx(torch.cuda.current_stream().cuda_stream, workspace_bytes=256 << 20)
+    _, _, params = synth.training_case(s, 1, 5)
+    m = Gpt(ctx, s.V, s.T, s.C, s.H, s.L, 1, mode="fp32")
+    m.load(params)
+    del params
+    res = bench_decode(ctx, m, s)
+    gk.gk_sync(ctx)
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -673,9 +693,9 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--only", choices=["sweep", "gemm-shapes"],
-                    help="run only the float32 op sweep, or only the bf16 products of one GPT-2 block at "
-                         "16384 rows, and print the result as one JSON line")
+    ap.add_argument("--only", choices=["sweep", "gemm-shapes", "decode"],
+                    help="run only the float32 op sweep, the bf16 products of one GPT-2 block at 16384 "
+                         "rows, or the KV-cache decode runs, and print the result as one JSON line")
     args = ap.parse_args()
     if args.only:
         import torch
@@ -683,6 +703,8 @@ def main():
         torch.cuda.init()
         if args.only == "sweep":
             print(json.dumps({"op_sweep": bench_op_sweep()}))
+        elif args.only == "decode":
+            print(json.dumps({"decode": bench_decode_only()}))
         else:
             print(json.dumps({"gemm_bf16_gpt2_b16": bench_gemm_shapes()}))
     elif args.impl == "reference":

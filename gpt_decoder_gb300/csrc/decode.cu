@@ -146,11 +146,17 @@ struct GemvArgs {
 // of X'[b, k] W[k, n] (X' = X or its LayerNorm); the last block of a column block to finish
 // (atomic ticket) adds the slices in slice order and applies bias, residual, GELU and the
 // key/value append. No block waits on another.
+// Offset of the reduction area after the staged rows: rounded up to four floats, so that
+// its float4 stores are aligned.
+__host__ __device__ __forceinline__ int gemv_red_offset(int nb, int kslice) { return (nb * kslice + 3) & ~3; }
+
+// Two blocks per SM (at most 128 registers a thread): a launch of up to 2 x SMs blocks then
+// runs in one wave.
 template <int NB>
-__global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
-    extern __shared__ float sm[];  // Xs[NB][kslice], red[8][NB][128], st[2 * NB]
+__global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) float sm[];  // Xs[NB][kslice], red[8][NB][128], st[2 * NB]
     float* Xs = sm;
-    float* red = sm + NB * a.kslice;
+    float* red = sm + gemv_red_offset(NB, a.kslice);
     float* st = red + 8 * NB * GEMV_COLS;
     __shared__ int last;
     const int s = blockIdx.y;
@@ -197,14 +203,14 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
                 acc[b][3] = fmaf(xv, wpre[i].w, acc[b][3]);
             }
         }
-        // the remaining rows, four in flight per warp (rows k, k + 8, k + 16, k + 24)
+        // the remaining rows, eight in flight per warp (rows k, k + 8, ..., k + 56)
         int k = k0 + warp + 8 * GEMV_PF;
-        for (; k + 24 < k1; k += 32) {
-            float4 w[4];
+        for (; k + 56 < k1; k += 64) {
+            float4 w[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) w[u] = *reinterpret_cast<const float4*>(a.W + (int64_t)(k + 8 * u) * a.ldw + n);
+            for (int u = 0; u < 8; ++u) w[u] = *reinterpret_cast<const float4*>(a.W + (int64_t)(k + 8 * u) * a.ldw + n);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
                     const float xv = Xs[b * a.kslice + (k + 8 * u - k0)];
@@ -229,8 +235,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
     const int col = (threadIdx.x & 31) * 4;
 #pragma unroll
     for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) red[(warp * NB + b) * GEMV_COLS + col + j] = acc[b][j];
+        *reinterpret_cast<float4*>(red + (warp * NB + b) * GEMV_COLS + col) =
+            make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
     __syncthreads();
     for (int e = threadIdx.x; e < NB * GEMV_COLS; e += GEMV_THREADS) {
         const int b = e / GEMV_COLS, c = e % GEMV_COLS;
@@ -250,36 +256,36 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
     const int pos = a.cache ? a.state[0] : 0;
     const int C = a.H * a.hs;
     // this thread's outputs e = threadIdx.x + 256 i (row e / 128, column e % 128 of the block);
-    // each adds the slices in slice order, the loads of all its outputs for four slices in
-    // flight together
+    // each adds the slices in slice order, the loads of all its outputs for SL slices (64 loads
+    // at the wide batches) in flight together
     constexpr int EPT = NB >= 2 ? NB / 2 : 1;
+    constexpr int SL = EPT >= 4 ? 8 : 16;
     const int S = (int)gridDim.y;
     const int64_t step = (int64_t)a.B * a.M;
     float tsum[EPT];
-    const float* src[EPT];
-    bool valid[EPT];
+    int src[EPT];  // offset of the output in a slice's partial sums (B x M < 2^31); -1 past the end
 #pragma unroll
     for (int i = 0; i < EPT; ++i) {
         const int e = threadIdx.x + GEMV_THREADS * i, b = e / GEMV_COLS, nn = blockIdx.x * GEMV_COLS + e % GEMV_COLS;
-        valid[i] = e < NB * GEMV_COLS && b < a.B && nn < a.M;
-        src[i] = a.partial + (int64_t)b * a.M + nn;
+        src[i] = (e < NB * GEMV_COLS && b < a.B && nn < a.M) ? b * a.M + nn : -1;
         tsum[i] = 0.f;
     }
-    for (int q = 0; q < S; q += 4) {
-        float v[EPT][4];
+    for (int q = 0; q < S; q += SL) {
+        float v[EPT][SL];
 #pragma unroll
         for (int i = 0; i < EPT; ++i)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[i][u] = (valid[i] && q + u < S) ? __ldcg(src[i] + (q + u) * step) : 0.f;
+            for (int u = 0; u < SL; ++u)
+                v[i][u] = (src[i] >= 0 && q + u < S) ? __ldcg(a.partial + (q + u) * step + src[i]) : 0.f;
 #pragma unroll
         for (int i = 0; i < EPT; ++i)
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < SL; ++u)
                 if (q + u < S) tsum[i] += v[i][u];
     }
 #pragma unroll
     for (int i = 0; i < EPT; ++i) {
-        if (!valid[i]) continue;
+        if (src[i] < 0) continue;
         const int e = threadIdx.x + GEMV_THREADS * i, b = e / GEMV_COLS, nn = blockIdx.x * GEMV_COLS + e % GEMV_COLS;
         float t = tsum[i];
         if (a.bias) t += a.bias[nn];
@@ -295,6 +301,28 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvArgs a) {
         }
     }
     if (threadIdx.x == 0) a.tickets[blockIdx.x] = 0;  // ready for the next launch
+}
+
+// Sum of v[i] over the 32 lanes for every i < N (N = 32 or 64), spread over the lanes: after
+// the call, lane l holds the sums of i = (N / 32) l + k in v[k], k < N / 32. Level o pairs the
+// lanes that differ in bit o (16 first, as warp_sum does, so each sum is the same as warp_sum's);
+// the lane keeps the half of its values that its bit selects and adds its partner's partial of
+// that half, so a level costs N / 2^(level+1) shuffles instead of N.
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
+    static_assert(N == 32 || N == 64, "32 or 64 values");
+#pragma unroll
+    for (int lv = 0; lv < 5; ++lv) {
+        const int o = 16 >> lv, half = (N >> lv) / 2;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float lo = v[i], hi = v[i + half];
+            const float send = up ? lo : hi;
+            const float keep = up ? hi : lo;
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
 }
 
 // logits[b, v] = sum_c X[b, c] wte[v, c]: one warp per vocabulary row (MatMulT head).
@@ -342,18 +370,35 @@ __global__ void lm_head_kernel(const float* __restrict__ X, const float* __restr
                     acc[r][b] = fmaf(w[r].x, xb.x, fmaf(w[r].y, xb.y, fmaf(w[r].z, xb.z, fmaf(w[r].w, xb.w, acc[r][b]))));
             }
         }
+        if constexpr (NB >= 8) {
+            // the 4 NB sums spread over the lanes: value i = r NB + b, lane l holds
+            // i = (4 NB / 32) l + k
+            constexpr int N = 4 * NB, PER = N / 32;
+            float f[N];
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int b = 0; b < NB; ++b) acc[r][b] = warp_sum(acc[r][b]);
+                for (int b = 0; b < NB; ++b) f[r * NB + b] = acc[r][b];
+            warp_reduce_scatter<N>(f, lane);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            if (lane < NB && lane < B && v0 + r < V) {
-                float o = 0.f;
+            for (int k = 0; k < PER; ++k) {
+                const int i = PER * lane + k, r = i / NB, b = i % NB;
+                if (b < B && v0 + r < V) logits[(int64_t)b * ldl + v0 + r] = f[k];
+            }
+        } else {
 #pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    if (b == lane) o = acc[r][b];
-                logits[(int64_t)lane * ldl + v0 + r] = o;
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int b = 0; b < NB; ++b) acc[r][b] = warp_sum(acc[r][b]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (lane < NB && lane < B && v0 + r < V) {
+                    float o = 0.f;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        if (b == lane) o = acc[r][b];
+                    logits[(int64_t)lane * ldl + v0 + r] = o;
+                }
             }
         }
     }
@@ -390,9 +435,11 @@ __global__ void kv_write_prefill_kernel(const float* __restrict__ qkv, float* __
 // Decode attention, split over key chunks of KCHUNK (flash-decoding): block (chunk, b*H+h)
 // of two warps writes (max, sum, unnormalised output[hs]) of its chunk (no mask: the cache
 // holds the past). Scores: lane = key, the key's row read as float4s; output: lane = head
-// dimension(s), the warp's 32 keys taken in turn (coalesced rows of V). The last chunk of
-// (b, h) to arrive (atomic ticket) combines the chunks in chunk order into y; no block waits
-// on another.
+// dimension(s), the warp's 32 keys taken in turn (coalesced rows of V). For hs <= 64 every
+// load of the chunk (the lane's key row and its two value dimensions of the warp's 32 keys) is
+// issued before the first use, so the chunk costs one round trip to memory. The last chunk of
+// (b, h) to arrive (atomic ticket) combines the chunks in chunk order into y, sixteen chunks'
+// partials in flight at a time; no block waits on another.
 __global__ void __launch_bounds__(64) decode_attn_kernel(const float* __restrict__ qkv,
                                                          const float* __restrict__ cache, int l, int B, int H, int hs,
                                                          int Tmax, const int* __restrict__ state,
@@ -416,62 +463,106 @@ __global__ void __launch_bounds__(64) decode_attn_kernel(const float* __restrict
             out[1] = 0.f;
         }
     } else {
-        for (int d = threadIdx.x; d < hs; d += blockDim.x) q[d] = qkv[(int64_t)b * 3 * C + h * hs + d];
-        __syncthreads();
         const float* K = cache + cache_index(l, 0, b, h, 0, B, H, Tmax, hs);
         const float* Vc = cache + cache_index(l, 1, b, h, 0, B, H, Tmax, hs);
         const int jw = j0 + warp * 32;  // this warp's first key
         const int j = jw + lane;
+        const int nk = max(0, min(32, n - jw));  // keys of this warp
         float sc = -INFINITY;
-        if (j < n) {
-            const float* kr = K + (int64_t)j * hs;
-            float a0 = 0.f, a1 = 0.f;
-            for (int d = 0; d < hs; d += 8) {
-                const float4 k4 = *reinterpret_cast<const float4*>(kr + d);
-                const float4 q4 = *reinterpret_cast<const float4*>(q + d);
-                a0 = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, a0))));
-                if (d + 4 < hs) {
-                    const float4 k5 = *reinterpret_cast<const float4*>(kr + d + 4);
-                    const float4 q5 = *reinterpret_cast<const float4*>(q + d + 4);
-                    a1 = fmaf(q5.x, k5.x, fmaf(q5.y, k5.y, fmaf(q5.z, k5.z, fmaf(q5.w, k5.w, a1))));
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        if (hs <= 64) {
+            float4 kr[16];
+            float v0[32], v1[32];
+            const float* kp = K + (int64_t)(j < n ? j : 0) * hs;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                kr[u] = (j < n && 4 * u < hs) ? *reinterpret_cast<const float4*>(kp + 4 * u)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                v0[t] = (t < nk && lane < hs) ? Vc[(int64_t)(jw + t) * hs + lane] : 0.f;
+                v1[t] = (t < nk && lane + 32 < hs) ? Vc[(int64_t)(jw + t) * hs + lane + 32] : 0.f;
+            }
+            for (int d = threadIdx.x; d < hs; d += blockDim.x) q[d] = qkv[(int64_t)b * 3 * C + h * hs + d];
+            __syncthreads();
+            if (j < n) {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; u += 2) {
+                    if (4 * u < hs) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * u);
+                        a0 = fmaf(q4.x, kr[u].x, fmaf(q4.y, kr[u].y, fmaf(q4.z, kr[u].z, fmaf(q4.w, kr[u].w, a0))));
+                    }
+                    if (4 * u + 4 < hs) {
+                        const float4 q5 = *reinterpret_cast<const float4*>(q + 4 * u + 4);
+                        a1 = fmaf(q5.x, kr[u + 1].x,
+                                  fmaf(q5.y, kr[u + 1].y, fmaf(q5.z, kr[u + 1].z, fmaf(q5.w, kr[u + 1].w, a1))));
+                    }
+                }
+                sc = (a0 + a1) * rsqrtf((float)hs);
+            }
+            float m = warp_max(sc);
+            if (lane == 0) red[0][warp] = m;
+            __syncthreads();
+            m = fmaxf(red[0][0], red[0][1]);
+            const float p = j < n ? expf(sc - m) : 0.f;
+            const float ls = warp_sum(p);
+            if (lane == 0) red[1][warp] = ls;
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                const float pt = __shfl_sync(0xffffffffu, p, t);
+                o[0] = fmaf(t < nk ? pt : 0.f, v0[t], o[0]);
+                o[1] = fmaf(t < nk ? pt : 0.f, v1[t], o[1]);
+            }
+            if (threadIdx.x == 0) out[0] = m;
+        } else {
+            for (int d = threadIdx.x; d < hs; d += blockDim.x) q[d] = qkv[(int64_t)b * 3 * C + h * hs + d];
+            __syncthreads();
+            if (j < n) {
+                const float* kr = K + (int64_t)j * hs;
+                float a0 = 0.f, a1 = 0.f;
+                for (int d = 0; d < hs; d += 8) {
+                    const float4 k4 = *reinterpret_cast<const float4*>(kr + d);
+                    const float4 q4 = *reinterpret_cast<const float4*>(q + d);
+                    a0 = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, fmaf(q4.w, k4.w, a0))));
+                    if (d + 4 < hs) {
+                        const float4 k5 = *reinterpret_cast<const float4*>(kr + d + 4);
+                        const float4 q5 = *reinterpret_cast<const float4*>(q + d + 4);
+                        a1 = fmaf(q5.x, k5.x, fmaf(q5.y, k5.y, fmaf(q5.z, k5.z, fmaf(q5.w, k5.w, a1))));
+                    }
+                }
+                sc = (a0 + a1) * rsqrtf((float)hs);
+            }
+            float m = warp_max(sc);
+            if (lane == 0) red[0][warp] = m;
+            __syncthreads();
+            m = fmaxf(red[0][0], red[0][1]);
+            const float p = j < n ? expf(sc - m) : 0.f;
+            const float ls = warp_sum(p);
+            if (lane == 0) red[1][warp] = ls;
+            // eight keys' rows of V in flight at a time
+            for (int t0 = 0; t0 < nk; t0 += 8) {
+                float vv[8][4];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        vv[u][i] = (t0 + u < nk && lane + 32 * i < hs) ? Vc[(int64_t)(jw + t0 + u) * hs + lane + 32 * i] : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float pt = __shfl_sync(0xffffffffu, p, (t0 + u) & 31);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] = fmaf(t0 + u < nk ? pt : 0.f, vv[u][i], o[i]);
                 }
             }
-            sc = (a0 + a1) * rsqrtf((float)hs);
-        }
-        float m = warp_max(sc);
-        if (lane == 0) red[0][warp] = m;
-        __syncthreads();
-        m = fmaxf(red[0][0], red[0][1]);
-        const float p = j < n ? expf(sc - m) : 0.f;
-        const float ls = warp_sum(p);
-        if (lane == 0) red[1][warp] = ls;
-        // output: lane takes dimensions lane, lane + 32, ...; the warp's keys in turn
-        float o[4] = {0.f, 0.f, 0.f, 0.f};
-        const int nk = max(0, min(32, n - jw));
-        // eight keys' rows of V in flight at a time
-        for (int t0 = 0; t0 < nk; t0 += 8) {
-            float vv[8][4];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    vv[u][i] = (t0 + u < nk && lane + 32 * i < hs) ? Vc[(int64_t)(jw + t0 + u) * hs + lane + 32 * i] : 0.f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float pt = __shfl_sync(0xffffffffu, p, (t0 + u) & 31);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) o[i] = fmaf(t0 + u < nk ? pt : 0.f, vv[u][i], o[i]);
-            }
+            if (threadIdx.x == 0) out[0] = m;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             if (lane + 32 * i < hs) ored[warp][lane + 32 * i] = o[i];
         __syncthreads();
         for (int d = threadIdx.x; d < hs; d += blockDim.x) out[2 + d] = ored[0][d] + ored[1][d];
-        if (threadIdx.x == 0) {
-            out[0] = m;
-            out[1] = red[1][0] + red[1][1];
-        }
+        if (threadIdx.x == 0) out[1] = red[1][0] + red[1][1];
     }
     __threadfence();
     __syncthreads();
@@ -479,22 +570,45 @@ __global__ void __launch_bounds__(64) decode_attn_kernel(const float* __restrict
     __syncthreads();
     if (!last) return;
     __threadfence();
+    // every thread: the chunks' maxima and sums (the same for all), and its output dimensions
+    // d = threadIdx.x, + 64; sixteen chunks' loads in flight at a time. One pass when
+    // nchunks <= 16 (the global maximum first); beyond that the running maximum rescales.
     const float* pp = part + (int64_t)bh * nchunks * (hs + 2);
-    float M = -INFINITY;
-    for (int c = 0; c < nchunks; ++c) M = fmaxf(M, __ldcg(pp + c * (hs + 2)));
-    float L = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
-        const float mc = __ldcg(pp + c * (hs + 2));
-        if (mc != -INFINITY) L += __ldcg(pp + c * (hs + 2) + 1) * expf(mc - M);
-    }
-    for (int d = threadIdx.x; d < hs; d += blockDim.x) {
-        float o = 0.f;
-        for (int c = 0; c < nchunks; ++c) {
-            const float mc = __ldcg(pp + c * (hs + 2));
-            if (mc != -INFINITY) o += __ldcg(pp + c * (hs + 2) + 2 + d) * expf(mc - M);
+    const int d0 = threadIdx.x, d1 = threadIdx.x + 64;
+    float M = -INFINITY, L = 0.f, od0 = 0.f, od1 = 0.f;
+    for (int c0 = 0; c0 < nchunks; c0 += 16) {
+        float mc[16], lc[16], p0[16], p1[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int c = c0 + u;
+            const bool in = c < nchunks;
+            mc[u] = in ? __ldcg(pp + (int64_t)c * (hs + 2)) : -INFINITY;
+            lc[u] = in ? __ldcg(pp + (int64_t)c * (hs + 2) + 1) : 0.f;
+            p0[u] = (in && d0 < hs) ? __ldcg(pp + (int64_t)c * (hs + 2) + 2 + d0) : 0.f;
+            p1[u] = (in && d1 < hs) ? __ldcg(pp + (int64_t)c * (hs + 2) + 2 + d1) : 0.f;
         }
-        y[(int64_t)b * C + h * hs + d] = o / L;
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) Mb = fmaxf(Mb, mc[u]);
+        if (Mb > M && M != -INFINITY) {
+            const float r = expf(M - Mb);
+            L *= r;
+            od0 *= r;
+            od1 *= r;
+        }
+        M = Mb;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            if (mc[u] != -INFINITY) {
+                const float e = expf(mc[u] - M);
+                L += lc[u] * e;
+                od0 += p0[u] * e;
+                od1 += p1[u] * e;
+            }
+        }
     }
+    if (d0 < hs) y[(int64_t)b * C + h * hs + d0] = od0 / L;
+    if (d1 < hs) y[(int64_t)b * C + h * hs + d1] = od1 / L;
     if (threadIdx.x == 0) tickets[bh] = 0;  // ready for the next launch
 }
 
@@ -743,7 +857,7 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
     S = (int)cdiv(K, kslice);
     GK_REQUIRE(ctx, (size_t)S * B * M <= kv->partial_floats, GK_ERR_WORKSPACE, "decode gemv: partial buffer too small");
     int nb = gemv_nb(B);
-    size_t smem = ((size_t)nb * kslice + 8 * (size_t)nb * GEMV_COLS + 2 * (size_t)nb) * sizeof(float);
+    size_t smem = ((size_t)gemv_red_offset(nb, kslice) + 8 * (size_t)nb * GEMV_COLS + 2 * (size_t)nb) * sizeof(float);
     GemvArgs a;
     a.X = X; a.ldx = ldx; a.ln_g = ln_g; a.ln_b = ln_b; a.W = W; a.ldw = ldw;
     a.B = B; a.K = K; a.M = M; a.kslice = kslice;

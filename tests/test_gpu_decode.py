@@ -59,7 +59,7 @@ def _teacher_forced(gkctx, s, B, Tp, n_steps, seed):
     return err, int(mismatch.sum()), int(near.sum()), got_ids, picks
 
 
-@pytest.mark.parametrize("B", [1, 2, 4])
+@pytest.mark.parametrize("B", [1, 2, 4, 8])  # 8: the batch-8 GEMVs and LM head of the per-layer launches
 def test_tiny_decode_teacher_forced(gkctx, B):
     err, mism, near, _, _ = _teacher_forced(gkctx, synth.TINY, B, 20, 40, 3)
     assert err <= 5e-4

@@ -50,6 +50,47 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// The same with the blocks grouped in clusters of cluster_y blocks along y (the K slices of one
+// column block of a GEMV).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               int cluster_y, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 1;
+    at[1].val.clusterDim.y = (unsigned)cluster_y;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Cluster helpers: every thread of every block of the cluster arrives, then waits (release /
+// acquire at cluster scope); the shared::cluster address of `p` (this block's shared memory) in
+// block `rank` of the cluster; a float32 load from such an address.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ int64_t cache_index(int l, int kv, int b, int h, int t, int B, int H, int Tmax, int hs) {
     return ((((int64_t)(l * 2 + kv) * B + b) * H + h) * Tmax + t) * hs;
 }
@@ -142,102 +183,11 @@ struct GemvArgs {
     const int* state;
 };
 
-// Split-K GEMV: block (column block, slice s) forms partial[s][b][n] = sum over k in slice s
-// of X'[b, k] W[k, n] (X' = X or its LayerNorm); the last block of a column block to finish
-// (atomic ticket) adds the slices in slice order and applies bias, residual, GELU and the
-// key/value append. No block waits on another.
-// Offset of the reduction area after the staged rows: rounded up to four floats, so that
-// its float4 stores are aligned.
-__host__ __device__ __forceinline__ int gemv_red_offset(int nb, int kslice) { return (nb * kslice + 3) & ~3; }
-
-// Two blocks per SM (at most 128 registers a thread): a launch of up to 2 x SMs blocks then
-// runs in one wave.
+// The non-cluster finish of gemv_kernel: the block's sums to partial[s], then the last block of
+// the column block (atomic ticket) adds the slices in slice order and applies the epilogue.
 template <int NB>
-__global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const GemvArgs a) {
-    extern __shared__ __align__(16) float sm[];  // Xs[NB][kslice], red[8][NB][128], st[2 * NB]
-    float* Xs = sm;
-    float* red = sm + gemv_red_offset(NB, a.kslice);
-    float* st = red + 8 * NB * GEMV_COLS;
+__device__ __forceinline__ void gemv_finish_by_ticket(const GemvArgs& a, const float* red, int s) {
     __shared__ int last;
-    const int s = blockIdx.y;
-    const int k0 = s * a.kslice, k1 = min(a.K, k0 + a.kslice);
-    const int n = blockIdx.x * GEMV_COLS + (threadIdx.x & 31) * 4;
-    const int warp = threadIdx.x >> 5;
-    pdl_trigger();
-    // this warp's first weight rows (k0 + warp + 8 i) while the previous kernel finishes
-    float4 wpre[GEMV_PF];
-#pragma unroll
-    for (int i = 0; i < GEMV_PF; ++i) {
-        const int k = k0 + warp + 8 * i;
-        wpre[i] = (n < a.M && k < k1) ? *reinterpret_cast<const float4*>(a.W + (int64_t)k * a.ldw + n)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    pdl_wait();
-    if (a.ln_g) {
-        row_stats(a.X, a.ldx, a.B, a.K, st);
-        __syncthreads();
-    }
-    for (int e = threadIdx.x; e < NB * a.kslice; e += GEMV_THREADS) {
-        const int b = e / a.kslice, k = k0 + e % a.kslice;
-        float v = 0.f;
-        if (b < a.B && k < k1) {
-            v = a.X[(int64_t)b * a.ldx + k];
-            if (a.ln_g) v = (v - st[2 * b]) * st[2 * b + 1] * a.ln_g[k] + a.ln_b[k];
-        }
-        Xs[e] = v;
-    }
-    __syncthreads();
-    float acc[NB][4];
-#pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
-    if (n < a.M) {
-#pragma unroll
-        for (int i = 0; i < GEMV_PF; ++i) {
-            const int kk = warp + 8 * i;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const float xv = k0 + kk < k1 ? Xs[b * a.kslice + kk] : 0.f;
-                acc[b][0] = fmaf(xv, wpre[i].x, acc[b][0]);
-                acc[b][1] = fmaf(xv, wpre[i].y, acc[b][1]);
-                acc[b][2] = fmaf(xv, wpre[i].z, acc[b][2]);
-                acc[b][3] = fmaf(xv, wpre[i].w, acc[b][3]);
-            }
-        }
-        // the remaining rows, eight in flight per warp (rows k, k + 8, ..., k + 56)
-        int k = k0 + warp + 8 * GEMV_PF;
-        for (; k + 56 < k1; k += 64) {
-            float4 w[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) w[u] = *reinterpret_cast<const float4*>(a.W + (int64_t)(k + 8 * u) * a.ldw + n);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const float xv = Xs[b * a.kslice + (k + 8 * u - k0)];
-                    acc[b][0] = fmaf(xv, w[u].x, acc[b][0]);
-                    acc[b][1] = fmaf(xv, w[u].y, acc[b][1]);
-                    acc[b][2] = fmaf(xv, w[u].z, acc[b][2]);
-                    acc[b][3] = fmaf(xv, w[u].w, acc[b][3]);
-                }
-        }
-        for (; k < k1; k += 8) {
-            const float4 w = *reinterpret_cast<const float4*>(a.W + (int64_t)k * a.ldw + n);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const float xv = Xs[b * a.kslice + (k - k0)];
-                acc[b][0] = fmaf(xv, w.x, acc[b][0]);
-                acc[b][1] = fmaf(xv, w.y, acc[b][1]);
-                acc[b][2] = fmaf(xv, w.z, acc[b][2]);
-                acc[b][3] = fmaf(xv, w.w, acc[b][3]);
-            }
-        }
-    }
-    const int col = (threadIdx.x & 31) * 4;
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-        *reinterpret_cast<float4*>(red + (warp * NB + b) * GEMV_COLS + col) =
-            make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
-    __syncthreads();
     for (int e = threadIdx.x; e < NB * GEMV_COLS; e += GEMV_THREADS) {
         const int b = e / GEMV_COLS, c = e % GEMV_COLS;
         const int nn = blockIdx.x * GEMV_COLS + c;
@@ -302,6 +252,146 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const GemvArgs a)
     }
     if (threadIdx.x == 0) a.tickets[blockIdx.x] = 0;  // ready for the next launch
 }
+
+// Split-K GEMV: block (column block, slice s) forms the sums over k in slice s of
+// X'[b, k] W[k, n] (X' = X or its LayerNorm) for the block's 128 columns and every row b. CL: the
+// slices of a column block form one cluster; each keeps its sums in its shared memory, and after
+// a cluster barrier block s adds the S slices' sums of its share of the outputs (in slice order,
+// read from the other blocks' shared memory) and applies bias, residual, GELU and the key/value
+// append. Otherwise the sums go to partial[s][b][n] and the last block of a column block to
+// finish (atomic ticket) adds the slices in slice order and applies the epilogue. No block
+// waits on another outside its cluster.
+// Offset of the reduction area after the staged rows: rounded up to four floats, so that
+// its float4 stores are aligned.
+__host__ __device__ __forceinline__ int gemv_red_offset(int nb, int kslice) { return (nb * kslice + 3) & ~3; }
+
+// Two blocks per SM (at most 128 registers a thread): a launch of up to 2 x SMs blocks then
+// runs in one wave.
+template <int NB, bool CL>
+__global__ void __launch_bounds__(GEMV_THREADS, 2) gemv_kernel(const GemvArgs a) {
+    // Xs[NB][kslice], red[8][NB][128], st[2 * NB] (padded to four floats), fin[NB][128] (CL)
+    extern __shared__ __align__(16) float sm[];
+    float* Xs = sm;
+    float* red = sm + gemv_red_offset(NB, a.kslice);
+    float* st = red + 8 * NB * GEMV_COLS;
+    float* fin = st + ((2 * NB + 3) & ~3);
+    const int s = blockIdx.y;
+    const int k0 = s * a.kslice, k1 = min(a.K, k0 + a.kslice);
+    const int n = blockIdx.x * GEMV_COLS + (threadIdx.x & 31) * 4;
+    const int warp = threadIdx.x >> 5;
+    pdl_trigger();
+    // this warp's first weight rows (k0 + warp + 8 i) while the previous kernel finishes
+    float4 wpre[GEMV_PF];
+#pragma unroll
+    for (int i = 0; i < GEMV_PF; ++i) {
+        const int k = k0 + warp + 8 * i;
+        wpre[i] = (n < a.M && k < k1) ? *reinterpret_cast<const float4*>(a.W + (int64_t)k * a.ldw + n)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
+    if (a.ln_g) {
+        row_stats(a.X, a.ldx, a.B, a.K, st);
+        __syncthreads();
+    }
+    for (int e = threadIdx.x; e < NB * a.kslice; e += GEMV_THREADS) {
+        const int b = e / a.kslice, k = k0 + e % a.kslice;
+        float v = 0.f;
+        if (b < a.B && k < k1) {
+            v = a.X[(int64_t)b * a.ldx + k];
+            if (a.ln_g) v = (v - st[2 * b]) * st[2 * b + 1] * a.ln_g[k] + a.ln_b[k];
+        }
+        Xs[e] = v;
+    }
+    __syncthreads();
+    float acc[NB][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
+    if (n < a.M) {
+#pragma unroll
+        for (int i = 0; i < GEMV_PF; ++i) {
+            const int kk = warp + 8 * i;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float xv = k0 + kk < k1 ? Xs[b * a.kslice + kk] : 0.f;
+                acc[b][0] = fmaf(xv, wpre[i].x, acc[b][0]);
+                acc[b][1] = fmaf(xv, wpre[i].y, acc[b][1]);
+                acc[b][2] = fmaf(xv, wpre[i].z, acc[b][2]);
+                acc[b][3] = fmaf(xv, wpre[i].w, acc[b][3]);
+            }
+        }
+        // the remaining rows, eight in flight per warp (rows k, k + 8, ..., k + 56 below k1; the
+        // row is the same for the whole warp)
+        for (int k = k0 + warp + 8 * GEMV_PF; k < k1; k += 64) {
+            float4 w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                w[u] = k + 8 * u < k1 ? *reinterpret_cast<const float4*>(a.W + (int64_t)(k + 8 * u) * a.ldw + n)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (k + 8 * u >= k1) break;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float xv = Xs[b * a.kslice + (k + 8 * u - k0)];
+                    acc[b][0] = fmaf(xv, w[u].x, acc[b][0]);
+                    acc[b][1] = fmaf(xv, w[u].y, acc[b][1]);
+                    acc[b][2] = fmaf(xv, w[u].z, acc[b][2]);
+                    acc[b][3] = fmaf(xv, w[u].w, acc[b][3]);
+                }
+            }
+        }
+    }
+    const int col = (threadIdx.x & 31) * 4;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+        *reinterpret_cast<float4*>(red + (warp * NB + b) * GEMV_COLS + col) =
+            make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+    __syncthreads();
+    if constexpr (CL) {
+        for (int e = threadIdx.x; e < NB * GEMV_COLS; e += GEMV_THREADS) {
+            const int b = e / GEMV_COLS, c = e % GEMV_COLS;
+            float t = 0.f;
+            for (int w = 0; w < 8; ++w) t += red[(w * NB + b) * GEMV_COLS + c];
+            fin[e] = t;
+        }
+        cluster_barrier();  // every slice's sums are in its block's shared memory
+        const int S = (int)gridDim.y;  // the cluster: the column block's S slices, rank = slice
+        const int per = (NB * GEMV_COLS + S - 1) / S;
+        const int e_end = min(NB * GEMV_COLS, (s + 1) * per);
+        const int pos = a.cache ? a.state[0] : 0;
+        const int C = a.H * a.hs;
+        for (int e = s * per + (int)threadIdx.x; e < e_end; e += GEMV_THREADS) {
+            const int b = e / GEMV_COLS, nn = blockIdx.x * GEMV_COLS + e % GEMV_COLS;
+            const bool valid = b < a.B && nn < a.M;
+            // the epilogue's operands requested with the slices' sums
+            const float bias = (valid && a.bias) ? a.bias[nn] : 0.f;
+            const float res = (valid && a.residual) ? a.residual[(int64_t)b * a.ldy + nn] : 0.f;
+            float v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] = u < S ? ld_cluster_f32(cluster_addr(fin + e, (uint32_t)u)) : 0.f;
+            float t = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (u < S) t += v[u];
+            if (!valid) continue;
+            if (a.bias) t += bias;
+            if (a.residual) t += res;
+            if (a.act == GK_ACT_GELU) {
+                if (a.preact) a.preact[(int64_t)b * a.M + nn] = t;
+                t = gelu_tanh(t);
+            }
+            a.Y[(int64_t)b * a.ldy + nn] = t;
+            if (a.cache && nn >= C && pos < a.Tmax) {
+                const int which = nn / C - 1, c = nn % C;
+                a.cache[cache_index(a.layer, which, b, c / a.hs, pos, a.B, a.H, a.Tmax, a.hs) + c % a.hs] = t;
+            }
+        }
+        cluster_barrier();  // no block leaves while another may still read its shared memory
+    } else {
+        gemv_finish_by_ticket<NB>(a, red, s);
+    }
+}
+
 
 // Sum of v[i] over the 32 lanes for every i < N (N = 32 or 64), spread over the lanes: after
 // the call, lane l holds the sums of i = (N / 32) l + k in v[k], k < N / 32. Level o pairs the
@@ -838,6 +928,41 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
 
 int gemv_nb(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16; }
 
+// Whether clusters of cs GEMV blocks (NB rows, smem bytes each) can be placed on this GPU.
+template <int NB>
+bool gemv_cluster_fits_nb(dim3 grid, size_t smem, int cs) {
+    auto k = gemv_kernel<NB, true>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
+    if (cs > 8 && cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return false;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(GEMV_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = (unsigned)cs;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    return cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n >= 1;
+}
+bool gemv_cluster_fits(gk_ctx* ctx, int nb, dim3 grid, size_t smem, int cs) {
+    bool ok = false;
+    switch (nb) {
+        case 1: ok = gemv_cluster_fits_nb<1>(grid, smem, cs); break;
+        case 2: ok = gemv_cluster_fits_nb<2>(grid, smem, cs); break;
+        case 4: ok = gemv_cluster_fits_nb<4>(grid, smem, cs); break;
+        case 8: ok = gemv_cluster_fits_nb<8>(grid, smem, cs); break;
+        default: ok = gemv_cluster_fits_nb<16>(grid, smem, cs); break;
+    }
+    cudaGetLastError();  // a refused query leaves no error behind
+    (void)ctx;
+    return ok;
+}
+
 // Y [B, M] = act(LN?(X) W + bias + residual), one launch (see gemv_kernel); append_layer >= 0
 // also appends the key/value columns to that layer of the cache.
 gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float* ln_g, const float* ln_b,
@@ -846,18 +971,33 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
     int B = kv->B;
     int colblocks = (int)cdiv(M, GEMV_COLS);
     GK_REQUIRE(ctx, colblocks <= 1024, GK_ERR_UNSUPPORTED, "decode gemv: %d columns", M);
-    // K slices: enough blocks for two per SM; at wide batches (more arithmetic per weight row,
-    // and every slice adds B x 128 partial sums for the finishing block to read) each slice
-    // keeps at least 64 rows
-    // (at least 128 rows for long K at wide batches: the finishing block reads S x B x 128
-    // partial sums, S / 4 rounds of loads)
-    const int min_rows = B >= 4 ? (K >= 2048 ? 128 : 64) : 8;
-    int S = (int)std::max<int64_t>(1, std::min<int64_t>(K / min_rows, cdiv(2 * ctx->num_sms, colblocks)));
+    int nb = gemv_nb(B);
+    // Clusters: the K slices of a column block as one cluster of S blocks (a power of two up to
+    // 16), the most whose grid still fits one wave at two blocks per SM with at least 8 rows per
+    // slice, if the GPU can place such a cluster.
+    int S = 0;
+    for (int cs = 16; cs >= 2 && !S; cs >>= 1) {
+        if ((int64_t)colblocks * cs > 2 * ctx->num_sms || K / cs < 8) continue;
+        const int ks = (int)cdiv(K, cs);
+        if (cdiv(K, ks) != cs) continue;  // every slice non-empty
+        const size_t sm = ((size_t)gemv_red_offset(nb, ks) + 8 * (size_t)nb * GEMV_COLS + ((2 * nb + 3) & ~3) +
+                           (size_t)nb * GEMV_COLS) * sizeof(float);
+        if (gemv_cluster_fits(ctx, nb, dim3(colblocks, cs), sm, cs)) S = cs;
+    }
+    const bool cl = S > 0;
+    if (!cl) {
+        // K slices: enough blocks for two per SM; at wide batches (more arithmetic per weight
+        // row, and every slice adds B x 128 partial sums for the finishing block to read) each
+        // slice keeps at least 64 rows (128 for long K)
+        const int min_rows = B >= 4 ? (K >= 2048 ? 128 : 64) : 8;
+        S = (int)std::max<int64_t>(1, std::min<int64_t>(K / min_rows, cdiv(2 * ctx->num_sms, colblocks)));
+    }
     int kslice = (int)cdiv(K, S);
     S = (int)cdiv(K, kslice);
-    GK_REQUIRE(ctx, (size_t)S * B * M <= kv->partial_floats, GK_ERR_WORKSPACE, "decode gemv: partial buffer too small");
-    int nb = gemv_nb(B);
-    size_t smem = ((size_t)gemv_red_offset(nb, kslice) + 8 * (size_t)nb * GEMV_COLS + 2 * (size_t)nb) * sizeof(float);
+    GK_REQUIRE(ctx, cl || (size_t)S * B * M <= kv->partial_floats, GK_ERR_WORKSPACE,
+               "decode gemv: partial buffer too small");
+    size_t smem = ((size_t)gemv_red_offset(nb, kslice) + 8 * (size_t)nb * GEMV_COLS + ((2 * nb + 3) & ~3) +
+                   (cl ? (size_t)nb * GEMV_COLS : 0)) * sizeof(float);
     GemvArgs a;
     a.X = X; a.ldx = ldx; a.ln_g = ln_g; a.ln_b = ln_b; a.W = W; a.ldw = ldw;
     a.B = B; a.K = K; a.M = M; a.kslice = kslice;
@@ -866,15 +1006,22 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
     a.cache = append_layer >= 0 ? kv->cache : nullptr;
     a.layer = append_layer; a.H = kv->cfg.H; a.hs = kv->cfg.C / kv->cfg.H; a.Tmax = kv->Tmax; a.state = kv->state;
     dim3 grid(colblocks, S);
+    cudaError_t e = cudaSuccess;
 #define GEMV_CASE(NBV)                                                                                       \
     case NBV:                                                                                                \
-        cudaFuncSetAttribute(gemv_kernel<NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
-        launch_pdl(gemv_kernel<NBV>, grid, dim3(GEMV_THREADS), smem, ctx->stream, a);                       \
+        if (cl) {                                                                                            \
+            cudaFuncSetAttribute(gemv_kernel<NBV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+            e = launch_pdl_cluster(gemv_kernel<NBV, true>, grid, dim3(GEMV_THREADS), smem, ctx->stream, S, a); \
+        } else {                                                                                             \
+            cudaFuncSetAttribute(gemv_kernel<NBV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+            e = launch_pdl(gemv_kernel<NBV, false>, grid, dim3(GEMV_THREADS), smem, ctx->stream, a);      \
+        }                                                                                                    \
         break;
     switch (nb) {
         GEMV_CASE(1) GEMV_CASE(2) GEMV_CASE(4) GEMV_CASE(8) GEMV_CASE(16)
     }
 #undef GEMV_CASE
+    if (e != cudaSuccess) return fail(ctx, GK_ERR_CUDA, "decode gemv launch failed: %s", cudaGetErrorString(e));
     return launched(ctx, "gemv");
 }
 

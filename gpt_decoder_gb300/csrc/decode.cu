@@ -775,9 +775,12 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 constexpr int SEL_THREADS = 1024;
 
 // One block per batch row. Greedy: lowest index of the maximum. Top-k: the k-th largest
-// value by a 4-pass radix select on ordered keys, keep l >= it (ties kept), weights
-// exp((l - max)/T) in float64, running sum over ascending indices (contiguous segments per
-// thread, combined in thread order), first index whose running sum exceeds u * total.
+// value by a 4-pass radix select on ordered keys (each pass's bin found by a parallel scan of
+// the 256 counts), keep l >= it (ties kept), weights exp((l - max)/T) in float64, running sum
+// over ascending indices, first index whose running sum exceeds u * total. The running sum is
+// taken per warp range: warp w owns indices [w R, (w + 1) R) (lanes on consecutive indices),
+// the warps' totals locate the range where u * total falls, and that warp walks its range in
+// index order, 32 indices at a time by a warp scan.
 __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __restrict__ logits, int64_t ld, int V,
                                                              int top_k, float temperature, uint64_t seed,
                                                              uint64_t counter, const int* __restrict__ state,
@@ -785,9 +788,10 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
     pdl_trigger();
     pdl_wait();
     __shared__ unsigned hist[256];
+    __shared__ unsigned wtot[8];
     __shared__ float fred[32];
     __shared__ int ired[32];
-    __shared__ double dscan[SEL_THREADS];
+    __shared__ double dscan[33];
     __shared__ uint32_t prefix_s, want_s;
     __shared__ int pick_s;
     int b = blockIdx.x;
@@ -860,67 +864,92 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
                 }
             }
             __syncthreads();
-            if (threadIdx.x == 0) {
-                uint32_t want = want_s, cum = 0;
-                int d = 255;
-                for (; d > 0; --d) {
-                    if (cum + hist[d] >= want) break;
-                    cum += hist[d];
+            // the bin of the want-th largest key: thread t < 256 takes bin 255 - t, and P(t), the
+            // count of bins 255 - t .. 255 (inclusive scan over t), first reaches want at
+            // t* = #{t : P(t) < want}; the keys above that bin number P(t*) - count(t*)
+            const uint32_t want = want_s;
+            uint32_t pt = 0, h = 0;
+            if (threadIdx.x < 256) {
+                h = hist[255 - threadIdx.x];
+                pt = h;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t nb = __shfl_up_sync(0xffffffffu, pt, o);
+                    if (lane >= o) pt += nb;
                 }
-                want_s = want - cum;
-                prefix_s = pre | ((uint32_t)d << shift);
+                if (lane == 31) wtot[warp] = pt;
+            }
+            __syncthreads();
+            if (threadIdx.x < 256)
+                for (int w = 0; w < warp; ++w) pt += wtot[w];
+            const int ts = min(__syncthreads_count(threadIdx.x < 256 && pt < want), 255);
+            if ((int)threadIdx.x == ts) {
+                want_s = want - (pt - h);
+                prefix_s = pre | ((uint32_t)(255 - ts) << shift);
             }
             __syncthreads();
         }
         kth = key_float(prefix_s);
     }
-    // float64 weights over contiguous index segments, running sums in index order
-    int seg = (V + SEL_THREADS - 1) / SEL_THREADS;
-    int i0 = threadIdx.x * seg, i1 = min(V, i0 + seg);
-    double inv_t = 1.0 / (double)temperature;
+    // float64 weights of the kept logits, summed per warp range (lanes on consecutive indices)
+    const int R = ((V + 31) / 32 + 31) / 32 * 32;  // V / 32 rounded up to a multiple of 32
+    const int r0 = warp * R, r1 = min(V, r0 + R);
+    const double inv_t = 1.0 / (double)temperature;
     double local = 0.0;
-    for (int i = i0; i < i1; ++i) {
-        float v = x[i];
+    for (int i = r0 + lane; i < r1; i += 32) {
+        const float v = x[i];
         if (v >= kth) local += exp(((double)v - (double)mx) * inv_t);
     }
-    dscan[threadIdx.x] = local;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+    if (lane == 0) dscan[warp] = local;
+    if (threadIdx.x == 0) pick_s = -1;
     __syncthreads();
     if (threadIdx.x == 0) {
         double run = 0.0;
-        for (int t = 0; t < SEL_THREADS; ++t) {
-            double s = dscan[t];
+        for (int t = 0; t < SEL_THREADS / 32; ++t) {
+            const double sw = dscan[t];
             dscan[t] = run;  // exclusive prefix
-            run += s;
+            run += sw;
         }
         uint32_t w0 = philox_word0((uint32_t)(counter + (uint64_t)state[1]), (uint32_t)b, 0u, 0u, (uint32_t)seed,
                                    (uint32_t)(seed >> 32));
         double u = (double)(w0 >> 8) * (1.0 / 16777216.0);
         double target = u * run;
-        pick_s = -1;
-        // the segment where the running sum first exceeds the target
-        int t = SEL_THREADS - 1;
+        // the last range whose prefix does not exceed the target
+        int t = SEL_THREADS / 32 - 1;
         while (t > 0 && dscan[t] > target) --t;
-        fred[1] = 0.f;
         ired[1] = t;
-        dscan[0] = target;  // reuse slot 0 for the target (segment 0's prefix is 0)
-        ired[2] = 0;
+        dscan[32] = target;
     }
     __syncthreads();
-    if ((int)threadIdx.x == ired[1]) {
-        double target = dscan[0];
-        double run = threadIdx.x == 0 ? 0.0 : dscan[threadIdx.x];
+    if (warp == ired[1]) {
+        // this range in index order: the first kept index whose running sum exceeds the target
+        // (the last kept one if rounding leaves the sum at or below it)
+        const double target = dscan[32];
+        double run = dscan[warp];
         int last_kept = -1, chosen = -1;
-        for (int i = i0; i < i1; ++i) {
-            float v = x[i];
-            if (!(v >= kth)) continue;
-            last_kept = i;
-            run += exp(((double)v - (double)mx) * inv_t);
-            if (run > target) {
-                chosen = i;
-                break;
+        for (int i0 = r0; i0 < r1 && chosen < 0; i0 += 32) {
+            const int i = i0 + lane;
+            const float v = i < r1 ? x[i] : -INFINITY;
+            const bool kept = i < r1 && v >= kth;
+            const unsigned kb = __ballot_sync(0xffffffffu, kept);
+            if (!kb) continue;
+            double sc = kept ? exp(((double)v - (double)mx) * inv_t) : 0.0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double nb = __shfl_up_sync(0xffffffffu, sc, o);
+                if (lane >= o) sc += nb;
+            }
+            const unsigned over = __ballot_sync(0xffffffffu, kept && run + sc > target);
+            if (over) {
+                chosen = i0 + __ffs(over) - 1;
+            } else {
+                last_kept = i0 + 31 - __clz(kb);
+                run += __shfl_sync(0xffffffffu, sc, 31);
             }
         }
-        pick_s = chosen >= 0 ? chosen : last_kept;
+        if (lane == 0) pick_s = chosen >= 0 ? chosen : last_kept;
     }
     __syncthreads();
     if (threadIdx.x == 0) next[b] = pick_s >= 0 ? pick_s : ired[0];

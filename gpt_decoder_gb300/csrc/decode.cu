@@ -418,7 +418,7 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
 // logits[b, v] = sum_c X[b, c] wte[v, c]: one warp per vocabulary row (MatMulT head).
 // With ln_g, the rows of X go through LayerNorm(ln_g, ln_b) first (ln_f fused in).
 template <int NB>
-__global__ void lm_head_kernel(const float* __restrict__ X, const float* __restrict__ ln_g,
+__global__ void __launch_bounds__(256, 2) lm_head_kernel(const float* __restrict__ X, const float* __restrict__ ln_g,
                                const float* __restrict__ ln_b, const float* __restrict__ wte, int B, int C, int V,
                                float* __restrict__ logits, int64_t ldl) {
     pdl_trigger();
@@ -438,35 +438,46 @@ __global__ void lm_head_kernel(const float* __restrict__ X, const float* __restr
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
-    // four vocabulary rows per warp and pass: each x value read from shared memory serves four
-    // weight values
-    for (int v0 = (blockIdx.x * warps + (threadIdx.x >> 5)) * 4; v0 < V; v0 += gridDim.x * warps * 4) {
-        float acc[4][NB];
+    // two vocabulary rows per warp and pass; every weight load of a 768-column tile (six float4
+    // a lane and row) is issued before the first use, so a pass waits for memory once per tile
+    constexpr int RH = 2, CT = 6;
+    for (int v0 = (blockIdx.x * warps + (threadIdx.x >> 5)) * RH; v0 < V; v0 += gridDim.x * warps * RH) {
+        float acc[RH][NB];
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < RH; ++r)
 #pragma unroll
             for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
-        for (int c = lane * 4; c < C; c += 128) {
-            float4 w[4];
+        for (int cb = 0; cb < C; cb += 128 * CT) {
+            float4 w[RH][CT];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                w[r] = v0 + r < V ? *reinterpret_cast<const float4*>(wte + (int64_t)(v0 + r) * C + c)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < RH; ++r)
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const float4 xb = *reinterpret_cast<const float4*>(xs + b * C + c);
+                for (int i = 0; i < CT; ++i) {
+                    const int c = cb + i * 128 + lane * 4;
+                    w[r][i] = (v0 + r < V && c < C) ? *reinterpret_cast<const float4*>(wte + (int64_t)(v0 + r) * C + c)
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    acc[r][b] = fmaf(w[r].x, xb.x, fmaf(w[r].y, xb.y, fmaf(w[r].z, xb.z, fmaf(w[r].w, xb.w, acc[r][b]))));
+            for (int i = 0; i < CT; ++i) {
+                const int c = cb + i * 128 + lane * 4;
+                if (c >= C) break;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float4 xb = *reinterpret_cast<const float4*>(xs + b * C + c);
+#pragma unroll
+                    for (int r = 0; r < RH; ++r)
+                        acc[r][b] = fmaf(w[r][i].x, xb.x,
+                                         fmaf(w[r][i].y, xb.y, fmaf(w[r][i].z, xb.z, fmaf(w[r][i].w, xb.w, acc[r][b]))));
+                }
             }
         }
-        if constexpr (NB >= 8) {
-            // the 4 NB sums spread over the lanes: value i = r NB + b, lane l holds
-            // i = (4 NB / 32) l + k
-            constexpr int N = 4 * NB, PER = N / 32;
+        if constexpr (RH * NB == 32 || RH * NB == 64) {
+            // the RH NB sums spread over the lanes: value i = r NB + b, lane l holds
+            // i = (RH NB / 32) l + k
+            constexpr int N = RH * NB, PER = N / 32;
             float f[N];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < RH; ++r)
 #pragma unroll
                 for (int b = 0; b < NB; ++b) f[r * NB + b] = acc[r][b];
             warp_reduce_scatter<N>(f, lane);
@@ -477,11 +488,11 @@ __global__ void lm_head_kernel(const float* __restrict__ X, const float* __restr
             }
         } else {
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < RH; ++r)
 #pragma unroll
                 for (int b = 0; b < NB; ++b) acc[r][b] = warp_sum(acc[r][b]);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
+            for (int r = 0; r < RH; ++r) {
                 if (lane < NB && lane < B && v0 + r < V) {
                     float o = 0.f;
 #pragma unroll
@@ -957,7 +968,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
 
 int gemv_nb(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16; }
 
-// Whether clusters of cs GEMV blocks (NB rows, smem bytes each) can be placed on this GPU.
+// Whether every cluster of the grid (clusters of cs GEMV blocks, NB rows, smem bytes each) can
+// be resident at once on this GPU: one wave.
 template <int NB>
 bool gemv_cluster_fits_nb(dim3 grid, size_t smem, int cs) {
     auto k = gemv_kernel<NB, true>;
@@ -976,7 +988,8 @@ bool gemv_cluster_fits_nb(dim3 grid, size_t smem, int cs) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    return cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n >= 1;
+    return cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess &&
+           (int64_t)n * cs >= (int64_t)grid.x * grid.y;
 }
 bool gemv_cluster_fits(gk_ctx* ctx, int nb, dim3 grid, size_t smem, int cs) {
     bool ok = false;
@@ -1002,8 +1015,9 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
     GK_REQUIRE(ctx, colblocks <= 1024, GK_ERR_UNSUPPORTED, "decode gemv: %d columns", M);
     int nb = gemv_nb(B);
     // Clusters: the K slices of a column block as one cluster of S blocks (a power of two up to
-    // 16), the most whose grid still fits one wave at two blocks per SM with at least 8 rows per
-    // slice, if the GPU can place such a cluster.
+    // 16), the most whose grid fits one wave at two blocks per SM, with at least 8 rows per slice
+    // and every cluster resident at once (a grid whose clusters cannot all be placed runs in
+    // waves, each a full latency chain).
     int S = 0;
     for (int cs = 16; cs >= 2 && !S; cs >>= 1) {
         if ((int64_t)colblocks * cs > 2 * ctx->num_sms || K / cs < 8) continue;
@@ -1059,7 +1073,7 @@ gk_status lm_head(gk_ctx* ctx, gk_kv* kv, const float* X, const float* ln_g, con
     int B = kv->B, C = kv->cfg.C, V = kv->cfg.V;
     int nb = gemv_nb(B);
     size_t smem = ((size_t)nb * C + 2 * (size_t)nb) * sizeof(float);
-    int blocks = ctx->num_sms * 4;
+    int blocks = ctx->num_sms * 2;  // one wave at two blocks per SM
 #define LM_CASE(NBV)                                                                                         \
     case NBV:                                                                                                \
         cudaFuncSetAttribute(lm_head_kernel<NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \

@@ -892,10 +892,12 @@ void mega_setup(gk_ctx* ctx, gk_kv* kv) {
         default: ok = mega_supported<16>(ctx, kv, &blocks); break;
     }
     cudaGetLastError();
-    // measured on GB300 (GPT-2-124M, 512-token prompt): the persistent step is faster at batch 1
-    // and 2 (457 vs 535 and 510 vs 559 us per step); from batch 4 on the per-layer launches win
-    // (705 vs 835 us at 4, 1508 vs 1625 us at 16): the persistent kernel's phases are latency
-    // bound at small batches, while its one block per SM limits wide batches' arithmetic
+    // measured on GB300 (GPT-2-124M, 512-token prompt), against the per-layer launches as they
+    // were before their GEMVs finished on clusters: the persistent step was faster at batch 1
+    // and 2 (457 vs 535 and 510 vs 559 us per step), the per-layer launches from batch 4 on
+    // (705 vs 835 us at 4, 1508 vs 1625 us at 16; they now take 815 us at 16): the persistent
+    // kernel's phases are latency bound at small batches, while its one block per SM limits
+    // wide batches' arithmetic
     kv->mega = ok && kv->bar && kv->B <= MEGA_MAX_B;
 }
 

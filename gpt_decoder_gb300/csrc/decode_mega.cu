@@ -22,7 +22,8 @@
 // (batch row, head, chunk of 32 keys), one per warp, write (max, sum, unnormalised output)
 // partials; the last chunk of a (row, head) combines them in chunk order. All sums run in a
 // fixed order, so a step is deterministic. The cache runs this kernel for batches of one or
-// two rows; wider batches keep the per-layer launches (decode.cu), which are faster there.
+// two rows of models narrower than 512; wider batches and models keep the per-layer launches
+// (decode.cu), which are faster there.
 //
 // Every wait is bounded (one second): a barrier or TMA wait that expires records
 // GK_ERR_TIMEOUT, raises the abort word so the other blocks leave at their next barrier, waits
@@ -55,6 +56,7 @@ struct Smem {
 };
 constexpr int KW = 32;                           // keys per attention work item (one warp)
 constexpr int MEGA_MAX_B = 2;                    // widest batch the persistent step runs
+constexpr int MEGA_MAX_C = 512;                  // widest model (C) the persistent step runs
 constexpr uint64_t LIMIT_NS = 1000000000ull;     // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 
@@ -897,8 +899,10 @@ void mega_setup(gk_ctx* ctx, gk_kv* kv) {
     // and 2 (457 vs 535 and 510 vs 559 us per step), the per-layer launches from batch 4 on
     // (705 vs 835 us at 4, 1508 vs 1625 us at 16; they now take 815 us at 16): the persistent
     // kernel's phases are latency bound at small batches, while its one block per SM limits
-    // wide batches' arithmetic
-    kv->mega = ok && kv->bar && kv->B <= MEGA_MAX_B;
+    // wide batches' arithmetic. With the GEMVs on clusters the per-layer launches also win for
+    // GPT-2-124M (C = 768) at batch 1: 0.376 vs 0.471 ms per step; the persistent step is kept
+    // for narrower models at batch 1-2
+    kv->mega = ok && kv->bar && kv->B <= MEGA_MAX_B && kv->cfg.C < MEGA_MAX_C;
 }
 
 gk_status mega_step(gk_ctx* ctx, gk_kv* kv, const float* params, const int32_t* tokens, float* logits) {

@@ -322,13 +322,16 @@ def _launches_per_step(gkctx, s, B, n_steps=4, Tp=6):
 
 
 def test_decode_step_is_one_persistent_launch_plus_selection(gkctx):
-    """A decode step at batch 1 or 2 runs as one persistent kernel (embedding, every layer, ln_f
-    and the head), then the selection and the position advance: three launches. From batch 4 on
+    """A decode step of a model narrower than 512 at batch 1 or 2 runs as one persistent kernel
+    (embedding, every layer, ln_f and the head), then the selection and the position advance:
+    three launches. From batch 4 on, and for models of width 512 and more (GPT-2-124M is 768),
     the step keeps the per-layer launches (five per layer)."""
     s = synth.GptShape(V=64, T=32, C=96, H=4, L=4)
     assert _launches_per_step(gkctx, s, 1) == 3
     assert _launches_per_step(gkctx, s, 2) == 3
     assert _launches_per_step(gkctx, s, 4) > 5 * s.L
+    wide = synth.GptShape(V=64, T=32, C=512, H=8, L=2)
+    assert _launches_per_step(gkctx, wide, 1) > 5 * wide.L
 
 
 @pytest.mark.parametrize("B", [1, 3])

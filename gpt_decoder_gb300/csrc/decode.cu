@@ -991,7 +991,10 @@ bool gemv_cluster_fits_nb(dim3 grid, size_t smem, int cs) {
     return cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess &&
            (int64_t)n * cs >= (int64_t)grid.x * grid.y;
 }
-bool gemv_cluster_fits(gk_ctx* ctx, int nb, dim3 grid, size_t smem, int cs) {
+// An error already pending from the caller's code is left in place (and the plain GEMV runs);
+// an error that the queries themselves raise is cleared.
+bool gemv_cluster_fits(int nb, dim3 grid, size_t smem, int cs) {
+    if (cudaPeekAtLastError() != cudaSuccess) return false;
     bool ok = false;
     switch (nb) {
         case 1: ok = gemv_cluster_fits_nb<1>(grid, smem, cs); break;
@@ -1000,8 +1003,7 @@ bool gemv_cluster_fits(gk_ctx* ctx, int nb, dim3 grid, size_t smem, int cs) {
         case 8: ok = gemv_cluster_fits_nb<8>(grid, smem, cs); break;
         default: ok = gemv_cluster_fits_nb<16>(grid, smem, cs); break;
     }
-    cudaGetLastError();  // a refused query leaves no error behind
-    (void)ctx;
+    cudaGetLastError();
     return ok;
 }
 
@@ -1025,7 +1027,7 @@ gk_status gemv(gk_ctx* ctx, gk_kv* kv, const float* X, int64_t ldx, const float*
         if (cdiv(K, ks) != cs) continue;  // every slice non-empty
         const size_t sm = ((size_t)gemv_red_offset(nb, ks) + 8 * (size_t)nb * GEMV_COLS + ((2 * nb + 3) & ~3) +
                            (size_t)nb * GEMV_COLS) * sizeof(float);
-        if (gemv_cluster_fits(ctx, nb, dim3(colblocks, cs), sm, cs)) S = cs;
+        if (gemv_cluster_fits(nb, dim3(colblocks, cs), sm, cs)) S = cs;
     }
     const bool cl = S > 0;
     if (!cl) {
